@@ -1,0 +1,272 @@
+"""dattn oracle: TEST INFRASTRUCTURE ONLY.
+
+This is a plain, slow, double-precision CPU implementation of what the split-KV decode path
+computes. The arithmetic lives in ``dattn_oracle.c``, which is plain C compiled with gcc
+without fast-math and without floating-point contraction. This module only marshals numpy
+arrays into it.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may import
+this package. The CUDA library never calls it, and it never calls the CUDA library.
+
+bf16 tensors travel as their raw 16-bit patterns (numpy ``uint16``). The C code widens them
+exactly to double.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dattn_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+# gcc flags: no fast-math and no contraction, so every rounding step is the one written in C.
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+          "-pthread", "-Wall", "-Wextra", "-Wno-unused-parameter"]
+
+
+def build_oracle(out_path: str = _LIB_PATH, extra_flags=()) -> str:
+    """Compile dattn_oracle.c into a shared library with gcc and return its path."""
+    cmd = ["gcc", *CFLAGS, *extra_flags, _SRC, "-o", out_path + ".tmp", "-lm"]
+    subprocess.run(cmd, check=True, cwd=_HERE)
+    os.replace(out_path + ".tmp", out_path)
+    return out_path
+
+
+def _needs_rebuild() -> bool:
+    if not os.path.exists(_LIB_PATH):
+        return True
+    lib_t = os.path.getmtime(_LIB_PATH)
+    return any(os.path.getmtime(os.path.join(_HERE, f)) > lib_t
+               for f in ("dattn_oracle.c", "dattn_oracle.h"))
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_D = ctypes.c_double
+
+_SIGS = {
+    "orc_bf16_to_double": (_D, [ctypes.c_uint16]),
+    "orc_attention": (None, [_P, _P, _P, _I64, _I, _P, _I64, _D, _P, _P, _P]),
+    "orc_partial": (None, [_P, _P, _P, _I64, _I, _P, _I64, _D, _P, _P, _P]),
+    "orc_merge": (None, [_I, _P, _P, _P, _I, _P, _P, _P, _P]),
+    "orc_kv_write": (_I64, [_P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _I64, _I64]),
+    "orc_logical_page_stats": (None, [_P, _I64, _I, _I64, _I64, _P, _P]),
+    "orc_logical_score_f64": (_D, [_P, _P, _P, _I]),
+    "orc_logical_score_f32": (ctypes.c_float, [_P, _P, _P, _I]),
+    "orc_page_scores": (None, [_P, _I, _P, _I64, _I, _I64, _I, _I, _P]),
+    "orc_topk": (None, [_P, _I64, _I, _P]),
+    "orc_sparse_rows": (_I64, [_I, _I64, _I, _P, _I, _I, _I, _P]),
+    "orc_attention_pairs_mt": (_I, [_P, _P, _P, _P, _I, _I, _I, _D, _P, _I64, _I, _P, _P, _P]),
+}
+
+
+def load(path: str | None = None):
+    """Load the compiled oracle, building it first if it is missing or stale."""
+    global _lib
+    with _lock:
+        if path is not None:
+            lib = ctypes.CDLL(path)
+        else:
+            if _lib is not None:
+                return _lib
+            if _needs_rebuild():
+                build_oracle()
+            lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+# ----------------------------------------------------------------------------- marshalling
+
+def bf16_bits(x) -> np.ndarray:
+    """Raw 16-bit patterns of a bf16 tensor (torch) or of an existing uint16 array."""
+    if isinstance(x, np.ndarray):
+        if x.dtype != np.uint16:
+            raise TypeError("expected bf16 bit patterns as uint16")
+        return np.ascontiguousarray(x)
+    import torch  # only for torch inputs
+    if x.dtype != torch.bfloat16:
+        raise TypeError(f"expected a bfloat16 tensor, got {x.dtype}")
+    return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy()
+                                .view(np.uint16))
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _rows(rows):
+    if rows is None:
+        return None
+    return np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+
+
+# ------------------------------------------------------------------------------ functions
+
+def attention(q, K, V, scale: float, rows=None, lib=None):
+    """Full softmax attention of one query (``q`` [d]) over rows of K, V ([n][d]).
+
+    Returns (out [d] float64, m, e). Infinite-LLM notes, full-attention equations.
+    """
+    lib = lib or load()
+    q, K, V = bf16_bits(q), bf16_bits(K), bf16_bits(V)
+    d = q.shape[-1]
+    K2 = K.reshape(-1, d)
+    V2 = V.reshape(-1, d)
+    r = _rows(rows)
+    n = K2.shape[0] if r is None else r.shape[0]
+    out = np.zeros(d, np.float64)
+    m = ctypes.c_double()
+    e = ctypes.c_double()
+    lib.orc_attention(_ptr(q), _ptr(K2), _ptr(V2), d, d, _ptr(r), n, scale, _ptr(out),
+                      ctypes.byref(m), ctypes.byref(e))
+    return out, m.value, e.value
+
+
+def partial(q, K, V, scale: float, rows=None, lib=None):
+    """MicroAttention triple (m_j, e_j, MA_j) over rows of K, V. Infinite-LLM notes."""
+    lib = lib or load()
+    q, K, V = bf16_bits(q), bf16_bits(K), bf16_bits(V)
+    d = q.shape[-1]
+    K2 = K.reshape(-1, d)
+    V2 = V.reshape(-1, d)
+    r = _rows(rows)
+    n = K2.shape[0] if r is None else r.shape[0]
+    MA = np.zeros(d, np.float64)
+    m = ctypes.c_double()
+    e = ctypes.c_double()
+    lib.orc_partial(_ptr(q), _ptr(K2), _ptr(V2), d, d, _ptr(r), n, scale, ctypes.byref(m),
+                    ctypes.byref(e), _ptr(MA))
+    return m.value, e.value, MA
+
+
+def merge(m, e, MA, lib=None):
+    """Aggregate b partials. Returns (m_g, e_g, out [d], MA_g [d]). Infinite-LLM notes."""
+    lib = lib or load()
+    m = np.ascontiguousarray(np.asarray(m, np.float64).reshape(-1))
+    e = np.ascontiguousarray(np.asarray(e, np.float64).reshape(-1))
+    MA = np.ascontiguousarray(np.asarray(MA, np.float64))
+    b = m.shape[0]
+    d = MA.shape[-1]
+    MA = MA.reshape(b, d)
+    out = np.zeros(d, np.float64)
+    MA_g = np.zeros(d, np.float64)
+    mg = ctypes.c_double()
+    eg = ctypes.c_double()
+    lib.orc_merge(b, _ptr(m), _ptr(e), _ptr(MA), d, ctypes.byref(mg), ctypes.byref(eg),
+                  _ptr(out), _ptr(MA_g))
+    return mg.value, eg.value, out, MA_g
+
+
+def kv_write(k_pool: np.ndarray, v_pool: np.ndarray, block_table_row, num_pages: int,
+             k_new, v_new, pos0: int, lib=None) -> int:
+    """Write T tokens of one request into uint16 pools [num_pages][Hkv][P][d] in place.
+
+    ``k_new``/``v_new`` are [T][Hkv][d]. Returns the number of tokens skipped because their
+    page is unmapped or out of range. LoongServe notes §4.2 (the master saves new KV).
+    """
+    lib = lib or load()
+    assert k_pool.dtype == np.uint16 and k_pool.flags.c_contiguous
+    assert v_pool.dtype == np.uint16 and v_pool.flags.c_contiguous
+    _, Hkv, P, d = k_pool.shape
+    kn, vn = bf16_bits(k_new), bf16_bits(v_new)
+    T = kn.shape[0]
+    bt = np.ascontiguousarray(np.asarray(block_table_row, np.int32))
+    return lib.orc_kv_write(_ptr(k_pool), _ptr(v_pool), Hkv, P, d, _ptr(bt), bt.shape[0],
+                            num_pages, _ptr(kn), _ptr(vn), pos0, T)
+
+
+def logical_page_stats(K, t0: int, t1: int, lib=None):
+    """(k_max, k_min) over token rows [t0, t1) of K ([n][d]). LServe notes §3.1.2."""
+    lib = lib or load()
+    K = bf16_bits(K)
+    d = K.shape[-1]
+    K2 = K.reshape(-1, d)
+    kmax = np.zeros(d, np.uint16)
+    kmin = np.zeros(d, np.uint16)
+    lib.orc_logical_page_stats(_ptr(K2), d, d, t0, t1, _ptr(kmax), _ptr(kmin))
+    return kmax, kmin
+
+
+def logical_score(q, kmax, kmin, precision64: bool = True, lib=None) -> float:
+    """Logical-page score sum_d max(q_d kmax_d, q_d kmin_d) (fp64 or fp32 decision order)."""
+    lib = lib or load()
+    q, kmax, kmin = bf16_bits(q), bf16_bits(kmax), bf16_bits(kmin)
+    fn = lib.orc_logical_score_f64 if precision64 else lib.orc_logical_score_f32
+    return float(fn(_ptr(q), _ptr(kmax), _ptr(kmin), q.shape[-1]))
+
+
+def page_scores(Q, K, L: int, P: int, precision64: bool, lib=None) -> np.ndarray:
+    """Physical-page scores of one request/KV head (Q: [g][d], K: [>=L][d] token order)."""
+    lib = lib or load()
+    Q, K = bf16_bits(Q), bf16_bits(K)
+    d = Q.shape[-1]
+    Q2 = Q.reshape(-1, d)
+    K2 = K.reshape(-1, d)
+    n = (L + P - 1) // P
+    score = np.zeros(max(n, 1), np.float64)
+    lib.orc_page_scores(_ptr(Q2), Q2.shape[0], _ptr(K2), d, d, L, P, 1 if precision64 else 0,
+                        _ptr(score))
+    return score[:n]
+
+
+def topk(score, top_k: int, lib=None) -> np.ndarray:
+    """Top-K page indices (ties to the lower index), ascending, padded with -1."""
+    lib = lib or load()
+    s = np.ascontiguousarray(np.asarray(score, np.float64))
+    sel = np.zeros(max(top_k, 1), np.int32)
+    lib.orc_topk(_ptr(s), s.shape[0], top_k, _ptr(sel))
+    return sel[:top_k]
+
+
+def select_pages(Q, K, L: int, P: int, top_k: int, lib=None) -> np.ndarray:
+    """Page selection of one request/KV head, decided in the fp32 score arithmetic."""
+    return topk(page_scores(Q, K, L, P, precision64=False, lib=lib), top_k, lib=lib)
+
+
+def sparse_rows(kind: int, L: int, P: int, sel, sinks: int, local: int, lib=None) -> np.ndarray:
+    """Token rows attended by one head: 0 dense, 1 retrieval (selected pages), 2 streaming."""
+    lib = lib or load()
+    s = np.ascontiguousarray(np.asarray(sel if sel is not None else [-1], np.int32))
+    rows = np.zeros(max(L, 1), np.int64)
+    n = lib.orc_sparse_rows(kind, L, P, _ptr(s), s.shape[0] if sel is not None else 0,
+                            sinks, local, _ptr(rows))
+    return rows[:n]
+
+
+def attention_pairs(q, K_cat, V_cat, offs, pairs, scale: float, nthreads: int | None = None,
+                    lib=None):
+    """Dense decode attention for (request, query head) pairs on host threads.
+
+    q: [B][Hq][d]; K_cat/V_cat: token-ordered [sum L][Hkv][d]; offs: [B+1] token offsets.
+    Returns (out [n][d], m [n], e [n], threads used).
+    """
+    lib = lib or load()
+    q, K, V = bf16_bits(q), bf16_bits(K_cat), bf16_bits(V_cat)
+    B, Hq, d = q.shape
+    Hkv = K.shape[-2]
+    offs = np.ascontiguousarray(np.asarray(offs, np.int64))
+    pairs = np.ascontiguousarray(np.asarray(pairs, np.int32).reshape(-1, 2))
+    n = pairs.shape[0]
+    out = np.zeros((n, d), np.float64)
+    m = np.zeros(n, np.float64)
+    e = np.zeros(n, np.float64)
+    if nthreads is None:
+        nthreads = len(os.sched_getaffinity(0))
+    used = lib.orc_attention_pairs_mt(_ptr(q), _ptr(K), _ptr(V), _ptr(offs), Hq, Hkv, d,
+                                      scale, _ptr(pairs), n, nthreads, _ptr(out), _ptr(m),
+                                      _ptr(e))
+    return out, m, e, used
