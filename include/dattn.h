@@ -1,0 +1,267 @@
+/*
+ * dattn: split-KV decode attention over a paged bf16 KV cache, for GB300 (sm_103a).
+ *
+ * The C ABI of libdattn.so. Every entry point takes plain pointers and sizes: no C++ and
+ * no framework types. It validates its arguments on the host, then launches asynchronously
+ * on the given CUDA stream. The library never allocates device memory, never frees it and
+ * never synchronises. All buffers belong to the caller.
+ *
+ * The operation comes from the pages this library restates:
+ *
+ *  [IL] "Infinite-LLM: Efficient LLM Service for Long Context with DistAttention and
+ *       Distributed KVCache". DistAttention splits the KV cache of one request into
+ *       sub-blocks. Each sub-block j yields a MicroAttention triple over its seq_p keys
+ *       (equations in 速读 and in "DistAttention 的等价数学变换"):
+ *           m_j  = max_i s_i
+ *           e_j  = sum_i exp(s_i - m_j)
+ *           MA_j = sum_i exp(s_i - m_j) v_i        (unnormalised)
+ *       The triples are then aggregated ("结果聚合与通信开销降低", Fig. 4b):
+ *           m_g = max_j m_j,  e_g = sum_j e_j exp(m_j - m_g),
+ *           out = sum_j MA_j exp(m_j - m_g) / e_g,
+ *       which equals full softmax attention ("分布式注意力机制的通信挑战").
+ *  [LS] "LoongServe: Efficiently Serving Long-Context Large Language Models with Elastic
+ *       Sequence Parallelism", §4.2. In single- and multi-master distributed decoding, the
+ *       master saves the new token's KV in its local pool, every instance computes local
+ *       attention over its share of the KV, and the results are merged.
+ *  [LV] "LLM长序列服务优化：LServe的块稀疏注意力技术". §2.2.2: 64-token physical pages hold
+ *       16-token logical pages with per-channel k_max/k_min, and the page selection is
+ *       reused over a window of decode steps. §3.1.2: the statistics are computed when the
+ *       KV cache is written, a physical page is scored as the max over its logical pages,
+ *       and the top-K pages are selected. §3.1.1: streaming heads attend sink tokens plus
+ *       a local window. The streaming and retrieval heads run in one fused kernel.
+ *
+ * Here the "instances" are CTAs on one GPU. The KV of every (request, KV head) is split
+ * into 16-token tiles. The tiles are spread evenly over num_splits CTAs, so each CTA
+ * computes MicroAttention triples over a contiguous range of tiles. Triples of the same
+ * (request, KV head) are merged in the same launch by whichever CTA finishes that head
+ * last.
+ *
+ * Notation and conventions
+ *  - B requests, Hq query heads, Hkv KV heads, g = Hq / Hkv query heads per KV head
+ *    (query head h reads KV head h / g), d = head_dim, P = page_size tokens.
+ *  - A logit is s_i = scale * (q . k_i). m values at this ABI are in natural-log units.
+ *  - bf16 arrays are passed as dattn_bf16 (raw IEEE bfloat16 bits). Floats are fp32.
+ *  - Device pointers are marked (device). Structs passed by pointer live in host memory.
+ *  - Sequence length L_b = seq_lens[b]: tokens 0..L_b-1 of request b are valid. Token t
+ *    lives in physical page block_table[b * max_pages_per_req + t / P], slot t % P.
+ *  - Pool layout: k_pool and v_pool are [num_pages][Hkv][P][d]. Every (page, KV head)
+ *    tile is one contiguous P*d run.
+ *  - Statistics layout: stats is [num_pages][Hkv][P/16][2][d]. Entry [..][lp][0][:] is
+ *    k_max and [..][lp][1][:] is k_min of logical page lp, the 16 tokens
+ *    lp*16..lp*16+15 of that physical page.
+ *  - Device data errors (an unmapped page, a page id outside the pool, a length beyond
+ *    the block table, a selected page beyond the length, a bounded wait that ran out) do
+ *    not trap. The kernel skips the offending tile or token and ORs a DATTN_DEVERR_* bit
+ *    into *dev_err when dev_err is not NULL. A skipped tile contributes nothing to the
+ *    attention.
+ *  - Workspace: calls that merge across CTAs need a caller-owned device workspace of at
+ *    least dattn_workspace_size(...) bytes, 256-byte aligned. Its counter region must be
+ *    all zero before the first use: allocate it zeroed or call dattn_workspace_init once.
+ *    Every call leaves the counters at zero again. Calls that share one workspace must
+ *    not run concurrently (use one workspace per stream).
+ *  - Supported shapes: d in {64, 128}; P a multiple of 16 from 16 to 256; 1 <= g <= 8;
+ *    Hkv <= 256; B (or C for dattn_partial) <= 4096; top_k <= 256.
+ */
+#ifndef DATTN_H
+#define DATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t dattn_bf16;
+
+typedef enum {
+    DATTN_OK = 0,
+    DATTN_ERR_INVALID_ARG = 1, /* a null pointer, a negative size or an inconsistent shape */
+    DATTN_ERR_UNSUPPORTED = 2, /* a valid shape outside the supported set (see above) */
+    DATTN_ERR_WORKSPACE = 3,   /* workspace missing, too small or misaligned */
+    DATTN_ERR_CUDA = 4         /* a CUDA runtime or driver call failed */
+} dattn_status_t;
+
+/* Bits OR-ed into the optional device error word. */
+#define DATTN_DEVERR_UNMAPPED_PAGE 0x1  /* block-table entry < 0 for a needed page */
+#define DATTN_DEVERR_PAGE_OOB 0x2       /* block-table entry >= num_pages */
+#define DATTN_DEVERR_LEN_OOB 0x4        /* seq_len < 0, or beyond max_pages_per_req * P */
+#define DATTN_DEVERR_TIMEOUT 0x8        /* a bounded pipeline wait ran out; output invalid */
+#define DATTN_DEVERR_CHUNK_OOB 0x10     /* chunk_req or a chunk page index out of range */
+#define DATTN_DEVERR_SELECT_OOB 0x20    /* a selected page lies beyond the request length */
+
+/* Head kinds of the block-sparse decode [LV §2.1.2, §3.1.1]. */
+#define DATTN_HEAD_DENSE 0
+#define DATTN_HEAD_RETRIEVAL 1
+#define DATTN_HEAD_STREAMING 2
+
+/* Shape of the paged KV pool and the block table. */
+typedef struct dattn_kv_layout {
+    int32_t num_pages;          /* physical pages in the pool */
+    int32_t num_kv_heads;       /* Hkv */
+    int32_t head_dim;           /* d: 64 or 128 */
+    int32_t page_size;          /* P: tokens per physical page, a multiple of 16 */
+    const int32_t *block_table; /* (device) [B][max_pages_per_req]; -1 = unmapped */
+    int32_t max_pages_per_req;  /* row width of block_table */
+} dattn_kv_layout;
+
+/* Block-sparse decode settings [LV §2.2.2, §3.1.1, §3.1.2]. */
+typedef struct dattn_sparse {
+    const int8_t *head_kind;  /* (device) [Hkv]: DATTN_HEAD_* per KV head */
+    int32_t sinks;            /* streaming heads: tokens [0, min(sinks, L)) */
+    int32_t local;            /* streaming heads: tokens [max(sinks, L - local), L) */
+    int32_t top_k;            /* retrieval heads: entries per row of selected */
+    const int32_t *selected;  /* (device) [B][Hkv][top_k] request-relative physical page
+                                 indices from dattn_page_select; -1 entries are ignored.
+                                 A page must not appear twice in one row. */
+} dattn_sparse;
+
+/*
+ * Append T new tokens per request to the paged pool [LS §4.2: the master saves the new
+ * token's KV locally]. If stats is not NULL, also update the logical-page statistics
+ * [LV §3.1.2: computed at KV-write time].
+ *
+ *   k_new, v_new (device) bf16 [B][T][Hkv][d]. Token t of request b is written at
+ *                position seq_lens[b] + t.
+ *   stats        (device, nullable) bf16 [num_pages][Hkv][P/16][2][d]. When a token
+ *                opens a logical page (position % 16 == 0), that page's k_max and k_min
+ *                are set to its key. Later tokens update them elementwise with strict
+ *                comparison, so on a tie the earlier value stays.
+ *   seq_lens     (device) int32 [B]. On entry, the current lengths; on exit, each is
+ *                increased by T. When T > 49 the update runs as a second small kernel on
+ *                the same stream.
+ *   dev_err      (device, nullable) int32 error word, see DATTN_DEVERR_*. A token whose
+ *                page is unmapped or out of range is not written.
+ * Returns DATTN_OK or an error status; nothing is launched on error.
+ */
+dattn_status_t dattn_kv_append(const dattn_kv_layout *layout, dattn_bf16 *k_pool,
+                               dattn_bf16 *v_pool, dattn_bf16 *stats, const dattn_bf16 *k_new,
+                               const dattn_bf16 *v_new, int32_t B, int32_t T,
+                               int32_t *seq_lens, int32_t *dev_err, void *stream);
+
+/*
+ * MicroAttention partials over explicit chunks of pages [IL, DistAttention 的等价数学变换].
+ * Chunk c covers the request-relative pages
+ * chunk_pages[chunk_page_indptr[c] .. chunk_page_indptr[c+1]) of request chunk_req[c].
+ * Only tokens < seq_lens[chunk_req[c]] count. For every chunk c and query head h it writes
+ *   m[c][h]  = max s_i (natural-log units),  e[c][h] = sum exp(s_i - m),
+ *   MA[c][h][:] = sum exp(s_i - m) v_i.
+ * An empty chunk gives m = -inf, e = 0, MA = 0.
+ *
+ *   q          (device) bf16 [B][Hq][d]
+ *   seq_lens   (device) int32 [B]
+ *   chunk_req  (device) int32 [C]
+ *   chunk_page_indptr (device) int32 [C+1], non-decreasing, starting at 0
+ *   chunk_pages (device) int32 [chunk_page_indptr[C]]
+ *   m, e       (device) fp32 [C][Hq];  MA (device) fp32 [C][Hq][d]
+ *   ws, ws_bytes  workspace, at least dattn_workspace_size(C, Hq, Hkv, d, 0, num_splits)
+ *   num_splits number of CTAs the tiles are spread over; 0 = automatic
+ */
+dattn_status_t dattn_partial(const dattn_kv_layout *layout, const dattn_bf16 *k_pool,
+                             const dattn_bf16 *v_pool, const dattn_bf16 *q, int32_t B,
+                             int32_t Hq, float scale, const int32_t *seq_lens, int32_t C,
+                             const int32_t *chunk_req, const int32_t *chunk_page_indptr,
+                             const int32_t *chunk_pages, float *m, float *e, float *MA,
+                             void *ws, size_t ws_bytes, int32_t num_splits, int32_t *dev_err,
+                             void *stream);
+
+/*
+ * Log-sum-exp aggregation of chunk partials [IL, 结果聚合与通信开销降低]. For request b
+ * and query head h it merges the chunks c in [chunk_indptr[b], chunk_indptr[b+1]):
+ *   m_g = max m_c,  e_g = sum e_c exp(m_c - m_g),
+ *   out = sum MA_c exp(m_c - m_g) / e_g,  MA_g = sum MA_c exp(m_c - m_g).
+ * Chunks with m = -inf are empty and add nothing. If every chunk is empty, then
+ * out = MA_g = 0, m_g = -inf and e_g = 0. (m_g, e_g, MA_g) is itself a partial, so
+ * merges nest.
+ *
+ *   C            number of chunk rows in m, e and MA
+ *   chunk_indptr (device) int32 [B+1]. A range outside [0, C] is clamped and flagged
+ *                with DATTN_DEVERR_CHUNK_OOB.
+ *   m, e (device) fp32 [C][Hq];  MA (device) fp32 [C][Hq][d]
+ *   out  (device, nullable) fp32 [B][Hq][d]
+ *   m_g, e_g (device, nullable) fp32 [B][Hq];  MA_g (device, nullable) fp32 [B][Hq][d]
+ */
+dattn_status_t dattn_merge(int32_t B, int32_t C, int32_t Hq, int32_t head_dim,
+                           const int32_t *chunk_indptr, const float *m, const float *e,
+                           const float *MA, float *out, float *m_g, float *e_g, float *MA_g,
+                           int32_t *dev_err, void *stream);
+
+/*
+ * Fused single-launch decode: split-KV partials plus merge, dense or block-sparse.
+ * Dense (sparse == NULL): every query head of request b attends tokens 0..L_b-1.
+ * Block-sparse [LV §2.2.2, §3.1.1]: per KV head kind,
+ *   DATTN_HEAD_DENSE      attends all tokens;
+ *   DATTN_HEAD_RETRIEVAL  attends the tokens (< L_b) of the pages in sparse->selected;
+ *   DATTN_HEAD_STREAMING  attends [0, min(sinks, L)) and [max(sinks, L - local), L).
+ * num_splits CTAs (0 = automatic, from the SM count and the work size) each take an equal
+ * share of the 16-token tiles of all (request, KV head) pairs. A head whose tiles span
+ * several CTAs is merged by the last of them.
+ *
+ *   q        (device) bf16 [B][Hq][d];  seq_lens (device) int32 [B]
+ *   out      (device) fp32 [B][Hq][d]
+ *   m_g, e_g (device, nullable) fp32 [B][Hq]: the merged max (natural-log units) and sum
+ *   ws, ws_bytes  workspace of at least dattn_workspace_size(B, Hq, Hkv, d, 0, num_splits)
+ */
+dattn_status_t dattn_decode(const dattn_kv_layout *layout, const dattn_bf16 *k_pool,
+                            const dattn_bf16 *v_pool, const dattn_bf16 *q, int32_t B,
+                            int32_t Hq, float scale, const int32_t *seq_lens,
+                            const dattn_sparse *sparse, int32_t num_splits, void *ws,
+                            size_t ws_bytes, float *out, float *m_g, float *e_g,
+                            int32_t *dev_err, void *stream);
+
+/*
+ * Page scoring and top-K selection for retrieval heads [LV §2.2.2, §3.1.2]. For every
+ * request b and KV head h of kind DATTN_HEAD_RETRIEVAL:
+ *   logical score  sigma(lp) = max over the g query heads j of
+ *                  sum_d max(q_jd * kmax_d, q_jd * kmin_d)
+ *                  (fp32, one fused multiply-add per channel in ascending channel order);
+ *   physical score = max of sigma over its logical pages that hold a token < L_b;
+ *   selection      the top_k physical pages by score, ties to the lower page index.
+ * They are written in ascending page order to selected[b][h][0..top_k), padded with -1.
+ * Rows of heads of other kinds are filled with -1. Call it once per reuse window and pass
+ * the result to dattn_decode through dattn_sparse.selected.
+ *
+ *   stats    (device) bf16 [num_pages][Hkv][P/16][2][d], kept by dattn_kv_append
+ *   q        (device) bf16 [B][Hq][d];  seq_lens (device) int32 [B]
+ *   head_kind (device) int8 [Hkv];  selected (device) int32 [B][Hkv][top_k]
+ *   ws, ws_bytes  workspace of at least dattn_workspace_size(B, Hq, Hkv, d, top_k, num_splits)
+ */
+dattn_status_t dattn_page_select(const dattn_kv_layout *layout, const dattn_bf16 *stats,
+                                 const dattn_bf16 *q, int32_t B, int32_t Hq,
+                                 const int32_t *seq_lens, const int8_t *head_kind,
+                                 int32_t top_k, int32_t *selected, void *ws, size_t ws_bytes,
+                                 int32_t num_splits, int32_t *dev_err, void *stream);
+
+/*
+ * Workspace bytes for dattn_partial (items = C, top_k = 0), dattn_decode (items = B,
+ * top_k = 0) and dattn_page_select (items = B, top_k > 0) with the given num_splits
+ * (0 = the automatic choice on the current device). Returns 0 for invalid arguments.
+ */
+size_t dattn_workspace_size(int32_t items, int32_t Hq, int32_t Hkv, int32_t head_dim,
+                            int32_t top_k, int32_t num_splits);
+
+/* Zero the workspace (cudaMemsetAsync on the stream). One call before first use suffices. */
+dattn_status_t dattn_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* The automatic num_splits for a work size of total_tiles 16-token tiles on the current
+ * device: SM count times resident CTAs per SM, capped so a CTA gets at least 16 tiles. */
+int32_t dattn_auto_splits(int64_t total_tiles);
+
+/* The balanced split: CTA c of G covers tiles [floor(c*W/G), floor((c+1)*W/G)). */
+void dattn_split_range(int64_t total_tiles, int32_t num_splits, int32_t cta, int64_t *begin,
+                       int64_t *end);
+
+/* The CTA that owns tile t of W under the balanced split of G CTAs. */
+int32_t dattn_split_owner(int64_t tile, int64_t total_tiles, int32_t num_splits);
+
+/* Human-readable name of a status code. */
+const char *dattn_status_string(dattn_status_t s);
+
+/* Library version string, e.g. "dattn 0.1.0 sm_103a". */
+const char *dattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DATTN_H */

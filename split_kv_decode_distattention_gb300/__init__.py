@@ -1,0 +1,284 @@
+"""split_kv_decode_distattention_gb300: split-KV decode attention over a paged KV cache.
+
+This module is a thin Python binding of libdattn.so, the C-ABI library built from ``csrc/``.
+It only marshals arguments: torch tensors become device pointers, and the current torch
+stream becomes the launch stream. Every step of the computation runs in the library's
+CUDA kernels. There is no CPU fallback: if the library is missing, the first call raises.
+
+Entry points, with the same names as in include/dattn.h:
+  dattn_kv_append    paged KV append, plus logical-page k_max/k_min statistics
+  dattn_partial      MicroAttention partials (m, e, MA) over explicit chunks of pages
+  dattn_merge        log-sum-exp aggregation of partials
+  dattn_decode       fused split-KV decode, dense or block-sparse
+  dattn_page_select  page scoring and top-K selection for retrieval heads
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "KVLayout", "SparseConfig", "DattnError", "load_library", "library_path",
+    "dattn_kv_append", "dattn_partial", "dattn_merge", "dattn_decode", "dattn_page_select",
+    "dattn_workspace_size", "dattn_workspace_init", "dattn_auto_splits", "dattn_split_range",
+    "dattn_split_owner", "dattn_status_string", "dattn_version", "Workspace",
+    "HEAD_DENSE", "HEAD_RETRIEVAL", "HEAD_STREAMING", "DEVERR",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libdattn.so")
+_lib = None
+_lock = threading.Lock()
+
+HEAD_DENSE, HEAD_RETRIEVAL, HEAD_STREAMING = 0, 1, 2
+DEVERR = {"UNMAPPED_PAGE": 0x1, "PAGE_OOB": 0x2, "LEN_OOB": 0x4, "TIMEOUT": 0x8,
+          "CHUNK_OOB": 0x10, "SELECT_OOB": 0x20}
+
+
+class DattnError(RuntimeError):
+    """A dattn call returned a status other than DATTN_OK."""
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("block_table", ctypes.c_void_p), ("max_pages_per_req", ctypes.c_int32)]
+
+
+class _Sparse(ctypes.Structure):
+    _fields_ = [("head_kind", ctypes.c_void_p), ("sinks", ctypes.c_int32),
+                ("local", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("selected", ctypes.c_void_p)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+_SIGS = {
+    "dattn_kv_append": (_I, [ctypes.POINTER(_Layout), _P, _P, _P, _P, _P, _I, _I, _P, _P, _P]),
+    "dattn_partial": (_I, [ctypes.POINTER(_Layout), _P, _P, _P, _I, _I, _F, _P, _I, _P, _P, _P,
+                           _P, _P, _P, _P, _SZ, _I, _P, _P]),
+    "dattn_merge": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "dattn_decode": (_I, [ctypes.POINTER(_Layout), _P, _P, _P, _I, _I, _F, _P,
+                          ctypes.POINTER(_Sparse), _I, _P, _SZ, _P, _P, _P, _P, _P]),
+    "dattn_page_select": (_I, [ctypes.POINTER(_Layout), _P, _P, _I, _I, _P, _P, _I, _P, _P, _SZ,
+                               _I, _P, _P]),
+    "dattn_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "dattn_workspace_init": (_I, [_P, _SZ, _P]),
+    "dattn_auto_splits": (_I, [_I64]),
+    "dattn_split_range": (None, [_I64, _I, _I, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
+    "dattn_split_owner": (_I, [_I64, _I64, _I]),
+    "dattn_status_string": (ctypes.c_char_p, [_I]),
+    "dattn_version": (ctypes.c_char_p, []),
+}
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library(path: str | None = None):
+    """Load libdattn.so (built in-tree by ``_build.build()``); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _LIB_PATH
+        if not os.path.exists(p):
+            raise DattnError(
+                f"{p} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        msg = load_library().dattn_status_string(status).decode()
+        raise DattnError(f"{what} failed: {msg}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _bf16(t, name):
+    if t is not None and t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16")
+    return t
+
+
+def _i32(t, name):
+    if t is not None and t.dtype != torch.int32:
+        raise TypeError(f"{name} must be int32")
+    return t
+
+
+def _f32(t, name):
+    if t is not None and t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32")
+    return t
+
+
+class KVLayout:
+    """Shape of a paged pool [num_pages][Hkv][P][d] plus its int32 block table [B][max_pages]."""
+
+    def __init__(self, num_pages: int, num_kv_heads: int, head_dim: int, page_size: int,
+                 block_table: torch.Tensor):
+        _i32(block_table, "block_table")
+        self.block_table = block_table  # keeps the tensor alive
+        self.c = _Layout(num_pages, num_kv_heads, head_dim, page_size,
+                         block_table.data_ptr(), block_table.shape[-1])
+
+    @property
+    def num_pages(self): return self.c.num_pages
+
+    @property
+    def num_kv_heads(self): return self.c.num_kv_heads
+
+    @property
+    def head_dim(self): return self.c.head_dim
+
+    @property
+    def page_size(self): return self.c.page_size
+
+
+class SparseConfig:
+    """Block-sparse settings: per-KV-head kinds, streaming window and retrieval selection."""
+
+    def __init__(self, head_kind: torch.Tensor, sinks: int, local: int, top_k: int,
+                 selected: torch.Tensor | None):
+        if head_kind.dtype != torch.int8:
+            raise TypeError("head_kind must be int8")
+        self.head_kind, self.selected = head_kind, selected
+        self.c = _Sparse(head_kind.data_ptr(), sinks, local, top_k,
+                         selected.data_ptr() if selected is not None else None)
+
+
+class Workspace:
+    """A zeroed device workspace sized by dattn_workspace_size (allocated by torch)."""
+
+    def __init__(self, items: int, Hq: int, Hkv: int, head_dim: int, top_k: int = 0,
+                 num_splits: int = 0, device=None):
+        self.nbytes = dattn_workspace_size(items, Hq, Hkv, head_dim, top_k, num_splits)
+        n = max(self.nbytes, 256)
+        self.buffer = torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def dattn_workspace_size(items, Hq, Hkv, head_dim, top_k=0, num_splits=0) -> int:
+    return int(load_library().dattn_workspace_size(items, Hq, Hkv, head_dim, top_k, num_splits))
+
+
+def dattn_workspace_init(ws: Workspace, stream=None):
+    _check(load_library().dattn_workspace_init(_ptr(ws.buffer), ws.buffer.numel(),
+                                               _stream(stream)), "dattn_workspace_init")
+
+
+def dattn_auto_splits(total_tiles: int) -> int:
+    return int(load_library().dattn_auto_splits(total_tiles))
+
+
+def dattn_split_range(total_tiles: int, num_splits: int, cta: int):
+    b, e = ctypes.c_int64(), ctypes.c_int64()
+    load_library().dattn_split_range(total_tiles, num_splits, cta, ctypes.byref(b),
+                                     ctypes.byref(e))
+    return b.value, e.value
+
+
+def dattn_split_owner(tile: int, total_tiles: int, num_splits: int) -> int:
+    return int(load_library().dattn_split_owner(tile, total_tiles, num_splits))
+
+
+def dattn_status_string(status: int) -> str:
+    return load_library().dattn_status_string(status).decode()
+
+
+def dattn_version() -> str:
+    return load_library().dattn_version().decode()
+
+
+def dattn_kv_append(layout: KVLayout, k_pool, v_pool, stats, k_new, v_new, seq_lens,
+                    dev_err=None, stream=None):
+    """Append k_new/v_new ([B][T][Hkv][d] bf16) at seq_lens (int32 [B], advanced by T)."""
+    _bf16(k_pool, "k_pool"); _bf16(v_pool, "v_pool"); _bf16(stats, "stats")
+    _bf16(k_new, "k_new"); _bf16(v_new, "v_new"); _i32(seq_lens, "seq_lens")
+    B, T = k_new.shape[0], k_new.shape[1]
+    _check(load_library().dattn_kv_append(
+        ctypes.byref(layout.c), _ptr(k_pool), _ptr(v_pool), _ptr(stats), _ptr(k_new),
+        _ptr(v_new), B, T, _ptr(seq_lens), _ptr(dev_err), _stream(stream)), "dattn_kv_append")
+
+
+def dattn_partial(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, chunk_req,
+                  chunk_page_indptr, chunk_pages, m, e, MA, ws: Workspace, num_splits=0,
+                  dev_err=None, stream=None):
+    """MicroAttention partials of C chunks: m, e fp32 [C][Hq], MA fp32 [C][Hq][d]."""
+    _bf16(q, "q"); _i32(seq_lens, "seq_lens"); _i32(chunk_req, "chunk_req")
+    _i32(chunk_page_indptr, "chunk_page_indptr"); _i32(chunk_pages, "chunk_pages")
+    _f32(m, "m"); _f32(e, "e"); _f32(MA, "MA")
+    B, Hq = q.shape[0], q.shape[1]
+    C = chunk_req.shape[0]
+    _check(load_library().dattn_partial(
+        ctypes.byref(layout.c), _ptr(k_pool), _ptr(v_pool), _ptr(q), B, Hq, scale,
+        _ptr(seq_lens), C, _ptr(chunk_req), _ptr(chunk_page_indptr), _ptr(chunk_pages),
+        _ptr(m), _ptr(e), _ptr(MA), _ptr(ws.buffer), ws.buffer.numel(), num_splits,
+        _ptr(dev_err), _stream(stream)), "dattn_partial")
+
+
+def dattn_merge(chunk_indptr, m, e, MA, out=None, m_g=None, e_g=None, MA_g=None, dev_err=None,
+                stream=None):
+    """Aggregate partials per request (chunk ranges from chunk_indptr int32 [B+1])."""
+    _i32(chunk_indptr, "chunk_indptr")
+    for t, n in ((m, "m"), (e, "e"), (MA, "MA"), (out, "out"), (m_g, "m_g"), (e_g, "e_g"),
+                 (MA_g, "MA_g")):
+        _f32(t, n)
+    B = chunk_indptr.shape[0] - 1
+    C, Hq, d = MA.shape
+    _check(load_library().dattn_merge(
+        B, C, Hq, d, _ptr(chunk_indptr), _ptr(m), _ptr(e), _ptr(MA), _ptr(out), _ptr(m_g),
+        _ptr(e_g), _ptr(MA_g), _ptr(dev_err), _stream(stream)), "dattn_merge")
+
+
+def dattn_decode(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, out,
+                 ws: Workspace, m_g=None, e_g=None, sparse: SparseConfig | None = None,
+                 num_splits=0, dev_err=None, stream=None):
+    """Fused split-KV decode: out fp32 [B][Hq][d] (+ m_g, e_g fp32 [B][Hq])."""
+    _bf16(q, "q"); _i32(seq_lens, "seq_lens"); _f32(out, "out")
+    B, Hq = q.shape[0], q.shape[1]
+    sp = ctypes.byref(sparse.c) if sparse is not None else None
+    _check(load_library().dattn_decode(
+        ctypes.byref(layout.c), _ptr(k_pool), _ptr(v_pool), _ptr(q), B, Hq, scale,
+        _ptr(seq_lens), sp, num_splits, _ptr(ws.buffer), ws.buffer.numel(), _ptr(out),
+        _ptr(m_g), _ptr(e_g), _ptr(dev_err), _stream(stream)), "dattn_decode")
+
+
+def dattn_page_select(layout: KVLayout, stats, q, seq_lens, head_kind, top_k: int, selected,
+                      ws: Workspace, num_splits=0, dev_err=None, stream=None):
+    """Top-K physical pages per retrieval head into selected int32 [B][Hkv][top_k]."""
+    _bf16(stats, "stats"); _bf16(q, "q"); _i32(seq_lens, "seq_lens"); _i32(selected, "selected")
+    B, Hq = q.shape[0], q.shape[1]
+    _check(load_library().dattn_page_select(
+        ctypes.byref(layout.c), _ptr(stats), _ptr(q), B, Hq, _ptr(seq_lens), _ptr(head_kind),
+        top_k, _ptr(selected), _ptr(ws.buffer), ws.buffer.numel(), num_splits, _ptr(dev_err),
+        _stream(stream)), "dattn_page_select")

@@ -1,0 +1,98 @@
+// Host-side declarations shared by the dattn translation units (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/dattn.h"
+
+namespace dattn {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 8;          // pipeline depth; a multiple of kConsumerWarps
+constexpr int kMaxItems = 4096;     // B (or C) bound
+constexpr int kMaxKvHeads = 256;
+constexpr int kMaxGroup = 8;        // query heads per KV head
+constexpr int kMaxTopK = 256;
+constexpr int kMaxCtasPerSm = 4;    // bound used for workspace sizing with automatic splits
+
+enum AttnMode : int { MODE_PARTIAL = 0, MODE_DENSE = 1, MODE_SPARSE = 2 };
+
+// Everything one launch of the attention engine needs (device pointers unless noted).
+struct AttnParams {
+    int32_t mode;
+    int32_t num_pages, Hkv, P, max_pages;
+    const int32_t* block_table;
+    const uint16_t* q;
+    int32_t B, Hq, g;
+    float sl2;  // scale * log2(e)
+    const int32_t* seq_lens;
+    // dattn_partial
+    int32_t C;
+    const int32_t* chunk_req;
+    const int32_t* chunk_indptr;
+    const int32_t* chunk_pages;
+    // block-sparse decode
+    const int8_t* head_kind;
+    int32_t sinks, local, top_k;
+    const int32_t* selected;
+    // outputs: decode -> out [B][Hq][D], m_out / e_out [B][Hq] (nullable)
+    //          partial -> out = MA [C][Hq][D], m_out / e_out [C][Hq]
+    float* out;
+    float* m_out;
+    float* e_out;
+    // workspace
+    int32_t* counters;  // [nseg]
+    float* slots;       // [(G + nseg)][g][D + 2]
+    int32_t nseg;
+    int32_t nitems;     // B for dense / sparse, C for partial
+    int32_t* dev_err;
+};
+
+// Shared-memory layout of the attention engine, identical on host and device.
+struct AttnSmem {
+    uint32_t stage_bytes, stages, bars, meta, flags, ws_m, ws_e, ws_o, kind_before, kinds,
+        item_start, item_len, scan, total;
+};
+
+__host__ __device__ inline AttnSmem attn_smem_layout(int D, int g, int nitems, int Hkv,
+                                                     bool sparse) {
+    AttnSmem s;
+    s.stage_bytes = 2u * (uint32_t)(D / 64) * 2048u;
+    uint32_t o = 0;
+    s.stages = o;      o += (uint32_t)kStages * s.stage_bytes;
+    s.bars = o;        o += 2u * kStages * 8u;
+    s.meta = o;        o += kStages * 4u;
+    s.flags = o;       o += 16u;
+    s.ws_m = o;        o += kConsumerWarps * kMaxGroup * 4u;
+    s.ws_e = o;        o += kConsumerWarps * kMaxGroup * 4u;
+    s.ws_o = o;        o += (uint32_t)(kConsumerWarps * g * D) * 4u;
+    s.kind_before = o; o += sparse ? (uint32_t)(Hkv + 1) * 3u * 4u : 0u;
+    s.kinds = o;       o += sparse ? (uint32_t)Hkv * 4u : 0u;
+    o = (o + 15u) & ~15u;
+    s.item_start = o;  o += (uint32_t)(nitems + 1) * 4u;
+    s.item_len = o;    o += (uint32_t)nitems * 4u;
+    o = (o + 15u) & ~15u;
+    s.scan = o;        o += 8u * 4u;
+    s.total = o + 1024u;  // slack to align the dynamic base to 1024 bytes
+    return s;
+}
+
+// Device properties and cached driver entry points.
+int sm_count_current();
+dattn_status_t make_kv_tensor_map(void* tmap_out, const void* pool, int64_t rows, int D);
+
+dattn_status_t launch_attention(const AttnParams& p, const void* k_pool, const void* v_pool,
+                                int D, int32_t num_splits, void* ws, size_t ws_bytes,
+                                cudaStream_t stream, int64_t tiles_bound);
+int32_t attention_occupancy(int D, int g, int nitems, int Hkv, bool sparse);
+
+// Number of CTAs for a launch with an upper bound of total_tiles tiles.
+int32_t choose_splits(int64_t total_tiles, int32_t requested, int occupancy);
+
+size_t attn_workspace_bytes(int32_t nseg, int32_t g, int32_t D, int32_t G);
+size_t select_workspace_bytes(int32_t nseg, int32_t top_k, int32_t G);
+
+}  // namespace dattn

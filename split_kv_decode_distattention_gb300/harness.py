@@ -1,0 +1,92 @@
+"""Device-side driver for a seeded workload: allocate the paged pool, fill it through
+dattn_kv_append, and run decode steps. Used by the smoke check, the GPU tests and the
+benchmark. It calls only the library's entry points; the workload values come from
+``workloads``.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (KVLayout, SparseConfig, Workspace, dattn_decode, dattn_kv_append,
+               dattn_page_select)
+from .workloads import Case
+
+
+class PagedCache:
+    """Pool [num_pages][Hkv][P][d] (K and V) plus statistics, block table and lengths."""
+
+    def __init__(self, case: Case, device="cuda", with_stats: bool = False, fill: bool = True,
+                 chunk_tokens: int = 8192, zero_pool: bool = False):
+        self.case = case
+        self.device = torch.device(device)
+        c = case
+        alloc = torch.zeros if zero_pool else torch.empty
+        self.k_pool = alloc(c.num_pages, c.Hkv, c.P, c.d, dtype=torch.bfloat16, device=device)
+        self.v_pool = alloc(c.num_pages, c.Hkv, c.P, c.d, dtype=torch.bfloat16, device=device)
+        self.stats = None
+        if with_stats:
+            self.stats = alloc(c.num_pages, c.Hkv, c.P // 16, 2, c.d, dtype=torch.bfloat16,
+                               device=device)
+        self.block_table = torch.as_tensor(c.block_table, dtype=torch.int32, device=device)
+        self.layout = KVLayout(c.num_pages, c.Hkv, c.d, c.P, self.block_table)
+        self.seq_lens = torch.zeros(c.B, dtype=torch.int32, device=device)
+        self.lens = [0] * c.B  # host mirror of seq_lens
+        self.dev_err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.chunk_tokens = chunk_tokens
+        if fill:
+            self.fill()
+
+    def _row_layout(self, b: int) -> KVLayout:
+        c = self.case
+        return KVLayout(c.num_pages, c.Hkv, c.d, c.P, self.block_table[b:b + 1])
+
+    def fill(self, lens=None):
+        """Append each request's tokens up to lens (default: the case's step-0 lengths)."""
+        lens = self.case.lens if lens is None else lens
+        for b, L in enumerate(lens):
+            lay = self._row_layout(b)
+            while self.lens[b] < L:
+                t0 = self.lens[b]
+                t1 = min(L, t0 + self.chunk_tokens)
+                K, V = self.case.kv(b, t0, t1, self.device)
+                dattn_kv_append(lay, self.k_pool, self.v_pool, self.stats,
+                                K.unsqueeze(0).contiguous(), V.unsqueeze(0).contiguous(),
+                                self.seq_lens[b:b + 1], self.dev_err)
+                self.lens[b] = t1
+
+    def new_tokens(self, T: int = 1):
+        """The next T tokens of every request (continuing each seeded stream): [B][T][Hkv][d]."""
+        ks, vs = [], []
+        for b in range(self.case.B):
+            K, V = self.case.kv(b, self.lens[b], self.lens[b] + T, self.device)
+            ks.append(K)
+            vs.append(V)
+        return torch.stack(ks).contiguous(), torch.stack(vs).contiguous()
+
+    def append(self, k_new, v_new):
+        """One batched append of k_new/v_new ([B][T][Hkv][d]) at the current lengths."""
+        T = k_new.shape[1]
+        dattn_kv_append(self.layout, self.k_pool, self.v_pool, self.stats, k_new, v_new,
+                        self.seq_lens, self.dev_err)
+        self.lens = [L + T for L in self.lens]
+
+    def workspace(self, top_k: int = 0, num_splits: int = 0) -> Workspace:
+        c = self.case
+        return Workspace(c.B, c.Hq, c.Hkv, c.d, top_k=top_k, num_splits=num_splits,
+                         device=self.device)
+
+    def sparse_config(self, selected) -> SparseConfig:
+        c = self.case
+        hk = torch.as_tensor(c.head_kind_array(), dtype=torch.int8, device=self.device)
+        return SparseConfig(hk, c.sinks, c.local, c.top_k, selected)
+
+    def decode(self, q, out, ws, m_g=None, e_g=None, sparse=None, num_splits=0):
+        dattn_decode(self.layout, self.k_pool, self.v_pool, q, self.case.scale, self.seq_lens,
+                     out, ws, m_g=m_g, e_g=e_g, sparse=sparse, num_splits=num_splits,
+                     dev_err=self.dev_err)
+
+    def select(self, q, selected, ws, num_splits=0):
+        c = self.case
+        hk = torch.as_tensor(c.head_kind_array(), dtype=torch.int8, device=self.device)
+        dattn_page_select(self.layout, self.stats, q, self.seq_lens, hk, c.top_k, selected, ws,
+                          num_splits=num_splits, dev_err=self.dev_err)

@@ -1,0 +1,162 @@
+"""Host-side checks of libdattn.so that need no GPU: it loads, it exports every symbol
+include/dattn.h declares, it rejects bad arguments before launching anything, and its
+balanced split plan partitions the tiles exactly."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def dattn():
+    from split_kv_decode_distattention_gb300 import _build
+    _build.build()
+    import split_kv_decode_distattention_gb300 as d
+    d.load_library()
+    return d
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "dattn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dattn_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(dattn):
+    names = _declared_symbols()
+    assert {"dattn_kv_append", "dattn_partial", "dattn_merge", "dattn_decode",
+            "dattn_page_select"} <= set(names)
+    lib = ctypes.CDLL(dattn.library_path())
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+
+
+def test_version_and_status_strings(dattn):
+    assert "sm_103a" in dattn.dattn_version()
+    assert dattn.dattn_status_string(0) == "DATTN_OK"
+    assert dattn.dattn_status_string(3) == "DATTN_ERR_WORKSPACE"
+    assert dattn.dattn_status_string(99) == "DATTN_UNKNOWN_STATUS"
+
+
+def test_split_plan_partitions_tiles_exactly(dattn):
+    rng = np.random.default_rng(0)
+    for _ in range(200):
+        W = int(rng.integers(0, 5000))
+        G = int(rng.integers(1, 700))
+        ranges = [dattn.dattn_split_range(W, G, c) for c in range(G)]
+        assert ranges[0][0] == 0 and ranges[-1][1] == W
+        sizes = [e - b for b, e in ranges]
+        assert all(ranges[c][1] == ranges[c + 1][0] for c in range(G - 1))
+        assert max(sizes) - min(sizes) <= 1
+        if W:
+            for t in rng.integers(0, W, size=20):
+                c = dattn.dattn_split_owner(int(t), W, G)
+                b, e = ranges[c]
+                assert b <= t < e
+    assert dattn.dattn_split_owner(5, 5, 3) == -1
+
+
+def test_split_slots_are_distinct_per_cta_and_segment(dattn):
+    """A piece of segment s in CTA c uses workspace slot c + s; slots never collide."""
+    rng = np.random.default_rng(1)
+    for _ in range(50):
+        lens = rng.integers(0, 40, size=int(rng.integers(1, 30)))
+        W = int(lens.sum())
+        G = int(rng.integers(1, 50))
+        if W == 0:
+            continue
+        starts = np.concatenate([[0], np.cumsum(lens)])
+        used = set()
+        for s, n in enumerate(lens):
+            if n == 0:
+                continue
+            c0 = dattn.dattn_split_owner(int(starts[s]), W, G)
+            c1 = dattn.dattn_split_owner(int(starts[s] + n - 1), W, G)
+            if c0 == c1:
+                continue  # finished inside one CTA, no slot
+            for c in range(c0, c1 + 1):
+                assert (c + s) not in used
+                used.add(c + s)
+                assert c + s < G + len(lens)
+
+
+def _lay(dattn, **kw):
+    import torch
+    bt = torch.zeros(1, 4, dtype=torch.int32)
+    args = dict(num_pages=8, num_kv_heads=2, head_dim=128, page_size=16)
+    args.update(kw)
+    return dattn.KVLayout(args["num_pages"], args["num_kv_heads"], args["head_dim"],
+                          args["page_size"], bt)
+
+
+def _decode_status(dattn, layout, B=1, Hq=4, sparse=None):
+    lib = dattn.load_library()
+    p = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    return lib.dattn_decode(ctypes.byref(layout.c) if layout else None, p, p, p, B, Hq, 0.1, p,
+                            sparse, 0, p, 1 << 20, p, None, None, None, None)
+
+
+def test_decode_rejects_bad_shapes_before_launch(dattn):
+    INVALID, UNSUPPORTED = 1, 2
+    assert _decode_status(dattn, None) == INVALID
+    assert _decode_status(dattn, _lay(dattn, head_dim=96)) == UNSUPPORTED
+    assert _decode_status(dattn, _lay(dattn, page_size=24)) == UNSUPPORTED
+    assert _decode_status(dattn, _lay(dattn, page_size=512)) == UNSUPPORTED
+    assert _decode_status(dattn, _lay(dattn), Hq=3) == INVALID          # Hq % Hkv != 0
+    assert _decode_status(dattn, _lay(dattn), Hq=18 * 2) == UNSUPPORTED  # group of 18
+    assert _decode_status(dattn, _lay(dattn), B=5000) == UNSUPPORTED
+    assert _decode_status(dattn, _lay(dattn), B=-1) == INVALID
+    assert _decode_status(dattn, _lay(dattn, num_pages=0)) == INVALID
+    # a block table too large for 32-bit TMA coordinates
+    assert _decode_status(dattn, _lay(dattn, num_pages=1 << 26, page_size=64)) == UNSUPPORTED
+
+
+def test_sparse_settings_are_validated(dattn):
+    import torch
+    hk = torch.zeros(2, dtype=torch.int8)
+    lay = _lay(dattn)
+    bad = dattn.SparseConfig(hk, -1, 8, 4, torch.zeros(1, 2, 4, dtype=torch.int32))
+    assert _decode_status(dattn, lay, sparse=ctypes.byref(bad.c)) == 1
+    big = dattn.SparseConfig(hk, 4, 8, 1000, torch.zeros(1, 2, 4, dtype=torch.int32))
+    assert _decode_status(dattn, lay, sparse=ctypes.byref(big.c)) == 2
+    nosel = dattn.SparseConfig(hk, 4, 8, 4, None)
+    assert _decode_status(dattn, lay, sparse=ctypes.byref(nosel.c)) == 1
+
+
+def test_other_entry_points_validate(dattn):
+    lib = dattn.load_library()
+    p = ctypes.c_void_p(16)
+    lay = _lay(dattn)
+    # append: negative sizes, misaligned pointers
+    assert lib.dattn_kv_append(ctypes.byref(lay.c), p, p, None, p, p, -1, 1, p, None, None) == 1
+    assert lib.dattn_kv_append(ctypes.byref(lay.c), ctypes.c_void_p(18), p, None, p, p, 1, 1, p,
+                               None, None) == 1
+    assert lib.dattn_kv_append(ctypes.byref(lay.c), p, p, None, p, p, 0, 5, p, None, None) == 0
+    # merge: unsupported head_dim, null indptr
+    assert lib.dattn_merge(1, 1, 4, 256, p, p, p, p, p, None, None, None, None, None) == 2
+    assert lib.dattn_merge(1, 1, 4, 64, None, p, p, p, p, None, None, None, None, None) == 1
+    assert lib.dattn_merge(0, 0, 4, 64, None, None, None, None, None, None, None, None, None,
+                           None) == 0
+    # partial: C too large, nulls
+    assert lib.dattn_partial(ctypes.byref(lay.c), p, p, p, 1, 4, 0.1, p, 5000, p, p, p, p, p, p,
+                             p, 1 << 20, 0, None, None) == 2
+    assert lib.dattn_partial(ctypes.byref(lay.c), p, p, p, 1, 4, 0.1, p, 2, None, p, p, p, p, p,
+                             p, 1 << 20, 0, None, None) == 1
+    # page select: top_k too large
+    assert lib.dattn_page_select(ctypes.byref(lay.c), p, p, 1, 4, p, p, 300, p, p, 1 << 20, 0,
+                                 None, None) == 2
+
+
+def test_workspace_size(dattn):
+    assert dattn.dattn_workspace_size(8, 32, 32, 128, 0, 304) > 0
+    assert dattn.dattn_workspace_size(8, 32, 32, 96, 0, 0) == 0
+    assert dattn.dattn_workspace_size(8, 30, 8, 128, 0, 0) == 0
+    a = dattn.dattn_workspace_size(8, 32, 8, 128, 0, 100)
+    b = dattn.dattn_workspace_size(8, 32, 8, 128, 64, 100)
+    assert b >= a
+    # counters (8*8 ints, padded to 256 B) + (G + segments) slots of g*(d+2) floats
+    assert a == 256 + (100 + 64) * 4 * 130 * 4
