@@ -1,0 +1,519 @@
+"""Benchmark of the split-KV decode path on GB300.
+
+One step is one decode layer-step of the whole batch through the library's C ABI:
+  dense workloads:  dattn_kv_append (one new token per request), then dattn_decode
+                    (split-KV MicroAttention partials plus the in-launch merge);
+  sparse-512k:      the same, plus dattn_page_select at the start of every reuse window.
+The metric is achieved HBM bandwidth in GB/s: the algorithmic bytes of the step (valid K/V
+read, statistics scanned, new tokens written, queries, outputs, block table) divided by
+the device time of the step. The time per layer-step and the fraction of the 8 TB/s
+roofline are reported beside it. L2 is flushed before every timed step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl dattn|reference]
+
+--impl reference times the CPU oracle (test infrastructure) on the host cores over a
+bounded sample of the same workload and prints the same JSON line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "split-KV decode attention: achieved HBM GB/s vs 8 TB/s; μs per layer-step"
+ROOFLINE_8TBS = 8000.0  # GB/s, the roofline the metric is quoted against
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOAD_TEXT = {
+    "dense-tiny": "dense GQA decode, batch 1, 8 q / 2 KV heads, head_dim 64, 4096 tokens, "
+                  "16-token pages, identity block table",
+    "mha-32k": "Llama-2-7B-shaped MHA decode, one layer: batch 8, 32 heads, head_dim 128, "
+               "32K tokens per sequence, bf16 paged KV (16-token pages, shuffled pool)",
+    "mha-1m": "single 1M-token request, 32 heads MHA, head_dim 128, 16-token pages, "
+              "64 needle keys",
+    "gqa-ragged": "ragged Llama-3-8B GQA batch: 64 requests, 32 q / 8 KV heads, head_dim 128, "
+                  "lengths log-uniform 1K-256K, 16-token pages",
+    "sparse-512k": "LServe-style block-sparse decode: batch 8, 32 q / 8 KV heads, head_dim "
+                   "128, 512K context, 64-token pages of four 16-token logical pages, "
+                   "4 retrieval + 4 streaming KV heads, top-64 pages reused 16 steps, "
+                   "4 sinks + 8 local",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="mha-32k", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--impl", default="dattn", choices=["dattn", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling only)")
+    ap.add_argument("--ctx", type=int, default=0, help="override the context (profiling only)")
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="short run for ncu: no e2e, no CPU baseline, no clock sampling")
+    return ap.parse_args()
+
+
+def make_case(args):
+    from split_kv_decode_distattention_gb300 import workloads as W
+    name = args.config
+    kw = {}
+    if name in ("mha-32k", "sparse-512k"):
+        if args.batch:
+            kw["B"] = args.batch
+        if args.ctx:
+            kw["L"] = args.ctx
+    elif name == "mha-1m" and args.ctx:
+        kw["L"] = args.ctx
+    elif name == "gqa-ragged" and args.batch:
+        kw["B"] = args.batch
+    case = W.CASES[name](seed=args.seed, **kw)
+    # room for the tokens the timed and warm-up steps append
+    case.reserve_tokens = max(case.reserve_tokens, 2 * (args.steps + args.warmup) + 64)
+    case._make_block_table()
+    return case
+
+
+def step_bytes(case, lens_after, sparse_sel_step: bool) -> dict:
+    """Algorithmic bytes of one layer-step, given the lengths after the append."""
+    B, Hq, Hkv, d, P = case.B, case.Hq, case.Hkv, case.d, case.P
+    q_bytes = B * Hq * d * 2
+    out_bytes = B * Hq * d * 4 + 2 * B * Hq * 4
+    new_kv = B * Hkv * d * 2 * 2 * 2  # read k_new/v_new, write into the pool
+    bt = sum(-(-L // P) for L in lens_after) * 4
+    if case.head_kind is None:
+        kv = sum(lens_after) * Hkv * d * 2 * 2
+        decode = kv + q_bytes + out_bytes + bt + B * 4
+        return {"decode": decode, "append": new_kv, "select": 0,
+                "step": decode + new_kv}
+    kinds = case.head_kind
+    nret = sum(1 for k in kinds if k == 1)
+    nstr = sum(1 for k in kinds if k == 2)
+    nden = sum(1 for k in kinds if k == 0)
+    kv = 0
+    for L in lens_after:
+        kv += nden * L * d * 4
+        kv += nret * min(case.top_k * P, L) * d * 4
+        s_end = min(case.sinks, L)
+        l0 = max(case.sinks, L - case.local)
+        kv += nstr * (s_end + max(0, L - l0)) * d * 4
+    sel_rows = B * nret * case.top_k * 4
+    decode = kv + q_bytes + out_bytes + sel_rows + B * 4
+    stats = sum(L // 16 + (1 if L % 16 else 0) for L in lens_after) * nret * 2 * d * 2
+    select = (stats + q_bytes + sel_rows + bt) if sparse_sel_step else 0
+    # the stats update inside the append (read + write one logical page per request/head)
+    new_kv += B * Hkv * 2 * d * 2 * 2
+    return {"decode": decode, "append": new_kv, "select": select,
+            "step": decode + new_kv + select}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "split_kv_decode_distattention_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(config: str):
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary, if it was
+    taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(p)).get(config)
+    except Exception:
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------------------ GPU arm
+
+def run_dattn(args, rank: int, world: int):
+    import torch
+    import torch.distributed as dist
+
+    import split_kv_decode_distattention_gb300 as dattn
+    from split_kv_decode_distattention_gb300.harness import PagedCache
+
+    dattn.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = make_case(args)
+    sparse = case.head_kind is not None
+    cache = PagedCache(case, dev, with_stats=sparse, chunk_tokens=16384)
+    B, Hq, d = case.B, case.Hq, case.d
+    ws = cache.workspace(top_k=case.top_k, num_splits=args.num_splits)
+    out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
+    m_g = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+    e_g = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+    sel = torch.full((B, case.Hkv, max(case.top_k, 1)), -1, dtype=torch.int32, device=dev)
+    spc = cache.sparse_config(sel) if sparse else None
+    stream = torch.cuda.current_stream()
+    total = args.warmup + args.steps
+    # per-step inputs prepared up front (device-resident for the kernel timing)
+    qs = [case.q(s, dev) for s in range(total)]
+    per_req = [case.kv(b, case.lens[b], case.lens[b] + total, dev) for b in range(B)]
+    k_all = torch.stack([k for k, _ in per_req])  # [B][total][Hkv][d]
+    v_all = torch.stack([v for _, v in per_req])
+    del per_req
+    news = [(k_all[:, s:s + 1].contiguous(), v_all[:, s:s + 1].contiguous())
+            for s in range(total)]
+    del k_all, v_all
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+
+    def one_step(s, ev=None):
+        kn, vn = news[s]
+        cache.append(kn, vn)
+        launches = 1
+        if sparse and s % case.reuse == 0:
+            cache.select(qs[s], sel, ws, num_splits=args.num_splits)
+            launches += 1
+        if ev is not None:
+            ev[0].record(stream)
+        cache.decode(qs[s], out, ws, m_g=m_g, e_g=e_g, sparse=spc, num_splits=args.num_splits)
+        if ev is not None:
+            ev[1].record(stream)
+        return launches + 1
+
+    for s in range(args.warmup):
+        one_step(s)
+    torch.cuda.synchronize()
+    lens0 = list(cache.lens)
+    clocks = ClockSampler(dev.index) if (rank == 0 and not args.no_clocks and
+                                         not args.profile) else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+    step_ms, dec_ms, launches = [], [], 0
+    bytes_total, dec_bytes_total = 0, 0
+    for i in range(args.steps):
+        s = args.warmup + i
+        flush.zero_()  # L2 flush, outside the timed region
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launches += one_step(s, (d0, d1))
+        e1.record(stream)
+        lens_after = [L + i + 1 for L in lens0]
+        sb = step_bytes(case, lens_after, sparse and s % case.reuse == 0)
+        bytes_total += sb["step"]
+        dec_bytes_total += sb["decode"]
+        step_ms.append((e0, e1))
+        dec_ms.append((d0, d1))
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    step_t = [a.elapsed_time(b) for a, b in step_ms]
+    dec_t = [a.elapsed_time(b) for a, b in dec_ms]
+    err = int(cache.dev_err.item())
+    if err:
+        raise RuntimeError(f"device error word {err:#x}")
+    ms_total = sum(step_t)
+    if world > 1:
+        t = torch.tensor([ms_total, float(bytes_total)], dtype=torch.float64, device=dev)
+        tmax = t.clone()
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        ms_max, bytes_all = float(tmax[0]), float(t[1])
+    else:
+        ms_max, bytes_all = ms_total, float(bytes_total)
+    res = {
+        "ms_total": ms_max, "bytes_all": bytes_all, "step_ms": step_t, "dec_ms": dec_t,
+        "dec_bytes": dec_bytes_total / args.steps, "launches": launches, "clocks": clk,
+        "case": case, "lens0": lens0,
+    }
+
+    # ---- end to end through the public API with host buffers (pinned) ----------------
+    if not args.no_e2e and not args.profile:
+        res["e2e"] = run_e2e(args, case, cache, ws, spc, sel, flush, dev)
+    return res
+
+
+def run_e2e(args, case, cache, ws, spc, sel, flush, dev):
+    import torch
+    B, Hq, Hkv, d = case.B, case.Hq, case.Hkv, case.d
+    steps = max(3, min(args.steps, 20))
+    hq = [case.q(100 + s, "cpu").pin_memory() for s in range(steps)]
+    hk = [torch.randn(B, 1, Hkv, d).to(torch.bfloat16).pin_memory() for _ in range(steps)]
+    hv = [torch.randn(B, 1, Hkv, d).to(torch.bfloat16).pin_memory() for _ in range(steps)]
+    hout = torch.empty(B, Hq, d, dtype=torch.float32).pin_memory()
+    dq = torch.empty(B, Hq, d, dtype=torch.bfloat16, device=dev)
+    dk = torch.empty(B, 1, Hkv, d, dtype=torch.bfloat16, device=dev)
+    dv = torch.empty_like(dk)
+    out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    lens0 = list(cache.lens)
+    tot_ms, tot_bytes = 0.0, 0
+    for i in range(steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dq.copy_(hq[i], non_blocking=True)
+        dk.copy_(hk[i], non_blocking=True)
+        dv.copy_(hv[i], non_blocking=True)
+        cache.append(dk, dv)
+        if spc is not None and i % case.reuse == 0:
+            cache.select(dq, sel, ws)
+        cache.decode(dq, out, ws, sparse=spc)
+        hout.copy_(out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        tot_ms += e0.elapsed_time(e1)
+        lens_after = [L + i + 1 for L in lens0]
+        tot_bytes += step_bytes(case, lens_after, spc is not None and i % case.reuse == 0)["step"]
+    h2d = hq[0].numel() * 2 + hk[0].numel() * 2 + hv[0].numel() * 2
+    d2h = hout.numel() * 4
+    return {"value": round(tot_bytes / (tot_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "us_per_layer_step": round(tot_ms / steps * 1e3, 2), "steps": steps}
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(case, device, max_pairs: int, seed_step: int = 0):
+    """Host copies of a bounded sample of the workload: (b, h) pairs over full contexts."""
+    import oracle
+    pairs = [(b, h) for b in range(case.B) for h in range(case.Hq)]
+    stride = max(1, len(pairs) // max_pairs)
+    pairs = pairs[::stride][:max_pairs]
+    q = oracle.bf16_bits(case.q(seed_step, device))
+    by_b = {}
+    for b, h in pairs:
+        by_b.setdefault(b, []).append(h)
+    data = []
+    for b, hs in by_b.items():
+        L = case.lens[b]
+        K, V = case.kv(b, 0, L, device)
+        data.append((b, hs, oracle.bf16_bits(K), oracle.bf16_bits(V), L))
+    return q, data
+
+
+def time_oracle(case, q, data, nthreads):
+    """Wall time of the oracle's dense attention over the sample; returns (s, bytes)."""
+    import oracle
+    t0 = time.perf_counter()
+    nbytes = 0
+    used = nthreads
+    for b, hs, K, V, L in data:
+        _, _, _, used = oracle.attention_pairs(q[b:b + 1], K, V, [0, L], [(0, h) for h in hs],
+                                               case.scale, nthreads=nthreads)
+        nbytes += len(hs) * L * case.d * 2 * 2
+    return time.perf_counter() - t0, nbytes, used
+
+
+def cpu_baseline(case, device):
+    import oracle
+    oracle.load()
+    nthreads = len(os.sched_getaffinity(0))
+    # sample: a fixed fraction of (request, query head) pairs over their full contexts
+    tokens = sum(case.lens)
+    budget_pairs = max(nthreads, int(6e9 / max(1, tokens // case.B * case.d * 4)))
+    q, data = oracle_sample(case, device, budget_pairs)
+    secs, nbytes, used = time_oracle(case, q, data, nthreads)
+    npairs = sum(len(hs) for _, hs, _, _, _ in data)
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": used,
+            "kind": "oracle",
+            "sample": f"{npairs} of {case.B * case.Hq} (request, query head) pairs of the "
+                      f"{case.name} workload over their full contexts (dense attention, "
+                      f"fp64), {secs:.2f} s"}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle timed on the host cores, on a bounded sample of the same workload."""
+    import oracle
+    if rank != 0:
+        return
+    import torch
+    oracle.load()
+    case = make_case(args)
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    nthreads = len(os.sched_getaffinity(0))
+    budget_pairs = max(nthreads, min(case.B * case.Hq, 64))
+    if case.name in ("mha-1m",):
+        budget_pairs = nthreads
+    q, data = oracle_sample(case, device, budget_pairs)
+    for _ in range(args.warmup):
+        time_oracle(case, q, data[:1], nthreads)
+    times, used = [], nthreads
+    nbytes = 0
+    for _ in range(args.steps):
+        secs, nbytes, used = time_oracle(case, q, data, nthreads)
+        times.append(secs)
+    npairs = sum(len(hs) for _, hs, _, _, _ in data)
+    total = sum(times)
+    value = nbytes * args.steps / total / 1e9
+    # a layer-step is the whole batch: scale the sample time to all pairs
+    us_step = total / args.steps * (case.B * case.Hq / npairs) * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "us_per_layer_step": round(us_step, 1),
+        "config": config_obj(case, args),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": used,
+                         "kind": "oracle",
+                         "sample": f"{npairs} of {case.B * case.Hq} (request, query head) pairs "
+                                   f"per step, full contexts, fp64 dense attention"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_obj(case, args):
+    c = {"workload": f"{case.name}: {WORKLOAD_TEXT[case.name]}", "batch": case.B,
+         "q_heads": case.Hq, "kv_heads": case.Hkv, "head_dim": case.d, "page_size": case.P,
+         "context_tokens": (case.lens[0] if len(set(case.lens)) == 1 else
+                            f"{min(case.lens)}-{max(case.lens)} (sum {sum(case.lens)})"),
+         "seed": args.seed, "l2": "flushed (512 MiB write) before every timed step",
+         "parallelism": "replicas" if args.gpus > 1 else "single GPU",
+         "step": ("dattn_kv_append (1 token/request) + dattn_decode" +
+                  (" + dattn_page_select every 16 steps (block-sparse)"
+                   if case.head_kind is not None else ""))}
+    if args.batch or args.ctx:
+        c["reduced_for_profiling"] = True
+    return c
+
+
+def main():
+    args = parse_args()
+    if args.profile:
+        args.no_e2e = args.no_cpu_baseline = args.no_clocks = True
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    res = run_dattn(args, rank, world)
+    case = res["case"]
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case, "cuda")
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    steps = args.steps
+    ms_step = res["ms_total"] / steps
+    value = res["bytes_all"] / (res["ms_total"] * 1e-3) / 1e9
+    dec_avg_ms = sum(res["dec_ms"]) / steps
+    achieved = res["dec_bytes"] / (dec_avg_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    traffic = traffic_record(args.config)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/Q)",
+        "us_per_layer_step": round(ms_step * 1e3, 2),
+        "frac_of_8tbs": round(value / ROOFLINE_8TBS, 4),
+        "config": config_obj(case, args),
+        "roofline": {"bound": "hbm", "kernel": "attention_kernel (dattn_decode)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "traffic": traffic, "algorithmic_bytes_per_launch": int(res["dec_bytes"]),
+                     "avg_launch_us": round(dec_avg_ms * 1e3, 2)},
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+        "cpu_baseline": cpu,
+    }
+    if "e2e" in res:
+        line["e2e"] = res["e2e"]
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

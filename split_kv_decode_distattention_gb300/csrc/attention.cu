@@ -493,8 +493,12 @@ attention_kernel(const __grid_constant__ AttnParams p,
     }
     const Plan plan(p, sm);
     const int32_t W = sm.item_start()[p.nitems];
-    const int32_t t_begin = (int32_t)split_begin(W, G, cta);
-    const int32_t t_end = (int32_t)split_begin(W, G, cta + 1);
+    // Only the first min(G, W) CTAs take tiles, so that every participating CTA owns at
+    // least one tile: the pieces of a segment then come from consecutive CTAs
+    // c_first..c_last, and each of them arrives on the segment's counter exactly once.
+    const int32_t Gw = W < G ? (W > 0 ? W : 1) : G;
+    const int32_t t_begin = cta < Gw ? (int32_t)split_begin(W, Gw, cta) : 0;
+    const int32_t t_end = cta < Gw ? (int32_t)split_begin(W, Gw, cta + 1) : 0;
 
     // segments without tiles have no owner: CTA (s mod G) writes their empty result
     for (int32_t s = cta; s < p.nseg; s += G) {
@@ -642,8 +646,8 @@ attention_kernel(const __grid_constant__ AttnParams p,
         if (!whole) {
             // hand the piece over: the CTA that delivers the last piece merges them all
             named_bar_sync(1, kConsumerWarps * 32);
-            const int32_t c_first = split_owner(sst, W, G);
-            const int32_t c_last = split_owner(sst + slen - 1, W, G);
+            const int32_t c_first = split_owner(sst, W, Gw);
+            const int32_t c_last = split_owner(sst + slen - 1, W, Gw);
             const int32_t npieces = c_last - c_first + 1;
             if (ctid == 0) {
                 __threadfence();

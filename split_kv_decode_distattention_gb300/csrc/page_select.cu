@@ -206,8 +206,10 @@ __global__ void __launch_bounds__(kSelThreads) page_select_kernel(const __grid_c
         const int32_t r = (t - item_start[lo]) / n;
         return lo * p.Hkv + ret_heads[r];
     };
-    const int32_t t_begin = (int32_t)split_begin(W, G, cta);
-    const int32_t t_end = (int32_t)split_begin(W, G, cta + 1);
+    // only the first min(G, W) CTAs take units, so each participating CTA owns at least one
+    const int32_t Gw = W < G ? (W > 0 ? W : 1) : G;
+    const int32_t t_begin = cta < Gw ? (int32_t)split_begin(W, Gw, cta) : 0;
+    const int32_t t_end = cta < Gw ? (int32_t)split_begin(W, Gw, cta + 1) : 0;
 
     // rows of heads without units (other kinds, or empty requests) are all -1
     for (int32_t s = cta; s < p.nseg; s += G) {
@@ -405,8 +407,8 @@ __global__ void __launch_bounds__(kSelThreads) page_select_kernel(const __grid_c
             uint64_t* my = p.slots + (int64_t)(cta + s) * K;
             for (int r = ctid; r < K; r += kConsumerWarps * 32) my[r] = sortbuf[r];
             named_bar_sync(1, kConsumerWarps * 32);
-            const int32_t c_first = split_owner(sst, W, G);
-            const int32_t c_last = split_owner(sst + slen - 1, W, G);
+            const int32_t c_first = split_owner(sst, W, Gw);
+            const int32_t c_last = split_owner(sst + slen - 1, W, Gw);
             const int32_t npieces = c_last - c_first + 1;
             if (ctid == 0) {
                 __threadfence();

@@ -85,6 +85,9 @@ DENSE_CASES = [
     (64, 16, 2, 64, [999, 1, 2048], 1),
     (128, 2, 2, 32, [480, 500], 2),
     (128, 6, 3, 16, [5000], 0),
+    # more CTAs than tiles: only the first W CTAs take work
+    (128, 4, 4, 16, [1, 15, 16, 17], 500),
+    (64, 8, 2, 64, [100, 3], 1000),
 ]
 
 
@@ -294,6 +297,7 @@ def _oracle_selection(case, cache, q):
     (64, 128, [5000, 20], 64, 7),
     (16, 64, [3000, 1, 777], 32, 0),
     (64, 64, [64 * 40], 64, 3),  # top_k covers every page
+    (64, 128, [64 * 50 + 3, 64 * 7], 8, 4000),  # more CTAs than pages
 ])
 def test_page_select_bit_exact(P, d, lens, top_k, splits):
     _lib()
