@@ -210,6 +210,31 @@ dattn_status_t dattn_decode(const dattn_kv_layout *layout, const dattn_bf16 *k_p
                             int32_t *dev_err, void *stream);
 
 /*
+ * dattn_decode without a workspace argument: the same fused decode as dattn_decode, with its
+ * scratch in a fixed 8 MiB device array inside the library instead of in caller memory.
+ * The pages have no counterpart to this call; it exists for callers that cannot allocate
+ * device memory. Examples: a plugin or custom op handed only its input and output
+ * pointers, code running under a framework allocator that owns all device memory, and
+ * latency-critical code that cannot risk the device synchronisation cudaMalloc may cause.
+ * The call allocates nothing.
+ *
+ *  - Arguments, outputs and results are those of dattn_decode, minus ws and ws_bytes.
+ *  - A problem whose dattn_workspace_size(B, Hq, Hkv, head_dim, 0, num_splits) exceeds
+ *    8 MiB (8388608 bytes) is rejected with DATTN_ERR_WORKSPACE before any launch.
+ *  - The first call on a device looks up the array's device address and caches it. Make
+ *    that first call before any stream capture on that device.
+ *  - All calls on a device share the one array, and it keeps the last call's contents. Each
+ *    call clears the part that must start at zero, on its own stream. Calls that overlap on
+ *    the GPU (unordered streams) race on the array and give wrong results.
+ */
+dattn_status_t dattn_decode_noalloc(const dattn_kv_layout *layout, const dattn_bf16 *k_pool,
+                                    const dattn_bf16 *v_pool, const dattn_bf16 *q, int32_t B,
+                                    int32_t Hq, float scale, const int32_t *seq_lens,
+                                    const dattn_sparse *sparse, int32_t num_splits,
+                                    float *out, float *m_g, float *e_g, int32_t *dev_err,
+                                    void *stream);
+
+/*
  * Page scoring and top-K selection for retrieval heads [LV §2.2.2, §3.1.2]. For every
  * request b and KV head h of kind DATTN_HEAD_RETRIEVAL:
  *   logical score  sigma(lp) = max over the g query heads j of

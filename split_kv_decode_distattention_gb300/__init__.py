@@ -23,6 +23,7 @@ import torch
 __all__ = [
     "KVLayout", "SparseConfig", "DattnError", "load_library", "library_path",
     "dattn_kv_append", "dattn_partial", "dattn_merge", "dattn_decode", "dattn_page_select",
+    "dattn_decode_noalloc",
     "dattn_workspace_size", "dattn_workspace_init", "dattn_auto_splits", "dattn_split_range",
     "dattn_split_owner", "dattn_status_string", "dattn_version", "Workspace",
     "HEAD_DENSE", "HEAD_RETRIEVAL", "HEAD_STREAMING", "DEVERR",
@@ -68,6 +69,8 @@ _SIGS = {
                           ctypes.POINTER(_Sparse), _I, _P, _SZ, _P, _P, _P, _P, _P]),
     "dattn_page_select": (_I, [ctypes.POINTER(_Layout), _P, _P, _I, _I, _P, _P, _I, _P, _P, _SZ,
                                _I, _P, _P]),
+    "dattn_decode_noalloc": (_I, [ctypes.POINTER(_Layout), _P, _P, _P, _I, _I, _F, _P,
+                                  ctypes.POINTER(_Sparse), _I, _P, _P, _P, _P, _P]),
     "dattn_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "dattn_workspace_init": (_I, [_P, _SZ, _P]),
     "dattn_auto_splits": (_I, [_I64]),
@@ -271,6 +274,24 @@ def dattn_decode(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, ou
         ctypes.byref(layout.c), _ptr(k_pool), _ptr(v_pool), _ptr(q), B, Hq, scale,
         _ptr(seq_lens), sp, num_splits, _ptr(ws.buffer), ws.buffer.numel(), _ptr(out),
         _ptr(m_g), _ptr(e_g), _ptr(dev_err), _stream(stream)), "dattn_decode")
+
+
+def dattn_decode_noalloc(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, out,
+                         m_g=None, e_g=None, sparse: SparseConfig | None = None, num_splits=0,
+                         dev_err=None, stream=None):
+    """dattn_decode with the library's fixed 8 MiB scratch array instead of a workspace.
+
+    For callers that cannot allocate device memory. Calls on one device share the array, so
+    they must not overlap on the GPU. The first call on a device should come before any
+    stream capture.
+    """
+    _bf16(q, "q"); _i32(seq_lens, "seq_lens"); _f32(out, "out")
+    B, Hq = q.shape[0], q.shape[1]
+    sp = ctypes.byref(sparse.c) if sparse is not None else None
+    _check(load_library().dattn_decode_noalloc(
+        ctypes.byref(layout.c), _ptr(k_pool), _ptr(v_pool), _ptr(q), B, Hq, scale,
+        _ptr(seq_lens), sp, num_splits, _ptr(out), _ptr(m_g), _ptr(e_g), _ptr(dev_err),
+        _stream(stream)), "dattn_decode_noalloc")
 
 
 def dattn_page_select(layout: KVLayout, stats, q, seq_lens, head_kind, top_k: int, selected,
