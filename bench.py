@@ -27,6 +27,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -64,6 +66,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--flush", action="store_true", help="flush L2 before every step")
     ap.add_argument("--profile", action="store_true",
                     help="short run for ncu: no e2e, no CPU baseline, no clock sampling")
     return ap.parse_args()
@@ -237,6 +240,12 @@ def run_dattn(args, rank: int, world: int):
     news = [(k_all[:, s:s + 1].contiguous(), v_all[:, s:s + 1].contiguous())
             for s in range(total)]
     del k_all, v_all
+    # L2 hygiene: a step whose K/V working set exceeds 4x the L2 evicts everything the
+    # previous step left there, so it is timed back to back; smaller steps are preceded by
+    # a 512 MiB write that flushes L2.
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    sb0 = step_bytes(case, list(cache.lens), sparse)
+    do_flush = sb0["decode"] < 4 * l2 or args.flush
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     torch.cuda.synchronize()
 
@@ -269,7 +278,8 @@ def run_dattn(args, rank: int, world: int):
     bytes_total, dec_bytes_total = 0, 0
     for i in range(args.steps):
         s = args.warmup + i
-        flush.zero_()  # L2 flush, outside the timed region
+        if do_flush:
+            flush.zero_()  # L2 flush, outside the timed region
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         d0 = torch.cuda.Event(enable_timing=True)
@@ -302,6 +312,9 @@ def run_dattn(args, rank: int, world: int):
     else:
         ms_max, bytes_all = ms_total, float(bytes_total)
     res = {
+        "l2_policy": (f"flushed (512 MiB write) before every timed step" if do_flush else
+                      f"inputs larger than L2: {sb0['decode'] / 1e9:.2f} GB of K/V per step "
+                      f"vs {l2 / 1e6:.0f} MB L2, timed back to back without a flush"),
         "ms_total": ms_max, "bytes_all": bytes_all, "step_ms": step_t, "dec_ms": dec_t,
         "dec_bytes": dec_bytes_total / args.steps, "launches": launches, "clocks": clk,
         "case": case, "lens0": lens0,
@@ -309,18 +322,20 @@ def run_dattn(args, rank: int, world: int):
 
     # ---- end to end through the public API with host buffers (pinned) ----------------
     if not args.no_e2e and not args.profile:
-        res["e2e"] = run_e2e(args, case, cache, ws, spc, sel, flush, dev)
+        res["e2e"] = run_e2e(args, case, cache, ws, spc, sel, flush if do_flush else None, dev)
     return res
 
 
 def run_e2e(args, case, cache, ws, spc, sel, flush, dev):
+    """The same steps through the public API with host buffers: every step copies its q and
+    new K/V from pinned host memory and reads its output back into pinned host memory."""
     import torch
     B, Hq, Hkv, d = case.B, case.Hq, case.Hkv, case.d
-    steps = max(3, min(args.steps, 20))
+    steps = max(3, min(args.steps, 50))
     hq = [case.q(100 + s, "cpu").pin_memory() for s in range(steps)]
     hk = [torch.randn(B, 1, Hkv, d).to(torch.bfloat16).pin_memory() for _ in range(steps)]
     hv = [torch.randn(B, 1, Hkv, d).to(torch.bfloat16).pin_memory() for _ in range(steps)]
-    hout = torch.empty(B, Hq, d, dtype=torch.float32).pin_memory()
+    houts = [torch.empty(B, Hq, d, dtype=torch.float32).pin_memory() for _ in range(steps)]
     dq = torch.empty(B, Hq, d, dtype=torch.bfloat16, device=dev)
     dk = torch.empty(B, 1, Hkv, d, dtype=torch.bfloat16, device=dev)
     dv = torch.empty_like(dk)
@@ -329,11 +344,16 @@ def run_e2e(args, case, cache, ws, spc, sel, flush, dev):
     torch.cuda.synchronize()
     lens0 = list(cache.lens)
     tot_ms, tot_bytes = 0.0, 0
+    pairs = []
+    e_all0 = torch.cuda.Event(enable_timing=True)
+    e_all1 = torch.cuda.Event(enable_timing=True)
+    if flush is None:
+        e_all0.record(stream)
     for i in range(steps):
-        flush.zero_()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        if flush is not None:
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
         dq.copy_(hq[i], non_blocking=True)
         dk.copy_(hk[i], non_blocking=True)
         dv.copy_(hv[i], non_blocking=True)
@@ -341,14 +361,20 @@ def run_e2e(args, case, cache, ws, spc, sel, flush, dev):
         if spc is not None and i % case.reuse == 0:
             cache.select(dq, sel, ws)
         cache.decode(dq, out, ws, sparse=spc)
-        hout.copy_(out, non_blocking=True)
-        e1.record(stream)
-        e1.synchronize()
-        tot_ms += e0.elapsed_time(e1)
+        houts[i].copy_(out, non_blocking=True)
+        if flush is not None:
+            e1 = torch.cuda.Event(enable_timing=True)
+            e1.record(stream)
+            pairs.append((e0, e1))
         lens_after = [L + i + 1 for L in lens0]
         tot_bytes += step_bytes(case, lens_after, spc is not None and i % case.reuse == 0)["step"]
+    if flush is None:
+        e_all1.record(stream)
+    torch.cuda.synchronize()
+    tot_ms = (sum(a.elapsed_time(b) for a, b in pairs) if flush is not None
+              else e_all0.elapsed_time(e_all1))
     h2d = hq[0].numel() * 2 + hk[0].numel() * 2 + hv[0].numel() * 2
-    d2h = hout.numel() * 4
+    d2h = houts[0].numel() * 4
     return {"value": round(tot_bytes / (tot_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "us_per_layer_step": round(tot_ms / steps * 1e3, 2), "steps": steps}
@@ -357,51 +383,69 @@ def run_e2e(args, case, cache, ws, spc, sel, flush, dev):
 # ------------------------------------------------------------------------------ CPU oracle
 
 def oracle_sample(case, device, max_pairs: int, seed_step: int = 0):
-    """Host copies of a bounded sample of the workload: (b, h) pairs over full contexts."""
+    """Host copies of a bounded sample of the workload: evenly spaced (request, query head)
+    pairs over their full contexts. Only the KV heads the sample reads are copied."""
     import oracle
-    pairs = [(b, h) for b in range(case.B) for h in range(case.Hq)]
-    stride = max(1, len(pairs) // max_pairs)
-    pairs = pairs[::stride][:max_pairs]
+    allp = [(b, h) for b in range(case.B) for h in range(case.Hq)]
+    stride = max(1, len(allp) // max_pairs)
+    pairs = allp[::stride][:max_pairs]
     q = oracle.bf16_bits(case.q(seed_step, device))
-    by_b = {}
+    need = {}
     for b, h in pairs:
-        by_b.setdefault(b, []).append(h)
-    data = []
-    for b, hs in by_b.items():
+        need.setdefault(b, set()).add(h // case.g)
+    kv = {}
+    for b, kvhs in need.items():
         L = case.lens[b]
-        K, V = case.kv(b, 0, L, device)
-        data.append((b, hs, oracle.bf16_bits(K), oracle.bf16_bits(V), L))
-    return q, data
+        kvhs = sorted(kvhs)
+        arrs = {h: (np.empty((L, case.d), np.uint16), np.empty((L, case.d), np.uint16))
+                for h in kvhs}
+        for t0 in range(0, L, 65536):
+            t1 = min(L, t0 + 65536)
+            K, V = case.kv(b, t0, t1, device)
+            for h in kvhs:
+                arrs[h][0][t0:t1] = oracle.bf16_bits(K[:, h])
+                arrs[h][1][t0:t1] = oracle.bf16_bits(V[:, h])
+        for h in kvhs:
+            kv[(b, h)] = arrs[h]
+    return q, pairs, kv
 
 
-def time_oracle(case, q, data, nthreads):
-    """Wall time of the oracle's dense attention over the sample; returns (s, bytes)."""
+def time_oracle(case, q, pairs, kv, nthreads):
+    """Wall time of the oracle's dense attention over the sampled pairs, run on nthreads
+    host threads (each call is one plain C routine that releases the GIL)."""
     import oracle
+    from concurrent.futures import ThreadPoolExecutor
+
+    def one(pair):
+        b, h = pair
+        K, V = kv[(b, h // case.g)]
+        oracle.attention(q[b, h], K, V, case.scale)
+        return K.shape[0] * case.d * 2 * 2
+
     t0 = time.perf_counter()
-    nbytes = 0
-    used = nthreads
-    for b, hs, K, V, L in data:
-        _, _, _, used = oracle.attention_pairs(q[b:b + 1], K, V, [0, L], [(0, h) for h in hs],
-                                               case.scale, nthreads=nthreads)
-        nbytes += len(hs) * L * case.d * 2 * 2
-    return time.perf_counter() - t0, nbytes, used
+    with ThreadPoolExecutor(max_workers=nthreads) as ex:
+        nbytes = sum(ex.map(one, pairs))
+    return time.perf_counter() - t0, nbytes, min(nthreads, len(pairs))
 
 
 def cpu_baseline(case, device):
     import oracle
     oracle.load()
     nthreads = len(os.sched_getaffinity(0))
-    # sample: a fixed fraction of (request, query head) pairs over their full contexts
-    tokens = sum(case.lens)
-    budget_pairs = max(nthreads, int(6e9 / max(1, tokens // case.B * case.d * 4)))
-    q, data = oracle_sample(case, device, budget_pairs)
-    secs, nbytes, used = time_oracle(case, q, data, nthreads)
-    npairs = sum(len(hs) for _, hs, _, _, _ in data)
+    per_pair = max(1, sum(case.lens) // case.B) * case.d * 4
+    budget = max(nthreads, min(case.B * case.Hq, int(4e9 // per_pair)))
+    q, pairs, kv = oracle_sample(case, device, budget)
+    # repeat the sample until about 10 s of CPU work has been timed
+    secs, nbytes, used = time_oracle(case, q, pairs, kv, nthreads)
+    reps = 1
+    while secs * used < 10.0 and reps < 64:
+        s2, n2, _ = time_oracle(case, q, pairs, kv, nthreads)
+        secs, nbytes, reps = secs + s2, nbytes + n2, reps + 1
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": used,
             "kind": "oracle",
-            "sample": f"{npairs} of {case.B * case.Hq} (request, query head) pairs of the "
-                      f"{case.name} workload over their full contexts (dense attention, "
-                      f"fp64), {secs:.2f} s"}
+            "sample": f"{len(pairs)} of {case.B * case.Hq} (request, query head) pairs of the "
+                      f"{case.name} workload over their full contexts (fp64 dense attention), "
+                      f"repeated {reps}x: {secs:.1f} s wall on {used} threads"}
 
 
 def run_reference(args, rank, world):
@@ -414,22 +458,20 @@ def run_reference(args, rank, world):
     case = make_case(args)
     device = "cuda" if torch.cuda.is_available() else "cpu"
     nthreads = len(os.sched_getaffinity(0))
-    budget_pairs = max(nthreads, min(case.B * case.Hq, 64))
-    if case.name in ("mha-1m",):
-        budget_pairs = nthreads
-    q, data = oracle_sample(case, device, budget_pairs)
-    for _ in range(args.warmup):
-        time_oracle(case, q, data[:1], nthreads)
-    times, used = [], nthreads
-    nbytes = 0
+    per_pair = max(1, sum(case.lens) // case.B) * case.d * 4
+    budget = max(nthreads, min(case.B * case.Hq, int(1e9 // per_pair)))
+    q, pairs, kv = oracle_sample(case, device, budget)
+    for _ in range(min(args.warmup, 1)):
+        time_oracle(case, q, pairs[:nthreads], kv, nthreads)
+    times, used, nbytes = [], nthreads, 0
     for _ in range(args.steps):
-        secs, nbytes, used = time_oracle(case, q, data, nthreads)
+        secs, nb, used = time_oracle(case, q, pairs, kv, nthreads)
         times.append(secs)
-    npairs = sum(len(hs) for _, hs, _, _, _ in data)
+        nbytes += nb
     total = sum(times)
-    value = nbytes * args.steps / total / 1e9
-    # a layer-step is the whole batch: scale the sample time to all pairs
-    us_step = total / args.steps * (case.B * case.Hq / npairs) * 1e6
+    value = nbytes / total / 1e9
+    # a layer-step is the whole batch: scale the sample time to every (request, head) pair
+    us_step = total / args.steps * (case.B * case.Hq / len(pairs)) * 1e6
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -439,8 +481,8 @@ def run_reference(args, rank, world):
         "config": config_obj(case, args),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": used,
                          "kind": "oracle",
-                         "sample": f"{npairs} of {case.B * case.Hq} (request, query head) pairs "
-                                   f"per step, full contexts, fp64 dense attention"},
+                         "sample": f"{len(pairs)} of {case.B * case.Hq} (request, query head) "
+                                   f"pairs per step, full contexts, fp64 dense attention"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -452,7 +494,7 @@ def config_obj(case, args):
          "q_heads": case.Hq, "kv_heads": case.Hkv, "head_dim": case.d, "page_size": case.P,
          "context_tokens": (case.lens[0] if len(set(case.lens)) == 1 else
                             f"{min(case.lens)}-{max(case.lens)} (sum {sum(case.lens)})"),
-         "seed": args.seed, "l2": "flushed (512 MiB write) before every timed step",
+         "seed": args.seed,
          "parallelism": "replicas" if args.gpus > 1 else "single GPU",
          "step": ("dattn_kv_append (1 token/request) + dattn_decode" +
                   (" + dattn_page_select every 16 steps (block-sparse)"
@@ -500,12 +542,15 @@ def main():
         "data": "synthetic (seeded N(0,1) bf16 K/V/Q)",
         "us_per_layer_step": round(ms_step * 1e3, 2),
         "frac_of_8tbs": round(value / ROOFLINE_8TBS, 4),
-        "config": config_obj(case, args),
+        "config": dict(config_obj(case, args), l2=res["l2_policy"]),
         "roofline": {"bound": "hbm", "kernel": "attention_kernel (dattn_decode)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": traffic, "algorithmic_bytes_per_launch": int(res["dec_bytes"]),
-                     "avg_launch_us": round(dec_avg_ms * 1e3, 2)},
+                     "avg_launch_us": round(dec_avg_ms * 1e3, 2),
+                     "launch_us_min_med_max": [round(min(res["dec_ms"]) * 1e3, 1),
+                                               round(statistics.median(res["dec_ms"]) * 1e3, 1),
+                                               round(max(res["dec_ms"]) * 1e3, 1)]},
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
         "cpu_baseline": cpu,

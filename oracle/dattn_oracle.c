@@ -40,9 +40,9 @@
  *  R7  A streaming head at length L attends [0, min(S, L)) U [max(S, L - W), L).
  *  R8  k_max/k_min use strict comparison in token order, so the first-seen value wins a
  *      tie (this matters only for +0/-0).
- *  R9  The page selection is decided in the kernel's arithmetic: fp32, a fused
- *      multiply-add chain over d in ascending order (see orc_logical_score_f32). The
- *      fp64 score is the definition, and the tests compare the two.
+ *  R9  The page selection is decided in the kernel's arithmetic: fp32 in a fixed blocked
+ *      order (see orc_logical_score_f32). The fp64 score is the definition, and the tests
+ *      check that the two differ by less than the fp32 error bound.
  */
 #include "dattn_oracle.h"
 
@@ -247,21 +247,43 @@ double orc_logical_score_f64(const uint16_t *q, const uint16_t *kmax, const uint
 }
 
 /*
- * The same score in the arithmetic that decides the selection (reading R9): fp32, with
- * one fused multiply-add per channel in ascending channel order, starting from +0. For
- * q_d >= 0 the larger product is q_d*kmax_d; otherwise it is q_d*kmin_d (kmax_d >= kmin_d).
- * Each product of two bf16 values is exact in fp32; only the running sum rounds.
+ * The same score in the arithmetic that decides the selection (reading R9). It is fp32 in
+ * a fixed order, so that both sides take the same integer decision:
+ *  - the channels are taken in chunks of `chunk` channels (16 when a KV head serves up to
+ *    4 query heads, 8 otherwise);
+ *  - within a chunk there are two fp32 sums, for even and odd channels, both from +0. Per
+ *    channel, each adds by fused multiply-add first max(q,0)*kmax, then min(q,0)*kmin. One
+ *    of the two products is an exact zero, so the sum gains exactly the product that the
+ *    definition's max picks (for q_d >= 0 it is q_d*kmax_d, else q_d*kmin_d);
+ *  - a chunk's partial is even + odd, and the partials are added by a pairwise tree
+ *    (adjacent chunks, then adjacent pairs, and so on).
+ * Each product of two bf16 values is exact in fp32; only the additions round.
  */
-float orc_logical_score_f32(const uint16_t *q, const uint16_t *kmax, const uint16_t *kmin, int d)
+float orc_logical_score_f32(const uint16_t *q, const uint16_t *kmax, const uint16_t *kmin, int d,
+                            int chunk)
 {
-    float acc = 0.0f;
-    for (int c = 0; c < d; ++c) {
-        const float qc = bf16_to_float(q[c]);
-        const float kc = qc >= 0.0f ? bf16_to_float(kmax[c]) : bf16_to_float(kmin[c]);
-        acc = fmaf(qc, kc, acc);
+    float part[64];
+    if (chunk > d) chunk = d;  /* a head narrower than one chunk is one chunk */
+    const int nch = d / chunk;
+    for (int c = 0; c < nch; ++c) {
+        float even = 0.0f, odd = 0.0f;
+        for (int i = 0; i < chunk; i += 2) {
+            const int d0 = c * chunk + i, d1 = d0 + 1;
+            const float q0 = bf16_to_float(q[d0]), q1 = bf16_to_float(q[d1]);
+            even = fmaf(q0 >= 0.0f ? q0 : 0.0f, bf16_to_float(kmax[d0]), even);
+            even = fmaf(q0 >= 0.0f ? 0.0f : q0, bf16_to_float(kmin[d0]), even);
+            odd = fmaf(q1 >= 0.0f ? q1 : 0.0f, bf16_to_float(kmax[d1]), odd);
+            odd = fmaf(q1 >= 0.0f ? 0.0f : q1, bf16_to_float(kmin[d1]), odd);
+        }
+        part[c] = even + odd;
     }
-    return acc;
+    for (int level = 1; level < nch; level <<= 1)
+        for (int c = 0; c < nch; c += 2 * level) part[c] = part[c] + part[c + level];
+    return part[0];
 }
+
+/* Chunk size of the decision arithmetic for a KV head serving g query heads. */
+int orc_decision_chunk(int g) { return g <= 4 ? 16 : 8; }
 
 /*
  * Physical-page scores of one request and one KV head [LV §3.1.2 score_pages: max over the
@@ -289,7 +311,8 @@ void orc_page_scores(const uint16_t *Q, int g, const uint16_t *K, int64_t row_st
                     const double s = orc_logical_score_f64(Q + (int64_t)j * d, kmax, kmin, d);
                     if (s > best) best = s;
                 } else {
-                    const float s = orc_logical_score_f32(Q + (int64_t)j * d, kmax, kmin, d);
+                    const float s = orc_logical_score_f32(Q + (int64_t)j * d, kmax, kmin, d,
+                                                          orc_decision_chunk(g));
                     if (s > best32) best32 = s;
                 }
             }

@@ -95,16 +95,19 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D map over the pool seen as rows of d bf16 values; box = 64 values x 16 rows, 128-byte
-// swizzle, so one box is one 128-byte half of a 16-token row group.
+// 3-D map over the pool seen as rows of d bf16 values, split into 128-byte halves:
+// dim0 = 64 values of one half (contiguous), dim1 = row (stride d*2 bytes), dim2 = half
+// (stride 128 bytes). One box {64, 16, d/64} is a whole 16-token row group of one (page, KV
+// head). It lands in shared memory as [half][row][64 values] with the 128-byte swizzle,
+// which keeps ldmatrix conflict-free. One TMA instruction moves the whole K (or V) tile.
 dattn_status_t make_kv_tensor_map(void* tmap_out, const void* pool, int64_t rows, int D) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (fn == nullptr) return DATTN_ERR_CUDA;
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, 16};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(static_cast<CUtensorMap*>(tmap_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(D / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
+    cuuint32_t box[3] = {64, 16, (cuuint32_t)(D / 64)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(static_cast<CUtensorMap*>(tmap_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                     const_cast<void*>(pool), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -209,8 +212,8 @@ dattn_status_t dattn_partial(const dattn_kv_layout* layout, const dattn_bf16* k_
         return DATTN_ERR_INVALID_ARG;
     if (B == 0) return DATTN_ERR_INVALID_ARG;  // chunks must name a request
     if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(q)) return DATTN_ERR_INVALID_ARG;
-    const int64_t bound = (int64_t)C * layout->num_kv_heads * layout->max_pages_per_req *
-                          (layout->page_size / 16);
+    const int64_t bound = (int64_t)C * layout->num_kv_heads *
+                          ((int64_t)layout->max_pages_per_req * (layout->page_size / 16) + kSegCost);
     if (bound >= (1ll << 31)) return DATTN_ERR_UNSUPPORTED;
     AttnParams p{};
     p.mode = MODE_PARTIAL;
@@ -288,7 +291,7 @@ dattn_status_t dattn_decode(const dattn_kv_layout* layout, const dattn_bf16* k_p
         if (retr > per_head) per_head = retr;
         if (strm > per_head) per_head = strm;
     }
-    const int64_t bound = (int64_t)B * layout->num_kv_heads * per_head;
+    const int64_t bound = (int64_t)B * layout->num_kv_heads * (per_head + kSegCost);
     if (bound >= (1ll << 31)) return DATTN_ERR_UNSUPPORTED;
     p.num_pages = layout->num_pages;
     p.Hkv = layout->num_kv_heads;

@@ -52,6 +52,8 @@ struct Smem {
     __device__ float* ws_m() const { return reinterpret_cast<float*>(base + L.ws_m); }
     __device__ float* ws_e() const { return reinterpret_cast<float*>(base + L.ws_e); }
     __device__ float* ws_o() const { return reinterpret_cast<float*>(base + L.ws_o); }
+    __device__ float* merge_w() const { return reinterpret_cast<float*>(base + L.merge_w); }
+    __device__ float* merge_e() const { return reinterpret_cast<float*>(base + L.merge_e); }
     __device__ int32_t* kind_before() const {
         return reinterpret_cast<int32_t*>(base + L.kind_before);
     }
@@ -85,11 +87,19 @@ __device__ __forceinline__ int32_t head_tiles(int kind, int32_t L, const AttnPar
     return ceil16(L);
 }
 
-// Segment geometry derived from the per-item prefix sums in shared memory.
+// Every segment (one KV head of one request or chunk) is laid out in "cost units": its real
+// 16-token tiles, then kSegCost units that stand for the fixed cost of a piece (fetching the
+// query, merging the warps, handing over a partial). The balanced split cuts the cost space,
+// so a CTA whose range crosses many small segments gets fewer tiles. The extra units are
+// never loaded or scheduled: producer and consumers walk real tiles only.
+
+// Segment geometry derived from the per-item prefix sums (in cost units) in shared memory.
 struct Plan {
     const AttnParams& p;
     const Smem& sm;
     __device__ Plan(const AttnParams& p_, const Smem& sm_) : p(p_), sm(sm_) {}
+
+    __device__ static int32_t cost_of(int32_t real) { return real > 0 ? real + kSegCost : 0; }
 
     // Largest item i with item_start[i] <= t (t < W).
     __device__ int32_t item_of(int32_t t) const {
@@ -102,54 +112,61 @@ struct Plan {
         return lo;
     }
 
-    // Offset of head h's tiles within item i, and head h's tile count.
-    __device__ void head_span(int32_t i, int32_t h, int32_t& off, int32_t& len) const {
+    // Cost offset of head h within item i, its real tile count and its cost.
+    __device__ void head_span(int32_t i, int32_t h, int32_t& off, int32_t& real,
+                              int32_t& cost) const {
         if (p.mode == MODE_SPARSE) {
             const int32_t L = sm.item_len()[i];
             const int32_t n0 = head_tiles(DATTN_HEAD_DENSE, L, p);
             const int32_t n1 = head_tiles(DATTN_HEAD_RETRIEVAL, L, p);
             const int32_t n2 = head_tiles(DATTN_HEAD_STREAMING, L, p);
             const int32_t* kb = sm.kind_before() + 3 * h;
-            off = kb[0] * n0 + kb[1] * n1 + kb[2] * n2;
+            off = kb[0] * cost_of(n0) + kb[1] * cost_of(n1) + kb[2] * cost_of(n2);
             const int k = sm.kinds()[h];
-            len = k == DATTN_HEAD_RETRIEVAL ? n1 : (k == DATTN_HEAD_STREAMING ? n2 : n0);
+            real = k == DATTN_HEAD_RETRIEVAL ? n1 : (k == DATTN_HEAD_STREAMING ? n2 : n0);
         } else {
-            const int32_t per = (sm.item_start()[i + 1] - sm.item_start()[i]) / p.Hkv;
-            off = h * per;
-            len = per;
+            // dense: item_len holds the length; partial: the real tiles per head
+            real = p.mode == MODE_PARTIAL ? sm.item_len()[i] : ceil16(sm.item_len()[i]);
+            off = h * cost_of(real);
         }
+        cost = cost_of(real);
     }
 
-    __device__ void seg_span(int32_t s, int32_t& start, int32_t& len) const {
+    __device__ void seg_span(int32_t s, int32_t& start, int32_t& real, int32_t& cost) const {
         const int32_t i = s / p.Hkv, h = s - i * p.Hkv;
         int32_t off;
-        head_span(i, h, off, len);
+        head_span(i, h, off, real, cost);
         start = sm.item_start()[i] + off;
     }
 
-    // Segment containing tile t, and t's index inside it.
-    __device__ void locate(int32_t t, int32_t& s, int32_t& local) const {
+    // Segment whose cost range contains position t (t < W).
+    __device__ int32_t segment_at(int32_t t) const {
         const int32_t i = item_of(t);
         const int32_t o = t - sm.item_start()[i];
-        int32_t h;
-        if (p.mode == MODE_SPARSE) {
-            // largest head whose offset is <= o; its range is non-empty and contains o
-            int32_t lo = 0, hi = p.Hkv - 1;
-            while (lo < hi) {
-                const int32_t mid = (lo + hi + 1) >> 1;
-                int32_t off, len;
-                head_span(i, mid, off, len);
-                if (off <= o) lo = mid; else hi = mid - 1;
-            }
-            h = lo;
-        } else {
-            const int32_t per = (sm.item_start()[i + 1] - sm.item_start()[i]) / p.Hkv;
-            h = o / per;
+        int32_t lo = 0, hi = p.Hkv - 1;  // largest head whose offset is <= o
+        while (lo < hi) {
+            const int32_t mid = (lo + hi + 1) >> 1;
+            int32_t off, real, cost;
+            head_span(i, mid, off, real, cost);
+            if (off <= o) lo = mid; else hi = mid - 1;
         }
-        int32_t off, len;
-        head_span(i, h, off, len);
-        s = i * p.Hkv + h;
-        local = o - off;
+        return i * p.Hkv + lo;
+    }
+
+    // The next piece of the range [X0, X1) at or after segment s: the real tiles
+    // [r0, r1) of segment s that fall in the range. Returns false when there is none.
+    __device__ bool next_piece(int32_t& s, int32_t X0, int32_t X1, int32_t& cs, int32_t& real,
+                               int32_t& r0, int32_t& r1) const {
+        for (; s < p.nseg; ++s) {
+            int32_t cost;
+            seg_span(s, cs, real, cost);
+            if (cs >= X1) return false;
+            if (cost == 0) continue;
+            r0 = max(X0 - cs, 0);
+            r1 = min(X1 - cs, real);
+            if (r0 < r1) return true;
+        }
+        return false;
     }
 };
 
@@ -255,7 +272,8 @@ struct Consumer {
     __device__ Consumer(const AttnParams& p_, const Smem& sm_, int w, int l)
         : p(p_), sm(sm_), warp(w), lane(l) {}
 
-    __device__ void load_q(int32_t s) {
+    // B fragments of the group's queries for segment s (query head = lane / 4).
+    __device__ void load_q(int32_t s, uint32_t (&dst)[KS][2]) const {
         const int32_t item = s / p.Hkv, kvh = s - item * p.Hkv;
         int32_t b = item;
         if (p.mode == MODE_PARTIAL) b = __ldg(p.chunk_req + item);
@@ -265,8 +283,8 @@ struct Consumer {
             p.q + ((int64_t)(ok ? b : 0) * p.Hq + kvh * p.g + (ok ? n : 0)) * D);
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-            qf[ks][0] = ok ? __ldg(qv + ks * 8 + tig) : 0u;
-            qf[ks][1] = ok ? __ldg(qv + ks * 8 + 4 + tig) : 0u;
+            dst[ks][0] = ok ? __ldg(qv + ks * 8 + tig) : 0u;
+            dst[ks][1] = ok ? __ldg(qv + ks * 8 + 4 + tig) : 0u;
         }
     }
 
@@ -403,6 +421,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
     const int32_t G = gridDim.x, cta = blockIdx.x;
 
     // ---------------------------------------------------------------- setup
+    // Before the dependency wait: only state that no kernel of this library writes.
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(sm.full_bar(s), 1);
@@ -415,21 +434,31 @@ attention_kernel(const __grid_constant__ AttnParams p,
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_v);
     }
-    if (p.mode == MODE_SPARSE && tid == 0) {
-        int32_t cnt[3] = {0, 0, 0};
-        for (int h = 0; h < p.Hkv; ++h) {
-            int k = p.head_kind[h];
-            if (k < 0 || k > 2) k = DATTN_HEAD_DENSE;
-            int32_t* kb = sm.kind_before() + 3 * h;
-            kb[0] = cnt[0]; kb[1] = cnt[1]; kb[2] = cnt[2];
-            sm.kinds()[h] = k;
-            ++cnt[k];
+    if (p.mode == MODE_SPARSE) {
+        for (int h = tid; h < p.Hkv; h += kAttnThreads) {
+            const int k = p.head_kind[h];
+            sm.kinds()[h] = (k < 0 || k > 2) ? DATTN_HEAD_DENSE : k;
         }
-        int32_t* kb = sm.kind_before() + 3 * p.Hkv;
-        kb[0] = cnt[0]; kb[1] = cnt[1]; kb[2] = cnt[2];
+        __syncthreads();
+        if (tid == 0) {
+            int32_t c0 = 0, c1 = 0, c2 = 0;
+            for (int h = 0; h < p.Hkv; ++h) {
+                int32_t* kb = sm.kind_before() + 3 * h;
+                kb[0] = c0; kb[1] = c1; kb[2] = c2;
+                const int k = sm.kinds()[h];
+                c0 += k == DATTN_HEAD_DENSE;
+                c1 += k == DATTN_HEAD_RETRIEVAL;
+                c2 += k == DATTN_HEAD_STREAMING;
+            }
+            int32_t* kb = sm.kind_before() + 3 * p.Hkv;
+            kb[0] = c0; kb[1] = c1; kb[2] = c2;
+        }
     }
+    // From here on the lengths, the selection and the pool may come from the previous kernel.
+    grid_dependency_wait();
+    grid_launch_dependents();
     __syncthreads();
-    // per-item tile counts, then an exclusive scan into item_start
+    // per-item costs, then an exclusive scan into item_start
     {
         int32_t* st = sm.item_start();
         int32_t* ln = sm.item_len();
@@ -446,8 +475,8 @@ attention_kernel(const __grid_constant__ AttnParams p,
                     set_err(p.dev_err, DATTN_DEVERR_CHUNK_OOB);
                     npg = 0;
                 }
-                ln[i] = 0;
-                cnt = p.Hkv * npg * (p.P >> 4);
+                ln[i] = npg * (p.P >> 4);  // real tiles per head
+                cnt = p.Hkv * Plan::cost_of(ln[i]);
             } else {
                 int32_t L = p.seq_lens[i];
                 const int32_t cap = p.max_pages * p.P;
@@ -458,11 +487,11 @@ attention_kernel(const __grid_constant__ AttnParams p,
                 ln[i] = L;
                 if (p.mode == MODE_SPARSE) {
                     const int32_t* kb = sm.kind_before() + 3 * p.Hkv;
-                    cnt = kb[0] * head_tiles(DATTN_HEAD_DENSE, L, p) +
-                          kb[1] * head_tiles(DATTN_HEAD_RETRIEVAL, L, p) +
-                          kb[2] * head_tiles(DATTN_HEAD_STREAMING, L, p);
+                    cnt = kb[0] * Plan::cost_of(head_tiles(DATTN_HEAD_DENSE, L, p)) +
+                          kb[1] * Plan::cost_of(head_tiles(DATTN_HEAD_RETRIEVAL, L, p)) +
+                          kb[2] * Plan::cost_of(head_tiles(DATTN_HEAD_STREAMING, L, p));
                 } else {
-                    cnt = p.Hkv * ceil16(L);
+                    cnt = p.Hkv * Plan::cost_of(ceil16(L));
                 }
             }
             local_sum += cnt;
@@ -493,80 +522,72 @@ attention_kernel(const __grid_constant__ AttnParams p,
     }
     const Plan plan(p, sm);
     const int32_t W = sm.item_start()[p.nitems];
-    // Only the first min(G, W) CTAs take tiles, so that every participating CTA owns at
-    // least one tile: the pieces of a segment then come from consecutive CTAs
-    // c_first..c_last, and each of them arrives on the segment's counter exactly once.
+    // Only the first min(G, W) CTAs take work, so that every participating CTA owns at
+    // least one cost unit. A CTA strictly between the first and the last owner of a
+    // segment's real tiles lies inside them, so the pieces of a segment come from
+    // consecutive CTAs c_first..c_last, each of which arrives on its counter once.
     const int32_t Gw = W < G ? (W > 0 ? W : 1) : G;
-    const int32_t t_begin = cta < Gw ? (int32_t)split_begin(W, Gw, cta) : 0;
-    const int32_t t_end = cta < Gw ? (int32_t)split_begin(W, Gw, cta + 1) : 0;
+    const int32_t X0 = cta < Gw ? (int32_t)split_begin(W, Gw, cta) : 0;
+    const int32_t X1 = cta < Gw ? (int32_t)split_begin(W, Gw, cta + 1) : 0;
 
     // segments without tiles have no owner: CTA (s mod G) writes their empty result
     for (int32_t s = cta; s < p.nseg; s += G) {
-        int32_t st, len;
-        plan.seg_span(s, st, len);
-        if (len == 0) {
+        int32_t st, real, cost;
+        plan.seg_span(s, st, real, cost);
+        if (real == 0) {
             for (int idx = tid; idx < p.g * D; idx += kAttnThreads)
                 write_final(p, s, idx / D, idx % D, D, kNegInf, 0.f, 0.f);
         }
     }
-    if (t_begin >= t_end) return;
+    if (X0 >= X1) return;
+    const int32_t s_first = plan.segment_at(X0);
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer warp
         const uint64_t pol = policy_evict_first();
         const uint32_t tile_bytes = (uint32_t)(D / 64) * 2048u;
-        const int32_t ntiles = t_end - t_begin;
-        int32_t issued = 0;
+        int32_t k = 0;  // real tiles issued so far: tile k uses stage k % kStages
         bool stop = false;
-        for (int32_t base = 0; base < ntiles && !stop; base += 32) {
-            TileRef ref{0, 1 << 16};
-            if (base + lane < ntiles) {
-                int32_t s, local;
-                plan.locate(t_begin + base + lane, s, local);
-                ref = resolve_tile(p, sm, s, local);
-            }
-            const int32_t nb = min(32, ntiles - base);
-            for (int32_t j = 0; j < nb; ++j) {
-                const int32_t y = __shfl_sync(0xffffffffu, ref.y, j);
-                const int32_t lohi = __shfl_sync(0xffffffffu, ref.lohi, j);
-                if (lane == 0) {
-                    const int32_t k = base + j;
+        int32_t s = s_first, cs, real, r0, r1;
+        while (!stop && plan.next_piece(s, X0, X1, cs, real, r0, r1)) {
+            for (int32_t base = r0; base < r1 && !stop; base += 32) {
+                TileRef ref{0, 1 << 16};
+                if (base + lane < r1) ref = resolve_tile(p, sm, s, base + lane);
+                const int32_t nb = min(32, r1 - base);
+                for (int32_t j = 0; j < nb; ++j, ++k) {
+                    const int32_t y = __shfl_sync(0xffffffffu, ref.y, j);
+                    const int32_t lohi = __shfl_sync(0xffffffffu, ref.lohi, j);
                     const int stg = k % kStages;
                     bool ok = true;
-                    if (k >= kStages)
+                    if (lane == 0 && k >= kStages)
                         ok = mbar_wait(sm.empty_bar(stg), ((k / kStages) - 1) & 1,
                                        sm.abort_flag(), p.dev_err);
-                    if (!ok) {
+                    if (__shfl_sync(0xffffffffu, ok ? 0 : 1, 0)) {
                         stop = true;
-                    } else {
-                        sm.meta()[stg] = lohi;
-                        const uint32_t full = sm.full_bar(stg);
-                        if (lohi >> 16) {
-                            mbar_arrive(full);
-                        } else {
-                            const uint32_t dst = smem_u32(sm.base + sm.L.stages) +
-                                                 (uint32_t)stg * sm.L.stage_bytes;
-                            mbar_arrive_expect_tx(full, 2u * tile_bytes);
-#pragma unroll
-                            for (int hf = 0; hf < D / 64; ++hf)
-                                tma_load_2d(dst + hf * 2048u, &tmap_k, hf * 64, y, full, pol);
-#pragma unroll
-                            for (int hf = 0; hf < D / 64; ++hf)
-                                tma_load_2d(dst + tile_bytes + hf * 2048u, &tmap_v, hf * 64, y,
-                                            full, pol);
-                        }
-                        issued = k + 1;
+                        break;
                     }
+                    const uint32_t full = sm.full_bar(stg);
+                    const uint32_t dst =
+                        smem_u32(sm.base + sm.L.stages) + (uint32_t)stg * sm.L.stage_bytes;
+                    if (lane == 0) {
+                        sm.meta()[stg] = lohi;
+                        if (lohi >> 16) mbar_arrive(full);
+                        else mbar_arrive_expect_tx(full, 2u * tile_bytes);
+                    }
+                    __syncwarp();
+                    // one instruction, two lanes: lane 0 brings the K tile, lane 1 the V tile
+                    if (!(lohi >> 16) && lane < 2)
+                        tma_load_3d(dst + (lane ? tile_bytes : 0u), lane ? &tmap_v : &tmap_k, 0,
+                                    y, 0, full, pol);
                 }
-                stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
-                if (stop) break;
             }
+            ++s;
         }
         // after an abort, wait (bounded) for copies still in flight before the CTA exits
         if (lane == 0 && *sm.abort_flag()) {
-            for (int32_t k = max(0, issued - kStages); k < issued; ++k) {
+            for (int32_t kk = max(0, k - kStages); kk < k; ++kk) {
                 const unsigned long long t0 = global_timer_ns();
-                while (!mbar_try_wait(sm.full_bar(k % kStages), (k / kStages) & 1) &&
+                while (!mbar_try_wait(sm.full_bar(kk % kStages), (kk / kStages) & 1) &&
                        global_timer_ns() - t0 < kWaitLimitNs) {
                 }
             }
@@ -577,22 +598,26 @@ attention_kernel(const __grid_constant__ AttnParams p,
     // ---------------------------------------------------------------- consumer warps
     Consumer<D> cons(p, sm, warp, lane);
     const uint32_t stage0 = smem_u32(sm.base + sm.L.stages);
-    int32_t s = 0, dummy = 0;
-    plan.locate(t_begin, s, dummy);
-    int32_t a = t_begin;
-    while (a < t_end) {
-        int32_t sst, slen;
-        plan.seg_span(s, sst, slen);
-        while (sst + slen <= a) {
-            ++s;
-            plan.seg_span(s, sst, slen);
+    int32_t kbase = 0;  // real tiles of earlier pieces
+    int32_t s = s_first, sst, sreal, r0, r1;
+    bool have = plan.next_piece(s, X0, X1, sst, sreal, r0, r1);
+    uint32_t qn[Consumer<D>::KS][2];
+    if (have) cons.load_q(s, qn);
+    while (have) {
+#pragma unroll
+        for (int ks = 0; ks < Consumer<D>::KS; ++ks) {
+            cons.qf[ks][0] = qn[ks][0];
+            cons.qf[ks][1] = qn[ks][1];
         }
-        const int32_t pe = min(sst + slen, t_end);
-        cons.load_q(s);
+        // the next piece's query is fetched while this piece streams
+        int32_t s2 = s + 1, c2, real2, a2, b2;
+        const bool have2 = plan.next_piece(s2, X0, X1, c2, real2, a2, b2);
+        if (have2) cons.load_q(s2, qn);
         cons.reset();
-        const int32_t ka = a - t_begin, kb = pe - t_begin;
-        for (int32_t k = ka + ((warp - ka % kConsumerWarps + kConsumerWarps) % kConsumerWarps);
-             k < kb; k += kConsumerWarps) {
+        const int32_t nr = r1 - r0;
+        for (int32_t i = (warp - kbase % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
+             i < nr; i += kConsumerWarps) {
+            const int32_t k = kbase + i;
             const int stg = k % kStages;
             // warp-uniform: the tile's ldmatrix / mma / movmatrix are warp-collective
             const bool ok = __all_sync(0xffffffffu, mbar_wait(sm.full_bar(stg), (k / kStages) & 1,
@@ -606,10 +631,13 @@ attention_kernel(const __grid_constant__ AttnParams p,
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty_bar(stg));
         }
+        kbase += nr;
         // ---- merge the four warps' states of this piece -------------------------------
         cons.publish();
         named_bar_sync(1, kConsumerWarps * 32);
-        const bool whole = (a == sst) && (pe == sst + slen);
+        const int32_t c_first = split_owner(sst, W, Gw);
+        const int32_t c_last = split_owner(sst + sreal - 1, W, Gw);
+        const bool whole = c_first == c_last;
         const int ctid = tid;  // 0..127
         float* wm = sm.ws_m();
         float* we = sm.ws_e();
@@ -646,8 +674,6 @@ attention_kernel(const __grid_constant__ AttnParams p,
         if (!whole) {
             // hand the piece over: the CTA that delivers the last piece merges them all
             named_bar_sync(1, kConsumerWarps * 32);
-            const int32_t c_first = split_owner(sst, W, Gw);
-            const int32_t c_last = split_owner(sst + slen - 1, W, Gw);
             const int32_t npieces = c_last - c_first + 1;
             if (ctid == 0) {
                 __threadfence();
@@ -657,30 +683,83 @@ attention_kernel(const __grid_constant__ AttnParams p,
             }
             named_bar_sync(1, kConsumerWarps * 32);
             if (*sm.last_flag()) {
+                // Merge all pieces of the segment. Per pass over up to kMergeChunk pieces:
+                // load their (m, e) at once, let one thread per head fold them into the
+                // running max and sum and turn each m into a weight, then accumulate the
+                // weighted MA with independent loads.
                 __threadfence();
                 const float* first = p.slots + (int64_t)(c_first + s) * slot_stride;
-                for (int idx = ctid; idx < gD; idx += kConsumerWarps * 32) {
-                    const int j = idx / D, d = idx - j * D;
-                    float mc = kNegInf;
-                    for (int32_t q = 0; q < npieces; ++q)
-                        mc = fmaxf(mc, __ldcg(first + (int64_t)q * slot_stride + gD + j));
-                    float ec = 0.f, ma = 0.f;
-                    if (mc != kNegInf) {
-                        for (int32_t q = 0; q < npieces; ++q) {
-                            const float* sl = first + (int64_t)q * slot_stride;
-                            const float mq = __ldcg(sl + gD + j);
-                            if (mq == kNegInf) continue;
-                            const float sc = exp2f(mq - mc);
-                            ec += __ldcg(sl + gD + p.g + j) * sc;
-                            ma += __ldcg(sl + j * D + d) * sc;
-                        }
+                float* mw = sm.merge_w();
+                float* me = sm.merge_e();
+                float* mrun = sm.ws_m();              // [g] running max
+                float* erun = sm.ws_e();              // [g] running sum
+                float* alpha = sm.ws_m() + kMaxGroup; // [g] rescale of earlier passes
+                constexpr int kOwn = (kMaxGroup * D + kConsumerWarps * 32 - 1) /
+                                     (kConsumerWarps * 32);
+                float acc[kOwn];
+#pragma unroll
+                for (int k = 0; k < kOwn; ++k) acc[k] = 0.f;
+                if (ctid < p.g) {
+                    mrun[ctid] = kNegInf;
+                    erun[ctid] = 0.f;
+                }
+                named_bar_sync(1, kConsumerWarps * 32);
+                for (int32_t q0 = 0; q0 < npieces; q0 += kMergeChunk) {
+                    const int nq = min(kMergeChunk, npieces - q0);
+                    for (int i = ctid; i < nq * p.g; i += kConsumerWarps * 32) {
+                        const int q = i / p.g, j = i - q * p.g;
+                        const float* sl = first + (int64_t)(q0 + q) * slot_stride;
+                        mw[i] = __ldcg(sl + gD + j);
+                        me[i] = __ldcg(sl + gD + p.g + j);
                     }
-                    write_final(p, s, j, d, D, mc, ec, ma);
+                    named_bar_sync(1, kConsumerWarps * 32);
+                    if (ctid < p.g) {
+                        const int j = ctid;
+                        float mx = mrun[j];
+                        for (int q = 0; q < nq; ++q) mx = fmaxf(mx, mw[q * p.g + j]);
+                        const float al = mx == kNegInf ? 0.f : exp2f(mrun[j] - mx);
+                        float e = erun[j] * al;
+                        for (int q = 0; q < nq; ++q) {
+                            const float mq = mw[q * p.g + j];
+                            const float w = mq == kNegInf ? 0.f : exp2f(mq - mx);
+                            e += me[q * p.g + j] * w;
+                            mw[q * p.g + j] = w;
+                        }
+                        mrun[j] = mx;
+                        erun[j] = e;
+                        alpha[j] = al;
+                    }
+                    named_bar_sync(1, kConsumerWarps * 32);
+#pragma unroll
+                    for (int k = 0; k < kOwn; ++k) {
+                        const int idx = ctid + k * kConsumerWarps * 32;
+                        if (idx >= gD) break;
+                        const int j = idx / D, d = idx - j * D;
+                        const float* col = first + (int64_t)q0 * slot_stride + j * D + d;
+                        float a = acc[k] * alpha[j];
+#pragma unroll 4
+                        for (int q = 0; q < nq; ++q)
+                            a += mw[q * p.g + j] * __ldcg(col + (int64_t)q * slot_stride);
+                        acc[k] = a;
+                    }
+                    named_bar_sync(1, kConsumerWarps * 32);
+                }
+#pragma unroll
+                for (int k = 0; k < kOwn; ++k) {
+                    const int idx = ctid + k * kConsumerWarps * 32;
+                    if (idx >= gD) break;
+                    const int j = idx / D, d = idx - j * D;
+                    write_final(p, s, j, d, D, mrun[j], erun[j], acc[k]);
                 }
             }
         }
         named_bar_sync(1, kConsumerWarps * 32);  // shared state is reused by the next piece
-        a = pe;
+        s = s2;
+        sst = c2;
+        sreal = real2;
+        r0 = a2;
+        r1 = b2;
+        have = have2;
     }
 }
 
@@ -746,8 +825,10 @@ static dattn_status_t launch_d(const AttnParams& p0, const void* k_pool, const v
     const int64_t rows = (int64_t)p.num_pages * p.Hkv * p.P;
     if ((st = make_kv_tensor_map(&tk, k_pool, rows, D)) != DATTN_OK) return st;
     if ((st = make_kv_tensor_map(&tv, v_pool, rows, D)) != DATTN_OK) return st;
-    attention_kernel<D><<<G, kAttnThreads, L.total, stream>>>(p, tk, tv);
-    return cudaGetLastError() == cudaSuccess ? DATTN_OK : DATTN_ERR_CUDA;
+    if (launch_pdl(attention_kernel<D>, dim3(G), dim3(kAttnThreads), L.total, stream, p, tk, tv) !=
+        cudaSuccess)
+        return DATTN_ERR_CUDA;
+    return DATTN_OK;
 }
 
 dattn_status_t launch_attention(const AttnParams& p, const void* k_pool, const void* v_pool,

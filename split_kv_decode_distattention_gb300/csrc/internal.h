@@ -17,6 +17,8 @@ constexpr int kMaxKvHeads = 256;
 constexpr int kMaxGroup = 8;        // query heads per KV head
 constexpr int kMaxTopK = 256;
 constexpr int kMaxCtasPerSm = 4;    // bound used for workspace sizing with automatic splits
+constexpr int kMergeChunk = 128;    // pieces merged per pass by the last-arriving CTA
+constexpr int32_t kSegCost = 6;     // cost units per segment in the balanced split
 
 enum AttnMode : int { MODE_PARTIAL = 0, MODE_DENSE = 1, MODE_SPARSE = 2 };
 
@@ -53,8 +55,8 @@ struct AttnParams {
 
 // Shared-memory layout of the attention engine, identical on host and device.
 struct AttnSmem {
-    uint32_t stage_bytes, stages, bars, meta, flags, ws_m, ws_e, ws_o, kind_before, kinds,
-        item_start, item_len, scan, total;
+    uint32_t stage_bytes, stages, bars, meta, flags, ws_m, ws_e, ws_o, merge_w, merge_e,
+        kind_before, kinds, item_start, item_len, scan, total;
 };
 
 __host__ __device__ inline AttnSmem attn_smem_layout(int D, int g, int nitems, int Hkv,
@@ -69,6 +71,8 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int D, int g, int nitems, i
     s.ws_m = o;        o += kConsumerWarps * kMaxGroup * 4u;
     s.ws_e = o;        o += kConsumerWarps * kMaxGroup * 4u;
     s.ws_o = o;        o += (uint32_t)(kConsumerWarps * g * D) * 4u;
+    s.merge_w = o;     o += (uint32_t)(kMergeChunk * g) * 4u;
+    s.merge_e = o;     o += (uint32_t)(kMergeChunk * g) * 4u;
     s.kind_before = o; o += sparse ? (uint32_t)(Hkv + 1) * 3u * 4u : 0u;
     s.kinds = o;       o += sparse ? (uint32_t)Hkv * 4u : 0u;
     o = (o + 15u) & ~15u;
@@ -88,6 +92,26 @@ dattn_status_t launch_attention(const AttnParams& p, const void* k_pool, const v
                                 int D, int32_t num_splits, void* ws, size_t ws_bytes,
                                 cudaStream_t stream, int64_t tiles_bound);
 int32_t attention_occupancy(int D, int g, int nitems, int Hkv, bool sparse);
+
+// Launches kernel<<<grid, block, smem, stream>>>(args...) with programmatic stream
+// serialization, so that its launch and prologue overlap the previous kernel on the stream.
+// Every kernel launched this way calls grid_dependency_wait() before reading data that an
+// earlier kernel may write.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 
 // Number of CTAs for a launch with an upper bound of total_tiles tiles.
 int32_t choose_splits(int64_t total_tiles, int32_t requested, int occupancy);

@@ -31,6 +31,8 @@ kv_append_kernel(dattn_kv_layout L, uint16_t* __restrict__ k_pool, uint16_t* __r
                  int32_t update_in_place, int32_t* dev_err) {
     const int32_t b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
     const int32_t Hkv = L.num_kv_heads, P = L.page_size;
+    grid_dependency_wait();  // the previous kernel may still read the pool or the lengths
+    grid_launch_dependents();
     const int32_t pos0 = seq_lens[b];
     if (pos0 < 0) {
         if (tid == 0) set_err(dev_err, DATTN_DEVERR_LEN_OOB);
@@ -122,6 +124,8 @@ kv_append_kernel(dattn_kv_layout L, uint16_t* __restrict__ k_pool, uint16_t* __r
 }
 
 __global__ void advance_lengths_kernel(int32_t* seq_lens, int32_t B, int32_t T) {
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int32_t b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b < B && seq_lens[b] >= 0) seq_lens[b] += T;
 }
@@ -137,16 +141,19 @@ dattn_status_t launch_kv_append(const dattn_kv_layout& L, uint16_t* k_pool, uint
     const bool single = T + 15 <= kAppendWindow;
     const int32_t nwin = single ? 1 : (T + 15 + kAppendWindow - 1) / kAppendWindow;
     const dim3 grid(nwin, B);
+    const int32_t inplace = single ? 1 : 0;
+    cudaError_t e;
     if (L.head_dim == 64)
-        kv_append_kernel<64><<<grid, kAppendThreads, 0, stream>>>(
-            L, k_pool, v_pool, stats, k_new, v_new, T, seq_lens, single ? 1 : 0, dev_err);
+        e = launch_pdl(kv_append_kernel<64>, grid, dim3(kAppendThreads), 0, stream, L, k_pool,
+                       v_pool, stats, k_new, v_new, T, seq_lens, inplace, dev_err);
     else
-        kv_append_kernel<128><<<grid, kAppendThreads, 0, stream>>>(
-            L, k_pool, v_pool, stats, k_new, v_new, T, seq_lens, single ? 1 : 0, dev_err);
-    if (cudaGetLastError() != cudaSuccess) return DATTN_ERR_CUDA;
+        e = launch_pdl(kv_append_kernel<128>, grid, dim3(kAppendThreads), 0, stream, L, k_pool,
+                       v_pool, stats, k_new, v_new, T, seq_lens, inplace, dev_err);
+    if (e != cudaSuccess) return DATTN_ERR_CUDA;
     if (!single) {
-        advance_lengths_kernel<<<(B + 255) / 256, 256, 0, stream>>>(seq_lens, B, T);
-        if (cudaGetLastError() != cudaSuccess) return DATTN_ERR_CUDA;
+        if (launch_pdl(advance_lengths_kernel, dim3((B + 255) / 256), dim3(256), 0, stream,
+                       seq_lens, B, T) != cudaSuccess)
+            return DATTN_ERR_CUDA;
     }
     return DATTN_OK;
 }

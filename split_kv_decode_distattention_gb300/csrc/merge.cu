@@ -21,6 +21,8 @@ merge_kernel(int32_t B, int32_t C, int32_t Hq, int32_t D, const int32_t* __restr
              const float* __restrict__ MA, float* __restrict__ out, float* __restrict__ m_g,
              float* __restrict__ e_g, float* __restrict__ MA_g, int32_t* dev_err) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    grid_dependency_wait();  // the partials may come from the previous kernel on the stream
+    grid_launch_dependents();
     const int32_t b = blockIdx.x;
     const int32_t h = blockIdx.y * kMergeWarps + warp;
     if (h >= Hq) return;
@@ -72,9 +74,10 @@ dattn_status_t launch_merge(int32_t B, int32_t C, int32_t Hq, int32_t D, const i
                             cudaStream_t stream) {
     if (B == 0 || Hq == 0) return DATTN_OK;
     const dim3 grid(B, (Hq + kMergeWarps - 1) / kMergeWarps);
-    merge_kernel<<<grid, kMergeWarps * 32, 0, stream>>>(B, C, Hq, D, indptr, m, e, MA, out, m_g,
-                                                        e_g, MA_g, dev_err);
-    return cudaGetLastError() == cudaSuccess ? DATTN_OK : DATTN_ERR_CUDA;
+    return launch_pdl(merge_kernel, grid, dim3(kMergeWarps * 32), 0, stream, B, C, Hq, D, indptr,
+                      m, e, MA, out, m_g, e_g, MA_g, dev_err) == cudaSuccess
+               ? DATTN_OK
+               : DATTN_ERR_CUDA;
 }
 
 }  // namespace dattn

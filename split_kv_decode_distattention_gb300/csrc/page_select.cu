@@ -13,15 +13,30 @@
 // product is q_d * kmax_d, otherwise q_d * kmin_d. This fixed arithmetic decides the
 // selection.
 //
-// GB300 design. The statistics scan is HBM-bound: every 16 decode steps it reads all k_max
-// and k_min of the retrieval heads. The physical pages of all retrieval (request, KV head)
-// pairs are laid end to end and cut into equal contiguous ranges, one per CTA. A producer
-// warp bulk-copies each page's statistics tile (contiguous in HBM) into a stage padded by 16
-// bytes per page, so the eight lanes of a shared-memory phase, which read eight different
-// pages, hit eight different banks. Four consumer warps score a stage together, keep the
-// pages that beat the running K-th key in a candidate buffer, and fold candidates into the
-// top K with a 512-entry bitonic sort in shared memory. A head split across CTAs leaves
-// each CTA's top K in the workspace, and the CTA that arrives last merges them.
+// GB300 design. The statistics scan is HBM-bound: every reuse window it reads all k_max and
+// k_min of the retrieval heads (512 B per logical page at d = 128), and it must score them
+// at that speed. The physical pages of all retrieval (request, KV head) pairs are laid end
+// to end and cut into equal contiguous ranges, one per CTA (one CTA per SM).
+//  - No staging: eight warps read the statistics straight into registers with coalesced
+//    16-byte loads, software-pipelined three groups deep. A logical page's 2*d values are
+//    spread over d/16 lanes (16 channels each), so each lane keeps the query values of its
+//    channels for four heads in registers for the whole piece.
+//  - A lane runs its 16 channels as two chains (even and odd channels) of packed fp32x2
+//    fused multiply-adds, four heads at once. The lanes of a logical page then combine
+//    their partial sums with a fixed butterfly.
+//  - Page maxima that beat the warp's running K-th key go to a per-warp candidate buffer.
+//    The buffer is folded into the warp's top K by a warp-synchronous bitonic sort.
+//  - At the end of a piece the eight warps' lists are merged. A head split across CTAs
+//    leaves each CTA's top K in the workspace, and the CTA that arrives last merges them.
+//
+// Decision arithmetic (the selection is an integer decided by floating point, so it is
+// fixed exactly, and the oracle repeats it). For head j, channels are taken in chunks of C
+// (C = 16 for groups of up to 4 query heads, C = 8 otherwise). Within a chunk there are two
+// fp32 accumulators, for even and odd channels, both starting at +0. Each channel adds, by
+// fused multiply-add, first max(q,0)*kmax then min(q,0)*kmin; one of the two is an exact
+// zero, so this adds exactly the product q*kmax or q*kmin that the score definition selects.
+// A chunk's partial is even + odd. The partials are summed by a pairwise tree: adjacent
+// chunks first, then pairs of pairs.
 #include "common.cuh"
 #include "internal.h"
 
@@ -29,9 +44,9 @@ namespace dattn {
 
 namespace {
 
-constexpr int kSelStages = 4;
-constexpr int kSortN = 512;
-constexpr int kSelThreads = kAttnThreads;  // 4 consumer warps + 1 producer warp
+constexpr int kSelWarps = 8;
+constexpr int kSelThreads = kSelWarps * 32;
+constexpr int kSelBlockPages = 1024;  // pages whose block-table entries are staged at once
 
 struct SelParams {
     int32_t num_pages, Hkv, P, max_pages;
@@ -46,29 +61,30 @@ struct SelParams {
     int32_t* counters;
     uint64_t* slots;
     int32_t nseg;
-    int32_t npg;          // physical pages per stage (power of two, <= 32)
-    uint32_t page_bytes;  // statistics bytes of one (page, head): (P/16) * 2 * D * 2
     int32_t* dev_err;
 };
 
+__host__ __device__ inline int next_pow2(int x) {
+    int n = 1;
+    while (n < x) n <<= 1;
+    return n;
+}
+
 struct SelSmem {
-    uint32_t stage_bytes, stages, bars, meta, flags, qs, scr, sortbuf, ret_before, ret_heads,
-        item_start, item_len, scan, total;
+    uint32_t flags, bt, wbuf, sortbuf, ret_before, ret_heads, item_start, item_len, scan, total;
+    int wn, sn;
 };
 
-__host__ __device__ inline SelSmem sel_smem_layout(int D, int g, int P, int npg, int B, int Hkv) {
+__host__ __device__ inline SelSmem sel_smem_layout(int B, int Hkv, int K) {
     SelSmem s;
-    const uint32_t page_bytes = (uint32_t)(P / 16) * 2u * D * 2u;
-    s.stage_bytes = (uint32_t)npg * (page_bytes + 16u);
+    s.wn = next_pow2(2 * K);                 // per-warp buffer: top K + candidates
+    s.sn = next_pow2(kSelWarps * K);         // CTA buffer: the warps' lists, or pieces to fold
     uint32_t o = 0;
-    s.stages = o;     o += kSelStages * s.stage_bytes;
-    s.bars = o;       o += 2u * kSelStages * 8u;
-    s.meta = o;       o += kSelStages * 4u;
     s.flags = o;      o += 16u;
-    s.qs = o;         o += (uint32_t)(g * D) * 4u;
-    s.scr = o;        o += (uint32_t)(npg * (P / 16) * g) * 4u;
+    s.bt = o;         o += kSelBlockPages * 4u;
     o = (o + 15u) & ~15u;
-    s.sortbuf = o;    o += kSortN * 8u;
+    s.wbuf = o;       o += (uint32_t)kSelWarps * s.wn * 8u;
+    s.sortbuf = o;    o += (uint32_t)s.sn * 8u;
     s.ret_before = o; o += (uint32_t)(Hkv + 1) * 4u;
     s.ret_heads = o;  o += (uint32_t)Hkv * 4u;
     o = (o + 15u) & ~15u;
@@ -86,12 +102,38 @@ __device__ __forceinline__ uint64_t make_key(float score, int32_t page) {
     return ((uint64_t)ord << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)page);
 }
 
-// Bitonic sort of buf[0..n) into descending order by the 128 consumer threads (n a power of
-// two). Ends with a barrier.
-__device__ void bitonic_desc(uint64_t* buf, int n, int ctid) {
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// acc = a * b + acc, two independent IEEE fp32 fused multiply-adds
+__device__ __forceinline__ void fma_f32x2(uint64_t& acc, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+// 16-byte streaming load (read once: no L1 allocation, evict-first in L2)
+__device__ __forceinline__ uint4 ldg_stream(const void* ptr, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr), "l"(pol));
+    return v;
+}
+
+// Bitonic sort of buf[0..n) into descending order by nthreads threads (index tid); sync()
+// separates the steps.
+template <typename Sync>
+__device__ __forceinline__ void bitonic_desc(uint64_t* buf, int n, int tid, int nthreads,
+                                             Sync sync) {
     for (int k = 2; k <= n; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int idx = ctid; idx < (n >> 1); idx += kConsumerWarps * 32) {
+            for (int idx = tid; idx < (n >> 1); idx += nthreads) {
                 const int i = 2 * j * (idx / j) + (idx % j);
                 const int l = i + j;
                 const uint64_t x = buf[i], y = buf[l];
@@ -101,29 +143,29 @@ __device__ void bitonic_desc(uint64_t* buf, int n, int ctid) {
                     buf[l] = x;
                 }
             }
-            named_bar_sync(1, kConsumerWarps * 32);
+            sync();
         }
     }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kSelThreads) page_select_kernel(const __grid_constant__ SelParams p) {
+// D: head_dim; CPL: channels per lane (16 or 8); HG: query heads per lane (4 or 8).
+template <int D, int CPL, int HG>
+__global__ void __launch_bounds__(kSelThreads, 1)
+page_select_kernel(const __grid_constant__ SelParams p) {
+    constexpr int LPR = D / CPL;     // lanes per logical page (row)
+    constexpr int RPW = 32 / LPR;    // rows per warp group
+    constexpr int NLD = CPL / 8;     // 16-byte loads per lane for k_max (and for k_min)
+    constexpr int NPAIR = CPL / 2;   // channel pairs per lane
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_off = smem_u32(smem_raw);
     uint8_t* base = smem_raw + (((raw_off + 127u) & ~127u) - raw_off);
-    const SelSmem L = sel_smem_layout(D, p.g, p.P, p.npg, p.B, p.Hkv);
+    const int K = p.top_k;
+    const SelSmem L = sel_smem_layout(p.B, p.Hkv, K);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t G = gridDim.x, cta = blockIdx.x;
     const int LPG = p.P >> 4;
-    const uint32_t bars = smem_u32(base + L.bars);
-    auto full_bar = [&](int s) { return bars + 8u * s; };
-    auto empty_bar = [&](int s) { return bars + 8u * (kSelStages + s); };
-    uint32_t* meta = reinterpret_cast<uint32_t*>(base + L.meta);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.flags);
-    int* cand_count = reinterpret_cast<int*>(base + L.flags + 4);
-    int* last_flag = reinterpret_cast<int*>(base + L.flags + 8);
-    float* qs = reinterpret_cast<float*>(base + L.qs);
-    float* scr = reinterpret_cast<float*>(base + L.scr);
+    int* last_flag = reinterpret_cast<int*>(base + L.flags);
+    int32_t* bt_blk = reinterpret_cast<int32_t*>(base + L.bt);
     uint64_t* sortbuf = reinterpret_cast<uint64_t*>(base + L.sortbuf);
     int32_t* ret_before = reinterpret_cast<int32_t*>(base + L.ret_before);
     int32_t* ret_heads = reinterpret_cast<int32_t*>(base + L.ret_heads);
@@ -131,18 +173,18 @@ __global__ void __launch_bounds__(kSelThreads) page_select_kernel(const __grid_c
     int32_t* item_len = reinterpret_cast<int32_t*>(base + L.item_len);
     int32_t* scan = reinterpret_cast<int32_t*>(base + L.scan);
 
+    grid_dependency_wait();  // lengths and statistics may come from the previous kernel
+    grid_launch_dependents();
     // ---------------------------------------------------------------- setup
+    for (int h = tid; h < p.Hkv; h += kSelThreads)
+        ret_heads[h] = p.head_kind[h] == DATTN_HEAD_RETRIEVAL ? 1 : 0;
+    __syncthreads();
     if (tid == 0) {
-        for (int s = 0; s < kSelStages; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
-        }
-        *abort_flag = 0;
-        fence_mbar_init();
         int32_t r = 0;
         for (int h = 0; h < p.Hkv; ++h) {
+            const int isr = ret_heads[h];
             ret_before[h] = r;
-            if (p.head_kind[h] == DATTN_HEAD_RETRIEVAL) ret_heads[r++] = h;
+            if (isr) ret_heads[r++] = h;  // compacts in place: r <= h
         }
         ret_before[p.Hkv] = r;
     }
@@ -182,7 +224,7 @@ __global__ void __launch_bounds__(kSelThreads) page_select_kernel(const __grid_c
         }
         if (tid == 0) {
             int32_t tot = 0;
-            for (int w = 0; w < kSelThreads / 32; ++w) tot += scan[w];
+            for (int w = 0; w < kSelWarps; ++w) tot += scan[w];
             item_start[n] = tot;
         }
         __syncthreads();
@@ -216,96 +258,43 @@ __global__ void __launch_bounds__(kSelThreads) page_select_kernel(const __grid_c
         int32_t st, len;
         seg_span(s, st, len);
         if (len == 0)
-            for (int r = tid; r < p.top_k; r += kSelThreads) p.selected[(int64_t)s * p.top_k + r] = -1;
+            for (int r = tid; r < K; r += kSelThreads) p.selected[(int64_t)s * K + r] = -1;
     }
     if (t_begin >= t_end) return;
 
-    const uint32_t stage0 = smem_u32(base + L.stages);
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------------ producer warp
-        const uint64_t pol = policy_evict_first();
-        int32_t u = 0;  // stage uses so far
-        int32_t a = t_begin;
-        int32_t s = locate(t_begin);
-        bool stop = false;
-        while (a < t_end && !stop) {
-            int32_t sst, slen;
-            seg_span(s, sst, slen);
-            while (sst + slen <= a) { ++s; seg_span(s, sst, slen); }
-            const int32_t pe = min(sst + slen, t_end);
-            const int32_t b = s / p.Hkv, h = s - b * p.Hkv;
-            for (int32_t x = a; x < pe && !stop; x += p.npg, ++u) {
-                const int stg = u % kSelStages;
-                bool ok = true;
-                if (lane == 0 && u >= kSelStages)
-                    ok = mbar_wait(empty_bar(stg), ((u / kSelStages) - 1) & 1, abort_flag, p.dev_err);
-                stop = __shfl_sync(0xffffffffu, ok ? 0 : 1, 0) != 0;
-                if (stop) break;
-                const int32_t cnt = min(p.npg, pe - x);
-                bool valid = false;
-                int32_t page = 0;
-                if (lane < cnt) {
-                    const int32_t pi = x - sst + lane;  // request-relative page index
-                    page = p.block_table[(int64_t)b * p.max_pages + pi];
-                    if (page < 0) set_err(p.dev_err, DATTN_DEVERR_UNMAPPED_PAGE);
-                    else if (page >= p.num_pages) set_err(p.dev_err, DATTN_DEVERR_PAGE_OOB);
-                    else valid = true;
-                }
-                const uint32_t mask = __ballot_sync(0xffffffffu, valid);
-                if (lane == 0) {
-                    meta[stg] = mask;
-                    if (mask) mbar_arrive_expect_tx(full_bar(stg), __popc(mask) * p.page_bytes);
-                    else mbar_arrive(full_bar(stg));
-                }
-                __syncwarp();
-                if (valid) {
-                    const uint16_t* src = p.stats + ((int64_t)page * p.Hkv + h) * (p.page_bytes / 2);
-                    bulk_load(stage0 + stg * L.stage_bytes + lane * (p.page_bytes + 16u), src,
-                              p.page_bytes, full_bar(stg), pol);
-                }
-            }
-            a = pe;
-        }
-        if (lane == 0 && *abort_flag) {  // bounded wait for copies still in flight
-            for (int32_t k = max(0, u - kSelStages); k < u; ++k) {
-                const unsigned long long t0 = global_timer_ns();
-                while (!mbar_try_wait(full_bar(k % kSelStages), (k / kSelStages) & 1) &&
-                       global_timer_ns() - t0 < kWaitLimitNs) {
-                }
-            }
-        }
-        return;
-    }
-
-    // ---------------------------------------------------------------- consumer warps
-    const int ctid = tid;
-    const int K = p.top_k;
-    const int nitem = p.npg * LPG * p.g;
-    int32_t u = 0;
-    int32_t a = t_begin;
-    int32_t s = locate(t_begin);
-    auto fold = [&]() {  // fold the candidates into the running top K
-        const int c = *cand_count;
-        for (int i = K + c + ctid; i < kSortN; i += kConsumerWarps * 32) sortbuf[i] = 0ull;
-        named_bar_sync(1, kConsumerWarps * 32);
-        bitonic_desc(sortbuf, kSortN, ctid);
-        if (ctid == 0) *cand_count = 0;
-        named_bar_sync(1, kConsumerWarps * 32);
+    const uint64_t pol = policy_evict_first();
+    const int NT = kSelThreads;
+    uint64_t* wbuf = reinterpret_cast<uint64_t*>(base + L.wbuf) + warp * L.wn;
+    const int capw = L.wn - K;
+    auto csync = [&]() { __syncthreads(); };
+    auto wsync = [&]() { __syncwarp(); };
+    auto warp_fold = [&](int cnt) {  // fold candidates wbuf[K .. K+cnt) into wbuf[0 .. K)
+        for (int i = K + cnt + lane; i < L.wn; i += 32) wbuf[i] = 0ull;
+        __syncwarp();
+        bitonic_desc(wbuf, L.wn, lane, 32, wsync);
     };
-    auto finalize = [&](int32_t seg) {  // sortbuf[0..K) holds the top K keys
-        for (int i = ctid; i < kSortN; i += kConsumerWarps * 32)
+    auto finalize = [&](int32_t seg) {  // sortbuf[0 .. K): top K keys -> ascending pages
+        for (int i = tid; i < L.sn; i += NT)
             sortbuf[i] = i < K ? (sortbuf[i] & 0xFFFFFFFFull) * (sortbuf[i] != 0ull) : 0ull;
-        named_bar_sync(1, kConsumerWarps * 32);
-        int n2 = 1;
-        while (n2 < K) n2 <<= 1;
-        bitonic_desc(sortbuf, n2, ctid);  // descending low word = ascending page index
-        for (int r = ctid; r < K; r += kConsumerWarps * 32) {
+        csync();
+        bitonic_desc(sortbuf, next_pow2(K), tid, NT, csync);  // low word desc = page asc
+        for (int r = tid; r < K; r += NT) {
             const uint64_t kk = sortbuf[r];
             p.selected[(int64_t)seg * K + r] = kk ? (int32_t)(0xFFFFFFFFu - (uint32_t)kk) : -1;
         }
-        named_bar_sync(1, kConsumerWarps * 32);
+        csync();
     };
 
+    // lane layout inside a warp group: row rr = lane / LPR, chunk c = lane % LPR
+    const int c = lane % LPR, rr = lane / LPR;
+    // rows of a unit: whole pages, at least one warp group
+    const int unit_rows = LPG > RPW ? LPG : RPW;
+    const int up = unit_rows / LPG;          // pages per unit
+    const int ngu = unit_rows / RPW;         // warp groups per unit
+    uint64_t qp2[HG][NPAIR], qn2[HG][NPAIR];  // the lane's query values: {ch 2i, ch 2i+1}
+
+    int32_t a = t_begin;
+    int32_t s = locate(t_begin);
     while (a < t_end) {
         int32_t sst, slen;
         seg_span(s, sst, slen);
@@ -313,154 +302,218 @@ __global__ void __launch_bounds__(kSelThreads) page_select_kernel(const __grid_c
         const int32_t pe = min(sst + slen, t_end);
         const int32_t b = s / p.Hkv, h = s - b * p.Hkv;
         const int32_t Lb = item_len[b];
-        // queries of the group, widened exactly to fp32
-        for (int i = ctid; i < p.g * D; i += kConsumerWarps * 32) {
-            const int j = i / D, d = i - j * D;
-            qs[i] = __uint_as_float((uint32_t)p.q[((int64_t)b * p.Hq + h * p.g + j) * D + d] << 16);
+        // the lane's query values, widened exactly, split by sign
+#pragma unroll
+        for (int j = 0; j < HG; ++j) {
+            const bool okj = j < p.g;
+            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                p.q + ((int64_t)b * p.Hq + h * p.g + (okj ? j : 0)) * D + c * CPL);
+#pragma unroll
+            for (int i = 0; i < NPAIR; ++i) {
+                const uint32_t w = okj ? __ldg(qrow + i) : 0u;
+                const float q0 = bf16_lo(w), q1 = bf16_hi(w);
+                qp2[j][i] = pack_f32x2(q0 >= 0.f ? q0 : 0.f, q1 >= 0.f ? q1 : 0.f);
+                qn2[j][i] = pack_f32x2(q0 >= 0.f ? 0.f : q0, q1 >= 0.f ? 0.f : q1);
+            }
         }
-        for (int i = ctid; i < kSortN; i += kConsumerWarps * 32) sortbuf[i] = 0ull;
-        if (ctid == 0) *cand_count = 0;
-        named_bar_sync(1, kConsumerWarps * 32);
+        for (int i = lane; i < L.wn; i += 32) wbuf[i] = 0ull;
+        __syncwarp();
+        int cnt_c = 0;
         uint64_t thresh = 0ull;
-        for (int32_t x = a; x < pe; x += p.npg, ++u) {
-            const int stg = u % kSelStages;
-            const bool ok = mbar_wait(full_bar(stg), (u / kSelStages) & 1, abort_flag, p.dev_err);
-            const uint32_t mask = ok ? meta[stg] : 0u;
-            const int32_t cnt = min(p.npg, pe - x);
-            const uint8_t* sb = base + L.stages + stg * L.stage_bytes;
-            // items (page-fastest): it = (lp * g + j) * npg + i
-            for (int it0 = ctid; it0 < nitem; it0 += 2 * kConsumerWarps * 32) {
-                float acc[2] = {0.f, 0.f};
-                const float* qrow[2];
-                const uint8_t* row[2];
-                bool val[2];
-                int idx[2];
-#pragma unroll
-                for (int w = 0; w < 2; ++w) {
-                    const int it = it0 + w * kConsumerWarps * 32;
-                    idx[w] = it;
-                    const int i = it % p.npg, r = it / p.npg;
-                    const int lp = r / p.g, j = r - lp * p.g;
-                    const int32_t pi = x - sst + i;
-                    val[w] = it < nitem && i < cnt && ((mask >> i) & 1u) &&
-                             (pi * p.P + lp * 16 < Lb);
-                    row[w] = sb + i * (p.page_bytes + 16u) + lp * (2 * D * 2);
-                    qrow[w] = qs + j * D;
+        const int32_t* btrow = p.block_table + (int64_t)b * p.max_pages;
+        // ---- blocks of pages: stage the block-table entries, then score ------------
+        for (int32_t pb = a; pb < pe; pb += kSelBlockPages) {
+            const int32_t nblk = min(kSelBlockPages, pe - pb);
+            const int32_t pr0 = pb - sst;  // request-relative index of the block's first page
+            for (int i = tid; i < nblk; i += NT) bt_blk[i] = __ldg(btrow + pr0 + i);
+            csync();
+            const int nunits = (nblk + up - 1) / up;
+            const int ng = ((nunits - warp + kSelWarps - 1) / kSelWarps) * ngu;  // my groups
+            // group k of this warp -> unit warp + 8*(k / ngu), part k % ngu
+            auto row_of = [&](int k, int& pib, int& lp, bool& valid, int32_t& phys) {
+                const int u = warp + kSelWarps * (k / ngu);
+                const int r = u * unit_rows + (k % ngu) * RPW + rr;  // row in the block
+                pib = r / LPG;
+                lp = r - pib * LPG;
+                valid = k < ng && pib < nblk && (pr0 + pib) * p.P + lp * 16 < Lb;
+                phys = valid ? bt_blk[pib] : -1;
+                if (valid && (phys < 0 || phys >= p.num_pages)) {
+                    set_err(p.dev_err, phys < 0 ? DATTN_DEVERR_UNMAPPED_PAGE
+                                                : DATTN_DEVERR_PAGE_OOB);
+                    valid = false;
                 }
-                if (val[0] || val[1]) {
-#pragma unroll 2
-                    for (int d8 = 0; d8 < D / 8; ++d8) {
+            };
+            auto issue = [&](int k, uint4 (&buf)[2 * NLD]) {
+                int pib, lp;
+                bool valid;
+                int32_t phys;
+                row_of(k, pib, lp, valid, phys);
+                if (valid) {
+                    const uint16_t* row = p.stats +
+                        (((int64_t)phys * p.Hkv + h) * LPG + lp) * (2 * D) + c * CPL;
 #pragma unroll
-                        for (int w = 0; w < 2; ++w) {
-                            if (!val[w]) continue;
-                            const uint4 mx = *reinterpret_cast<const uint4*>(row[w] + d8 * 16);
-                            const uint4 mn = *reinterpret_cast<const uint4*>(row[w] + D * 2 + d8 * 16);
-                            const uint32_t xs[4] = {mx.x, mx.y, mx.z, mx.w};
-                            const uint32_t ns[4] = {mn.x, mn.y, mn.z, mn.w};
+                    for (int i = 0; i < NLD; ++i) {
+                        buf[i] = ldg_stream(row + i * 8, pol);
+                        buf[NLD + i] = ldg_stream(row + D + i * 8, pol);
+                    }
+                }
+            };
+            float run = -__int_as_float(0x7f800000);  // running page max across a unit's groups
+            auto process = [&](int k, const uint4 (&buf)[2 * NLD]) {
+                if (k >= ng) return;  // warp-uniform
+                int pib, lp;
+                bool valid;
+                int32_t phys;
+                row_of(k, pib, lp, valid, phys);
+                float best = -__int_as_float(0x7f800000);
+                {
+                    uint64_t acc[HG];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float q0 = qrow[w][d8 * 8 + 2 * e];
-                                const float q1 = qrow[w][d8 * 8 + 2 * e + 1];
-                                acc[w] = fmaf(q0, q0 >= 0.f ? bf16_lo(xs[e]) : bf16_lo(ns[e]), acc[w]);
-                                acc[w] = fmaf(q1, q1 >= 0.f ? bf16_hi(xs[e]) : bf16_hi(ns[e]), acc[w]);
-                            }
+                    for (int j = 0; j < HG; ++j) acc[j] = 0ull;
+                    const uint32_t* xw = reinterpret_cast<const uint32_t*>(&buf[0]);
+                    const uint32_t* nw = reinterpret_cast<const uint32_t*>(&buf[NLD]);
+#pragma unroll
+                    for (int i = 0; i < NPAIR; ++i) {
+                        const uint64_t kx2 = pack_f32x2(bf16_lo(xw[i]), bf16_hi(xw[i]));
+                        const uint64_t kn2 = pack_f32x2(bf16_lo(nw[i]), bf16_hi(nw[i]));
+#pragma unroll
+                        for (int j = 0; j < HG; ++j) {
+                            fma_f32x2(acc[j], qp2[j][i], kx2);
+                            fma_f32x2(acc[j], qn2[j][i], kn2);
                         }
                     }
-                }
 #pragma unroll
-                for (int w = 0; w < 2; ++w)
-                    if (idx[w] < nitem) scr[idx[w]] = val[w] ? acc[w] : -__int_as_float(0x7f800000);
-            }
-            named_bar_sync(1, kConsumerWarps * 32);
-            if (ctid == 0) mbar_arrive(empty_bar(stg));  // the stage has been read
-            // physical-page keys; keep those above the running K-th key
-            for (int i = ctid; i < cnt; i += kConsumerWarps * 32) {
-                float best = -__int_as_float(0x7f800000);
-                bool any = false;
-                for (int r = 0; r < LPG * p.g; ++r) {
-                    const int it = r * p.npg + i;
-                    const int lp = r / p.g;
-                    if ((x - sst + i) * p.P + lp * 16 < Lb && ((mask >> i) & 1u)) {
-                        best = any ? fmaxf(best, scr[it]) : scr[it];
-                        any = true;
+                    for (int j = 0; j < HG; ++j) {
+                        float ev, od;
+                        unpack_f32x2(acc[j], ev, od);
+                        float t = ev + od;
+#pragma unroll
+                        for (int off = 1; off < LPR; off <<= 1)
+                            t = t + __shfl_xor_sync(0xffffffffu, t, off);
+                        if (j < p.g) best = fmaxf(best, t);
                     }
                 }
-                if (any) {
-                    const uint64_t key = make_key(best, x - sst + i);
-                    if (key > thresh) {
-                        const int slot = atomicAdd(cand_count, 1);
-                        sortbuf[K + slot] = key;
-                    }
+                if (!valid) best = -__int_as_float(0x7f800000);
+                // page maximum over its logical pages (rows)
+                if (LPG <= RPW) {
+                    for (int off = LPR; off < LPR * LPG; off <<= 1)
+                        best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, off));
+                } else {
+                    for (int off = LPR; off < 32; off <<= 1)
+                        best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, off));
+                    run = fmaxf(run, best);
+                    best = run;
+                    if ((k % ngu) != ngu - 1) return;  // the page continues in the next group
+                    run = -__int_as_float(0x7f800000);
                 }
+                // one lane per page proposes the page's key
+                const int u = warp + kSelWarps * (k / ngu);
+                const int first_row = (k % ngu) * RPW + rr;  // row within the unit
+                const int pib0 = (u * unit_rows + first_row) / LPG;
+                const bool leader = c == 0 && (first_row % LPG == 0 || LPG > RPW) &&
+                                    (LPG <= RPW || rr == 0) && pib0 < nblk;
+                uint64_t key = 0ull;
+                if (leader && best != -__int_as_float(0x7f800000)) key = make_key(best, pr0 + pib0);
+                const bool take = key > thresh;
+                const uint32_t bal = __ballot_sync(0xffffffffu, take);
+                if (take) wbuf[K + cnt_c + __popc(bal & ((1u << lane) - 1u))] = key;
+                cnt_c += __popc(bal);
+                __syncwarp();
+                if (cnt_c > capw - 32) {
+                    warp_fold(cnt_c);
+                    cnt_c = 0;
+                    thresh = wbuf[K - 1];
+                }
+            };
+            // three groups in flight per warp
+            uint4 b0[2 * NLD], b1[2 * NLD], b2[2 * NLD];
+            issue(0, b0);
+            issue(1, b1);
+            issue(2, b2);
+            for (int k = 0; k < ng; k += 3) {
+                process(k, b0);
+                issue(k + 3, b0);
+                process(k + 1, b1);
+                issue(k + 4, b1);
+                process(k + 2, b2);
+                issue(k + 5, b2);
             }
-            named_bar_sync(1, kConsumerWarps * 32);
-            if (*cand_count > kSortN - K - p.npg) {
-                fold();
-                thresh = sortbuf[K - 1];
-            }
+            csync();  // bt_blk is rewritten by the next block
         }
-        if (*cand_count > 0) fold();
+        if (cnt_c > 0) warp_fold(cnt_c);
+        csync();
+        // merge the warps' lists of this piece
+        for (int i = tid; i < L.sn; i += NT) {
+            const int w = i / K, r = i - w * K;
+            sortbuf[i] = w < kSelWarps ? reinterpret_cast<uint64_t*>(base + L.wbuf)[w * L.wn + r]
+                                       : 0ull;
+        }
+        csync();
+        bitonic_desc(sortbuf, L.sn, tid, NT, csync);
         const bool whole = (a == sst) && (pe == sst + slen);
         if (whole) {
             finalize(s);
         } else {
             uint64_t* my = p.slots + (int64_t)(cta + s) * K;
-            for (int r = ctid; r < K; r += kConsumerWarps * 32) my[r] = sortbuf[r];
-            named_bar_sync(1, kConsumerWarps * 32);
+            for (int r = tid; r < K; r += NT) my[r] = sortbuf[r];
+            csync();
             const int32_t c_first = split_owner(sst, W, Gw);
             const int32_t c_last = split_owner(sst + slen - 1, W, Gw);
             const int32_t npieces = c_last - c_first + 1;
-            if (ctid == 0) {
+            if (tid == 0) {
                 __threadfence();
                 const int32_t prev = atomicAdd(p.counters + s, 1);
                 *last_flag = (prev == npieces - 1) ? 1 : 0;
                 if (prev == npieces - 1) p.counters[s] = 0;
             }
-            named_bar_sync(1, kConsumerWarps * 32);
+            csync();
             if (*last_flag) {
                 __threadfence();
-                for (int i = ctid; i < kSortN; i += kConsumerWarps * 32) sortbuf[i] = 0ull;
-                named_bar_sync(1, kConsumerWarps * 32);
-                const int per_fold = (kSortN - K) / K;
+                // fold the pieces in groups: sortbuf = [top K | up to (sn - K) new keys]
+                for (int i = tid; i < L.sn; i += NT) sortbuf[i] = 0ull;
+                csync();
+                const int per_fold = (L.sn - K) / K;
                 for (int32_t q0 = 0; q0 < npieces; q0 += per_fold) {
                     const int32_t nq = min(per_fold, npieces - q0);
-                    for (int i = ctid; i < nq * K; i += kConsumerWarps * 32) {
+                    for (int i = tid; i < L.sn - K; i += NT) {
                         const int32_t qq = q0 + i / K, r = i % K;
-                        sortbuf[K + i] = __ldcg(reinterpret_cast<const unsigned long long*>(
-                            p.slots + (int64_t)(c_first + qq + s) * K + r));
+                        sortbuf[K + i] = (i < nq * K)
+                            ? __ldcg(reinterpret_cast<const unsigned long long*>(
+                                  p.slots + (int64_t)(c_first + qq + s) * K + r))
+                            : 0ull;
                     }
-                    if (ctid == 0) *cand_count = nq * K;
-                    named_bar_sync(1, kConsumerWarps * 32);
-                    fold();
+                    csync();
+                    bitonic_desc(sortbuf, L.sn, tid, NT, csync);
                 }
                 finalize(s);
             }
         }
-        named_bar_sync(1, kConsumerWarps * 32);
+        csync();
         a = pe;
     }
 }
 
-int pick_npg(uint32_t page_bytes) {
-    int n = 32;
-    while (n > 1 && (uint32_t)n * (page_bytes + 16u) > 34000u) n >>= 1;
-    return n;
-}
-
-template <int D>
-int sel_occupancy(uint32_t smem) {
+template <int D, int CPL, int HG>
+int sel_prepare(uint32_t smem) {
     static int max_set = 0;
     if ((int)smem > max_set) {
-        if (cudaFuncSetAttribute(page_select_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
+        if (cudaFuncSetAttribute(page_select_kernel<D, CPL, HG>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
             return -1;
         max_set = (int)smem;
     }
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, page_select_kernel<D>, kSelThreads,
-                                                      smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, page_select_kernel<D, CPL, HG>,
+                                                      kSelThreads, smem) != cudaSuccess)
         return 1;
     return n < 1 ? 1 : n;
+}
+
+template <int D, int CPL, int HG>
+cudaError_t sel_launch(int32_t G, uint32_t smem, cudaStream_t stream, const SelParams& p) {
+    return launch_pdl(page_select_kernel<D, CPL, HG>, dim3(G), dim3(kSelThreads), smem, stream,
+                      p);
 }
 
 }  // namespace
@@ -493,12 +546,14 @@ dattn_status_t launch_page_select(const dattn_kv_layout& Lay, const uint16_t* st
     p.top_k = top_k;
     p.selected = selected;
     p.nseg = B * p.Hkv;
-    const int D = Lay.head_dim;
-    p.page_bytes = (uint32_t)(p.P / 16) * 2u * D * 2u;
-    p.npg = pick_npg(p.page_bytes);
     p.dev_err = dev_err;
-    const SelSmem L = sel_smem_layout(D, p.g, p.P, p.npg, B, p.Hkv);
-    const int occ = D == 64 ? sel_occupancy<64>(L.total) : sel_occupancy<128>(L.total);
+    const int D = Lay.head_dim;
+    const bool wide = p.g > 4;  // 8 channels x 8 heads per lane instead of 16 x 4
+    const SelSmem L = sel_smem_layout(B, p.Hkv, top_k);
+    if (L.total > 227u * 1024u) return DATTN_ERR_UNSUPPORTED;
+    int occ;
+    if (D == 64) occ = wide ? sel_prepare<64, 8, 8>(L.total) : sel_prepare<64, 16, 4>(L.total);
+    else occ = wide ? sel_prepare<128, 8, 8>(L.total) : sel_prepare<128, 16, 4>(L.total);
     if (occ < 0) return DATTN_ERR_CUDA;
     const int32_t G = choose_splits(units_bound * 4, num_splits, occ);
     const size_t counters = ((size_t)p.nseg * 4 + 255) & ~(size_t)255;
@@ -507,11 +562,14 @@ dattn_status_t launch_page_select(const dattn_kv_layout& Lay, const uint16_t* st
         return DATTN_ERR_WORKSPACE;
     p.counters = static_cast<int32_t*>(ws);
     p.slots = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + counters);
+    cudaError_t e;
     if (D == 64)
-        page_select_kernel<64><<<G, kSelThreads, L.total, stream>>>(p);
+        e = wide ? sel_launch<64, 8, 8>(G, L.total, stream, p)
+                 : sel_launch<64, 16, 4>(G, L.total, stream, p);
     else
-        page_select_kernel<128><<<G, kSelThreads, L.total, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? DATTN_OK : DATTN_ERR_CUDA;
+        e = wide ? sel_launch<128, 8, 8>(G, L.total, stream, p)
+                 : sel_launch<128, 16, 4>(G, L.total, stream, p);
+    return e == cudaSuccess ? DATTN_OK : DATTN_ERR_CUDA;
 }
 
 }  // namespace dattn

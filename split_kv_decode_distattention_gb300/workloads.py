@@ -90,6 +90,7 @@ class Case:
     max_pages: int = 0
 
     def __post_init__(self):
+        self._memo = {}
         if self.scale == 0.0:
             self.scale = 1.0 / math.sqrt(self.d)
         self.lens = [int(x) for x in self.lens]
@@ -127,22 +128,32 @@ class Case:
         n = min(self.n_needles, L)
         if n <= 0:
             return np.zeros(0, np.int64)
-        return np.sort(_np_rng(self.seed, _TAG["needle"], b).choice(L, size=n, replace=False))
+        key = ("needle", b)
+        if key not in self._memo:
+            self._memo[key] = np.sort(_np_rng(self.seed, _TAG["needle"], b)
+                                      .choice(L, size=n, replace=False))
+        return self._memo[key]
 
     def highsim_pages(self, b: int, kvh: int) -> np.ndarray:
         """Request-relative physical pages whose keys lean toward the group's query."""
         if self.n_highsim <= 0 or self.head_kind is None or \
                 self.head_kind[kvh] != HEAD_RETRIEVAL:
             return np.zeros(0, np.int64)
-        npages = -(-self.lens[b] // self.P)
-        n = min(self.n_highsim, npages)
-        return np.sort(_np_rng(self.seed, _TAG["highsim"], b, kvh)
-                       .choice(npages, size=n, replace=False))
+        key = ("hs", b, kvh)
+        if key not in self._memo:
+            npages = -(-self.lens[b] // self.P)
+            n = min(self.n_highsim, npages)
+            self._memo[key] = np.sort(_np_rng(self.seed, _TAG["highsim"], b, kvh)
+                                      .choice(npages, size=n, replace=False))
+        return self._memo[key]
 
     def _direction(self, b: int, kvh: int, device) -> torch.Tensor:
         """Unit vector of the mean query of KV head kvh's group at step 0 (fp32, [d])."""
-        q = self.q(0, device)[b, kvh * self.g:(kvh + 1) * self.g].float().mean(0)
-        return q / q.norm()
+        key = ("dir", str(device), b, kvh)
+        if key not in self._memo:
+            q = self.q(0, device)[b, kvh * self.g:(kvh + 1) * self.g].float().mean(0)
+            self._memo[key] = q / q.norm()
+        return self._memo[key]
 
     def kv(self, b: int, t0: int, t1: int, device="cpu"):
         """Token-ordered K and V of request b, tokens [t0, t1): bf16 [t1-t0][Hkv][d] each.
@@ -166,12 +177,16 @@ class Case:
                     pages = self.highsim_pages(b, kvh)
                     if pages.size == 0:
                         continue
+                    lo_p, hi_p = base // self.P, (base + GEN_CHUNK - 1) // self.P
+                    inside = pages[(pages >= lo_p) & (pages <= hi_p)]
+                    if inside.size == 0:
+                        continue
                     u = self._direction(b, kvh, device)
-                    for p in pages:
+                    for p in inside:
                         a = max(int(p) * self.P, base)
                         z = min((int(p) + 1) * self.P, base + GEN_CHUNK)
                         if a < z:
-                            Kc[a - base:z - base, kvh] += 2.0 * u
+                            Kc[a - base:z - base, kvh] += 8.0 * u
             lo, hi = max(t0, base), min(t1, base + GEN_CHUNK)
             K[lo - t0:hi - t0] = Kc[lo - base:hi - base].to(torch.bfloat16)
             V[lo - t0:hi - t0] = Vc[lo - base:hi - base].to(torch.bfloat16)

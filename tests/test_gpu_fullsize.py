@@ -1,0 +1,175 @@
+"""Full-size parity of the five workloads, run in the launch configuration the benchmark
+times (automatic split count). Outputs are checked against the oracle on sampled
+(request, head) pairs, which the oracle computes one at a time. Properties that hold at any
+size are checked on everything: the page-set merge equals the fused decode, the selection
+is bit-exact, and no device error is flagged."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from split_kv_decode_distattention_gb300 import workloads as W
+
+from _util import assert_e_close, assert_m_close, assert_out_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _lib():
+    import split_kv_decode_distattention_gb300 as dattn
+    dattn.load_library()
+    return dattn
+
+
+def _cache(case, **kw):
+    from split_kv_decode_distattention_gb300.harness import PagedCache
+    kw.setdefault("chunk_tokens", 32768)
+    return PagedCache(case, DEV, **kw)
+
+
+def _host_heads(case, b, L, heads, chunk=65536):
+    """Token-ordered K, V of request b for the given KV heads: uint16 [len(heads)][L][d]."""
+    Ks = np.empty((len(heads), L, case.d), np.uint16)
+    Vs = np.empty_like(Ks)
+    for t0 in range(0, L, chunk):
+        t1 = min(L, t0 + chunk)
+        K, V = case.kv(b, t0, t1, DEV)
+        for i, h in enumerate(heads):
+            Ks[i, t0:t1] = oracle.bf16_bits(K[:, h])
+            Vs[i, t0:t1] = oracle.bf16_bits(V[:, h])
+    return Ks, Vs
+
+
+def _check_pairs(case, q, lens, out, m_g, e_g, pairs, what, rows_of=None):
+    qb = oracle.bf16_bits(q)
+    o, mg, eg = out.cpu().numpy(), m_g.cpu().numpy(), e_g.cpu().numpy()
+    by_b = {}
+    for b, h in pairs:
+        by_b.setdefault(b, set()).add(h // case.g)
+    for b, kvhs in by_b.items():
+        kvhs = sorted(kvhs)
+        Ks, Vs = _host_heads(case, b, lens[b], kvhs)
+        for bb, h in pairs:
+            if bb != b:
+                continue
+            i = kvhs.index(h // case.g)
+            rows = rows_of(b, h // case.g) if rows_of else None
+            r, rm, re = oracle.attention(qb[b, h], Ks[i], Vs[i], case.scale, rows=rows)
+            assert_out_close(o[b, h], r, f"{what} b={b} h={h}")
+            assert_m_close(mg[b, h], rm, f"{what} b={b} h={h}")
+            assert_e_close(eg[b, h], re, f"{what} b={b} h={h}")
+
+
+def _step(cache, case, sparse=None):
+    kn, vn = cache.new_tokens(1)
+    cache.append(kn, vn)
+    q = case.q(1, DEV)
+    out = torch.empty(case.B, case.Hq, case.d, device=DEV)
+    m_g = torch.empty(case.B, case.Hq, device=DEV)
+    e_g = torch.empty_like(m_g)
+    cache.decode(q, out, cache.workspace(), m_g=m_g, e_g=e_g, sparse=sparse)
+    torch.cuda.synchronize()
+    assert int(cache.dev_err.item()) == 0
+    return q, out, m_g, e_g
+
+
+def test_mha_32k_batch8_full_size():
+    """Llama-2-7B MHA: batch 8, 32 heads, d 128, 32K tokens, shuffled 16-token pages."""
+    _lib()
+    case = W.mha_32k(seed=0)
+    cache = _cache(case)
+    q, out, m_g, e_g = _step(cache, case)
+    assert torch.isfinite(out).all()
+    pairs = [(b, (7 * b + 3) % 32) for b in range(8)] + [(0, 0), (7, 31)]
+    _check_pairs(case, q, cache.lens, out, m_g, e_g, pairs, "mha-32k")
+    # the paged append wrote the new token where the block table says, bit for bit
+    K1, V1 = case.kv(5, cache.lens[5] - 1, cache.lens[5], DEV)
+    pos = cache.lens[5] - 1
+    page = case.block_table[5][pos // case.P]
+    assert torch.equal(cache.k_pool[page, :, pos % case.P], K1[0])
+    assert torch.equal(cache.v_pool[page, :, pos % case.P], V1[0])
+
+
+def test_mha_1m_single_request_full_size():
+    """One request of 2^20 tokens, 32 heads MHA, 64 needle keys; split across all SMs."""
+    _lib()
+    case = W.mha_1m(seed=0)
+    cache = _cache(case)
+    q, out, m_g, e_g = _step(cache, case)
+    _check_pairs(case, q, cache.lens, out, m_g, e_g, [(0, 0), (0, 13), (0, 31)], "mha-1m")
+
+
+def test_gqa_ragged_full_size_and_page_set_merge():
+    """64 requests, 32 q / 8 KV heads, lengths 1K-256K; page-set partials merge to fused."""
+    dattn = _lib()
+    case = W.gqa_ragged(seed=0)
+    cache = _cache(case)
+    q, out, m_g, e_g = _step(cache, case)
+    order = np.argsort(case.lens)
+    sample_b = [int(order[0]), int(order[31]), int(order[-1])]
+    pairs = [(b, h) for b in sample_b for h in (0, 13, 31)]
+    _check_pairs(case, q, cache.lens, out, m_g, e_g, pairs, "gqa-ragged")
+    # every request split into 2-8 disjoint page sets: partials + merge == fused decode
+    reqs, indptr, pages, ranges = [], [0], [], [0]
+    for b in range(case.B):
+        for s in case.page_sets_of(b, cache.lens[b]):
+            reqs.append(b)
+            pages.extend(s.tolist())
+            indptr.append(len(pages))
+        ranges.append(len(reqs))
+    C = len(reqs)
+    m = torch.empty(C, case.Hq, device=DEV)
+    e = torch.empty_like(m)
+    MA = torch.empty(C, case.Hq, case.d, device=DEV)
+    dattn.dattn_partial(cache.layout, cache.k_pool, cache.v_pool, q, case.scale, cache.seq_lens,
+                        torch.tensor(reqs, dtype=torch.int32, device=DEV),
+                        torch.tensor(indptr, dtype=torch.int32, device=DEV),
+                        torch.tensor(pages, dtype=torch.int32, device=DEV), m, e, MA,
+                        dattn.Workspace(C, case.Hq, case.Hkv, case.d), dev_err=cache.dev_err)
+    merged = torch.empty_like(out)
+    mm = torch.empty_like(m_g)
+    me = torch.empty_like(e_g)
+    dattn.dattn_merge(torch.tensor(ranges, dtype=torch.int32, device=DEV), m, e, MA, out=merged,
+                      m_g=mm, e_g=me)
+    torch.cuda.synchronize()
+    assert int(cache.dev_err.item()) == 0
+    assert_out_close(merged.cpu().numpy(), out.cpu().numpy(), "page-set merge vs fused")
+    np.testing.assert_allclose(mm.cpu().numpy(), m_g.cpu().numpy(), rtol=1e-5)
+    np.testing.assert_allclose(me.cpu().numpy(), e_g.cpu().numpy(), rtol=1e-4)
+
+
+def test_sparse_512k_full_size():
+    """LServe block-sparse: batch 8, 32 q / 8 KV heads, 512K, 64-token pages, top-64."""
+    _lib()
+    case = W.sparse_512k(seed=0)
+    cache = _cache(case, with_stats=True)
+    kn, vn = cache.new_tokens(1)
+    cache.append(kn, vn)  # the first step of the window appends, then selects
+    q0 = case.q(0, DEV)
+    sel = torch.empty(case.B, case.Hkv, case.top_k, dtype=torch.int32, device=DEV)
+    cache.select(q0, sel, cache.workspace(top_k=case.top_k))
+    torch.cuda.synchronize()
+    assert int(cache.dev_err.item()) == 0
+    got = sel.cpu().numpy()
+    # non-retrieval rows are all -1; retrieval rows are sorted, distinct and in range
+    for h in range(case.Hkv):
+        if case.head_kind[h] != W.HEAD_RETRIEVAL:
+            assert (got[:, h] == -1).all()
+    qb = oracle.bf16_bits(q0)
+    for b, h in [(0, 0), (3, 2), (7, 3)]:
+        Ks, _ = _host_heads(case, b, cache.lens[b], [h])
+        want = oracle.select_pages(qb[b, h * case.g:(h + 1) * case.g], Ks[0], cache.lens[b],
+                                   case.P, case.top_k)
+        np.testing.assert_array_equal(got[b, h], want, err_msg=f"selection b={b} h={h}")
+        # the seeded high-similarity pages are all selected
+        assert set(case.highsim_pages(b, h).tolist()) <= set(want.tolist())
+    # decode with the selection reused for the rest of the window
+    sp = cache.sparse_config(sel)
+    q, out, m_g, e_g = _step(cache, case, sparse=sp)
+
+    def rows_of(b, kvh):
+        return oracle.sparse_rows(case.head_kind[kvh], cache.lens[b], case.P, got[b, kvh],
+                                  case.sinks, case.local)
+    pairs = [(0, 0), (0, 17), (3, 8), (7, 15), (7, 31), (5, 20)]
+    _check_pairs(case, q, cache.lens, out, m_g, e_g, pairs, "sparse-512k", rows_of=rows_of)

@@ -405,3 +405,20 @@ def test_decode_length_beyond_table_is_flagged_and_clamped():
     cache.decode(case.q(0, DEV), out, cache.workspace())
     torch.cuda.synchronize()
     assert int(cache.dev_err.item()) & dattn.DEVERR["LEN_OOB"]
+
+
+@pytest.mark.parametrize("Hq,Hkv,d,P", [(16, 2, 128, 64), (8, 8, 128, 16), (24, 3, 64, 64),
+                                       (8, 1, 64, 128)])
+def test_page_select_bit_exact_group_sizes(Hq, Hkv, d, P):
+    """GQA groups of 8 (8-channel chunks), 1 and 3, and 128-token pages (8 logical pages)."""
+    _lib()
+    kinds = [1] * Hkv
+    case = W.Case("selg", B=2, Hq=Hq, Hkv=Hkv, d=d, P=P, lens=[P * 70 + 9, P * 33], seed=Hq + P,
+                  head_kind=kinds, top_k=16, n_highsim=4)
+    cache = _cache(case, with_stats=True)
+    q = case.q(0, DEV)
+    sel = torch.full((case.B, case.Hkv, 16), 7777, dtype=torch.int32, device=DEV)
+    cache.select(q, sel, cache.workspace(top_k=16))
+    torch.cuda.synchronize()
+    assert int(cache.dev_err.item()) == 0
+    np.testing.assert_array_equal(sel.cpu().numpy(), _oracle_selection(case, cache, q))
