@@ -60,8 +60,7 @@ _SIGS = {
     "orc_kv_write": (_I64, [_P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _I64, _I64]),
     "orc_logical_page_stats": (None, [_P, _I64, _I, _I64, _I64, _P, _P]),
     "orc_logical_score_f64": (_D, [_P, _P, _P, _I]),
-    "orc_logical_score_f32": (ctypes.c_float, [_P, _P, _P, _I, _I]),
-    "orc_decision_chunk": (_I, [_I]),
+    "orc_logical_score_f32": (ctypes.c_float, [_P, _P, _P, _I]),
     "orc_page_scores": (None, [_P, _I, _P, _I64, _I, _I64, _I, _I, _P]),
     "orc_topk": (None, [_P, _I64, _I, _P]),
     "orc_sparse_rows": (_I64, [_I, _I64, _I, _P, _I, _I, _I, _P]),
@@ -202,15 +201,14 @@ def logical_page_stats(K, t0: int, t1: int, lib=None):
     return kmax, kmin
 
 
-def logical_score(q, kmax, kmin, precision64: bool = True, g: int = 1, lib=None) -> float:
+def logical_score(q, kmax, kmin, precision64: bool = True, lib=None) -> float:
     """Logical-page score sum_d max(q_d kmax_d, q_d kmin_d): the fp64 definition, or the
-    fp32 decision arithmetic of a KV head serving g query heads."""
+    fp32 decision arithmetic."""
     lib = lib or load()
     q, kmax, kmin = bf16_bits(q), bf16_bits(kmax), bf16_bits(kmin)
     if precision64:
         return float(lib.orc_logical_score_f64(_ptr(q), _ptr(kmax), _ptr(kmin), q.shape[-1]))
-    return float(lib.orc_logical_score_f32(_ptr(q), _ptr(kmax), _ptr(kmin), q.shape[-1],
-                                           lib.orc_decision_chunk(g)))
+    return float(lib.orc_logical_score_f32(_ptr(q), _ptr(kmax), _ptr(kmin), q.shape[-1]))
 
 
 def page_scores(Q, K, L: int, P: int, precision64: bool, lib=None) -> np.ndarray:

@@ -40,8 +40,8 @@
  *  R7  A streaming head at length L attends [0, min(S, L)) U [max(S, L - W), L).
  *  R8  k_max/k_min use strict comparison in token order, so the first-seen value wins a
  *      tie (this matters only for +0/-0).
- *  R9  The page selection is decided in the kernel's arithmetic: fp32 in a fixed blocked
- *      order (see orc_logical_score_f32). The fp64 score is the definition, and the tests
+ *  R9  The page selection is decided in the kernel's arithmetic: fp32 in a fixed order
+ *      (see orc_logical_score_f32). The fp64 score is the definition, and the tests
  *      check that the two differ by less than the fp32 error bound.
  */
 #include "dattn_oracle.h"
@@ -247,43 +247,51 @@ double orc_logical_score_f64(const uint16_t *q, const uint16_t *kmax, const uint
 }
 
 /*
- * The same score in the arithmetic that decides the selection (reading R9). It is fp32 in
- * a fixed order, so that both sides take the same integer decision:
- *  - the channels are taken in chunks of `chunk` channels (16 when a KV head serves up to
- *    4 query heads, 8 otherwise);
- *  - within a chunk there are two fp32 sums, for even and odd channels, both from +0. Per
- *    channel, each adds by fused multiply-add first max(q,0)*kmax, then min(q,0)*kmin. One
- *    of the two products is an exact zero, so the sum gains exactly the product that the
- *    definition's max picks (for q_d >= 0 it is q_d*kmax_d, else q_d*kmin_d);
- *  - a chunk's partial is even + odd, and the partials are added by a pairwise tree
- *    (adjacent chunks, then adjacent pairs, and so on).
- * Each product of two bf16 values is exact in fp32; only the additions round.
+ * One partial of the decision arithmetic: two fp32 fused multiply-add chains from +0, over
+ * the even and over the odd channels of [c0, c0 + n) in ascending order, then even + odd.
+ * The query factor is the positive part max(q,0) (neg == 0, paired with k_max) or the
+ * negative part min(q,0) (neg == 1, paired with k_min).
  */
-float orc_logical_score_f32(const uint16_t *q, const uint16_t *kmax, const uint16_t *kmin, int d,
-                            int chunk)
+static float decision_partial(const uint16_t *q, const uint16_t *k, int c0, int n, int neg)
 {
-    float part[64];
-    if (chunk > d) chunk = d;  /* a head narrower than one chunk is one chunk */
-    const int nch = d / chunk;
-    for (int c = 0; c < nch; ++c) {
-        float even = 0.0f, odd = 0.0f;
-        for (int i = 0; i < chunk; i += 2) {
-            const int d0 = c * chunk + i, d1 = d0 + 1;
-            const float q0 = bf16_to_float(q[d0]), q1 = bf16_to_float(q[d1]);
-            even = fmaf(q0 >= 0.0f ? q0 : 0.0f, bf16_to_float(kmax[d0]), even);
-            even = fmaf(q0 >= 0.0f ? 0.0f : q0, bf16_to_float(kmin[d0]), even);
-            odd = fmaf(q1 >= 0.0f ? q1 : 0.0f, bf16_to_float(kmax[d1]), odd);
-            odd = fmaf(q1 >= 0.0f ? 0.0f : q1, bf16_to_float(kmin[d1]), odd);
-        }
-        part[c] = even + odd;
+    float even = 0.0f, odd = 0.0f;
+    for (int i = 0; i < n; i += 2) {
+        const float q0 = bf16_to_float(q[c0 + i]), q1 = bf16_to_float(q[c0 + i + 1]);
+        const float f0 = neg ? (q0 >= 0.0f ? 0.0f : q0) : (q0 >= 0.0f ? q0 : 0.0f);
+        const float f1 = neg ? (q1 >= 0.0f ? 0.0f : q1) : (q1 >= 0.0f ? q1 : 0.0f);
+        even = fmaf(f0, bf16_to_float(k[c0 + i]), even);
+        odd = fmaf(f1, bf16_to_float(k[c0 + i + 1]), odd);
     }
-    for (int level = 1; level < nch; level <<= 1)
-        for (int c = 0; c < nch; c += 2 * level) part[c] = part[c] + part[c + level];
-    return part[0];
+    return even + odd;
 }
 
-/* Chunk size of the decision arithmetic for a KV head serving g query heads. */
-int orc_decision_chunk(int g) { return g <= 4 ? 16 : 8; }
+/*
+ * The same score in the arithmetic that decides the selection (reading R9). It is fp32 in
+ * a fixed order, so that both sides take the same integer decision:
+ *  - the channels form nch chunks of w = d/16 channels (w = 2, nch = d/2 when d < 32);
+ *  - chunk c gives two partials (decision_partial): k_max with max(q,0) and k_min with
+ *    min(q,0). One of the two query factors is an exact zero, so together they add exactly
+ *    the product that the definition's max picks (q_d*kmax_d for q_d >= 0, else q_d*kmin_d);
+ *  - x[c] is the k_max partial of chunk c and x[nch + c] its k_min partial; they are added
+ *    by the tree x[i] = x[i] + x[i + n] for n = nch, nch/2, ..., 1 (i < n), and the score
+ *    is x[0].
+ * Each product of two bf16 values is exact in fp32; only the additions round. d must be
+ * even with nch a power of two (d = 2, 4, 8, 16, or a multiple of 32).
+ */
+float orc_logical_score_f32(const uint16_t *q, const uint16_t *kmax, const uint16_t *kmin, int d)
+{
+    float x[64];
+    const int w = d >= 32 ? d / 16 : 2;
+    const int nch = d / w;
+    if (d % 2 != 0 || nch > 32 || (nch & (nch - 1)) != 0 || nch * w != d) return NAN;
+    for (int c = 0; c < nch; ++c) {
+        x[c] = decision_partial(q, kmax, c * w, w, 0);
+        x[nch + c] = decision_partial(q, kmin, c * w, w, 1);
+    }
+    for (int n = nch; n >= 1; n >>= 1)
+        for (int i = 0; i < n; ++i) x[i] = x[i] + x[i + n];
+    return x[0];
+}
 
 /*
  * Physical-page scores of one request and one KV head [LV §3.1.2 score_pages: max over the
@@ -311,8 +319,7 @@ void orc_page_scores(const uint16_t *Q, int g, const uint16_t *K, int64_t row_st
                     const double s = orc_logical_score_f64(Q + (int64_t)j * d, kmax, kmin, d);
                     if (s > best) best = s;
                 } else {
-                    const float s = orc_logical_score_f32(Q + (int64_t)j * d, kmax, kmin, d,
-                                                          orc_decision_chunk(g));
+                    const float s = orc_logical_score_f32(Q + (int64_t)j * d, kmax, kmin, d);
                     if (s > best32) best32 = s;
                 }
             }

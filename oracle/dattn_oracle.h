@@ -34,10 +34,7 @@ void orc_logical_page_stats(const uint16_t *K, int64_t row_stride, int d, int64_
 
 double orc_logical_score_f64(const uint16_t *q, const uint16_t *kmax, const uint16_t *kmin, int d);
 
-float orc_logical_score_f32(const uint16_t *q, const uint16_t *kmax, const uint16_t *kmin, int d,
-                            int chunk);
-
-int orc_decision_chunk(int g);
+float orc_logical_score_f32(const uint16_t *q, const uint16_t *kmax, const uint16_t *kmin, int d);
 
 void orc_page_scores(const uint16_t *Q, int g, const uint16_t *K, int64_t row_stride, int d,
                      int64_t L, int P, int precision64, double *score);

@@ -8,35 +8,38 @@
 //     pages, and the K highest-scoring physical pages are kept.
 // The logical score is sum_d max(q_d * kmax_d, q_d * kmin_d), an upper bound of q . k for
 // every key of the logical page. With g query heads per KV head, the score is the max over
-// the g heads, so one selection serves the whole group. The sum is accumulated in fp32,
-// one fused multiply-add per channel in ascending channel order. For q_d >= 0 the larger
-// product is q_d * kmax_d, otherwise q_d * kmin_d. This fixed arithmetic decides the
-// selection.
+// the g heads, so one selection serves the whole group.
 //
 // GB300 design. The statistics scan is HBM-bound: every reuse window it reads all k_max and
 // k_min of the retrieval heads (512 B per logical page at d = 128), and it must score them
 // at that speed. The physical pages of all retrieval (request, KV head) pairs are laid end
-// to end and cut into equal contiguous ranges, one per CTA (one CTA per SM).
-//  - No staging: eight warps read the statistics straight into registers with coalesced
-//    16-byte loads, software-pipelined three groups deep. A logical page's 2*d values are
-//    spread over d/16 lanes (16 channels each), so each lane keeps the query values of its
-//    channels for four heads in registers for the whole piece.
-//  - A lane runs its 16 channels as two chains (even and odd channels) of packed fp32x2
-//    fused multiply-adds, four heads at once. The lanes of a logical page then combine
-//    their partial sums with a fixed butterfly.
-//  - Page maxima that beat the warp's running K-th key go to a per-warp candidate buffer.
-//    The buffer is folded into the warp's top K by a warp-synchronous bitonic sort.
+// to end and cut into equal contiguous ranges, one per CTA.
+//  - A warp reads one logical page per load instruction, fully coalesced: lanes 0-15 take
+//    d/16 channels each of k_max, lanes 16-31 the same channels of k_min. The query values
+//    of those channels stay in the lane's registers for the whole piece (their positive
+//    part for k_max lanes, their negative part for k_min lanes), as fp32 pairs for packed
+//    fp32x2 fused multiply-adds.
+//  - A batch is 32 / HG logical pages. Each lane leaves one partial sum per (page, head):
+//    32 values. One transposed butterfly over the 32 lanes (31 shuffles) sums them, after
+//    which lane l holds the full score of page l / HG and head l % HG.
+//  - Loads run one batch ahead: the register holding a page's data is refilled with the
+//    same page of the warp's next batch as soon as it has been used. Block-table entries of
+//    the piece are staged in shared memory first, so no load waits on another.
+//  - The physical-page score is a max over adjacent lanes (heads, then logical pages). Page
+//    maxima that beat the warp's running K-th key go to a per-warp candidate buffer, folded
+//    into the warp's top K by a warp-synchronous bitonic sort.
 //  - At the end of a piece the eight warps' lists are merged. A head split across CTAs
 //    leaves each CTA's top K in the workspace, and the CTA that arrives last merges them.
 //
 // Decision arithmetic (the selection is an integer decided by floating point, so it is
-// fixed exactly, and the oracle repeats it). For head j, channels are taken in chunks of C
-// (C = 16 for groups of up to 4 query heads, C = 8 otherwise). Within a chunk there are two
-// fp32 accumulators, for even and odd channels, both starting at +0. Each channel adds, by
-// fused multiply-add, first max(q,0)*kmax then min(q,0)*kmin; one of the two is an exact
-// zero, so this adds exactly the product q*kmax or q*kmin that the score definition selects.
-// A chunk's partial is even + odd. The partials are summed by a pairwise tree: adjacent
-// chunks first, then pairs of pairs.
+// fixed exactly, and the oracle repeats it). Channels form 16 chunks of d/16. For each chunk
+// c there are two partials: k_max with the positive part max(q,0), and k_min with the
+// negative part min(q,0). A partial runs two fp32 fused multiply-add chains from +0, over
+// the chunk's even and its odd channels in ascending order, and is even + odd. Since one of
+// max(q,0), min(q,0) is an exact zero, the two partials together add exactly the product
+// q*kmax or q*kmin that the score definition selects. The 32 partials x[0..15] (k_max
+// chunks) and x[16..31] (k_min chunks) are then added by the tree
+// x[i] = x[i] + x[i + n] for n = 16, 8, 4, 2, 1 (i < n), and the score is x[0].
 #include "common.cuh"
 #include "internal.h"
 
@@ -46,7 +49,6 @@ namespace {
 
 constexpr int kSelWarps = 8;
 constexpr int kSelThreads = kSelWarps * 32;
-constexpr int kSelBlockPages = 1024;  // pages whose block-table entries are staged at once
 
 struct SelParams {
     int32_t num_pages, Hkv, P, max_pages;
@@ -70,21 +72,23 @@ __host__ __device__ inline int next_pow2(int x) {
     return n;
 }
 
+constexpr int kSelBT = 2048;  // block-table entries staged in shared memory at once
+
 struct SelSmem {
-    uint32_t flags, bt, wbuf, sortbuf, ret_before, ret_heads, item_start, item_len, scan, total;
-    int wn, sn;
+    uint32_t flags, bt, wbuf, ret_before, ret_heads, item_start, item_len, scan, total;
+    int kp, wn;
 };
 
 __host__ __device__ inline SelSmem sel_smem_layout(int B, int Hkv, int K) {
     SelSmem s;
-    s.wn = next_pow2(2 * K);                 // per-warp buffer: top K + candidates
-    s.sn = next_pow2(kSelWarps * K);         // CTA buffer: the warps' lists, or pieces to fold
+    s.kp = next_pow2(K);                     // list length: K rounded up to a power of two
+    // per-warp buffer: running list + at least max(Kp, 32) candidates (a batch adds up to
+    // 32 before a fold), a power of two for the sort
+    s.wn = next_pow2(s.kp + (s.kp > 32 ? s.kp : 32));
     uint32_t o = 0;
     s.flags = o;      o += 16u;
-    s.bt = o;         o += kSelBlockPages * 4u;
-    o = (o + 15u) & ~15u;
+    s.bt = o;         o += kSelBT * 4u;
     s.wbuf = o;       o += (uint32_t)kSelWarps * s.wn * 8u;
-    s.sortbuf = o;    o += (uint32_t)s.sn * 8u;
     s.ret_before = o; o += (uint32_t)(Hkv + 1) * 4u;
     s.ret_heads = o;  o += (uint32_t)Hkv * 4u;
     o = (o + 15u) & ~15u;
@@ -117,15 +121,6 @@ __device__ __forceinline__ void fma_f32x2(uint64_t& acc, uint64_t a, uint64_t b)
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
 
-// 16-byte streaming load (read once: no L1 allocation, evict-first in L2)
-__device__ __forceinline__ uint4 ldg_stream(const void* ptr, uint64_t pol) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(ptr), "l"(pol));
-    return v;
-}
-
 // Bitonic sort of buf[0..n) into descending order by nthreads threads (index tid); sync()
 // separates the steps.
 template <typename Sync>
@@ -148,14 +143,68 @@ __device__ __forceinline__ void bitonic_desc(uint64_t* buf, int n, int tid, int 
     }
 }
 
-// D: head_dim; CPL: channels per lane (16 or 8); HG: query heads per lane (4 or 8).
-template <int D, int CPL, int HG>
-__global__ void __launch_bounds__(kSelThreads, 1)
+// Warp-synchronous merge of two descending lists a[0..n) and b[0..n) (n a power of two):
+// a becomes the n largest keys of both, descending. c[i] = max(a[i], b[n-1-i]) holds those
+// keys as a bitonic sequence, which a cascade of half-cleaners sorts.
+__device__ __forceinline__ void warp_merge_desc(uint64_t* a, const uint64_t* b, int n, int lane) {
+    for (int i = lane; i < n; i += 32) {
+        const uint64_t x = a[i], y = b[n - 1 - i];
+        a[i] = x > y ? x : y;
+    }
+    __syncwarp();
+    for (int j = n >> 1; j > 0; j >>= 1) {
+        for (int idx = lane; idx < (n >> 1); idx += 32) {
+            const int i = ((idx & ~(j - 1)) << 1) | (idx & (j - 1));
+            const uint64_t x = a[i], y = a[i + j];
+            if (x < y) {
+                a[i] = y;
+                a[i + j] = x;
+            }
+        }
+        __syncwarp();
+    }
+}
+
+template <int CPL> struct ChunkVec;
+template <> struct ChunkVec<8> { using type = uint4; };  // 8 bf16 channels
+template <> struct ChunkVec<4> { using type = uint2; };  // 4 bf16 channels
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& v, uint64_t (&k)[4]) {
+    k[0] = pack_f32x2(bf16_lo(v.x), bf16_hi(v.x));
+    k[1] = pack_f32x2(bf16_lo(v.y), bf16_hi(v.y));
+    k[2] = pack_f32x2(bf16_lo(v.z), bf16_hi(v.z));
+    k[3] = pack_f32x2(bf16_lo(v.w), bf16_hi(v.w));
+}
+__device__ __forceinline__ void unpack_bf16x8(const uint2& v, uint64_t (&k)[2]) {
+    k[0] = pack_f32x2(bf16_lo(v.x), bf16_hi(v.x));
+    k[1] = pack_f32x2(bf16_lo(v.y), bf16_hi(v.y));
+}
+
+// Read-once load of a lane's chunk of one logical page (no L1 allocation, evict-first L2).
+__device__ __forceinline__ void ld_chunk(uint4& v, const uint16_t* ptr, uint64_t pol) {
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr), "l"(pol));
+}
+__device__ __forceinline__ void ld_chunk(uint2& v, const uint16_t* ptr, uint64_t pol) {
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
+                 : "=r"(v.x), "=r"(v.y)
+                 : "l"(ptr), "l"(pol));
+}
+
+// D: head_dim; HG: query heads scored per KV head (4 or 8, unused ones masked);
+// LPG: logical pages per physical page (P / 16, a power of two).
+template <int D, int HG, int LPG>
+__global__ void __launch_bounds__(kSelThreads, HG == 4 ? 2 : 1)
 page_select_kernel(const __grid_constant__ SelParams p) {
-    constexpr int LPR = D / CPL;     // lanes per logical page (row)
-    constexpr int RPW = 32 / LPR;    // rows per warp group
-    constexpr int NLD = CPL / 8;     // 16-byte loads per lane for k_max (and for k_min)
-    constexpr int NPAIR = CPL / 2;   // channel pairs per lane
+    constexpr int CPL = D / 16;              // channels per lane
+    constexpr int NPR = CPL / 2;             // channel pairs per lane
+    constexpr int R = 32 / HG;               // logical pages per batch
+    constexpr int UNIT = LPG > R ? LPG : R;  // logical pages per warp unit (whole pages)
+    constexpr int NB = UNIT / R;             // batches per unit
+    constexpr int PPU = UNIT / LPG;          // physical pages per unit
+    using Vec = typename ChunkVec<CPL>::type;
+    const float kNInf = -__int_as_float(0x7f800000);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_off = smem_u32(smem_raw);
     uint8_t* base = smem_raw + (((raw_off + 127u) & ~127u) - raw_off);
@@ -163,10 +212,7 @@ page_select_kernel(const __grid_constant__ SelParams p) {
     const SelSmem L = sel_smem_layout(p.B, p.Hkv, K);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t G = gridDim.x, cta = blockIdx.x;
-    const int LPG = p.P >> 4;
     int* last_flag = reinterpret_cast<int*>(base + L.flags);
-    int32_t* bt_blk = reinterpret_cast<int32_t*>(base + L.bt);
-    uint64_t* sortbuf = reinterpret_cast<uint64_t*>(base + L.sortbuf);
     int32_t* ret_before = reinterpret_cast<int32_t*>(base + L.ret_before);
     int32_t* ret_heads = reinterpret_cast<int32_t*>(base + L.ret_heads);
     int32_t* item_start = reinterpret_cast<int32_t*>(base + L.item_start);
@@ -262,36 +308,54 @@ page_select_kernel(const __grid_constant__ SelParams p) {
     }
     if (t_begin >= t_end) return;
 
-    const uint64_t pol = policy_evict_first();
     const int NT = kSelThreads;
-    uint64_t* wbuf = reinterpret_cast<uint64_t*>(base + L.wbuf) + warp * L.wn;
-    const int capw = L.wn - K;
+    const int Kp = L.kp;  // K rounded up to a power of two; key 0 marks an empty entry
+    uint64_t* wbuf_all = reinterpret_cast<uint64_t*>(base + L.wbuf);
+    uint64_t* wbuf = wbuf_all + warp * L.wn;  // [0, Kp): running top keys; then candidates
+    const int capw = L.wn - Kp;
     auto csync = [&]() { __syncthreads(); };
     auto wsync = [&]() { __syncwarp(); };
-    auto warp_fold = [&](int cnt) {  // fold candidates wbuf[K .. K+cnt) into wbuf[0 .. K)
-        for (int i = K + cnt + lane; i < L.wn; i += 32) wbuf[i] = 0ull;
+    auto warp_fold = [&](int cnt) {  // fold candidates wbuf[Kp .. Kp+cnt) into wbuf[0 .. Kp)
+        for (int i = Kp + cnt + lane; i < L.wn; i += 32) wbuf[i] = 0ull;
         __syncwarp();
         bitonic_desc(wbuf, L.wn, lane, 32, wsync);
     };
-    auto finalize = [&](int32_t seg) {  // sortbuf[0 .. K): top K keys -> ascending pages
-        for (int i = tid; i < L.sn; i += NT)
-            sortbuf[i] = i < K ? (sortbuf[i] & 0xFFFFFFFFull) * (sortbuf[i] != 0ull) : 0ull;
-        csync();
-        bitonic_desc(sortbuf, next_pow2(K), tid, NT, csync);  // low word desc = page asc
-        for (int r = tid; r < K; r += NT) {
-            const uint64_t kk = sortbuf[r];
-            p.selected[(int64_t)seg * K + r] = kk ? (int32_t)(0xFFFFFFFFu - (uint32_t)kk) : -1;
+    // the list of warp w after the pieces' and warps' lists are merged: sorted descending
+    auto list_of = [&](int w) { return wbuf_all + w * L.wn; };
+    // merges the warps' running lists into list_of(0) (three levels of pairwise merges)
+    auto merge_warps = [&]() {
+#pragma unroll 1
+        for (int n = kSelWarps / 2; n >= 1; n >>= 1) {
+            if (warp < n) warp_merge_desc(list_of(warp), list_of(warp + n), Kp, lane);
+            csync();
+        }
+    };
+    // list_of(0)[0 .. K): top K keys -> selected row of segment seg, ascending pages
+    auto finalize = [&](int32_t seg) {
+        if (warp == 0) {
+            uint64_t* f = list_of(0);
+            for (int i = lane; i < Kp; i += 32)
+                f[i] = (i < K && f[i] != 0ull) ? (f[i] & 0xFFFFFFFFull) : 0ull;
+            __syncwarp();
+            bitonic_desc(f, Kp, lane, 32, wsync);  // low word descending = page ascending
+            for (int r = lane; r < K; r += 32) {
+                const uint64_t kk = f[r];
+                p.selected[(int64_t)seg * K + r] = kk ? (int32_t)(0xFFFFFFFFu - (uint32_t)kk) : -1;
+            }
         }
         csync();
     };
 
-    // lane layout inside a warp group: row rr = lane / LPR, chunk c = lane % LPR
-    const int c = lane % LPR, rr = lane / LPR;
-    // rows of a unit: whole pages, at least one warp group
-    const int unit_rows = LPG > RPW ? LPG : RPW;
-    const int up = unit_rows / LPG;          // pages per unit
-    const int ngu = unit_rows / RPW;         // warp groups per unit
-    uint64_t qp2[HG][NPAIR], qn2[HG][NPAIR];  // the lane's query values: {ch 2i, ch 2i+1}
+    const uint64_t pol = policy_evict_first();
+    int32_t* bt_s = reinterpret_cast<int32_t*>(base + L.bt);
+    const int half = lane >> 4;           // 0: k_max lanes, 1: k_min lanes
+    const int c0 = CPL * (lane & 15);     // first channel of the lane
+    const int lane_off = half * D + c0;   // element offset inside a logical-page row
+    const uint16_t* stats_lane = p.stats + lane_off;
+    const int hj = lane % HG;             // head of the score the lane holds after reduction
+    const int ri = lane / HG;             // logical page (in the batch) of that score
+    constexpr int LPB = LPG < R ? LPG : R;  // logical pages of one physical page in a batch
+    constexpr int PPB = R / LPB;            // physical pages in a batch
 
     int32_t a = t_begin;
     int32_t s = locate(t_begin);
@@ -302,160 +366,171 @@ page_select_kernel(const __grid_constant__ SelParams p) {
         const int32_t pe = min(sst + slen, t_end);
         const int32_t b = s / p.Hkv, h = s - b * p.Hkv;
         const int32_t Lb = item_len[b];
-        // the lane's query values, widened exactly, split by sign
+        // query values of the lane's channels: positive part (k_max lanes) or negative part
+        // (k_min lanes), as fp32 pairs {even channel, odd channel}
+        uint64_t qv[HG][NPR];
 #pragma unroll
         for (int j = 0; j < HG; ++j) {
-            const bool okj = j < p.g;
-            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-                p.q + ((int64_t)b * p.Hq + h * p.g + (okj ? j : 0)) * D + c * CPL);
+            Vec w{};
+            if (j < p.g)
+                w = *reinterpret_cast<const Vec*>(p.q + ((int64_t)b * p.Hq + h * p.g + j) * D + c0);
+            const uint32_t* ww = reinterpret_cast<const uint32_t*>(&w);
 #pragma unroll
-            for (int i = 0; i < NPAIR; ++i) {
-                const uint32_t w = okj ? __ldg(qrow + i) : 0u;
-                const float q0 = bf16_lo(w), q1 = bf16_hi(w);
-                qp2[j][i] = pack_f32x2(q0 >= 0.f ? q0 : 0.f, q1 >= 0.f ? q1 : 0.f);
-                qn2[j][i] = pack_f32x2(q0 >= 0.f ? 0.f : q0, q1 >= 0.f ? 0.f : q1);
+            for (int m = 0; m < NPR; ++m) {
+                const float q0 = bf16_lo(ww[m]), q1 = bf16_hi(ww[m]);
+                qv[j][m] = half == 0 ? pack_f32x2(q0 >= 0.f ? q0 : 0.f, q1 >= 0.f ? q1 : 0.f)
+                                     : pack_f32x2(q0 >= 0.f ? 0.f : q0, q1 >= 0.f ? 0.f : q1);
             }
         }
         for (int i = lane; i < L.wn; i += 32) wbuf[i] = 0ull;
-        __syncwarp();
         int cnt_c = 0;
         uint64_t thresh = 0ull;
         const int32_t* btrow = p.block_table + (int64_t)b * p.max_pages;
-        // ---- blocks of pages: stage the block-table entries, then score ------------
-        for (int32_t pb = a; pb < pe; pb += kSelBlockPages) {
-            const int32_t nblk = min(kSelBlockPages, pe - pb);
-            const int32_t pr0 = pb - sst;  // request-relative index of the block's first page
-            for (int i = tid; i < nblk; i += NT) bt_blk[i] = __ldg(btrow + pr0 + i);
+        const int32_t pr0 = a - sst;  // first page of the piece (request-relative)
+        for (int32_t cb = 0; cb < pe - a; cb += kSelBT) {
+            const int32_t nc = min(kSelBT, pe - a - cb);  // pages of this block
+            const int32_t pg0 = pr0 + cb;                 // request-relative page of bt_s[0]
+            for (int i = tid; i < nc; i += NT) bt_s[i] = btrow[pg0 + i];
             csync();
-            const int nunits = (nblk + up - 1) / up;
-            const int ng = ((nunits - warp + kSelWarps - 1) / kSelWarps) * ngu;  // my groups
-            // group k of this warp -> unit warp + 8*(k / ngu), part k % ngu
-            auto row_of = [&](int k, int& pib, int& lp, bool& valid, int32_t& phys) {
-                const int u = warp + kSelWarps * (k / ngu);
-                const int r = u * unit_rows + (k % ngu) * RPW + rr;  // row in the block
-                pib = r / LPG;
-                lp = r - pib * LPG;
-                valid = k < ng && pib < nblk && (pr0 + pib) * p.P + lp * 16 < Lb;
-                phys = valid ? bt_blk[pib] : -1;
-                if (valid && (phys < 0 || phys >= p.num_pages)) {
-                    set_err(p.dev_err, phys < 0 ? DATTN_DEVERR_UNMAPPED_PAGE
-                                                : DATTN_DEVERR_PAGE_OOB);
-                    valid = false;
-                }
-            };
-            auto issue = [&](int k, uint4 (&buf)[2 * NLD]) {
-                int pib, lp;
-                bool valid;
-                int32_t phys;
-                row_of(k, pib, lp, valid, phys);
-                if (valid) {
-                    const uint16_t* row = p.stats +
-                        (((int64_t)phys * p.Hkv + h) * LPG + lp) * (2 * D) + c * CPL;
+            const int32_t nunits = (nc + PPU - 1) / PPU;
+            const int32_t nbat = warp < nunits ? ((nunits - 1 - warp) / kSelWarps + 1) * NB : 0;
+            // Batch k of the warp: unit warp + 8 (k / NB), sub-batch k % NB. Its R logical
+            // pages are PPB physical pages (block-relative first page pc_of(k)) of LPB logical
+            // pages each, starting at logical page lp_of(k).
+            auto pc_of = [&](int32_t k) { return (warp + kSelWarps * (k / NB)) * PPU; };
+            auto lp_of = [&](int32_t k) { return (k % NB) * R; };
+            // first statistics row of each physical page of batch k (rows of
+            // [num_pages][Hkv][LPG], 2D elements each) and the mask of rows that hold tokens
+            auto plan = [&](int32_t k, uint32_t (&rowi)[PPB]) -> uint32_t {
+                uint32_t m = 0u;
+                const int32_t pc0 = pc_of(k), lp0 = lp_of(k);
 #pragma unroll
-                    for (int i = 0; i < NLD; ++i) {
-                        buf[i] = ldg_stream(row + i * 8, pol);
-                        buf[NLD + i] = ldg_stream(row + D + i * 8, pol);
+                for (int t = 0; t < PPB; ++t) {
+                    const int32_t pc = pc0 + t;
+                    int32_t nv = 0;  // logical pages of this batch's part of the page with tokens
+                    rowi[t] = 0u;
+                    if (pc < nc) {
+                        const int32_t rem = Lb - (pg0 + pc) * p.P - lp0 * 16;
+                        nv = min(max((rem + 15) >> 4, 0), LPB);
+                        const int32_t phys = bt_s[pc];
+                        if (nv > 0 && (phys < 0 || phys >= p.num_pages)) {
+                            if (lane == 0 && lp0 == 0)
+                                set_err(p.dev_err, phys < 0 ? DATTN_DEVERR_UNMAPPED_PAGE
+                                                            : DATTN_DEVERR_PAGE_OOB);
+                            nv = 0;
+                        }
+                        if (nv > 0) rowi[t] = ((uint32_t)phys * p.Hkv + h) * LPG + lp0;
                     }
+                    m |= ((1u << nv) - 1u) << (t * LPB);
                 }
+                return m;
             };
-            float run = -__int_as_float(0x7f800000);  // running page max across a unit's groups
-            auto process = [&](int k, const uint4 (&buf)[2 * NLD]) {
-                if (k >= ng) return;  // warp-uniform
-                int pib, lp;
-                bool valid;
-                int32_t phys;
-                row_of(k, pib, lp, valid, phys);
-                float best = -__int_as_float(0x7f800000);
-                {
-                    uint64_t acc[HG];
+            auto load_row = [&](Vec& dst, const uint32_t (&rowi)[PPB], int i) {
+                ld_chunk(dst, stats_lane + (uint64_t)(rowi[i / LPB] + (i % LPB)) * (2 * D), pol);
+            };
+            Vec ring[R];
 #pragma unroll
-                    for (int j = 0; j < HG; ++j) acc[j] = 0ull;
-                    const uint32_t* xw = reinterpret_cast<const uint32_t*>(&buf[0]);
-                    const uint32_t* nw = reinterpret_cast<const uint32_t*>(&buf[NLD]);
+            for (int i = 0; i < R; ++i) ring[i] = Vec{};
+            uint32_t nmask = 0u;
+            if (nbat > 0) {
+                uint32_t rowi[PPB];
+                nmask = plan(0, rowi);
 #pragma unroll
-                    for (int i = 0; i < NPAIR; ++i) {
-                        const uint64_t kx2 = pack_f32x2(bf16_lo(xw[i]), bf16_hi(xw[i]));
-                        const uint64_t kn2 = pack_f32x2(bf16_lo(nw[i]), bf16_hi(nw[i]));
+                for (int i = 0; i < R; ++i)
+                    if ((nmask >> i) & 1u) load_row(ring[i], rowi, i);
+            }
+            float pmax = kNInf;  // running physical-page max when a page spans batches
+            for (int32_t k = 0; k < nbat; ++k) {
+                const uint32_t cmask = nmask;
+                uint32_t rowi[PPB];
+                nmask = k + 1 < nbat ? plan(k + 1, rowi) : 0u;
+                // Partials of rows i and i + R/2 are made together so that the first
+                // butterfly level (offset 16, which pairs exactly those two rows) can run at
+                // once and only 16 values stay live. Transposed butterfly: at offset o the
+                // lane keeps the half of its values selected by lane bit o and adds the
+                // partner's copy of that half.
+                float x[16];
+                const bool up16 = (lane & 16) != 0;
+#pragma unroll
+                for (int ip = 0; ip < R / 2; ++ip) {
+                    float y[2][HG];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int i = ip + u * (R / 2);
+                        uint64_t kp[NPR];
+                        unpack_bf16x8(ring[i], kp);
+                        if ((nmask >> i) & 1u) load_row(ring[i], rowi, i);
 #pragma unroll
                         for (int j = 0; j < HG; ++j) {
-                            fma_f32x2(acc[j], qp2[j][i], kx2);
-                            fma_f32x2(acc[j], qn2[j][i], kn2);
+                            uint64_t acc = 0ull;  // {even, odd}, both +0
+#pragma unroll
+                            for (int m = 0; m < NPR; ++m) fma_f32x2(acc, qv[j][m], kp[m]);
+                            float ev, od;
+                            unpack_f32x2(acc, ev, od);
+                            y[u][j] = ev + od;
                         }
                     }
 #pragma unroll
                     for (int j = 0; j < HG; ++j) {
-                        float ev, od;
-                        unpack_f32x2(acc[j], ev, od);
-                        float t = ev + od;
-#pragma unroll
-                        for (int off = 1; off < LPR; off <<= 1)
-                            t = t + __shfl_xor_sync(0xffffffffu, t, off);
-                        if (j < p.g) best = fmaxf(best, t);
+                        const float send = up16 ? y[0][j] : y[1][j];
+                        const float keep = up16 ? y[1][j] : y[0][j];
+                        x[ip * HG + j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
                     }
                 }
-                if (!valid) best = -__int_as_float(0x7f800000);
-                // page maximum over its logical pages (rows)
-                if (LPG <= RPW) {
-                    for (int off = LPR; off < LPR * LPG; off <<= 1)
-                        best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, off));
-                } else {
-                    for (int off = LPR; off < 32; off <<= 1)
-                        best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, off));
-                    run = fmaxf(run, best);
-                    best = run;
-                    if ((k % ngu) != ngu - 1) return;  // the page continues in the next group
-                    run = -__int_as_float(0x7f800000);
+#pragma unroll
+                for (int lv = 1; lv < 5; ++lv) {
+                    const int o = 16 >> lv, n = 16 >> lv;
+                    const bool up = (lane & o) != 0;
+#pragma unroll
+                    for (int t = 0; t < n; ++t) {
+                        const float send = up ? x[t] : x[t + n];
+                        const float keep = up ? x[t + n] : x[t];
+                        x[t] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                    }
                 }
-                // one lane per page proposes the page's key
-                const int u = warp + kSelWarps * (k / ngu);
-                const int first_row = (k % ngu) * RPW + rr;  // row within the unit
-                const int pib0 = (u * unit_rows + first_row) / LPG;
-                const bool leader = c == 0 && (first_row % LPG == 0 || LPG > RPW) &&
-                                    (LPG <= RPW || rr == 0) && pib0 < nblk;
+                // lane holds the score of logical page ri, head hj
+                float sc = (hj < p.g && ((cmask >> ri) & 1u)) ? x[0] : kNInf;
+#pragma unroll
+                for (int o = 1; o < HG; o <<= 1)
+                    sc = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, o));
+#pragma unroll
+                for (int o = HG; o < HG * LPB; o <<= 1)
+                    sc = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, o));
                 uint64_t key = 0ull;
-                if (leader && best != -__int_as_float(0x7f800000)) key = make_key(best, pr0 + pib0);
+                if constexpr (NB == 1) {
+                    const int32_t pc = pc_of(k) + lane / (HG * LPB);
+                    if (lane % (HG * LPB) == 0 && sc != kNInf) key = make_key(sc, pg0 + pc);
+                } else {
+                    pmax = fmaxf(pmax, sc);
+                    if (k % NB == NB - 1) {
+                        if (lane == 0 && pmax != kNInf) key = make_key(pmax, pg0 + pc_of(k));
+                        pmax = kNInf;
+                    }
+                }
                 const bool take = key > thresh;
                 const uint32_t bal = __ballot_sync(0xffffffffu, take);
-                if (take) wbuf[K + cnt_c + __popc(bal & ((1u << lane) - 1u))] = key;
-                cnt_c += __popc(bal);
-                __syncwarp();
-                if (cnt_c > capw - 32) {
-                    warp_fold(cnt_c);
-                    cnt_c = 0;
-                    thresh = wbuf[K - 1];
+                if (bal) {
+                    if (take) wbuf[Kp + cnt_c + __popc(bal & ((1u << lane) - 1u))] = key;
+                    cnt_c += __popc(bal);
+                    __syncwarp();
+                    if (cnt_c > capw - 32) {
+                        warp_fold(cnt_c);
+                        cnt_c = 0;
+                        thresh = wbuf[K - 1];
+                    }
                 }
-            };
-            // three groups in flight per warp
-            uint4 b0[2 * NLD], b1[2 * NLD], b2[2 * NLD];
-            issue(0, b0);
-            issue(1, b1);
-            issue(2, b2);
-            for (int k = 0; k < ng; k += 3) {
-                process(k, b0);
-                issue(k + 3, b0);
-                process(k + 1, b1);
-                issue(k + 4, b1);
-                process(k + 2, b2);
-                issue(k + 5, b2);
             }
-            csync();  // bt_blk is rewritten by the next block
+            csync();  // bt_s is restaged for the next block of pages
         }
         if (cnt_c > 0) warp_fold(cnt_c);
         csync();
-        // merge the warps' lists of this piece
-        for (int i = tid; i < L.sn; i += NT) {
-            const int w = i / K, r = i - w * K;
-            sortbuf[i] = w < kSelWarps ? reinterpret_cast<uint64_t*>(base + L.wbuf)[w * L.wn + r]
-                                       : 0ull;
-        }
-        csync();
-        bitonic_desc(sortbuf, L.sn, tid, NT, csync);
+        merge_warps();
         const bool whole = (a == sst) && (pe == sst + slen);
         if (whole) {
             finalize(s);
         } else {
             uint64_t* my = p.slots + (int64_t)(cta + s) * K;
-            for (int r = tid; r < K; r += NT) my[r] = sortbuf[r];
+            for (int r = tid; r < K; r += NT) my[r] = list_of(0)[r];
             csync();
             const int32_t c_first = split_owner(sst, W, Gw);
             const int32_t c_last = split_owner(sst + slen - 1, W, Gw);
@@ -469,22 +544,19 @@ page_select_kernel(const __grid_constant__ SelParams p) {
             csync();
             if (*last_flag) {
                 __threadfence();
-                // fold the pieces in groups: sortbuf = [top K | up to (sn - K) new keys]
-                for (int i = tid; i < L.sn; i += NT) sortbuf[i] = 0ull;
-                csync();
-                const int per_fold = (L.sn - K) / K;
-                for (int32_t q0 = 0; q0 < npieces; q0 += per_fold) {
-                    const int32_t nq = min(per_fold, npieces - q0);
-                    for (int i = tid; i < L.sn - K; i += NT) {
-                        const int32_t qq = q0 + i / K, r = i % K;
-                        sortbuf[K + i] = (i < nq * K)
-                            ? __ldcg(reinterpret_cast<const unsigned long long*>(
-                                  p.slots + (int64_t)(c_first + qq + s) * K + r))
-                            : 0ull;
-                    }
-                    csync();
-                    bitonic_desc(sortbuf, L.sn, tid, NT, csync);
+                // warp w folds pieces w, w + 8, ... into its running list, then the warps'
+                // lists are merged
+                for (int i = lane; i < Kp; i += 32) wbuf[i] = 0ull;
+                uint64_t* scratch = wbuf + Kp;
+                for (int32_t qq = warp; qq < npieces; qq += kSelWarps) {
+                    const unsigned long long* src = reinterpret_cast<const unsigned long long*>(
+                        p.slots + (int64_t)(c_first + qq + s) * K);
+                    for (int i = lane; i < Kp; i += 32) scratch[i] = i < K ? __ldcg(src + i) : 0ull;
+                    __syncwarp();
+                    warp_merge_desc(wbuf, scratch, Kp, lane);
                 }
+                csync();
+                merge_warps();
                 finalize(s);
             }
         }
@@ -493,27 +565,49 @@ page_select_kernel(const __grid_constant__ SelParams p) {
     }
 }
 
-template <int D, int CPL, int HG>
+template <int D, int HG, int LPG>
 int sel_prepare(uint32_t smem) {
     static int max_set = 0;
     if ((int)smem > max_set) {
-        if (cudaFuncSetAttribute(page_select_kernel<D, CPL, HG>,
+        if (cudaFuncSetAttribute(page_select_kernel<D, HG, LPG>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return -1;
         max_set = (int)smem;
     }
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, page_select_kernel<D, CPL, HG>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, page_select_kernel<D, HG, LPG>,
                                                       kSelThreads, smem) != cudaSuccess)
         return 1;
     return n < 1 ? 1 : n;
 }
 
-template <int D, int CPL, int HG>
-cudaError_t sel_launch(int32_t G, uint32_t smem, cudaStream_t stream, const SelParams& p) {
-    return launch_pdl(page_select_kernel<D, CPL, HG>, dim3(G), dim3(kSelThreads), smem, stream,
+template <int D, int HG, int LPG>
+cudaError_t sel_go(int32_t G_req, int64_t units_bound, uint32_t smem, cudaStream_t stream,
+                   SelParams& p, void* ws, size_t ws_bytes, bool& ws_ok) {
+    const int occ = sel_prepare<D, HG, LPG>(smem);
+    if (occ < 0) return cudaErrorInvalidValue;
+    const int32_t G = choose_splits(units_bound * 4, G_req, occ);
+    const size_t counters = ((size_t)p.nseg * 4 + 255) & ~(size_t)255;
+    ws_ok = !(ws == nullptr || ws_bytes < select_workspace_bytes(p.nseg, p.top_k, G) ||
+              (reinterpret_cast<uintptr_t>(ws) & 255));
+    if (!ws_ok) return cudaSuccess;
+    p.counters = static_cast<int32_t*>(ws);
+    p.slots = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + counters);
+    return launch_pdl(page_select_kernel<D, HG, LPG>, dim3(G), dim3(kSelThreads), smem, stream,
                       p);
+}
+
+template <int D, int HG>
+cudaError_t sel_go_lpg(int lpg, int32_t G_req, int64_t units_bound, uint32_t smem,
+                       cudaStream_t stream, SelParams& p, void* ws, size_t ws_bytes, bool& ok) {
+    switch (lpg) {
+        case 1: return sel_go<D, HG, 1>(G_req, units_bound, smem, stream, p, ws, ws_bytes, ok);
+        case 2: return sel_go<D, HG, 2>(G_req, units_bound, smem, stream, p, ws, ws_bytes, ok);
+        case 4: return sel_go<D, HG, 4>(G_req, units_bound, smem, stream, p, ws, ws_bytes, ok);
+        case 8: return sel_go<D, HG, 8>(G_req, units_bound, smem, stream, p, ws, ws_bytes, ok);
+        default: return sel_go<D, HG, 16>(G_req, units_bound, smem, stream, p, ws, ws_bytes, ok);
+    }
 }
 
 }  // namespace
@@ -548,27 +642,24 @@ dattn_status_t launch_page_select(const dattn_kv_layout& Lay, const uint16_t* st
     p.nseg = B * p.Hkv;
     p.dev_err = dev_err;
     const int D = Lay.head_dim;
-    const bool wide = p.g > 4;  // 8 channels x 8 heads per lane instead of 16 x 4
+    const int lpg = p.P / 16;
+    if (lpg & (lpg - 1)) return DATTN_ERR_UNSUPPORTED;  // P / 16 must be a power of two
     const SelSmem L = sel_smem_layout(B, p.Hkv, top_k);
     if (L.total > 227u * 1024u) return DATTN_ERR_UNSUPPORTED;
-    int occ;
-    if (D == 64) occ = wide ? sel_prepare<64, 8, 8>(L.total) : sel_prepare<64, 16, 4>(L.total);
-    else occ = wide ? sel_prepare<128, 8, 8>(L.total) : sel_prepare<128, 16, 4>(L.total);
-    if (occ < 0) return DATTN_ERR_CUDA;
-    const int32_t G = choose_splits(units_bound * 4, num_splits, occ);
-    const size_t counters = ((size_t)p.nseg * 4 + 255) & ~(size_t)255;
-    if (ws == nullptr || ws_bytes < select_workspace_bytes(p.nseg, top_k, G) ||
-        (reinterpret_cast<uintptr_t>(ws) & 255))
-        return DATTN_ERR_WORKSPACE;
-    p.counters = static_cast<int32_t*>(ws);
-    p.slots = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + counters);
+    bool ws_ok = true;
     cudaError_t e;
+    const bool wide = p.g > 4;  // 8 query heads per KV head instead of 4
     if (D == 64)
-        e = wide ? sel_launch<64, 8, 8>(G, L.total, stream, p)
-                 : sel_launch<64, 16, 4>(G, L.total, stream, p);
+        e = wide ? sel_go_lpg<64, 8>(lpg, num_splits, units_bound, L.total, stream, p, ws,
+                                     ws_bytes, ws_ok)
+                 : sel_go_lpg<64, 4>(lpg, num_splits, units_bound, L.total, stream, p, ws,
+                                     ws_bytes, ws_ok);
     else
-        e = wide ? sel_launch<128, 8, 8>(G, L.total, stream, p)
-                 : sel_launch<128, 16, 4>(G, L.total, stream, p);
+        e = wide ? sel_go_lpg<128, 8>(lpg, num_splits, units_bound, L.total, stream, p, ws,
+                                      ws_bytes, ws_ok)
+                 : sel_go_lpg<128, 4>(lpg, num_splits, units_bound, L.total, stream, p, ws,
+                                      ws_bytes, ws_ok);
+    if (!ws_ok) return DATTN_ERR_WORKSPACE;
     return e == cudaSuccess ? DATTN_OK : DATTN_ERR_CUDA;
 }
 

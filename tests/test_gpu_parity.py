@@ -298,6 +298,10 @@ def _oracle_selection(case, cache, q):
     (16, 64, [3000, 1, 777], 32, 0),
     (64, 64, [64 * 40], 64, 3),  # top_k covers every page
     (64, 128, [64 * 50 + 3, 64 * 7], 8, 4000),  # more CTAs than pages
+    (256, 128, [256 * 30 + 100, 256 * 3], 5, 0),  # 16 logical pages per page, odd top_k
+    (32, 128, [32 * 500 + 7], 100, 5),  # 2 logical pages per page, top_k not a power of two
+    (64, 128, [64 * 600, 64 * 300 + 1], 256, 0),  # the largest top_k
+    (128, 64, [128 * 40 + 77, 129], 1, 2),  # top-1
 ])
 def test_page_select_bit_exact(P, d, lens, top_k, splits):
     _lib()
