@@ -7,7 +7,8 @@ One step is one decode layer-step of the whole batch through the library's C ABI
 The metric is achieved HBM bandwidth in GB/s: the algorithmic bytes of the step (valid K/V
 read, statistics scanned, new tokens written, queries, outputs, block table) divided by
 the device time of the step. The time per layer-step and the fraction of the 8 TB/s
-roofline are reported beside it. L2 is flushed before every timed step.
+roofline are reported beside it. L2 is flushed before every timed step whose K/V is under
+four times the L2; larger steps evict it themselves and run back to back.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl dattn|reference]
 
@@ -210,6 +211,25 @@ def traffic_record(config: str):
 
 # ------------------------------------------------------------------------------ GPU arm
 
+class L2Flush:
+    """Evicts every line of L2 without leaving dirty ones behind: a 512 MiB write pushes
+    everything out, then a 512 MiB read replaces the written (dirty) lines with clean ones.
+    Their write-back therefore lands before the timed region instead of inside it."""
+    TEXT = "512 MiB write, then 512 MiB read, so L2 holds only clean unrelated lines"
+
+    def __init__(self, dev):
+        import torch
+        n = 512 * 1024 * 1024 // 4
+        self.w = torch.empty(n, dtype=torch.float32, device=dev)
+        self.r = torch.ones(n, dtype=torch.float32, device=dev)
+        self.acc = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.acc)
+
+
 def run_dattn(args, rank: int, world: int):
     import torch
     import torch.distributed as dist
@@ -242,11 +262,11 @@ def run_dattn(args, rank: int, world: int):
     del k_all, v_all
     # L2 hygiene: a step whose K/V working set exceeds 4x the L2 evicts everything the
     # previous step left there, so it is timed back to back; smaller steps are preceded by
-    # a 512 MiB write that flushes L2.
+    # an L2 flush (see L2Flush).
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     sb0 = step_bytes(case, list(cache.lens), sparse)
     do_flush = sb0["decode"] < 4 * l2 or args.flush
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     torch.cuda.synchronize()
 
     def one_step(s, ev=None):
@@ -279,7 +299,7 @@ def run_dattn(args, rank: int, world: int):
     for i in range(args.steps):
         s = args.warmup + i
         if do_flush:
-            flush.zero_()  # L2 flush, outside the timed region
+            flush()  # outside the timed region
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         d0 = torch.cuda.Event(enable_timing=True)
@@ -312,7 +332,7 @@ def run_dattn(args, rank: int, world: int):
     else:
         ms_max, bytes_all = ms_total, float(bytes_total)
     res = {
-        "l2_policy": (f"flushed (512 MiB write) before every timed step" if do_flush else
+        "l2_policy": (f"flushed before every timed step ({L2Flush.TEXT})" if do_flush else
                       f"inputs larger than L2: {sb0['decode'] / 1e9:.2f} GB of K/V per step "
                       f"vs {l2 / 1e6:.0f} MB L2, timed back to back without a flush"),
         "ms_total": ms_max, "bytes_all": bytes_all, "step_ms": step_t, "dec_ms": dec_t,
@@ -351,7 +371,7 @@ def run_e2e(args, case, cache, ws, spc, sel, flush, dev):
         e_all0.record(stream)
     for i in range(steps):
         if flush is not None:
-            flush.zero_()
+            flush()
             e0 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
         dq.copy_(hq[i], non_blocking=True)

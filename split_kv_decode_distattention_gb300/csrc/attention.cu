@@ -53,7 +53,6 @@ struct Smem {
     __device__ float* ws_e() const { return reinterpret_cast<float*>(base + L.ws_e); }
     __device__ float* ws_o() const { return reinterpret_cast<float*>(base + L.ws_o); }
     __device__ float* merge_w() const { return reinterpret_cast<float*>(base + L.merge_w); }
-    __device__ float* merge_e() const { return reinterpret_cast<float*>(base + L.merge_e); }
     __device__ int32_t* kind_before() const {
         return reinterpret_cast<int32_t*>(base + L.kind_before);
     }
@@ -639,18 +638,22 @@ attention_kernel(const __grid_constant__ AttnParams p,
         const int32_t c_last = split_owner(sst + sreal - 1, W, Gw);
         const bool whole = c_first == c_last;
         const int ctid = tid;  // 0..127
-        float* wm = sm.ws_m();
-        float* we = sm.ws_e();
-        float* wo = sm.ws_o();
+        constexpr int kCT = kConsumerWarps * 32;
+        const float* wm = sm.ws_m();
+        const float* we = sm.ws_e();
+        const float* wo = sm.ws_o();
         const int gD = p.g * D;
-        const int32_t slot_stride = p.g * (D + 2);
+        const int32_t slot_stride = slot_floats(p.g, D);
         float* my_slot = whole ? nullptr : p.slots + (int64_t)(cta + s) * slot_stride;
-        for (int idx = ctid; idx < gD; idx += kConsumerWarps * 32) {
-            const int j = idx / D, d = idx - j * D;
+        // a thread combines float4 columns of the g x D state; D is a multiple of 4, so a
+        // column never spans two heads
+        for (int c4 = ctid; c4 < gD / 4; c4 += kCT) {
+            const int j = (4 * c4) / D, d = 4 * c4 - j * D;
             float mc = kNegInf;
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) mc = fmaxf(mc, wm[w * kMaxGroup + j]);
-            float ec = 0.f, ma = 0.f;
+            float ec = 0.f;
+            float4 ma = make_float4(0.f, 0.f, 0.f, 0.f);
             if (mc != kNegInf) {
 #pragma unroll
                 for (int w = 0; w < kConsumerWarps; ++w) {
@@ -658,13 +661,20 @@ attention_kernel(const __grid_constant__ AttnParams p,
                     if (mw == kNegInf) continue;
                     const float sc = exp2f(mw - mc);
                     ec += we[w * kMaxGroup + j] * sc;
-                    ma += wo[w * gD + j * D + d] * sc;
+                    const float4 v = *reinterpret_cast<const float4*>(wo + w * gD + 4 * c4);
+                    ma.x += v.x * sc;
+                    ma.y += v.y * sc;
+                    ma.z += v.z * sc;
+                    ma.w += v.w * sc;
                 }
             }
             if (whole) {
-                write_final(p, s, j, d, D, mc, ec, ma);
+                write_final(p, s, j, d, D, mc, ec, ma.x);
+                write_final(p, s, j, d + 1, D, mc, ec, ma.y);
+                write_final(p, s, j, d + 2, D, mc, ec, ma.z);
+                write_final(p, s, j, d + 3, D, mc, ec, ma.w);
             } else {
-                my_slot[j * D + d] = ma;
+                *reinterpret_cast<float4*>(my_slot + 4 * c4) = ma;
                 if (d == 0) {
                     my_slot[gD + j] = mc;
                     my_slot[gD + p.g + j] = ec;
@@ -673,7 +683,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
         }
         if (!whole) {
             // hand the piece over: the CTA that delivers the last piece merges them all
-            named_bar_sync(1, kConsumerWarps * 32);
+            named_bar_sync(1, kCT);
             const int32_t npieces = c_last - c_first + 1;
             if (ctid == 0) {
                 __threadfence();
@@ -681,75 +691,102 @@ attention_kernel(const __grid_constant__ AttnParams p,
                 *sm.last_flag() = (prev == npieces - 1) ? 1 : 0;
                 if (prev == npieces - 1) p.counters[s] = 0;  // ready for the next launch
             }
-            named_bar_sync(1, kConsumerWarps * 32);
+            named_bar_sync(1, kCT);
             if (*sm.last_flag()) {
-                // Merge all pieces of the segment. Per pass over up to kMergeChunk pieces:
-                // load their (m, e) at once, let one thread per head fold them into the
-                // running max and sum and turn each m into a weight, then accumulate the
-                // weighted MA with independent loads.
+                // Merge all pieces of the segment, up to kMergeChunk per pass. Warp w turns
+                // the (m, e) of heads w, w + 4 into weights (lanes over pieces, warp-shuffle
+                // max and sum) and keeps a running max and sum across passes. Then every
+                // thread accumulates its float4 columns of MA with independent loads.
                 __threadfence();
                 const float* first = p.slots + (int64_t)(c_first + s) * slot_stride;
-                float* mw = sm.merge_w();
-                float* me = sm.merge_e();
-                float* mrun = sm.ws_m();              // [g] running max
-                float* erun = sm.ws_e();              // [g] running sum
-                float* alpha = sm.ws_m() + kMaxGroup; // [g] rescale of earlier passes
-                constexpr int kOwn = (kMaxGroup * D + kConsumerWarps * 32 - 1) /
-                                     (kConsumerWarps * 32);
-                float acc[kOwn];
+                float* mw = sm.merge_w();              // [kMergeChunk][g] weights of a pass
+                float* mrun = sm.ws_m();               // [g] running max
+                float* erun = sm.ws_e();               // [g] running sum
+                float* alpha = sm.ws_m() + kMaxGroup;  // [g] rescale of earlier passes
+                constexpr int kCols = (kMaxGroup * D / 4 + kCT - 1) / kCT;
+                float4 acc[kCols];
 #pragma unroll
-                for (int k = 0; k < kOwn; ++k) acc[k] = 0.f;
+                for (int k = 0; k < kCols; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (ctid < p.g) {
                     mrun[ctid] = kNegInf;
                     erun[ctid] = 0.f;
                 }
-                named_bar_sync(1, kConsumerWarps * 32);
+                named_bar_sync(1, kCT);
                 for (int32_t q0 = 0; q0 < npieces; q0 += kMergeChunk) {
                     const int nq = min(kMergeChunk, npieces - q0);
-                    for (int i = ctid; i < nq * p.g; i += kConsumerWarps * 32) {
-                        const int q = i / p.g, j = i - q * p.g;
-                        const float* sl = first + (int64_t)(q0 + q) * slot_stride;
-                        mw[i] = __ldcg(sl + gD + j);
-                        me[i] = __ldcg(sl + gD + p.g + j);
-                    }
-                    named_bar_sync(1, kConsumerWarps * 32);
-                    if (ctid < p.g) {
-                        const int j = ctid;
-                        float mx = mrun[j];
-                        for (int q = 0; q < nq; ++q) mx = fmaxf(mx, mw[q * p.g + j]);
-                        const float al = mx == kNegInf ? 0.f : exp2f(mrun[j] - mx);
-                        float e = erun[j] * al;
-                        for (int q = 0; q < nq; ++q) {
-                            const float mq = mw[q * p.g + j];
-                            const float w = mq == kNegInf ? 0.f : exp2f(mq - mx);
-                            e += me[q * p.g + j] * w;
-                            mw[q * p.g + j] = w;
-                        }
-                        mrun[j] = mx;
-                        erun[j] = e;
-                        alpha[j] = al;
-                    }
-                    named_bar_sync(1, kConsumerWarps * 32);
+                    const float* pass = first + (int64_t)q0 * slot_stride;
+                    for (int j = warp; j < p.g; j += kConsumerWarps) {
+                        constexpr int kPer = kMergeChunk / 32;
+                        float mq[kPer], eq[kPer];
 #pragma unroll
-                    for (int k = 0; k < kOwn; ++k) {
-                        const int idx = ctid + k * kConsumerWarps * 32;
-                        if (idx >= gD) break;
-                        const int j = idx / D, d = idx - j * D;
-                        const float* col = first + (int64_t)q0 * slot_stride + j * D + d;
-                        float a = acc[k] * alpha[j];
-#pragma unroll 4
-                        for (int q = 0; q < nq; ++q)
-                            a += mw[q * p.g + j] * __ldcg(col + (int64_t)q * slot_stride);
+                        for (int t = 0; t < kPer; ++t) {
+                            const int q = lane + 32 * t;
+                            mq[t] = q < nq ? __ldcg(pass + (int64_t)q * slot_stride + gD + j)
+                                           : kNegInf;
+                            eq[t] = q < nq ? __ldcg(pass + (int64_t)q * slot_stride + gD + p.g + j)
+                                           : 0.f;
+                        }
+                        const float m_old = mrun[j];
+                        float mx = m_old;
+#pragma unroll
+                        for (int t = 0; t < kPer; ++t) mx = fmaxf(mx, mq[t]);
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1)
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                        float e = 0.f;
+#pragma unroll
+                        for (int t = 0; t < kPer; ++t) {
+                            const int q = lane + 32 * t;
+                            const float w = mq[t] == kNegInf ? 0.f : exp2f(mq[t] - mx);
+                            e += eq[t] * w;
+                            if (q < nq) mw[q * p.g + j] = w;
+                        }
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1)
+                            e += __shfl_xor_sync(0xffffffffu, e, off);
+                        if (lane == 0) {
+                            const float al = mx == kNegInf ? 0.f : exp2f(m_old - mx);
+                            erun[j] = erun[j] * al + e;
+                            mrun[j] = mx;
+                            alpha[j] = al;
+                        }
+                    }
+                    named_bar_sync(1, kCT);
+#pragma unroll
+                    for (int k = 0; k < kCols; ++k) {
+                        const int c4 = ctid + k * kCT;
+                        if (c4 >= gD / 4) break;
+                        const int j = (4 * c4) / D;
+                        const float al = alpha[j];
+                        float4 a = acc[k];
+                        a.x *= al;
+                        a.y *= al;
+                        a.z *= al;
+                        a.w *= al;
+                        const float4* col = reinterpret_cast<const float4*>(pass + 4 * c4);
+                        const int64_t step4 = slot_stride / 4;
+#pragma unroll 16
+                        for (int q = 0; q < nq; ++q) {
+                            const float w = mw[q * p.g + j];
+                            const float4 v = __ldcg(col + q * step4);
+                            a.x += w * v.x;
+                            a.y += w * v.y;
+                            a.z += w * v.z;
+                            a.w += w * v.w;
+                        }
                         acc[k] = a;
                     }
-                    named_bar_sync(1, kConsumerWarps * 32);
+                    named_bar_sync(1, kCT);
                 }
 #pragma unroll
-                for (int k = 0; k < kOwn; ++k) {
-                    const int idx = ctid + k * kConsumerWarps * 32;
-                    if (idx >= gD) break;
-                    const int j = idx / D, d = idx - j * D;
-                    write_final(p, s, j, d, D, mrun[j], erun[j], acc[k]);
+                for (int k = 0; k < kCols; ++k) {
+                    const int c4 = ctid + k * kCT;
+                    if (c4 >= gD / 4) break;
+                    const int j = (4 * c4) / D, d = 4 * c4 - j * D;
+                    write_final(p, s, j, d, D, mrun[j], erun[j], acc[k].x);
+                    write_final(p, s, j, d + 1, D, mrun[j], erun[j], acc[k].y);
+                    write_final(p, s, j, d + 2, D, mrun[j], erun[j], acc[k].z);
+                    write_final(p, s, j, d + 3, D, mrun[j], erun[j], acc[k].w);
                 }
             }
         }
@@ -802,7 +839,7 @@ int occupancy(uint32_t smem) {
 
 size_t attn_workspace_bytes(int32_t nseg, int32_t g, int32_t D, int32_t G) {
     const size_t counters = ((size_t)nseg * 4 + 255) & ~(size_t)255;
-    return counters + (size_t)(G + nseg) * g * (D + 2) * 4;
+    return counters + (size_t)(G + nseg) * slot_floats(g, D) * 4;
 }
 
 template <int D>

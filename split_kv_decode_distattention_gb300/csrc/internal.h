@@ -47,16 +47,22 @@ struct AttnParams {
     float* e_out;
     // workspace
     int32_t* counters;  // [nseg]
-    float* slots;       // [(G + nseg)][g][D + 2]
+    float* slots;       // [(G + nseg)][slot_floats(g, D)]: MA [g][D], m [g], e [g], padding
     int32_t nseg;
     int32_t nitems;     // B for dense / sparse, C for partial
     int32_t* dev_err;
 };
 
+// Floats of one workspace slot (a piece's partial): MA [g][D], then m [g] and e [g],
+// padded to a multiple of four floats so that every slot starts on 16 bytes.
+__host__ __device__ inline int32_t slot_floats(int32_t g, int32_t D) {
+    return g * D + ((2 * g + 3) & ~3);
+}
+
 // Shared-memory layout of the attention engine, identical on host and device.
 struct AttnSmem {
-    uint32_t stage_bytes, stages, bars, meta, flags, ws_m, ws_e, ws_o, merge_w, merge_e,
-        kind_before, kinds, item_start, item_len, scan, total;
+    uint32_t stage_bytes, stages, bars, meta, flags, ws_m, ws_e, ws_o, merge_w, kind_before,
+        kinds, item_start, item_len, scan, total;
 };
 
 __host__ __device__ inline AttnSmem attn_smem_layout(int D, int g, int nitems, int Hkv,
@@ -72,7 +78,6 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int D, int g, int nitems, i
     s.ws_e = o;        o += kConsumerWarps * kMaxGroup * 4u;
     s.ws_o = o;        o += (uint32_t)(kConsumerWarps * g * D) * 4u;
     s.merge_w = o;     o += (uint32_t)(kMergeChunk * g) * 4u;
-    s.merge_e = o;     o += (uint32_t)(kMergeChunk * g) * 4u;
     s.kind_before = o; o += sparse ? (uint32_t)(Hkv + 1) * 3u * 4u : 0u;
     s.kinds = o;       o += sparse ? (uint32_t)Hkv * 4u : 0u;
     o = (o + 15u) & ~15u;

@@ -158,5 +158,8 @@ def test_workspace_size(dattn):
     a = dattn.dattn_workspace_size(8, 32, 8, 128, 0, 100)
     b = dattn.dattn_workspace_size(8, 32, 8, 128, 64, 100)
     assert b >= a
-    # counters (8*8 ints, padded to 256 B) + (G + segments) slots of g*(d+2) floats
-    assert a == 256 + (100 + 64) * 4 * 130 * 4
+    # counters (8*8 ints, padded to 256 B) + (G + segments) slots of g*d + 2g floats,
+    # rounded up to a multiple of 4 floats
+    assert a == 256 + (100 + 64) * (4 * 128 + 8) * 4
+    c = dattn.dattn_workspace_size(8, 24, 8, 128, 0, 100)  # g = 3: 6 -> 8 trailing floats
+    assert c == 256 + (100 + 64) * (3 * 128 + 8) * 4
