@@ -6,11 +6,13 @@
 // k_max / k_min of each 16-token logical page are computed when the KV cache is written,
 // so decoding pays nothing for them.
 //
-// Each CTA owns a window of 64 token positions aligned to logical pages (16 tokens). It
-// copies the K and V rows of its tokens with 16-byte vectors into their (page, head, slot)
-// places, then folds its tokens into the statistics of the logical pages it covers.
-// Because the windows are aligned to logical pages, no two CTAs touch the same logical page,
-// so the statistics need no atomics and come out the same on every run.
+// Each CTA owns a window of 64 token positions aligned to logical pages (16 tokens), and
+// each thread one (KV head, 8-channel chunk) of every token in it: it copies that chunk of
+// the K and V rows with 16-byte vectors into their (page, head, slot) places and folds the
+// same K chunk into the statistics of the logical page, keeping the running k_max / k_min
+// of the open logical page in registers. Because the windows are aligned to logical
+// pages, no two CTAs touch the same logical page, so the statistics need no atomics and
+// come out the same on every run.
 #include "common.cuh"
 #include "internal.h"
 
@@ -18,103 +20,125 @@ namespace dattn {
 
 namespace {
 
-constexpr int kAppendThreads = 128;
+constexpr int kAppendMaxThreads = 512;  // one thread per (KV head, 8-channel chunk)
 constexpr int kAppendWindow = 64;  // token positions per CTA, a multiple of 16
 
-__device__ __forceinline__ float bf(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+__device__ __forceinline__ float bf(uint32_t h) { return __uint_as_float(h << 16); }
+
+// strict comparisons per bf16 channel: on a tie the earlier value stays
+__device__ __forceinline__ void fold8(const uint4& k, uint4& mx, uint4& mn) {
+    const uint32_t kw[4] = {k.x, k.y, k.z, k.w};
+    uint32_t xw[4] = {mx.x, mx.y, mx.z, mx.w};
+    uint32_t nw[4] = {mn.x, mn.y, mn.z, mn.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t a = kw[i] & 0xffffu, z = kw[i] >> 16;
+        uint32_t x0 = xw[i] & 0xffffu, x1 = xw[i] >> 16;
+        uint32_t n0 = nw[i] & 0xffffu, n1 = nw[i] >> 16;
+        if (bf(a) > bf(x0)) x0 = a;
+        if (bf(a) < bf(n0)) n0 = a;
+        if (bf(z) > bf(x1)) x1 = z;
+        if (bf(z) < bf(n1)) n1 = z;
+        xw[i] = x0 | (x1 << 16);
+        nw[i] = n0 | (n1 << 16);
+    }
+    mx = make_uint4(xw[0], xw[1], xw[2], xw[3]);
+    mn = make_uint4(nw[0], nw[1], nw[2], nw[3]);
+}
 
 template <int D>
-__global__ void __launch_bounds__(kAppendThreads)
+__global__ void __launch_bounds__(kAppendMaxThreads)
 kv_append_kernel(dattn_kv_layout L, uint16_t* __restrict__ k_pool, uint16_t* __restrict__ v_pool,
                  uint16_t* __restrict__ stats, const uint16_t* __restrict__ k_new,
                  const uint16_t* __restrict__ v_new, int32_t T, int32_t* seq_lens,
                  int32_t update_in_place, int32_t* dev_err) {
+    constexpr int VPR = D / 8;  // 8-channel chunks per (token, head) row
     const int32_t b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
     const int32_t Hkv = L.num_kv_heads, P = L.page_size;
     grid_dependency_wait();  // the previous kernel may still read the pool or the lengths
     grid_launch_dependents();
+    // In a single-window launch the CTA takes the new tokens 0 .. T-1 whatever seq_lens
+    // holds, so the first token's K/V chunk is loaded while the length is still in flight.
+    const bool single = update_in_place != 0;
+    const int64_t tstride = (int64_t)Hkv * D;  // elements between consecutive new tokens
+    const uint16_t* kb = k_new + (int64_t)b * T * tstride;
+    const uint16_t* vb = v_new + (int64_t)b * T * tstride;
+    uint4 k0 = make_uint4(0u, 0u, 0u, 0u), v0 = k0;
+    if (single && tid < Hkv * VPR) {
+        k0 = *reinterpret_cast<const uint4*>(kb + (int64_t)tid * 8);
+        v0 = *reinterpret_cast<const uint4*>(vb + (int64_t)tid * 8);
+    }
     const int32_t pos0 = seq_lens[b];
     if (pos0 < 0) {
         if (tid == 0) set_err(dev_err, DATTN_DEVERR_LEN_OOB);
         return;
     }
     const int32_t base = pos0 - (pos0 & 15);
-    const int32_t p_lo = max(pos0, base + c * kAppendWindow);
-    const int32_t p_hi = min(pos0 + T, base + (c + 1) * kAppendWindow);
+    const int32_t i_lo = max(pos0, base + c * kAppendWindow) - pos0;  // new-token range
+    const int32_t i_hi = min(pos0 + T, base + (c + 1) * kAppendWindow) - pos0;
     const int32_t* bt = L.block_table + (int64_t)b * L.max_pages_per_req;
+    const int32_t lpg = P >> 4;
 
-    if (p_lo < p_hi) {
-        // ---- K and V rows: 16-byte vectors ---------------------------------------------
-        constexpr int VPR = D / 8;  // vectors per (token, head) row
-        const int32_t nvec = (p_hi - p_lo) * Hkv * VPR;
-        for (int32_t v = tid; v < nvec; v += kAppendThreads) {
-            const int32_t t = p_lo + v / (Hkv * VPR);
-            const int32_t rem = v - (t - p_lo) * (Hkv * VPR);
-            const int32_t h = rem / VPR, dv = rem - h * VPR;
+    for (int32_t item = tid; item < Hkv * VPR && i_lo < i_hi; item += blockDim.x) {
+        const int32_t h = item / VPR, c8 = item - h * VPR;
+        int32_t cur_lp = -1, page = -1;
+        int32_t cur_lq = -1;
+        uint16_t* st = nullptr;  // statistics row of the open logical page (k_max; k_min + D)
+        uint4 mx = make_uint4(0u, 0u, 0u, 0u), mn = mx;
+        for (int32_t i = i_lo; i < i_hi; ++i) {
+            const int32_t t = pos0 + i;
+            uint4 kv, vv;
+            if (single && i == 0 && item == tid) {
+                kv = k0;
+                vv = v0;
+            } else {
+                kv = *reinterpret_cast<const uint4*>(kb + i * tstride + (int64_t)item * 8);
+                vv = *reinterpret_cast<const uint4*>(vb + i * tstride + (int64_t)item * 8);
+            }
             const int32_t lp = t / P;
-            if (lp >= L.max_pages_per_req) {
-                set_err(dev_err, DATTN_DEVERR_LEN_OOB);
-                continue;
-            }
-            const int32_t page = bt[lp];
-            if (page < 0) {
-                set_err(dev_err, DATTN_DEVERR_UNMAPPED_PAGE);
-                continue;
-            }
-            if (page >= L.num_pages) {
-                set_err(dev_err, DATTN_DEVERR_PAGE_OOB);
-                continue;
-            }
-            const int64_t src = (((int64_t)b * T + (t - pos0)) * Hkv + h) * D + dv * 8;
-            const int64_t dst = (((int64_t)page * Hkv + h) * P + (t - lp * P)) * D + dv * 8;
-            *reinterpret_cast<uint4*>(k_pool + dst) = *reinterpret_cast<const uint4*>(k_new + src);
-            *reinterpret_cast<uint4*>(v_pool + dst) = *reinterpret_cast<const uint4*>(v_new + src);
-        }
-        // ---- statistics of the logical pages in this window ------------------------------
-        if (stats != nullptr) {
-            const int32_t lq0 = p_lo >> 4, lq1 = (p_hi - 1) >> 4;
-            constexpr int PAIRS = D / 2;
-            const int32_t nwork = (lq1 - lq0 + 1) * Hkv * PAIRS;
-            for (int32_t w = tid; w < nwork; w += kAppendThreads) {
-                const int32_t lq = lq0 + w / (Hkv * PAIRS);
-                const int32_t rem = w - (lq - lq0) * (Hkv * PAIRS);
-                const int32_t h = rem / PAIRS, dp = rem - h * PAIRS;
-                const int32_t first = lq * 16;
-                const int32_t ta = max(first, p_lo), tb = min(first + 16, p_hi);
-                const int32_t lp = first / P;
-                if (lp >= L.max_pages_per_req) continue;  // flagged by the copy above
-                const int32_t page = bt[lp];
-                if (page < 0 || page >= L.num_pages) continue;
-                uint16_t* st = stats + ((((int64_t)page * Hkv + h) * (P / 16) +
-                                         (first - lp * P) / 16) * 2) * D + 2 * dp;
-                const uint16_t* kr = k_new + (((int64_t)b * T + (ta - pos0)) * Hkv + h) * D + 2 * dp;
-                const int64_t tstride = (int64_t)Hkv * D;
-                uint16_t mx0, mx1, mn0, mn1;
-                int32_t t = ta;
-                if (ta == first) {  // this append opens the logical page
-                    const uint32_t k2 = *reinterpret_cast<const uint32_t*>(kr);
-                    mx0 = mn0 = (uint16_t)(k2 & 0xffff);
-                    mx1 = mn1 = (uint16_t)(k2 >> 16);
-                    ++t;
+            if (lp != cur_lp) {
+                cur_lp = lp;
+                page = -1;
+                if (lp >= L.max_pages_per_req) {
+                    set_err(dev_err, DATTN_DEVERR_LEN_OOB);
                 } else {
-                    const uint32_t x2 = *reinterpret_cast<const uint32_t*>(st);
-                    const uint32_t n2 = *reinterpret_cast<const uint32_t*>(st + D);
-                    mx0 = (uint16_t)(x2 & 0xffff); mx1 = (uint16_t)(x2 >> 16);
-                    mn0 = (uint16_t)(n2 & 0xffff); mn1 = (uint16_t)(n2 >> 16);
+                    const int32_t pg = bt[lp];
+                    if (pg < 0) set_err(dev_err, DATTN_DEVERR_UNMAPPED_PAGE);
+                    else if (pg >= L.num_pages) set_err(dev_err, DATTN_DEVERR_PAGE_OOB);
+                    else page = pg;
                 }
-                for (; t < tb; ++t) {
-                    const uint32_t k2 =
-                        *reinterpret_cast<const uint32_t*>(kr + (int64_t)(t - ta) * tstride);
-                    const uint16_t a = (uint16_t)(k2 & 0xffff), z = (uint16_t)(k2 >> 16);
-                    // strict comparisons: on a tie the earlier value stays
-                    if (bf(a) > bf(mx0)) mx0 = a;
-                    if (bf(a) < bf(mn0)) mn0 = a;
-                    if (bf(z) > bf(mx1)) mx1 = z;
-                    if (bf(z) < bf(mn1)) mn1 = z;
-                }
-                *reinterpret_cast<uint32_t*>(st) = (uint32_t)mx0 | ((uint32_t)mx1 << 16);
-                *reinterpret_cast<uint32_t*>(st + D) = (uint32_t)mn0 | ((uint32_t)mn1 << 16);
             }
+            if (page >= 0) {
+                const int64_t dst = (((int64_t)page * Hkv + h) * P + (t - lp * P)) * D + c8 * 8;
+                *reinterpret_cast<uint4*>(k_pool + dst) = kv;
+                *reinterpret_cast<uint4*>(v_pool + dst) = vv;
+            }
+            if (stats == nullptr) continue;
+            const int32_t lq = t >> 4;
+            if (lq != cur_lq) {
+                if (st != nullptr) {
+                    *reinterpret_cast<uint4*>(st) = mx;
+                    *reinterpret_cast<uint4*>(st + D) = mn;
+                }
+                cur_lq = lq;
+                st = page >= 0
+                    ? stats + (((int64_t)page * Hkv + h) * lpg + (t - lp * P) / 16) * 2 * D +
+                          c8 * 8
+                    : nullptr;
+                if ((t & 15) == 0) {  // this append opens the logical page
+                    mx = mn = kv;
+                    continue;
+                }
+                if (st != nullptr) {
+                    mx = *reinterpret_cast<const uint4*>(st);
+                    mn = *reinterpret_cast<const uint4*>(st + D);
+                }
+            }
+            fold8(kv, mx, mn);
+        }
+        if (st != nullptr) {
+            *reinterpret_cast<uint4*>(st) = mx;
+            *reinterpret_cast<uint4*>(st + D) = mn;
         }
     }
     if (update_in_place) {
@@ -142,13 +166,15 @@ dattn_status_t launch_kv_append(const dattn_kv_layout& L, uint16_t* k_pool, uint
     const int32_t nwin = single ? 1 : (T + 15 + kAppendWindow - 1) / kAppendWindow;
     const dim3 grid(nwin, B);
     const int32_t inplace = single ? 1 : 0;
+    const int32_t items = L.num_kv_heads * (L.head_dim / 8);
+    const dim3 block(min(kAppendMaxThreads, (items + 31) / 32 * 32));
     cudaError_t e;
     if (L.head_dim == 64)
-        e = launch_pdl(kv_append_kernel<64>, grid, dim3(kAppendThreads), 0, stream, L, k_pool,
-                       v_pool, stats, k_new, v_new, T, seq_lens, inplace, dev_err);
+        e = launch_pdl(kv_append_kernel<64>, grid, block, 0, stream, L, k_pool, v_pool, stats,
+                       k_new, v_new, T, seq_lens, inplace, dev_err);
     else
-        e = launch_pdl(kv_append_kernel<128>, grid, dim3(kAppendThreads), 0, stream, L, k_pool,
-                       v_pool, stats, k_new, v_new, T, seq_lens, inplace, dev_err);
+        e = launch_pdl(kv_append_kernel<128>, grid, block, 0, stream, L, k_pool, v_pool, stats,
+                       k_new, v_new, T, seq_lens, inplace, dev_err);
     if (e != cudaSuccess) return DATTN_ERR_CUDA;
     if (!single) {
         if (launch_pdl(advance_lengths_kernel, dim3((B + 255) / 256), dim3(256), 0, stream,
