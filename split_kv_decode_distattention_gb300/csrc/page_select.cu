@@ -82,9 +82,9 @@ struct SelSmem {
 __host__ __device__ inline SelSmem sel_smem_layout(int B, int Hkv, int K) {
     SelSmem s;
     s.kp = next_pow2(K);                     // list length: K rounded up to a power of two
-    // per-warp buffer: running list + at least max(Kp, 32) candidates (a batch adds up to
-    // 32 before a fold), a power of two for the sort
-    s.wn = next_pow2(s.kp + (s.kp > 32 ? s.kp : 32));
+    // per-warp buffer: running list, then room for max(Kp, 32) candidates (a power of two;
+    // a batch adds up to 32 before a fold)
+    s.wn = s.kp + (s.kp > 32 ? s.kp : 32);
     uint32_t o = 0;
     s.flags = o;      o += 16u;
     s.bt = o;         o += kSelBT * 4u;
@@ -129,7 +129,7 @@ __device__ __forceinline__ void bitonic_desc(uint64_t* buf, int n, int tid, int 
     for (int k = 2; k <= n; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
             for (int idx = tid; idx < (n >> 1); idx += nthreads) {
-                const int i = 2 * j * (idx / j) + (idx % j);
+                const int i = ((idx & ~(j - 1)) << 1) | (idx & (j - 1));  // j is a power of 2
                 const int l = i + j;
                 const uint64_t x = buf[i], y = buf[l];
                 const bool desc = (i & k) == 0;
@@ -315,10 +315,15 @@ page_select_kernel(const __grid_constant__ SelParams p) {
     const int capw = L.wn - Kp;
     auto csync = [&]() { __syncthreads(); };
     auto wsync = [&]() { __syncwarp(); };
-    auto warp_fold = [&](int cnt) {  // fold candidates wbuf[Kp .. Kp+cnt) into wbuf[0 .. Kp)
-        for (int i = Kp + cnt + lane; i < L.wn; i += 32) wbuf[i] = 0ull;
+    // Folds the candidates wbuf[Kp .. Kp+cnt) into the running list wbuf[0 .. Kp): sorts
+    // the candidates (padded to a power of two), then merges their top Kp into the list.
+    auto warp_fold = [&](int cnt) {
+        const int m = next_pow2(cnt);
+        const int top = m > Kp ? m : Kp;
+        for (int i = Kp + cnt + lane; i < Kp + top; i += 32) wbuf[i] = 0ull;
         __syncwarp();
-        bitonic_desc(wbuf, L.wn, lane, 32, wsync);
+        bitonic_desc(wbuf + Kp, m, lane, 32, wsync);
+        warp_merge_desc(wbuf, wbuf + Kp, Kp, lane);
     };
     // the list of warp w after the pieces' and warps' lists are merged: sorted descending
     auto list_of = [&](int w) { return wbuf_all + w * L.wn; };
@@ -356,6 +361,12 @@ page_select_kernel(const __grid_constant__ SelParams p) {
     const int ri = lane / HG;             // logical page (in the batch) of that score
     constexpr int LPB = LPG < R ? LPG : R;  // logical pages of one physical page in a batch
     constexpr int PPB = R / LPB;            // physical pages in a batch
+    constexpr int LB = LPB == 1 ? 0 : LPB == 2 ? 1 : LPB == 4 ? 2 : 3;  // log2(LPB)
+    // Lane l computes its partials in a permuted order: register slot (i, j) holds the
+    // partial of logical page i ^ ri and head j ^ hj. Then in every level of the transposed
+    // butterfly the half a lane keeps is the same register range in all lanes, and the
+    // reduction needs no selects; afterwards lane l holds (page ri, head hj).
+    const int fp = ri >> LB, fl = ri & (LPB - 1);  // the permutation split as (page, slot)
 
     int32_t a = t_begin;
     int32_t s = locate(t_begin);
@@ -372,8 +383,9 @@ page_select_kernel(const __grid_constant__ SelParams p) {
 #pragma unroll
         for (int j = 0; j < HG; ++j) {
             Vec w{};
-            if (j < p.g)
-                w = *reinterpret_cast<const Vec*>(p.q + ((int64_t)b * p.Hq + h * p.g + j) * D + c0);
+            const int jj = j ^ hj;  // head of register slot j
+            if (jj < p.g)
+                w = *reinterpret_cast<const Vec*>(p.q + ((int64_t)b * p.Hq + h * p.g + jj) * D + c0);
             const uint32_t* ww = reinterpret_cast<const uint32_t*>(&w);
 #pragma unroll
             for (int m = 0; m < NPR; ++m) {
@@ -399,14 +411,15 @@ page_select_kernel(const __grid_constant__ SelParams p) {
             // pages each, starting at logical page lp_of(k).
             auto pc_of = [&](int32_t k) { return (warp + kSelWarps * (k / NB)) * PPU; };
             auto lp_of = [&](int32_t k) { return (k % NB) * R; };
-            // first statistics row of each physical page of batch k (rows of
-            // [num_pages][Hkv][LPG], 2D elements each) and the mask of rows that hold tokens
+            // For register page slot u of batch k (physical page u ^ fp of the batch): its
+            // first statistics row (rows of [num_pages][Hkv][LPG], 2D elements each). Returns
+            // the mask of register row slots whose logical page holds tokens.
             auto plan = [&](int32_t k, uint32_t (&rowi)[PPB]) -> uint32_t {
                 uint32_t m = 0u;
                 const int32_t pc0 = pc_of(k), lp0 = lp_of(k);
 #pragma unroll
                 for (int t = 0; t < PPB; ++t) {
-                    const int32_t pc = pc0 + t;
+                    const int32_t pc = pc0 + (t ^ fp);
                     int32_t nv = 0;  // logical pages of this batch's part of the page with tokens
                     rowi[t] = 0u;
                     if (pc < nc) {
@@ -421,12 +434,17 @@ page_select_kernel(const __grid_constant__ SelParams p) {
                         }
                         if (nv > 0) rowi[t] = ((uint32_t)phys * p.Hkv + h) * LPG + lp0;
                     }
-                    m |= ((1u << nv) - 1u) << (t * LPB);
+#pragma unroll
+                    for (int il = 0; il < LPB; ++il)
+                        m |= (uint32_t)((il ^ fl) < nv) << (t * LPB + il);
                 }
                 return m;
             };
+            // register row slot i holds logical page i ^ ri of the batch
             auto load_row = [&](Vec& dst, const uint32_t (&rowi)[PPB], int i) {
-                ld_chunk(dst, stats_lane + (uint64_t)(rowi[i / LPB] + (i % LPB)) * (2 * D), pol);
+                ld_chunk(dst,
+                         stats_lane + (uint64_t)(rowi[i >> LB] + ((i & (LPB - 1)) ^ fl)) * (2 * D),
+                         pol);
             };
             Vec ring[R];
 #pragma unroll
@@ -444,13 +462,12 @@ page_select_kernel(const __grid_constant__ SelParams p) {
                 const uint32_t cmask = nmask;
                 uint32_t rowi[PPB];
                 nmask = k + 1 < nbat ? plan(k + 1, rowi) : 0u;
-                // Partials of rows i and i + R/2 are made together so that the first
-                // butterfly level (offset 16, which pairs exactly those two rows) can run at
-                // once and only 16 values stay live. Transposed butterfly: at offset o the
-                // lane keeps the half of its values selected by lane bit o and adds the
-                // partner's copy of that half.
+                // Partials of row slots i and i + R/2 are made together so that the first
+                // butterfly level (offset 16, which pairs exactly those two slots) can run at
+                // once and only 16 values stay live. Transposed butterfly: at offset o every
+                // lane keeps x[t] and adds the partner's x[t + n], which thanks to the
+                // permutation holds the same (page, head) partial.
                 float x[16];
-                const bool up16 = (lane & 16) != 0;
 #pragma unroll
                 for (int ip = 0; ip < R / 2; ++ip) {
                     float y[2][HG];
@@ -471,25 +488,18 @@ page_select_kernel(const __grid_constant__ SelParams p) {
                         }
                     }
 #pragma unroll
-                    for (int j = 0; j < HG; ++j) {
-                        const float send = up16 ? y[0][j] : y[1][j];
-                        const float keep = up16 ? y[1][j] : y[0][j];
-                        x[ip * HG + j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-                    }
+                    for (int j = 0; j < HG; ++j)
+                        x[ip * HG + j] = y[0][j] + __shfl_xor_sync(0xffffffffu, y[1][j], 16);
                 }
 #pragma unroll
                 for (int lv = 1; lv < 5; ++lv) {
                     const int o = 16 >> lv, n = 16 >> lv;
-                    const bool up = (lane & o) != 0;
 #pragma unroll
-                    for (int t = 0; t < n; ++t) {
-                        const float send = up ? x[t] : x[t + n];
-                        const float keep = up ? x[t + n] : x[t];
-                        x[t] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                    }
+                    for (int t = 0; t < n; ++t)
+                        x[t] = x[t] + __shfl_xor_sync(0xffffffffu, x[t + n], o);
                 }
-                // lane holds the score of logical page ri, head hj
-                float sc = (hj < p.g && ((cmask >> ri) & 1u)) ? x[0] : kNInf;
+                // lane holds the score of logical page ri, head hj (register row slot 0)
+                float sc = (hj < p.g && (cmask & 1u)) ? x[0] : kNInf;
 #pragma unroll
                 for (int o = 1; o < HG; o <<= 1)
                     sc = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, o));
