@@ -187,10 +187,14 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# the sources that build the decode kernel and choose its launch configuration
+DECODE_SOURCES = ("abi.cu", "attention.cu", "common.cuh", "internal.h")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "split_kv_decode_distattention_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in DECODE_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]

@@ -239,7 +239,11 @@ dattn_status_t dattn_decode_noalloc(const dattn_kv_layout *layout, const dattn_b
  * request b and KV head h of kind DATTN_HEAD_RETRIEVAL:
  *   logical score  sigma(lp) = max over the g query heads j of
  *                  sum_d max(q_jd * kmax_d, q_jd * kmin_d)
- *                  (fp32, one fused multiply-add per channel in ascending channel order);
+ *                  in fp32 and a fixed order: 16 chunks of d/16 channels; per chunk a
+ *                  k_max partial with max(q,0) and a k_min partial with min(q,0), each two
+ *                  fused multiply-add chains from +0 (even and odd channels, ascending)
+ *                  added as even + odd; the 32 partials x[0..15] (k_max), x[16..31]
+ *                  (k_min) added by the tree x[i] += x[i + n], n = 16, 8, 4, 2, 1;
  *   physical score = max of sigma over its logical pages that hold a token < L_b;
  *   selection      the top_k physical pages by score, ties to the lower page index.
  * They are written in ascending page order to selected[b][h][0..top_k), padded with -1.
@@ -250,6 +254,8 @@ dattn_status_t dattn_decode_noalloc(const dattn_kv_layout *layout, const dattn_b
  *   q        (device) bf16 [B][Hq][d];  seq_lens (device) int32 [B]
  *   head_kind (device) int8 [Hkv];  selected (device) int32 [B][Hkv][top_k]
  *   ws, ws_bytes  workspace of at least dattn_workspace_size(B, Hq, Hkv, d, top_k, num_splits)
+ * Besides the common limits it needs P/16 to be a power of two (P = 16, 32, 64, 128 or 256)
+ * and returns DATTN_ERR_UNSUPPORTED otherwise.
  */
 dattn_status_t dattn_page_select(const dattn_kv_layout *layout, const dattn_bf16 *stats,
                                  const dattn_bf16 *q, int32_t B, int32_t Hq,

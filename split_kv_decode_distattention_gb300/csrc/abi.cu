@@ -324,6 +324,8 @@ dattn_status_t dattn_page_select(const dattn_kv_layout* layout, const dattn_bf16
     if ((st = check_heads(layout, B, Hq)) != DATTN_OK) return st;
     if (top_k < 0 || num_splits < 0) return DATTN_ERR_INVALID_ARG;
     if (top_k > kMaxTopK) return DATTN_ERR_UNSUPPORTED;
+    const int32_t lpg = layout->page_size / 16;  // logical pages per physical page
+    if (lpg & (lpg - 1)) return DATTN_ERR_UNSUPPORTED;
     if (B == 0 || top_k == 0) return DATTN_OK;
     if (!stats || !q || !seq_lens || !head_kind || !selected) return DATTN_ERR_INVALID_ARG;
     if (!aligned16(stats)) return DATTN_ERR_INVALID_ARG;

@@ -12,8 +12,9 @@
 // streaming heads, fused into the same kernel as the retrieval heads).
 //
 // GB300 design. The page tile of one (page, KV head) is contiguous in HBM. A producer warp
-// streams 16-token K and V row groups into an 8-stage shared-memory ring with 2-D TMA
-// tensor loads: 128-byte swizzle, evict-first L2 policy, completion on mbarriers. Four
+// streams 16-token K and V row groups into an 8-stage shared-memory ring with one 3-D TMA
+// box each ({64, 16, d/64}: 128-byte swizzle, evict-first L2 policy, completion on
+// mbarriers). Four
 // consumer warps each own every fourth stage. A consumer runs the small QK^T tile with
 // tokens as the M dimension and the GQA group as N (mma.sync m16n8k16, bf16 in, fp32
 // accumulate). It does an online softmax in base 2 with warp shuffles, transposes P with

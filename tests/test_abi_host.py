@@ -115,6 +115,17 @@ def test_decode_rejects_bad_shapes_before_launch(dattn):
     assert _decode_status(dattn, _lay(dattn, num_pages=1 << 26, page_size=64)) == UNSUPPORTED
 
 
+def test_page_select_needs_power_of_two_logical_pages(dattn):
+    lib = dattn.load_library()
+    p = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    lay = _lay(dattn, page_size=48)  # three logical pages per physical page
+    assert lib.dattn_page_select(ctypes.byref(lay.c), p, p, 1, 4, p, p, 8, p, p, 1 << 20, 0,
+                                 None, None) == 2  # DATTN_ERR_UNSUPPORTED
+    lay = _lay(dattn, page_size=64)
+    assert lib.dattn_page_select(ctypes.byref(lay.c), p, p, 1, 4, p, p, 300, p, p, 1 << 20, 0,
+                                 None, None) == 2  # top_k above 256
+
+
 def test_sparse_settings_are_validated(dattn):
     import torch
     hk = torch.zeros(2, dtype=torch.int8)
