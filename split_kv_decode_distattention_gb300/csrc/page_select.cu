@@ -47,8 +47,10 @@ namespace dattn {
 
 namespace {
 
-constexpr int kSelWarps = 8;
-constexpr int kSelThreads = kSelWarps * 32;
+// Warps per CTA (one CTA per SM): 16 when a lane scores 4 query heads, 8 when it scores 8
+// (their query values take twice the registers).
+__host__ __device__ constexpr int sel_warps(int hg) { return hg == 4 ? 16 : 8; }
+constexpr int kSelMaxWarps = 16;
 
 struct SelParams {
     int32_t num_pages, Hkv, P, max_pages;
@@ -63,6 +65,7 @@ struct SelParams {
     int32_t* counters;
     uint64_t* slots;
     int32_t nseg;
+    int32_t stages;  // statistics batches staged per warp
     int32_t* dev_err;
 };
 
@@ -72,30 +75,41 @@ __host__ __device__ inline int next_pow2(int x) {
     return n;
 }
 
-constexpr int kSelBT = 2048;  // block-table entries staged in shared memory at once
+constexpr int kSelBT = 1024;  // block-table entries staged in shared memory at once
 
 struct SelSmem {
-    uint32_t flags, bt, wbuf, ret_before, ret_heads, item_start, item_len, scan, total;
-    int kp, wn;
+    uint32_t flags, stage, bars, masks, batches, bt, wbuf, ret_before, ret_heads, item_start,
+        item_len, scan, total;
+    int kp, wn, stages;
 };
 
-__host__ __device__ inline SelSmem sel_smem_layout(int B, int Hkv, int K) {
+// nw: warps per CTA; stage_bytes: one batch of statistics rows; stages: batches staged per
+// warp.
+__host__ __device__ inline SelSmem sel_smem_layout(int B, int Hkv, int K, int nw,
+                                                   uint32_t stage_bytes, int stages) {
     SelSmem s;
+    s.stages = stages;
     s.kp = next_pow2(K);                     // list length: K rounded up to a power of two
     // per-warp buffer: running list, then room for max(Kp, 32) candidates (a power of two;
     // a batch adds up to 32 before a fold)
     s.wn = s.kp + (s.kp > 32 ? s.kp : 32);
     uint32_t o = 0;
-    s.flags = o;      o += 16u;
+    // +0: last-arrival flag, +4: abort flag, +8: next unit, +16: CTA-wide K-th key
+    s.flags = o;      o += 32u;
+    o = (o + 127u) & ~127u;
+    s.stage = o;      o += (uint32_t)(nw * stages) * stage_bytes;
+    s.bars = o;       o += (uint32_t)(nw * stages) * 8u;
+    s.masks = o;      o += (uint32_t)(nw * stages) * 4u;
+    s.batches = o;    o += (uint32_t)(nw * stages) * 4u;
     s.bt = o;         o += kSelBT * 4u;
-    s.wbuf = o;       o += (uint32_t)kSelWarps * s.wn * 8u;
+    s.wbuf = o;       o += (uint32_t)nw * s.wn * 8u;
     s.ret_before = o; o += (uint32_t)(Hkv + 1) * 4u;
     s.ret_heads = o;  o += (uint32_t)Hkv * 4u;
     o = (o + 15u) & ~15u;
     s.item_start = o; o += (uint32_t)(B + 1) * 4u;
     s.item_len = o;   o += (uint32_t)B * 4u;
     o = (o + 15u) & ~15u;
-    s.scan = o;       o += 8u * 4u;
+    s.scan = o;       o += (uint32_t)kSelMaxWarps * 4u;
     s.total = o + 128u;
     return s;
 }
@@ -106,6 +120,13 @@ __device__ __forceinline__ uint64_t make_key(float score, int32_t page) {
     return ((uint64_t)ord << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)page);
 }
 
+// Score of a key from make_key (-inf for the empty key 0).
+__device__ __forceinline__ float key_score(uint64_t key) {
+    if (key == 0ull) return -__int_as_float(0x7f800000);
+    const uint32_t ord = (uint32_t)(key >> 32);
+    return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7fffffffu) : ~ord);
+}
+
 __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
@@ -114,6 +135,13 @@ __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
 
 __device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// a * b, two independent IEEE fp32 products
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
 }
 
 // acc = a * b + acc, two independent IEEE fp32 fused multiply-adds
@@ -169,34 +197,63 @@ template <int CPL> struct ChunkVec;
 template <> struct ChunkVec<8> { using type = uint4; };  // 8 bf16 channels
 template <> struct ChunkVec<4> { using type = uint2; };  // 4 bf16 channels
 
+// Two bf16 (low half: even channel, high half: odd channel) -> the fp32 pair {even, odd},
+// built in one 64-bit register pair so that the packed FMA needs no moves.
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
+    uint64_t r;
+    asm("{\n\t.reg .b32 lo, hi;\n\t"
+        "shl.b32 lo, %1, 16;\n\t"
+        "and.b32 hi, %1, 0xffff0000;\n\t"
+        "mov.b64 %0, {lo, hi};\n\t}"
+        : "=l"(r)
+        : "r"(w));
+    return r;
+}
 __device__ __forceinline__ void unpack_bf16x8(const uint4& v, uint64_t (&k)[4]) {
-    k[0] = pack_f32x2(bf16_lo(v.x), bf16_hi(v.x));
-    k[1] = pack_f32x2(bf16_lo(v.y), bf16_hi(v.y));
-    k[2] = pack_f32x2(bf16_lo(v.z), bf16_hi(v.z));
-    k[3] = pack_f32x2(bf16_lo(v.w), bf16_hi(v.w));
+    k[0] = bf16x2_to_f32x2(v.x);
+    k[1] = bf16x2_to_f32x2(v.y);
+    k[2] = bf16x2_to_f32x2(v.z);
+    k[3] = bf16x2_to_f32x2(v.w);
 }
 __device__ __forceinline__ void unpack_bf16x8(const uint2& v, uint64_t (&k)[2]) {
-    k[0] = pack_f32x2(bf16_lo(v.x), bf16_hi(v.x));
-    k[1] = pack_f32x2(bf16_lo(v.y), bf16_hi(v.y));
+    k[0] = bf16x2_to_f32x2(v.x);
+    k[1] = bf16x2_to_f32x2(v.y);
 }
 
-// Read-once load of a lane's chunk of one logical page (no L1 allocation, evict-first L2).
-__device__ __forceinline__ void ld_chunk(uint4& v, const uint16_t* ptr, uint64_t pol) {
-    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+// A lane's chunk of one logical page's row in a shared-memory stage.
+__device__ __forceinline__ void lds_chunk(uint4& v, uint32_t addr) {
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(ptr), "l"(pol));
+                 : "r"(addr));
 }
-__device__ __forceinline__ void ld_chunk(uint2& v, const uint16_t* ptr, uint64_t pol) {
-    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
-                 : "=r"(v.x), "=r"(v.y)
-                 : "l"(ptr), "l"(pol));
+__device__ __forceinline__ void lds_chunk(uint2& v, uint32_t addr) {
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+}
+
+// Adds bytes to the transaction count of the barrier's current phase (no arrival).
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// Bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16), completing on
+// the barrier's transaction count, with an L2 policy for the source.
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
 }
 
 // D: head_dim; HG: query heads scored per KV head (4 or 8, unused ones masked);
 // LPG: logical pages per physical page (P / 16, a power of two).
 template <int D, int HG, int LPG>
-__global__ void __launch_bounds__(kSelThreads, HG == 4 ? 2 : 1)
+__global__ void __launch_bounds__(sel_warps(HG) * 32, 1)
 page_select_kernel(const __grid_constant__ SelParams p) {
+    constexpr int NW = sel_warps(HG);        // warps per CTA
+    constexpr int NT = NW * 32;
     constexpr int CPL = D / 16;              // channels per lane
     constexpr int NPR = CPL / 2;             // channel pairs per lane
     constexpr int R = 32 / HG;               // logical pages per batch
@@ -209,7 +266,7 @@ page_select_kernel(const __grid_constant__ SelParams p) {
     const uint32_t raw_off = smem_u32(smem_raw);
     uint8_t* base = smem_raw + (((raw_off + 127u) & ~127u) - raw_off);
     const int K = p.top_k;
-    const SelSmem L = sel_smem_layout(p.B, p.Hkv, K);
+    const SelSmem L = sel_smem_layout(p.B, p.Hkv, K, NW, R * 4u * D, p.stages);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t G = gridDim.x, cta = blockIdx.x;
     int* last_flag = reinterpret_cast<int*>(base + L.flags);
@@ -219,10 +276,11 @@ page_select_kernel(const __grid_constant__ SelParams p) {
     int32_t* item_len = reinterpret_cast<int32_t*>(base + L.item_len);
     int32_t* scan = reinterpret_cast<int32_t*>(base + L.scan);
 
+    if (tid == 0) reinterpret_cast<volatile int*>(base + L.flags)[1] = 0;  // abort flag
     grid_dependency_wait();  // lengths and statistics may come from the previous kernel
     grid_launch_dependents();
     // ---------------------------------------------------------------- setup
-    for (int h = tid; h < p.Hkv; h += kSelThreads)
+    for (int h = tid; h < p.Hkv; h += NT)
         ret_heads[h] = p.head_kind[h] == DATTN_HEAD_RETRIEVAL ? 1 : 0;
     __syncthreads();
     if (tid == 0) {
@@ -238,7 +296,7 @@ page_select_kernel(const __grid_constant__ SelParams p) {
     const int32_t nret = ret_before[p.Hkv];
     {
         const int32_t n = p.B;
-        const int32_t per = (n + kSelThreads - 1) / kSelThreads;
+        const int32_t per = (n + NT - 1) / NT;
         const int32_t i0 = min(n, tid * per), i1 = min(n, i0 + per);
         int32_t local_sum = 0;
         for (int32_t i = i0; i < i1; ++i) {
@@ -270,7 +328,7 @@ page_select_kernel(const __grid_constant__ SelParams p) {
         }
         if (tid == 0) {
             int32_t tot = 0;
-            for (int w = 0; w < kSelWarps; ++w) tot += scan[w];
+            for (int w = 0; w < NW; ++w) tot += scan[w];
             item_start[n] = tot;
         }
         __syncthreads();
@@ -304,11 +362,10 @@ page_select_kernel(const __grid_constant__ SelParams p) {
         int32_t st, len;
         seg_span(s, st, len);
         if (len == 0)
-            for (int r = tid; r < K; r += kSelThreads) p.selected[(int64_t)s * K + r] = -1;
+            for (int r = tid; r < K; r += NT) p.selected[(int64_t)s * K + r] = -1;
     }
     if (t_begin >= t_end) return;
 
-    const int NT = kSelThreads;
     const int Kp = L.kp;  // K rounded up to a power of two; key 0 marks an empty entry
     uint64_t* wbuf_all = reinterpret_cast<uint64_t*>(base + L.wbuf);
     uint64_t* wbuf = wbuf_all + warp * L.wn;  // [0, Kp): running top keys; then candidates
@@ -327,10 +384,10 @@ page_select_kernel(const __grid_constant__ SelParams p) {
     };
     // the list of warp w after the pieces' and warps' lists are merged: sorted descending
     auto list_of = [&](int w) { return wbuf_all + w * L.wn; };
-    // merges the warps' running lists into list_of(0) (three levels of pairwise merges)
+    // merges the warps' running lists into list_of(0) (log2(NW) levels of pairwise merges)
     auto merge_warps = [&]() {
 #pragma unroll 1
-        for (int n = kSelWarps / 2; n >= 1; n >>= 1) {
+        for (int n = NW / 2; n >= 1; n >>= 1) {
             if (warp < n) warp_merge_desc(list_of(warp), list_of(warp + n), Kp, lane);
             csync();
         }
@@ -356,21 +413,44 @@ page_select_kernel(const __grid_constant__ SelParams p) {
     const int half = lane >> 4;           // 0: k_max lanes, 1: k_min lanes
     const int c0 = CPL * (lane & 15);     // first channel of the lane
     const int lane_off = half * D + c0;   // element offset inside a logical-page row
-    const uint16_t* stats_lane = p.stats + lane_off;
     const int hj = lane % HG;             // head of the score the lane holds after reduction
     const int ri = lane / HG;             // logical page (in the batch) of that score
     constexpr int LPB = LPG < R ? LPG : R;  // logical pages of one physical page in a batch
     constexpr int PPB = R / LPB;            // physical pages in a batch
-    constexpr int LB = LPB == 1 ? 0 : LPB == 2 ? 1 : LPB == 4 ? 2 : 3;  // log2(LPB)
+    constexpr uint32_t kRowBytes = 4 * D;   // one logical page's row: k_max and k_min
+    constexpr uint32_t kStageBytes = R * kRowBytes;
     // Lane l computes its partials in a permuted order: register slot (i, j) holds the
     // partial of logical page i ^ ri and head j ^ hj. Then in every level of the transposed
     // butterfly the half a lane keeps is the same register range in all lanes, and the
     // reduction needs no selects; afterwards lane l holds (page ri, head hj).
-    const int fp = ri >> LB, fl = ri & (LPB - 1);  // the permutation split as (page, slot)
+    // This warp's stages: S buffers of one batch each, filled by bulk copies.
+    const int S = L.stages;
+    const uint32_t stage0 = smem_u32(base + L.stage) + (uint32_t)(warp * S) * kStageBytes;
+    const uint32_t bar0 = smem_u32(base + L.bars) + (uint32_t)(warp * S) * 8u;
+    uint32_t* smask = reinterpret_cast<uint32_t*>(base + L.masks) + warp * S;
+    int32_t* sbatch = reinterpret_cast<int32_t*>(base + L.batches) + warp * S;
+    int32_t* next_unit = reinterpret_cast<int32_t*>(base + L.flags + 8);
+    unsigned long long* cta_thresh_u = reinterpret_cast<unsigned long long*>(base + L.flags + 16);
+    volatile uint64_t* cta_thresh = reinterpret_cast<volatile uint64_t*>(cta_thresh_u);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.flags + 4);
+    if (lane < S) mbar_init(bar0 + 8u * lane, 1);
+    fence_mbar_init();
+    __syncwarp();
+    // The warp uses its stages round robin over the whole kernel. (st, par) is the stage of
+    // the next batch to wait for and the parity of the phase that batch completes; every
+    // batch issued is eventually waited for or skipped with advance().
+    int st = 0;
+    uint32_t par = 0u;
+    auto advance = [&]() {
+        if (++st == S) {
+            st = 0;
+            par ^= 1u;
+        }
+    };
 
     int32_t a = t_begin;
     int32_t s = locate(t_begin);
-    while (a < t_end) {
+    while (a < t_end && !*abort_flag) {
         int32_t sst, slen;
         seg_span(s, sst, slen);
         while (sst + slen <= a) { ++s; seg_span(s, sst, slen); }
@@ -396,72 +476,92 @@ page_select_kernel(const __grid_constant__ SelParams p) {
         }
         for (int i = lane; i < L.wn; i += 32) wbuf[i] = 0ull;
         int cnt_c = 0;
-        uint64_t thresh = 0ull;
+        uint64_t thresh = 0ull;  // running K-th key of the warp (0 while fewer than K)
+        float thr_sc = kNInf;    // its score
         const int32_t* btrow = p.block_table + (int64_t)b * p.max_pages;
         const int32_t pr0 = a - sst;  // first page of the piece (request-relative)
-        for (int32_t cb = 0; cb < pe - a; cb += kSelBT) {
+        for (int32_t cb = 0; cb < pe - a && !*abort_flag; cb += kSelBT) {
             const int32_t nc = min(kSelBT, pe - a - cb);  // pages of this block
             const int32_t pg0 = pr0 + cb;                 // request-relative page of bt_s[0]
             for (int i = tid; i < nc; i += NT) bt_s[i] = btrow[pg0 + i];
+            if (tid == 0) {
+                *next_unit = 0;
+                if (cb == 0) *cta_thresh = 0ull;
+            }
             csync();
             const int32_t nunits = (nc + PPU - 1) / PPU;
-            const int32_t nbat = warp < nunits ? ((nunits - 1 - warp) / kSelWarps + 1) * NB : 0;
-            // Batch k of the warp: unit warp + 8 (k / NB), sub-batch k % NB. Its R logical
-            // pages are PPB physical pages (block-relative first page pc_of(k)) of LPB logical
-            // pages each, starting at logical page lp_of(k).
-            auto pc_of = [&](int32_t k) { return (warp + kSelWarps * (k / NB)) * PPU; };
-            auto lp_of = [&](int32_t k) { return (k % NB) * R; };
-            // For register page slot u of batch k (physical page u ^ fp of the batch): its
-            // first statistics row (rows of [num_pages][Hkv][LPG], 2D elements each). Returns
-            // the mask of register row slots whose logical page holds tokens.
-            auto plan = [&](int32_t k, uint32_t (&rowi)[PPB]) -> uint32_t {
-                uint32_t m = 0u;
-                const int32_t pc0 = pc_of(k), lp0 = lp_of(k);
-#pragma unroll
-                for (int t = 0; t < PPB; ++t) {
-                    const int32_t pc = pc0 + (t ^ fp);
-                    int32_t nv = 0;  // logical pages of this batch's part of the page with tokens
-                    rowi[t] = 0u;
+            // Units (PPU physical pages, NB batches) are handed out to the warps by a shared
+            // counter, so warps that run faster take more of them. A warp takes a unit when
+            // it issues the copies of its first batch, S batches before it scores it. Batch
+            // index bi = unit * NB + sub; its R logical pages are PPB physical pages
+            // (block-relative first page pc_of(bi)) of LPB logical pages each, starting at
+            // logical page lp_of(bi).
+            auto pc_of = [&](int32_t bi) { return (bi / NB) * PPU; };
+            auto lp_of = [&](int32_t bi) { return (bi % NB) * R; };
+            int32_t iss_unit = 0, iss_sub = NB;  // the unit whose sub-batches are being issued
+            // Issues the next batch of this warp into stage st, or marks the stage empty
+            // (batch -1) once the units are exhausted. Lane t < PPB takes physical page t of
+            // the batch: its logical pages that hold tokens are one contiguous run of rows.
+            // smask[st] gets the mask of rows (in batch order) that were copied; the others
+            // are never read as scores.
+            auto issue = [&](int st) {
+                if (iss_sub == NB) {
+                    int32_t u = 0;
+                    if (lane == 0) u = atomicAdd(next_unit, 1);
+                    iss_unit = __shfl_sync(0xffffffffu, u, 0);
+                    iss_sub = 0;
+                }
+                const int32_t bi = iss_unit < nunits ? iss_unit * NB + iss_sub : -1;
+                ++iss_sub;
+                const uint32_t bar = bar0 + 8u * st;
+                uint32_t part = 0u, bytes = 0u;
+                int32_t phys = -1;
+                if (bi >= 0 && lane < PPB) {
+                    const int32_t pc = pc_of(bi) + lane, lp0 = lp_of(bi);
                     if (pc < nc) {
                         const int32_t rem = Lb - (pg0 + pc) * p.P - lp0 * 16;
-                        nv = min(max((rem + 15) >> 4, 0), LPB);
-                        const int32_t phys = bt_s[pc];
+                        const int32_t nv = min(max((rem + 15) >> 4, 0), LPB);
+                        phys = bt_s[pc];
                         if (nv > 0 && (phys < 0 || phys >= p.num_pages)) {
-                            if (lane == 0 && lp0 == 0)
+                            if (lp0 == 0)
                                 set_err(p.dev_err, phys < 0 ? DATTN_DEVERR_UNMAPPED_PAGE
                                                             : DATTN_DEVERR_PAGE_OOB);
-                            nv = 0;
+                        } else if (nv > 0) {
+                            part = ((1u << nv) - 1u) << (lane * LPB);
+                            bytes = (uint32_t)nv * kRowBytes;
                         }
-                        if (nv > 0) rowi[t] = ((uint32_t)phys * p.Hkv + h) * LPG + lp0;
                     }
-#pragma unroll
-                    for (int il = 0; il < LPB; ++il)
-                        m |= (uint32_t)((il ^ fl) < nv) << (t * LPB + il);
                 }
-                return m;
+                const uint32_t mask = __reduce_or_sync(0xffffffffu, part);
+                if (bytes) mbar_expect_tx(bar, bytes);
+                __syncwarp();
+                if (lane == 0) {
+                    smask[st] = mask;
+                    sbatch[st] = bi;
+                    mbar_arrive(bar);
+                }
+                if (bytes) {
+                    const uint16_t* src =
+                        p.stats + (((int64_t)phys * p.Hkv + h) * LPG + lp_of(bi)) * (2 * D);
+                    bulk_copy(stage0 + (uint32_t)st * kStageBytes + (uint32_t)(lane * LPB) * kRowBytes,
+                              src, bytes, bar, pol);
+                }
             };
-            // register row slot i holds logical page i ^ ri of the batch
-            auto load_row = [&](Vec& dst, const uint32_t (&rowi)[PPB], int i) {
-                ld_chunk(dst,
-                         stats_lane + (uint64_t)(rowi[i >> LB] + ((i & (LPB - 1)) ^ fl)) * (2 * D),
-                         pol);
-            };
-            Vec ring[R];
-#pragma unroll
-            for (int i = 0; i < R; ++i) ring[i] = Vec{};
-            uint32_t nmask = 0u;
-            if (nbat > 0) {
-                uint32_t rowi[PPB];
-                nmask = plan(0, rowi);
-#pragma unroll
-                for (int i = 0; i < R; ++i)
-                    if ((nmask >> i) & 1u) load_row(ring[i], rowi, i);
-            }
+            for (int k = 0, t = st; k < S; ++k, t = (t + 1 == S) ? 0 : t + 1) issue(t);
+            int32_t pending = S;  // batches issued and not yet waited for
             float pmax = kNInf;  // running physical-page max when a page spans batches
-            for (int32_t k = 0; k < nbat; ++k) {
-                const uint32_t cmask = nmask;
-                uint32_t rowi[PPB];
-                nmask = k + 1 < nbat ? plan(k + 1, rowi) : 0u;
+            while (true) {
+                // warp-uniform, bounded wait for the stage's copies
+                const bool ok = __all_sync(0xffffffffu,
+                                           mbar_wait(bar0 + 8u * st, par, abort_flag, p.dev_err));
+                if (!ok) break;
+                const int cst = st;
+                advance();
+                --pending;
+                const int32_t bi = sbatch[cst];
+                if (bi < 0) break;  // the units are exhausted; later stages are empty too
+                const uint32_t mask = smask[cst];
+                const uint32_t sbase = stage0 + (uint32_t)cst * kStageBytes + (uint32_t)lane_off * 2u;
                 // Partials of row slots i and i + R/2 are made together so that the first
                 // butterfly level (offset 16, which pairs exactly those two slots) can run at
                 // once and only 16 values stay live. Transposed butterfly: at offset o every
@@ -474,14 +574,18 @@ page_select_kernel(const __grid_constant__ SelParams p) {
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int i = ip + u * (R / 2);
+                        Vec v;
+                        lds_chunk(v, sbase + (uint32_t)(i ^ ri) * kRowBytes);
                         uint64_t kp[NPR];
-                        unpack_bf16x8(ring[i], kp);
-                        if ((nmask >> i) & 1u) load_row(ring[i], rowi, i);
+                        unpack_bf16x8(v, kp);
 #pragma unroll
                         for (int j = 0; j < HG; ++j) {
-                            uint64_t acc = 0ull;  // {even, odd}, both +0
+                            // {even, odd} chains; the first term is an exact product (two
+                            // bf16 values), the same as a fused multiply-add onto +0 except
+                            // for the sign of an exact zero, which keys do not see
+                            uint64_t acc = mul_f32x2(qv[j][0], kp[0]);
 #pragma unroll
-                            for (int m = 0; m < NPR; ++m) fma_f32x2(acc, qv[j][m], kp[m]);
+                            for (int m = 1; m < NPR; ++m) fma_f32x2(acc, qv[j][m], kp[m]);
                             float ev, od;
                             unpack_f32x2(acc, ev, od);
                             y[u][j] = ev + od;
@@ -491,6 +595,11 @@ page_select_kernel(const __grid_constant__ SelParams p) {
                     for (int j = 0; j < HG; ++j)
                         x[ip * HG + j] = y[0][j] + __shfl_xor_sync(0xffffffffu, y[1][j], 16);
                 }
+                // every lane has read the stage: refill it with the warp's next batch
+                __syncwarp();
+                fence_proxy_async_smem();
+                issue(cst);
+                ++pending;
 #pragma unroll
                 for (int lv = 1; lv < 5; ++lv) {
                     const int o = 16 >> lv, n = 16 >> lv;
@@ -498,28 +607,37 @@ page_select_kernel(const __grid_constant__ SelParams p) {
                     for (int t = 0; t < n; ++t)
                         x[t] = x[t] + __shfl_xor_sync(0xffffffffu, x[t + n], o);
                 }
-                // lane holds the score of logical page ri, head hj (register row slot 0)
-                float sc = (hj < p.g && (cmask & 1u)) ? x[0] : kNInf;
+                // lane holds the score of logical page ri, head hj
+                float sc = (hj < p.g && ((mask >> ri) & 1u)) ? x[0] : kNInf;
 #pragma unroll
                 for (int o = 1; o < HG; o <<= 1)
                     sc = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, o));
 #pragma unroll
                 for (int o = HG; o < HG * LPB; o <<= 1)
                     sc = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, o));
-                uint64_t key = 0ull;
+                // the lanes that own a physical page's score, and that score
+                bool own;
+                int32_t own_pc;
                 if constexpr (NB == 1) {
-                    const int32_t pc = pc_of(k) + lane / (HG * LPB);
-                    if (lane % (HG * LPB) == 0 && sc != kNInf) key = make_key(sc, pg0 + pc);
+                    own = lane % (HG * LPB) == 0;
+                    own_pc = pc_of(bi) + lane / (HG * LPB);
                 } else {
                     pmax = fmaxf(pmax, sc);
-                    if (k % NB == NB - 1) {
-                        if (lane == 0 && pmax != kNInf) key = make_key(pmax, pg0 + pc_of(k));
-                        pmax = kNInf;
-                    }
+                    own = lane == 0 && bi % NB == NB - 1;
+                    own_pc = pc_of(bi);
+                    sc = pmax;
+                    if (bi % NB == NB - 1) pmax = kNInf;
                 }
-                const bool take = key > thresh;
-                const uint32_t bal = __ballot_sync(0xffffffffu, take);
-                if (bal) {
+                // Keys are built only when some page reaches the K-th score so far (the
+                // larger of the warp's and the CTA's); ties are settled by the full key,
+                // which includes the page.
+                const uint64_t th = max(thresh, *cta_thresh);
+                const float th_sc = th == thresh ? thr_sc : key_score(th);
+                const bool cand = own && sc != kNInf && sc >= th_sc;
+                if (__any_sync(0xffffffffu, cand)) {
+                    const uint64_t key = cand ? make_key(sc, pg0 + own_pc) : 0ull;
+                    const bool take = key > th;
+                    const uint32_t bal = __ballot_sync(0xffffffffu, take);
                     if (take) wbuf[Kp + cnt_c + __popc(bal & ((1u << lane) - 1u))] = key;
                     cnt_c += __popc(bal);
                     __syncwarp();
@@ -527,8 +645,22 @@ page_select_kernel(const __grid_constant__ SelParams p) {
                         warp_fold(cnt_c);
                         cnt_c = 0;
                         thresh = wbuf[K - 1];
+                        thr_sc = key_score(thresh);
+                        if (lane == 0 && thresh) atomicMax(cta_thresh_u, thresh);
                     }
                 }
+            }
+            // Step over the batches issued and not waited for. After a normal end they are
+            // empty stages (no copies, their phases complete at once); after an abort, wait
+            // (bounded) for the copies still in flight.
+            for (; pending > 0; --pending) {
+                if (*abort_flag) {
+                    const unsigned long long t0 = global_timer_ns();
+                    while (!mbar_try_wait(bar0 + 8u * st, par) &&
+                           global_timer_ns() - t0 < kWaitLimitNs) {
+                    }
+                }
+                advance();
             }
             csync();  // bt_s is restaged for the next block of pages
         }
@@ -558,7 +690,7 @@ page_select_kernel(const __grid_constant__ SelParams p) {
                 // lists are merged
                 for (int i = lane; i < Kp; i += 32) wbuf[i] = 0ull;
                 uint64_t* scratch = wbuf + Kp;
-                for (int32_t qq = warp; qq < npieces; qq += kSelWarps) {
+                for (int32_t qq = warp; qq < npieces; qq += NW) {
                     const unsigned long long* src = reinterpret_cast<const unsigned long long*>(
                         p.slots + (int64_t)(c_first + qq + s) * K);
                     for (int i = lane; i < Kp; i += 32) scratch[i] = i < K ? __ldcg(src + i) : 0ull;
@@ -587,7 +719,7 @@ int sel_prepare(uint32_t smem) {
     }
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, page_select_kernel<D, HG, LPG>,
-                                                      kSelThreads, smem) != cudaSuccess)
+                                                      sel_warps(HG) * 32, smem) != cudaSuccess)
         return 1;
     return n < 1 ? 1 : n;
 }
@@ -604,7 +736,7 @@ cudaError_t sel_go(int32_t G_req, int64_t units_bound, uint32_t smem, cudaStream
     if (!ws_ok) return cudaSuccess;
     p.counters = static_cast<int32_t*>(ws);
     p.slots = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + counters);
-    return launch_pdl(page_select_kernel<D, HG, LPG>, dim3(G), dim3(kSelThreads), smem, stream,
+    return launch_pdl(page_select_kernel<D, HG, LPG>, dim3(G), dim3(sel_warps(HG) * 32), smem, stream,
                       p);
 }
 
@@ -654,11 +786,19 @@ dattn_status_t launch_page_select(const dattn_kv_layout& Lay, const uint16_t* st
     const int D = Lay.head_dim;
     const int lpg = p.P / 16;
     if (lpg & (lpg - 1)) return DATTN_ERR_UNSUPPORTED;  // P / 16 must be a power of two
-    const SelSmem L = sel_smem_layout(B, p.Hkv, top_k);
-    if (L.total > 227u * 1024u) return DATTN_ERR_UNSUPPORTED;
+    const bool wide = p.g > 4;  // 8 query heads per KV head instead of 4
+    // one batch is 32 / (4 or 8) logical pages of 4d bytes; up to three batches in flight
+    // per warp, as many as the shared memory of one CTA per SM holds
+    const uint32_t stage_bytes = (wide ? 4u : 8u) * 4u * (uint32_t)D;
+    const int nw = sel_warps(wide ? 8 : 4);
+    SelSmem L{};
+    for (p.stages = 3; p.stages >= 1; --p.stages) {
+        L = sel_smem_layout(B, p.Hkv, top_k, nw, stage_bytes, p.stages);
+        if (L.total <= 227u * 1024u) break;
+    }
+    if (p.stages < 1) return DATTN_ERR_UNSUPPORTED;
     bool ws_ok = true;
     cudaError_t e;
-    const bool wide = p.g > 4;  // 8 query heads per KV head instead of 4
     if (D == 64)
         e = wide ? sel_go_lpg<64, 8>(lpg, num_splits, units_bound, L.total, stream, p, ws,
                                      ws_bytes, ws_ok)

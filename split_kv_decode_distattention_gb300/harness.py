@@ -33,6 +33,7 @@ class PagedCache:
         self.lens = [0] * c.B  # host mirror of seq_lens
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=device)
         self.chunk_tokens = chunk_tokens
+        self._head_kind = None
         if fill:
             self.fill()
 
@@ -75,10 +76,17 @@ class PagedCache:
         return Workspace(c.B, c.Hq, c.Hkv, c.d, top_k=top_k, num_splits=num_splits,
                          device=self.device)
 
+    def head_kind(self) -> torch.Tensor:
+        """The per-KV-head kinds on the device, copied once: a copy from pageable host memory
+        would make every later call wait for the GPU to drain."""
+        if self._head_kind is None:
+            self._head_kind = torch.as_tensor(self.case.head_kind_array(), dtype=torch.int8,
+                                              device=self.device)
+        return self._head_kind
+
     def sparse_config(self, selected) -> SparseConfig:
         c = self.case
-        hk = torch.as_tensor(c.head_kind_array(), dtype=torch.int8, device=self.device)
-        return SparseConfig(hk, c.sinks, c.local, c.top_k, selected)
+        return SparseConfig(self.head_kind(), c.sinks, c.local, c.top_k, selected)
 
     def decode(self, q, out, ws, m_g=None, e_g=None, sparse=None, num_splits=0):
         dattn_decode(self.layout, self.k_pool, self.v_pool, q, self.case.scale, self.seq_lens,
@@ -87,6 +95,5 @@ class PagedCache:
 
     def select(self, q, selected, ws, num_splits=0):
         c = self.case
-        hk = torch.as_tensor(c.head_kind_array(), dtype=torch.int8, device=self.device)
-        dattn_page_select(self.layout, self.stats, q, self.seq_lens, hk, c.top_k, selected, ws,
-                          num_splits=num_splits, dev_err=self.dev_err)
+        dattn_page_select(self.layout, self.stats, q, self.seq_lens, self.head_kind(), c.top_k,
+                          selected, ws, num_splits=num_splits, dev_err=self.dev_err)
