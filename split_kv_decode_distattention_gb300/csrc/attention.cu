@@ -53,7 +53,6 @@ struct Smem {
     __device__ float* ws_m() const { return reinterpret_cast<float*>(base + L.ws_m); }
     __device__ float* ws_e() const { return reinterpret_cast<float*>(base + L.ws_e); }
     __device__ float* ws_o() const { return reinterpret_cast<float*>(base + L.ws_o); }
-    __device__ float* merge_w() const { return reinterpret_cast<float*>(base + L.merge_w); }
     __device__ int32_t* kind_before() const {
         return reinterpret_cast<int32_t*>(base + L.kind_before);
     }
@@ -454,6 +453,20 @@ attention_kernel(const __grid_constant__ AttnParams p,
             kb[0] = c0; kb[1] = c1; kb[2] = c2;
         }
     }
+    {  // warm L2 with the metadata read right after the wait (each line by one thread)
+        constexpr size_t kPrefetchCap = 16u << 20;
+        const int64_t gt = (int64_t)cta * kAttnThreads + tid, gn = (int64_t)G * kAttnThreads;
+        prefetch_l2_range(p.seq_lens, (size_t)p.B * 4u, gt, gn);
+        const size_t bt_bytes = (size_t)p.B * p.max_pages * 4u;
+        if (bt_bytes <= kPrefetchCap) prefetch_l2_range(p.block_table, bt_bytes, gt, gn);
+        prefetch_l2_range(p.q, (size_t)p.B * p.Hq * D * 2u, gt, gn);
+        if (p.mode == MODE_SPARSE && p.selected)
+            prefetch_l2_range(p.selected, (size_t)p.B * p.Hkv * p.top_k * 4u, gt, gn);
+        if (p.mode == MODE_PARTIAL) {
+            prefetch_l2_range(p.chunk_req, (size_t)p.C * 4u, gt, gn);
+            prefetch_l2_range(p.chunk_indptr, (size_t)(p.C + 1) * 4u, gt, gn);
+        }
+    }
     // From here on the lengths, the selection and the pool may come from the previous kernel.
     grid_dependency_wait();
     grid_launch_dependents();
@@ -687,107 +700,62 @@ attention_kernel(const __grid_constant__ AttnParams p,
             named_bar_sync(1, kCT);
             const int32_t npieces = c_last - c_first + 1;
             if (ctid == 0) {
-                __threadfence();
-                const int32_t prev = atomicAdd(p.counters + s, 1);
+                // release: this CTA's slot writes (ordered before by the barrier) become
+                // visible before the count; acquire: the last arrival sees every slot
+                const int32_t prev = atom_add_acq_rel_gpu(p.counters + s, 1);
                 *sm.last_flag() = (prev == npieces - 1) ? 1 : 0;
                 if (prev == npieces - 1) p.counters[s] = 0;  // ready for the next launch
             }
             named_bar_sync(1, kCT);
             if (*sm.last_flag()) {
-                // Merge all pieces of the segment, up to kMergeChunk per pass. Warp w turns
-                // the (m, e) of heads w, w + 4 into weights (lanes over pieces, warp-shuffle
-                // max and sum) and keeps a running max and sum across passes. Then every
-                // thread accumulates its float4 columns of MA with independent loads.
-                __threadfence();
+                // Merge all pieces of the segment. Each thread owns float4 columns of one
+                // head's MA; for up to kMergeBatch pieces at a time it loads the pieces' (m, e)
+                // of that head and its MA columns together, then folds them into a running
+                // max, sum and accumulator (the weights are recomputed per thread).
                 const float* first = p.slots + (int64_t)(c_first + s) * slot_stride;
-                float* mw = sm.merge_w();              // [kMergeChunk][g] weights of a pass
-                float* mrun = sm.ws_m();               // [g] running max
-                float* erun = sm.ws_e();               // [g] running sum
-                float* alpha = sm.ws_m() + kMaxGroup;  // [g] rescale of earlier passes
-                constexpr int kCols = (kMaxGroup * D / 4 + kCT - 1) / kCT;
-                float4 acc[kCols];
-#pragma unroll
-                for (int k = 0; k < kCols; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (ctid < p.g) {
-                    mrun[ctid] = kNegInf;
-                    erun[ctid] = 0.f;
-                }
-                named_bar_sync(1, kCT);
-                for (int32_t q0 = 0; q0 < npieces; q0 += kMergeChunk) {
-                    const int nq = min(kMergeChunk, npieces - q0);
-                    const float* pass = first + (int64_t)q0 * slot_stride;
-                    for (int j = warp; j < p.g; j += kConsumerWarps) {
-                        constexpr int kPer = kMergeChunk / 32;
-                        float mq[kPer], eq[kPer];
-#pragma unroll
-                        for (int t = 0; t < kPer; ++t) {
-                            const int q = lane + 32 * t;
-                            mq[t] = q < nq ? __ldcg(pass + (int64_t)q * slot_stride + gD + j)
-                                           : kNegInf;
-                            eq[t] = q < nq ? __ldcg(pass + (int64_t)q * slot_stride + gD + p.g + j)
-                                           : 0.f;
-                        }
-                        const float m_old = mrun[j];
-                        float mx = m_old;
-#pragma unroll
-                        for (int t = 0; t < kPer; ++t) mx = fmaxf(mx, mq[t]);
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1)
-                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                        float e = 0.f;
-#pragma unroll
-                        for (int t = 0; t < kPer; ++t) {
-                            const int q = lane + 32 * t;
-                            const float w = mq[t] == kNegInf ? 0.f : exp2f(mq[t] - mx);
-                            e += eq[t] * w;
-                            if (q < nq) mw[q * p.g + j] = w;
-                        }
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1)
-                            e += __shfl_xor_sync(0xffffffffu, e, off);
-                        if (lane == 0) {
-                            const float al = mx == kNegInf ? 0.f : exp2f(m_old - mx);
-                            erun[j] = erun[j] * al + e;
-                            mrun[j] = mx;
-                            alpha[j] = al;
-                        }
-                    }
-                    named_bar_sync(1, kCT);
-#pragma unroll
-                    for (int k = 0; k < kCols; ++k) {
-                        const int c4 = ctid + k * kCT;
-                        if (c4 >= gD / 4) break;
-                        const int j = (4 * c4) / D;
-                        const float al = alpha[j];
-                        float4 a = acc[k];
-                        a.x *= al;
-                        a.y *= al;
-                        a.z *= al;
-                        a.w *= al;
-                        const float4* col = reinterpret_cast<const float4*>(pass + 4 * c4);
-                        const int64_t step4 = slot_stride / 4;
-#pragma unroll 16
-                        for (int q = 0; q < nq; ++q) {
-                            const float w = mw[q * p.g + j];
-                            const float4 v = __ldcg(col + q * step4);
-                            a.x += w * v.x;
-                            a.y += w * v.y;
-                            a.z += w * v.z;
-                            a.w += w * v.w;
-                        }
-                        acc[k] = a;
-                    }
-                    named_bar_sync(1, kCT);
-                }
-#pragma unroll
-                for (int k = 0; k < kCols; ++k) {
-                    const int c4 = ctid + k * kCT;
-                    if (c4 >= gD / 4) break;
+                constexpr int kMergeBatch = 8;
+                for (int c4 = ctid; c4 < gD / 4; c4 += kCT) {
                     const int j = (4 * c4) / D, d = 4 * c4 - j * D;
-                    write_final(p, s, j, d, D, mrun[j], erun[j], acc[k].x);
-                    write_final(p, s, j, d + 1, D, mrun[j], erun[j], acc[k].y);
-                    write_final(p, s, j, d + 2, D, mrun[j], erun[j], acc[k].z);
-                    write_final(p, s, j, d + 3, D, mrun[j], erun[j], acc[k].w);
+                    float mrun = kNegInf, erun = 0.f;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int32_t q0 = 0; q0 < npieces; q0 += kMergeBatch) {
+                        const float* pass = first + (int64_t)q0 * slot_stride;
+                        float mq[kMergeBatch], eq[kMergeBatch];
+                        float4 vq[kMergeBatch];
+#pragma unroll
+                        for (int t = 0; t < kMergeBatch; ++t) {
+                            const bool in = q0 + t < npieces;
+                            const float* sl = pass + (int64_t)t * slot_stride;
+                            mq[t] = in ? __ldcg(sl + gD + j) : kNegInf;
+                            eq[t] = in ? __ldcg(sl + gD + p.g + j) : 0.f;
+                            vq[t] = in ? __ldcg(reinterpret_cast<const float4*>(sl + 4 * c4))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                        float mx = mrun;
+#pragma unroll
+                        for (int t = 0; t < kMergeBatch; ++t) mx = fmaxf(mx, mq[t]);
+                        if (mx == kNegInf) continue;  // every piece so far is empty
+                        const float al = mrun == kNegInf ? 0.f : exp2f(mrun - mx);
+                        erun *= al;
+                        acc.x *= al;
+                        acc.y *= al;
+                        acc.z *= al;
+                        acc.w *= al;
+#pragma unroll
+                        for (int t = 0; t < kMergeBatch; ++t) {
+                            const float w = mq[t] == kNegInf ? 0.f : exp2f(mq[t] - mx);
+                            erun += eq[t] * w;
+                            acc.x += w * vq[t].x;
+                            acc.y += w * vq[t].y;
+                            acc.z += w * vq[t].z;
+                            acc.w += w * vq[t].w;
+                        }
+                        mrun = mx;
+                    }
+                    write_final(p, s, j, d, D, mrun, erun, acc.x);
+                    write_final(p, s, j, d + 1, D, mrun, erun, acc.y);
+                    write_final(p, s, j, d + 2, D, mrun, erun, acc.z);
+                    write_final(p, s, j, d + 3, D, mrun, erun, acc.w);
                 }
             }
         }

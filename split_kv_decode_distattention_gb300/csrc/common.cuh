@@ -92,6 +92,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Atomic add at GPU scope with acquire-release semantics; returns the old value.
+__device__ __forceinline__ int32_t atom_add_acq_rel_gpu(int32_t* ptr, int32_t v) {
+    int32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(ptr), "r"(v)
+                 : "memory");
+    return old;
+}
+
+// Warms L2 with [ptr, ptr + bytes): thread gt of gthreads prefetches every gthreads-th
+// 128-byte line. A prefetch returns no data, so it may run before the dependency wait even
+// for data the previous kernel writes (L2 is where those writes land).
+__device__ __forceinline__ void prefetch_l2_range(const void* ptr, size_t bytes, int64_t gt,
+                                                  int64_t gthreads) {
+    const char* c = static_cast<const char*>(ptr);
+    for (size_t off = (size_t)gt * 128u; off < bytes; off += (size_t)gthreads * 128u)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(c + off));
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));

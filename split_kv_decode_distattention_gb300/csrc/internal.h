@@ -17,7 +17,6 @@ constexpr int kMaxKvHeads = 256;
 constexpr int kMaxGroup = 8;        // query heads per KV head
 constexpr int kMaxTopK = 256;
 constexpr int kMaxCtasPerSm = 4;    // bound used for workspace sizing with automatic splits
-constexpr int kMergeChunk = 128;    // pieces merged per pass by the last-arriving CTA
 constexpr int32_t kSegCost = 6;     // cost units per segment in the balanced split
 
 enum AttnMode : int { MODE_PARTIAL = 0, MODE_DENSE = 1, MODE_SPARSE = 2 };
@@ -61,8 +60,8 @@ __host__ __device__ inline int32_t slot_floats(int32_t g, int32_t D) {
 
 // Shared-memory layout of the attention engine, identical on host and device.
 struct AttnSmem {
-    uint32_t stage_bytes, stages, bars, meta, flags, ws_m, ws_e, ws_o, merge_w, kind_before,
-        kinds, item_start, item_len, scan, total;
+    uint32_t stage_bytes, stages, bars, meta, flags, ws_m, ws_e, ws_o, kind_before, kinds,
+        item_start, item_len, scan, total;
 };
 
 __host__ __device__ inline AttnSmem attn_smem_layout(int D, int g, int nitems, int Hkv,
@@ -77,7 +76,6 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int D, int g, int nitems, i
     s.ws_m = o;        o += kConsumerWarps * kMaxGroup * 4u;
     s.ws_e = o;        o += kConsumerWarps * kMaxGroup * 4u;
     s.ws_o = o;        o += (uint32_t)(kConsumerWarps * g * D) * 4u;
-    s.merge_w = o;     o += (uint32_t)(kMergeChunk * g) * 4u;
     s.kind_before = o; o += sparse ? (uint32_t)(Hkv + 1) * 3u * 4u : 0u;
     s.kinds = o;       o += sparse ? (uint32_t)Hkv * 4u : 0u;
     o = (o + 15u) & ~15u;

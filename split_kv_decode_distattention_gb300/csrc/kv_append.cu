@@ -55,6 +55,7 @@ kv_append_kernel(dattn_kv_layout L, uint16_t* __restrict__ k_pool, uint16_t* __r
     constexpr int VPR = D / 8;  // 8-channel chunks per (token, head) row
     const int32_t b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
     const int32_t Hkv = L.num_kv_heads, P = L.page_size;
+    if (tid == 0) prefetch_l2_range(seq_lens + b, 4u, 0, 1);  // the length is read first
     grid_dependency_wait();  // the previous kernel may still read the pool or the lengths
     grid_launch_dependents();
     // In a single-window launch the CTA takes the new tokens 0 .. T-1 whatever seq_lens

@@ -277,6 +277,13 @@ page_select_kernel(const __grid_constant__ SelParams p) {
     int32_t* scan = reinterpret_cast<int32_t*>(base + L.scan);
 
     if (tid == 0) reinterpret_cast<volatile int*>(base + L.flags)[1] = 0;  // abort flag
+    {  // warm L2 with the metadata read right after the wait (each line by one thread)
+        const int64_t gt = (int64_t)cta * NT + tid, gn = (int64_t)G * NT;
+        prefetch_l2_range(p.seq_lens, (size_t)p.B * 4u, gt, gn);
+        const size_t bt_bytes = (size_t)p.B * p.max_pages * 4u;
+        if (bt_bytes <= (16u << 20)) prefetch_l2_range(p.block_table, bt_bytes, gt, gn);
+        prefetch_l2_range(p.q, (size_t)p.B * p.Hq * D * 2u, gt, gn);
+    }
     grid_dependency_wait();  // lengths and statistics may come from the previous kernel
     grid_launch_dependents();
     // ---------------------------------------------------------------- setup
@@ -678,14 +685,13 @@ page_select_kernel(const __grid_constant__ SelParams p) {
             const int32_t c_last = split_owner(sst + slen - 1, W, Gw);
             const int32_t npieces = c_last - c_first + 1;
             if (tid == 0) {
-                __threadfence();
-                const int32_t prev = atomicAdd(p.counters + s, 1);
+                // release this CTA's list, acquire the others' if this is the last piece
+                const int32_t prev = atom_add_acq_rel_gpu(p.counters + s, 1);
                 *last_flag = (prev == npieces - 1) ? 1 : 0;
                 if (prev == npieces - 1) p.counters[s] = 0;
             }
             csync();
             if (*last_flag) {
-                __threadfence();
                 // warp w folds pieces w, w + 8, ... into its running list, then the warps'
                 // lists are merged
                 for (int i = lane; i < Kp; i += 32) wbuf[i] = 0ull;
