@@ -67,10 +67,19 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay one CUDA graph per timed step instead of eager library calls")
+    ap.add_argument("--no-info", action="store_true",
+                    help="skip the informational warm-L2 / CUDA-graph / append timings")
     ap.add_argument("--flush", action="store_true", help="flush L2 before every step")
     ap.add_argument("--profile", action="store_true",
                     help="short run for ncu: no e2e, no CPU baseline, no clock sampling")
     return ap.parse_args()
+
+
+def info_steps(args) -> int:
+    """Steps of each informational pass after the timed region (warm L2, CUDA graphs)."""
+    return 0 if (args.profile or args.no_info) else min(64, args.steps)
 
 
 def make_case(args):
@@ -88,7 +97,8 @@ def make_case(args):
         kw["B"] = args.batch
     case = W.CASES[name](seed=args.seed, **kw)
     # room for the tokens the timed and warm-up steps append
-    case.reserve_tokens = max(case.reserve_tokens, 2 * (args.steps + args.warmup) + 64)
+    case.reserve_tokens = max(case.reserve_tokens,
+                              2 * (args.steps + args.warmup + 3 * info_steps(args)) + 64)
     case._make_block_table()
     return case
 
@@ -257,7 +267,8 @@ def run_dattn(args, rank: int, world: int):
     sel = torch.full((B, case.Hkv, max(case.top_k, 1)), -1, dtype=torch.int32, device=dev)
     spc = cache.sparse_config(sel) if sparse else None
     stream = torch.cuda.current_stream()
-    total = args.warmup + args.steps
+    n_info = info_steps(args)
+    total = args.warmup + args.steps + 3 * n_info + 1
     # per-step inputs prepared up front (device-resident for the kernel timing)
     qs = [case.q(s, dev) for s in range(total)]
     per_req = [case.kv(b, case.lens[b], case.lens[b] + total, dev) for b in range(B)]
@@ -276,24 +287,52 @@ def run_dattn(args, rank: int, world: int):
     flush = L2Flush(dev)
     torch.cuda.synchronize()
 
-    def one_step(s, ev=None):
+    def pre_step(s):  # the append, and at the start of a reuse window the selection
         kn, vn = news[s]
         cache.append(kn, vn)
-        launches = 1
         if sparse and s % case.reuse == 0:
             cache.select(qs[s], sel, ws, num_splits=args.num_splits)
-            launches += 1
+            return 2
+        return 1
+
+    def dec_step(s):
+        cache.decode(qs[s], out, ws, m_g=m_g, e_g=e_g, sparse=spc, num_splits=args.num_splits)
+        return 1
+
+    def one_step(s, ev=None):
+        launches = pre_step(s)
         if ev is not None:
             ev[0].record(stream)
-        cache.decode(qs[s], out, ws, m_g=m_g, e_g=e_g, sparse=spc, num_splits=args.num_splits)
+        launches += dec_step(s)
         if ev is not None:
             ev[1].record(stream)
-        return launches + 1
+        return launches
 
     for s in range(args.warmup):
         one_step(s)
     torch.cuda.synchronize()
     lens0 = list(cache.lens)
+    # With --graph each timed step is replayed from a CUDA graph captured beforehand (one per
+    # step, as the steps' inputs differ). A step whose decode kernel is timed on its own is
+    # captured as two graphs with the events between them.
+    graphs = {}
+    if args.graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+
+        def capture(fn, s):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side, capture_error_mode="relaxed"):
+                n = fn(s)
+            return g, n
+        for i in range(args.steps):
+            s = args.warmup + i
+            if i % KERNEL_EVERY == 0:
+                graphs[s] = (capture(pre_step, s), capture(dec_step, s))
+            else:
+                graphs[s] = (capture(one_step, s),)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
     clocks = ClockSampler(dev.index) if (rank == 0 and not args.no_clocks and
                                          not args.profile) else None
     if world > 1:
@@ -316,7 +355,19 @@ def run_dattn(args, rank: int, world: int):
         if i % KERNEL_EVERY == 0:
             kev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         e0.record(stream)
-        launches += one_step(s, kev)
+        if not args.graph:
+            launches += one_step(s, kev)
+        elif kev is None:
+            (g, n), = graphs[s]
+            g.replay()
+            launches += n
+        else:
+            (g1, n1), (g2, n2) = graphs[s]
+            g1.replay()
+            kev[0].record(stream)
+            g2.replay()
+            kev[1].record(stream)
+            launches += n1 + n2
         e1.record(stream)
         lens_after = [L + i + 1 for L in lens0]
         sb = step_bytes(case, lens_after, sparse and s % case.reuse == 0)
@@ -352,10 +403,85 @@ def run_dattn(args, rank: int, world: int):
         "case": case, "lens0": lens0,
     }
 
+    # ---- information only (outside the timed region): warm L2, CUDA graphs, the append ---
+    if n_info:
+        res["info"] = run_info(args, case, cache, one_step, news, qs, ws, out, m_g, e_g, spc, sel,
+                               flush if do_flush else None, args.warmup + args.steps, n_info)
+
     # ---- end to end through the public API with host buffers (pinned) ----------------
     if not args.no_e2e and not args.profile:
         res["e2e"] = run_e2e(args, case, cache, ws, spc, sel, flush if do_flush else None, dev)
     return res
+
+
+def run_info(args, case, cache, one_step, news, qs, ws, out, m_g, e_g, spc, sel, flush, s0, n):
+    """Informational timings after the timed region, microseconds per step as mean (the
+    headline's averaging: it includes the steps that run the selection) and median:
+    - eager: eager library calls, flushed like the timed steps;
+    - graph: each step captured once in a CUDA graph and replayed, flushed likewise;
+    - warm_l2: the captured steps replayed back to back without an L2 flush;
+    - append: the kv append kernel of an eager step timed on its own."""
+    import torch
+    stream = torch.cuda.current_stream()
+    sparse = case.head_kind is not None
+
+    def stat(pairs):
+        t = sorted(a.elapsed_time(b) * 1e3 for a, b in pairs)
+        return {"mean": round(sum(t) / len(t), 2), "median": round(t[len(t) // 2], 2)}
+
+    info = {"steps": n}
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    steps, apps = [], []
+    for i in range(n):
+        s = s0 + i
+        if flush is not None:
+            flush()
+        e0, e1, e2 = ev(), ev(), ev()
+        e0.record(stream)
+        kn, vn = news[s]
+        cache.append(kn, vn)
+        e1.record(stream)
+        if sparse and s % case.reuse == 0:
+            cache.select(qs[s], sel, ws, num_splits=args.num_splits)
+        cache.decode(qs[s], out, ws, m_g=m_g, e_g=e_g, sparse=spc, num_splits=args.num_splits)
+        e2.record(stream)
+        steps.append((e0, e2))
+        apps.append((e0, e1))
+    torch.cuda.synchronize()
+    info["eager_us_per_step"] = stat(steps)
+    info["append_us"] = stat(apps)
+    # CUDA graphs: one graph per step (its inputs differ), replayed in order
+    graphs = []
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    for i in range(2 * n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side, capture_error_mode="relaxed"):
+            one_step(s0 + n + i)
+        graphs.append(g)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    steps = []
+    for g in graphs[:n]:
+        if flush is not None:
+            flush()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        steps.append((e0, e1))
+    torch.cuda.synchronize()
+    info["graph_us_per_step"] = stat(steps)
+    events = [ev() for _ in range(n + 1)]
+    events[0].record(stream)
+    for i, g in enumerate(graphs[n:]):
+        g.replay()
+        events[i + 1].record(stream)
+    torch.cuda.synchronize()
+    info["warm_l2_graph_us_per_step"] = stat(list(zip(events[:-1], events[1:])))
+    info["l2"] = ("eager and graph steps flushed like the timed steps; warm_l2 back to back"
+                  if flush is not None else "every pass back to back (steps larger than L2)")
+    return info
 
 
 def run_e2e(args, case, cache, ws, spc, sel, flush, dev):
@@ -460,8 +586,108 @@ def time_oracle(case, q, pairs, kv, nthreads):
     return time.perf_counter() - t0, nbytes, min(nthreads, len(pairs))
 
 
+def sparse_oracle_sample(case, device, n_ret: int = 2, n_str: int = 2):
+    """Host copies for the oracle's block-sparse step: full K/V of n_ret retrieval KV heads
+    and the sink and local-window tokens of n_str streaming KV heads of request 0."""
+    import oracle
+    b, L = 0, case.lens[0]
+    kinds = list(case.head_kind)
+    ret = [h for h in range(case.Hkv) if kinds[h] == 1][:n_ret]
+    strm = [h for h in range(case.Hkv) if kinds[h] == 2][:n_str]
+    q = oracle.bf16_bits(case.q(0, device))
+    kv = {h: (np.empty((L, case.d), np.uint16), np.empty((L, case.d), np.uint16)) for h in ret}
+    for t0 in range(0, L, 65536):
+        t1 = min(L, t0 + 65536)
+        K, V = case.kv(b, t0, t1, device)
+        for h in ret:
+            kv[h][0][t0:t1] = oracle.bf16_bits(K[:, h])
+            kv[h][1][t0:t1] = oracle.bf16_bits(V[:, h])
+    rows = oracle.sparse_rows(2, L, case.P, None, case.sinks, case.local)
+    for h in strm:
+        parts = [case.kv(b, int(r), int(r) + 1, device) for r in rows]
+        K = np.stack([oracle.bf16_bits(k[0, h]) for k, _ in parts])
+        V = np.stack([oracle.bf16_bits(v[0, h]) for _, v in parts])
+        kv[h] = (K, V)
+    return q, b, ret, strm, kv
+
+
+class SparseOracleStep:
+    """The oracle's block-sparse layer-step on the sampled KV heads, on host threads. A
+    retrieval head selects its pages from its keys (statistics, fp32 scores, top-K) at the
+    start of each reuse window and attends the selected tokens; a streaming head attends its
+    sinks and local window. Bytes are counted as the GPU metric counts them."""
+
+    def __init__(self, case, q, b, ret, strm, kv, nthreads):
+        from concurrent.futures import ThreadPoolExecutor
+        self.case, self.q, self.b, self.ret, self.strm, self.kv = case, q, b, ret, strm, kv
+        self.used = min(nthreads, len(ret) + len(strm))
+        self.ex = ThreadPoolExecutor(max_workers=self.used)
+        self.sels = {}
+
+    def select(self):
+        """Returns (seconds, statistics bytes scanned)."""
+        import oracle
+        c, b = self.case, self.b
+        L, g = c.lens[b], c.g
+
+        def one(h):
+            self.sels[h] = oracle.select_pages(self.q[b, h * g:(h + 1) * g], self.kv[h][0], L,
+                                               c.P, c.top_k)
+        t0 = time.perf_counter()
+        list(self.ex.map(one, self.ret))
+        return time.perf_counter() - t0, len(self.ret) * ((L + 15) // 16) * 2 * c.d * 2
+
+    def attend(self):
+        """Returns (seconds, K/V bytes of the attended tokens)."""
+        import oracle
+        c, b = self.case, self.b
+        L, g = c.lens[b], c.g
+
+        def one(h):
+            K, V = self.kv[h]
+            if h in self.ret:
+                rows = oracle.sparse_rows(1, L, c.P, self.sels[h], c.sinks, c.local)
+            else:
+                rows = np.arange(K.shape[0], dtype=np.int64)
+            for j in range(g):
+                oracle.attention(self.q[b, h * g + j], K, V, c.scale, rows=rows)
+            return rows.shape[0] * c.d * 2 * 2
+        t0 = time.perf_counter()
+        nbytes = sum(self.ex.map(one, self.ret + self.strm))
+        return time.perf_counter() - t0, nbytes
+
+    def window(self):
+        """One reuse window: a selection, then reuse steps. Returns (seconds, bytes)."""
+        secs, nbytes = self.select()
+        for _ in range(self.case.reuse):
+            s1, n1 = self.attend()
+            secs, nbytes = secs + s1, nbytes + n1
+        return secs, nbytes
+
+
+def cpu_baseline_sparse(case, device):
+    import oracle
+    oracle.load()
+    nthreads = len(os.sched_getaffinity(0))
+    q, b, ret, strm, kv = sparse_oracle_sample(case, device)
+    st = SparseOracleStep(case, q, b, ret, strm, kv, nthreads)
+    secs, nbytes = st.window()
+    windows = 1
+    while secs * st.used < 10.0 and windows < 8:
+        s2, n2 = st.window()
+        secs, nbytes, windows = secs + s2, nbytes + n2, windows + 1
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": st.used,
+            "kind": "oracle",
+            "sample": f"request 0, retrieval KV heads {ret} (selection from the keys, then "
+                      f"attention over the selected pages) and streaming KV heads {strm} "
+                      f"(sinks and local window), {case.g} query heads each; {windows} reuse "
+                      f"window(s) of 1 selection + {case.reuse} steps, {secs:.1f} s wall"}
+
+
 def cpu_baseline(case, device):
     import oracle
+    if case.head_kind is not None:
+        return cpu_baseline_sparse(case, device)
     oracle.load()
     nthreads = len(os.sched_getaffinity(0))
     per_pair = max(1, sum(case.lens) // case.B) * case.d * 4
@@ -480,6 +706,39 @@ def cpu_baseline(case, device):
                       f"repeated {reps}x: {secs:.1f} s wall on {used} threads"}
 
 
+def run_reference_sparse(args, world, case, device, nthreads):
+    q, b, ret, strm, kv = sparse_oracle_sample(case, device)
+    st = SparseOracleStep(case, q, b, ret, strm, kv, nthreads)
+    st.select()
+    for _ in range(min(args.warmup, 1)):
+        st.attend()
+    secs, nbytes = 0.0, 0.0
+    for i in range(args.steps):  # a selection at the start of every reuse window
+        if i % case.reuse == 0:
+            s1, n1 = st.select()
+            secs, nbytes = secs + s1, nbytes + n1 / case.reuse * min(case.reuse, args.steps - i)
+        s1, n1 = st.attend()
+        secs, nbytes = secs + s1, nbytes + n1
+    value = nbytes / secs / 1e9
+    # a layer-step is the whole batch: scale the sampled heads to every (request, KV head)
+    us_step = secs / args.steps * (case.B * case.Hkv / (len(ret) + len(strm))) * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "us_per_layer_step": round(us_step, 1),
+        "config": config_obj(case, args),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": st.used,
+                         "kind": "oracle",
+                         "sample": f"request 0, retrieval KV heads {ret} and streaming KV heads "
+                                   f"{strm} per step, a selection every {case.reuse} steps"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, rank, world):
     """The CPU oracle timed on the host cores, on a bounded sample of the same workload."""
     import oracle
@@ -490,6 +749,9 @@ def run_reference(args, rank, world):
     case = make_case(args)
     device = "cuda" if torch.cuda.is_available() else "cpu"
     nthreads = len(os.sched_getaffinity(0))
+    if case.head_kind is not None:
+        run_reference_sparse(args, world, case, device, nthreads)
+        return
     per_pair = max(1, sum(case.lens) // case.B) * case.d * 4
     budget = max(nthreads, min(case.B * case.Hq, int(1e9 // per_pair)))
     q, pairs, kv = oracle_sample(case, device, budget)
@@ -530,7 +792,9 @@ def config_obj(case, args):
          "parallelism": "replicas" if args.gpus > 1 else "single GPU",
          "step": ("dattn_kv_append (1 token/request) + dattn_decode" +
                   (" + dattn_page_select every 16 steps (block-sparse)"
-                   if case.head_kind is not None else ""))}
+                   if case.head_kind is not None else "")),
+         "launch": ("one CUDA graph per step, captured from the library calls"
+                    if getattr(args, "graph", False) else "eager library calls")}
     if args.batch or args.ctx:
         c["reduced_for_profiling"] = True
     return c
@@ -590,6 +854,8 @@ def main():
         "clocks": res["clocks"],
         "cpu_baseline": cpu,
     }
+    if "info" in res:
+        line["info"] = res["info"]
     if "e2e" in res:
         line["e2e"] = res["e2e"]
     print(json.dumps(line), flush=True)
