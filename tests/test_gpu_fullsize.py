@@ -13,6 +13,8 @@ from split_kv_decode_distattention_gb300 import workloads as W
 from _util import assert_e_close, assert_m_close, assert_out_close
 
 pytestmark = pytest.mark.gpu
+# every workload is also run with seeds 1 and 2
+SEEDS = [0, 1, 2]
 DEV = "cuda"
 
 
@@ -74,10 +76,11 @@ def _step(cache, case, sparse=None):
     return q, out, m_g, e_g
 
 
-def test_mha_32k_batch8_full_size():
+@pytest.mark.parametrize("seed", SEEDS)
+def test_mha_32k_batch8_full_size(seed):
     """Llama-2-7B MHA: batch 8, 32 heads, d 128, 32K tokens, shuffled 16-token pages."""
     _lib()
-    case = W.mha_32k(seed=0)
+    case = W.mha_32k(seed=seed)
     cache = _cache(case)
     q, out, m_g, e_g = _step(cache, case)
     assert torch.isfinite(out).all()
@@ -91,19 +94,21 @@ def test_mha_32k_batch8_full_size():
     assert torch.equal(cache.v_pool[page, :, pos % case.P], V1[0])
 
 
-def test_mha_1m_single_request_full_size():
+@pytest.mark.parametrize("seed", SEEDS)
+def test_mha_1m_single_request_full_size(seed):
     """One request of 2^20 tokens, 32 heads MHA, 64 needle keys; split across all SMs."""
     _lib()
-    case = W.mha_1m(seed=0)
+    case = W.mha_1m(seed=seed)
     cache = _cache(case)
     q, out, m_g, e_g = _step(cache, case)
     _check_pairs(case, q, cache.lens, out, m_g, e_g, [(0, 0), (0, 13), (0, 31)], "mha-1m")
 
 
-def test_gqa_ragged_full_size_and_page_set_merge():
+@pytest.mark.parametrize("seed", SEEDS)
+def test_gqa_ragged_full_size_and_page_set_merge(seed):
     """64 requests, 32 q / 8 KV heads, lengths 1K-256K; page-set partials merge to fused."""
     dattn = _lib()
-    case = W.gqa_ragged(seed=0)
+    case = W.gqa_ragged(seed=seed)
     cache = _cache(case)
     q, out, m_g, e_g = _step(cache, case)
     order = np.argsort(case.lens)
@@ -139,10 +144,11 @@ def test_gqa_ragged_full_size_and_page_set_merge():
     np.testing.assert_allclose(me.cpu().numpy(), e_g.cpu().numpy(), rtol=1e-4)
 
 
-def test_sparse_512k_full_size():
+@pytest.mark.parametrize("seed", SEEDS)
+def test_sparse_512k_full_size(seed):
     """LServe block-sparse: batch 8, 32 q / 8 KV heads, 512K, 64-token pages, top-64."""
     _lib()
-    case = W.sparse_512k(seed=0)
+    case = W.sparse_512k(seed=seed)
     cache = _cache(case, with_stats=True)
     kn, vn = cache.new_tokens(1)
     cache.append(kn, vn)  # the first step of the window appends, then selects

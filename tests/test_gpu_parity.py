@@ -146,10 +146,11 @@ def test_decode_after_append_step_includes_new_token():
 
 # ---------------------------------------------------------------- partial + merge
 
-def test_dense_tiny_partial_then_merge():
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_dense_tiny_partial_then_merge(seed):
     """Batch 1, 8 q / 2 KV heads, d 64, 4096 tokens, 4 chunks of 1024 (identity table)."""
     dattn = _lib()
-    case = W.dense_tiny(seed=0)
+    case = W.dense_tiny(seed=seed)
     cache = _cache(case)
     q = case.q(0, DEV)
     pages_per_chunk = case.chunk_tokens // case.P

@@ -1,0 +1,116 @@
+"""The pins must catch a wrong oracle.
+
+Each case plants one plausible mistake in a copy of the oracle's C source: a dropped term, a
+wrong sign, an off-by-one index, a swapped operand or a reversed tie rule (none of them
+writes outside its buffers). It builds that copy and runs every pin of test_oracle_pins.py
+against it, and at least one pin must fail. The mistakes live only in the temporary copy;
+the oracle itself is untouched.
+"""
+import inspect
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+# (name, text in dattn_oracle.c, replacement)
+MUTATIONS = [
+    ("logit without the scale", "    return scale * acc;\n}", "    return acc;\n}"),
+    ("attention drops the last key",
+     "    for (int64_t i = 0; i < n; ++i) e += exp(s[i] - m);",
+     "    for (int64_t i = 0; i + 1 < n; ++i) e += exp(s[i] - m);"),
+    ("partial weights with the wrong sign",
+     "        const double w = exp(s[i] - m);\n        const uint16_t *v",
+     "        const double w = exp(m - s[i]);\n        const uint16_t *v"),
+    ("merge weights with the wrong sign", "            const double w = exp(m[j] - mg);",
+     "            const double w = exp(mg - m[j]);"),
+    ("merge forgets e_j", "            eg += e[j] * w;", "            eg += w;"),
+    ("merged partial normalised twice", "        if (MA_g) MA_g[c] = acc[c];",
+     "        if (MA_g) MA_g[c] = eg > 0.0 ? acc[c] / eg : 0.0;"),
+    ("kv write one slot late", "        const int64_t slot = pos % P;",
+     "        const int64_t slot = (pos + 1) % P;"),
+    ("kv write does not count skipped tokens",
+     "        if (page < 0 || page >= num_pages) { ++skipped; continue; }",
+     "        if (page < 0 || page >= num_pages) { continue; }"),
+    ("stats min uses max", "            if (bf16_to_float(k) < bf16_to_float(lo)) lo = k;",
+     "            if (bf16_to_float(k) > bf16_to_float(lo)) lo = k;"),
+    ("stats miss the last token of a page", "        for (int64_t t = t0 + 1; t < t1; ++t) {",
+     "        for (int64_t t = t0 + 1; t + 1 < t1; ++t) {"),
+    ("score ignores k_min", "        acc += a > b ? a : b;", "        acc += a;"),
+    ("fp32 score pairs k_min with the positive part",
+     "        x[nch + c] = decision_partial(q, kmin, c * w, w, 1);",
+     "        x[nch + c] = decision_partial(q, kmin, c * w, w, 0);"),
+    ("physical score keeps the last logical page", "                    if (s > best) best = s;",
+     "                    best = s;"),
+    ("top-K ties go to the higher page",
+     "            if (best < 0 || score[i] > score[best]) best = i; /* strict: lower index wins ties */",
+     "            if (best < 0 || score[i] >= score[best]) best = i;"),
+    ("top-K output not sorted", "        while (j >= 0 && sel[j] > v) { sel[j + 1] = sel[j]; --j; }",
+     "        while (0) { sel[j + 1] = sel[j]; --j; }"),
+    ("streaming window one token short", "        int64_t l0 = L - local;",
+     "        int64_t l0 = L - local + 1;"),
+    ("retrieval rows skip the partial last page",
+     "            for (int64_t t = p * P; t < (p + 1) * P && t < L; ++t) rows[n++] = t;",
+     "            if ((p + 1) * P > L) continue;\n"
+     "            for (int64_t t = p * P; t < (p + 1) * P && t < L; ++t) rows[n++] = t;"),
+]
+
+
+def _pin_calls():
+    """Every pin of test_oracle_pins as a list of zero-argument callables."""
+    calls = []
+    for name, fn in inspect.getmembers(pins, inspect.isfunction):
+        if not name.startswith("test_"):
+            continue
+        params = list(inspect.signature(fn).parameters)
+        marks = getattr(fn, "pytestmark", [])
+        grids = [m.args for m in marks if m.name == "parametrize"]
+        combos = [{}]
+        for argnames, values in grids:
+            names = [a.strip() for a in argnames.split(",")]
+            new = []
+            for c in combos:
+                for v in values:
+                    vv = v if len(names) > 1 else (v,)
+                    new.append({**c, **dict(zip(names, vv))})
+            combos = new
+        for c in combos:
+            kwargs = dict(c)
+            if "orc" in params:
+                kwargs["orc"] = oracle
+            calls.append((f"{name}{c or ''}", lambda fn=fn, kw=kwargs: fn(**kw)))
+    return calls
+
+
+@pytest.fixture(scope="module")
+def source():
+    here = os.path.dirname(oracle.__file__)
+    with open(os.path.join(here, "dattn_oracle.c")) as f:
+        return f.read(), here
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_planted_mistake(source, tmp_path, name, old, new):
+    src, here = source
+    assert src.count(old) == 1, f"the mutation anchor for '{name}' must occur exactly once"
+    shutil.copy(os.path.join(here, "dattn_oracle.h"), tmp_path / "dattn_oracle.h")
+    (tmp_path / "dattn_oracle.c").write_text(src.replace(old, new))
+    lib_path = str(tmp_path / "libmutant.so")
+    subprocess.run(["gcc", *oracle.CFLAGS, str(tmp_path / "dattn_oracle.c"), "-o", lib_path,
+                    "-lm"], check=True, cwd=tmp_path)
+    mutant = oracle.load(lib_path)
+    saved = oracle._lib
+    oracle._lib = mutant  # the oracle's functions now call the mutant
+    failed = []
+    try:
+        for label, call in _pin_calls():
+            try:
+                call()
+            except AssertionError:
+                failed.append(label)
+    finally:
+        oracle._lib = saved
+    assert failed, f"no pin failed for the planted mistake: {name}"
