@@ -65,6 +65,13 @@ _SIGS = {
     "orc_topk": (None, [_P, _I64, _I, _P]),
     "orc_sparse_rows": (_I64, [_I, _I64, _I, _P, _I, _I, _I, _P]),
     "orc_attention_pairs_mt": (_I, [_P, _P, _P, _P, _I, _I, _I, _D, _P, _I64, _I, _P, _P, _P]),
+    "orc_e4m3_value": (_D, [ctypes.c_uint8]),
+    "orc_e4m3_code": (ctypes.c_uint8, [ctypes.c_float]),
+    "orc_quantize_row_fp8": (None, [_P, _I, _P, _P]),
+    "orc_dequantize_row_fp8": (None, [_P, ctypes.c_float, _I, _P]),
+    "orc_kv_write_fp8": (_I64, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _I64, _I64]),
+    "orc_attention_f64": (None, [_P, _P, _P, _I64, _I, _P, _I64, _D, _P, _P, _P]),
+    "orc_partial_f64": (None, [_P, _P, _P, _I64, _I, _P, _I64, _D, _P, _P, _P]),
 }
 
 
@@ -272,3 +279,88 @@ def attention_pairs(q, K_cat, V_cat, offs, pairs, scale: float, nthreads: int | 
                                       scale, _ptr(pairs), n, nthreads, _ptr(out), _ptr(m),
                                       _ptr(e))
     return out, m, e, used
+
+
+# ----------------------------------------------------------------- 8-bit KV (reading R10)
+
+def e4m3_value(code: int, lib=None) -> float:
+    """Value of an FP8 E4M3 code."""
+    return float((lib or load()).orc_e4m3_value(int(code)))
+
+
+def e4m3_code(f: float, lib=None) -> int:
+    """E4M3 code of a float (rounded to fp32 first): nearest, ties to even, saturating."""
+    return int((lib or load()).orc_e4m3_code(float(np.float32(f))))
+
+
+def quantize_rows_fp8(X, lib=None):
+    """Rows of bf16 values ([n][d] or [d]) -> (codes uint8 [n][d], scales float32 [n])."""
+    lib = lib or load()
+    X = bf16_bits(X)
+    d = X.shape[-1]
+    X2 = np.ascontiguousarray(X.reshape(-1, d))
+    codes = np.zeros(X2.shape, np.uint8)
+    scales = np.zeros(X2.shape[0], np.float32)
+    for r in range(X2.shape[0]):
+        lib.orc_quantize_row_fp8(_ptr(X2[r]), d, _ptr(codes[r]), _ptr(scales[r:r + 1]))
+    return codes.reshape(X.shape), scales.reshape(X.shape[:-1])
+
+
+def dequantize_rows_fp8(codes, scales, lib=None) -> np.ndarray:
+    """code * scale of every row, in float64."""
+    lib = lib or load()
+    codes = np.ascontiguousarray(codes, np.uint8)
+    d = codes.shape[-1]
+    c2 = codes.reshape(-1, d)
+    s2 = np.ascontiguousarray(np.asarray(scales, np.float32).reshape(-1))
+    out = np.zeros(c2.shape, np.float64)
+    for r in range(c2.shape[0]):
+        lib.orc_dequantize_row_fp8(_ptr(c2[r]), float(s2[r]), d, _ptr(out[r]))
+    return out.reshape(codes.shape)
+
+
+def kv_write_fp8(k_pool, v_pool, k_scale, v_scale, P: int, block_table_row, num_pages: int,
+                 k_new, v_new, pos0: int, lib=None) -> int:
+    """Paged 8-bit write of k_new/v_new ([T][Hkv][d] bf16) into uint8 pools
+    [num_pages][Hkv][P][d] and float32 scales [num_pages][Hkv][P]; returns skipped tokens."""
+    lib = lib or load()
+    k_new, v_new = bf16_bits(k_new), bf16_bits(v_new)
+    T, Hkv, d = k_new.shape
+    bt = np.ascontiguousarray(np.asarray(block_table_row, np.int32))
+    return int(lib.orc_kv_write_fp8(_ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), Hkv,
+                                    P, d, _ptr(bt), bt.shape[0], num_pages, _ptr(k_new),
+                                    _ptr(v_new), pos0, T))
+
+
+def attention_f64(q, K, V, scale: float, rows=None, lib=None):
+    """orc_attention over float64 keys and values ([n][d]): (out [d], m, e)."""
+    lib = lib or load()
+    q = bf16_bits(q)
+    K2 = np.ascontiguousarray(np.asarray(K, np.float64))
+    V2 = np.ascontiguousarray(np.asarray(V, np.float64))
+    d = q.shape[-1]
+    r = _rows(rows)
+    n = K2.shape[0] if r is None else r.shape[0]
+    out = np.zeros(d, np.float64)
+    m = ctypes.c_double()
+    e = ctypes.c_double()
+    lib.orc_attention_f64(_ptr(q), _ptr(K2), _ptr(V2), d, d, _ptr(r), n, scale, _ptr(out),
+                          ctypes.byref(m), ctypes.byref(e))
+    return out, m.value, e.value
+
+
+def partial_f64(q, K, V, scale: float, rows=None, lib=None):
+    """orc_partial over float64 keys and values: (m_j, e_j, MA_j [d])."""
+    lib = lib or load()
+    q = bf16_bits(q)
+    K2 = np.ascontiguousarray(np.asarray(K, np.float64))
+    V2 = np.ascontiguousarray(np.asarray(V, np.float64))
+    d = q.shape[-1]
+    r = _rows(rows)
+    n = K2.shape[0] if r is None else r.shape[0]
+    MA = np.zeros(d, np.float64)
+    m = ctypes.c_double()
+    e = ctypes.c_double()
+    lib.orc_partial_f64(_ptr(q), _ptr(K2), _ptr(V2), d, d, _ptr(r), n, scale, ctypes.byref(m),
+                        ctypes.byref(e), _ptr(MA))
+    return m.value, e.value, MA

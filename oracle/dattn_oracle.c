@@ -43,6 +43,11 @@
  *  R9  The page selection is decided in the kernel's arithmetic: fp32 in a fixed order
  *      (see orc_logical_score_f32). The fp64 score is the definition, and the tests
  *      check that the two differ by less than the fp32 error bound.
+ *  R10 The 8-bit KV cache: the pages give retrieval heads 2-8 bit configurable quantization
+ *      and no scheme. Here: FP8 E4M3 codes with one fp32 scale per (token, KV head) row of
+ *      K and of V, scale = max|x| / 448, code = E4M3(x / scale) rounded to nearest even;
+ *      attention runs over code * scale. Statistics for page selection are still taken
+ *      from the bf16 keys as written.
  */
 #include "dattn_oracle.h"
 
@@ -395,6 +400,165 @@ int64_t orc_sparse_rows(int kind, int64_t L, int P, const int32_t *sel, int top_
         for (int64_t t = l0; t < L; ++t) rows[n++] = t;
     }
     return n;
+}
+
+/* ---- 8-bit KV cache (reading R10): FP8 E4M3 codes with one fp32 scale per row ---------- */
+
+/*
+ * Value of an E4M3 code (the OCP 8-bit floating-point format: 1 sign bit, 4 exponent bits
+ * with bias 7, 3 mantissa bits; exponent field 0 holds the subnormals mantissa/8 * 2^-6;
+ * there are no infinities, and S.1111.111 is NaN).
+ */
+double orc_e4m3_value(uint8_t code)
+{
+    const int sgn = code >> 7, ef = (code >> 3) & 15, mf = code & 7;
+    if (ef == 15 && mf == 7) return NAN;
+    const double v = ef == 0 ? ldexp((double)mf, -9) : ldexp(8.0 + mf, ef - 10);
+    return sgn ? -v : v;
+}
+
+/*
+ * E4M3 code of a finite float: round to the nearest representable value, ties to the even
+ * mantissa, and saturate at the largest finite magnitude 448 (code 0x7E). The sign of a
+ * result that rounds to zero is kept.
+ */
+uint8_t orc_e4m3_code(float f)
+{
+    const uint8_t sgn = signbit(f) ? 0x80 : 0x00;
+    const double a = fabs((double)f);
+    if (a == 0.0) return sgn;
+    int e;
+    frexp(a, &e);
+    int E = e - 1; /* a = (1.mmm...) * 2^E */
+    if (E < -6) {  /* subnormal range: multiples of 2^-9 */
+        const int n = (int)rint(a / ldexp(1.0, -9)); /* 0 .. 8, ties to even */
+        return sgn | (uint8_t)(n == 8 ? 0x08 : n);  /* 8 * 2^-9 is the smallest normal */
+    }
+    int n = (int)rint(a / ldexp(1.0, E - 3)); /* 8 .. 16: 1 + mantissa/8 in units of 1/8 */
+    if (n == 16) {
+        n = 8;
+        E += 1;
+    }
+    if (E > 8 || (E == 8 && n > 14)) return sgn | 0x7E; /* saturate at 448 */
+    return sgn | (uint8_t)(((E + 7) << 3) | (n - 8));
+}
+
+/*
+ * One row of d bf16 values in the 8-bit format: scale = max_c |x_c| / 448 and
+ * code_c = E4M3(x_c / scale), both divisions in IEEE fp32. A row whose scale is 0 has +0
+ * codes. The row's values are code * scale.
+ */
+void orc_quantize_row_fp8(const uint16_t *x, int d, uint8_t *codes, float *scale)
+{
+    float mx = 0.0f;
+    for (int c = 0; c < d; ++c) {
+        const float v = fabsf(bf16_to_float(x[c]));
+        if (v > mx) mx = v;
+    }
+    const float s = mx / 448.0f;
+    *scale = s;
+    for (int c = 0; c < d; ++c) codes[c] = s > 0.0f ? orc_e4m3_code(bf16_to_float(x[c]) / s) : 0;
+}
+
+/* code * scale of one row, exactly (an E4M3 value times an fp32 value fits in a double). */
+void orc_dequantize_row_fp8(const uint8_t *codes, float scale, int d, double *out)
+{
+    for (int c = 0; c < d; ++c) out[c] = orc_e4m3_value(codes[c]) * (double)scale;
+}
+
+/*
+ * Paged write of T new tokens in the 8-bit format [LS §4.2, with reading R10]: the codes of
+ * each (token, KV head) row go to k_pool / v_pool [num_pages][Hkv][P][d] and its scale to
+ * k_scale / v_scale [num_pages][Hkv][P], at the place orc_kv_write uses. Returns the number
+ * of skipped tokens, as orc_kv_write does.
+ */
+int64_t orc_kv_write_fp8(uint8_t *k_pool, uint8_t *v_pool, float *k_scale, float *v_scale,
+                         int Hkv, int P, int d, const int32_t *block_table_row, int max_pages,
+                         int num_pages, const uint16_t *k_new, const uint16_t *v_new,
+                         int64_t pos0, int64_t T)
+{
+    int64_t skipped = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t pos = pos0 + t;
+        const int64_t lp = pos / P;
+        if (lp >= max_pages) { ++skipped; continue; }
+        const int32_t page = block_table_row[lp];
+        if (page < 0 || page >= num_pages) { ++skipped; continue; }
+        for (int h = 0; h < Hkv; ++h) {
+            const int64_t row = ((int64_t)page * Hkv + h) * P + pos % P;
+            const int64_t src = (t * Hkv + h) * (int64_t)d;
+            orc_quantize_row_fp8(k_new + src, d, k_pool + row * d, k_scale + row);
+            orc_quantize_row_fp8(v_new + src, d, v_pool + row * d, v_scale + row);
+        }
+    }
+    return skipped;
+}
+
+/*
+ * orc_attention and orc_partial over keys and values given as doubles (row r of K and V
+ * starts at K + r * row_stride): the same equations, for the dequantized 8-bit format.
+ */
+static double logit_f64(const uint16_t *q, const double *k, int d, double scale)
+{
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) acc += orc_bf16_to_double(q[c]) * k[c];
+    return scale * acc;
+}
+
+void orc_attention_f64(const uint16_t *q, const double *K, const double *V, int64_t row_stride,
+                       int d, const int64_t *rows, int64_t n, double scale, double *out,
+                       double *m_out, double *e_out)
+{
+    for (int c = 0; c < d; ++c) out[c] = 0.0;
+    if (n <= 0) {
+        *m_out = -INFINITY;
+        *e_out = 0.0;
+        return;
+    }
+    double *s = (double *)malloc((size_t)n * sizeof(double));
+    double m = -INFINITY;
+    for (int64_t i = 0; i < n; ++i) {
+        s[i] = logit_f64(q, K + row_of(rows, i) * row_stride, d, scale);
+        if (s[i] > m) m = s[i];
+    }
+    double e = 0.0;
+    for (int64_t i = 0; i < n; ++i) e += exp(s[i] - m);
+    for (int64_t i = 0; i < n; ++i) {
+        const double w = exp(s[i] - m) / e;
+        const double *v = V + row_of(rows, i) * row_stride;
+        for (int c = 0; c < d; ++c) out[c] += w * v[c];
+    }
+    free(s);
+    *m_out = m;
+    *e_out = e;
+}
+
+void orc_partial_f64(const uint16_t *q, const double *K, const double *V, int64_t row_stride,
+                     int d, const int64_t *rows, int64_t n, double scale, double *m_j,
+                     double *e_j, double *MA_j)
+{
+    for (int c = 0; c < d; ++c) MA_j[c] = 0.0;
+    if (n <= 0) {
+        *m_j = -INFINITY;
+        *e_j = 0.0;
+        return;
+    }
+    double *s = (double *)malloc((size_t)n * sizeof(double));
+    double m = -INFINITY;
+    for (int64_t i = 0; i < n; ++i) {
+        s[i] = logit_f64(q, K + row_of(rows, i) * row_stride, d, scale);
+        if (s[i] > m) m = s[i];
+    }
+    double e = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        const double w = exp(s[i] - m);
+        const double *v = V + row_of(rows, i) * row_stride;
+        e += w;
+        for (int c = 0; c < d; ++c) MA_j[c] += w * v[c];
+    }
+    free(s);
+    *m_j = m;
+    *e_j = e;
 }
 
 /* ---- batch driver: plain attention over many (request, head) pairs on host threads ---- */

@@ -44,6 +44,27 @@ void orc_topk(const double *score, int64_t n, int top_k, int32_t *sel);
 int64_t orc_sparse_rows(int kind, int64_t L, int P, const int32_t *sel, int top_k, int sinks,
                         int local, int64_t *rows);
 
+double orc_e4m3_value(uint8_t code);
+
+uint8_t orc_e4m3_code(float f);
+
+void orc_quantize_row_fp8(const uint16_t *x, int d, uint8_t *codes, float *scale);
+
+void orc_dequantize_row_fp8(const uint8_t *codes, float scale, int d, double *out);
+
+int64_t orc_kv_write_fp8(uint8_t *k_pool, uint8_t *v_pool, float *k_scale, float *v_scale,
+                         int Hkv, int P, int d, const int32_t *block_table_row, int max_pages,
+                         int num_pages, const uint16_t *k_new, const uint16_t *v_new,
+                         int64_t pos0, int64_t T);
+
+void orc_attention_f64(const uint16_t *q, const double *K, const double *V, int64_t row_stride,
+                       int d, const int64_t *rows, int64_t n, double scale, double *out,
+                       double *m_out, double *e_out);
+
+void orc_partial_f64(const uint16_t *q, const double *K, const double *V, int64_t row_stride,
+                     int d, const int64_t *rows, int64_t n, double scale, double *m_j,
+                     double *e_j, double *MA_j);
+
 int orc_attention_pairs_mt(const uint16_t *q, const uint16_t *K, const uint16_t *V,
                            const int64_t *offs, int Hq, int Hkv, int d, double scale,
                            const int32_t *pairs, int64_t npairs, int nthreads, double *out,

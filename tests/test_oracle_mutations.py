@@ -3,8 +3,8 @@
 Each case plants one plausible mistake in a copy of the oracle's C source: a dropped term, a
 wrong sign, an off-by-one index, a swapped operand or a reversed tie rule (none of them
 writes outside its buffers). It builds that copy and runs every pin of test_oracle_pins.py
-against it, and at least one pin must fail. The mistakes live only in the temporary copy;
-the oracle itself is untouched.
+and test_oracle_fp8.py against it, and at least one pin must fail. The mistakes live only in
+the temporary copy; the oracle itself is untouched.
 """
 import inspect
 import os
@@ -14,14 +14,19 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_fp8 as pins_fp8
 import test_oracle_pins as pins
 
 # (name, text in dattn_oracle.c, replacement)
 MUTATIONS = [
-    ("logit without the scale", "    return scale * acc;\n}", "    return acc;\n}"),
+    ("logit without the scale",
+     "        acc += orc_bf16_to_double(q[c]) * orc_bf16_to_double(k[c]);\n    return scale * acc;",
+     "        acc += orc_bf16_to_double(q[c]) * orc_bf16_to_double(k[c]);\n    return acc;"),
     ("attention drops the last key",
-     "    for (int64_t i = 0; i < n; ++i) e += exp(s[i] - m);",
-     "    for (int64_t i = 0; i + 1 < n; ++i) e += exp(s[i] - m);"),
+     "    for (int64_t i = 0; i < n; ++i) e += exp(s[i] - m);\n    for (int64_t i = 0; i < n; ++i) {\n"
+     "        const double w = exp(s[i] - m) / e;\n        const uint16_t *v",
+     "    for (int64_t i = 0; i + 1 < n; ++i) e += exp(s[i] - m);\n    for (int64_t i = 0; i < n; ++i) {\n"
+     "        const double w = exp(s[i] - m) / e;\n        const uint16_t *v"),
     ("partial weights with the wrong sign",
      "        const double w = exp(s[i] - m);\n        const uint16_t *v",
      "        const double w = exp(m - s[i]);\n        const uint16_t *v"),
@@ -33,8 +38,8 @@ MUTATIONS = [
     ("kv write one slot late", "        const int64_t slot = pos % P;",
      "        const int64_t slot = (pos + 1) % P;"),
     ("kv write does not count skipped tokens",
-     "        if (page < 0 || page >= num_pages) { ++skipped; continue; }",
-     "        if (page < 0 || page >= num_pages) { continue; }"),
+     "        if (page < 0 || page >= num_pages) { ++skipped; continue; }\n        const int64_t slot",
+     "        if (page < 0 || page >= num_pages) { continue; }\n        const int64_t slot"),
     ("stats min uses max", "            if (bf16_to_float(k) < bf16_to_float(lo)) lo = k;",
      "            if (bf16_to_float(k) > bf16_to_float(lo)) lo = k;"),
     ("stats miss the last token of a page", "        for (int64_t t = t0 + 1; t < t1; ++t) {",
@@ -52,6 +57,13 @@ MUTATIONS = [
      "        while (0) { sel[j + 1] = sel[j]; --j; }"),
     ("streaming window one token short", "        int64_t l0 = L - local;",
      "        int64_t l0 = L - local + 1;"),
+    ("E4M3 rounds half away from zero", "    int n = (int)rint(a / ldexp(1.0, E - 3));",
+     "    int n = (int)round(a / ldexp(1.0, E - 3));"),
+    ("8-bit scale over 127 instead of 448", "    const float s = mx / 448.0f;",
+     "    const float s = mx / 127.0f;"),
+    ("8-bit write stores the V scale in the K scale pool",
+     "            orc_quantize_row_fp8(v_new + src, d, v_pool + row * d, v_scale + row);",
+     "            orc_quantize_row_fp8(v_new + src, d, v_pool + row * d, k_scale + row);"),
     ("retrieval rows skip the partial last page",
      "            for (int64_t t = p * P; t < (p + 1) * P && t < L; ++t) rows[n++] = t;",
      "            if ((p + 1) * P > L) continue;\n"
@@ -60,9 +72,11 @@ MUTATIONS = [
 
 
 def _pin_calls():
-    """Every pin of test_oracle_pins as a list of zero-argument callables."""
+    """Every pin of the oracle's pin modules as a list of zero-argument callables."""
     calls = []
-    for name, fn in inspect.getmembers(pins, inspect.isfunction):
+    fns = inspect.getmembers(pins, inspect.isfunction) + \
+        inspect.getmembers(pins_fp8, inspect.isfunction)
+    for name, fn in fns:
         if not name.startswith("test_"):
             continue
         params = list(inspect.signature(fn).parameters)
