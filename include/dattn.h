@@ -1,5 +1,6 @@
 /*
- * dattn: split-KV decode attention over a paged bf16 KV cache, for GB300 (sm_103a).
+ * dattn: split-KV decode attention over a paged KV cache (bf16, or 8-bit FP8 E4M3 codes with
+ * one fp32 scale per row), for GB300 (sm_103a).
  *
  * The C ABI of libdattn.so. Every entry point takes plain pointers and sizes: no C++ and
  * no framework types. It validates its arguments on the host, then launches asynchronously
@@ -29,6 +30,8 @@
  *       KV cache is written, a physical page is scored as the max over its logical pages,
  *       and the top-K pages are selected. §3.1.1: streaming heads attend sink tokens plus
  *       a local window. The streaming and retrieval heads run in one fused kernel.
+ *       §3.2.1: the retrieval-head cache is paged and quantized at a configurable 2-8 bits,
+ *       with no scheme given; the 8-bit format below is this library's reading of it.
  *
  * Here the "instances" are CTAs on one GPU. The KV of every (request, KV head) is split
  * into 16-token tiles. The tiles are spread evenly over num_splits CTAs, so each CTA
@@ -44,8 +47,16 @@
  *  - Device pointers are marked (device). Structs passed by pointer live in host memory.
  *  - Sequence length L_b = seq_lens[b]: tokens 0..L_b-1 of request b are valid. Token t
  *    lives in physical page block_table[b * max_pages_per_req + t / P], slot t % P.
- *  - Pool layout: k_pool and v_pool are [num_pages][Hkv][P][d]. Every (page, KV head)
- *    tile is one contiguous P*d run.
+ *  - Pool layout: k_pool and v_pool are [num_pages][Hkv][P][d] elements of the layout's
+ *    kv_format. Every (page, KV head) tile is one contiguous P*d run.
+ *  - The 8-bit format (kv_format = DATTN_KV_FP8_E4M3): every (token, KV head) row x of d
+ *    values is stored as d one-byte codes plus one fp32 scale in k_scale / v_scale
+ *    [num_pages][Hkv][P] (the same place as the row, without d). scale = max_i |x_i| / 448
+ *    and code_i = E4M3(x_i / scale), both divisions in IEEE fp32; E4M3 is the OCP 8-bit
+ *    float (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, largest finite 448),
+ *    rounded to nearest even and saturated to +-448. A row with scale 0 has +0 codes. The
+ *    row's values are code_i * scale, and the attention runs over exactly these values.
+ *    The query stays bf16; the statistics are still taken from the bf16 keys.
  *  - Statistics layout: stats is [num_pages][Hkv][P/16][2][d]. Entry [..][lp][0][:] is
  *    k_max and [..][lp][1][:] is k_min of logical page lp, the 16 tokens
  *    lp*16..lp*16+15 of that physical page.
@@ -95,7 +106,12 @@ typedef enum {
 #define DATTN_HEAD_RETRIEVAL 1
 #define DATTN_HEAD_STREAMING 2
 
-/* Shape of the paged KV pool and the block table. */
+/* Element formats of the KV pool (dattn_kv_layout.kv_format). */
+#define DATTN_KV_BF16 0      /* bf16 values */
+#define DATTN_KV_FP8_E4M3 1  /* FP8 E4M3 codes with one fp32 scale per (token, KV head) row */
+
+/* Shape of the paged KV pool and the block table. A zero-initialised tail (kv_format 0,
+ * NULL scales) is the bf16 pool. */
 typedef struct dattn_kv_layout {
     int32_t num_pages;          /* physical pages in the pool */
     int32_t num_kv_heads;       /* Hkv */
@@ -103,6 +119,9 @@ typedef struct dattn_kv_layout {
     int32_t page_size;          /* P: tokens per physical page, a multiple of 16 */
     const int32_t *block_table; /* (device) [B][max_pages_per_req]; -1 = unmapped */
     int32_t max_pages_per_req;  /* row width of block_table */
+    int32_t kv_format;          /* DATTN_KV_BF16 or DATTN_KV_FP8_E4M3 */
+    float *k_scale;             /* (device) fp32 [num_pages][Hkv][P], 16-byte aligned; the 8-bit */
+    float *v_scale;             /* format only (ignored for bf16). Written by dattn_kv_append. */
 } dattn_kv_layout;
 
 /* Block-sparse decode settings [LV §2.2.2, §3.1.1, §3.1.2]. */
@@ -121,6 +140,9 @@ typedef struct dattn_sparse {
  * token's KV locally]. If stats is not NULL, also update the logical-page statistics
  * [LV §3.1.2: computed at KV-write time].
  *
+ *   k_pool, v_pool (device) the pool in the layout's kv_format; for the 8-bit format each
+ *                row is quantized as described above and its scales go to layout->k_scale
+ *                and layout->v_scale.
  *   k_new, v_new (device) bf16 [B][T][Hkv][d]. Token t of request b is written at
  *                position seq_lens[b] + t.
  *   stats        (device, nullable) bf16 [num_pages][Hkv][P/16][2][d]. When a token
@@ -134,8 +156,8 @@ typedef struct dattn_sparse {
  *                page is unmapped or out of range is not written.
  * Returns DATTN_OK or an error status; nothing is launched on error.
  */
-dattn_status_t dattn_kv_append(const dattn_kv_layout *layout, dattn_bf16 *k_pool,
-                               dattn_bf16 *v_pool, dattn_bf16 *stats, const dattn_bf16 *k_new,
+dattn_status_t dattn_kv_append(const dattn_kv_layout *layout, void *k_pool,
+                               void *v_pool, dattn_bf16 *stats, const dattn_bf16 *k_new,
                                const dattn_bf16 *v_new, int32_t B, int32_t T,
                                int32_t *seq_lens, int32_t *dev_err, void *stream);
 
@@ -148,6 +170,7 @@ dattn_status_t dattn_kv_append(const dattn_kv_layout *layout, dattn_bf16 *k_pool
  *   MA[c][h][:] = sum exp(s_i - m) v_i.
  * An empty chunk gives m = -inf, e = 0, MA = 0.
  *
+ *   k_pool, v_pool (device) the pool in the layout's kv_format
  *   q          (device) bf16 [B][Hq][d]
  *   seq_lens   (device) int32 [B]
  *   chunk_req  (device) int32 [C]
@@ -157,8 +180,8 @@ dattn_status_t dattn_kv_append(const dattn_kv_layout *layout, dattn_bf16 *k_pool
  *   ws, ws_bytes  workspace, at least dattn_workspace_size(C, Hq, Hkv, d, 0, num_splits)
  *   num_splits number of CTAs the tiles are spread over; 0 = automatic
  */
-dattn_status_t dattn_partial(const dattn_kv_layout *layout, const dattn_bf16 *k_pool,
-                             const dattn_bf16 *v_pool, const dattn_bf16 *q, int32_t B,
+dattn_status_t dattn_partial(const dattn_kv_layout *layout, const void *k_pool,
+                             const void *v_pool, const dattn_bf16 *q, int32_t B,
                              int32_t Hq, float scale, const int32_t *seq_lens, int32_t C,
                              const int32_t *chunk_req, const int32_t *chunk_page_indptr,
                              const int32_t *chunk_pages, float *m, float *e, float *MA,
@@ -197,13 +220,14 @@ dattn_status_t dattn_merge(int32_t B, int32_t C, int32_t Hq, int32_t head_dim,
  * share of the 16-token tiles of all (request, KV head) pairs. A head whose tiles span
  * several CTAs is merged by the last of them.
  *
+ *   k_pool, v_pool (device) the pool in the layout's kv_format
  *   q        (device) bf16 [B][Hq][d];  seq_lens (device) int32 [B]
  *   out      (device) fp32 [B][Hq][d]
  *   m_g, e_g (device, nullable) fp32 [B][Hq]: the merged max (natural-log units) and sum
  *   ws, ws_bytes  workspace of at least dattn_workspace_size(B, Hq, Hkv, d, 0, num_splits)
  */
-dattn_status_t dattn_decode(const dattn_kv_layout *layout, const dattn_bf16 *k_pool,
-                            const dattn_bf16 *v_pool, const dattn_bf16 *q, int32_t B,
+dattn_status_t dattn_decode(const dattn_kv_layout *layout, const void *k_pool,
+                            const void *v_pool, const dattn_bf16 *q, int32_t B,
                             int32_t Hq, float scale, const int32_t *seq_lens,
                             const dattn_sparse *sparse, int32_t num_splits, void *ws,
                             size_t ws_bytes, float *out, float *m_g, float *e_g,
@@ -227,8 +251,8 @@ dattn_status_t dattn_decode(const dattn_kv_layout *layout, const dattn_bf16 *k_p
  *    call clears the part that must start at zero, on its own stream. Calls that overlap on
  *    the GPU (unordered streams) race on the array and give wrong results.
  */
-dattn_status_t dattn_decode_noalloc(const dattn_kv_layout *layout, const dattn_bf16 *k_pool,
-                                    const dattn_bf16 *v_pool, const dattn_bf16 *q, int32_t B,
+dattn_status_t dattn_decode_noalloc(const dattn_kv_layout *layout, const void *k_pool,
+                                    const void *v_pool, const dattn_bf16 *q, int32_t B,
                                     int32_t Hq, float scale, const int32_t *seq_lens,
                                     const dattn_sparse *sparse, int32_t num_splits,
                                     float *out, float *m_g, float *e_g, int32_t *dev_err,

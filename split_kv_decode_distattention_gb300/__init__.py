@@ -6,7 +6,8 @@ stream becomes the launch stream. Every step of the computation runs in the libr
 CUDA kernels. There is no CPU fallback: if the library is missing, the first call raises.
 
 Entry points, with the same names as in include/dattn.h:
-  dattn_kv_append    paged KV append, plus logical-page k_max/k_min statistics
+  dattn_kv_append    paged KV append (bf16, or 8-bit E4M3 codes with row scales), plus
+                     logical-page k_max/k_min statistics
   dattn_partial      MicroAttention partials (m, e, MA) over explicit chunks of pages
   dattn_merge        log-sum-exp aggregation of partials
   dattn_decode       fused split-KV decode, dense or block-sparse
@@ -26,7 +27,7 @@ __all__ = [
     "dattn_decode_noalloc",
     "dattn_workspace_size", "dattn_workspace_init", "dattn_auto_splits", "dattn_split_range",
     "dattn_split_owner", "dattn_status_string", "dattn_version", "Workspace",
-    "HEAD_DENSE", "HEAD_RETRIEVAL", "HEAD_STREAMING", "DEVERR",
+    "HEAD_DENSE", "HEAD_RETRIEVAL", "HEAD_STREAMING", "DEVERR", "KV_BF16", "KV_FP8_E4M3",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -35,6 +36,7 @@ _lib = None
 _lock = threading.Lock()
 
 HEAD_DENSE, HEAD_RETRIEVAL, HEAD_STREAMING = 0, 1, 2
+KV_BF16, KV_FP8_E4M3 = 0, 1
 DEVERR = {"UNMAPPED_PAGE": 0x1, "PAGE_OOB": 0x2, "LEN_OOB": 0x4, "TIMEOUT": 0x8,
           "CHUNK_OOB": 0x10, "SELECT_OOB": 0x20}
 
@@ -46,7 +48,9 @@ class DattnError(RuntimeError):
 class _Layout(ctypes.Structure):
     _fields_ = [("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
-                ("block_table", ctypes.c_void_p), ("max_pages_per_req", ctypes.c_int32)]
+                ("block_table", ctypes.c_void_p), ("max_pages_per_req", ctypes.c_int32),
+                ("kv_format", ctypes.c_int32), ("k_scale", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p)]
 
 
 class _Sparse(ctypes.Structure):
@@ -145,15 +149,39 @@ def _f32(t, name):
     return t
 
 
+def _pool(layout, t, name):
+    """A K or V pool must hold the layout's element type: bf16, or uint8 E4M3 codes."""
+    want = torch.uint8 if layout.kv_format == KV_FP8_E4M3 else torch.bfloat16
+    if t is not None and t.dtype != want and not (
+            want == torch.uint8 and t.dtype == getattr(torch, "float8_e4m3fn", None)):
+        raise TypeError(f"{name} must be {want} for this layout")
+    return t
+
+
 class KVLayout:
-    """Shape of a paged pool [num_pages][Hkv][P][d] plus its int32 block table [B][max_pages]."""
+    """Shape of a paged pool [num_pages][Hkv][P][d] plus its int32 block table [B][max_pages].
+
+    kv_format KV_BF16: the pools hold bf16 values. KV_FP8_E4M3: they hold uint8 E4M3 codes,
+    and k_scale / v_scale (float32 [num_pages][Hkv][P]) hold one scale per row.
+    """
 
     def __init__(self, num_pages: int, num_kv_heads: int, head_dim: int, page_size: int,
-                 block_table: torch.Tensor):
+                 block_table: torch.Tensor, kv_format: int = KV_BF16,
+                 k_scale: torch.Tensor | None = None, v_scale: torch.Tensor | None = None):
         _i32(block_table, "block_table")
-        self.block_table = block_table  # keeps the tensor alive
+        if kv_format == KV_FP8_E4M3:
+            if k_scale is None or v_scale is None:
+                raise ValueError("the 8-bit format needs k_scale and v_scale")
+            _f32(k_scale, "k_scale"); _f32(v_scale, "v_scale")
+        self.block_table = block_table  # keeps the tensors alive
+        self.k_scale, self.v_scale = k_scale, v_scale
         self.c = _Layout(num_pages, num_kv_heads, head_dim, page_size,
-                         block_table.data_ptr(), block_table.shape[-1])
+                         block_table.data_ptr(), block_table.shape[-1], kv_format,
+                         k_scale.data_ptr() if k_scale is not None else None,
+                         v_scale.data_ptr() if v_scale is not None else None)
+
+    @property
+    def kv_format(self): return self.c.kv_format
 
     @property
     def num_pages(self): return self.c.num_pages
@@ -225,7 +253,7 @@ def dattn_version() -> str:
 def dattn_kv_append(layout: KVLayout, k_pool, v_pool, stats, k_new, v_new, seq_lens,
                     dev_err=None, stream=None):
     """Append k_new/v_new ([B][T][Hkv][d] bf16) at seq_lens (int32 [B], advanced by T)."""
-    _bf16(k_pool, "k_pool"); _bf16(v_pool, "v_pool"); _bf16(stats, "stats")
+    _pool(layout, k_pool, "k_pool"); _pool(layout, v_pool, "v_pool"); _bf16(stats, "stats")
     _bf16(k_new, "k_new"); _bf16(v_new, "v_new"); _i32(seq_lens, "seq_lens")
     B, T = k_new.shape[0], k_new.shape[1]
     _check(load_library().dattn_kv_append(
@@ -237,7 +265,7 @@ def dattn_partial(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, c
                   chunk_page_indptr, chunk_pages, m, e, MA, ws: Workspace, num_splits=0,
                   dev_err=None, stream=None):
     """MicroAttention partials of C chunks: m, e fp32 [C][Hq], MA fp32 [C][Hq][d]."""
-    _bf16(q, "q"); _i32(seq_lens, "seq_lens"); _i32(chunk_req, "chunk_req")
+    _pool(layout, k_pool, "k_pool"); _pool(layout, v_pool, "v_pool"); _bf16(q, "q"); _i32(seq_lens, "seq_lens"); _i32(chunk_req, "chunk_req")
     _i32(chunk_page_indptr, "chunk_page_indptr"); _i32(chunk_pages, "chunk_pages")
     _f32(m, "m"); _f32(e, "e"); _f32(MA, "MA")
     B, Hq = q.shape[0], q.shape[1]
@@ -267,7 +295,7 @@ def dattn_decode(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, ou
                  ws: Workspace, m_g=None, e_g=None, sparse: SparseConfig | None = None,
                  num_splits=0, dev_err=None, stream=None):
     """Fused split-KV decode: out fp32 [B][Hq][d] (+ m_g, e_g fp32 [B][Hq])."""
-    _bf16(q, "q"); _i32(seq_lens, "seq_lens"); _f32(out, "out")
+    _pool(layout, k_pool, "k_pool"); _pool(layout, v_pool, "v_pool"); _bf16(q, "q"); _i32(seq_lens, "seq_lens"); _f32(out, "out")
     B, Hq = q.shape[0], q.shape[1]
     sp = ctypes.byref(sparse.c) if sparse is not None else None
     _check(load_library().dattn_decode(
@@ -285,7 +313,7 @@ def dattn_decode_noalloc(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_
     they must not overlap on the GPU. The first call on a device should come before any
     stream capture.
     """
-    _bf16(q, "q"); _i32(seq_lens, "seq_lens"); _f32(out, "out")
+    _pool(layout, k_pool, "k_pool"); _pool(layout, v_pool, "v_pool"); _bf16(q, "q"); _i32(seq_lens, "seq_lens"); _f32(out, "out")
     B, Hq = q.shape[0], q.shape[1]
     sp = ctypes.byref(sparse.c) if sparse is not None else None
     _check(load_library().dattn_decode_noalloc(

@@ -16,7 +16,7 @@ dattn_status_t launch_merge(int32_t B, int32_t C, int32_t Hq, int32_t D, const i
                             const float* m, const float* e, const float* MA, float* out,
                             float* m_g, float* e_g, float* MA_g, int32_t* dev_err,
                             cudaStream_t stream);
-dattn_status_t launch_kv_append(const dattn_kv_layout& L, uint16_t* k_pool, uint16_t* v_pool,
+dattn_status_t launch_kv_append(const dattn_kv_layout& L, void* k_pool, void* v_pool,
                                 uint16_t* stats, const uint16_t* k_new, const uint16_t* v_new,
                                 int32_t B, int32_t T, int32_t* seq_lens, int32_t* dev_err,
                                 cudaStream_t stream);
@@ -47,6 +47,11 @@ dattn_status_t check_layout(const dattn_kv_layout* L) {
     if ((int64_t)L->num_pages * L->num_kv_heads * L->page_size >= (1ll << 31))
         return DATTN_ERR_UNSUPPORTED;
     if ((int64_t)L->max_pages_per_req * L->page_size >= (1ll << 30)) return DATTN_ERR_UNSUPPORTED;
+    if (L->kv_format != DATTN_KV_BF16 && L->kv_format != DATTN_KV_FP8_E4M3)
+        return DATTN_ERR_INVALID_ARG;
+    if (L->kv_format == DATTN_KV_FP8_E4M3 &&
+        (!L->k_scale || !L->v_scale || !aligned16(L->k_scale) || !aligned16(L->v_scale)))
+        return DATTN_ERR_INVALID_ARG;
     return DATTN_OK;
 }
 
@@ -93,6 +98,24 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     });
     return fn;
+}
+
+// 2-D map over a pool of 8-bit codes seen as rows of d bytes: one box {d, 16} is a 16-token
+// row group of one (page, KV head), landing as [row][d bytes] with the 128-byte (d = 128)
+// or 64-byte (d = 64) swizzle, which keeps ldmatrix conflict-free.
+dattn_status_t make_kv_tensor_map_u8(void* tmap_out, const void* pool, int64_t rows, int D) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (fn == nullptr) return DATTN_ERR_CUDA;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D};
+    cuuint32_t box[2] = {(cuuint32_t)D, 16};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(static_cast<CUtensorMap*>(tmap_out), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                    const_cast<void*>(pool), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DATTN_OK : DATTN_ERR_CUDA;
 }
 
 // 3-D map over the pool seen as rows of d bf16 values, split into 128-byte halves:
@@ -176,8 +199,8 @@ dattn_status_t dattn_workspace_init(void* ws, size_t ws_bytes, void* stream) {
                : DATTN_ERR_CUDA;
 }
 
-dattn_status_t dattn_kv_append(const dattn_kv_layout* layout, dattn_bf16* k_pool,
-                               dattn_bf16* v_pool, dattn_bf16* stats, const dattn_bf16* k_new,
+dattn_status_t dattn_kv_append(const dattn_kv_layout* layout, void* k_pool,
+                               void* v_pool, dattn_bf16* stats, const dattn_bf16* k_new,
                                const dattn_bf16* v_new, int32_t B, int32_t T,
                                int32_t* seq_lens, int32_t* dev_err, void* stream) {
     dattn_status_t st = check_layout(layout);
@@ -194,8 +217,8 @@ dattn_status_t dattn_kv_append(const dattn_kv_layout* layout, dattn_bf16* k_pool
                             static_cast<cudaStream_t>(stream));
 }
 
-dattn_status_t dattn_partial(const dattn_kv_layout* layout, const dattn_bf16* k_pool,
-                             const dattn_bf16* v_pool, const dattn_bf16* q, int32_t B,
+dattn_status_t dattn_partial(const dattn_kv_layout* layout, const void* k_pool,
+                             const void* v_pool, const dattn_bf16* q, int32_t B,
                              int32_t Hq, float scale, const int32_t* seq_lens, int32_t C,
                              const int32_t* chunk_req, const int32_t* chunk_page_indptr,
                              const int32_t* chunk_pages, float* m, float* e, float* MA,
@@ -238,6 +261,9 @@ dattn_status_t dattn_partial(const dattn_kv_layout* layout, const dattn_bf16* k_
     p.nseg = C * p.Hkv;
     p.nitems = C;
     p.dev_err = dev_err;
+    p.f8 = layout->kv_format == DATTN_KV_FP8_E4M3 ? 1 : 0;
+    p.k_scale = layout->k_scale;
+    p.v_scale = layout->v_scale;
     return launch_attention(p, k_pool, v_pool, layout->head_dim, num_splits, ws, ws_bytes,
                             static_cast<cudaStream_t>(stream), bound);
 }
@@ -256,8 +282,8 @@ dattn_status_t dattn_merge(int32_t B, int32_t C, int32_t Hq, int32_t head_dim,
                         static_cast<cudaStream_t>(stream));
 }
 
-dattn_status_t dattn_decode(const dattn_kv_layout* layout, const dattn_bf16* k_pool,
-                            const dattn_bf16* v_pool, const dattn_bf16* q, int32_t B,
+dattn_status_t dattn_decode(const dattn_kv_layout* layout, const void* k_pool,
+                            const void* v_pool, const dattn_bf16* q, int32_t B,
                             int32_t Hq, float scale, const int32_t* seq_lens,
                             const dattn_sparse* sparse, int32_t num_splits, void* ws,
                             size_t ws_bytes, float* out, float* m_g, float* e_g,
@@ -310,6 +336,9 @@ dattn_status_t dattn_decode(const dattn_kv_layout* layout, const dattn_bf16* k_p
     p.nseg = B * p.Hkv;
     p.nitems = B;
     p.dev_err = dev_err;
+    p.f8 = layout->kv_format == DATTN_KV_FP8_E4M3 ? 1 : 0;
+    p.k_scale = layout->k_scale;
+    p.v_scale = layout->v_scale;
     return launch_attention(p, k_pool, v_pool, layout->head_dim, num_splits, ws, ws_bytes,
                             static_cast<cudaStream_t>(stream), bound);
 }

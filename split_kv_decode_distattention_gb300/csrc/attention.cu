@@ -24,7 +24,9 @@
 // CTA therefore gets the same number of bytes, whatever the length mix. A segment that
 // lies inside one CTA is finished there. A segment cut across CTAs leaves one partial
 // triple per CTA in the workspace, and the CTA that arrives last (atomic counter) merges
-// them. No CTA ever waits on another.
+// them. No CTA ever waits on another. The 8-bit pool (FP8 E4M3 codes with one fp32 scale per
+// row) streams half the bytes through the same pipeline and runs on fp16 tensor cores (see
+// Consumer).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -62,7 +64,17 @@ struct Smem {
     }
     __device__ int32_t* item_len() const { return reinterpret_cast<int32_t*>(base + L.item_len); }
     __device__ int32_t* scan() const { return reinterpret_cast<int32_t*>(base + L.scan); }
+    // the 8-bit pool's row scales of stage s: 16 K scales, then 16 V scales
+    __device__ const float* scales(int s) const {
+        return reinterpret_cast<const float*>(base + L.scales) + 32 * s;
+    }
 };
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in an 8-bit tile of d-byte rows.
+template <int D>
+__device__ __forceinline__ uint32_t swz_u8(uint32_t row, uint32_t chunk) {
+    return D == 128 ? swz128(row, chunk) : swz64(row, chunk);
+}
 
 __device__ __forceinline__ int32_t ceil16(int32_t x) { return (x + 15) >> 4; }
 
@@ -257,7 +269,18 @@ __device__ __forceinline__ void write_final(const AttnParams& p, int32_t s, int3
     }
 }
 
-template <int D>
+// The 8-bit pool (FP8 E4M3 codes with one fp32 scale per row) runs on fp16 tensor cores:
+// every E4M3 value is an fp16 value, so a code converts exactly with one cvt per pair,
+// straight from the ldmatrix fragment. The query is scaled by a power of two 2^a, chosen
+// per piece so that its largest element lies in [2^14, 2^15), and rounded to fp16; this is
+// exact for every element within 2^28 of the largest. The logit of row i is then
+// (q' . code_i) * k_scale_i * scale * log2(e) * 2^-a. For PV the V scale of a row goes
+// into its softmax weight: w_i = p_i * v_scale_i * 2^15 / r, where r is a power of two at
+// least the largest V scale seen so far in the piece (raised, and the accumulator rescaled,
+// when a tile brings a larger one). So 0 <= w_i <= 2^15 always fits fp16, and w_i is
+// split into two fp16 terms (22 significant bits) as the bf16 path splits p_i. The
+// accumulator is multiplied by r * 2^-15 when the piece is published.
+template <int D, bool F8>
 struct Consumer {
     static constexpr int KS = D / 16;  // k-steps of QK^T and m-tiles of PV
 
@@ -267,12 +290,16 @@ struct Consumer {
     uint32_t qf[KS][2];
     float o[KS][4];
     float m0, m1, e0, e1;
+    float qsc;     // scale * log2(e) (8-bit pool: times 2^-a) for the current piece's query
+    int32_t rk;    // 8-bit pool: r = 2^rk bounds the V scales seen in this piece
+    float rv, inv;  // 8-bit pool: r and 2^15 / r
 
     __device__ Consumer(const AttnParams& p_, const Smem& sm_, int w, int l)
         : p(p_), sm(sm_), warp(w), lane(l) {}
 
-    // B fragments of the group's queries for segment s (query head = lane / 4).
-    __device__ void load_q(int32_t s, uint32_t (&dst)[KS][2]) const {
+    // B fragments of the group's queries for segment s (query head = lane / 4), and the
+    // factor that turns a raw dot product into a base-2 logit.
+    __device__ void load_q(int32_t s, uint32_t (&dst)[KS][2], float& qs) const {
         const int32_t item = s / p.Hkv, kvh = s - item * p.Hkv;
         int32_t b = item;
         if (p.mode == MODE_PARTIAL) b = __ldg(p.chunk_req + item);
@@ -280,10 +307,38 @@ struct Consumer {
         const bool ok = n < p.g && b >= 0 && b < p.B;
         const uint32_t* qv = reinterpret_cast<const uint32_t*>(
             p.q + ((int64_t)(ok ? b : 0) * p.Hq + kvh * p.g + (ok ? n : 0)) * D);
+        if constexpr (!F8) {
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            dst[ks][0] = ok ? __ldg(qv + ks * 8 + tig) : 0u;
-            dst[ks][1] = ok ? __ldg(qv + ks * 8 + 4 + tig) : 0u;
+            for (int ks = 0; ks < KS; ++ks) {
+                dst[ks][0] = ok ? __ldg(qv + ks * 8 + tig) : 0u;
+                dst[ks][1] = ok ? __ldg(qv + ks * 8 + 4 + tig) : 0u;
+            }
+            qs = p.sl2;
+        } else {
+            // k-step ks covers channels 16ks..16ks+15 in the order the 8-bit K fragment
+            // brings them: b0 = channels 16ks + 4tig + {0, 1}, b1 = 16ks + 4tig + {2, 3}
+            float mx = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                dst[ks][0] = ok ? __ldg(qv + ks * 8 + 2 * tig) : 0u;
+                dst[ks][1] = ok ? __ldg(qv + ks * 8 + 2 * tig + 1) : 0u;
+                mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_lo(dst[ks][0])), fabsf(bf16_hi(dst[ks][0]))),
+                                     fmaxf(fabsf(bf16_lo(dst[ks][1])), fabsf(bf16_hi(dst[ks][1])))));
+            }
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1)
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            int32_t a = 0;  // 2^a * max|q| in [2^14, 2^15)
+            if (mx > 0.f) a = min(127, max(-113, 14 - (((__float_as_int(mx) >> 23) & 0xff) - 127)));
+            const float up = __int_as_float((127 + a) << 23);
+            const float down = a < 127 ? __int_as_float((127 - a) << 23) : 5.877471754e-39f;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    dst[ks][j] = pack_f16(bf16_lo(dst[ks][j]) * up, bf16_hi(dst[ks][j]) * up);
+            }
+            qs = p.sl2 * down;
         }
     }
 
@@ -292,6 +347,40 @@ struct Consumer {
         for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
         m0 = m1 = kNegInf;
         e0 = e1 = 0.f;
+        rk = -112;
+        rv = __int_as_float((127 - 112) << 23);
+        inv = __int_as_float((142 + 112) << 23);
+    }
+
+    // Online softmax (base 2) over one tile's logits: rows g8 (s0, s1) and g8 + 8 (s2, s3),
+    // heads 2tig and 2tig + 1. Returns the weights relative to the new running max.
+    __device__ __forceinline__ void softmax(float s0, float s1, float s2, float s3, float& p0,
+                                            float& p1, float& p2, float& p3) {
+        float c0 = fmaxf(s0, s2), c1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            c0 = fmaxf(c0, __shfl_xor_sync(0xffffffffu, c0, off));
+            c1 = fmaxf(c1, __shfl_xor_sync(0xffffffffu, c1, off));
+        }
+        const float mn0 = fmaxf(m0, c0), mn1 = fmaxf(m1, c1);
+        const float mu0 = mn0 == kNegInf ? 0.f : mn0, mu1 = mn1 == kNegInf ? 0.f : mn1;
+        p0 = exp2f(s0 - mu0);
+        p1 = exp2f(s1 - mu1);
+        p2 = exp2f(s2 - mu0);
+        p3 = exp2f(s3 - mu1);
+        if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
+            const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
+            e0 *= al0;
+            e1 *= al1;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+            }
+        }
+        m0 = mn0;
+        m1 = mn1;
+        e0 += p0 + p2;
+        e1 += p1 + p3;
     }
 
     // One 16-token tile in stage buffer `st`; rows outside [lo, hi) are masked.
@@ -314,34 +403,12 @@ struct Consumer {
             }
         }
         const bool v0 = g8 >= lo && g8 < hi, v1 = g8 + 8 >= lo && g8 + 8 < hi;
-        const float s0 = v0 ? (sa[0] + sb[0]) * p.sl2 : kNegInf;
-        const float s1 = v0 ? (sa[1] + sb[1]) * p.sl2 : kNegInf;
-        const float s2 = v1 ? (sa[2] + sb[2]) * p.sl2 : kNegInf;
-        const float s3 = v1 ? (sa[3] + sb[3]) * p.sl2 : kNegInf;
-        // ---- online softmax (base 2) ------------------------------------------------
-        float c0 = fmaxf(s0, s2), c1 = fmaxf(s1, s3);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            c0 = fmaxf(c0, __shfl_xor_sync(0xffffffffu, c0, off));
-            c1 = fmaxf(c1, __shfl_xor_sync(0xffffffffu, c1, off));
-        }
-        const float mn0 = fmaxf(m0, c0), mn1 = fmaxf(m1, c1);
-        const float mu0 = mn0 == kNegInf ? 0.f : mn0, mu1 = mn1 == kNegInf ? 0.f : mn1;
-        const float p0 = exp2f(s0 - mu0), p1 = exp2f(s1 - mu1);
-        const float p2 = exp2f(s2 - mu0), p3 = exp2f(s3 - mu1);
-        if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
-            const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
-            e0 *= al0;
-            e1 *= al1;
-#pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
-            }
-        }
-        m0 = mn0;
-        m1 = mn1;
-        e0 += p0 + p2;
-        e1 += p1 + p3;
+        const float s0 = v0 ? (sa[0] + sb[0]) * qsc : kNegInf;
+        const float s1 = v0 ? (sa[1] + sb[1]) * qsc : kNegInf;
+        const float s2 = v1 ? (sa[2] + sb[2]) * qsc : kNegInf;
+        const float s3 = v1 ? (sa[3] + sb[3]) * qsc : kNegInf;
+        float p0, p1, p2, p3;
+        softmax(s0, s1, s2, s3, p0, p1, p2, p3);
         // ---- P^T as the B operand: two bf16 terms, transposed with movmatrix ---------
         const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
         const uint32_t l01 = pack_bf16(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
@@ -378,6 +445,93 @@ struct Consumer {
         }
     }
 
+    // One 16-token tile of the 8-bit pool in stage buffer `st` (K codes, then V codes) with
+    // its row scales `sc`; rows outside [lo, hi) are masked.
+    __device__ void tile_f8(uint32_t st, const float* sc, int lo, int hi) {
+        const uint32_t kbase = st, vbase = st + 16u * D;
+        const int g8 = lane >> 2, tig = lane & 3;
+        // ldmatrix lane addresses: matrices (rows 0-7 | 8-15) x (chunk 2c | 2c + 1)
+        const uint32_t row = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const uint32_t csel = lane >> 4;
+        // ---- S^T = K Q^T: a thread's 4 codes are 4 adjacent channels of one token ------
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
+            ldsm_x4(kbase + swz_u8<D>(row, 2u * c + csel), r0, r1, r2, r3);
+            e4m3x4_to_f16(r0, a0, a2);
+            e4m3x4_to_f16(r1, a1, a3);
+            mma_f16(sa, a0, a1, a2, a3, qf[2 * c][0], qf[2 * c][1]);
+            e4m3x4_to_f16(r2, a0, a2);
+            e4m3x4_to_f16(r3, a1, a3);
+            mma_f16(sb, a0, a1, a2, a3, qf[2 * c + 1][0], qf[2 * c + 1][1]);
+        }
+        const bool v0 = g8 >= lo && g8 < hi, v1 = g8 + 8 >= lo && g8 + 8 < hi;
+        const float kc0 = sc[g8] * qsc, kc1 = sc[g8 + 8] * qsc;
+        const float s0 = v0 ? (sa[0] + sb[0]) * kc0 : kNegInf;
+        const float s1 = v0 ? (sa[1] + sb[1]) * kc0 : kNegInf;
+        const float s2 = v1 ? (sa[2] + sb[2]) * kc1 : kNegInf;
+        const float s3 = v1 ? (sa[3] + sb[3]) * kc1 : kNegInf;
+        float p0, p1, p2, p3;
+        softmax(s0, s1, s2, s3, p0, p1, p2, p3);
+        // ---- V scales: raise r to a power of two >= every V scale of the tile ---------
+        const float vs0 = v0 ? sc[16 + g8] : 0.f, vs1 = v1 ? sc[24 + g8] : 0.f;
+        float vt = fmaxf(vs0, vs1);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) vt = fmaxf(vt, __shfl_xor_sync(0xffffffffu, vt, off));
+        if (vt > rv) {  // warp-uniform; vt > 2^-112 is a normal number
+            const int32_t bits = __float_as_int(vt);
+            const int32_t k = min(127, ((bits >> 23) & 0xff) - 127 + ((bits & 0x7fffff) != 0));
+            const int32_t dk = rk - k;
+            const float f = dk >= -126 ? __int_as_float((127 + dk) << 23) : 0.f;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                o[mt][0] *= f; o[mt][1] *= f; o[mt][2] *= f; o[mt][3] *= f;
+            }
+            rk = k;
+            rv = __int_as_float((127 + k) << 23);
+            inv = __int_as_float((142 - k) << 23);
+        }
+        const float vn0 = vs0 * inv, vn1 = vs1 * inv;  // in [0, 2^15], exact
+        const float w0 = p0 * vn0, w1 = p1 * vn0, w2 = p2 * vn1, w3 = p3 * vn1;
+        // ---- W^T as the B operand: two fp16 terms, transposed with movmatrix ----------
+        const uint32_t h01 = pack_f16(w0, w1), h23 = pack_f16(w2, w3);
+        const uint32_t l01 = pack_f16(w0 - f16_lo(h01), w1 - f16_hi(h01));
+        const uint32_t l23 = pack_f16(w2 - f16_lo(h23), w3 - f16_hi(h23));
+        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+        const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+        // ---- O^T += V^T W^T ------------------------------------------------------------
+        // After the transposing ldmatrix a thread holds tokens 2tig, 2tig + 1 (or 8 + ...)
+        // of channels 2g8, 2g8 + 1 of a 16-channel chunk; codes of masked tokens are zeroed
+        // so that a stale NaN code cannot meet a zero weight. Row g8 of m-tile mt is
+        // channel 16mt + 2g8 and row g8 + 8 is channel 16mt + 2g8 + 1.
+        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+        if (lo > 0 || hi < 16) {
+            const int t0 = 2 * tig, t1 = 2 * tig + 1;
+            mlo = (t0 >= lo && t0 < hi ? 0x0000ffffu : 0u) | (t1 >= lo && t1 < hi ? 0xffff0000u : 0u);
+            mhi = (t0 + 8 >= lo && t0 + 8 < hi ? 0x0000ffffu : 0u) |
+                  (t1 + 8 >= lo && t1 + 8 < hi ? 0xffff0000u : 0u);
+        }
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
+            ldsm_x4_trans(vbase + swz_u8<D>(row, 2u * c + csel), r0, r1, r2, r3);
+            // [t0 cA, t0 cB, t1 cA, t1 cB] -> [t0 cA, t1 cA, t0 cB, t1 cB]
+            r0 = __byte_perm(r0 & mlo, 0u, 0x3120);
+            r1 = __byte_perm(r1 & mhi, 0u, 0x3120);
+            r2 = __byte_perm(r2 & mlo, 0u, 0x3120);
+            r3 = __byte_perm(r3 & mhi, 0u, 0x3120);
+            e4m3x4_to_f16(r0, a0, a1);
+            e4m3x4_to_f16(r1, a2, a3);
+            mma_f16(o[2 * c], a0, a1, a2, a3, bh0, bh1);
+            mma_f16(o[2 * c], a0, a1, a2, a3, bl0, bl1);
+            e4m3x4_to_f16(r2, a0, a1);
+            e4m3x4_to_f16(r3, a2, a3);
+            mma_f16(o[2 * c + 1], a0, a1, a2, a3, bh0, bh1);
+            mma_f16(o[2 * c + 1], a0, a1, a2, a3, bl0, bl1);
+        }
+    }
+
     // Publishes this warp's state for the CTA-level merge of the piece.
     __device__ void publish() {
         float t0 = e0, t1 = e1;
@@ -395,16 +549,30 @@ struct Consumer {
             if (hA < p.g) { wm[hA] = m0; we[hA] = t0; }
             if (hB < p.g) { wm[hB] = m1; we[hB] = t1; }
         }
+        if constexpr (!F8) {
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            const int dd = mt * 16 + g8;
-            if (hA < p.g) { wo[hA * D + dd] = o[mt][0]; wo[hA * D + dd + 8] = o[mt][2]; }
-            if (hB < p.g) { wo[hB * D + dd] = o[mt][1]; wo[hB * D + dd + 8] = o[mt][3]; }
+            for (int mt = 0; mt < KS; ++mt) {
+                const int dd = mt * 16 + g8;
+                if (hA < p.g) { wo[hA * D + dd] = o[mt][0]; wo[hA * D + dd + 8] = o[mt][2]; }
+                if (hB < p.g) { wo[hB * D + dd] = o[mt][1]; wo[hB * D + dd + 8] = o[mt][3]; }
+            }
+        } else {
+            const float rs = rv * 3.0517578125e-05f;  // r * 2^-15, exact
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                const int dd = mt * 16 + 2 * g8;
+                if (hA < p.g)
+                    *reinterpret_cast<float2*>(wo + hA * D + dd) =
+                        make_float2(o[mt][0] * rs, o[mt][2] * rs);
+                if (hB < p.g)
+                    *reinterpret_cast<float2*>(wo + hB * D + dd) =
+                        make_float2(o[mt][1] * rs, o[mt][3] * rs);
+            }
         }
     }
 };
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kAttnThreads)
 attention_kernel(const __grid_constant__ AttnParams p,
                  const __grid_constant__ CUtensorMap tmap_k,
@@ -415,7 +583,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
         const uint32_t off = smem_u32(smem_raw);
         sm.base = smem_raw + (((off + 1023u) & ~1023u) - off);
     }
-    sm.L = attn_smem_layout(D, p.g, p.nitems, p.Hkv, p.mode == MODE_SPARSE);
+    sm.L = attn_smem_layout(D, p.g, p.nitems, p.Hkv, p.mode == MODE_SPARSE, F8);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t G = gridDim.x, cta = blockIdx.x;
 
@@ -558,7 +726,8 @@ attention_kernel(const __grid_constant__ AttnParams p,
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer warp
         const uint64_t pol = policy_evict_first();
-        const uint32_t tile_bytes = (uint32_t)(D / 64) * 2048u;
+        const uint32_t tile_bytes = (F8 ? 16u : 32u) * (uint32_t)D;
+        const uint32_t tx = 2u * tile_bytes + (F8 ? 128u : 0u);
         int32_t k = 0;  // real tiles issued so far: tile k uses stage k % kStages
         bool stop = false;
         int32_t s = s_first, cs, real, r0, r1;
@@ -585,13 +754,25 @@ attention_kernel(const __grid_constant__ AttnParams p,
                     if (lane == 0) {
                         sm.meta()[stg] = lohi;
                         if (lohi >> 16) mbar_arrive(full);
-                        else mbar_arrive_expect_tx(full, 2u * tile_bytes);
+                        else mbar_arrive_expect_tx(full, tx);
                     }
                     __syncwarp();
                     // one instruction, two lanes: lane 0 brings the K tile, lane 1 the V tile
-                    if (!(lohi >> 16) && lane < 2)
+                    // (8-bit pool: lanes 2 and 3 bring the 16 K and 16 V row scales)
+                    if constexpr (F8) {
+                        if (!(lohi >> 16) && lane < 4) {
+                            if (lane < 2)
+                                tma_load_2d(dst + (lane ? tile_bytes : 0u),
+                                            lane ? &tmap_v : &tmap_k, 0, y, full, pol);
+                            else
+                                bulk_copy(smem_u32(sm.scales(stg)) + (lane - 2u) * 64u,
+                                          (lane == 2 ? p.k_scale : p.v_scale) + y, 64u, full,
+                                          pol);
+                        }
+                    } else if (!(lohi >> 16) && lane < 2) {
                         tma_load_3d(dst + (lane ? tile_bytes : 0u), lane ? &tmap_v : &tmap_k, 0,
                                     y, 0, full, pol);
+                    }
                 }
             }
             ++s;
@@ -609,23 +790,25 @@ attention_kernel(const __grid_constant__ AttnParams p,
     }
 
     // ---------------------------------------------------------------- consumer warps
-    Consumer<D> cons(p, sm, warp, lane);
+    Consumer<D, F8> cons(p, sm, warp, lane);
     const uint32_t stage0 = smem_u32(sm.base + sm.L.stages);
     int32_t kbase = 0;  // real tiles of earlier pieces
     int32_t s = s_first, sst, sreal, r0, r1;
     bool have = plan.next_piece(s, X0, X1, sst, sreal, r0, r1);
-    uint32_t qn[Consumer<D>::KS][2];
-    if (have) cons.load_q(s, qn);
+    uint32_t qn[Consumer<D, F8>::KS][2];
+    float qsn = 0.f;
+    if (have) cons.load_q(s, qn, qsn);
     while (have) {
 #pragma unroll
-        for (int ks = 0; ks < Consumer<D>::KS; ++ks) {
+        for (int ks = 0; ks < Consumer<D, F8>::KS; ++ks) {
             cons.qf[ks][0] = qn[ks][0];
             cons.qf[ks][1] = qn[ks][1];
         }
+        cons.qsc = qsn;
         // the next piece's query is fetched while this piece streams
         int32_t s2 = s + 1, c2, real2, a2, b2;
         const bool have2 = plan.next_piece(s2, X0, X1, c2, real2, a2, b2);
-        if (have2) cons.load_q(s2, qn);
+        if (have2) cons.load_q(s2, qn, qsn);
         cons.reset();
         const int32_t nr = r1 - r0;
         for (int32_t i = (warp - kbase % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
@@ -638,8 +821,12 @@ attention_kernel(const __grid_constant__ AttnParams p,
             const int32_t lohi = sm.meta()[stg];
             const int lo = lohi & 0xff, hi = (lohi >> 8) & 0xff;
             if (ok && !(lohi >> 16)) {
-                cons.tile(stage0 + (uint32_t)stg * sm.L.stage_bytes, lo, hi);
-                if (lo > 0 || hi < 16) fence_proxy_async_smem();
+                if constexpr (F8) {
+                    cons.tile_f8(stage0 + (uint32_t)stg * sm.L.stage_bytes, sm.scales(stg), lo, hi);
+                } else {
+                    cons.tile(stage0 + (uint32_t)stg * sm.L.stage_bytes, lo, hi);
+                    if (lo > 0 || hi < 16) fence_proxy_async_smem();
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty_bar(stg));
@@ -774,7 +961,7 @@ struct KernelInfo {
     int max_smem_set = 0;
 };
 
-template <int D>
+template <int D, bool F8>
 KernelInfo& kernel_info() {
     static KernelInfo info;
     return info;
@@ -782,12 +969,13 @@ KernelInfo& kernel_info() {
 
 std::mutex g_attr_mutex;
 
-template <int D>
+template <int D, bool F8>
 dattn_status_t ensure_smem(uint32_t bytes) {
     std::lock_guard<std::mutex> lock(g_attr_mutex);
-    KernelInfo& ki = kernel_info<D>();
+    KernelInfo& ki = kernel_info<D, F8>();
     if ((int)bytes > ki.max_smem_set) {
-        if (cudaFuncSetAttribute(attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(attention_kernel<D, F8>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bytes) != cudaSuccess)
             return DATTN_ERR_CUDA;
         ki.max_smem_set = (int)bytes;
@@ -795,10 +983,10 @@ dattn_status_t ensure_smem(uint32_t bytes) {
     return DATTN_OK;
 }
 
-template <int D>
+template <int D, bool F8>
 int occupancy(uint32_t smem) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attention_kernel<D>, kAttnThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attention_kernel<D, F8>, kAttnThreads,
                                                       smem) != cudaSuccess)
         return 1;
     return n < 1 ? 1 : n;
@@ -811,15 +999,15 @@ size_t attn_workspace_bytes(int32_t nseg, int32_t g, int32_t D, int32_t G) {
     return counters + (size_t)(G + nseg) * slot_floats(g, D) * 4;
 }
 
-template <int D>
+template <int D, bool F8>
 static dattn_status_t launch_d(const AttnParams& p0, const void* k_pool, const void* v_pool,
                                int32_t num_splits, void* ws, size_t ws_bytes,
                                cudaStream_t stream, int64_t tiles_bound) {
     AttnParams p = p0;
-    const AttnSmem L = attn_smem_layout(D, p.g, p.nitems, p.Hkv, p.mode == MODE_SPARSE);
-    dattn_status_t st = ensure_smem<D>(L.total);
+    const AttnSmem L = attn_smem_layout(D, p.g, p.nitems, p.Hkv, p.mode == MODE_SPARSE, F8);
+    dattn_status_t st = ensure_smem<D, F8>(L.total);
     if (st != DATTN_OK) return st;
-    const int32_t G = choose_splits(tiles_bound, num_splits, occupancy<D>(L.total));
+    const int32_t G = choose_splits(tiles_bound, num_splits, occupancy<D, F8>(L.total));
     const size_t counters = ((size_t)p.nseg * 4 + 255) & ~(size_t)255;
     if (ws == nullptr || ws_bytes < attn_workspace_bytes(p.nseg, p.g, D, G) ||
         (reinterpret_cast<uintptr_t>(ws) & 255))
@@ -829,10 +1017,11 @@ static dattn_status_t launch_d(const AttnParams& p0, const void* k_pool, const v
     alignas(64) CUtensorMap tk;
     alignas(64) CUtensorMap tv;
     const int64_t rows = (int64_t)p.num_pages * p.Hkv * p.P;
-    if ((st = make_kv_tensor_map(&tk, k_pool, rows, D)) != DATTN_OK) return st;
-    if ((st = make_kv_tensor_map(&tv, v_pool, rows, D)) != DATTN_OK) return st;
-    if (launch_pdl(attention_kernel<D>, dim3(G), dim3(kAttnThreads), L.total, stream, p, tk, tv) !=
-        cudaSuccess)
+    auto make_map = F8 ? make_kv_tensor_map_u8 : make_kv_tensor_map;
+    if ((st = make_map(&tk, k_pool, rows, D)) != DATTN_OK) return st;
+    if ((st = make_map(&tv, v_pool, rows, D)) != DATTN_OK) return st;
+    if (launch_pdl(attention_kernel<D, F8>, dim3(G), dim3(kAttnThreads), L.total, stream, p, tk,
+                   tv) != cudaSuccess)
         return DATTN_ERR_CUDA;
     return DATTN_OK;
 }
@@ -840,18 +1029,11 @@ static dattn_status_t launch_d(const AttnParams& p0, const void* k_pool, const v
 dattn_status_t launch_attention(const AttnParams& p, const void* k_pool, const void* v_pool,
                                 int D, int32_t num_splits, void* ws, size_t ws_bytes,
                                 cudaStream_t stream, int64_t tiles_bound) {
-    if (D == 64) return launch_d<64>(p, k_pool, v_pool, num_splits, ws, ws_bytes, stream,
-                                     tiles_bound);
-    if (D == 128) return launch_d<128>(p, k_pool, v_pool, num_splits, ws, ws_bytes, stream,
-                                       tiles_bound);
-    return DATTN_ERR_UNSUPPORTED;
-}
-
-int32_t attention_occupancy(int D, int g, int nitems, int Hkv, bool sparse) {
-    const AttnSmem L = attn_smem_layout(D, g, nitems, Hkv, sparse);
-    if (D == 64) { if (ensure_smem<64>(L.total) != DATTN_OK) return 1; return occupancy<64>(L.total); }
-    if (ensure_smem<128>(L.total) != DATTN_OK) return 1;
-    return occupancy<128>(L.total);
+    const bool f8 = p.f8 != 0;
+    auto launch = D == 64 ? (f8 ? launch_d<64, true> : launch_d<64, false>)
+                          : (f8 ? launch_d<128, true> : launch_d<128, false>);
+    if (D != 64 && D != 128) return DATTN_ERR_UNSUPPORTED;
+    return launch(p, k_pool, v_pool, num_splits, ws, ws_bytes, stream, tiles_bound);
 }
 
 }  // namespace dattn

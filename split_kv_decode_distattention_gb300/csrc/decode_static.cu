@@ -60,8 +60,8 @@ dattn_status_t scratch_address(void** out) {
 }  // namespace dattn
 
 extern "C" dattn_status_t dattn_decode_noalloc(const dattn_kv_layout* layout,
-                                               const dattn_bf16* k_pool,
-                                               const dattn_bf16* v_pool, const dattn_bf16* q,
+                                               const void* k_pool,
+                                               const void* v_pool, const dattn_bf16* q,
                                                int32_t B, int32_t Hq, float scale,
                                                const int32_t* seq_lens,
                                                const dattn_sparse* sparse, int32_t num_splits,

@@ -50,6 +50,10 @@ struct AttnParams {
     int32_t nseg;
     int32_t nitems;     // B for dense / sparse, C for partial
     int32_t* dev_err;
+    // 8-bit pool: FP8 E4M3 codes plus one fp32 scale per (token, KV head) row
+    int32_t f8;
+    const float* k_scale;
+    const float* v_scale;
 };
 
 // Floats of one workspace slot (a piece's partial): MA [g][D], then m [g] and e [g],
@@ -58,18 +62,21 @@ __host__ __device__ inline int32_t slot_floats(int32_t g, int32_t D) {
     return g * D + ((2 * g + 3) & ~3);
 }
 
-// Shared-memory layout of the attention engine, identical on host and device.
+// Shared-memory layout of the attention engine, identical on host and device. A stage holds
+// the K tile then the V tile of 16 tokens (bf16: 32*d bytes each; 8-bit: 16*d bytes each);
+// with the 8-bit pool, the stage's 16 K scales and 16 V scales sit in `scales`.
 struct AttnSmem {
-    uint32_t stage_bytes, stages, bars, meta, flags, ws_m, ws_e, ws_o, kind_before, kinds,
-        item_start, item_len, scan, total;
+    uint32_t stage_bytes, stages, scales, bars, meta, flags, ws_m, ws_e, ws_o, kind_before,
+        kinds, item_start, item_len, scan, total;
 };
 
 __host__ __device__ inline AttnSmem attn_smem_layout(int D, int g, int nitems, int Hkv,
-                                                     bool sparse) {
+                                                     bool sparse, bool f8) {
     AttnSmem s;
-    s.stage_bytes = 2u * (uint32_t)(D / 64) * 2048u;
+    s.stage_bytes = (f8 ? 32u : 64u) * (uint32_t)D;
     uint32_t o = 0;
     s.stages = o;      o += (uint32_t)kStages * s.stage_bytes;
+    s.scales = o;      o += f8 ? (uint32_t)kStages * 128u : 0u;
     s.bars = o;        o += 2u * kStages * 8u;
     s.meta = o;        o += kStages * 4u;
     s.flags = o;       o += 16u;
@@ -90,11 +97,11 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int D, int g, int nitems, i
 // Device properties and cached driver entry points.
 int sm_count_current();
 dattn_status_t make_kv_tensor_map(void* tmap_out, const void* pool, int64_t rows, int D);
+dattn_status_t make_kv_tensor_map_u8(void* tmap_out, const void* pool, int64_t rows, int D);
 
 dattn_status_t launch_attention(const AttnParams& p, const void* k_pool, const void* v_pool,
                                 int D, int32_t num_splits, void* ws, size_t ws_bytes,
                                 cudaStream_t stream, int64_t tiles_bound);
-int32_t attention_occupancy(int D, int g, int nitems, int Hkv, bool sparse);
 
 // Launches kernel<<<grid, block, smem, stream>>>(args...) with programmatic stream
 // serialization, so that its launch and prologue overlap the previous kernel on the stream.

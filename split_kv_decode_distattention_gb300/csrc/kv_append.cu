@@ -13,6 +13,13 @@
 // of the open logical page in registers. Because the windows are aligned to logical
 // pages, no two CTAs touch the same logical page, so the statistics need no atomics and
 // come out the same on every run.
+//
+// The 8-bit pool (FP8 E4M3 codes, one fp32 scale per (token, KV head) row; the retrieval
+// cache of "LLM长序列服务优化：LServe的块稀疏注意力技术" §3.2.1 is quantized at 2-8 bits):
+// the d/8 threads of one row sit in consecutive lanes, so the row's max |x| is a shuffle
+// reduction among them. scale = max|x| / 448 and each code is E4M3(x / scale), both
+// divisions in IEEE fp32, the conversion rounding to nearest even with saturation. The
+// statistics are still taken from the bf16 key.
 #include "common.cuh"
 #include "internal.h"
 
@@ -46,9 +53,42 @@ __device__ __forceinline__ void fold8(const uint4& k, uint4& mx, uint4& mn) {
     mn = make_uint4(nw[0], nw[1], nw[2], nw[3]);
 }
 
-template <int D>
+// Max |x| of the 8 bf16 values of a 16-byte chunk.
+__device__ __forceinline__ float absmax8(const uint4& v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        m = fmaxf(m, fmaxf(fabsf(bf(w[i] & 0xffffu)), fabsf(bf(w[i] >> 16))));
+    return m;
+}
+
+// E4M3 codes of the 8 bf16 values of a chunk divided by s (s > 0), code i in byte i.
+__device__ __forceinline__ uint2 quant8(const uint4& v, float s) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __fdiv_rn(bf(w[i] & 0xffffu), s);
+        x[2 * i + 1] = __fdiv_rn(bf(w[i] >> 16), s);
+    }
+    return make_uint2(f32x4_to_e4m3(x[0], x[1], x[2], x[3]), f32x4_to_e4m3(x[4], x[5], x[6], x[7]));
+}
+
+// Row scale and codes of one 8-channel chunk; `mask` holds the lanes of this warp in the
+// loop, and the VPR lanes of a row are consecutive and all in it.
+template <int VPR>
+__device__ __forceinline__ uint2 quant_row_chunk(const uint4& v, unsigned mask, float& scale) {
+    float m = absmax8(v);
+#pragma unroll
+    for (int off = 1; off < VPR; off <<= 1) m = fmaxf(m, __shfl_xor_sync(mask, m, off));
+    scale = __fdiv_rn(m, 448.0f);
+    return scale > 0.f ? quant8(v, scale) : make_uint2(0u, 0u);
+}
+
+template <int D, bool F8>
 __global__ void __launch_bounds__(kAppendMaxThreads)
-kv_append_kernel(dattn_kv_layout L, uint16_t* __restrict__ k_pool, uint16_t* __restrict__ v_pool,
+kv_append_kernel(dattn_kv_layout L, void* __restrict__ k_pool_v, void* __restrict__ v_pool_v,
                  uint16_t* __restrict__ stats, const uint16_t* __restrict__ k_new,
                  const uint16_t* __restrict__ v_new, int32_t T, int32_t* seq_lens,
                  int32_t update_in_place, int32_t* dev_err) {
@@ -79,8 +119,16 @@ kv_append_kernel(dattn_kv_layout L, uint16_t* __restrict__ k_pool, uint16_t* __r
     const int32_t i_hi = min(pos0 + T, base + (c + 1) * kAppendWindow) - pos0;
     const int32_t* bt = L.block_table + (int64_t)b * L.max_pages_per_req;
     const int32_t lpg = P >> 4;
+    uint16_t* k_pool = static_cast<uint16_t*>(k_pool_v);
+    uint16_t* v_pool = static_cast<uint16_t*>(v_pool_v);
+    uint8_t* k_code = static_cast<uint8_t*>(k_pool_v);
+    uint8_t* v_code = static_cast<uint8_t*>(v_pool_v);
 
     for (int32_t item = tid; item < Hkv * VPR && i_lo < i_hi; item += blockDim.x) {
+        // lanes of this warp inside the loop: a prefix of the warp, whole rows only
+        const int32_t warp_items = Hkv * VPR - (item - (tid & 31));
+        const unsigned mask = warp_items >= 32 ? 0xffffffffu : ((1u << warp_items) - 1u);
+        (void)mask;
         const int32_t h = item / VPR, c8 = item - h * VPR;
         int32_t cur_lp = -1, page = -1;
         int32_t cur_lq = -1;
@@ -109,7 +157,21 @@ kv_append_kernel(dattn_kv_layout L, uint16_t* __restrict__ k_pool, uint16_t* __r
                     else page = pg;
                 }
             }
-            if (page >= 0) {
+            if constexpr (F8) {
+                // every lane of a row takes part in the reductions, mapped page or not
+                float ks, vs;
+                const uint2 kc = quant_row_chunk<VPR>(kv, mask, ks);
+                const uint2 vc = quant_row_chunk<VPR>(vv, mask, vs);
+                if (page >= 0) {
+                    const int64_t row = ((int64_t)page * Hkv + h) * P + (t - lp * P);
+                    *reinterpret_cast<uint2*>(k_code + row * D + c8 * 8) = kc;
+                    *reinterpret_cast<uint2*>(v_code + row * D + c8 * 8) = vc;
+                    if (c8 == 0) {
+                        L.k_scale[row] = ks;
+                        L.v_scale[row] = vs;
+                    }
+                }
+            } else if (page >= 0) {
                 const int64_t dst = (((int64_t)page * Hkv + h) * P + (t - lp * P)) * D + c8 * 8;
                 *reinterpret_cast<uint4*>(k_pool + dst) = kv;
                 *reinterpret_cast<uint4*>(v_pool + dst) = vv;
@@ -157,7 +219,7 @@ __global__ void advance_lengths_kernel(int32_t* seq_lens, int32_t B, int32_t T) 
 
 }  // namespace
 
-dattn_status_t launch_kv_append(const dattn_kv_layout& L, uint16_t* k_pool, uint16_t* v_pool,
+dattn_status_t launch_kv_append(const dattn_kv_layout& L, void* k_pool, void* v_pool,
                                 uint16_t* stats, const uint16_t* k_new, const uint16_t* v_new,
                                 int32_t B, int32_t T, int32_t* seq_lens, int32_t* dev_err,
                                 cudaStream_t stream) {
@@ -169,13 +231,11 @@ dattn_status_t launch_kv_append(const dattn_kv_layout& L, uint16_t* k_pool, uint
     const int32_t inplace = single ? 1 : 0;
     const int32_t items = L.num_kv_heads * (L.head_dim / 8);
     const dim3 block(min(kAppendMaxThreads, (items + 31) / 32 * 32));
-    cudaError_t e;
-    if (L.head_dim == 64)
-        e = launch_pdl(kv_append_kernel<64>, grid, block, 0, stream, L, k_pool, v_pool, stats,
-                       k_new, v_new, T, seq_lens, inplace, dev_err);
-    else
-        e = launch_pdl(kv_append_kernel<128>, grid, block, 0, stream, L, k_pool, v_pool, stats,
-                       k_new, v_new, T, seq_lens, inplace, dev_err);
+    const bool f8 = L.kv_format == DATTN_KV_FP8_E4M3;
+    auto kern = L.head_dim == 64 ? (f8 ? kv_append_kernel<64, true> : kv_append_kernel<64, false>)
+                                 : (f8 ? kv_append_kernel<128, true> : kv_append_kernel<128, false>);
+    const cudaError_t e = launch_pdl(kern, grid, block, 0, stream, L, k_pool, v_pool, stats,
+                                     k_new, v_new, T, seq_lens, inplace, dev_err);
     if (e != cudaSuccess) return DATTN_ERR_CUDA;
     if (!single) {
         if (launch_pdl(advance_lengths_kernel, dim3((B + 255) / 256), dim3(256), 0, stream,

@@ -236,17 +236,6 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                  : "memory");
 }
 
-// Bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16), completing on
-// the barrier's transaction count, with an L2 policy for the source.
-__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-        : "memory");
-}
-
 // D: head_dim; HG: query heads scored per KV head (4 or 8, unused ones masked);
 // LPG: logical pages per physical page (P / 16, a power of two).
 template <int D, int HG, int LPG>

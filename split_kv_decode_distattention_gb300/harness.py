@@ -7,28 +7,38 @@ from __future__ import annotations
 
 import torch
 
-from . import (KVLayout, SparseConfig, Workspace, dattn_decode, dattn_kv_append,
-               dattn_page_select)
+from . import (KV_BF16, KV_FP8_E4M3, KVLayout, SparseConfig, Workspace, dattn_decode,
+               dattn_kv_append, dattn_page_select)
 from .workloads import Case
 
 
 class PagedCache:
-    """Pool [num_pages][Hkv][P][d] (K and V) plus statistics, block table and lengths."""
+    """Pool [num_pages][Hkv][P][d] (K and V) plus statistics, block table and lengths.
+
+    kv_format KV_BF16 keeps bf16 values; KV_FP8_E4M3 keeps uint8 E4M3 codes plus one float32
+    scale per (token, KV head) row in k_scale / v_scale [num_pages][Hkv][P].
+    """
 
     def __init__(self, case: Case, device="cuda", with_stats: bool = False, fill: bool = True,
-                 chunk_tokens: int = 8192, zero_pool: bool = False):
+                 chunk_tokens: int = 8192, zero_pool: bool = False, kv_format: int = KV_BF16):
         self.case = case
         self.device = torch.device(device)
         c = case
         alloc = torch.zeros if zero_pool else torch.empty
-        self.k_pool = alloc(c.num_pages, c.Hkv, c.P, c.d, dtype=torch.bfloat16, device=device)
-        self.v_pool = alloc(c.num_pages, c.Hkv, c.P, c.d, dtype=torch.bfloat16, device=device)
+        self.kv_format = kv_format
+        elem = torch.uint8 if kv_format == KV_FP8_E4M3 else torch.bfloat16
+        self.k_pool = alloc(c.num_pages, c.Hkv, c.P, c.d, dtype=elem, device=device)
+        self.v_pool = alloc(c.num_pages, c.Hkv, c.P, c.d, dtype=elem, device=device)
+        self.k_scale = self.v_scale = None
+        if kv_format == KV_FP8_E4M3:
+            self.k_scale = alloc(c.num_pages, c.Hkv, c.P, dtype=torch.float32, device=device)
+            self.v_scale = alloc(c.num_pages, c.Hkv, c.P, dtype=torch.float32, device=device)
         self.stats = None
         if with_stats:
             self.stats = alloc(c.num_pages, c.Hkv, c.P // 16, 2, c.d, dtype=torch.bfloat16,
                                device=device)
         self.block_table = torch.as_tensor(c.block_table, dtype=torch.int32, device=device)
-        self.layout = KVLayout(c.num_pages, c.Hkv, c.d, c.P, self.block_table)
+        self.layout = self._layout(self.block_table)
         self.seq_lens = torch.zeros(c.B, dtype=torch.int32, device=device)
         self.lens = [0] * c.B  # host mirror of seq_lens
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=device)
@@ -37,9 +47,13 @@ class PagedCache:
         if fill:
             self.fill()
 
-    def _row_layout(self, b: int) -> KVLayout:
+    def _layout(self, block_table) -> KVLayout:
         c = self.case
-        return KVLayout(c.num_pages, c.Hkv, c.d, c.P, self.block_table[b:b + 1])
+        return KVLayout(c.num_pages, c.Hkv, c.d, c.P, block_table, self.kv_format,
+                        self.k_scale, self.v_scale)
+
+    def _row_layout(self, b: int) -> KVLayout:
+        return self._layout(self.block_table[b:b + 1])
 
     def fill(self, lens=None):
         """Append each request's tokens up to lens (default: the case's step-0 lengths)."""
