@@ -11,6 +11,10 @@ roofline are reported beside it. L2 is flushed before every timed step whose K/V
 four times the L2; larger steps evict it themselves and run back to back.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl dattn|reference]
+                  [--kv-format bf16|fp8]
+
+--kv-format fp8 runs the same workload over the 8-bit pool (FP8 E4M3 codes with one fp32
+scale per (token, KV head) row): a K or V row then moves d + 4 bytes instead of 2 d.
 
 --impl reference times the CPU oracle (test infrastructure) on the host cores over a
 bounded sample of the same workload and prints the same JSON line with "impl": "reference".
@@ -60,6 +64,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="mha-32k", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--impl", default="dattn", choices=["dattn", "reference"])
+    ap.add_argument("--kv-format", default="bf16", choices=["bf16", "fp8"],
+                    help="element format of the paged KV pool")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling only)")
     ap.add_argument("--ctx", type=int, default=0, help="override the context (profiling only)")
@@ -103,15 +109,21 @@ def make_case(args):
     return case
 
 
-def step_bytes(case, lens_after, sparse_sel_step: bool) -> dict:
+def row_bytes(d: int, fp8: bool) -> int:
+    """Bytes of one K (or V) row of one token and KV head in the pool."""
+    return d + 4 if fp8 else 2 * d
+
+
+def step_bytes(case, lens_after, sparse_sel_step: bool, fp8: bool = False) -> dict:
     """Algorithmic bytes of one layer-step, given the lengths after the append."""
     B, Hq, Hkv, d, P = case.B, case.Hq, case.Hkv, case.d, case.P
+    rb = row_bytes(d, fp8)
     q_bytes = B * Hq * d * 2
     out_bytes = B * Hq * d * 4 + 2 * B * Hq * 4
-    new_kv = B * Hkv * d * 2 * 2 * 2  # read k_new/v_new, write into the pool
+    new_kv = B * Hkv * (d * 2 + rb) * 2  # read k_new/v_new (bf16), write into the pool
     bt = sum(-(-L // P) for L in lens_after) * 4
     if case.head_kind is None:
-        kv = sum(lens_after) * Hkv * d * 2 * 2
+        kv = sum(lens_after) * Hkv * rb * 2
         decode = kv + q_bytes + out_bytes + bt + B * 4
         return {"decode": decode, "append": new_kv, "select": 0,
                 "step": decode + new_kv}
@@ -121,11 +133,11 @@ def step_bytes(case, lens_after, sparse_sel_step: bool) -> dict:
     nden = sum(1 for k in kinds if k == 0)
     kv = 0
     for L in lens_after:
-        kv += nden * L * d * 4
-        kv += nret * min(case.top_k * P, L) * d * 4
+        kv += nden * L * rb * 2
+        kv += nret * min(case.top_k * P, L) * rb * 2
         s_end = min(case.sinks, L)
         l0 = max(case.sinks, L - case.local)
-        kv += nstr * (s_end + max(0, L - l0)) * d * 4
+        kv += nstr * (s_end + max(0, L - l0)) * rb * 2
     sel_rows = B * nret * case.top_k * 4
     decode = kv + q_bytes + out_bytes + sel_rows + B * 4
     stats = sum(L // 16 + (1 if L % 16 else 0) for L in lens_after) * nret * 2 * d * 2
@@ -210,6 +222,10 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def traffic_key(args) -> str:
+    return args.config + ("/fp8" if args.kv_format == "fp8" else "")
+
+
 def traffic_record(config: str):
     """DRAM bytes per launch of the decode kernel from the committed ncu summary, if it was
     taken on the current kernel sources."""
@@ -258,7 +274,9 @@ def run_dattn(args, rank: int, world: int):
     dev = torch.device("cuda", torch.cuda.current_device())
     case = make_case(args)
     sparse = case.head_kind is not None
-    cache = PagedCache(case, dev, with_stats=sparse, chunk_tokens=16384)
+    fp8 = args.kv_format == "fp8"
+    cache = PagedCache(case, dev, with_stats=sparse, chunk_tokens=16384,
+                       kv_format=dattn.KV_FP8_E4M3 if fp8 else dattn.KV_BF16)
     B, Hq, d = case.B, case.Hq, case.d
     ws = cache.workspace(top_k=case.top_k, num_splits=args.num_splits)
     out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
@@ -282,7 +300,7 @@ def run_dattn(args, rank: int, world: int):
     # previous step left there, so it is timed back to back; smaller steps are preceded by
     # an L2 flush (see L2Flush).
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    sb0 = step_bytes(case, list(cache.lens), sparse)
+    sb0 = step_bytes(case, list(cache.lens), sparse, fp8)
     do_flush = sb0["decode"] < 4 * l2 or args.flush
     flush = L2Flush(dev)
     torch.cuda.synchronize()
@@ -370,7 +388,7 @@ def run_dattn(args, rank: int, world: int):
             launches += n1 + n2
         e1.record(stream)
         lens_after = [L + i + 1 for L in lens0]
-        sb = step_bytes(case, lens_after, sparse and s % case.reuse == 0)
+        sb = step_bytes(case, lens_after, sparse and s % case.reuse == 0, fp8)
         bytes_total += sb["step"]
         step_ms.append((e0, e1))
         if kev is not None:
@@ -525,7 +543,8 @@ def run_e2e(args, case, cache, ws, spc, sel, flush, dev):
             e1.record(stream)
             pairs.append((e0, e1))
         lens_after = [L + i + 1 for L in lens0]
-        tot_bytes += step_bytes(case, lens_after, spc is not None and i % case.reuse == 0)["step"]
+        tot_bytes += step_bytes(case, lens_after, spc is not None and i % case.reuse == 0,
+                                args.kv_format == "fp8")["step"]
     if flush is None:
         e_all1.record(stream)
     torch.cuda.synchronize()
@@ -540,9 +559,10 @@ def run_e2e(args, case, cache, ws, spc, sel, flush, dev):
 
 # ------------------------------------------------------------------------------ CPU oracle
 
-def oracle_sample(case, device, max_pairs: int, seed_step: int = 0):
+def oracle_sample(case, device, max_pairs: int, seed_step: int = 0, fp8: bool = False):
     """Host copies of a bounded sample of the workload: evenly spaced (request, query head)
-    pairs over their full contexts. Only the KV heads the sample reads are copied."""
+    pairs over their full contexts. Only the KV heads the sample reads are copied. With fp8
+    the rows are the oracle's dequantized 8-bit values (float64), made before any timing."""
     import oracle
     allp = [(b, h) for b in range(case.B) for h in range(case.Hq)]
     stride = max(1, len(allp) // max_pairs)
@@ -564,21 +584,28 @@ def oracle_sample(case, device, max_pairs: int, seed_step: int = 0):
                 arrs[h][0][t0:t1] = oracle.bf16_bits(K[:, h])
                 arrs[h][1][t0:t1] = oracle.bf16_bits(V[:, h])
         for h in kvhs:
-            kv[(b, h)] = arrs[h]
+            kv[(b, h)] = dequantized(arrs[h]) if fp8 else arrs[h]
     return q, pairs, kv
 
 
-def time_oracle(case, q, pairs, kv, nthreads):
+def dequantized(kv):
+    """The oracle's 8-bit round trip of (K, V) rows: float64 code * scale."""
+    import oracle
+    return tuple(oracle.dequantize_rows_fp8(*oracle.quantize_rows_fp8(x)) for x in kv)
+
+
+def time_oracle(case, q, pairs, kv, nthreads, fp8: bool = False):
     """Wall time of the oracle's dense attention over the sampled pairs, run on nthreads
     host threads (each call is one plain C routine that releases the GIL)."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
+    attend = oracle.attention_f64 if fp8 else oracle.attention
 
     def one(pair):
         b, h = pair
         K, V = kv[(b, h // case.g)]
-        oracle.attention(q[b, h], K, V, case.scale)
-        return K.shape[0] * case.d * 2 * 2
+        attend(q[b, h], K, V, case.scale)
+        return K.shape[0] * row_bytes(case.d, fp8) * 2
 
     t0 = time.perf_counter()
     with ThreadPoolExecutor(max_workers=nthreads) as ex:
@@ -588,7 +615,7 @@ def time_oracle(case, q, pairs, kv, nthreads):
 
 def sparse_oracle_sample(case, device, n_ret: int = 2, n_str: int = 2):
     """Host copies for the oracle's block-sparse step: full K/V of n_ret retrieval KV heads
-    and the sink and local-window tokens of n_str streaming KV heads of request 0."""
+    and the sink and local-window tokens of n_str streaming KV heads of request 0 (bf16)."""
     import oracle
     b, L = 0, case.lens[0]
     kinds = list(case.head_kind)
@@ -617,9 +644,13 @@ class SparseOracleStep:
     start of each reuse window and attends the selected tokens; a streaming head attends its
     sinks and local window. Bytes are counted as the GPU metric counts them."""
 
-    def __init__(self, case, q, b, ret, strm, kv, nthreads):
+    def __init__(self, case, q, b, ret, strm, kv, nthreads, fp8: bool = False):
         from concurrent.futures import ThreadPoolExecutor
         self.case, self.q, self.b, self.ret, self.strm, self.kv = case, q, b, ret, strm, kv
+        # with fp8 the attention runs over the dequantized 8-bit rows (the selection still
+        # reads the bf16 keys, as the statistics do)
+        self.fp8 = fp8
+        self.att = {h: dequantized(kv[h]) for h in kv} if fp8 else kv
         self.used = min(nthreads, len(ret) + len(strm))
         self.ex = ThreadPoolExecutor(max_workers=self.used)
         self.sels = {}
@@ -643,15 +674,17 @@ class SparseOracleStep:
         c, b = self.case, self.b
         L, g = c.lens[b], c.g
 
+        attend = oracle.attention_f64 if self.fp8 else oracle.attention
+
         def one(h):
-            K, V = self.kv[h]
+            K, V = self.att[h]
             if h in self.ret:
                 rows = oracle.sparse_rows(1, L, c.P, self.sels[h], c.sinks, c.local)
             else:
                 rows = np.arange(K.shape[0], dtype=np.int64)
             for j in range(g):
-                oracle.attention(self.q[b, h * g + j], K, V, c.scale, rows=rows)
-            return rows.shape[0] * c.d * 2 * 2
+                attend(self.q[b, h * g + j], K, V, c.scale, rows=rows)
+            return rows.shape[0] * row_bytes(c.d, self.fp8) * 2
         t0 = time.perf_counter()
         nbytes = sum(self.ex.map(one, self.ret + self.strm))
         return time.perf_counter() - t0, nbytes
@@ -665,12 +698,12 @@ class SparseOracleStep:
         return secs, nbytes
 
 
-def cpu_baseline_sparse(case, device):
+def cpu_baseline_sparse(case, device, fp8: bool = False):
     import oracle
     oracle.load()
     nthreads = len(os.sched_getaffinity(0))
     q, b, ret, strm, kv = sparse_oracle_sample(case, device)
-    st = SparseOracleStep(case, q, b, ret, strm, kv, nthreads)
+    st = SparseOracleStep(case, q, b, ret, strm, kv, nthreads, fp8)
     secs, nbytes = st.window()
     windows = 1
     while secs * st.used < 10.0 and windows < 8:
@@ -684,31 +717,32 @@ def cpu_baseline_sparse(case, device):
                       f"window(s) of 1 selection + {case.reuse} steps, {secs:.1f} s wall"}
 
 
-def cpu_baseline(case, device):
+def cpu_baseline(case, device, fp8: bool = False):
     import oracle
     if case.head_kind is not None:
-        return cpu_baseline_sparse(case, device)
+        return cpu_baseline_sparse(case, device, fp8)
     oracle.load()
     nthreads = len(os.sched_getaffinity(0))
-    per_pair = max(1, sum(case.lens) // case.B) * case.d * 4
+    per_pair = max(1, sum(case.lens) // case.B) * case.d * (16 if fp8 else 4)
     budget = max(nthreads, min(case.B * case.Hq, int(4e9 // per_pair)))
-    q, pairs, kv = oracle_sample(case, device, budget)
+    q, pairs, kv = oracle_sample(case, device, budget, fp8=fp8)
     # repeat the sample until about 10 s of CPU work has been timed
-    secs, nbytes, used = time_oracle(case, q, pairs, kv, nthreads)
+    secs, nbytes, used = time_oracle(case, q, pairs, kv, nthreads, fp8)
     reps = 1
     while secs * used < 10.0 and reps < 64:
-        s2, n2, _ = time_oracle(case, q, pairs, kv, nthreads)
+        s2, n2, _ = time_oracle(case, q, pairs, kv, nthreads, fp8)
         secs, nbytes, reps = secs + s2, nbytes + n2, reps + 1
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": used,
             "kind": "oracle",
             "sample": f"{len(pairs)} of {case.B * case.Hq} (request, query head) pairs of the "
-                      f"{case.name} workload over their full contexts (fp64 dense attention), "
+                      f"{case.name} workload over their full contexts (fp64 dense attention"
+                      f"{' over the dequantized 8-bit rows' if fp8 else ''}), "
                       f"repeated {reps}x: {secs:.1f} s wall on {used} threads"}
 
 
 def run_reference_sparse(args, world, case, device, nthreads):
     q, b, ret, strm, kv = sparse_oracle_sample(case, device)
-    st = SparseOracleStep(case, q, b, ret, strm, kv, nthreads)
+    st = SparseOracleStep(case, q, b, ret, strm, kv, nthreads, args.kv_format == "fp8")
     st.select()
     for _ in range(min(args.warmup, 1)):
         st.attend()
@@ -752,14 +786,15 @@ def run_reference(args, rank, world):
     if case.head_kind is not None:
         run_reference_sparse(args, world, case, device, nthreads)
         return
-    per_pair = max(1, sum(case.lens) // case.B) * case.d * 4
+    fp8 = args.kv_format == "fp8"
+    per_pair = max(1, sum(case.lens) // case.B) * case.d * (16 if fp8 else 4)
     budget = max(nthreads, min(case.B * case.Hq, int(1e9 // per_pair)))
-    q, pairs, kv = oracle_sample(case, device, budget)
+    q, pairs, kv = oracle_sample(case, device, budget, fp8=fp8)
     for _ in range(min(args.warmup, 1)):
-        time_oracle(case, q, pairs[:nthreads], kv, nthreads)
+        time_oracle(case, q, pairs[:nthreads], kv, nthreads, fp8)
     times, used, nbytes = [], nthreads, 0
     for _ in range(args.steps):
-        secs, nb, used = time_oracle(case, q, pairs, kv, nthreads)
+        secs, nb, used = time_oracle(case, q, pairs, kv, nthreads, fp8)
         times.append(secs)
         nbytes += nb
     total = sum(times)
@@ -789,6 +824,8 @@ def config_obj(case, args):
          "context_tokens": (case.lens[0] if len(set(case.lens)) == 1 else
                             f"{min(case.lens)}-{max(case.lens)} (sum {sum(case.lens)})"),
          "seed": args.seed,
+         "kv_format": ("fp8_e4m3 codes + one fp32 scale per (token, KV head) row"
+                       if args.kv_format == "fp8" else "bf16"),
          "parallelism": "replicas" if args.gpus > 1 else "single GPU",
          "step": ("dattn_kv_append (1 token/request) + dattn_decode" +
                   (" + dattn_page_select every 16 steps (block-sparse)"
@@ -819,7 +856,7 @@ def main():
     case = res["case"]
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(case, "cuda")
+        cpu = cpu_baseline(case, "cuda", args.kv_format == "fp8")
     if world > 1:
         dist.destroy_process_group()
     if rank != 0:
@@ -830,12 +867,15 @@ def main():
     dec_avg_ms = sum(res["dec_ms"]) / len(res["dec_ms"])
     achieved = res["dec_bytes"] / (dec_avg_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
-    traffic = traffic_record(args.config)
+    traffic = traffic_record(traffic_key(args))
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16 K/V/Q)",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": ("fp8_e4m3 KV (fp16 tensor-core products, fp32 accumulate)"
+                  if args.kv_format == "fp8" else "bf16"),
+        "data": "synthetic (seeded N(0,1) bf16 K/V/Q" +
+                ("; K/V quantized to 8 bits by the append)" if args.kv_format == "fp8" else ")"),
         "us_per_layer_step": round(ms_step * 1e3, 2),
         "frac_of_8tbs": round(value / ROOFLINE_8TBS, 4),
         "config": dict(config_obj(case, args), l2=res["l2_policy"]),

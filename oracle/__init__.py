@@ -69,6 +69,8 @@ _SIGS = {
     "orc_e4m3_code": (ctypes.c_uint8, [ctypes.c_float]),
     "orc_quantize_row_fp8": (None, [_P, _I, _P, _P]),
     "orc_dequantize_row_fp8": (None, [_P, ctypes.c_float, _I, _P]),
+    "orc_quantize_rows_fp8": (None, [_P, _I64, _I, _P, _P]),
+    "orc_dequantize_rows_fp8": (None, [_P, _P, _I64, _I, _P]),
     "orc_kv_write_fp8": (_I64, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _I64, _I64]),
     "orc_attention_f64": (None, [_P, _P, _P, _I64, _I, _P, _I64, _D, _P, _P, _P]),
     "orc_partial_f64": (None, [_P, _P, _P, _I64, _I, _P, _I64, _D, _P, _P, _P]),
@@ -301,8 +303,7 @@ def quantize_rows_fp8(X, lib=None):
     X2 = np.ascontiguousarray(X.reshape(-1, d))
     codes = np.zeros(X2.shape, np.uint8)
     scales = np.zeros(X2.shape[0], np.float32)
-    for r in range(X2.shape[0]):
-        lib.orc_quantize_row_fp8(_ptr(X2[r]), d, _ptr(codes[r]), _ptr(scales[r:r + 1]))
+    lib.orc_quantize_rows_fp8(_ptr(X2), X2.shape[0], d, _ptr(codes), _ptr(scales))
     return codes.reshape(X.shape), scales.reshape(X.shape[:-1])
 
 
@@ -314,8 +315,7 @@ def dequantize_rows_fp8(codes, scales, lib=None) -> np.ndarray:
     c2 = codes.reshape(-1, d)
     s2 = np.ascontiguousarray(np.asarray(scales, np.float32).reshape(-1))
     out = np.zeros(c2.shape, np.float64)
-    for r in range(c2.shape[0]):
-        lib.orc_dequantize_row_fp8(_ptr(c2[r]), float(s2[r]), d, _ptr(out[r]))
+    lib.orc_dequantize_rows_fp8(_ptr(c2), _ptr(s2), c2.shape[0], d, _ptr(out))
     return out.reshape(codes.shape)
 
 

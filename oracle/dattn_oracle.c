@@ -466,6 +466,19 @@ void orc_dequantize_row_fp8(const uint8_t *codes, float scale, int d, double *ou
     for (int c = 0; c < d; ++c) out[c] = orc_e4m3_value(codes[c]) * (double)scale;
 }
 
+/* The two row functions above over n consecutive rows of d values. */
+void orc_quantize_rows_fp8(const uint16_t *x, int64_t n, int d, uint8_t *codes, float *scales)
+{
+    for (int64_t r = 0; r < n; ++r) orc_quantize_row_fp8(x + r * d, d, codes + r * d, scales + r);
+}
+
+void orc_dequantize_rows_fp8(const uint8_t *codes, const float *scales, int64_t n, int d,
+                             double *out)
+{
+    for (int64_t r = 0; r < n; ++r)
+        orc_dequantize_row_fp8(codes + r * d, scales[r], d, out + r * d);
+}
+
 /*
  * Paged write of T new tokens in the 8-bit format [LS §4.2, with reading R10]: the codes of
  * each (token, KV head) row go to k_pool / v_pool [num_pages][Hkv][P][d] and its scale to

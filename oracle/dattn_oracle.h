@@ -51,6 +51,9 @@ uint8_t orc_e4m3_code(float f);
 void orc_quantize_row_fp8(const uint16_t *x, int d, uint8_t *codes, float *scale);
 
 void orc_dequantize_row_fp8(const uint8_t *codes, float scale, int d, double *out);
+void orc_quantize_rows_fp8(const uint16_t *x, int64_t n, int d, uint8_t *codes, float *scales);
+void orc_dequantize_rows_fp8(const uint8_t *codes, const float *scales, int64_t n, int d,
+                             double *out);
 
 int64_t orc_kv_write_fp8(uint8_t *k_pool, uint8_t *v_pool, float *k_scale, float *v_scale,
                          int Hkv, int P, int d, const int32_t *block_table_row, int max_pages,

@@ -12,21 +12,20 @@
 // streaming heads, fused into the same kernel as the retrieval heads).
 //
 // GB300 design. The page tile of one (page, KV head) is contiguous in HBM. A producer warp
-// streams 16-token K and V row groups into an 8-stage shared-memory ring with one 3-D TMA
-// box each ({64, 16, d/64}: 128-byte swizzle, evict-first L2 policy, completion on
-// mbarriers). Four
-// consumer warps each own every fourth stage. A consumer runs the small QK^T tile with
-// tokens as the M dimension and the GQA group as N (mma.sync m16n8k16, bf16 in, fp32
-// accumulate). It does an online softmax in base 2 with warp shuffles, transposes P with
-// movmatrix, and accumulates O^T = V^T P^T with P split into two bf16 terms, so the weights
-// keep 16 significant bits. The work of all (segment = request or chunk, KV head) pairs is
-// laid end to end in 16-token tiles and cut into equal contiguous ranges, one per CTA. Each
-// CTA therefore gets the same number of bytes, whatever the length mix. A segment that
-// lies inside one CTA is finished there. A segment cut across CTAs leaves one partial
-// triple per CTA in the workspace, and the CTA that arrives last (atomic counter) merges
-// them. No CTA ever waits on another. The 8-bit pool (FP8 E4M3 codes with one fp32 scale per
-// row) streams half the bytes through the same pipeline and runs on fp16 tensor cores (see
-// Consumer).
+// streams 16-token K and V row groups into an 8-stage (8-bit pool: 12-stage) shared-memory
+// ring with one 3-D TMA box each ({64, 16, d/64}: 128-byte swizzle, evict-first L2 policy,
+// completion on mbarriers). Four consumer warps each own every fourth stage. A consumer
+// runs the small QK^T tile with tokens as the M dimension and the GQA group as N (mma.sync
+// m16n8k16, bf16 in, fp32 accumulate). It does an online softmax in base 2 with warp
+// shuffles, transposes P with movmatrix, and accumulates O^T = V^T P^T with P split into
+// two bf16 terms, so the weights keep 16 significant bits. The work of all (segment =
+// request or chunk, KV head) pairs is laid end to end in 16-token tiles and cut into equal
+// contiguous ranges, one per CTA. Each CTA therefore gets the same number of bytes,
+// whatever the length mix. A segment that lies inside one CTA is finished there. A segment
+// cut across CTAs leaves one partial triple per CTA in the workspace, and the CTA that
+// arrives last (atomic counter) merges them. No CTA ever waits on another. The 8-bit pool
+// (FP8 E4M3 codes with one fp32 scale per row) streams half the bytes through the same
+// pipeline and runs on fp16 tensor cores (see Consumer).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -40,12 +39,14 @@ namespace {
 
 #define kNegInf (-__int_as_float(0x7f800000))
 
+constexpr int kIssue = kConsumerWarps;  // tiles the producer issues side by side
+
 struct Smem {
     uint8_t* base;
     AttnSmem L;
     __device__ uint32_t full_bar(int s) const { return smem_u32(base + L.bars) + 8u * s; }
     __device__ uint32_t empty_bar(int s) const {
-        return smem_u32(base + L.bars) + 8u * (kStages + s);
+        return smem_u32(base + L.bars) + 8u * (L.nstages + s);
     }
     __device__ int32_t* meta() const { return reinterpret_cast<int32_t*>(base + L.meta); }
     __device__ volatile int* abort_flag() const {
@@ -586,11 +587,12 @@ attention_kernel(const __grid_constant__ AttnParams p,
     sm.L = attn_smem_layout(D, p.g, p.nitems, p.Hkv, p.mode == MODE_SPARSE, F8);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t G = gridDim.x, cta = blockIdx.x;
+    constexpr int NS = attn_stages(F8);
 
     // ---------------------------------------------------------------- setup
     // Before the dependency wait: only state that no kernel of this library writes.
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(sm.full_bar(s), 1);
             mbar_init(sm.empty_bar(s), 1);
         }
@@ -728,7 +730,8 @@ attention_kernel(const __grid_constant__ AttnParams p,
         const uint64_t pol = policy_evict_first();
         const uint32_t tile_bytes = (F8 ? 16u : 32u) * (uint32_t)D;
         const uint32_t tx = 2u * tile_bytes + (F8 ? 128u : 0u);
-        int32_t k = 0;  // real tiles issued so far: tile k uses stage k % kStages
+        const uint32_t stages0 = smem_u32(sm.base + sm.L.stages);
+        int32_t k = 0;  // real tiles issued so far: tile k uses stage k % NS
         bool stop = false;
         int32_t s = s_first, cs, real, r0, r1;
         while (!stop && plan.next_piece(s, X0, X1, cs, real, r0, r1)) {
@@ -736,52 +739,58 @@ attention_kernel(const __grid_constant__ AttnParams p,
                 TileRef ref{0, 1 << 16};
                 if (base + lane < r1) ref = resolve_tile(p, sm, s, base + lane);
                 const int32_t nb = min(32, r1 - base);
-                for (int32_t j = 0; j < nb; ++j, ++k) {
-                    const int32_t y = __shfl_sync(0xffffffffu, ref.y, j);
-                    const int32_t lohi = __shfl_sync(0xffffffffu, ref.lohi, j);
-                    const int stg = k % kStages;
+                // Tiles go out kIssue at a time, lane j of a group taking tile k + j: it waits
+                // for its stage to be released, posts the tile's token range, arms the full
+                // barrier and issues the tile's copies (K and V boxes; with the 8-bit pool
+                // also the 16 K and 16 V row scales).
+                for (int32_t j0 = 0; j0 < nb; j0 += kIssue) {
+                    const int32_t n = min(kIssue, nb - j0);
+                    const int32_t src = min(j0 + lane, 31);
+                    const int32_t y = __shfl_sync(0xffffffffu, ref.y, src);
+                    const int32_t lohi = __shfl_sync(0xffffffffu, ref.lohi, src);
                     bool ok = true;
-                    if (lane == 0 && k >= kStages)
-                        ok = mbar_wait(sm.empty_bar(stg), ((k / kStages) - 1) & 1,
-                                       sm.abort_flag(), p.dev_err);
-                    if (__shfl_sync(0xffffffffu, ok ? 0 : 1, 0)) {
+                    if (lane < n) {
+                        const int32_t kk = k + lane;
+                        const int stg = kk % NS;
+                        if (kk >= NS)
+                            ok = mbar_wait(sm.empty_bar(stg), ((kk / NS) - 1) & 1,
+                                           sm.abort_flag(), p.dev_err);
+                        if (ok) {
+                            const uint32_t full = sm.full_bar(stg);
+                            sm.meta()[stg] = lohi;
+                            if (lohi >> 16) {
+                                mbar_arrive(full);
+                            } else {
+                                mbar_arrive_expect_tx(full, tx);
+                                const uint32_t dst = stages0 + (uint32_t)stg * sm.L.stage_bytes;
+                                if constexpr (F8) {
+                                    tma_load_2d(dst, &tmap_k, 0, y, full, pol);
+                                    tma_load_2d(dst + tile_bytes, &tmap_v, 0, y, full, pol);
+                                    const uint32_t sc = smem_u32(sm.scales(stg));
+                                    bulk_copy(sc, p.k_scale + y, 64u, full, pol);
+                                    bulk_copy(sc + 64u, p.v_scale + y, 64u, full, pol);
+                                } else {
+                                    tma_load_3d(dst, &tmap_k, 0, y, 0, full, pol);
+                                    tma_load_3d(dst + tile_bytes, &tmap_v, 0, y, 0, full, pol);
+                                }
+                            }
+                        }
+                    }
+                    k += n;
+                    if (__any_sync(0xffffffffu, !ok)) {
                         stop = true;
                         break;
-                    }
-                    const uint32_t full = sm.full_bar(stg);
-                    const uint32_t dst =
-                        smem_u32(sm.base + sm.L.stages) + (uint32_t)stg * sm.L.stage_bytes;
-                    if (lane == 0) {
-                        sm.meta()[stg] = lohi;
-                        if (lohi >> 16) mbar_arrive(full);
-                        else mbar_arrive_expect_tx(full, tx);
-                    }
-                    __syncwarp();
-                    // one instruction, two lanes: lane 0 brings the K tile, lane 1 the V tile
-                    // (8-bit pool: lanes 2 and 3 bring the 16 K and 16 V row scales)
-                    if constexpr (F8) {
-                        if (!(lohi >> 16) && lane < 4) {
-                            if (lane < 2)
-                                tma_load_2d(dst + (lane ? tile_bytes : 0u),
-                                            lane ? &tmap_v : &tmap_k, 0, y, full, pol);
-                            else
-                                bulk_copy(smem_u32(sm.scales(stg)) + (lane - 2u) * 64u,
-                                          (lane == 2 ? p.k_scale : p.v_scale) + y, 64u, full,
-                                          pol);
-                        }
-                    } else if (!(lohi >> 16) && lane < 2) {
-                        tma_load_3d(dst + (lane ? tile_bytes : 0u), lane ? &tmap_v : &tmap_k, 0,
-                                    y, 0, full, pol);
                     }
                 }
             }
             ++s;
         }
-        // after an abort, wait (bounded) for copies still in flight before the CTA exits
+        // after an abort, wait (bounded in total) for copies still in flight before the CTA
+        // exits; stages whose tiles were never issued simply run into the deadline
         if (lane == 0 && *sm.abort_flag()) {
-            for (int32_t kk = max(0, k - kStages); kk < k; ++kk) {
-                const unsigned long long t0 = global_timer_ns();
-                while (!mbar_try_wait(sm.full_bar(kk % kStages), (kk / kStages) & 1) &&
+            const unsigned long long t0 = global_timer_ns();
+            for (int32_t kk = max(0, k - NS); kk < k; ++kk) {
+                while (!mbar_try_wait(sm.full_bar(kk % NS), (kk / NS) & 1) &&
                        global_timer_ns() - t0 < kWaitLimitNs) {
                 }
             }
@@ -814,9 +823,9 @@ attention_kernel(const __grid_constant__ AttnParams p,
         for (int32_t i = (warp - kbase % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
              i < nr; i += kConsumerWarps) {
             const int32_t k = kbase + i;
-            const int stg = k % kStages;
+            const int stg = k % NS;
             // warp-uniform: the tile's ldmatrix / mma / movmatrix are warp-collective
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(sm.full_bar(stg), (k / kStages) & 1,
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(sm.full_bar(stg), (k / NS) & 1,
                                                               sm.abort_flag(), p.dev_err));
             const int32_t lohi = sm.meta()[stg];
             const int lo = lohi & 0xff, hi = (lohi >> 8) & 0xff;

@@ -11,7 +11,13 @@ namespace dattn {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 8;          // pipeline depth; a multiple of kConsumerWarps
+// Pipeline depth, a multiple of kConsumerWarps: consumer warp w takes the tiles k = w mod 4,
+// so it has depth/4 - 1 tiles loading while it works on one. The 8-bit stages are half as
+// large; 12 of them (48 KB for d = 128) keep more bytes in flight per warp without lowering
+// the CTAs per SM, which 16 stages did for grouped heads.
+constexpr int kStagesBf16 = 8;
+constexpr int kStagesF8 = 12;
+__host__ __device__ constexpr int attn_stages(bool f8) { return f8 ? kStagesF8 : kStagesBf16; }
 constexpr int kMaxItems = 4096;     // B (or C) bound
 constexpr int kMaxKvHeads = 256;
 constexpr int kMaxGroup = 8;        // query heads per KV head
@@ -66,19 +72,21 @@ __host__ __device__ inline int32_t slot_floats(int32_t g, int32_t D) {
 // the K tile then the V tile of 16 tokens (bf16: 32*d bytes each; 8-bit: 16*d bytes each);
 // with the 8-bit pool, the stage's 16 K scales and 16 V scales sit in `scales`.
 struct AttnSmem {
-    uint32_t stage_bytes, stages, scales, bars, meta, flags, ws_m, ws_e, ws_o, kind_before,
+    uint32_t nstages, stage_bytes, stages, scales, bars, meta, flags, ws_m, ws_e, ws_o, kind_before,
         kinds, item_start, item_len, scan, total;
 };
 
 __host__ __device__ inline AttnSmem attn_smem_layout(int D, int g, int nitems, int Hkv,
                                                      bool sparse, bool f8) {
     AttnSmem s;
+    const uint32_t ns = (uint32_t)attn_stages(f8);
+    s.nstages = ns;
     s.stage_bytes = (f8 ? 32u : 64u) * (uint32_t)D;
     uint32_t o = 0;
-    s.stages = o;      o += (uint32_t)kStages * s.stage_bytes;
-    s.scales = o;      o += f8 ? (uint32_t)kStages * 128u : 0u;
-    s.bars = o;        o += 2u * kStages * 8u;
-    s.meta = o;        o += kStages * 4u;
+    s.stages = o;      o += ns * s.stage_bytes;
+    s.scales = o;      o += f8 ? ns * 128u : 0u;
+    s.bars = o;        o += 2u * ns * 8u;
+    s.meta = o;        o += ns * 4u;
     s.flags = o;       o += 16u;
     s.ws_m = o;        o += kConsumerWarps * kMaxGroup * 4u;
     s.ws_e = o;        o += kConsumerWarps * kMaxGroup * 4u;
