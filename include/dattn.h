@@ -50,8 +50,10 @@
  *  - Pool layout: k_pool and v_pool are [num_pages][Hkv][P][d] elements of the layout's
  *    kv_format. Every (page, KV head) tile is one contiguous P*d run.
  *  - The 8-bit format (kv_format = DATTN_KV_FP8_E4M3): every (token, KV head) row x of d
- *    values is stored as d one-byte codes plus one fp32 scale in k_scale / v_scale
- *    [num_pages][Hkv][P] (the same place as the row, without d). scale = max_i |x_i| / 448
+ *    values is stored as d one-byte codes plus one fp32 scale. The scales of the 16 tokens
+ *    of logical page lp of (page, KV head) form one 128-byte run of kv_scale
+ *    [num_pages][Hkv][P/16][2][16]: [..][lp][0][j] is the K scale and [..][lp][1][j] the V
+ *    scale of token lp*16 + j of that page. scale = max_i |x_i| / 448
  *    and code_i = E4M3(x_i / scale), both divisions in IEEE fp32; E4M3 is the OCP 8-bit
  *    float (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, largest finite 448),
  *    rounded to nearest even and saturated to +-448. A row with scale 0 has +0 codes. The
@@ -120,8 +122,9 @@ typedef struct dattn_kv_layout {
     const int32_t *block_table; /* (device) [B][max_pages_per_req]; -1 = unmapped */
     int32_t max_pages_per_req;  /* row width of block_table */
     int32_t kv_format;          /* DATTN_KV_BF16 or DATTN_KV_FP8_E4M3 */
-    float *k_scale;             /* (device) fp32 [num_pages][Hkv][P], 16-byte aligned; the 8-bit */
-    float *v_scale;             /* format only (ignored for bf16). Written by dattn_kv_append. */
+    float *kv_scale;            /* (device) fp32 [num_pages][Hkv][P/16][2][16], 16-byte aligned:
+                                   the 8-bit format's row scales (ignored for bf16), written by
+                                   dattn_kv_append; see the layout note above */
 } dattn_kv_layout;
 
 /* Block-sparse decode settings [LV §2.2.2, §3.1.1, §3.1.2]. */
@@ -141,8 +144,7 @@ typedef struct dattn_sparse {
  * [LV §3.1.2: computed at KV-write time].
  *
  *   k_pool, v_pool (device) the pool in the layout's kv_format; for the 8-bit format each
- *                row is quantized as described above and its scales go to layout->k_scale
- *                and layout->v_scale.
+ *                row is quantized as described above and its scales go to layout->kv_scale.
  *   k_new, v_new (device) bf16 [B][T][Hkv][d]. Token t of request b is written at
  *                position seq_lens[b] + t.
  *   stats        (device, nullable) bf16 [num_pages][Hkv][P/16][2][d]. When a token

@@ -49,8 +49,7 @@ class _Layout(ctypes.Structure):
     _fields_ = [("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("block_table", ctypes.c_void_p), ("max_pages_per_req", ctypes.c_int32),
-                ("kv_format", ctypes.c_int32), ("k_scale", ctypes.c_void_p),
-                ("v_scale", ctypes.c_void_p)]
+                ("kv_format", ctypes.c_int32), ("kv_scale", ctypes.c_void_p)]
 
 
 class _Sparse(ctypes.Structure):
@@ -162,23 +161,23 @@ class KVLayout:
     """Shape of a paged pool [num_pages][Hkv][P][d] plus its int32 block table [B][max_pages].
 
     kv_format KV_BF16: the pools hold bf16 values. KV_FP8_E4M3: they hold uint8 E4M3 codes,
-    and k_scale / v_scale (float32 [num_pages][Hkv][P]) hold one scale per row.
+    and kv_scale (float32 [num_pages][Hkv][P/16][2][16]) holds one scale per row: for the 16
+    tokens of each logical page, their K scales, then their V scales.
     """
 
     def __init__(self, num_pages: int, num_kv_heads: int, head_dim: int, page_size: int,
                  block_table: torch.Tensor, kv_format: int = KV_BF16,
-                 k_scale: torch.Tensor | None = None, v_scale: torch.Tensor | None = None):
+                 kv_scale: torch.Tensor | None = None):
         _i32(block_table, "block_table")
         if kv_format == KV_FP8_E4M3:
-            if k_scale is None or v_scale is None:
-                raise ValueError("the 8-bit format needs k_scale and v_scale")
-            _f32(k_scale, "k_scale"); _f32(v_scale, "v_scale")
+            if kv_scale is None:
+                raise ValueError("the 8-bit format needs kv_scale")
+            _f32(kv_scale, "kv_scale")
         self.block_table = block_table  # keeps the tensors alive
-        self.k_scale, self.v_scale = k_scale, v_scale
+        self.kv_scale = kv_scale
         self.c = _Layout(num_pages, num_kv_heads, head_dim, page_size,
                          block_table.data_ptr(), block_table.shape[-1], kv_format,
-                         k_scale.data_ptr() if k_scale is not None else None,
-                         v_scale.data_ptr() if v_scale is not None else None)
+                         kv_scale.data_ptr() if kv_scale is not None else None)
 
     @property
     def kv_format(self): return self.c.kv_format

@@ -49,8 +49,7 @@ dattn_status_t check_layout(const dattn_kv_layout* L) {
     if ((int64_t)L->max_pages_per_req * L->page_size >= (1ll << 30)) return DATTN_ERR_UNSUPPORTED;
     if (L->kv_format != DATTN_KV_BF16 && L->kv_format != DATTN_KV_FP8_E4M3)
         return DATTN_ERR_INVALID_ARG;
-    if (L->kv_format == DATTN_KV_FP8_E4M3 &&
-        (!L->k_scale || !L->v_scale || !aligned16(L->k_scale) || !aligned16(L->v_scale)))
+    if (L->kv_format == DATTN_KV_FP8_E4M3 && (!L->kv_scale || !aligned16(L->kv_scale)))
         return DATTN_ERR_INVALID_ARG;
     return DATTN_OK;
 }
@@ -262,8 +261,7 @@ dattn_status_t dattn_partial(const dattn_kv_layout* layout, const void* k_pool,
     p.nitems = C;
     p.dev_err = dev_err;
     p.f8 = layout->kv_format == DATTN_KV_FP8_E4M3 ? 1 : 0;
-    p.k_scale = layout->k_scale;
-    p.v_scale = layout->v_scale;
+    p.kv_scale = layout->kv_scale;
     return launch_attention(p, k_pool, v_pool, layout->head_dim, num_splits, ws, ws_bytes,
                             static_cast<cudaStream_t>(stream), bound);
 }
@@ -337,8 +335,7 @@ dattn_status_t dattn_decode(const dattn_kv_layout* layout, const void* k_pool,
     p.nitems = B;
     p.dev_err = dev_err;
     p.f8 = layout->kv_format == DATTN_KV_FP8_E4M3 ? 1 : 0;
-    p.k_scale = layout->k_scale;
-    p.v_scale = layout->v_scale;
+    p.kv_scale = layout->kv_scale;
     return launch_attention(p, k_pool, v_pool, layout->head_dim, num_splits, ws, ws_bytes,
                             static_cast<cudaStream_t>(stream), bound);
 }

@@ -729,7 +729,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
         // ------------------------------------------------------------ producer warp
         const uint64_t pol = policy_evict_first();
         const uint32_t tile_bytes = (F8 ? 16u : 32u) * (uint32_t)D;
-        const uint32_t tx = 2u * tile_bytes + (F8 ? 128u : 0u);
+        const uint32_t tx = 2u * tile_bytes + (F8 ? 128u : 0u);  // + the tile's 32 scales
         const uint32_t stages0 = smem_u32(sm.base + sm.L.stages);
         int32_t k = 0;  // real tiles issued so far: tile k uses stage k % NS
         bool stop = false;
@@ -742,7 +742,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
                 // Tiles go out kIssue at a time, lane j of a group taking tile k + j: it waits
                 // for its stage to be released, posts the tile's token range, arms the full
                 // barrier and issues the tile's copies (K and V boxes; with the 8-bit pool
-                // also the 16 K and 16 V row scales).
+                // also the run of 16 K and 16 V row scales).
                 for (int32_t j0 = 0; j0 < nb; j0 += kIssue) {
                     const int32_t n = min(kIssue, nb - j0);
                     const int32_t src = min(j0 + lane, 31);
@@ -766,9 +766,9 @@ attention_kernel(const __grid_constant__ AttnParams p,
                                 if constexpr (F8) {
                                     tma_load_2d(dst, &tmap_k, 0, y, full, pol);
                                     tma_load_2d(dst + tile_bytes, &tmap_v, 0, y, full, pol);
-                                    const uint32_t sc = smem_u32(sm.scales(stg));
-                                    bulk_copy(sc, p.k_scale + y, 64u, full, pol);
-                                    bulk_copy(sc + 64u, p.v_scale + y, 64u, full, pol);
+                                    // the tile's scales: 128 bytes at tile index y / 16
+                                    bulk_copy(smem_u32(sm.scales(stg)), p.kv_scale + 2 * y,
+                                              128u, full, pol);
                                 } else {
                                     tma_load_3d(dst, &tmap_k, 0, y, 0, full, pol);
                                     tma_load_3d(dst + tile_bytes, &tmap_v, 0, y, 0, full, pol);

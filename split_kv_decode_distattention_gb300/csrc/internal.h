@@ -56,10 +56,10 @@ struct AttnParams {
     int32_t nseg;
     int32_t nitems;     // B for dense / sparse, C for partial
     int32_t* dev_err;
-    // 8-bit pool: FP8 E4M3 codes plus one fp32 scale per (token, KV head) row
+    // 8-bit pool: FP8 E4M3 codes plus one fp32 scale per (token, KV head) row; the scales
+    // of a 16-token tile are one 128-byte run [16 K scales][16 V scales]
     int32_t f8;
-    const float* k_scale;
-    const float* v_scale;
+    const float* kv_scale;
 };
 
 // Floats of one workspace slot (a piece's partial): MA [g][D], then m [g] and e [g],

@@ -166,9 +166,10 @@ kv_append_kernel(dattn_kv_layout L, void* __restrict__ k_pool_v, void* __restric
                     const int64_t row = ((int64_t)page * Hkv + h) * P + (t - lp * P);
                     *reinterpret_cast<uint2*>(k_code + row * D + c8 * 8) = kc;
                     *reinterpret_cast<uint2*>(v_code + row * D + c8 * 8) = vc;
-                    if (c8 == 0) {
-                        L.k_scale[row] = ks;
-                        L.v_scale[row] = vs;
+                    if (c8 == 0) {  // [row / 16][K, V][row % 16]
+                        float* sc = L.kv_scale + (row >> 4) * 32 + (row & 15);
+                        sc[0] = ks;
+                        sc[16] = vs;
                     }
                 }
             } else if (page >= 0) {

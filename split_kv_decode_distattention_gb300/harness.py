@@ -16,7 +16,8 @@ class PagedCache:
     """Pool [num_pages][Hkv][P][d] (K and V) plus statistics, block table and lengths.
 
     kv_format KV_BF16 keeps bf16 values; KV_FP8_E4M3 keeps uint8 E4M3 codes plus one float32
-    scale per (token, KV head) row in k_scale / v_scale [num_pages][Hkv][P].
+    scale per (token, KV head) row in kv_scale [num_pages][Hkv][P/16][2][16] (per logical
+    page: 16 K scales, then 16 V scales).
     """
 
     def __init__(self, case: Case, device="cuda", with_stats: bool = False, fill: bool = True,
@@ -29,10 +30,10 @@ class PagedCache:
         elem = torch.uint8 if kv_format == KV_FP8_E4M3 else torch.bfloat16
         self.k_pool = alloc(c.num_pages, c.Hkv, c.P, c.d, dtype=elem, device=device)
         self.v_pool = alloc(c.num_pages, c.Hkv, c.P, c.d, dtype=elem, device=device)
-        self.k_scale = self.v_scale = None
+        self.kv_scale = None
         if kv_format == KV_FP8_E4M3:
-            self.k_scale = alloc(c.num_pages, c.Hkv, c.P, dtype=torch.float32, device=device)
-            self.v_scale = alloc(c.num_pages, c.Hkv, c.P, dtype=torch.float32, device=device)
+            self.kv_scale = alloc(c.num_pages, c.Hkv, c.P // 16, 2, 16, dtype=torch.float32,
+                                  device=device)
         self.stats = None
         if with_stats:
             self.stats = alloc(c.num_pages, c.Hkv, c.P // 16, 2, c.d, dtype=torch.bfloat16,
@@ -50,7 +51,7 @@ class PagedCache:
     def _layout(self, block_table) -> KVLayout:
         c = self.case
         return KVLayout(c.num_pages, c.Hkv, c.d, c.P, block_table, self.kv_format,
-                        self.k_scale, self.v_scale)
+                        self.kv_scale)
 
     def _row_layout(self, b: int) -> KVLayout:
         return self._layout(self.block_table[b:b + 1])

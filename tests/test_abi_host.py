@@ -118,19 +118,18 @@ def test_decode_rejects_bad_shapes_before_launch(dattn):
 def test_kv_format_is_validated(dattn):
     INVALID, UNSUPPORTED = 1, 2
 
-    def lay(fmt, k_scale, v_scale):
+    def lay(fmt, kv_scale):
         out = _lay(dattn)
-        out.c.kv_format, out.c.k_scale, out.c.v_scale = fmt, k_scale, v_scale
+        out.c.kv_format, out.c.kv_scale = fmt, kv_scale
         return out
 
-    assert _decode_status(dattn, lay(2, None, None)) == INVALID    # unknown format
-    assert _decode_status(dattn, lay(-1, None, None)) == INVALID
-    assert _decode_status(dattn, lay(1, None, 64)) == INVALID      # a scale pool missing
-    assert _decode_status(dattn, lay(1, 64, None)) == INVALID
-    assert _decode_status(dattn, lay(1, 64, 72)) == INVALID        # not 16-byte aligned
+    assert _decode_status(dattn, lay(2, None)) == INVALID    # unknown format
+    assert _decode_status(dattn, lay(-1, None)) == INVALID
+    assert _decode_status(dattn, lay(1, None)) == INVALID    # the scale pool missing
+    assert _decode_status(dattn, lay(1, 72)) == INVALID      # not 16-byte aligned
     # well-formed layouts pass the layout checks: the group-size check answers next
-    assert _decode_status(dattn, lay(1, 64, 128), Hq=36) == UNSUPPORTED
-    assert _decode_status(dattn, lay(0, None, None), Hq=36) == UNSUPPORTED
+    assert _decode_status(dattn, lay(1, 128), Hq=36) == UNSUPPORTED
+    assert _decode_status(dattn, lay(0, None), Hq=36) == UNSUPPORTED
     import torch
     with pytest.raises(ValueError):
         dattn.KVLayout(8, 2, 128, 16, torch.zeros(1, 4, dtype=torch.int32), kv_format=1)

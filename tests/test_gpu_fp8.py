@@ -87,9 +87,13 @@ def _assert_pool(cache, want):
     kp, vp, ks, vs, st = want
     np.testing.assert_array_equal(cache.k_pool.cpu().numpy(), kp)
     np.testing.assert_array_equal(cache.v_pool.cpu().numpy(), vp)
-    # scales bit for bit
-    np.testing.assert_array_equal(cache.k_scale.cpu().numpy().view(np.uint32), ks.view(np.uint32))
-    np.testing.assert_array_equal(cache.v_scale.cpu().numpy().view(np.uint32), vs.view(np.uint32))
+    # scales bit for bit; the pool keeps them as [page][head][P/16][K, V][16]
+    sc = cache.kv_scale.cpu().numpy()
+    n, h, P = ks.shape
+    gk = sc[:, :, :, 0, :].reshape(n, h, P)
+    gv = sc[:, :, :, 1, :].reshape(n, h, P)
+    np.testing.assert_array_equal(gk.view(np.uint32), ks.view(np.uint32))
+    np.testing.assert_array_equal(gv.view(np.uint32), vs.view(np.uint32))
     if cache.stats is not None:
         np.testing.assert_array_equal(oracle.bf16_bits(cache.stats), st)
 
