@@ -236,6 +236,29 @@ dattn_status_t dattn_decode(const dattn_kv_layout *layout, const void *k_pool,
                             int32_t *dev_err, void *stream);
 
 /*
+ * Multi-query decode: T new query tokens per request attend the cache causally. This is the
+ * step beside decode: [LS] "背景知识与设计动机" splits a long input into chunks processed
+ * alongside decoding (chunked prefill), and a speculative or chunked step brings several new
+ * tokens at once. The T new tokens of request b are the last T of its L_b = seq_lens[b]
+ * tokens (append them first with dattn_kv_append). Query token t (0 <= t < T) attends tokens
+ * 0 .. L_b - T + t; one that sees no token (L_b - T + t < 0) gives out = 0, m = -inf, e = 0.
+ * The split, the partials and the merge are those of dattn_decode; with T = 1 this is
+ * dattn_decode without block sparsity.
+ *
+ *   q        (device) bf16 [B][T][Hq][d]
+ *   out      (device) fp32 [B][T][Hq][d];  m_g, e_g (device, nullable) fp32 [B][T][Hq]
+ *   ws, ws_bytes  workspace of at least dattn_workspace_size(B, T * Hq, Hkv, d, 0, num_splits)
+ * Besides the common limits it needs g * T <= 8 (the query heads and tokens of one KV head
+ * share one tensor-core tile) and returns DATTN_ERR_UNSUPPORTED otherwise; T < 1 is
+ * DATTN_ERR_INVALID_ARG.
+ */
+dattn_status_t dattn_decode_multi(const dattn_kv_layout *layout, const void *k_pool,
+                                  const void *v_pool, const dattn_bf16 *q, int32_t B, int32_t T,
+                                  int32_t Hq, float scale, const int32_t *seq_lens,
+                                  int32_t num_splits, void *ws, size_t ws_bytes, float *out,
+                                  float *m_g, float *e_g, int32_t *dev_err, void *stream);
+
+/*
  * dattn_decode without a workspace argument: the same fused decode as dattn_decode, with its
  * scratch in a fixed 8 MiB device array inside the library instead of in caller memory.
  * The pages have no counterpart to this call; it exists for callers that cannot allocate

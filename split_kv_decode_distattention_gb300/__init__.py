@@ -11,6 +11,7 @@ Entry points, with the same names as in include/dattn.h:
   dattn_partial      MicroAttention partials (m, e, MA) over explicit chunks of pages
   dattn_merge        log-sum-exp aggregation of partials
   dattn_decode       fused split-KV decode, dense or block-sparse
+  dattn_decode_multi fused decode of T new query tokens per request, causal over them
   dattn_page_select  page scoring and top-K selection for retrieval heads
 """
 from __future__ import annotations
@@ -24,7 +25,7 @@ import torch
 __all__ = [
     "KVLayout", "SparseConfig", "DattnError", "load_library", "library_path",
     "dattn_kv_append", "dattn_partial", "dattn_merge", "dattn_decode", "dattn_page_select",
-    "dattn_decode_noalloc",
+    "dattn_decode_noalloc", "dattn_decode_multi",
     "dattn_workspace_size", "dattn_workspace_init", "dattn_auto_splits", "dattn_split_range",
     "dattn_split_owner", "dattn_status_string", "dattn_version", "Workspace",
     "HEAD_DENSE", "HEAD_RETRIEVAL", "HEAD_STREAMING", "DEVERR", "KV_BF16", "KV_FP8_E4M3",
@@ -74,6 +75,8 @@ _SIGS = {
                                _I, _P, _P]),
     "dattn_decode_noalloc": (_I, [ctypes.POINTER(_Layout), _P, _P, _P, _I, _I, _F, _P,
                                   ctypes.POINTER(_Sparse), _I, _P, _P, _P, _P, _P]),
+    "dattn_decode_multi": (_I, [ctypes.POINTER(_Layout), _P, _P, _P, _I, _I, _I, _F, _P, _I, _P,
+                                _SZ, _P, _P, _P, _P, _P]),
     "dattn_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "dattn_workspace_init": (_I, [_P, _SZ, _P]),
     "dattn_auto_splits": (_I, [_I64]),
@@ -301,6 +304,20 @@ def dattn_decode(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, ou
         ctypes.byref(layout.c), _ptr(k_pool), _ptr(v_pool), _ptr(q), B, Hq, scale,
         _ptr(seq_lens), sp, num_splits, _ptr(ws.buffer), ws.buffer.numel(), _ptr(out),
         _ptr(m_g), _ptr(e_g), _ptr(dev_err), _stream(stream)), "dattn_decode")
+
+
+def dattn_decode_multi(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, out,
+                       ws: Workspace, m_g=None, e_g=None, num_splits=0, dev_err=None, stream=None):
+    """T query tokens per request (q bf16 [B][T][Hq][d]), causal over the T newest tokens:
+    out fp32 [B][T][Hq][d] (+ m_g, e_g fp32 [B][T][Hq]). The workspace is sized for T * Hq
+    query heads."""
+    _pool(layout, k_pool, "k_pool"); _pool(layout, v_pool, "v_pool"); _bf16(q, "q")
+    _i32(seq_lens, "seq_lens"); _f32(out, "out")
+    B, T, Hq = q.shape[0], q.shape[1], q.shape[2]
+    _check(load_library().dattn_decode_multi(
+        ctypes.byref(layout.c), _ptr(k_pool), _ptr(v_pool), _ptr(q), B, T, Hq, scale,
+        _ptr(seq_lens), num_splits, _ptr(ws.buffer), ws.buffer.numel(), _ptr(out), _ptr(m_g),
+        _ptr(e_g), _ptr(dev_err), _stream(stream)), "dattn_decode_multi")
 
 
 def dattn_decode_noalloc(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, out,

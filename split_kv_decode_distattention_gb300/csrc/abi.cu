@@ -248,6 +248,8 @@ dattn_status_t dattn_partial(const dattn_kv_layout* layout, const void* k_pool,
     p.B = B;
     p.Hq = Hq;
     p.g = Hq / p.Hkv;
+    p.T = 1;
+    p.gq = p.g;
     p.sl2 = scale * kLog2e;
     p.seq_lens = seq_lens;
     p.C = C;
@@ -280,16 +282,22 @@ dattn_status_t dattn_merge(int32_t B, int32_t C, int32_t Hq, int32_t head_dim,
                         static_cast<cudaStream_t>(stream));
 }
 
-dattn_status_t dattn_decode(const dattn_kv_layout* layout, const void* k_pool,
-                            const void* v_pool, const dattn_bf16* q, int32_t B,
-                            int32_t Hq, float scale, const int32_t* seq_lens,
-                            const dattn_sparse* sparse, int32_t num_splits, void* ws,
-                            size_t ws_bytes, float* out, float* m_g, float* e_g,
-                            int32_t* dev_err, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The fused decode of dattn_decode (T = 1) and dattn_decode_multi (T query tokens).
+dattn_status_t decode_impl(const dattn_kv_layout* layout, const void* k_pool, const void* v_pool,
+                           const dattn_bf16* q, int32_t B, int32_t T, int32_t Hq, float scale,
+                           const int32_t* seq_lens, const dattn_sparse* sparse,
+                           int32_t num_splits, void* ws, size_t ws_bytes, float* out, float* m_g,
+                           float* e_g, int32_t* dev_err, void* stream) {
     dattn_status_t st = check_layout(layout);
     if (st != DATTN_OK) return st;
     if ((st = check_heads(layout, B, Hq)) != DATTN_OK) return st;
-    if (num_splits < 0) return DATTN_ERR_INVALID_ARG;
+    if (num_splits < 0 || T < 1) return DATTN_ERR_INVALID_ARG;
+    if ((Hq / layout->num_kv_heads) * (int64_t)T > kMaxGroup) return DATTN_ERR_UNSUPPORTED;
+    if (T > 1 && sparse != nullptr) return DATTN_ERR_UNSUPPORTED;
     if (B == 0) return DATTN_OK;
     if (!k_pool || !v_pool || !q || !seq_lens || !out) return DATTN_ERR_INVALID_ARG;
     if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(q)) return DATTN_ERR_INVALID_ARG;
@@ -326,6 +334,8 @@ dattn_status_t dattn_decode(const dattn_kv_layout* layout, const void* k_pool,
     p.B = B;
     p.Hq = Hq;
     p.g = Hq / p.Hkv;
+    p.T = T;
+    p.gq = p.g * T;
     p.sl2 = scale * kLog2e;
     p.seq_lens = seq_lens;
     p.out = out;
@@ -338,6 +348,29 @@ dattn_status_t dattn_decode(const dattn_kv_layout* layout, const void* k_pool,
     p.kv_scale = layout->kv_scale;
     return launch_attention(p, k_pool, v_pool, layout->head_dim, num_splits, ws, ws_bytes,
                             static_cast<cudaStream_t>(stream), bound);
+}
+
+}  // namespace
+
+extern "C" {
+
+dattn_status_t dattn_decode(const dattn_kv_layout* layout, const void* k_pool,
+                            const void* v_pool, const dattn_bf16* q, int32_t B,
+                            int32_t Hq, float scale, const int32_t* seq_lens,
+                            const dattn_sparse* sparse, int32_t num_splits, void* ws,
+                            size_t ws_bytes, float* out, float* m_g, float* e_g,
+                            int32_t* dev_err, void* stream) {
+    return decode_impl(layout, k_pool, v_pool, q, B, 1, Hq, scale, seq_lens, sparse, num_splits,
+                       ws, ws_bytes, out, m_g, e_g, dev_err, stream);
+}
+
+dattn_status_t dattn_decode_multi(const dattn_kv_layout* layout, const void* k_pool,
+                                  const void* v_pool, const dattn_bf16* q, int32_t B, int32_t T,
+                                  int32_t Hq, float scale, const int32_t* seq_lens,
+                                  int32_t num_splits, void* ws, size_t ws_bytes, float* out,
+                                  float* m_g, float* e_g, int32_t* dev_err, void* stream) {
+    return decode_impl(layout, k_pool, v_pool, q, B, T, Hq, scale, seq_lens, nullptr, num_splits,
+                       ws, ws_bytes, out, m_g, e_g, dev_err, stream);
 }
 
 dattn_status_t dattn_page_select(const dattn_kv_layout* layout, const dattn_bf16* stats,

@@ -182,17 +182,22 @@ struct Plan {
     }
 };
 
-// Resolved tile: TMA row coordinate and the valid token range [lo, hi) within its 16 rows.
+// Resolved tile: TMA row coordinate, the valid token range [lo, hi) within its 16 rows and
+// the causal cut of multi-query decode: row r is visible to query token t iff r <= cut + t.
 struct TileRef {
     int32_t y;
-    int32_t lohi;  // lo | hi << 8 | skip << 16
+    int32_t lohi;  // lo | hi << 8 | skip << 16 | (cut + 16) << 24, cut clamped to [-16, 16]
 };
+constexpr int32_t kTileSkip = 1 << 16;
+__device__ __forceinline__ int32_t tile_lo(int32_t m) { return m & 0xff; }
+__device__ __forceinline__ int32_t tile_hi(int32_t m) { return (m >> 8) & 0xff; }
+__device__ __forceinline__ int32_t tile_cut(int32_t m) { return ((m >> 24) & 63) - 16; }
 
 __device__ __forceinline__ TileRef resolve_tile(const AttnParams& p, const Smem& sm, int32_t s,
                                                 int32_t local) {
-    TileRef r{0, 1 << 16};
+    TileRef r{0, kTileSkip};
     const int32_t item = s / p.Hkv, h = s - item * p.Hkv;
-    int32_t b, L, t0, lo = 0, hi = 16;
+    int32_t b, L, t0, lo = 0, hi = 16, cut = 16;
     if (p.mode == MODE_PARTIAL) {
         b = __ldg(p.chunk_req + item);
         if (b < 0 || b >= p.B) return r;  // such a chunk has no tiles
@@ -236,6 +241,8 @@ __device__ __forceinline__ TileRef resolve_tile(const AttnParams& p, const Smem&
         } else {
             t0 = local * 16;
             hi = min(16, L - t0);
+            // multi-query decode: query token t sees the tokens < L - T + t + 1
+            if (p.T > 1) cut = min(16, max(-16, L - p.T - t0));
         }
     }
     const int32_t lp = t0 / p.P;
@@ -249,16 +256,17 @@ __device__ __forceinline__ TileRef resolve_tile(const AttnParams& p, const Smem&
         return r;
     }
     r.y = (page * p.Hkv + h) * p.P + (t0 - lp * p.P);
-    r.lohi = lo | (hi << 8);
+    r.lohi = lo | (hi << 8) | ((cut + 16) << 24);
     return r;
 }
 
-// Writes the final result of query heads [kvh*g, kvh*g + g) of segment s.
-// MA is unnormalised; m is in log2 units.
-__device__ __forceinline__ void write_final(const AttnParams& p, int32_t s, int32_t j, int32_t d,
+// Writes the final result of column c of segment s: query token t = c / g of query head
+// kvh*g + c % g. MA is unnormalised; m is in log2 units.
+__device__ __forceinline__ void write_final(const AttnParams& p, int32_t s, int32_t c, int32_t d,
                                             int D, float m, float e, float ma) {
     const int32_t item = s / p.Hkv, kvh = s - item * p.Hkv;
-    const int64_t row = (int64_t)item * p.Hq + kvh * p.g + j;
+    const int32_t t = c / p.g, j = c - t * p.g;
+    const int64_t row = ((int64_t)item * p.T + t) * p.Hq + kvh * p.g + j;
     if (p.mode == MODE_PARTIAL) {
         p.out[row * D + d] = ma;
     } else {
@@ -298,16 +306,36 @@ struct Consumer {
     __device__ Consumer(const AttnParams& p_, const Smem& sm_, int w, int l)
         : p(p_), sm(sm_), warp(w), lane(l) {}
 
-    // B fragments of the group's queries for segment s (query head = lane / 4), and the
-    // factor that turns a raw dot product into a base-2 logit.
+    // Visibility of this lane's four logits (rows g8, g8 + 8; columns 2tig, 2tig + 1): the row
+    // lies in [lo, hi) and, in a tile of multi-query decode that holds new tokens (cut < 15,
+    // warp-uniform), row r is visible to column c's query token t = c / g iff r <= cut + t.
+    __device__ __forceinline__ void visible(int lo, int hi, int cut, bool& a0, bool& a1,
+                                            bool& a2, bool& a3) const {
+        const int g8 = lane >> 2, tig = lane & 3;
+        const bool v0 = g8 >= lo && g8 < hi, v1 = g8 + 8 >= lo && g8 + 8 < hi;
+        a0 = a1 = v0;
+        a2 = a3 = v1;
+        if (cut < 15) {
+            const int tA = (2 * tig) / p.g, tB = (2 * tig + 1) / p.g;
+            a0 = a0 && g8 <= cut + tA;
+            a1 = a1 && g8 <= cut + tB;
+            a2 = a2 && g8 + 8 <= cut + tA;
+            a3 = a3 && g8 + 8 <= cut + tB;
+        }
+    }
+
+    // B fragments of the segment's query columns for segment s (column n = lane / 4 is query
+    // token n / g of query head kvh*g + n % g), and the factor that turns a raw dot product
+    // into a base-2 logit.
     __device__ void load_q(int32_t s, uint32_t (&dst)[KS][2], float& qs) const {
         const int32_t item = s / p.Hkv, kvh = s - item * p.Hkv;
         int32_t b = item;
         if (p.mode == MODE_PARTIAL) b = __ldg(p.chunk_req + item);
         const int n = lane >> 2, tig = lane & 3;
-        const bool ok = n < p.g && b >= 0 && b < p.B;
+        const bool ok = n < p.gq && b >= 0 && b < p.B;
+        const int32_t t = ok ? n / p.g : 0, j = ok ? n - t * p.g : 0;
         const uint32_t* qv = reinterpret_cast<const uint32_t*>(
-            p.q + ((int64_t)(ok ? b : 0) * p.Hq + kvh * p.g + (ok ? n : 0)) * D);
+            p.q + (((int64_t)(ok ? b : 0) * p.T + t) * p.Hq + kvh * p.g + j) * D);
         if constexpr (!F8) {
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
@@ -384,8 +412,9 @@ struct Consumer {
         e1 += p1 + p3;
     }
 
-    // One 16-token tile in stage buffer `st`; rows outside [lo, hi) are masked.
-    __device__ void tile(uint32_t st, int lo, int hi) {
+    // One 16-token tile in stage buffer `st`; rows outside [lo, hi) are masked, and row r is
+    // masked for query token t when r > cut + t.
+    __device__ void tile(uint32_t st, int lo, int hi, int cut) {
         const uint32_t kbase = st, vbase = st + (uint32_t)(D / 64) * 2048u;
         const int g8 = lane >> 2;
         // ---- S^T = K Q^T (tokens x heads) -------------------------------------------
@@ -403,11 +432,12 @@ struct Consumer {
                 else        mma_bf16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
             }
         }
-        const bool v0 = g8 >= lo && g8 < hi, v1 = g8 + 8 >= lo && g8 + 8 < hi;
-        const float s0 = v0 ? (sa[0] + sb[0]) * qsc : kNegInf;
-        const float s1 = v0 ? (sa[1] + sb[1]) * qsc : kNegInf;
-        const float s2 = v1 ? (sa[2] + sb[2]) * qsc : kNegInf;
-        const float s3 = v1 ? (sa[3] + sb[3]) * qsc : kNegInf;
+        bool a0, a1, a2, a3;
+        visible(lo, hi, cut, a0, a1, a2, a3);
+        const float s0 = a0 ? (sa[0] + sb[0]) * qsc : kNegInf;
+        const float s1 = a1 ? (sa[1] + sb[1]) * qsc : kNegInf;
+        const float s2 = a2 ? (sa[2] + sb[2]) * qsc : kNegInf;
+        const float s3 = a3 ? (sa[3] + sb[3]) * qsc : kNegInf;
         float p0, p1, p2, p3;
         softmax(s0, s1, s2, s3, p0, p1, p2, p3);
         // ---- P^T as the B operand: two bf16 terms, transposed with movmatrix ---------
@@ -447,8 +477,8 @@ struct Consumer {
     }
 
     // One 16-token tile of the 8-bit pool in stage buffer `st` (K codes, then V codes) with
-    // its row scales `sc`; rows outside [lo, hi) are masked.
-    __device__ void tile_f8(uint32_t st, const float* sc, int lo, int hi) {
+    // its row scales `sc`; rows are masked as in tile().
+    __device__ void tile_f8(uint32_t st, const float* sc, int lo, int hi, int cut) {
         const uint32_t kbase = st, vbase = st + 16u * D;
         const int g8 = lane >> 2, tig = lane & 3;
         // ldmatrix lane addresses: matrices (rows 0-7 | 8-15) x (chunk 2c | 2c + 1)
@@ -469,10 +499,12 @@ struct Consumer {
         }
         const bool v0 = g8 >= lo && g8 < hi, v1 = g8 + 8 >= lo && g8 + 8 < hi;
         const float kc0 = sc[g8] * qsc, kc1 = sc[g8 + 8] * qsc;
-        const float s0 = v0 ? (sa[0] + sb[0]) * kc0 : kNegInf;
-        const float s1 = v0 ? (sa[1] + sb[1]) * kc0 : kNegInf;
-        const float s2 = v1 ? (sa[2] + sb[2]) * kc1 : kNegInf;
-        const float s3 = v1 ? (sa[3] + sb[3]) * kc1 : kNegInf;
+        bool a0, a1, a2, a3;
+        visible(lo, hi, cut, a0, a1, a2, a3);
+        const float s0 = a0 ? (sa[0] + sb[0]) * kc0 : kNegInf;
+        const float s1 = a1 ? (sa[1] + sb[1]) * kc0 : kNegInf;
+        const float s2 = a2 ? (sa[2] + sb[2]) * kc1 : kNegInf;
+        const float s3 = a3 ? (sa[3] + sb[3]) * kc1 : kNegInf;
         float p0, p1, p2, p3;
         softmax(s0, s1, s2, s3, p0, p1, p2, p3);
         // ---- V scales: raise r to a power of two >= every V scale of the tile ---------
@@ -545,27 +577,27 @@ struct Consumer {
         const int hA = 2 * tig, hB = 2 * tig + 1;
         float* wm = sm.ws_m() + warp * kMaxGroup;
         float* we = sm.ws_e() + warp * kMaxGroup;
-        float* wo = sm.ws_o() + warp * p.g * D;
+        float* wo = sm.ws_o() + warp * p.gq * D;
         if (g8 == 0) {
-            if (hA < p.g) { wm[hA] = m0; we[hA] = t0; }
-            if (hB < p.g) { wm[hB] = m1; we[hB] = t1; }
+            if (hA < p.gq) { wm[hA] = m0; we[hA] = t0; }
+            if (hB < p.gq) { wm[hB] = m1; we[hB] = t1; }
         }
         if constexpr (!F8) {
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 const int dd = mt * 16 + g8;
-                if (hA < p.g) { wo[hA * D + dd] = o[mt][0]; wo[hA * D + dd + 8] = o[mt][2]; }
-                if (hB < p.g) { wo[hB * D + dd] = o[mt][1]; wo[hB * D + dd + 8] = o[mt][3]; }
+                if (hA < p.gq) { wo[hA * D + dd] = o[mt][0]; wo[hA * D + dd + 8] = o[mt][2]; }
+                if (hB < p.gq) { wo[hB * D + dd] = o[mt][1]; wo[hB * D + dd + 8] = o[mt][3]; }
             }
         } else {
             const float rs = rv * 3.0517578125e-05f;  // r * 2^-15, exact
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 const int dd = mt * 16 + 2 * g8;
-                if (hA < p.g)
+                if (hA < p.gq)
                     *reinterpret_cast<float2*>(wo + hA * D + dd) =
                         make_float2(o[mt][0] * rs, o[mt][2] * rs);
-                if (hB < p.g)
+                if (hB < p.gq)
                     *reinterpret_cast<float2*>(wo + hB * D + dd) =
                         make_float2(o[mt][1] * rs, o[mt][3] * rs);
             }
@@ -584,7 +616,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
         const uint32_t off = smem_u32(smem_raw);
         sm.base = smem_raw + (((off + 1023u) & ~1023u) - off);
     }
-    sm.L = attn_smem_layout(D, p.g, p.nitems, p.Hkv, p.mode == MODE_SPARSE, F8);
+    sm.L = attn_smem_layout(D, p.gq, p.nitems, p.Hkv, p.mode == MODE_SPARSE, F8);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t G = gridDim.x, cta = blockIdx.x;
     constexpr int NS = attn_stages(F8);
@@ -718,7 +750,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
         int32_t st, real, cost;
         plan.seg_span(s, st, real, cost);
         if (real == 0) {
-            for (int idx = tid; idx < p.g * D; idx += kAttnThreads)
+            for (int idx = tid; idx < p.gq * D; idx += kAttnThreads)
                 write_final(p, s, idx / D, idx % D, D, kNegInf, 0.f, 0.f);
         }
     }
@@ -758,7 +790,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
                         if (ok) {
                             const uint32_t full = sm.full_bar(stg);
                             sm.meta()[stg] = lohi;
-                            if (lohi >> 16) {
+                            if (lohi & kTileSkip) {
                                 mbar_arrive(full);
                             } else {
                                 mbar_arrive_expect_tx(full, tx);
@@ -828,12 +860,13 @@ attention_kernel(const __grid_constant__ AttnParams p,
             const bool ok = __all_sync(0xffffffffu, mbar_wait(sm.full_bar(stg), (k / NS) & 1,
                                                               sm.abort_flag(), p.dev_err));
             const int32_t lohi = sm.meta()[stg];
-            const int lo = lohi & 0xff, hi = (lohi >> 8) & 0xff;
-            if (ok && !(lohi >> 16)) {
+            const int lo = tile_lo(lohi), hi = tile_hi(lohi), cut = tile_cut(lohi);
+            if (ok && !(lohi & kTileSkip)) {
                 if constexpr (F8) {
-                    cons.tile_f8(stage0 + (uint32_t)stg * sm.L.stage_bytes, sm.scales(stg), lo, hi);
+                    cons.tile_f8(stage0 + (uint32_t)stg * sm.L.stage_bytes, sm.scales(stg), lo, hi,
+                                 cut);
                 } else {
-                    cons.tile(stage0 + (uint32_t)stg * sm.L.stage_bytes, lo, hi);
+                    cons.tile(stage0 + (uint32_t)stg * sm.L.stage_bytes, lo, hi, cut);
                     if (lo > 0 || hi < 16) fence_proxy_async_smem();
                 }
             }
@@ -852,8 +885,8 @@ attention_kernel(const __grid_constant__ AttnParams p,
         const float* wm = sm.ws_m();
         const float* we = sm.ws_e();
         const float* wo = sm.ws_o();
-        const int gD = p.g * D;
-        const int32_t slot_stride = slot_floats(p.g, D);
+        const int gD = p.gq * D;
+        const int32_t slot_stride = slot_floats(p.gq, D);
         float* my_slot = whole ? nullptr : p.slots + (int64_t)(cta + s) * slot_stride;
         // a thread combines float4 columns of the g x D state; D is a multiple of 4, so a
         // column never spans two heads
@@ -887,7 +920,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
                 *reinterpret_cast<float4*>(my_slot + 4 * c4) = ma;
                 if (d == 0) {
                     my_slot[gD + j] = mc;
-                    my_slot[gD + p.g + j] = ec;
+                    my_slot[gD + p.gq + j] = ec;
                 }
             }
         }
@@ -923,7 +956,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
                             const bool in = q0 + t < npieces;
                             const float* sl = pass + (int64_t)t * slot_stride;
                             mq[t] = in ? __ldcg(sl + gD + j) : kNegInf;
-                            eq[t] = in ? __ldcg(sl + gD + p.g + j) : 0.f;
+                            eq[t] = in ? __ldcg(sl + gD + p.gq + j) : 0.f;
                             vq[t] = in ? __ldcg(reinterpret_cast<const float4*>(sl + 4 * c4))
                                        : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
@@ -1013,12 +1046,12 @@ static dattn_status_t launch_d(const AttnParams& p0, const void* k_pool, const v
                                int32_t num_splits, void* ws, size_t ws_bytes,
                                cudaStream_t stream, int64_t tiles_bound) {
     AttnParams p = p0;
-    const AttnSmem L = attn_smem_layout(D, p.g, p.nitems, p.Hkv, p.mode == MODE_SPARSE, F8);
+    const AttnSmem L = attn_smem_layout(D, p.gq, p.nitems, p.Hkv, p.mode == MODE_SPARSE, F8);
     dattn_status_t st = ensure_smem<D, F8>(L.total);
     if (st != DATTN_OK) return st;
     const int32_t G = choose_splits(tiles_bound, num_splits, occupancy<D, F8>(L.total));
     const size_t counters = ((size_t)p.nseg * 4 + 255) & ~(size_t)255;
-    if (ws == nullptr || ws_bytes < attn_workspace_bytes(p.nseg, p.g, D, G) ||
+    if (ws == nullptr || ws_bytes < attn_workspace_bytes(p.nseg, p.gq, D, G) ||
         (reinterpret_cast<uintptr_t>(ws) & 255))
         return DATTN_ERR_WORKSPACE;
     p.counters = static_cast<int32_t*>(ws);

@@ -34,6 +34,9 @@ struct AttnParams {
     const int32_t* block_table;
     const uint16_t* q;
     int32_t B, Hq, g;
+    // query tokens per request (1 = decode; T > 1: multi-query decode, causal over the T
+    // newest tokens) and the columns of a segment's tile, gq = g * T <= 8
+    int32_t T, gq;
     float sl2;  // scale * log2(e)
     const int32_t* seq_lens;
     // dattn_partial

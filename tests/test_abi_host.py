@@ -135,6 +135,24 @@ def test_kv_format_is_validated(dattn):
         dattn.KVLayout(8, 2, 128, 16, torch.zeros(1, 4, dtype=torch.int32), kv_format=1)
 
 
+def test_decode_multi_is_validated(dattn):
+    INVALID, UNSUPPORTED = 1, 2
+    lib = dattn.load_library()
+    p = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+
+    def status(T, Hq, lay=None):
+        lay = lay or _lay(dattn)  # Hkv = 2
+        return lib.dattn_decode_multi(ctypes.byref(lay.c), p, p, p, 1, T, Hq, 0.1, p, 0, p,
+                                      1 << 20, p, None, None, None, None)
+
+    assert status(0, 4) == INVALID             # no query token
+    assert status(-2, 4) == INVALID
+    assert status(3, 8) == UNSUPPORTED         # group 4 x 3 tokens > 8 columns
+    assert status(9, 2) == UNSUPPORTED         # group 1 x 9 tokens
+    assert status(2, 3) == INVALID             # Hq % Hkv != 0
+    assert status(2, 4, _lay(dattn, head_dim=96)) == UNSUPPORTED
+
+
 def test_page_select_needs_power_of_two_logical_pages(dattn):
     lib = dattn.load_library()
     p = ctypes.c_void_p(16)  # never dereferenced: validation fails first
