@@ -11,10 +11,14 @@ roofline are reported beside it. L2 is flushed before every timed step whose K/V
 four times the L2; larger steps evict it themselves and run back to back.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl dattn|reference]
-                  [--kv-format bf16|fp8]
+                  [--kv-format bf16|fp8] [--queries T]
 
 --kv-format fp8 runs the same workload over the 8-bit pool (FP8 E4M3 codes with one fp32
 scale per (token, KV head) row): a K or V row then moves d + 4 bytes instead of 2 d.
+
+--queries T (dense workloads) makes each step a chunked one: T new tokens per request are
+appended, then dattn_decode_multi attends all T query tokens, causal over the new tokens.
+The K/V is read once per step, as for T = 1; queries, outputs and appends scale with T.
 
 --impl reference times the CPU oracle (test infrastructure) on the host cores over a
 bounded sample of the same workload and prints the same JSON line with "impl": "reference".
@@ -66,6 +70,8 @@ def parse_args():
     ap.add_argument("--impl", default="dattn", choices=["dattn", "reference"])
     ap.add_argument("--kv-format", default="bf16", choices=["bf16", "fp8"],
                     help="element format of the paged KV pool")
+    ap.add_argument("--queries", type=int, default=1,
+                    help="query tokens per request and step (dense workloads; 1 = decode)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling only)")
     ap.add_argument("--ctx", type=int, default=0, help="override the context (profiling only)")
@@ -102,9 +108,11 @@ def make_case(args):
     elif name == "gqa-ragged" and args.batch:
         kw["B"] = args.batch
     case = W.CASES[name](seed=args.seed, **kw)
+    if args.queries < 1 or (args.queries > 1 and case.head_kind is not None):
+        raise SystemExit("--queries T needs T >= 1 and a dense workload")
     # room for the tokens the timed and warm-up steps append
-    case.reserve_tokens = max(case.reserve_tokens,
-                              2 * (args.steps + args.warmup + 3 * info_steps(args)) + 64)
+    case.reserve_tokens = max(case.reserve_tokens, 2 * args.queries *
+                              (args.steps + args.warmup + 3 * info_steps(args)) + 64)
     case._make_block_table()
     return case
 
@@ -114,13 +122,14 @@ def row_bytes(d: int, fp8: bool) -> int:
     return d + 4 if fp8 else 2 * d
 
 
-def step_bytes(case, lens_after, sparse_sel_step: bool, fp8: bool = False) -> dict:
-    """Algorithmic bytes of one layer-step, given the lengths after the append."""
+def step_bytes(case, lens_after, sparse_sel_step: bool, fp8: bool = False, T: int = 1) -> dict:
+    """Algorithmic bytes of one layer-step, given the lengths after the append (T query
+    tokens per request: T appended tokens, T queries and outputs, the K/V read once)."""
     B, Hq, Hkv, d, P = case.B, case.Hq, case.Hkv, case.d, case.P
     rb = row_bytes(d, fp8)
-    q_bytes = B * Hq * d * 2
-    out_bytes = B * Hq * d * 4 + 2 * B * Hq * 4
-    new_kv = B * Hkv * (d * 2 + rb) * 2  # read k_new/v_new (bf16), write into the pool
+    q_bytes = T * B * Hq * d * 2
+    out_bytes = T * (B * Hq * d * 4 + 2 * B * Hq * 4)
+    new_kv = T * B * Hkv * (d * 2 + rb) * 2  # read k_new/v_new (bf16), write into the pool
     bt = sum(-(-L // P) for L in lens_after) * 4
     if case.head_kind is None:
         kv = sum(lens_after) * Hkv * rb * 2
@@ -223,7 +232,8 @@ def kernel_source_hash() -> str:
 
 
 def traffic_key(args) -> str:
-    return args.config + ("/fp8" if args.kv_format == "fp8" else "")
+    return (args.config + ("/fp8" if args.kv_format == "fp8" else "") +
+            (f"/T{args.queries}" if args.queries > 1 else ""))
 
 
 def traffic_record(config: str):
@@ -278,29 +288,35 @@ def run_dattn(args, rank: int, world: int):
     cache = PagedCache(case, dev, with_stats=sparse, chunk_tokens=16384,
                        kv_format=dattn.KV_FP8_E4M3 if fp8 else dattn.KV_BF16)
     B, Hq, d = case.B, case.Hq, case.d
-    ws = cache.workspace(top_k=case.top_k, num_splits=args.num_splits)
-    out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
-    m_g = torch.empty(B, Hq, dtype=torch.float32, device=dev)
-    e_g = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+    T = args.queries
+    ws = cache.workspace(top_k=case.top_k, num_splits=args.num_splits, queries=T)
+    qshape = (B, Hq) if T == 1 else (B, T, Hq)  # one query token, or T of them
+    out = torch.empty(*qshape, d, dtype=torch.float32, device=dev)
+    m_g = torch.empty(*qshape, dtype=torch.float32, device=dev)
+    e_g = torch.empty(*qshape, dtype=torch.float32, device=dev)
     sel = torch.full((B, case.Hkv, max(case.top_k, 1)), -1, dtype=torch.int32, device=dev)
     spc = cache.sparse_config(sel) if sparse else None
     stream = torch.cuda.current_stream()
     n_info = info_steps(args)
     total = args.warmup + args.steps + 3 * n_info + 1
     # per-step inputs prepared up front (device-resident for the kernel timing)
-    qs = [case.q(s, dev) for s in range(total)]
-    per_req = [case.kv(b, case.lens[b], case.lens[b] + total, dev) for b in range(B)]
-    k_all = torch.stack([k for k, _ in per_req])  # [B][total][Hkv][d]
+    if T == 1:
+        qs = [case.q(s, dev) for s in range(total)]
+    else:
+        qs = [torch.stack([case.q(s * T + t, dev) for t in range(T)], dim=1).contiguous()
+              for s in range(total)]
+    per_req = [case.kv(b, case.lens[b], case.lens[b] + total * T, dev) for b in range(B)]
+    k_all = torch.stack([k for k, _ in per_req])  # [B][total * T][Hkv][d]
     v_all = torch.stack([v for _, v in per_req])
     del per_req
-    news = [(k_all[:, s:s + 1].contiguous(), v_all[:, s:s + 1].contiguous())
+    news = [(k_all[:, s * T:(s + 1) * T].contiguous(), v_all[:, s * T:(s + 1) * T].contiguous())
             for s in range(total)]
     del k_all, v_all
     # L2 hygiene: a step whose K/V working set exceeds 4x the L2 evicts everything the
     # previous step left there, so it is timed back to back; smaller steps are preceded by
     # an L2 flush (see L2Flush).
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    sb0 = step_bytes(case, list(cache.lens), sparse, fp8)
+    sb0 = step_bytes(case, list(cache.lens), sparse, fp8, T)
     do_flush = sb0["decode"] < 4 * l2 or args.flush
     flush = L2Flush(dev)
     torch.cuda.synchronize()
@@ -387,8 +403,8 @@ def run_dattn(args, rank: int, world: int):
             kev[1].record(stream)
             launches += n1 + n2
         e1.record(stream)
-        lens_after = [L + i + 1 for L in lens0]
-        sb = step_bytes(case, lens_after, sparse and s % case.reuse == 0, fp8)
+        lens_after = [L + (i + 1) * T for L in lens0]
+        sb = step_bytes(case, lens_after, sparse and s % case.reuse == 0, fp8, T)
         bytes_total += sb["step"]
         step_ms.append((e0, e1))
         if kev is not None:
@@ -508,14 +524,18 @@ def run_e2e(args, case, cache, ws, spc, sel, flush, dev):
     import torch
     B, Hq, Hkv, d = case.B, case.Hq, case.Hkv, case.d
     steps = max(3, min(args.steps, 50))
-    hq = [case.q(100 + s, "cpu").pin_memory() for s in range(steps)]
-    hk = [torch.randn(B, 1, Hkv, d).to(torch.bfloat16).pin_memory() for _ in range(steps)]
-    hv = [torch.randn(B, 1, Hkv, d).to(torch.bfloat16).pin_memory() for _ in range(steps)]
-    houts = [torch.empty(B, Hq, d, dtype=torch.float32).pin_memory() for _ in range(steps)]
-    dq = torch.empty(B, Hq, d, dtype=torch.bfloat16, device=dev)
-    dk = torch.empty(B, 1, Hkv, d, dtype=torch.bfloat16, device=dev)
+    T = args.queries
+    qsh = (B, Hq, d) if T == 1 else (B, T, Hq, d)
+    hq = [(case.q(100 + s, "cpu") if T == 1 else
+           torch.stack([case.q(100 + s * T + t, "cpu") for t in range(T)], dim=1)).pin_memory()
+          for s in range(steps)]
+    hk = [torch.randn(B, T, Hkv, d).to(torch.bfloat16).pin_memory() for _ in range(steps)]
+    hv = [torch.randn(B, T, Hkv, d).to(torch.bfloat16).pin_memory() for _ in range(steps)]
+    houts = [torch.empty(*qsh, dtype=torch.float32).pin_memory() for _ in range(steps)]
+    dq = torch.empty(*qsh, dtype=torch.bfloat16, device=dev)
+    dk = torch.empty(B, T, Hkv, d, dtype=torch.bfloat16, device=dev)
     dv = torch.empty_like(dk)
-    out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
+    out = torch.empty(*qsh, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
     lens0 = list(cache.lens)
@@ -542,9 +562,9 @@ def run_e2e(args, case, cache, ws, spc, sel, flush, dev):
             e1 = torch.cuda.Event(enable_timing=True)
             e1.record(stream)
             pairs.append((e0, e1))
-        lens_after = [L + i + 1 for L in lens0]
+        lens_after = [L + (i + 1) * T for L in lens0]
         tot_bytes += step_bytes(case, lens_after, spc is not None and i % case.reuse == 0,
-                                args.kv_format == "fp8")["step"]
+                                args.kv_format == "fp8", T)["step"]
     if flush is None:
         e_all1.record(stream)
     torch.cuda.synchronize()
@@ -594,9 +614,10 @@ def dequantized(kv):
     return tuple(oracle.dequantize_rows_fp8(*oracle.quantize_rows_fp8(x)) for x in kv)
 
 
-def time_oracle(case, q, pairs, kv, nthreads, fp8: bool = False):
+def time_oracle(case, q, pairs, kv, nthreads, fp8: bool = False, qs=None):
     """Wall time of the oracle's dense attention over the sampled pairs, run on nthreads
-    host threads (each call is one plain C routine that releases the GIL)."""
+    host threads (each call is one plain C routine that releases the GIL). With qs (T query
+    arrays) each pair attends T query tokens, token t over the rows 0 .. L - T + t."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
     attend = oracle.attention_f64 if fp8 else oracle.attention
@@ -604,7 +625,13 @@ def time_oracle(case, q, pairs, kv, nthreads, fp8: bool = False):
     def one(pair):
         b, h = pair
         K, V = kv[(b, h // case.g)]
-        attend(q[b, h], K, V, case.scale)
+        if qs is None:
+            attend(q[b, h], K, V, case.scale)
+        else:
+            L, T = K.shape[0], len(qs)
+            for t in range(T):
+                attend(qs[t][b, h], K, V, case.scale,
+                       rows=np.arange(max(0, L - T + t + 1), dtype=np.int64))
         return K.shape[0] * row_bytes(case.d, fp8) * 2
 
     t0 = time.perf_counter()
@@ -717,26 +744,28 @@ def cpu_baseline_sparse(case, device, fp8: bool = False):
                       f"window(s) of 1 selection + {case.reuse} steps, {secs:.1f} s wall"}
 
 
-def cpu_baseline(case, device, fp8: bool = False):
+def cpu_baseline(case, device, fp8: bool = False, T: int = 1):
     import oracle
     if case.head_kind is not None:
         return cpu_baseline_sparse(case, device, fp8)
     oracle.load()
     nthreads = len(os.sched_getaffinity(0))
     per_pair = max(1, sum(case.lens) // case.B) * case.d * (16 if fp8 else 4)
-    budget = max(nthreads, min(case.B * case.Hq, int(4e9 // per_pair)))
+    budget = max(nthreads, min(case.B * case.Hq, int(4e9 // per_pair) // T))
     q, pairs, kv = oracle_sample(case, device, budget, fp8=fp8)
+    qs = None if T == 1 else [oracle.bf16_bits(case.q(t, device)) for t in range(T)]
     # repeat the sample until about 10 s of CPU work has been timed
-    secs, nbytes, used = time_oracle(case, q, pairs, kv, nthreads, fp8)
+    secs, nbytes, used = time_oracle(case, q, pairs, kv, nthreads, fp8, qs)
     reps = 1
     while secs * used < 10.0 and reps < 64:
-        s2, n2, _ = time_oracle(case, q, pairs, kv, nthreads, fp8)
+        s2, n2, _ = time_oracle(case, q, pairs, kv, nthreads, fp8, qs)
         secs, nbytes, reps = secs + s2, nbytes + n2, reps + 1
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": used,
             "kind": "oracle",
             "sample": f"{len(pairs)} of {case.B * case.Hq} (request, query head) pairs of the "
                       f"{case.name} workload over their full contexts (fp64 dense attention"
-                      f"{' over the dequantized 8-bit rows' if fp8 else ''}), "
+                      f"{' over the dequantized 8-bit rows' if fp8 else ''}"
+                      f"{f', {T} causal query tokens each' if T > 1 else ''}), "
                       f"repeated {reps}x: {secs:.1f} s wall on {used} threads"}
 
 
@@ -790,11 +819,13 @@ def run_reference(args, rank, world):
     per_pair = max(1, sum(case.lens) // case.B) * case.d * (16 if fp8 else 4)
     budget = max(nthreads, min(case.B * case.Hq, int(1e9 // per_pair)))
     q, pairs, kv = oracle_sample(case, device, budget, fp8=fp8)
+    T = args.queries
+    qs = None if T == 1 else [oracle.bf16_bits(case.q(t, device)) for t in range(T)]
     for _ in range(min(args.warmup, 1)):
-        time_oracle(case, q, pairs[:nthreads], kv, nthreads, fp8)
+        time_oracle(case, q, pairs[:nthreads], kv, nthreads, fp8, qs)
     times, used, nbytes = [], nthreads, 0
     for _ in range(args.steps):
-        secs, nb, used = time_oracle(case, q, pairs, kv, nthreads, fp8)
+        secs, nb, used = time_oracle(case, q, pairs, kv, nthreads, fp8, qs)
         times.append(secs)
         nbytes += nb
     total = sum(times)
@@ -829,9 +860,14 @@ def config_obj(case, args):
          "parallelism": "replicas" if args.gpus > 1 else "single GPU",
          "step": ("dattn_kv_append (1 token/request) + dattn_decode" +
                   (" + dattn_page_select every 16 steps (block-sparse)"
-                   if case.head_kind is not None else "")),
+                   if case.head_kind is not None else "")
+                  if args.queries == 1 else
+                  f"dattn_kv_append ({args.queries} tokens/request) + dattn_decode_multi "
+                  f"({args.queries} query tokens/request, causal over the new tokens)"),
          "launch": ("one CUDA graph per step, captured from the library calls"
                     if getattr(args, "graph", False) else "eager library calls")}
+    if args.queries > 1:
+        c["queries_per_request"] = args.queries
     if args.batch or args.ctx:
         c["reduced_for_profiling"] = True
     return c
@@ -856,7 +892,7 @@ def main():
     case = res["case"]
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(case, "cuda", args.kv_format == "fp8")
+        cpu = cpu_baseline(case, "cuda", args.kv_format == "fp8", args.queries)
     if world > 1:
         dist.destroy_process_group()
     if rank != 0:

@@ -8,7 +8,7 @@ from __future__ import annotations
 import torch
 
 from . import (KV_BF16, KV_FP8_E4M3, KVLayout, SparseConfig, Workspace, dattn_decode,
-               dattn_kv_append, dattn_page_select)
+               dattn_decode_multi, dattn_kv_append, dattn_page_select)
 from .workloads import Case
 
 
@@ -86,9 +86,10 @@ class PagedCache:
                         self.seq_lens, self.dev_err)
         self.lens = [L + T for L in self.lens]
 
-    def workspace(self, top_k: int = 0, num_splits: int = 0) -> Workspace:
+    def workspace(self, top_k: int = 0, num_splits: int = 0, queries: int = 1) -> Workspace:
+        """A workspace for decode (T query tokens per request: queries = T) or selection."""
         c = self.case
-        return Workspace(c.B, c.Hq, c.Hkv, c.d, top_k=top_k, num_splits=num_splits,
+        return Workspace(c.B, c.Hq * queries, c.Hkv, c.d, top_k=top_k, num_splits=num_splits,
                          device=self.device)
 
     def head_kind(self) -> torch.Tensor:
@@ -104,6 +105,14 @@ class PagedCache:
         return SparseConfig(self.head_kind(), c.sinks, c.local, c.top_k, selected)
 
     def decode(self, q, out, ws, m_g=None, e_g=None, sparse=None, num_splits=0):
+        """q [B][Hq][d]: dattn_decode; q [B][T][Hq][d]: dattn_decode_multi (dense only)."""
+        if q.dim() == 4:
+            if sparse is not None:
+                raise ValueError("the multi-query decode is dense only")
+            dattn_decode_multi(self.layout, self.k_pool, self.v_pool, q, self.case.scale,
+                               self.seq_lens, out, ws, m_g=m_g, e_g=e_g, num_splits=num_splits,
+                               dev_err=self.dev_err)
+            return
         dattn_decode(self.layout, self.k_pool, self.v_pool, q, self.case.scale, self.seq_lens,
                      out, ws, m_g=m_g, e_g=e_g, sparse=sparse, num_splits=num_splits,
                      dev_err=self.dev_err)
