@@ -64,6 +64,7 @@ _SIGS = {
     "orc_page_scores": (None, [_P, _I, _P, _I64, _I, _I64, _I, _I, _P]),
     "orc_topk": (None, [_P, _I64, _I, _P]),
     "orc_sparse_rows": (_I64, [_I, _I64, _I, _P, _I, _I, _I, _P]),
+    "orc_prefill_rows": (_I64, [_I, _I64, _I64, _I64, _I, _I, _P, _I, _P]),
     "orc_attention_pairs_mt": (_I, [_P, _P, _P, _P, _I, _I, _I, _D, _P, _I64, _I, _P, _P, _P]),
     "orc_e4m3_value": (_D, [ctypes.c_uint8]),
     "orc_e4m3_code": (ctypes.c_uint8, [ctypes.c_float]),
@@ -255,6 +256,18 @@ def sparse_rows(kind: int, L: int, P: int, sel, sinks: int, local: int, lib=None
     rows = np.zeros(max(L, 1), np.int64)
     n = lib.orc_sparse_rows(kind, L, P, _ptr(s), s.shape[0] if sel is not None else 0,
                             sinks, local, _ptr(rows))
+    return rows[:n]
+
+
+def prefill_rows(kind: int, L: int, Tq: int, t: int, sink_blocks: int = 0,
+                 local_blocks: int = 0, blocks=None, lib=None) -> np.ndarray:
+    """Key rows query token t of a Tq-token chunk attends in the block-sparse prefill:
+    kind 0 dense, 1 retrieval (blocks: its query block's key-block list), 2 streaming."""
+    lib = lib or load()
+    b = np.ascontiguousarray(np.asarray(blocks if blocks is not None else [-1], np.int32))
+    rows = np.zeros(max(L, 1), np.int64)
+    n = lib.orc_prefill_rows(kind, L, Tq, t, sink_blocks, local_blocks, _ptr(b),
+                             b.shape[0] if blocks is not None else 0, _ptr(rows))
     return rows[:n]
 
 

@@ -48,6 +48,12 @@
  *      K and of V, scale = max|x| / 448, code = E4M3(x / scale) rounded to nearest even;
  *      attention runs over code * scale. Statistics for page selection are still taken
  *      from the bf16 keys as written.
+ *  R11 Block-sparse prefill [LV §2.1.1, §2.1.2, §2.2.1]: key blocks of 64 tokens. Query token
+ *      t of a chunk of Tq new tokens sits at position p = L - Tq + t (L counts the chunk) and
+ *      attends the keys i <= p whose block kb = i / 64 its head keeps for the query's block
+ *      qb = p / 64: every kb <= qb (dense head); kb < sink_blocks or qb - local_blocks <
+ *      kb <= qb (streaming head, the Lambda shape); the listed blocks (retrieval head, the
+ *      caller's runtime selection, taken literally as the decode takes its page selection).
  */
 #include "dattn_oracle.h"
 
@@ -398,6 +404,34 @@ int64_t orc_sparse_rows(int kind, int64_t L, int P, const int32_t *sel, int top_
         int64_t l0 = L - local;
         if (l0 < sinks) l0 = sinks;
         for (int64_t t = l0; t < L; ++t) rows[n++] = t;
+    }
+    return n;
+}
+
+/*
+ * Key rows that query token t of a Tq-token chunk attends in the block-sparse prefill
+ * (reading R11). kind 0 dense, 1 retrieval (blocks = the key-block list of the query's
+ * block, nblk entries, -1 ignored), 2 streaming (sink_blocks, local_blocks). rows must have
+ * room for L entries. Returns the number of rows, in ascending order.
+ */
+int64_t orc_prefill_rows(int kind, int64_t L, int64_t Tq, int64_t t, int sink_blocks,
+                         int local_blocks, const int32_t *blocks, int nblk, int64_t *rows)
+{
+    const int64_t p = L - Tq + t;
+    const int64_t qb = p / 64;
+    int64_t n = 0;
+    for (int64_t i = 0; i <= p; ++i) {
+        const int64_t kb = i / 64;
+        int keep = 0;
+        if (kind == 0) {
+            keep = 1;
+        } else if (kind == 2) {
+            keep = kb < sink_blocks || kb > qb - local_blocks;
+        } else {
+            for (int j = 0; j < nblk; ++j)
+                if (blocks[j] == kb) keep = 1;
+        }
+        if (keep) rows[n++] = i;
     }
     return n;
 }

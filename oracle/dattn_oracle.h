@@ -43,6 +43,8 @@ void orc_topk(const double *score, int64_t n, int top_k, int32_t *sel);
 
 int64_t orc_sparse_rows(int kind, int64_t L, int P, const int32_t *sel, int top_k, int sinks,
                         int local, int64_t *rows);
+int64_t orc_prefill_rows(int kind, int64_t L, int64_t Tq, int64_t t, int sink_blocks,
+                         int local_blocks, const int32_t *blocks, int nblk, int64_t *rows);
 
 double orc_e4m3_value(uint8_t code);
 

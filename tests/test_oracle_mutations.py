@@ -2,8 +2,8 @@
 
 Each case plants one plausible mistake in a copy of the oracle's C source: a dropped term, a
 wrong sign, an off-by-one index, a swapped operand or a reversed tie rule (none of them
-writes outside its buffers). It builds that copy and runs every pin of test_oracle_pins.py
-and test_oracle_fp8.py against it, and at least one pin must fail. The mistakes live only in
+writes outside its buffers). It builds that copy and runs every pin of test_oracle_pins.py,
+test_oracle_fp8.py and test_oracle_prefill.py against it, and at least one pin must fail. The mistakes live only in
 the temporary copy; the oracle itself is untouched.
 """
 import inspect
@@ -16,6 +16,7 @@ import pytest
 import oracle
 import test_oracle_fp8 as pins_fp8
 import test_oracle_pins as pins
+import test_oracle_prefill as pins_prefill
 
 # (name, text in dattn_oracle.c, replacement)
 MUTATIONS = [
@@ -68,6 +69,12 @@ MUTATIONS = [
      "            for (int64_t t = p * P; t < (p + 1) * P && t < L; ++t) rows[n++] = t;",
      "            if ((p + 1) * P > L) continue;\n"
      "            for (int64_t t = p * P; t < (p + 1) * P && t < L; ++t) rows[n++] = t;"),
+    ("prefill band one block short", "            keep = kb < sink_blocks || kb > qb - local_blocks;",
+     "            keep = kb < sink_blocks || kb > qb - local_blocks + 1;"),
+    ("prefill ignores the causal bound", "    for (int64_t i = 0; i <= p; ++i) {",
+     "    for (int64_t i = 0; i < L; ++i) {"),
+    ("prefill query position off by one", "    const int64_t p = L - Tq + t;",
+     "    const int64_t p = L - Tq + t - 1;"),
 ]
 
 
@@ -75,7 +82,8 @@ def _pin_calls():
     """Every pin of the oracle's pin modules as a list of zero-argument callables."""
     calls = []
     fns = inspect.getmembers(pins, inspect.isfunction) + \
-        inspect.getmembers(pins_fp8, inspect.isfunction)
+        inspect.getmembers(pins_fp8, inspect.isfunction) + \
+        inspect.getmembers(pins_prefill, inspect.isfunction)
     for name, fn in fns:
         if not name.startswith("test_"):
             continue
