@@ -283,6 +283,49 @@ dattn_status_t dattn_decode_noalloc(const dattn_kv_layout *layout, const void *k
                                     float *out, float *m_g, float *e_g, int32_t *dev_err,
                                     void *stream);
 
+/* Block-sparse prefill settings [LV §2.1.1, §2.1.2, §2.2.1]. Key and query blocks are 64
+ * tokens: key block kb holds tokens 64*kb .. 64*kb + 63. */
+typedef struct dattn_prefill_sparse {
+    const int8_t *head_kind;     /* (device) [Hkv]: DATTN_HEAD_* per KV head */
+    int32_t sink_blocks;         /* streaming heads: key blocks [0, sink_blocks) ... */
+    int32_t local_blocks;        /* ... and the local_blocks key blocks ending at the query's */
+    int32_t max_sel;             /* retrieval heads: entries per row of block_lists */
+    int32_t qblock_stride;       /* rows of block_lists per (request, KV head) */
+    const int32_t *block_lists;  /* (device) [B][Hkv][qblock_stride][max_sel]: row qb lists the
+                                    key blocks the queries of block qb attend; -1 entries are
+                                    ignored, and a block must not appear twice in one row */
+} dattn_prefill_sparse;
+
+/*
+ * Block-sparse prefill of a chunk of Tq new tokens per request [LV §2.1.1: the KV history is
+ * cut into fixed 64-token blocks and only the chosen blocks are loaded and computed; §2.1.2:
+ * streaming heads keep a static Lambda pattern of the initial and the neighbouring blocks,
+ * retrieval heads a set of blocks chosen at run time; §2.2.1: a block iterator walks the
+ * chosen blocks without branches]. The chunk is the last Tq of the L_b = seq_lens[b] tokens
+ * of request b (append it first with dattn_kv_append). Query token t, at position
+ * p = L_b - Tq + t in query block qb = p / 64, attends the keys i <= p whose block
+ * kb = i / 64 its KV head keeps for qb:
+ *   sparse == NULL or DATTN_HEAD_DENSE: every kb <= qb (causal attention);
+ *   DATTN_HEAD_STREAMING: kb < sink_blocks, or qb - local_blocks < kb <= qb;
+ *   DATTN_HEAD_RETRIEVAL: the blocks listed in row qb of block_lists (blocks after qb add
+ *                         nothing); a query that keeps no key gives out = 0, m = -inf, e = 0.
+ * One CTA computes one 64-token query block of one query head over all its key blocks, so
+ * no workspace is needed.
+ *
+ *   k_pool, v_pool (device) the pool, bf16 only (DATTN_ERR_UNSUPPORTED for the 8-bit format)
+ *   q        (device) bf16 [B][Tq][Hq][d];  seq_lens (device) int32 [B]
+ *   out      (device) fp32 [B][Tq][Hq][d]
+ *   m, e     (device, nullable) fp32 [B][Tq][Hq]: the row max (natural-log units) and sum,
+ *            so a chunk's result merges with others by dattn_merge's equations
+ * A seq_len below Tq, or a query block beyond qblock_stride, is flagged with
+ * DATTN_DEVERR_LEN_OOB and that query block is skipped (its outputs are left untouched).
+ */
+dattn_status_t dattn_prefill(const dattn_kv_layout *layout, const void *k_pool,
+                             const void *v_pool, const dattn_bf16 *q, int32_t B, int32_t Tq,
+                             int32_t Hq, float scale, const int32_t *seq_lens,
+                             const dattn_prefill_sparse *sparse, float *out, float *m, float *e,
+                             int32_t *dev_err, void *stream);
+
 /*
  * Page scoring and top-K selection for retrieval heads [LV §2.2.2, §3.1.2]. For every
  * request b and KV head h of kind DATTN_HEAD_RETRIEVAL:

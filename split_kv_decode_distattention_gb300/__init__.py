@@ -13,6 +13,7 @@ Entry points, with the same names as in include/dattn.h:
   dattn_decode       fused split-KV decode, dense or block-sparse
   dattn_decode_multi fused decode of T new query tokens per request, causal over them
   dattn_page_select  page scoring and top-K selection for retrieval heads
+  dattn_prefill      block-sparse prefill of a chunk of new tokens (64-token key blocks)
 """
 from __future__ import annotations
 
@@ -25,7 +26,7 @@ import torch
 __all__ = [
     "KVLayout", "SparseConfig", "DattnError", "load_library", "library_path",
     "dattn_kv_append", "dattn_partial", "dattn_merge", "dattn_decode", "dattn_page_select",
-    "dattn_decode_noalloc", "dattn_decode_multi",
+    "dattn_decode_noalloc", "dattn_decode_multi", "dattn_prefill", "PrefillSparseConfig",
     "dattn_workspace_size", "dattn_workspace_init", "dattn_auto_splits", "dattn_split_range",
     "dattn_split_owner", "dattn_status_string", "dattn_version", "Workspace",
     "HEAD_DENSE", "HEAD_RETRIEVAL", "HEAD_STREAMING", "DEVERR", "KV_BF16", "KV_FP8_E4M3",
@@ -59,6 +60,12 @@ class _Sparse(ctypes.Structure):
                 ("selected", ctypes.c_void_p)]
 
 
+class _PrefillSparse(ctypes.Structure):
+    _fields_ = [("head_kind", ctypes.c_void_p), ("sink_blocks", ctypes.c_int32),
+                ("local_blocks", ctypes.c_int32), ("max_sel", ctypes.c_int32),
+                ("qblock_stride", ctypes.c_int32), ("block_lists", ctypes.c_void_p)]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int32
 _I64 = ctypes.c_int64
@@ -77,6 +84,8 @@ _SIGS = {
                                   ctypes.POINTER(_Sparse), _I, _P, _P, _P, _P, _P]),
     "dattn_decode_multi": (_I, [ctypes.POINTER(_Layout), _P, _P, _P, _I, _I, _I, _F, _P, _I, _P,
                                 _SZ, _P, _P, _P, _P, _P]),
+    "dattn_prefill": (_I, [ctypes.POINTER(_Layout), _P, _P, _P, _I, _I, _I, _F, _P,
+                           ctypes.POINTER(_PrefillSparse), _P, _P, _P, _P, _P]),
     "dattn_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "dattn_workspace_init": (_I, [_P, _SZ, _P]),
     "dattn_auto_splits": (_I, [_I64]),
@@ -210,6 +219,22 @@ class SparseConfig:
                          selected.data_ptr() if selected is not None else None)
 
 
+class PrefillSparseConfig:
+    """Block-sparse prefill settings: per-KV-head kinds, the streaming heads' sink and local
+    block counts, and the retrieval heads' key-block lists (int32 [B][Hkv][qblock_stride]
+    [max_sel], row qb for query block qb, -1 padded)."""
+
+    def __init__(self, head_kind: torch.Tensor, sink_blocks: int, local_blocks: int,
+                 block_lists: torch.Tensor | None = None):
+        if head_kind.dtype != torch.int8:
+            raise TypeError("head_kind must be int8")
+        _i32(block_lists, "block_lists")
+        self.head_kind, self.block_lists = head_kind, block_lists
+        qs, ms = (block_lists.shape[2], block_lists.shape[3]) if block_lists is not None else (0, 0)
+        self.c = _PrefillSparse(head_kind.data_ptr(), sink_blocks, local_blocks, ms, qs,
+                                block_lists.data_ptr() if block_lists is not None else None)
+
+
 class Workspace:
     """A zeroed device workspace sized by dattn_workspace_size (allocated by torch)."""
 
@@ -318,6 +343,20 @@ def dattn_decode_multi(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_le
         ctypes.byref(layout.c), _ptr(k_pool), _ptr(v_pool), _ptr(q), B, T, Hq, scale,
         _ptr(seq_lens), num_splits, _ptr(ws.buffer), ws.buffer.numel(), _ptr(out), _ptr(m_g),
         _ptr(e_g), _ptr(dev_err), _stream(stream)), "dattn_decode_multi")
+
+
+def dattn_prefill(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, out, m=None,
+                  e=None, sparse: PrefillSparseConfig | None = None, dev_err=None, stream=None):
+    """Block-sparse (sparse given) or causal prefill of q bf16 [B][Tq][Hq][d], the last Tq
+    tokens of each request: out fp32 [B][Tq][Hq][d] (+ m, e fp32 [B][Tq][Hq])."""
+    _pool(layout, k_pool, "k_pool"); _pool(layout, v_pool, "v_pool"); _bf16(q, "q")
+    _i32(seq_lens, "seq_lens"); _f32(out, "out"); _f32(m, "m"); _f32(e, "e")
+    B, Tq, Hq = q.shape[0], q.shape[1], q.shape[2]
+    sp = ctypes.byref(sparse.c) if sparse is not None else None
+    _check(load_library().dattn_prefill(
+        ctypes.byref(layout.c), _ptr(k_pool), _ptr(v_pool), _ptr(q), B, Tq, Hq, scale,
+        _ptr(seq_lens), sp, _ptr(out), _ptr(m), _ptr(e), _ptr(dev_err), _stream(stream)),
+        "dattn_prefill")
 
 
 def dattn_decode_noalloc(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, out,
