@@ -58,6 +58,10 @@ WORKLOAD_TEXT = {
                    "128, 512K context, 64-token pages of four 16-token logical pages, "
                    "4 retrieval + 4 streaming KV heads, top-64 pages reused 16 steps, "
                    "4 sinks + 8 local",
+    "prefill-32k": "LServe-style block-sparse prefill, Llama-3-8B GQA (32 q / 8 KV heads, head_dim "
+                   "128): one 32K-token request prefilled as one chunk, 64-token key blocks; 4 "
+                   "retrieval KV heads keep a seeded 65% of the earlier blocks plus their own, 4 "
+                   "streaming KV heads keep 1 sink block and 16 local blocks",
 }
 
 
@@ -70,6 +74,8 @@ def parse_args():
     ap.add_argument("--impl", default="dattn", choices=["dattn", "reference"])
     ap.add_argument("--kv-format", default="bf16", choices=["bf16", "fp8"],
                     help="element format of the paged KV pool")
+    ap.add_argument("--prefill-dense", action="store_true",
+                    help="prefill-32k: every head dense (causal) instead of the LServe mix")
     ap.add_argument("--queries", type=int, default=1,
                     help="query tokens per request and step (dense workloads; 1 = decode)")
     ap.add_argument("--seed", type=int, default=0)
@@ -107,6 +113,8 @@ def make_case(args):
         kw["L"] = args.ctx
     elif name == "gqa-ragged" and args.batch:
         kw["B"] = args.batch
+    elif name == "prefill-32k" and args.ctx:
+        kw["L"] = args.ctx
     case = W.CASES[name](seed=args.seed, **kw)
     if args.queries < 1 or (args.queries > 1 and case.head_kind is not None):
         raise SystemExit("--queries T needs T >= 1 and a dense workload")
@@ -807,6 +815,23 @@ def run_reference(args, rank, world):
     import oracle
     if rank != 0:
         return
+    if args.config == "prefill-32k":
+        from split_kv_decode_distattention_gb300 import workloads as W
+        import torch
+        case = make_case(args)
+        kinds = [0] * case.Hkv if args.prefill_dense else list(case.head_kind)
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        cpu = prefill_cpu_baseline(case, dev, kinds, case.prefill_block_lists(W.PREFILL_KEEP),
+                                   W.PREFILL_SINK_BLOCKS, W.PREFILL_LOCAL_BLOCKS, case.lens[0])
+        print(json.dumps({"impl": "reference", "metric": PREFILL_METRIC, "value": cpu["value"],
+                          "unit": "TFLOP/s", "n_gpus": world, "steps": 1, "warmup": 0,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                          "dtype": "f64", "data": "synthetic", "cpu_baseline": cpu,
+                          "config": {"workload": f"{case.name}: {WORKLOAD_TEXT[case.name]}"},
+                          "e2e": {"value": cpu["value"], "unit": "TFLOP/s",
+                                  "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
     import torch
     oracle.load()
     case = make_case(args)
@@ -849,6 +874,224 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------------------ prefill leg
+
+PREFILL_METRIC = ("block-sparse prefill: achieved TFLOP/s (4*d flops per attended query-key "
+                  "pair) vs the measured bf16 tensor peak; ms per layer-step")
+
+
+def prefill_pairs(case, Tq: int, kinds, lists, sinks: int, local: int) -> int:
+    """Attended (query, key) pairs of one prefill chunk, summed over query heads, from the
+    block rules: a query at position p sees 64 keys of every kept block before its own block
+    qb, and p - 64*qb + 1 keys of block qb when it is kept."""
+    total = 0
+    for b, L in enumerate(case.lens):
+        for qb in range((L - Tq) // 64, (L - 1) // 64 + 1):
+            p0, p1 = max(L - Tq, 64 * qb), min(L, 64 * qb + 64)
+            nq = p1 - p0
+            diag = sum(p - 64 * qb + 1 for p in range(p0, p1))
+            for kvh in range(case.Hkv):
+                kind = kinds[kvh]
+                if kind == 0:
+                    before, own = qb, True
+                elif kind == 2:
+                    s_end = min(sinks, qb + 1)
+                    l0 = max(s_end, qb - local + 1)
+                    blocks = set(range(s_end)) | set(range(l0, qb + 1))
+                    before, own = len([k for k in blocks if k < qb]), qb in blocks
+                else:
+                    row = set(int(x) for x in lists[b, kvh, qb] if 0 <= x <= qb)
+                    before, own = len([k for k in row if k < qb]), qb in row
+                total += case.g * (nq * 64 * before + (diag if own else 0))
+    return total
+
+
+def run_prefill(args, rank: int, world: int):
+    """One layer-step of block-sparse prefill: the chunk's K/V appended through
+    dattn_kv_append, then dattn_prefill over the whole chunk (the lengths are reset outside the
+    timed region, so every step prefills the same chunk)."""
+    import torch
+
+    import split_kv_decode_distattention_gb300 as dattn
+    from split_kv_decode_distattention_gb300 import workloads as W
+    from split_kv_decode_distattention_gb300.harness import PagedCache
+
+    dattn.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = make_case(args)
+    L = case.lens[0]
+    Tq = L
+    dense = args.prefill_dense
+    kinds = [0] * case.Hkv if dense else list(case.head_kind)
+    sinks, local = W.PREFILL_SINK_BLOCKS, W.PREFILL_LOCAL_BLOCKS
+    cache = PagedCache(case, dev, fill=False)
+    q = case.prefill_queries(Tq, dev)
+    K, V = case.kv(0, 0, L, dev)
+    kn, vn = K.unsqueeze(0).contiguous(), V.unsqueeze(0).contiguous()
+    del K, V
+    lists = case.prefill_block_lists(W.PREFILL_KEEP)
+    sp = None
+    if not dense:
+        sp = dattn.PrefillSparseConfig(torch.tensor(kinds, dtype=torch.int8, device=dev), sinks,
+                                       local, torch.from_numpy(lists).to(dev))
+    out = torch.empty(1, Tq, case.Hq, case.d, dtype=torch.float32, device=dev)
+    flops = 4 * case.d * prefill_pairs(case, Tq, kinds, lists, sinks, local)
+    stream = torch.cuda.current_stream()
+    flush = L2Flush(dev)
+
+    def step(ev=None):
+        cache.append(kn, vn)
+        if ev is not None:
+            ev[0].record(stream)
+        dattn.dattn_prefill(cache.layout, cache.k_pool, cache.v_pool, q, case.scale,
+                            cache.seq_lens, out, sparse=sp, dev_err=cache.dev_err)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        cache.seq_lens.zero_()
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index) if not args.no_clocks else None
+    if clocks:
+        clocks.start()
+    times, kern = [], []
+    for _ in range(args.steps):
+        cache.seq_lens.zero_()
+        flush()  # outside the timed region
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        kev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        e0.record(stream)
+        step(kev)
+        e1.record(stream)
+        times.append((e0, e1))
+        kern.append(kev)
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    err = int(cache.dev_err.item())
+    if err:
+        raise RuntimeError(f"device error word {err:#x}")
+    step_ms = [a.elapsed_time(b) for a, b in times]
+    kern_ms = [a.elapsed_time(b) for a, b in kern]
+    ms = sum(step_ms) / len(step_ms)
+    kms = sum(kern_ms) / len(kern_ms)
+    res = {"flops": flops, "ms": ms, "kms": kms, "kern_ms": kern_ms, "clocks": clk,
+           "case": case, "Tq": Tq}
+    # end to end: the chunk's q and K/V from pinned host memory, out back to pinned memory
+    if not args.no_e2e:
+        hq, hk, hv = q.cpu().pin_memory(), kn.cpu().pin_memory(), vn.cpu().pin_memory()
+        hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+        n = max(2, min(args.steps, 5))
+        tot = 0.0
+        for _ in range(n):
+            cache.seq_lens.zero_()
+            flush()
+            a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            cache.append(dk, dv)
+            dattn.dattn_prefill(cache.layout, cache.k_pool, cache.v_pool, dq, case.scale,
+                                cache.seq_lens, out, sparse=sp, dev_err=cache.dev_err)
+            hout.copy_(out, non_blocking=True)
+            b2.record(stream)
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b2)
+        res["e2e"] = {"value": round(flops / (tot / n * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                      "h2d_bytes_per_step": hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2,
+                      "d2h_bytes_per_step": hout.numel() * 4,
+                      "ms_per_layer_step": round(tot / n, 3), "steps": n}
+    return res
+
+
+def prefill_cpu_baseline(case, device, kinds, lists, sinks, local, Tq):
+    """The oracle's prefill attention on the host cores over a sample of query rows of two
+    heads (the first of each kind present), as TFLOP/s."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    oracle.load()
+    nthreads = len(os.sched_getaffinity(0))
+    L = case.lens[0]
+    q = oracle.bf16_bits(case.prefill_queries(Tq, device))
+    heads = sorted({kinds.index(k) for k in set(kinds)})
+    kv = {}
+    for h in heads:
+        K, V = case.kv(0, 0, L, device)
+        kv[h] = (oracle.bf16_bits(K[:, h]), oracle.bf16_bits(V[:, h]))
+    ts = np.linspace(0, Tq - 1, 96).astype(np.int64)
+    work = [(h, int(t)) for h in heads for t in ts]
+
+    def one(ht):
+        h, t = ht
+        qblk = (L - Tq + t) // 64
+        rows = oracle.prefill_rows(kinds[h], L, Tq, t, sinks, local,
+                                   blocks=lists[0, h, qblk] if kinds[h] == 1 else None)
+        oracle.attention(q[0, t, h * case.g], kv[h][0], kv[h][1], case.scale, rows=rows)
+        return rows.shape[0]
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=nthreads) as ex:
+        pairs = sum(ex.map(one, work))
+    secs = time.perf_counter() - t0
+    return {"value": round(4 * case.d * pairs / secs / 1e12, 6), "unit": "TFLOP/s",
+            "cores": min(nthreads, len(work)), "kind": "oracle",
+            "sample": f"{len(ts)} query rows spread over the chunk for KV heads {heads} "
+                      f"(one query head each), fp64 attention over their prefill rows: "
+                      f"{secs:.1f} s wall"}
+
+
+def prefill_main(args, rank: int, world: int):
+    from split_kv_decode_distattention_gb300 import workloads as W
+    res = run_prefill(args, rank, world)
+    case = res["case"]
+    dense = args.prefill_dense
+    kinds = [0] * case.Hkv if dense else list(case.head_kind)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = prefill_cpu_baseline(case, "cuda", kinds, case.prefill_block_lists(W.PREFILL_KEEP),
+                                   W.PREFILL_SINK_BLOCKS, W.PREFILL_LOCAL_BLOCKS, res["Tq"])
+    if rank != 0:
+        return
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        pass
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    tflops = res["flops"] / (res["ms"] * 1e-3) / 1e12
+    ktf = res["flops"] / (res["kms"] * 1e-3) / 1e12
+    cfg = {"workload": f"{case.name}: {WORKLOAD_TEXT[case.name]}" +
+                       (" (every head dense: causal attention)" if dense else ""),
+           "batch": case.B, "q_heads": case.Hq, "kv_heads": case.Hkv, "head_dim": case.d,
+           "page_size": case.P, "context_tokens": case.lens[0], "chunk_tokens": res["Tq"],
+           "seed": args.seed, "parallelism": "replicas" if args.gpus > 1 else "single GPU",
+           "step": "dattn_kv_append (the chunk's K/V) + dattn_prefill",
+           "l2": f"flushed before every timed step ({L2Flush.TEXT})",
+           "launch": "eager library calls"}
+    line = {
+        "metric": PREFILL_METRIC, "value": round(tflops, 2), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(res["ms"], 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/Q)", "config": cfg,
+        "roofline": {"bound": "tensor", "kernel": "prefill_kernel (dattn_prefill)",
+                     "achieved": round(ktf, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(ktf / peak, 4),
+                     "peak_source": "measured" if "bf16_tflops" in peaks else "fallback",
+                     "traffic": None, "algorithmic_flops_per_launch": int(res["flops"]),
+                     "avg_launch_ms": round(res["kms"], 4),
+                     "kernel_timing": "CUDA events around the prefill kernel in every step"},
+        # the chunk's append is two launches (the kernel, then the length update), then one
+        "gpu_launches": 3 * args.steps,
+        "clocks": res["clocks"], "cpu_baseline": cpu,
+    }
+    if "e2e" in res:
+        line["e2e"] = res["e2e"]
+    print(json.dumps(line), flush=True)
+
+
 def config_obj(case, args):
     c = {"workload": f"{case.name}: {WORKLOAD_TEXT[case.name]}", "batch": case.B,
          "q_heads": case.Hq, "kv_heads": case.Hkv, "head_dim": case.d, "page_size": case.P,
@@ -888,6 +1131,11 @@ def main():
         local = int(os.environ.get("LOCAL_RANK", "0"))
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
+    if args.config == "prefill-32k":
+        prefill_main(args, rank, world)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     res = run_dattn(args, rank, world)
     case = res["case"]
     cpu = None

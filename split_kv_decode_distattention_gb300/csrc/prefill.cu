@@ -13,7 +13,7 @@
 // 16-token K and V row groups through an 8-stage shared-memory ring with 3-D TMA boxes (the
 // decode's boxes and swizzle), issuing four tiles side by side, one lane each. Four consumer
 // warps own 16 query rows each and take a whole key block per step: S = Q K^T on mma.sync
-// m16n8k16 (bf16, fp32 accumulate; the query block stays in registers), the causal and
+// m16n8k16 (bf16, fp32 accumulate; the query rows stay in shared memory), the causal and
 // length mask, an online softmax in base 2 whose row sums stay per thread until the end, and
 // O += P V with P taken straight from the S accumulators (as two bf16 terms). Every warp reads every stage, so a
 // stage is released after four arrivals. No CTA depends on another: no workspace, no merge.
@@ -54,10 +54,11 @@ struct PfParams {
     int32_t* dev_err;
 };
 
-// Shared memory: the ring of stages (K tile, then V tile), the full and empty barriers and the
-// per-stage metadata (valid rows | skip flag).
+// Shared memory: the ring of stages (K tile, then V tile), each consumer warp's 16 query rows
+// (in the K tiles' swizzled layout, read by ldmatrix), the full and empty barriers, the
+// per-stage metadata (valid rows | skip flag) and the producer's compacted block ids.
 struct PfSmem {
-    uint32_t stage_bytes, stages, bars, meta, total;
+    uint32_t stage_bytes, stages, qs, bars, meta, comp, total;
 };
 
 __host__ __device__ inline PfSmem pf_smem_layout(int D) {
@@ -65,8 +66,10 @@ __host__ __device__ inline PfSmem pf_smem_layout(int D) {
     s.stage_bytes = 64u * (uint32_t)D;  // K and V: 16 rows of D bf16 each
     uint32_t o = 0;
     s.stages = o; o += kPfStages * s.stage_bytes;
+    s.qs = o;     o += kPfWarps * 32u * (uint32_t)D;  // each warp's 16 query rows
     s.bars = o;   o += 2u * kPfStages * 8u;
     s.meta = o;   o += kPfStages * 4u;
+    s.comp = o;   o += 32u * 4u;  // the producer's compacted block ids
     s.total = o + 1024u;  // slack to align the base to 1024 bytes (TMA swizzle)
     return s;
 }
@@ -79,7 +82,9 @@ struct BlockIter {
     int32_t s_end, l0;          // streaming: sinks [0, s_end), band [l0, qb]
     const int32_t* list;        // retrieval: the row of block_lists
     __device__ int32_t count() const { return n; }
-    // the i-th block (i < n); a retrieval entry that is not a block at or before qb gives -1
+    // the i-th entry (i < n): a key block, or -1 for a retrieval entry that is not a block at
+    // or before qb. Both the producer and the consumers skip the -1 entries the same way:
+    // 32 entries at a time, a ballot of the valid ones, then those blocks in order.
     __device__ int32_t at(int32_t i) const {
         if (kind == DATTN_HEAD_STREAMING) return i < s_end ? i : l0 + (i - s_end);
         if (kind == DATTN_HEAD_RETRIEVAL) {
@@ -120,7 +125,7 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kPfThreads)
+__global__ void __launch_bounds__(kPfThreads, 2)
 prefill_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CUtensorMap tmap_k,
                const __grid_constant__ CUtensorMap tmap_v) {
     constexpr int KS = D / 16;  // k-steps of Q K^T
@@ -182,57 +187,66 @@ prefill_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CUten
         const uint64_t pol = policy_evict_normal();  // later query blocks read the same K/V
         const uint32_t tile_bytes = 32u * (uint32_t)D;
         const uint32_t stages0 = smem_u32(base + L.stages);
+        int32_t* comp = reinterpret_cast<int32_t*>(base + L.comp);
         int32_t k = 0;  // tiles issued: tile k uses stage k % kPfStages
         bool stop = false;
-        for (int32_t i0 = 0; i0 < nblk && !stop; i0 += 32 / kPfTiles) {
-            // resolve up to 8 blocks (32 tiles): lane l takes tile l % 4 of block i0 + l / 4
-            const int32_t nb = min(32 / kPfTiles, nblk - i0);
-            int32_t y = 0, lohi = kPfSkip;
-            if (lane < nb * kPfTiles) {
-                const int32_t kb = it.at(i0 + lane / kPfTiles);
-                const int32_t t0 = kb * kPfBlock + 16 * (lane % kPfTiles);
-                if (kb >= 0 && t0 < p_hi) {  // keys after the last query are never visible
-                    const int32_t lp = t0 / p.P;
-                    const int32_t page = __ldg(p.block_table + (int64_t)b * p.max_pages + lp);
-                    if (page < 0) {
-                        set_err(p.dev_err, DATTN_DEVERR_UNMAPPED_PAGE);
-                    } else if (page >= p.num_pages) {
-                        set_err(p.dev_err, DATTN_DEVERR_PAGE_OOB);
-                    } else {
-                        y = (page * p.Hkv + kvh) * p.P + (t0 - lp * p.P);
-                        lohi = min(16, Ln - t0);
-                    }
-                }
-            }
-            // issue a block at a time, lane u of the group taking tile u
-            for (int32_t bi = 0; bi < nb; ++bi, k += kPfTiles) {
-                const int32_t src = min(bi * kPfTiles + lane, 31);
-                const int32_t ty = __shfl_sync(0xffffffffu, y, src);
-                const int32_t tm = __shfl_sync(0xffffffffu, lohi, src);
-                bool ok = true;
-                if (lane < kPfTiles) {
-                    const int32_t kk = k + lane, stg = kk % kPfStages;
-                    if (kk >= kPfStages)
-                        ok = mbar_wait(bars + 8u * (kPfStages + stg), ((kk / kPfStages) - 1) & 1,
-                                       abort_p, p.dev_err);
-                    if (ok) {
-                        const uint32_t full = bars + 8u * stg;
-                        meta[stg] = tm;
-                        if (tm & kPfSkip) {
-                            mbar_arrive(full);
+        for (int32_t i0 = 0; i0 < nblk && !stop; i0 += 32) {
+            const int32_t kbl = i0 + lane < nblk ? it.at(i0 + lane) : -1;
+            const unsigned vm = __ballot_sync(0xffffffffu, kbl >= 0);
+            if (kbl >= 0) comp[__popc(vm & ((1u << lane) - 1u))] = kbl;
+            __syncwarp();
+            const int32_t nv = __popc(vm);
+            for (int32_t v0 = 0; v0 < nv && !stop; v0 += 32 / kPfTiles) {
+                // resolve up to 8 blocks (32 tiles): lane l takes tile l % 4 of block v0 + l / 4
+                const int32_t nb = min(32 / kPfTiles, nv - v0);
+                int32_t y = 0, lohi = kPfSkip;
+                if (lane < nb * kPfTiles) {
+                    const int32_t kb = comp[v0 + lane / kPfTiles];
+                    const int32_t t0 = kb * kPfBlock + 16 * (lane % kPfTiles);
+                    if (t0 < p_hi) {  // keys after the last query are never visible
+                        const int32_t lp = t0 / p.P;
+                        const int32_t page = __ldg(p.block_table + (int64_t)b * p.max_pages + lp);
+                        if (page < 0) {
+                            set_err(p.dev_err, DATTN_DEVERR_UNMAPPED_PAGE);
+                        } else if (page >= p.num_pages) {
+                            set_err(p.dev_err, DATTN_DEVERR_PAGE_OOB);
                         } else {
-                            mbar_arrive_expect_tx(full, 2u * tile_bytes);
-                            const uint32_t dst = stages0 + (uint32_t)stg * L.stage_bytes;
-                            tma_load_3d(dst, &tmap_k, 0, ty, 0, full, pol);
-                            tma_load_3d(dst + tile_bytes, &tmap_v, 0, ty, 0, full, pol);
+                            y = (page * p.Hkv + kvh) * p.P + (t0 - lp * p.P);
+                            lohi = min(16, Ln - t0);
                         }
                     }
                 }
-                if (__any_sync(0xffffffffu, !ok)) {
-                    stop = true;
-                    break;
+                // issue a block at a time, lane u of the group taking tile u
+                for (int32_t bi = 0; bi < nb; ++bi, k += kPfTiles) {
+                    const int32_t src = min(bi * kPfTiles + lane, 31);
+                    const int32_t ty = __shfl_sync(0xffffffffu, y, src);
+                    const int32_t tm = __shfl_sync(0xffffffffu, lohi, src);
+                    bool ok = true;
+                    if (lane < kPfTiles) {
+                        const int32_t kk = k + lane, stg = kk % kPfStages;
+                        if (kk >= kPfStages)
+                            ok = mbar_wait(bars + 8u * (kPfStages + stg),
+                                           ((kk / kPfStages) - 1) & 1, abort_p, p.dev_err);
+                        if (ok) {
+                            const uint32_t full = bars + 8u * stg;
+                            meta[stg] = tm;
+                            if (tm & kPfSkip) {
+                                mbar_arrive(full);
+                            } else {
+                                mbar_arrive_expect_tx(full, 2u * tile_bytes);
+                                const uint32_t dst = stages0 + (uint32_t)stg * L.stage_bytes;
+                                tma_load_3d(dst, &tmap_k, 0, ty, 0, full, pol);
+                                tma_load_3d(dst + tile_bytes, &tmap_v, 0, ty, 0, full, pol);
+                            }
+                        }
+                    }
+                    if (__any_sync(0xffffffffu, !ok)) {
+                        stop = true;
+                        break;
+                    }
                 }
             }
+            __syncwarp();  // comp is rewritten for the next 32 entries
         }
         // after an abort, wait (bounded in total) for copies still in flight
         if (lane == 0 && *abort_p) {
@@ -250,21 +264,23 @@ prefill_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CUten
     const int g8 = lane >> 2, tig = lane & 3;
     const int32_t pos0 = qb * kPfBlock + warp * 16 + g8, pos1 = pos0 + 8;  // query positions
     const bool ok0 = pos0 >= p_lo && pos0 < p_hi, ok1 = pos1 >= p_lo && pos1 < p_hi;
-    // the query rows as mma A fragments, kept for the whole block loop
-    uint32_t qa[KS][4];
-    {
-        const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
-            p.q + (((int64_t)b * p.Tq + (ok0 ? pos0 - c0 : 0)) * p.Hq + h) * D);
-        const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
-            p.q + (((int64_t)b * p.Tq + (ok1 ? pos1 - c0 : 0)) * p.Hq + h) * D);
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            qa[ks][0] = ok0 ? __ldg(q0 + ks * 8 + tig) : 0u;
-            qa[ks][1] = ok1 ? __ldg(q1 + ks * 8 + tig) : 0u;
-            qa[ks][2] = ok0 ? __ldg(q0 + ks * 8 + 4 + tig) : 0u;
-            qa[ks][3] = ok1 ? __ldg(q1 + ks * 8 + 4 + tig) : 0u;
-        }
+    const bool all_rows = p_lo == qb * kPfBlock && p_hi == qb * kPfBlock + kPfBlock;
+    // The warp's 16 query rows go to shared memory once, in the K tiles' swizzled layout
+    // ([half][row][64 values]); each k-step reads them as mma A fragments with ldmatrix, which
+    // leaves the registers to the accumulator.
+    const uint32_t qbase = smem_u32(base + L.qs) + (uint32_t)warp * 32u * (uint32_t)D;
+    for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
+        const int r = idx / (D / 8), ch = idx - r * (D / 8);
+        const int32_t pos = qb * kPfBlock + warp * 16 + r;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (pos >= p_lo && pos < p_hi)
+            v = __ldg(reinterpret_cast<const uint4*>(
+                p.q + (((int64_t)b * p.Tq + (pos - c0)) * p.Hq + h) * D) + ch);
+        *reinterpret_cast<uint4*>(base + (qbase - smem_u32(base)) + (ch >> 3) * 2048u +
+                                  swz128((uint32_t)r, (uint32_t)(ch & 7))) = v;
     }
+    __syncwarp();
+    const uint32_t qrow = (lane & 7) + (((lane >> 3) & 1) << 3), qcs = lane >> 4;
     float o[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
@@ -276,55 +292,87 @@ prefill_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CUten
     const uint32_t krow = (lane & 7) + ((lane >> 4) << 3), kcs = (lane >> 3) & 1;
     const uint32_t vrow = (lane & 7) + (((lane >> 3) & 1) << 3), vcs = lane >> 4;
     int32_t k = 0;
-    for (int32_t i = 0; i < nblk; ++i, k += kPfTiles) {
+    bool aborted = false;
+    for (int32_t i0 = 0; i0 < nblk && !aborted; i0 += 32) {
+      const int32_t kbl = i0 + lane < nblk ? it.at(i0 + lane) : -1;
+      unsigned vm = __ballot_sync(0xffffffffu, kbl >= 0);
+      for (; vm != 0u; vm &= vm - 1u, k += kPfTiles) {
+        const int32_t kb = __shfl_sync(0xffffffffu, kbl, __ffs(vm) - 1);
         bool ok = true;
 #pragma unroll
         for (int u = 0; u < kPfTiles; ++u)
             ok = ok && mbar_wait(bars + 8u * ((k + u) % kPfStages), ((k + u) / kPfStages) & 1,
                                  abort_p, p.dev_err);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        const int32_t kb = it.at(i);
+        if (!__all_sync(0xffffffffu, ok)) {
+            aborted = true;
+            break;
+        }
         const bool diag = kb == qb;  // only the diagonal block needs the causal test
         int32_t hi[kPfTiles];
+        bool full_tiles = true;  // every tile holds 16 valid keys
 #pragma unroll
         for (int u = 0; u < kPfTiles; ++u) {
             const int32_t mt = meta[(k + u) % kPfStages];
             hi[u] = (mt & kPfSkip) ? -1 : mt;  // valid rows of the tile; -1: no data
+            full_tiles = full_tiles && hi[u] == 16;
         }
-        // ---- S = Q K^T over the block's 64 keys -----------------------------------------
-        float s[kPfTiles][2][4];
+        // warp-uniform: only the diagonal block, a short tile or a partly filled query block
+        // needs the per-element mask
+        const bool masked = diag || !full_tiles || !all_rows;
+        // The block's four tiles go two at a time (32 keys), which keeps the scores of a half
+        // in registers next to the query fragments and the accumulator.
 #pragma unroll
-        for (int u = 0; u < kPfTiles; ++u) {
+        for (int hb = 0; hb < kPfTiles / 2; ++hb) {
+        // ---- S = Q K^T over 32 keys (each query fragment serves both tiles) ---------------
+        float s[2][2][4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) s[u][0][e] = s[u][1][e] = 0.f;
-            if (hi[u] < 0) continue;  // warp-uniform
-            const uint32_t kbase = stage0 + (uint32_t)((k + u) % kPfStages) * L.stage_bytes;
+        for (int uu = 0; uu < 2; ++uu)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[uu][0][e] = s[uu][1][e] = 0.f;
+        const bool t0ok = hi[2 * hb] >= 0, t1ok = hi[2 * hb + 1] >= 0;  // warp-uniform
+        if (t0ok || t1ok) {
+            const uint32_t kb0 = stage0 + (uint32_t)((k + 2 * hb) % kPfStages) * L.stage_bytes;
+            const uint32_t kb1 = stage0 + (uint32_t)((k + 2 * hb + 1) % kPfStages) * L.stage_bytes;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                const uint32_t chunk = 2u * ks + kcs;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kbase + (chunk >> 3) * 2048u + swz128(krow, chunk & 7u), b0, b1, b2, b3);
-                mma_bf16(s[u][0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-                mma_bf16(s[u][1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+                const uint32_t qchunk = 2u * ks + qcs, chunk = 2u * ks + kcs;
+                const uint32_t koff = (chunk >> 3) * 2048u + swz128(krow, chunk & 7u);
+                uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+                ldsm_x4(qbase + (qchunk >> 3) * 2048u + swz128(qrow, qchunk & 7u), a0, a1, a2, a3);
+                if (t0ok) {
+                    ldsm_x4(kb0 + koff, b0, b1, b2, b3);
+                    mma_bf16(s[0][0], a0, a1, a2, a3, b0, b1);
+                    mma_bf16(s[0][1], a0, a1, a2, a3, b2, b3);
+                }
+                if (t1ok) {
+                    ldsm_x4(kb1 + koff, b0, b1, b2, b3);
+                    mma_bf16(s[1][0], a0, a1, a2, a3, b0, b1);
+                    mma_bf16(s[1][1], a0, a1, a2, a3, b2, b3);
+                }
             }
         }
         // ---- mask (length, causal, empty tiles), scale to base 2, row maxima -------------
         float mx0 = kPfNegInf, mx1 = kPfNegInf;
 #pragma unroll
-        for (int u = 0; u < kPfTiles; ++u) {
+        for (int uu = 0; uu < 2; ++uu) {
+            const int u = 2 * hb + uu;
 #pragma unroll
             for (int n = 0; n < 2; ++n) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int32_t r = 8 * n + 2 * tig + (e & 1);  // key row within the tile
-                    const int32_t key = kb * kPfBlock + 16 * u + r;
-                    const bool row1 = e >= 2;
-                    bool v = r < hi[u] && (row1 ? ok1 : ok0);
-                    if (diag) v = v && key <= (row1 ? pos1 : pos0);
-                    s[u][n][e] = v ? s[u][n][e] * p.sl2 : kPfNegInf;
+                    if (masked) {
+                        const int32_t r = 8 * n + 2 * tig + (e & 1);  // key row within the tile
+                        const int32_t key = kb * kPfBlock + 16 * u + r;
+                        const bool row1 = e >= 2;
+                        bool v = r < hi[u] && (row1 ? ok1 : ok0);
+                        if (diag) v = v && key <= (row1 ? pos1 : pos0);
+                        s[uu][n][e] = v ? s[uu][n][e] * p.sl2 : kPfNegInf;
+                    } else {
+                        s[uu][n][e] *= p.sl2;
+                    }
                 }
-                mx0 = fmaxf(mx0, fmaxf(s[u][n][0], s[u][n][1]));
-                mx1 = fmaxf(mx1, fmaxf(s[u][n][2], s[u][n][3]));
+                mx0 = fmaxf(mx0, fmaxf(s[uu][n][0], s[uu][n][1]));
+                mx1 = fmaxf(mx1, fmaxf(s[uu][n][2], s[uu][n][3]));
             }
         }
 #pragma unroll
@@ -347,30 +395,31 @@ prefill_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CUten
         m0 = mn0;
         m1 = mn1;
 #pragma unroll
-        for (int u = 0; u < kPfTiles; ++u) {
+        for (int uu = 0; uu < 2; ++uu) {
 #pragma unroll
             for (int n = 0; n < 2; ++n) {
-                s[u][n][0] = exp2f(s[u][n][0] - mu0);
-                s[u][n][1] = exp2f(s[u][n][1] - mu0);
-                s[u][n][2] = exp2f(s[u][n][2] - mu1);
-                s[u][n][3] = exp2f(s[u][n][3] - mu1);
-                l0 += s[u][n][0] + s[u][n][1];
-                l1 += s[u][n][2] + s[u][n][3];
+                s[uu][n][0] = exp2f(s[uu][n][0] - mu0);
+                s[uu][n][1] = exp2f(s[uu][n][1] - mu0);
+                s[uu][n][2] = exp2f(s[uu][n][2] - mu1);
+                s[uu][n][3] = exp2f(s[uu][n][3] - mu1);
+                l0 += s[uu][n][0] + s[uu][n][1];
+                l1 += s[uu][n][2] + s[uu][n][3];
             }
         }
         // ---- O += P V, one 16-key step per tile; P is the S accumulator in A layout -------
 #pragma unroll
-        for (int u = 0; u < kPfTiles; ++u) {
+        for (int uu = 0; uu < 2; ++uu) {
+            const int u = 2 * hb + uu;
             if (hi[u] < 0) continue;  // warp-uniform
             // P as two bf16 terms (hi + lo: 16 significant bits), as the decode takes it
-            const uint32_t a0 = pack_bf16(s[u][0][0], s[u][0][1]);
-            const uint32_t a1 = pack_bf16(s[u][0][2], s[u][0][3]);
-            const uint32_t a2 = pack_bf16(s[u][1][0], s[u][1][1]);
-            const uint32_t a3 = pack_bf16(s[u][1][2], s[u][1][3]);
-            const uint32_t e0 = pack_bf16(s[u][0][0] - bf16_lo(a0), s[u][0][1] - bf16_hi(a0));
-            const uint32_t e1 = pack_bf16(s[u][0][2] - bf16_lo(a1), s[u][0][3] - bf16_hi(a1));
-            const uint32_t e2 = pack_bf16(s[u][1][0] - bf16_lo(a2), s[u][1][1] - bf16_hi(a2));
-            const uint32_t e3 = pack_bf16(s[u][1][2] - bf16_lo(a3), s[u][1][3] - bf16_hi(a3));
+            const uint32_t a0 = pack_bf16(s[uu][0][0], s[uu][0][1]);
+            const uint32_t a1 = pack_bf16(s[uu][0][2], s[uu][0][3]);
+            const uint32_t a2 = pack_bf16(s[uu][1][0], s[uu][1][1]);
+            const uint32_t a3 = pack_bf16(s[uu][1][2], s[uu][1][3]);
+            const uint32_t e0 = pack_bf16(s[uu][0][0] - bf16_lo(a0), s[uu][0][1] - bf16_hi(a0));
+            const uint32_t e1 = pack_bf16(s[uu][0][2] - bf16_lo(a1), s[uu][0][3] - bf16_hi(a1));
+            const uint32_t e2 = pack_bf16(s[uu][1][0] - bf16_lo(a2), s[uu][1][1] - bf16_hi(a2));
+            const uint32_t e3 = pack_bf16(s[uu][1][2] - bf16_lo(a3), s[uu][1][3] - bf16_hi(a3));
             // V rows past the length hold stale data: zero them so that 0 * stale stays 0
             uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
             if (hi[u] < 16) {
@@ -386,22 +435,26 @@ prefill_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CUten
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4_trans(vbase + (chunk >> 3) * 2048u + swz128(vrow, chunk & 7u), b0, b1, b2,
                               b3);
-                b0 &= mlo;
-                b1 &= mhi;
-                b2 &= mlo;
-                b3 &= mhi;
+                if (hi[u] < 16) {  // warp-uniform
+                    b0 &= mlo;
+                    b1 &= mhi;
+                    b2 &= mlo;
+                    b3 &= mhi;
+                }
                 mma_bf16(o[nt], a0, a1, a2, a3, b0, b1);
                 mma_bf16(o[nt], e0, e1, e2, e3, b0, b1);
                 mma_bf16(o[nt + 1], a0, a1, a2, a3, b2, b3);
                 mma_bf16(o[nt + 1], e0, e1, e2, e3, b2, b3);
             }
         }
+        }  // half of the block
         __syncwarp();
         if (lane == 0) {
 #pragma unroll
             for (int u = 0; u < kPfTiles; ++u)
                 mbar_arrive(bars + 8u * (kPfStages + (k + u) % kPfStages));
         }
+      }
     }
     // ---- epilogue: row sums across the four lanes of a row, then out = O / l -------------
 #pragma unroll

@@ -21,6 +21,11 @@ The workload shapes follow the pages' settings:
   * "sparse-512k": the LServe block-sparse decode. It uses 64-token physical pages of four
     16-token logical pages, retrieval heads (top-64 pages) and streaming heads (4 sinks plus
     8 local tokens), with 32 high-similarity pages per retrieval head.
+  * "prefill-32k": the LServe block-sparse prefill of one 32K-token request of Llama-3-8B
+    GQA shape, as one chunk: half the KV heads streaming (one sink block and 16 local blocks
+    of 64 tokens), half retrieval, whose key-block lists keep a seeded 65% of the earlier
+    blocks plus the query's own block (the pages report that block sparsity skips about 35%
+    of the retrieval heads' prefill work).
 """
 from __future__ import annotations
 
@@ -49,7 +54,7 @@ def _mix(*vals: int) -> int:
 
 
 _TAG = {"q": 1, "kv": 2, "table": 3, "lens": 4, "needle": 5, "highsim": 6, "sets": 7,
-        "new": 8}
+        "new": 8, "blocks": 9, "qchunk": 10}
 
 
 def _gen(device, *key) -> torch.Generator:
@@ -217,6 +222,26 @@ class Case:
             if all(s.size for s in sets) or npages == 0:
                 return sets
 
+    def prefill_queries(self, Tq: int, device="cpu", step: int = 0) -> torch.Tensor:
+        """Query vectors [B][Tq][Hq][d] (bf16) of a prefill chunk of Tq tokens."""
+        g = _gen(device, self.seed, _TAG["qchunk"], step)
+        x = torch.randn(self.B, Tq, self.Hq, self.d, generator=g, device=device)
+        return x.to(torch.bfloat16)
+
+    def prefill_block_lists(self, keep: float = 0.65, stride: int | None = None) -> np.ndarray:
+        """Key-block lists [B][Hkv][stride][stride] (int32, -1 padded) for retrieval heads:
+        row qb holds a seeded fraction `keep` of the blocks 0 .. qb-1, then qb itself."""
+        stride = stride or max(-(-L // 64) for L in self.lens)
+        out = np.full((self.B, self.Hkv, stride, stride), -1, np.int32)
+        for b in range(self.B):
+            for h in range(self.Hkv):
+                rng = _np_rng(self.seed, _TAG["blocks"], b, h)
+                for qb in range(stride):
+                    kept = np.nonzero(rng.random(qb) < keep)[0]
+                    row = np.concatenate([kept, [qb]]).astype(np.int32)
+                    out[b, h, qb, :row.size] = row
+        return out
+
     def head_kind_array(self) -> np.ndarray:
         hk = self.head_kind if self.head_kind is not None else [HEAD_DENSE] * self.Hkv
         return np.asarray(hk, np.int8)
@@ -260,12 +285,23 @@ def sparse_512k(seed: int = 0, B: int = 8, L: int = 524288) -> Case:
                 head_kind=kinds, top_k=64, sinks=4, local=8, reuse=16, n_highsim=32)
 
 
+def prefill_32k(seed: int = 0, L: int = 32768) -> Case:
+    """LServe block-sparse prefill: one 32K request, 32 q / 8 KV heads, head_dim 128, as one
+    chunk; KV heads 0-3 retrieval (65% of earlier blocks), 4-7 streaming (1 + 16 blocks)."""
+    kinds = [HEAD_RETRIEVAL] * 4 + [HEAD_STREAMING] * 4
+    return Case("prefill-32k", B=1, Hq=32, Hkv=8, d=128, P=16, lens=[L], seed=seed,
+                head_kind=kinds, reserve_tokens=0)
+
+
+PREFILL_SINK_BLOCKS, PREFILL_LOCAL_BLOCKS, PREFILL_KEEP = 1, 16, 0.65
+
 CASES = {
     "dense-tiny": dense_tiny,
     "mha-32k": mha_32k,
     "mha-1m": mha_1m,
     "gqa-ragged": gqa_ragged,
     "sparse-512k": sparse_512k,
+    "prefill-32k": prefill_32k,
 }
 
 
