@@ -7,16 +7,26 @@
 // heads a set of blocks chosen at run time; §2.2.1 walks the chosen blocks with a block
 // iterator, so the compute loop has no branches on the mask.
 //
-// GB300 design. One CTA takes one 64-token query block of one query head (the g heads of a
-// KV head are neighbouring CTAs, so their K/V reads meet in L2). A producer warp is the block
-// iterator: it walks the head's key blocks for this query block and streams each block's four
-// 16-token K and V row groups through an 8-stage shared-memory ring with 3-D TMA boxes (the
-// decode's boxes and swizzle), issuing four tiles side by side, one lane each. Four consumer
-// warps own 16 query rows each and take a whole key block per step: S = Q K^T on mma.sync
-// m16n8k16 (bf16, fp32 accumulate; the query rows stay in shared memory), the causal and
-// length mask, an online softmax in base 2 whose row sums stay per thread until the end, and
-// O += P V with P taken straight from the S accumulators (as two bf16 terms). Every warp reads every stage, so a
-// stage is released after four arrivals. No CTA depends on another: no workspace, no merge.
+// GB300 design: the contraction runs on the 5th-generation tensor cores. One CTA takes 128
+// query rows (two 64-token query blocks) of one query head; the g heads of a KV head are
+// neighbouring CTAs, so their K/V reads meet in L2, and a request's last rows (the most key
+// blocks under the causal mask) start first. The key blocks both query blocks keep are built
+// into shared-memory bitmaps, and every role walks their union in the same order: the block
+// iterator. Six warps:
+//   - a producer warp streams each key block's four 16-token tiles by TMA, one lane per
+//     tile, into a two-stage ring (K and V as [d/64 halves][64 rows][128 B] with the 128-byte
+//     swizzle, one box per half and tile);
+//   - one thread issues tcgen05.mma: S = Q K^T (M 128, N 64, K d; Q and K from shared
+//     memory, fp32 accumulator in tensor memory, double-buffered so the next block's scores
+//     are computed during this block's softmax), then O += P V (M 128, N d, K 64; P from
+//     tensor memory, V from shared memory as an MN-major operand), and commits each to an
+//     mbarrier;
+//   - four warps hold one query row per thread: they read the row's 64 scores from tensor
+//     memory, mask them (the row's query block keeps the block, the key is written and at or
+//     before the query), keep the online softmax in base 2 and write P back into the score
+//     buffer as two bf16 terms (hi + lo, 16 significant bits), which the PV product reads.
+// O is rescaled lazily, only when a row's maximum grows by more than 2^8, so most blocks touch
+// tensor memory only through the products. No CTA depends on another: no workspace, no merge.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -31,9 +41,6 @@ namespace {
 #define kPfNegInf (-__int_as_float(0x7f800000))
 
 constexpr int kPfBlock = 64;                       // query and key block, tokens
-constexpr int kPfWarps = 4;                        // consumer warps, 16 query rows each
-constexpr int kPfThreads = (kPfWarps + 1) * 32;
-constexpr int kPfStages = 8;                       // 16-token tiles in the ring: two key blocks
 constexpr int kPfTiles = kPfBlock / 16;            // tiles per key block
 
 struct PfParams {
@@ -54,156 +61,310 @@ struct PfParams {
     int32_t* dev_err;
 };
 
-// Shared memory: the ring of stages (K tile, then V tile), each consumer warp's 16 query rows
-// (in the K tiles' swizzled layout, read by ldmatrix), the full and empty barriers, the
-// per-stage metadata (valid rows | skip flag) and the producer's compacted block ids.
-struct PfSmem {
-    uint32_t stage_bytes, stages, qs, bars, meta, comp, total;
-};
-
-__host__ __device__ inline PfSmem pf_smem_layout(int D) {
-    PfSmem s;
-    s.stage_bytes = 64u * (uint32_t)D;  // K and V: 16 rows of D bf16 each
-    uint32_t o = 0;
-    s.stages = o; o += kPfStages * s.stage_bytes;
-    s.qs = o;     o += kPfWarps * 32u * (uint32_t)D;  // each warp's 16 query rows
-    s.bars = o;   o += 2u * kPfStages * 8u;
-    s.meta = o;   o += kPfStages * 4u;
-    s.comp = o;   o += 32u * 4u;  // the producer's compacted block ids
-    s.total = o + 1024u;  // slack to align the base to 1024 bytes (TMA swizzle)
-    return s;
-}
-
-// The key blocks one (request, KV head) attends for query block qb, in the order the
-// producer loads them: the block iterator of the head's kind.
-struct BlockIter {
-    int kind;
-    int32_t qb, n;
-    int32_t s_end, l0;          // streaming: sinks [0, s_end), band [l0, qb]
-    const int32_t* list;        // retrieval: the row of block_lists
-    __device__ int32_t count() const { return n; }
-    // the i-th entry (i < n): a key block, or -1 for a retrieval entry that is not a block at
-    // or before qb. Both the producer and the consumers skip the -1 entries the same way:
-    // 32 entries at a time, a ballot of the valid ones, then those blocks in order.
-    __device__ int32_t at(int32_t i) const {
-        if (kind == DATTN_HEAD_STREAMING) return i < s_end ? i : l0 + (i - s_end);
-        if (kind == DATTN_HEAD_RETRIEVAL) {
-            const int32_t kb = __ldg(list + i);
-            return (kb >= 0 && kb <= qb) ? kb : -1;
-        }
-        return i;
-    }
-};
-
-__device__ __forceinline__ BlockIter make_iter(const PfParams& p, int32_t b, int32_t kvh,
-                                               int32_t qb) {
-    BlockIter it;
-    it.qb = qb;
-    it.kind = p.head_kind ? p.head_kind[kvh] : DATTN_HEAD_DENSE;
-    if (it.kind < 0 || it.kind > 2) it.kind = DATTN_HEAD_DENSE;
-    it.list = nullptr;
-    it.s_end = it.l0 = 0;
-    if (it.kind == DATTN_HEAD_STREAMING) {
-        it.s_end = min(max(p.sink_blocks, 0), qb + 1);
-        it.l0 = max(it.s_end, qb - p.local_blocks + 1);
-        it.n = it.s_end + max(0, qb + 1 - it.l0);
-    } else if (it.kind == DATTN_HEAD_RETRIEVAL) {
-        it.list = p.block_lists + (((int64_t)b * p.Hkv + kvh) * p.qblock_stride + qb) * p.max_sel;
-        it.n = p.max_sel;
-    } else {
-        it.n = qb + 1;
-    }
-    return it;
-}
-
-constexpr int32_t kPfSkip = 1 << 16;  // stage metadata: no data in this stage
-
 __device__ __forceinline__ uint64_t policy_evict_normal() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
 
+// ------------------------------------------------------------------ tcgen05 prefill
+
+constexpr int kTcRows = 128;         // query rows per CTA (M of both products)
+constexpr int kTcSoftWarps = 4;      // one thread per row
+constexpr int kTcProdWarp = 4;       // TMA producer
+constexpr int kTcMmaWarp = 5;        // tcgen05.mma issuer
+constexpr int kTcThreads = 6 * 32;
+constexpr int kTcStages = 2;         // key blocks in flight
+constexpr uint32_t kTcCols = 256;    // TMEM: O [0, 128), S0 [128, 192), S1 [192, 256)
+constexpr float kTcRescale = 8.f;    // lazy rescale threshold (log2 units)
+
+__device__ __forceinline__ void tc_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D (TMEM) (+)= A (smem descriptor) * B (smem descriptor)
+__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// D (TMEM) (+)= A (TMEM) * B (smem descriptor)
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrives once on the mbarrier when every tcgen05.mma issued so far by this thread is done.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// 32 consecutive TMEM columns of this thread's lane (the warp's 32 lanes at once)
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a 128-byte-swizzled operand: start address, leading and
+// stride byte offsets (16-byte units), the descriptor version of this architecture (1 at bit
+// 46) and the 128-byte swizzle mode (2 at bits 61-63).
+__device__ __forceinline__ uint64_t tc_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A K-major, B K-major
+// (b_mn = 0) or MN-major (b_mn = 1), shape M x N.
+__host__ __device__ constexpr uint32_t tc_idesc(uint32_t M, uint32_t N, uint32_t b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+// Shared memory of the tcgen05 prefill (offsets from a 1024-byte aligned base): the query rows
+// [D/64][128 rows][128 B], two stages of a key block's K and V ([D/64][64 rows][128 B] each),
+// the two query blocks' key-block bitmaps, the barriers, the stage metadata and the TMEM base.
+struct TcSmem {
+    uint32_t q, stage_bytes, stages, bmA, bmB, bars, meta, taddr, total;
+};
+
+__host__ __device__ inline TcSmem tc_smem_layout(int D, int nwords) {
+    TcSmem s;
+    uint32_t o = 0;
+    s.q = o;           o += (uint32_t)kTcRows * D * 2u;
+    s.stage_bytes = 2u * 64u * D * 2u;
+    s.stages = o;      o += kTcStages * s.stage_bytes;
+    s.bmA = o;         o += (uint32_t)nwords * 4u;
+    s.bmB = o;         o += (uint32_t)nwords * 4u;
+    o = (o + 15u) & ~15u;
+    s.bars = o;        o += 10u * 8u;
+    s.meta = o;        o += kTcStages * 16u;
+    s.taddr = o;       o += 16u;
+    s.total = o + 1024u;
+    return s;
+}
+
+// The key blocks of the CTA's two query blocks, as bitmaps over blocks 0 .. qb_b: bit kb of
+// bmA is set when query block qa keeps kb, of bmB when qb_b = qa + 1 keeps it (an empty bmB
+// when the chunk has no query in qb_b). Both are built by all threads; a retrieval list may
+// hold repeats, which the bitmap absorbs.
+__device__ __forceinline__ void tc_build_bitmaps(const PfParams& p, int32_t b, int32_t kvh,
+                                                 int32_t qa, bool hasB, uint32_t* bmA,
+                                                 uint32_t* bmB, int32_t nw, int tid) {
+    const int32_t qbb = qa + 1;
+    int kind = p.head_kind ? p.head_kind[kvh] : DATTN_HEAD_DENSE;
+    if (kind < 0 || kind > 2) kind = DATTN_HEAD_DENSE;
+    for (int32_t w = tid; w < nw; w += kTcThreads) {
+        uint32_t a = 0u, bb = 0u;
+        if (kind != DATTN_HEAD_RETRIEVAL) {
+            for (int bit = 0; bit < 32; ++bit) {
+                const int32_t kb = 32 * w + bit;
+                bool ka, kb_in;
+                if (kind == DATTN_HEAD_STREAMING) {
+                    ka = kb <= qa && (kb < p.sink_blocks || kb > qa - p.local_blocks);
+                    kb_in = kb <= qbb && (kb < p.sink_blocks || kb > qbb - p.local_blocks);
+                } else {
+                    ka = kb <= qa;
+                    kb_in = kb <= qbb;
+                }
+                a |= (ka ? 1u : 0u) << bit;
+                bb |= (hasB && kb_in ? 1u : 0u) << bit;
+            }
+        }
+        bmA[w] = a;
+        bmB[w] = bb;
+    }
+    if (kind == DATTN_HEAD_RETRIEVAL) {
+        __syncthreads();
+        const int32_t* la = p.block_lists + (((int64_t)b * p.Hkv + kvh) * p.qblock_stride + qa) *
+                                                p.max_sel;
+        for (int32_t i = tid; i < 2 * p.max_sel; i += kTcThreads) {
+            const bool second = i >= p.max_sel;
+            if (second && !hasB) continue;
+            const int32_t kb = __ldg(la + i);  // row qa, then row qa + 1 right after it
+            const int32_t lim = second ? qbb : qa;
+            if (kb >= 0 && kb <= lim)
+                atomicOr(second ? bmB + (kb >> 5) : bmA + (kb >> 5), 1u << (kb & 31));
+        }
+    }
+}
+
 template <int D>
-__global__ void __launch_bounds__(kPfThreads, 2)
-prefill_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CUtensorMap tmap_k,
-               const __grid_constant__ CUtensorMap tmap_v) {
-    constexpr int KS = D / 16;  // k-steps of Q K^T
-    constexpr int NT = D / 8;   // n-tiles (8 channels) of P V
+__global__ void __launch_bounds__(kTcThreads, 1)
+prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v, int32_t nwords) {
+    constexpr int KH = D / 64;  // 128-byte halves of a row
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
     uint8_t* base;
-    {  // align by the shared-window offset: the TMA swizzle pattern is defined on it
+    {
         const uint32_t off = smem_u32(smem_raw);
         base = smem_raw + (((off + 1023u) & ~1023u) - off);
     }
-    const PfSmem L = pf_smem_layout(D);
+    const TcSmem L = tc_smem_layout(D, nwords);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // CTA -> (request, query-block slot, query head): the heads of one query block are
-    // neighbours, and a request's last query blocks (the most key blocks) start first.
     int32_t c = blockIdx.x;
     const int32_t h = c % p.Hq;
     c /= p.Hq;
-    const int32_t j = p.nqb - 1 - c % p.nqb;
+    const int32_t J = p.nqb - 1 - c % p.nqb;  // 128-row tile; the last ones start first
     const int32_t b = c / p.nqb;
     const uint32_t bars = smem_u32(base + L.bars);
+    auto kv_full = [&](int s) { return bars + 8u * s; };
+    auto kv_empty = [&](int s) { return bars + 8u * (2 + s); };
+    auto s_full = [&](int s) { return bars + 8u * (4 + s); };
+    auto p_full = [&](int s) { return bars + 8u * (6 + s); };
+    const uint32_t pv_done = bars + 64u, drain = bars + 72u;
     int32_t* meta = reinterpret_cast<int32_t*>(base + L.meta);
+    uint32_t* bmA = reinterpret_cast<uint32_t*>(base + L.bmA);
+    uint32_t* bmB = reinterpret_cast<uint32_t*>(base + L.bmB);
     volatile int* abort_p = &abort_flag;
     if (tid == 0) {
-        for (int s = 0; s < kPfStages; ++s) {
-            mbar_init(bars + 8u * s, 1);
-            mbar_init(bars + 8u * (kPfStages + s), kPfWarps);
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+            mbar_init(s_full(s), 1);
+            mbar_init(p_full(s), kTcSoftWarps * 32);
         }
+        mbar_init(pv_done, 1);
+        mbar_init(drain, 1);
         *abort_p = 0;
         fence_mbar_init();
     }
-    if (warp == kPfWarps && lane == 0) {
+    if (warp == kTcProdWarp && lane == 0) {
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_v);
     }
+    if (warp == 0) {  // the whole warp allocates the CTA's tensor memory
+        tc_alloc(smem_u32(base + L.taddr), kTcCols);
+        tc_relinquish();
+    }
+    // stale operand data must be finite: zero the query rows and both stages once
+    for (uint32_t i = tid; i < (L.stages + kTcStages * L.stage_bytes) / 16u; i += kTcThreads)
+        reinterpret_cast<uint4*>(base)[i] = make_uint4(0u, 0u, 0u, 0u);
+    tc_fence_before();
     grid_dependency_wait();  // the lengths and the pool may come from the previous kernel
     grid_launch_dependents();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(base + L.taddr);
 
+    // ---- the CTA's query rows and key blocks (uniform over the CTA) --------------------------
     const int32_t Ln = p.seq_lens[b];
-    if (Ln < p.Tq || Ln > p.max_pages * p.P) {
-        if (tid == 0 && h == 0 && j == 0) set_err(p.dev_err, DATTN_DEVERR_LEN_OOB);
-        return;
-    }
-    const int32_t c0 = Ln - p.Tq;  // position of the chunk's first token
-    const int32_t qb = c0 / kPfBlock + j;
-    const int32_t p_lo = max(c0, qb * kPfBlock), p_hi = min(Ln, qb * kPfBlock + kPfBlock);
-    if (p_lo >= p_hi) return;  // no query of the chunk in this slot
+    bool active = Ln >= p.Tq && Ln <= p.max_pages * p.P;
+    if (!active && tid == 0 && h == 0 && J == 0) set_err(p.dev_err, DATTN_DEVERR_LEN_OOB);
+    const int32_t c0 = Ln - p.Tq;
+    const int32_t qa = (active ? c0 : 0) / kPfBlock + 2 * J;
+    const int32_t p_lo = max(c0, qa * kPfBlock), p_hi = min(Ln, qa * kPfBlock + kTcRows);
+    active = active && p_lo < p_hi;
+    const bool hasB = p_hi > (qa + 1) * kPfBlock;
     const int32_t kvh = h / p.g;
-    const BlockIter it = make_iter(p, b, kvh, qb);
-    if (it.kind == DATTN_HEAD_RETRIEVAL && qb >= p.qblock_stride) {
+    if (active && p.head_kind != nullptr && p.head_kind[kvh] == DATTN_HEAD_RETRIEVAL &&
+        (qa + (hasB ? 1 : 0)) >= p.qblock_stride) {
         if (tid == 0) set_err(p.dev_err, DATTN_DEVERR_LEN_OOB);
-        return;
+        active = false;
     }
-    const int32_t nblk = it.count();
+    const int32_t nw = active ? (qa + 1 + 1 + 31) / 32 : 0;  // words over blocks 0 .. qa + 1
+    if (active) {
+        tc_build_bitmaps(p, b, kvh, qa, hasB, bmA, bmB, nw, tid);
+        // the query rows, in the K tiles' swizzled layout ([half][row][128 B])
+        for (int idx = tid; idx < kTcRows * (D / 8); idx += kTcThreads) {
+            const int r = idx / (D / 8), ch = idx - r * (D / 8);
+            const int32_t pos = qa * kPfBlock + r;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (pos >= p_lo && pos < p_hi)
+                v = __ldg(reinterpret_cast<const uint4*>(
+                    p.q + (((int64_t)b * p.Tq + (pos - c0)) * p.Hq + h) * D) + ch);
+            *reinterpret_cast<uint4*>(base + L.q + (ch >> 3) * (kTcRows * 128u) +
+                                      swz128((uint32_t)r, (uint32_t)(ch & 7))) = v;
+        }
+        fence_proxy_async_smem();  // the tensor cores read these rows through the async proxy
+    }
+    __syncthreads();
+    // Every role walks the same blocks in the same order: the set bits of bmA | bmB.
+    int32_t nblk = 0;
+    for (int32_t w = 0; w < nw; ++w) nblk += __popc(bmA[w] | bmB[w]);
 
-    if (warp == kPfWarps) {
-        // -------------------------------------------------- producer warp: the block iterator
-        const uint64_t pol = policy_evict_normal();  // later query blocks read the same K/V
-        const uint32_t tile_bytes = 32u * (uint32_t)D;
-        const uint32_t stages0 = smem_u32(base + L.stages);
-        int32_t* comp = reinterpret_cast<int32_t*>(base + L.comp);
-        int32_t k = 0;  // tiles issued: tile k uses stage k % kPfStages
-        bool stop = false;
-        for (int32_t i0 = 0; i0 < nblk && !stop; i0 += 32) {
-            const int32_t kbl = i0 + lane < nblk ? it.at(i0 + lane) : -1;
-            const unsigned vm = __ballot_sync(0xffffffffu, kbl >= 0);
-            if (kbl >= 0) comp[__popc(vm & ((1u << lane) - 1u))] = kbl;
-            __syncwarp();
-            const int32_t nv = __popc(vm);
-            for (int32_t v0 = 0; v0 < nv && !stop; v0 += 32 / kPfTiles) {
-                // resolve up to 8 blocks (32 tiles): lane l takes tile l % 4 of block v0 + l / 4
-                const int32_t nb = min(32 / kPfTiles, nv - v0);
-                int32_t y = 0, lohi = kPfSkip;
-                if (lane < nb * kPfTiles) {
-                    const int32_t kb = comp[v0 + lane / kPfTiles];
-                    const int32_t t0 = kb * kPfBlock + 16 * (lane % kPfTiles);
-                    if (t0 < p_hi) {  // keys after the last query are never visible
+    if (active && warp == kTcProdWarp) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane < kPfTiles) {
+            const uint64_t pol = policy_evict_normal();
+            const uint32_t half_bytes = 64u * 128u;  // one half of a K (or V) block
+            int32_t j = 0;
+            bool ok = true;
+            for (int32_t w = 0; w < nw && ok; ++w) {
+                uint32_t word = bmA[w] | bmB[w];
+                while (word != 0u && ok) {
+                    const int bit = __ffs(word) - 1;
+                    word &= word - 1u;
+                    const int32_t kb = 32 * w + bit;
+                    const int s = j & 1;
+                    if (j >= kTcStages && lane == 0)
+                        ok = mbar_wait(kv_empty(s), ((j >> 1) - 1) & 1, abort_p, p.dev_err);
+                    ok = __shfl_sync(0xfu, ok ? 1 : 0, 0) != 0;
+                    if (!ok) break;
+                    // lane u resolves tile u of the block
+                    const int32_t t0 = kb * kPfBlock + 16 * lane;
+                    int32_t y = 0, hi = 0;
+                    if (t0 < p_hi) {
                         const int32_t lp = t0 / p.P;
                         const int32_t page = __ldg(p.block_table + (int64_t)b * p.max_pages + lp);
                         if (page < 0) {
@@ -212,289 +373,311 @@ prefill_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CUten
                             set_err(p.dev_err, DATTN_DEVERR_PAGE_OOB);
                         } else {
                             y = (page * p.Hkv + kvh) * p.P + (t0 - lp * p.P);
-                            lohi = min(16, Ln - t0);
+                            hi = min(16, Ln - t0);
                         }
                     }
-                }
-                // issue a block at a time, lane u of the group taking tile u
-                for (int32_t bi = 0; bi < nb; ++bi, k += kPfTiles) {
-                    const int32_t src = min(bi * kPfTiles + lane, 31);
-                    const int32_t ty = __shfl_sync(0xffffffffu, y, src);
-                    const int32_t tm = __shfl_sync(0xffffffffu, lohi, src);
-                    bool ok = true;
-                    if (lane < kPfTiles) {
-                        const int32_t kk = k + lane, stg = kk % kPfStages;
-                        if (kk >= kPfStages)
-                            ok = mbar_wait(bars + 8u * (kPfStages + stg),
-                                           ((kk / kPfStages) - 1) & 1, abort_p, p.dev_err);
-                        if (ok) {
-                            const uint32_t full = bars + 8u * stg;
-                            meta[stg] = tm;
-                            if (tm & kPfSkip) {
-                                mbar_arrive(full);
-                            } else {
-                                mbar_arrive_expect_tx(full, 2u * tile_bytes);
-                                const uint32_t dst = stages0 + (uint32_t)stg * L.stage_bytes;
-                                tma_load_3d(dst, &tmap_k, 0, ty, 0, full, pol);
-                                tma_load_3d(dst + tile_bytes, &tmap_v, 0, ty, 0, full, pol);
-                            }
-                        }
-                    }
-                    if (__any_sync(0xffffffffu, !ok)) {
-                        stop = true;
-                        break;
-                    }
-                }
-            }
-            __syncwarp();  // comp is rewritten for the next 32 entries
-        }
-        // after an abort, wait (bounded in total) for copies still in flight
-        if (lane == 0 && *abort_p) {
-            const unsigned long long t0 = global_timer_ns();
-            for (int32_t kk = max(0, k - kPfStages); kk < k; ++kk) {
-                while (!mbar_try_wait(bars + 8u * (kk % kPfStages), (kk / kPfStages) & 1) &&
-                       global_timer_ns() - t0 < kWaitLimitNs) {
-                }
-            }
-        }
-        return;
-    }
-
-    // -------------------------------------------------- consumer warps: 16 query rows each
-    const int g8 = lane >> 2, tig = lane & 3;
-    const int32_t pos0 = qb * kPfBlock + warp * 16 + g8, pos1 = pos0 + 8;  // query positions
-    const bool ok0 = pos0 >= p_lo && pos0 < p_hi, ok1 = pos1 >= p_lo && pos1 < p_hi;
-    const bool all_rows = p_lo == qb * kPfBlock && p_hi == qb * kPfBlock + kPfBlock;
-    // The warp's 16 query rows go to shared memory once, in the K tiles' swizzled layout
-    // ([half][row][64 values]); each k-step reads them as mma A fragments with ldmatrix, which
-    // leaves the registers to the accumulator.
-    const uint32_t qbase = smem_u32(base + L.qs) + (uint32_t)warp * 32u * (uint32_t)D;
-    for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
-        const int r = idx / (D / 8), ch = idx - r * (D / 8);
-        const int32_t pos = qb * kPfBlock + warp * 16 + r;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (pos >= p_lo && pos < p_hi)
-            v = __ldg(reinterpret_cast<const uint4*>(
-                p.q + (((int64_t)b * p.Tq + (pos - c0)) * p.Hq + h) * D) + ch);
-        *reinterpret_cast<uint4*>(base + (qbase - smem_u32(base)) + (ch >> 3) * 2048u +
-                                  swz128((uint32_t)r, (uint32_t)(ch & 7))) = v;
-    }
-    __syncwarp();
-    const uint32_t qrow = (lane & 7) + (((lane >> 3) & 1) << 3), qcs = lane >> 4;
-    float o[NT][4];
+                    int32_t his = hi << (5 * lane), nvalid = hi > 0 ? 1 : 0;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    float m0 = kPfNegInf, m1 = kPfNegInf, l0 = 0.f, l1 = 0.f;  // row max (base 2), partial sums
-    const uint32_t stage0 = smem_u32(base + L.stages);
-    // ldmatrix lane addresses. K (B of S = Q K^T): matrices (keys 0-7 | 8-15) x (chunk
-    // 2ks | 2ks + 1) give b0, b1 of both 8-key n-tiles. V (B of O = P V, transposed):
-    // matrices (keys 0-7 | 8-15) x (chunk c | c + 1) give b0, b1 of n-tiles c and c + 1.
-    const uint32_t krow = (lane & 7) + ((lane >> 4) << 3), kcs = (lane >> 3) & 1;
-    const uint32_t vrow = (lane & 7) + (((lane >> 3) & 1) << 3), vcs = lane >> 4;
-    int32_t k = 0;
-    bool aborted = false;
-    for (int32_t i0 = 0; i0 < nblk && !aborted; i0 += 32) {
-      const int32_t kbl = i0 + lane < nblk ? it.at(i0 + lane) : -1;
-      unsigned vm = __ballot_sync(0xffffffffu, kbl >= 0);
-      for (; vm != 0u; vm &= vm - 1u, k += kPfTiles) {
-        const int32_t kb = __shfl_sync(0xffffffffu, kbl, __ffs(vm) - 1);
+                    for (int o2 = 1; o2 < kPfTiles; o2 <<= 1) {
+                        his |= __shfl_xor_sync(0xfu, his, o2);
+                        nvalid += __shfl_xor_sync(0xfu, nvalid, o2);
+                    }
+                    const uint32_t kst = smem_u32(base + L.stages) + (uint32_t)s * L.stage_bytes;
+                    const uint32_t vst = kst + KH * half_bytes;
+                    if (lane == 0) {
+                        const uint32_t flags = ((bmA[w] >> bit) & 1u) | (((bmB[w] >> bit) & 1u) << 1);
+                        meta[4 * s + 0] = kb;
+                        meta[4 * s + 1] = (int32_t)flags;
+                        meta[4 * s + 2] = his;
+                        mbar_arrive_expect_tx(kv_full(s), (uint32_t)nvalid * 2u * KH * 2048u);
+                    }
+                    __syncwarp(0xfu);
+                    if (hi > 0) {
+#pragma unroll
+                        for (int hh = 0; hh < KH; ++hh) {
+                            tma_load_3d(kst + hh * half_bytes + lane * 2048u, &tmap_k, 0, y, hh,
+                                        kv_full(s), pol);
+                            tma_load_3d(vst + hh * half_bytes + lane * 2048u, &tmap_v, 0, y, hh,
+                                        kv_full(s), pol);
+                        }
+                    }
+                    ++j;
+                }
+            }
+            // after an abort, wait (bounded in total) for copies still in flight
+            if (lane == 0 && *abort_p) {
+                const unsigned long long t0 = global_timer_ns();
+                for (int32_t jj = max(0, j - kTcStages); jj < j; ++jj)
+                    while (!mbar_try_wait(kv_full(jj & 1), (jj >> 1) & 1) &&
+                           global_timer_ns() - t0 < kWaitLimitNs) {
+                    }
+            }
+        }
+    } else if (active && warp == kTcMmaWarp) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0 && nblk > 0) {
+            constexpr uint32_t idesc_s = tc_idesc(kTcRows, 64, 0);
+            constexpr uint32_t idesc_o = tc_idesc(kTcRows, D, 1);
+            const uint32_t qs = smem_u32(base + L.q);
+            const uint32_t st0 = smem_u32(base + L.stages);
+            const uint32_t half_bytes = 64u * 128u;
+            bool ok = true;
+            // S_j = Q K_j^T into S buffer j % 2 (TMEM columns 128 + 64 (j % 2))
+            auto issue_s = [&](int32_t j) {
+                const int s = j & 1;
+                const uint32_t kst = st0 + (uint32_t)s * L.stage_bytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t ad =
+                        tc_sdesc(qs + (kk >> 2) * (kTcRows * 128u) + (kk & 3) * 32u, 16u, 1024u);
+                    const uint64_t bd = tc_sdesc(kst + (kk >> 2) * half_bytes + (kk & 3) * 32u, 16u,
+                                                 1024u);
+                    tc_mma_ss(tbase + 128u + 64u * s, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(s_full(s));
+            };
+            ok = mbar_wait(kv_full(0), 0, abort_p, p.dev_err);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+            }
+            for (int32_t j = 0; j < nblk && ok; ++j) {
+                const int s = j & 1;
+                if (j + 1 < nblk) {
+                    ok = mbar_wait(kv_full((j + 1) & 1), ((j + 1) >> 1) & 1, abort_p, p.dev_err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(j + 1);
+                }
+                ok = mbar_wait(p_full(s), (j >> 1) & 1, abort_p, p.dev_err);
+                if (!ok) break;
+                tc_fence_after();
+                // O += P_j V_j: P from TMEM (hi terms, then lo terms), V from shared memory
+                const uint32_t vst = st0 + (uint32_t)s * L.stage_bytes + KH * half_bytes;
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t bd = tc_sdesc(vst + kk * 2048u, half_bytes, 1024u);
+                        tc_mma_ts(tbase, tbase + 128u + 64u * s + 32u * part + 8u * kk, bd, idesc_o,
+                                  (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                tc_commit(kv_empty(s));
+                tc_commit(pv_done);
+            }
+            // nothing of this CTA's may still run on the tensor cores when it exits
+            tc_commit(drain);
+            mbar_wait(drain, 0, abort_p, p.dev_err);
+        }
+    } else if (active) {
+        // ---------------------------------------------------------------- softmax threads
+        const int r = tid;  // this thread's query row and TMEM lane
+        const int32_t pos = qa * kPfBlock + r;
+        const bool rowok = pos >= p_lo && pos < p_hi;
+        const uint32_t rbit = r >= 64 ? 2u : 1u;
+        const uint32_t lanes = (uint32_t)(32 * warp) << 16;
+        float m_used = kPfNegInf, m_true = kPfNegInf, l = 0.f;  // l is relative to m_used
+        int32_t j = 0;
         bool ok = true;
-#pragma unroll
-        for (int u = 0; u < kPfTiles; ++u)
-            ok = ok && mbar_wait(bars + 8u * ((k + u) % kPfStages), ((k + u) / kPfStages) & 1,
-                                 abort_p, p.dev_err);
-        if (!__all_sync(0xffffffffu, ok)) {
-            aborted = true;
-            break;
-        }
-        const bool diag = kb == qb;  // only the diagonal block needs the causal test
-        int32_t hi[kPfTiles];
-        bool full_tiles = true;  // every tile holds 16 valid keys
-#pragma unroll
-        for (int u = 0; u < kPfTiles; ++u) {
-            const int32_t mt = meta[(k + u) % kPfStages];
-            hi[u] = (mt & kPfSkip) ? -1 : mt;  // valid rows of the tile; -1: no data
-            full_tiles = full_tiles && hi[u] == 16;
-        }
-        // warp-uniform: only the diagonal block, a short tile or a partly filled query block
-        // needs the per-element mask
-        const bool masked = diag || !full_tiles || !all_rows;
-        // The block's four tiles go two at a time (32 keys), which keeps the scores of a half
-        // in registers next to the query fragments and the accumulator.
-#pragma unroll
-        for (int hb = 0; hb < kPfTiles / 2; ++hb) {
-        // ---- S = Q K^T over 32 keys (each query fragment serves both tiles) ---------------
-        float s[2][2][4];
-#pragma unroll
-        for (int uu = 0; uu < 2; ++uu)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) s[uu][0][e] = s[uu][1][e] = 0.f;
-        const bool t0ok = hi[2 * hb] >= 0, t1ok = hi[2 * hb + 1] >= 0;  // warp-uniform
-        if (t0ok || t1ok) {
-            const uint32_t kb0 = stage0 + (uint32_t)((k + 2 * hb) % kPfStages) * L.stage_bytes;
-            const uint32_t kb1 = stage0 + (uint32_t)((k + 2 * hb + 1) % kPfStages) * L.stage_bytes;
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                const uint32_t qchunk = 2u * ks + qcs, chunk = 2u * ks + kcs;
-                const uint32_t koff = (chunk >> 3) * 2048u + swz128(krow, chunk & 7u);
-                uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-                ldsm_x4(qbase + (qchunk >> 3) * 2048u + swz128(qrow, qchunk & 7u), a0, a1, a2, a3);
-                if (t0ok) {
-                    ldsm_x4(kb0 + koff, b0, b1, b2, b3);
-                    mma_bf16(s[0][0], a0, a1, a2, a3, b0, b1);
-                    mma_bf16(s[0][1], a0, a1, a2, a3, b2, b3);
+        for (int32_t w = 0; w < nw && ok; ++w) {
+            uint32_t word = bmA[w] | bmB[w];
+            while (word != 0u) {
+                word &= word - 1u;
+                const int s = j & 1;
+                // the stage's data and metadata (kv_full), then its scores (s_full)
+                ok = mbar_wait(kv_full(s), (j >> 1) & 1, abort_p, p.dev_err) &&
+                     mbar_wait(s_full(s), (j >> 1) & 1, abort_p, p.dev_err);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
                 }
-                if (t1ok) {
-                    ldsm_x4(kb1 + koff, b0, b1, b2, b3);
-                    mma_bf16(s[1][0], a0, a1, a2, a3, b0, b1);
-                    mma_bf16(s[1][1], a0, a1, a2, a3, b2, b3);
+                tc_fence_after();
+                const int32_t kb = meta[4 * s + 0];
+                const uint32_t flags = (uint32_t)meta[4 * s + 1];
+                const int32_t his = meta[4 * s + 2];
+                const uint32_t sbuf = tbase + lanes + 128u + 64u * s;
+                float x[64];
+                {
+                    float t[32];
+                    tc_ld32(sbuf, t);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[i] = t[i];
+                    tc_ld32(sbuf + 32u, t);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[32 + i] = t[i];
+                    tc_wait_ld();
                 }
-            }
-        }
-        // ---- mask (length, causal, empty tiles), scale to base 2, row maxima -------------
-        float mx0 = kPfNegInf, mx1 = kPfNegInf;
+                // mask: the row's query block keeps kb, the key is written (< length) and
+                // at or before the query
+                const bool keep = rowok && (flags & rbit) != 0u;
+                float mx = kPfNegInf;
 #pragma unroll
-        for (int uu = 0; uu < 2; ++uu) {
-            const int u = 2 * hb + uu;
+                for (int i = 0; i < 64; ++i) {
+                    const int32_t hi = (his >> (5 * (i >> 4))) & 31;
+                    const bool v = keep && (i & 15) < hi && kb * kPfBlock + i <= pos;
+                    x[i] = v ? x[i] * p.sl2 : kPfNegInf;
+                    mx = fmaxf(mx, x[i]);
+                }
+                m_true = fmaxf(m_true, mx);
+                // lazy rescale of O and l when the row maximum grows by more than 2^8; the TMEM
+                // traffic is warp-collective, so a warp rescales when any of its rows must (the
+                // others with factor 1)
+                const bool need = mx > m_used + kTcRescale || (m_used == kPfNegInf && mx != kPfNegInf);
+                const float f = need && m_used != kPfNegInf ? exp2f(m_used - mx) : 1.f;
+                l *= f;
+                if (__any_sync(0xffffffffu, f != 1.f) && j > 0) {
+                    // O holds the blocks before this one: wait for them, then scale it
+                    mbar_wait(pv_done, (j - 1) & 1, abort_p, p.dev_err);
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        float t[32];
+                        tc_ld32(tbase + lanes + 32u * cc, t);
+                        tc_wait_ld();
+                        uint32_t u32[32];
 #pragma unroll
-            for (int n = 0; n < 2; ++n) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if (masked) {
-                        const int32_t r = 8 * n + 2 * tig + (e & 1);  // key row within the tile
-                        const int32_t key = kb * kPfBlock + 16 * u + r;
-                        const bool row1 = e >= 2;
-                        bool v = r < hi[u] && (row1 ? ok1 : ok0);
-                        if (diag) v = v && key <= (row1 ? pos1 : pos0);
-                        s[uu][n][e] = v ? s[uu][n][e] * p.sl2 : kPfNegInf;
-                    } else {
-                        s[uu][n][e] *= p.sl2;
+                        for (int i = 0; i < 32; ++i) u32[i] = __float_as_uint(t[i] * f);
+                        tc_st32(tbase + lanes + 32u * cc, u32);
                     }
+                    tc_wait_st();
                 }
-                mx0 = fmaxf(mx0, fmaxf(s[uu][n][0], s[uu][n][1]));
-                mx1 = fmaxf(mx1, fmaxf(s[uu][n][2], s[uu][n][3]));
-            }
-        }
+                if (need) m_used = mx;
+                const float mu = m_used == kPfNegInf ? 0.f : m_used;
+                // P as two bf16 terms: hi into columns [0, 32) of the S buffer, lo into [32, 64)
 #pragma unroll
-        for (int off = 1; off < 4; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        // ---- online softmax ---------------------------------------------------------------
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float mu0 = mn0 == kPfNegInf ? 0.f : mn0, mu1 = mn1 == kPfNegInf ? 0.f : mn1;
-        if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
-            const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
-            l0 *= al0;
-            l1 *= al1;
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t ph[16], pl[16];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                o[nt][0] *= al0; o[nt][1] *= al0; o[nt][2] *= al1; o[nt][3] *= al1;
-            }
-        }
-        m0 = mn0;
-        m1 = mn1;
-#pragma unroll
-        for (int uu = 0; uu < 2; ++uu) {
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-                s[uu][n][0] = exp2f(s[uu][n][0] - mu0);
-                s[uu][n][1] = exp2f(s[uu][n][1] - mu0);
-                s[uu][n][2] = exp2f(s[uu][n][2] - mu1);
-                s[uu][n][3] = exp2f(s[uu][n][3] - mu1);
-                l0 += s[uu][n][0] + s[uu][n][1];
-                l1 += s[uu][n][2] + s[uu][n][3];
-            }
-        }
-        // ---- O += P V, one 16-key step per tile; P is the S accumulator in A layout -------
-#pragma unroll
-        for (int uu = 0; uu < 2; ++uu) {
-            const int u = 2 * hb + uu;
-            if (hi[u] < 0) continue;  // warp-uniform
-            // P as two bf16 terms (hi + lo: 16 significant bits), as the decode takes it
-            const uint32_t a0 = pack_bf16(s[uu][0][0], s[uu][0][1]);
-            const uint32_t a1 = pack_bf16(s[uu][0][2], s[uu][0][3]);
-            const uint32_t a2 = pack_bf16(s[uu][1][0], s[uu][1][1]);
-            const uint32_t a3 = pack_bf16(s[uu][1][2], s[uu][1][3]);
-            const uint32_t e0 = pack_bf16(s[uu][0][0] - bf16_lo(a0), s[uu][0][1] - bf16_hi(a0));
-            const uint32_t e1 = pack_bf16(s[uu][0][2] - bf16_lo(a1), s[uu][0][3] - bf16_hi(a1));
-            const uint32_t e2 = pack_bf16(s[uu][1][0] - bf16_lo(a2), s[uu][1][1] - bf16_hi(a2));
-            const uint32_t e3 = pack_bf16(s[uu][1][2] - bf16_lo(a3), s[uu][1][3] - bf16_hi(a3));
-            // V rows past the length hold stale data: zero them so that 0 * stale stays 0
-            uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-            if (hi[u] < 16) {
-                const int t0 = 2 * tig, t1 = 2 * tig + 1;
-                mlo = (t0 < hi[u] ? 0x0000ffffu : 0u) | (t1 < hi[u] ? 0xffff0000u : 0u);
-                mhi = (t0 + 8 < hi[u] ? 0x0000ffffu : 0u) | (t1 + 8 < hi[u] ? 0xffff0000u : 0u);
-            }
-            const uint32_t vbase = stage0 + (uint32_t)((k + u) % kPfStages) * L.stage_bytes +
-                                   32u * (uint32_t)D;
-#pragma unroll
-            for (int nt = 0; nt < NT; nt += 2) {
-                const uint32_t chunk = (uint32_t)nt + vcs;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(vbase + (chunk >> 3) * 2048u + swz128(vrow, chunk & 7u), b0, b1, b2,
-                              b3);
-                if (hi[u] < 16) {  // warp-uniform
-                    b0 &= mlo;
-                    b1 &= mhi;
-                    b2 &= mlo;
-                    b3 &= mhi;
+                    for (int cc = 0; cc < 16; ++cc) {
+                        const float p0 = exp2f(x[32 * hf + 2 * cc] - mu);
+                        const float p1 = exp2f(x[32 * hf + 2 * cc + 1] - mu);
+                        l += p0 + p1;
+                        ph[cc] = pack_bf16(p0, p1);
+                        pl[cc] = pack_bf16(p0 - bf16_lo(ph[cc]), p1 - bf16_hi(ph[cc]));
+                    }
+                    tc_st16(sbuf + 16u * hf, ph);
+                    tc_st16(sbuf + 32u + 16u * hf, pl);
                 }
-                mma_bf16(o[nt], a0, a1, a2, a3, b0, b1);
-                mma_bf16(o[nt], e0, e1, e2, e3, b0, b1);
-                mma_bf16(o[nt + 1], a0, a1, a2, a3, b2, b3);
-                mma_bf16(o[nt + 1], e0, e1, e2, e3, b2, b3);
+                tc_wait_st();
+                // V rows past the length in a short tile hold stale pool data: zero them so
+                // that a zero weight cannot meet a NaN
+                bool short_tile = false;
+#pragma unroll
+                for (int u = 0; u < kPfTiles; ++u) {
+                    const int32_t hi = (his >> (5 * u)) & 31;
+                    short_tile = short_tile || (hi > 0 && hi < 16);
+                }
+                if (short_tile) {
+                    uint8_t* vst = base + L.stages + (uint32_t)s * L.stage_bytes + KH * 64u * 128u;
+                    for (int idx = r; idx < kPfTiles * 16 * KH * 8; idx += kTcSoftWarps * 32) {
+                        const int u = idx / (16 * KH * 8), rem = idx - u * (16 * KH * 8);
+                        const int kr = rem / (KH * 8), rem2 = rem - kr * (KH * 8);
+                        const int hh = rem2 >> 3, ch = rem2 & 7;
+                        const int32_t hi = (his >> (5 * u)) & 31;
+                        if (hi > 0 && kr >= hi)
+                            *reinterpret_cast<uint4*>(vst + hh * 64u * 128u + (16 * u + kr) * 128 +
+                                                      ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before();
+                mbar_arrive(p_full(s));
+                ++j;
             }
         }
-        }  // half of the block
-        __syncwarp();
-        if (lane == 0) {
-#pragma unroll
-            for (int u = 0; u < kPfTiles; ++u)
-                mbar_arrive(bars + 8u * (kPfStages + (k + u) % kPfStages));
+        // ---- epilogue: O / l for this row (TMEM loads by the whole warp) --------------------
+        if (ok && nblk > 0) {
+            ok = mbar_wait(pv_done, (nblk - 1) & 1, abort_p, p.dev_err);
+            tc_fence_after();
         }
-      }
-    }
-    // ---- epilogue: row sums across the four lanes of a row, then out = O / l -------------
-#pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
-    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const bool okr = half ? ok1 : ok0;
-        if (!okr) continue;
-        const int32_t pos = half ? pos1 : pos0;
-        const int64_t row = ((int64_t)b * p.Tq + (pos - c0)) * p.Hq + h;
-        const float inv = half ? inv1 : inv0;
+        ok = __all_sync(0xffffffffu, ok);
+        const int64_t row = ((int64_t)b * p.Tq + (rowok ? pos - c0 : 0)) * p.Hq + h;
         float* orow = p.out + row * D;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+            float t[32];
+            if (nblk > 0 && ok) {
+                tc_ld32(tbase + lanes + 32u * cc, t);
+                tc_wait_ld();
+            } else {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-            *reinterpret_cast<float2*>(orow + 8 * nt + 2 * tig) =
-                make_float2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
-        if (tig == 0) {
-            const float m = half ? m1 : m0;
-            if (p.m_out) p.m_out[row] = m == kPfNegInf ? kPfNegInf : m * kLn2;
-            if (p.e_out) p.e_out[row] = half ? l1 : l0;
+                for (int i = 0; i < 32; ++i) t[i] = 0.f;
+            }
+            if (rowok) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 4)
+                    *reinterpret_cast<float4*>(orow + 32 * cc + i) =
+                        make_float4(t[i] * inv, t[i + 1] * inv, t[i + 2] * inv, t[i + 3] * inv);
+            }
         }
+        if (rowok) {
+            // report the true row max and the sum relative to it
+            if (p.m_out) p.m_out[row] = m_true == kPfNegInf ? kPfNegInf : m_true * kLn2;
+            if (p.e_out) p.e_out[row] = m_true == kPfNegInf ? 0.f : l * exp2f(m_used - m_true);
+        }
+    }
+    // ---- teardown: the allocating warp frees the tensor memory --------------------------------
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tc_dealloc(tbase, kTcCols);
     }
 }
 
 std::mutex g_pf_mutex;
-int g_pf_smem_set[2] = {0, 0};
+
+// The pool as rows of d bf16 values split into 128-byte halves (dims {64, rows, d/64}), with
+// a box of one half of 16 rows: the tcgen05 operands keep each half of a key block as 64
+// contiguous 128-byte rows.
+PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+dattn_status_t make_half_tensor_map(void* tmap_out, const void* pool, int64_t rows, int D) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = tc_encode_fn();
+    if (fn == nullptr) return DATTN_ERR_CUDA;
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(D / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
+    cuuint32_t box[3] = {64, 16, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(static_cast<CUtensorMap*>(tmap_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<void*>(pool), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DATTN_OK : DATTN_ERR_CUDA;
+}
+
+int g_tc_smem_set[2] = {0, 0};
 
 template <int D>
-dattn_status_t launch_prefill_d(const PfParams& p, const void* k_pool, const void* v_pool,
-                                int64_t ctas, cudaStream_t stream) {
-    const PfSmem L = pf_smem_layout(D);
+dattn_status_t launch_prefill_tc_d(const PfParams& p0, const void* k_pool, const void* v_pool,
+                                   cudaStream_t stream) {
+    PfParams p = p0;
+    p.nqb = ((p.Tq + kPfBlock - 1) / kPfBlock + 2) / 2;  // 128-row tiles a chunk can touch
+    const int64_t ctas = (int64_t)p.B * p.nqb * p.Hq;
+    if (ctas >= (1ll << 31)) return DATTN_ERR_UNSUPPORTED;
+    const int32_t nwords = (p.max_pages * p.P / kPfBlock + 2 + 31) / 32;
+    const TcSmem L = tc_smem_layout(D, nwords);
+    if (L.total > 227u * 1024u) return DATTN_ERR_UNSUPPORTED;
     {
         std::lock_guard<std::mutex> lock(g_pf_mutex);
-        int& set = g_pf_smem_set[D == 128 ? 1 : 0];
+        int& set = g_tc_smem_set[D == 128 ? 1 : 0];
         if ((int)L.total > set) {
-            if (cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(prefill_tc_kernel<D>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)L.total) != cudaSuccess)
                 return DATTN_ERR_CUDA;
             set = (int)L.total;
@@ -504,10 +687,10 @@ dattn_status_t launch_prefill_d(const PfParams& p, const void* k_pool, const voi
     alignas(64) CUtensorMap tv;
     const int64_t rows = (int64_t)p.num_pages * p.Hkv * p.P;
     dattn_status_t st;
-    if ((st = make_kv_tensor_map(&tk, k_pool, rows, D)) != DATTN_OK) return st;
-    if ((st = make_kv_tensor_map(&tv, v_pool, rows, D)) != DATTN_OK) return st;
-    if (launch_pdl(prefill_kernel<D>, dim3((unsigned)ctas), dim3(kPfThreads), L.total, stream, p,
-                   tk, tv) != cudaSuccess)
+    if ((st = make_half_tensor_map(&tk, k_pool, rows, D)) != DATTN_OK) return st;
+    if ((st = make_half_tensor_map(&tv, v_pool, rows, D)) != DATTN_OK) return st;
+    if (launch_pdl(prefill_tc_kernel<D>, dim3((unsigned)ctas), dim3(kTcThreads), L.total, stream,
+                   p, tk, tv, nwords) != cudaSuccess)
         return DATTN_ERR_CUDA;
     return DATTN_OK;
 }
@@ -588,6 +771,6 @@ extern "C" dattn_status_t dattn_prefill(const dattn_kv_layout* layout, const voi
     const int64_t ctas = (int64_t)B * p.nqb * Hq;
     if (ctas >= (1ll << 31)) return DATTN_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return layout->head_dim == 64 ? launch_prefill_d<64>(p, k_pool, v_pool, ctas, s)
-                                  : launch_prefill_d<128>(p, k_pool, v_pool, ctas, s);
+    return layout->head_dim == 64 ? launch_prefill_tc_d<64>(p, k_pool, v_pool, s)
+                                  : launch_prefill_tc_d<128>(p, k_pool, v_pool, s);
 }
