@@ -466,7 +466,8 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
                 tc_commit(kv_empty(s));
                 tc_commit(pv_done);
             }
-            // nothing of this CTA's may still run on the tensor cores when it exits
+            // every product is done: the epilogue's signal, and nothing of this CTA's may
+            // still run on the tensor cores when it exits
             tc_commit(drain);
             mbar_wait(drain, 0, abort_p, p.dev_err);
         }
@@ -587,8 +588,11 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
             }
         }
         // ---- epilogue: O / l for this row (TMEM loads by the whole warp) --------------------
+        // Wait for the last product on the one-phase drain barrier: pv_done may still be two
+        // phases behind a warp that ran ahead of its siblings (a parity wait cannot tell those
+        // phases apart).
         if (ok && nblk > 0) {
-            ok = mbar_wait(pv_done, (nblk - 1) & 1, abort_p, p.dev_err);
+            ok = mbar_wait(drain, 0, abort_p, p.dev_err);
             tc_fence_after();
         }
         ok = __all_sync(0xffffffffu, ok);
