@@ -157,6 +157,14 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32])
         : "memory");
 }
 
+// 2^x by the special-function unit (ex2.approx.ftz: relative error near 2^-22, subnormal results
+// flushed to +0, 2^-inf = +0)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Shared-memory matrix descriptor of a 128-byte-swizzled operand: start address, leading and
 // stride byte offsets (16-byte units), the descriptor version of this architecture (1 at bit
 // 46) and the 128-byte swizzle mode (2 at bits 61-63).
@@ -509,24 +517,30 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
                     for (int i = 0; i < 32; ++i) x[32 + i] = t[i];
                     tc_wait_ld();
                 }
-                // mask: the row's query block keeps kb, the key is written (< length) and
-                // at or before the query
+                // mask: the row's query block keeps kb, the key is written (< length) and at
+                // or before the query. Key i of tile u is kept iff i < lim[u].
                 const bool keep = rowok && (flags & rbit) != 0u;
-                float mx = kPfNegInf;
+                const int32_t cut = keep ? pos - kb * kPfBlock + 1 : 0;
+                int32_t lim[kPfTiles];
+#pragma unroll
+                for (int u = 0; u < kPfTiles; ++u) lim[u] = min(16 * u + ((his >> (5 * u)) & 31), cut);
+                // row maximum over eight partial maxima (short dependency chains)
+                float mx8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mx8[k] = kPfNegInf;
 #pragma unroll
                 for (int i = 0; i < 64; ++i) {
-                    const int32_t hi = (his >> (5 * (i >> 4))) & 31;
-                    const bool v = keep && (i & 15) < hi && kb * kPfBlock + i <= pos;
-                    x[i] = v ? x[i] * p.sl2 : kPfNegInf;
-                    mx = fmaxf(mx, x[i]);
+                    x[i] = i < lim[i >> 4] ? x[i] * p.sl2 : kPfNegInf;
+                    mx8[i & 7] = fmaxf(mx8[i & 7], x[i]);
                 }
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 m_true = fmaxf(m_true, mx);
                 // lazy rescale of O and l when the row maximum grows by more than 2^8; the TMEM
                 // traffic is warp-collective, so a warp rescales when any of its rows must (the
                 // others with factor 1)
                 const bool need = mx > m_used + kTcRescale || (m_used == kPfNegInf && mx != kPfNegInf);
                 const float f = need && m_used != kPfNegInf ? exp2f(m_used - mx) : 1.f;
-                l *= f;
                 if (__any_sync(0xffffffffu, f != 1.f) && j > 0) {
                     // O holds the blocks before this one: wait for them, then scale it
                     mbar_wait(pv_done, (j - 1) & 1, abort_p, p.dev_err);
@@ -545,21 +559,24 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
                 }
                 if (need) m_used = mx;
                 const float mu = m_used == kPfNegInf ? 0.f : m_used;
-                // P as two bf16 terms: hi into columns [0, 32) of the S buffer, lo into [32, 64)
+                // P as two bf16 terms: hi into columns [0, 32) of the S buffer, lo into [32, 64);
+                // exp2 of a masked key (-inf) is +0. The block's sum runs over four partials.
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     uint32_t ph[16], pl[16];
 #pragma unroll
                     for (int cc = 0; cc < 16; ++cc) {
-                        const float p0 = exp2f(x[32 * hf + 2 * cc] - mu);
-                        const float p1 = exp2f(x[32 * hf + 2 * cc + 1] - mu);
-                        l += p0 + p1;
+                        const float p0 = ex2_approx(x[32 * hf + 2 * cc] - mu);
+                        const float p1 = ex2_approx(x[32 * hf + 2 * cc + 1] - mu);
+                        ls[cc & 3] += p0 + p1;
                         ph[cc] = pack_bf16(p0, p1);
                         pl[cc] = pack_bf16(p0 - bf16_lo(ph[cc]), p1 - bf16_hi(ph[cc]));
                     }
                     tc_st16(sbuf + 16u * hf, ph);
                     tc_st16(sbuf + 32u + 16u * hf, pl);
                 }
+                l = l * f + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
                 tc_wait_st();
                 // V rows past the length in a short tile hold stale pool data: zero them so
                 // that a zero weight cannot meet a NaN
