@@ -74,7 +74,9 @@ constexpr int kTcSoftWarps = 4;      // one thread per row
 constexpr int kTcProdWarp = 4;       // TMA producer
 constexpr int kTcMmaWarp = 5;        // tcgen05.mma issuer
 constexpr int kTcThreads = 6 * 32;
-constexpr int kTcStages = 2;         // key blocks in flight
+constexpr int kTcStages = 2;         // K (and V) stages of the ring
+constexpr int kTcMetaSlots = 4;      // per-block metadata slots (block j in slot j % 4)
+constexpr int kTcBars = 18;          // mbarriers of the pipeline
 constexpr uint32_t kTcCols = 256;    // TMEM: O [0, 128), S0 [128, 192), S1 [192, 256)
 constexpr float kTcRescale = 8.f;    // lazy rescale threshold (log2 units)
 
@@ -204,8 +206,8 @@ __host__ __device__ inline TcSmem tc_smem_layout(int D, int nwords) {
     s.bmA = o;         o += (uint32_t)nwords * 4u;
     s.bmB = o;         o += (uint32_t)nwords * 4u;
     o = (o + 15u) & ~15u;
-    s.bars = o;        o += 10u * 8u;
-    s.meta = o;        o += kTcStages * 16u;
+    s.bars = o;        o += kTcBars * 8u;
+    s.meta = o;        o += kTcMetaSlots * 16u;
     s.taddr = o;       o += 16u;
     s.total = o + 1024u;
     return s;
@@ -276,22 +278,30 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
     const int32_t J = p.nqb - 1 - c % p.nqb;  // 128-row tile; the last ones start first
     const int32_t b = c / p.nqb;
     const uint32_t bars = smem_u32(base + L.bars);
-    auto kv_full = [&](int s) { return bars + 8u * s; };
-    auto kv_empty = [&](int s) { return bars + 8u * (2 + s); };
-    auto s_full = [&](int s) { return bars + 8u * (4 + s); };
-    auto p_full = [&](int s) { return bars + 8u * (6 + s); };
-    const uint32_t pv_done = bars + 64u, drain = bars + 72u;
+    // K and V stages are tracked apart: K_j's stage is free once S_j is computed, V_j's once
+    // P_j V_j is, so the next key blocks' K loads run during this block's softmax.
+    auto k_full = [&](int s) { return bars + 8u * s; };
+    auto k_empty = [&](int s) { return bars + 8u * (2 + s); };
+    auto v_full = [&](int s) { return bars + 8u * (4 + s); };
+    auto v_empty = [&](int s) { return bars + 8u * (6 + s); };
+    auto s_full = [&](int s) { return bars + 8u * (8 + s); };
+    auto p_full = [&](int s) { return bars + 8u * (10 + s); };
+    auto meta_full = [&](int m) { return bars + 8u * (12 + m); };
+    const uint32_t pv_done = bars + 8u * 16u, drain = bars + 8u * 17u;
     int32_t* meta = reinterpret_cast<int32_t*>(base + L.meta);
     uint32_t* bmA = reinterpret_cast<uint32_t*>(base + L.bmA);
     uint32_t* bmB = reinterpret_cast<uint32_t*>(base + L.bmB);
     volatile int* abort_p = &abort_flag;
     if (tid == 0) {
         for (int s = 0; s < kTcStages; ++s) {
-            mbar_init(kv_full(s), 1);
-            mbar_init(kv_empty(s), 1);
+            mbar_init(k_full(s), 1);
+            mbar_init(k_empty(s), 1);
+            mbar_init(v_full(s), 1);
+            mbar_init(v_empty(s), 1);
             mbar_init(s_full(s), 1);
             mbar_init(p_full(s), kTcSoftWarps * 32);
         }
+        for (int m = 0; m < kTcMetaSlots; ++m) mbar_init(meta_full(m), 1);
         mbar_init(pv_done, 1);
         mbar_init(drain, 1);
         *abort_p = 0;
@@ -356,20 +366,39 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
         if (lane < kPfTiles) {
             const uint64_t pol = policy_evict_normal();
             const uint32_t half_bytes = 64u * 128u;  // one half of a K (or V) block
-            int32_t j = 0;
+            const uint32_t st0 = smem_u32(base + L.stages);
+            // V_j is issued after K_{j+1}: the softmax of block j stands between S_j (which
+            // needs K_j) and P_j V_j (which needs V_j)
+            int32_t jk = 0, jv = 0;  // blocks whose K, whose V were issued
+            int32_t vy = 0, vhi = 0, vn = 0;  // the V copy of block jk - 1: tile row, rows, tiles
             bool ok = true;
+            auto issue_v = [&]() -> bool {
+                const int s = jv & 1;
+                bool okv = true;
+                if (jv >= kTcStages && lane == 0)
+                    okv = mbar_wait(v_empty(s), ((jv >> 1) + 1) & 1, abort_p, p.dev_err);
+                okv = __shfl_sync(0xfu, okv ? 1 : 0, 0) != 0;
+                if (!okv) return false;
+                const uint32_t vst = st0 + (uint32_t)s * L.stage_bytes + KH * half_bytes;
+                if (lane == 0) mbar_arrive_expect_tx(v_full(s), (uint32_t)vn * KH * 2048u);
+                __syncwarp(0xfu);
+                if (vhi > 0) {
+#pragma unroll
+                    for (int hh = 0; hh < KH; ++hh)
+                        tma_load_3d(vst + hh * half_bytes + lane * 2048u, &tmap_v, 0, vy, hh,
+                                    v_full(s), pol);
+                }
+                ++jv;
+                return true;
+            };
             for (int32_t w = 0; w < nw && ok; ++w) {
                 uint32_t word = bmA[w] | bmB[w];
                 while (word != 0u && ok) {
                     const int bit = __ffs(word) - 1;
                     word &= word - 1u;
                     const int32_t kb = 32 * w + bit;
-                    const int s = j & 1;
-                    if (j >= kTcStages && lane == 0)
-                        ok = mbar_wait(kv_empty(s), ((j >> 1) - 1) & 1, abort_p, p.dev_err);
-                    ok = __shfl_sync(0xfu, ok ? 1 : 0, 0) != 0;
-                    if (!ok) break;
-                    // lane u resolves tile u of the block
+                    // lane u resolves tile u of the block (before the stage wait, which the
+                    // page-table read overlaps)
                     const int32_t t0 = kb * kPfBlock + 16 * lane;
                     int32_t y = 0, hi = 0;
                     if (t0 < p_hi) {
@@ -390,33 +419,46 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
                         his |= __shfl_xor_sync(0xfu, his, o2);
                         nvalid += __shfl_xor_sync(0xfu, nvalid, o2);
                     }
-                    const uint32_t kst = smem_u32(base + L.stages) + (uint32_t)s * L.stage_bytes;
-                    const uint32_t vst = kst + KH * half_bytes;
+                    const int s = jk & 1;
+                    if (jk >= kTcStages && lane == 0)
+                        ok = mbar_wait(k_empty(s), ((jk >> 1) + 1) & 1, abort_p, p.dev_err);
+                    ok = __shfl_sync(0xfu, ok ? 1 : 0, 0) != 0;
+                    if (!ok) break;
+                    const uint32_t kst = st0 + (uint32_t)s * L.stage_bytes;
                     if (lane == 0) {
-                        const uint32_t flags = ((bmA[w] >> bit) & 1u) | (((bmB[w] >> bit) & 1u) << 1);
-                        meta[4 * s + 0] = kb;
-                        meta[4 * s + 1] = (int32_t)flags;
-                        meta[4 * s + 2] = his;
-                        mbar_arrive_expect_tx(kv_full(s), (uint32_t)nvalid * 2u * KH * 2048u);
+                        // metadata slot jk % 4 is free: block jk - 4's softmax ended before
+                        // S_{jk-2} was issued, and K_jk waited for S_{jk-2}
+                        int32_t* mt = meta + 4 * (jk & (kTcMetaSlots - 1));
+                        mt[0] = kb;
+                        mt[1] = (int32_t)(((bmA[w] >> bit) & 1u) | (((bmB[w] >> bit) & 1u) << 1));
+                        mt[2] = his;
+                        mbar_arrive(meta_full(jk & (kTcMetaSlots - 1)));
+                        mbar_arrive_expect_tx(k_full(s), (uint32_t)nvalid * KH * 2048u);
                     }
                     __syncwarp(0xfu);
                     if (hi > 0) {
 #pragma unroll
-                        for (int hh = 0; hh < KH; ++hh) {
+                        for (int hh = 0; hh < KH; ++hh)
                             tma_load_3d(kst + hh * half_bytes + lane * 2048u, &tmap_k, 0, y, hh,
-                                        kv_full(s), pol);
-                            tma_load_3d(vst + hh * half_bytes + lane * 2048u, &tmap_v, 0, y, hh,
-                                        kv_full(s), pol);
-                        }
+                                        k_full(s), pol);
                     }
-                    ++j;
+                    ++jk;
+                    if (jk > 1) ok = issue_v();
+                    vy = y;
+                    vhi = hi;
+                    vn = nvalid;
                 }
             }
+            if (ok && jk > 0) ok = issue_v();
             // after an abort, wait (bounded in total) for copies still in flight
             if (lane == 0 && *abort_p) {
                 const unsigned long long t0 = global_timer_ns();
-                for (int32_t jj = max(0, j - kTcStages); jj < j; ++jj)
-                    while (!mbar_try_wait(kv_full(jj & 1), (jj >> 1) & 1) &&
+                for (int32_t jj = max(0, jk - kTcStages); jj < jk; ++jj)
+                    while (!mbar_try_wait(k_full(jj & 1), (jj >> 1) & 1) &&
+                           global_timer_ns() - t0 < kWaitLimitNs) {
+                    }
+                for (int32_t jj = max(0, jv - kTcStages); jj < jv; ++jj)
+                    while (!mbar_try_wait(v_full(jj & 1), (jj >> 1) & 1) &&
                            global_timer_ns() - t0 < kWaitLimitNs) {
                     }
             }
@@ -442,9 +484,10 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
                                                  1024u);
                     tc_mma_ss(tbase + 128u + 64u * s, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
                 }
+                tc_commit(k_empty(s));
                 tc_commit(s_full(s));
             };
-            ok = mbar_wait(kv_full(0), 0, abort_p, p.dev_err);
+            ok = mbar_wait(k_full(0), 0, abort_p, p.dev_err);
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
@@ -452,12 +495,13 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
             for (int32_t j = 0; j < nblk && ok; ++j) {
                 const int s = j & 1;
                 if (j + 1 < nblk) {
-                    ok = mbar_wait(kv_full((j + 1) & 1), ((j + 1) >> 1) & 1, abort_p, p.dev_err);
+                    ok = mbar_wait(k_full((j + 1) & 1), ((j + 1) >> 1) & 1, abort_p, p.dev_err);
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(j + 1);
                 }
-                ok = mbar_wait(p_full(s), (j >> 1) & 1, abort_p, p.dev_err);
+                ok = mbar_wait(p_full(s), (j >> 1) & 1, abort_p, p.dev_err) &&
+                     mbar_wait(v_full(s), (j >> 1) & 1, abort_p, p.dev_err);
                 if (!ok) break;
                 tc_fence_after();
                 // O += P_j V_j: P from TMEM (hi terms, then lo terms), V from shared memory
@@ -471,7 +515,7 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
                                   (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
-                tc_commit(kv_empty(s));
+                tc_commit(v_empty(s));
                 tc_commit(pv_done);
             }
             // every product is done: the epilogue's signal, and nothing of this CTA's may
@@ -494,17 +538,18 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
             while (word != 0u) {
                 word &= word - 1u;
                 const int s = j & 1;
-                // the stage's data and metadata (kv_full), then its scores (s_full)
-                ok = mbar_wait(kv_full(s), (j >> 1) & 1, abort_p, p.dev_err) &&
+                // the block's metadata (slot j % 4), then its scores (s_full)
+                const int ms = j & (kTcMetaSlots - 1);
+                ok = mbar_wait(meta_full(ms), (j >> 2) & 1, abort_p, p.dev_err) &&
                      mbar_wait(s_full(s), (j >> 1) & 1, abort_p, p.dev_err);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const int32_t kb = meta[4 * s + 0];
-                const uint32_t flags = (uint32_t)meta[4 * s + 1];
-                const int32_t his = meta[4 * s + 2];
+                const int32_t kb = meta[4 * ms + 0];
+                const uint32_t flags = (uint32_t)meta[4 * ms + 1];
+                const int32_t his = meta[4 * ms + 2];
                 const uint32_t sbuf = tbase + lanes + 128u + 64u * s;
                 float x[64];
                 {
@@ -586,7 +631,8 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
                     const int32_t hi = (his >> (5 * u)) & 31;
                     short_tile = short_tile || (hi > 0 && hi < 16);
                 }
-                if (short_tile) {
+                if (short_tile && mbar_wait(v_full(s), (j >> 1) & 1, abort_p, p.dev_err)) {
+                    // (V_j's stage is refilled only after P_j V_j, which waits for this warp)
                     uint8_t* vst = base + L.stages + (uint32_t)s * L.stage_bytes + KH * 64u * 128u;
                     for (int idx = r; idx < kPfTiles * 16 * KH * 8; idx += kTcSoftWarps * 32) {
                         const int u = idx / (16 * KH * 8), rem = idx - u * (16 * KH * 8);
