@@ -363,105 +363,122 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
 
     if (active && warp == kTcProdWarp) {
         // ---------------------------------------------------------------- TMA producer
-        if (lane < kPfTiles) {
-            const uint64_t pol = policy_evict_normal();
-            const uint32_t half_bytes = 64u * 128u;  // one half of a K (or V) block
-            const uint32_t st0 = smem_u32(base + L.stages);
-            // V_j is issued after K_{j+1}: the softmax of block j stands between S_j (which
-            // needs K_j) and P_j V_j (which needs V_j)
-            int32_t jk = 0, jv = 0;  // blocks whose K, whose V were issued
-            int32_t vy = 0, vhi = 0, vn = 0;  // the V copy of block jk - 1: tile row, rows, tiles
-            bool ok = true;
-            auto issue_v = [&]() -> bool {
-                const int s = jv & 1;
-                bool okv = true;
-                if (jv >= kTcStages && lane == 0)
-                    okv = mbar_wait(v_empty(s), ((jv >> 1) + 1) & 1, abort_p, p.dev_err);
-                okv = __shfl_sync(0xfu, okv ? 1 : 0, 0) != 0;
-                if (!okv) return false;
-                const uint32_t vst = st0 + (uint32_t)s * L.stage_bytes + KH * half_bytes;
-                if (lane == 0) mbar_arrive_expect_tx(v_full(s), (uint32_t)vn * KH * 2048u);
-                __syncwarp(0xfu);
-                if (vhi > 0) {
+        const uint64_t pol = policy_evict_normal();
+        const uint32_t half_bytes = 64u * 128u;  // one half of a K (or V) block
+        const uint32_t st0 = smem_u32(base + L.stages);
+        const int grp = lane >> 2, u = lane & 3;  // lane (grp, u): tile u of the group's block grp
+        // V_j is issued after K_{j+1}: the softmax of block j stands between S_j (which needs
+        // K_j) and P_j V_j (which needs V_j)
+        int32_t jk = 0, jv = 0;           // blocks whose K, whose V were issued
+        int32_t vy = 0, vhi = 0, vn = 0;  // the V copy owed for block jk - 1 (lane u: tile u)
+        bool ok = true;
+        auto issue_v = [&]() -> bool {
+            const int s = jv & 1;
+            bool okv = true;
+            if (jv >= kTcStages && lane == 0)
+                okv = mbar_wait(v_empty(s), ((jv >> 1) + 1) & 1, abort_p, p.dev_err);
+            okv = __shfl_sync(0xffffffffu, okv ? 1 : 0, 0) != 0;
+            if (!okv) return false;
+            const uint32_t vst = st0 + (uint32_t)s * L.stage_bytes + KH * half_bytes;
+            if (lane == 0) mbar_arrive_expect_tx(v_full(s), (uint32_t)vn * KH * 2048u);
+            __syncwarp();
+            if (lane < kPfTiles && vhi > 0) {
+#pragma unroll
+                for (int hh = 0; hh < KH; ++hh)
+                    tma_load_3d(vst + hh * half_bytes + lane * 2048u, &tmap_v, 0, vy, hh, v_full(s),
+                                pol);
+            }
+            ++jv;
+            return true;
+        };
+        int32_t w = 0;
+        uint32_t word = nw > 0 ? (bmA[0] | bmB[0]) : 0u;
+        while (ok) {
+            // the walk's next (up to) eight key blocks, one per group of four lanes
+            int32_t mykb = -1, cnt = 0;
+            uint32_t myflags = 0u;
+            for (int i = 0; i < 8; ++i) {
+                while (word == 0u && ++w < nw) word = bmA[w] | bmB[w];
+                if (word == 0u) break;
+                const int bit = __ffs(word) - 1;
+                word &= word - 1u;
+                if (grp == i) {
+                    mykb = 32 * w + bit;
+                    myflags = ((bmA[w] >> bit) & 1u) | (((bmB[w] >> bit) & 1u) << 1);
+                }
+                ++cnt;
+            }
+            if (cnt == 0) break;
+            // all page-table reads of the group at once: lane (i, u) resolves tile u of block i
+            int32_t y = 0, hi = 0;
+            const int32_t t0 = mykb * kPfBlock + 16 * u;
+            if (mykb >= 0 && t0 < p_hi) {
+                const int32_t lp = t0 / p.P;
+                const int32_t page = __ldg(p.block_table + (int64_t)b * p.max_pages + lp);
+                if (page < 0) {
+                    set_err(p.dev_err, DATTN_DEVERR_UNMAPPED_PAGE);
+                } else if (page >= p.num_pages) {
+                    set_err(p.dev_err, DATTN_DEVERR_PAGE_OOB);
+                } else {
+                    y = (page * p.Hkv + kvh) * p.P + (t0 - lp * p.P);
+                    hi = min(16, Ln - t0);
+                }
+            }
+            int32_t his = hi << (5 * u), nvalid = hi > 0 ? 1 : 0;
+#pragma unroll
+            for (int o2 = 1; o2 < kPfTiles; o2 <<= 1) {
+                his |= __shfl_xor_sync(0xffffffffu, his, o2);
+                nvalid += __shfl_xor_sync(0xffffffffu, nvalid, o2);
+            }
+            for (int i = 0; i < cnt; ++i) {
+                const int s = jk & 1;
+                if (jk >= kTcStages && lane == 0)
+                    ok = mbar_wait(k_empty(s), ((jk >> 1) + 1) & 1, abort_p, p.dev_err);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                const int32_t bkb = __shfl_sync(0xffffffffu, mykb, 4 * i);
+                const uint32_t bfl = __shfl_sync(0xffffffffu, myflags, 4 * i);
+                const int32_t bhis = __shfl_sync(0xffffffffu, his, 4 * i);
+                const int32_t bn = __shfl_sync(0xffffffffu, nvalid, 4 * i);
+                const uint32_t kst = st0 + (uint32_t)s * L.stage_bytes;
+                if (lane == 0) {
+                    // metadata slot jk % 4 is free: block jk - 4's softmax ended before
+                    // S_{jk-2} was issued, and K_jk waited for S_{jk-2}
+                    int32_t* mt = meta + 4 * (jk & (kTcMetaSlots - 1));
+                    mt[0] = bkb;
+                    mt[1] = (int32_t)bfl;
+                    mt[2] = bhis;
+                    mbar_arrive(meta_full(jk & (kTcMetaSlots - 1)));
+                    mbar_arrive_expect_tx(k_full(s), (uint32_t)bn * KH * 2048u);
+                }
+                __syncwarp();
+                if (grp == i && hi > 0) {
 #pragma unroll
                     for (int hh = 0; hh < KH; ++hh)
-                        tma_load_3d(vst + hh * half_bytes + lane * 2048u, &tmap_v, 0, vy, hh,
-                                    v_full(s), pol);
+                        tma_load_3d(kst + hh * half_bytes + u * 2048u, &tmap_k, 0, y, hh,
+                                    k_full(s), pol);
                 }
-                ++jv;
-                return true;
-            };
-            for (int32_t w = 0; w < nw && ok; ++w) {
-                uint32_t word = bmA[w] | bmB[w];
-                while (word != 0u && ok) {
-                    const int bit = __ffs(word) - 1;
-                    word &= word - 1u;
-                    const int32_t kb = 32 * w + bit;
-                    // lane u resolves tile u of the block (before the stage wait, which the
-                    // page-table read overlaps)
-                    const int32_t t0 = kb * kPfBlock + 16 * lane;
-                    int32_t y = 0, hi = 0;
-                    if (t0 < p_hi) {
-                        const int32_t lp = t0 / p.P;
-                        const int32_t page = __ldg(p.block_table + (int64_t)b * p.max_pages + lp);
-                        if (page < 0) {
-                            set_err(p.dev_err, DATTN_DEVERR_UNMAPPED_PAGE);
-                        } else if (page >= p.num_pages) {
-                            set_err(p.dev_err, DATTN_DEVERR_PAGE_OOB);
-                        } else {
-                            y = (page * p.Hkv + kvh) * p.P + (t0 - lp * p.P);
-                            hi = min(16, Ln - t0);
-                        }
-                    }
-                    int32_t his = hi << (5 * lane), nvalid = hi > 0 ? 1 : 0;
-#pragma unroll
-                    for (int o2 = 1; o2 < kPfTiles; o2 <<= 1) {
-                        his |= __shfl_xor_sync(0xfu, his, o2);
-                        nvalid += __shfl_xor_sync(0xfu, nvalid, o2);
-                    }
-                    const int s = jk & 1;
-                    if (jk >= kTcStages && lane == 0)
-                        ok = mbar_wait(k_empty(s), ((jk >> 1) + 1) & 1, abort_p, p.dev_err);
-                    ok = __shfl_sync(0xfu, ok ? 1 : 0, 0) != 0;
-                    if (!ok) break;
-                    const uint32_t kst = st0 + (uint32_t)s * L.stage_bytes;
-                    if (lane == 0) {
-                        // metadata slot jk % 4 is free: block jk - 4's softmax ended before
-                        // S_{jk-2} was issued, and K_jk waited for S_{jk-2}
-                        int32_t* mt = meta + 4 * (jk & (kTcMetaSlots - 1));
-                        mt[0] = kb;
-                        mt[1] = (int32_t)(((bmA[w] >> bit) & 1u) | (((bmB[w] >> bit) & 1u) << 1));
-                        mt[2] = his;
-                        mbar_arrive(meta_full(jk & (kTcMetaSlots - 1)));
-                        mbar_arrive_expect_tx(k_full(s), (uint32_t)nvalid * KH * 2048u);
-                    }
-                    __syncwarp(0xfu);
-                    if (hi > 0) {
-#pragma unroll
-                        for (int hh = 0; hh < KH; ++hh)
-                            tma_load_3d(kst + hh * half_bytes + lane * 2048u, &tmap_k, 0, y, hh,
-                                        k_full(s), pol);
-                    }
-                    ++jk;
-                    if (jk > 1) ok = issue_v();
-                    vy = y;
-                    vhi = hi;
-                    vn = nvalid;
+                ++jk;
+                if (jk > 1) ok = issue_v();
+                // block i's V copy is owed next (lane u takes tile u's row and length)
+                vy = __shfl_sync(0xffffffffu, y, 4 * i + u);
+                vhi = __shfl_sync(0xffffffffu, hi, 4 * i + u);
+                vn = bn;
+                if (!ok) break;
+            }
+        }
+        if (ok && jk > 0) ok = issue_v();
+        // after an abort, wait (bounded in total) for copies still in flight
+        if (lane == 0 && *abort_p) {
+            const unsigned long long t0w = global_timer_ns();
+            for (int32_t jj = max(0, jk - kTcStages); jj < jk; ++jj)
+                while (!mbar_try_wait(k_full(jj & 1), (jj >> 1) & 1) &&
+                       global_timer_ns() - t0w < kWaitLimitNs) {
                 }
-            }
-            if (ok && jk > 0) ok = issue_v();
-            // after an abort, wait (bounded in total) for copies still in flight
-            if (lane == 0 && *abort_p) {
-                const unsigned long long t0 = global_timer_ns();
-                for (int32_t jj = max(0, jk - kTcStages); jj < jk; ++jj)
-                    while (!mbar_try_wait(k_full(jj & 1), (jj >> 1) & 1) &&
-                           global_timer_ns() - t0 < kWaitLimitNs) {
-                    }
-                for (int32_t jj = max(0, jv - kTcStages); jj < jv; ++jj)
-                    while (!mbar_try_wait(v_full(jj & 1), (jj >> 1) & 1) &&
-                           global_timer_ns() - t0 < kWaitLimitNs) {
-                    }
-            }
+            for (int32_t jj = max(0, jv - kTcStages); jj < jv; ++jj)
+                while (!mbar_try_wait(v_full(jj & 1), (jj >> 1) & 1) &&
+                       global_timer_ns() - t0w < kWaitLimitNs) {
+                }
         }
     } else if (active && warp == kTcMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
