@@ -71,9 +71,10 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
 
 constexpr int kTcRows = 128;         // query rows per CTA (M of both products)
 constexpr int kTcSoftWarps = 4;      // one thread per row
-constexpr int kTcProdWarp = 4;       // TMA producer
+constexpr int kTcProdWarp = 4;       // TMA producer of K (and the block metadata)
 constexpr int kTcMmaWarp = 5;        // tcgen05.mma issuer
-constexpr int kTcThreads = 6 * 32;
+constexpr int kTcVWarp = 6;          // TMA producer of V
+constexpr int kTcThreads = 7 * 32;
 constexpr int kTcStages = 2;         // K (and V) stages of the ring
 constexpr int kTcMetaSlots = 4;      // per-block metadata slots (block j in slot j % 4)
 constexpr int kTcBars = 18;          // mbarriers of the pipeline
@@ -259,7 +260,7 @@ __device__ __forceinline__ void tc_build_bitmaps(const PfParams& p, int32_t b, i
 }
 
 template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 2)
 prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, int32_t nwords) {
     constexpr int KH = D / 64;  // 128-byte halves of a row
@@ -361,66 +362,65 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
     int32_t nblk = 0;
     for (int32_t w = 0; w < nw; ++w) nblk += __popc(bmA[w] | bmB[w]);
 
-    if (active && warp == kTcProdWarp) {
-        // ---------------------------------------------------------------- TMA producer
+    if (active && (warp == kTcProdWarp || warp == kTcVWarp)) {
+        // ------------------------------------------------------ TMA producers (K, and V)
+        // Both warps walk the key blocks in the same order; the K warp's ring is released by
+        // S_j, the V warp's by P_j V_j, so the V copies trail the K copies by about a block.
+        const bool isv = warp == kTcVWarp;
+        const CUtensorMap* tmap = isv ? &tmap_v : &tmap_k;
         const uint64_t pol = policy_evict_normal();
         const uint32_t half_bytes = 64u * 128u;  // one half of a K (or V) block
-        const uint32_t st0 = smem_u32(base + L.stages);
+        const uint32_t st0 = smem_u32(base + L.stages) + (isv ? KH * half_bytes : 0u);
         const int grp = lane >> 2, u = lane & 3;  // lane (grp, u): tile u of the group's block grp
-        // V_j is issued after K_{j+1}: the softmax of block j stands between S_j (which needs
-        // K_j) and P_j V_j (which needs V_j)
-        int32_t jk = 0, jv = 0;           // blocks whose K, whose V were issued
-        int32_t vy = 0, vhi = 0, vn = 0;  // the V copy owed for block jk - 1 (lane u: tile u)
+        int32_t jk = 0;  // blocks issued
         bool ok = true;
-        auto issue_v = [&]() -> bool {
-            const int s = jv & 1;
-            bool okv = true;
-            if (jv >= kTcStages && lane == 0)
-                okv = mbar_wait(v_empty(s), ((jv >> 1) + 1) & 1, abort_p, p.dev_err);
-            okv = __shfl_sync(0xffffffffu, okv ? 1 : 0, 0) != 0;
-            if (!okv) return false;
-            const uint32_t vst = st0 + (uint32_t)s * L.stage_bytes + KH * half_bytes;
-            if (lane == 0) mbar_arrive_expect_tx(v_full(s), (uint32_t)vn * KH * 2048u);
-            __syncwarp();
-            if (lane < kPfTiles && vhi > 0) {
-#pragma unroll
-                for (int hh = 0; hh < KH; ++hh)
-                    tma_load_3d(vst + hh * half_bytes + lane * 2048u, &tmap_v, 0, vy, hh, v_full(s),
-                                pol);
-            }
-            ++jv;
-            return true;
-        };
         int32_t w = 0;
         uint32_t word = nw > 0 ? (bmA[0] | bmB[0]) : 0u;
-        while (ok) {
-            // the walk's next (up to) eight key blocks, one per group of four lanes
-            int32_t mykb = -1, cnt = 0;
-            uint32_t myflags = 0u;
+        // the walk's next (up to) eight key blocks, one per group of four lanes; returns their
+        // count and this lane's block (-1 when it has none) and flags
+        auto walk = [&](int32_t& kb_o, uint32_t& fl_o) -> int {
+            int n = 0;
+            kb_o = -1;
+            fl_o = 0u;
             for (int i = 0; i < 8; ++i) {
                 while (word == 0u && ++w < nw) word = bmA[w] | bmB[w];
                 if (word == 0u) break;
                 const int bit = __ffs(word) - 1;
                 word &= word - 1u;
                 if (grp == i) {
-                    mykb = 32 * w + bit;
-                    myflags = ((bmA[w] >> bit) & 1u) | (((bmB[w] >> bit) & 1u) << 1);
+                    kb_o = 32 * w + bit;
+                    fl_o = ((bmA[w] >> bit) & 1u) | (((bmB[w] >> bit) & 1u) << 1);
                 }
-                ++cnt;
+                ++n;
             }
-            if (cnt == 0) break;
-            // all page-table reads of the group at once: lane (i, u) resolves tile u of block i
+            return n;
+        };
+        // the page of this lane's tile (read one group ahead, so its latency hides behind the
+        // current group's copies)
+        auto read_page = [&](int32_t kb) -> int32_t {
+            const int32_t t0 = kb * kPfBlock + 16 * u;
+            return kb >= 0 && t0 < p_hi ? __ldg(p.block_table + (int64_t)b * p.max_pages + t0 / p.P)
+                                        : 0;
+        };
+        int32_t mykb;
+        uint32_t myflags;
+        int cnt = walk(mykb, myflags);
+        int32_t page = read_page(mykb);
+        while (ok && cnt > 0) {
+            int32_t nkb;
+            uint32_t nflags;
+            const int ncnt = walk(nkb, nflags);
+            const int32_t npage = read_page(nkb);
+            // lane (i, u) resolves tile u of block i of this group
             int32_t y = 0, hi = 0;
             const int32_t t0 = mykb * kPfBlock + 16 * u;
             if (mykb >= 0 && t0 < p_hi) {
-                const int32_t lp = t0 / p.P;
-                const int32_t page = __ldg(p.block_table + (int64_t)b * p.max_pages + lp);
                 if (page < 0) {
-                    set_err(p.dev_err, DATTN_DEVERR_UNMAPPED_PAGE);
+                    if (!isv) set_err(p.dev_err, DATTN_DEVERR_UNMAPPED_PAGE);
                 } else if (page >= p.num_pages) {
-                    set_err(p.dev_err, DATTN_DEVERR_PAGE_OOB);
+                    if (!isv) set_err(p.dev_err, DATTN_DEVERR_PAGE_OOB);
                 } else {
-                    y = (page * p.Hkv + kvh) * p.P + (t0 - lp * p.P);
+                    y = (page * p.Hkv + kvh) * p.P + (t0 - (t0 / p.P) * p.P);
                     hi = min(16, Ln - t0);
                 }
             }
@@ -432,51 +432,47 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
             }
             for (int i = 0; i < cnt; ++i) {
                 const int s = jk & 1;
+                const uint32_t full = isv ? v_full(s) : k_full(s);
                 if (jk >= kTcStages && lane == 0)
-                    ok = mbar_wait(k_empty(s), ((jk >> 1) + 1) & 1, abort_p, p.dev_err);
+                    ok = mbar_wait(isv ? v_empty(s) : k_empty(s), ((jk >> 1) + 1) & 1, abort_p,
+                                   p.dev_err);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
-                const int32_t bkb = __shfl_sync(0xffffffffu, mykb, 4 * i);
-                const uint32_t bfl = __shfl_sync(0xffffffffu, myflags, 4 * i);
-                const int32_t bhis = __shfl_sync(0xffffffffu, his, 4 * i);
                 const int32_t bn = __shfl_sync(0xffffffffu, nvalid, 4 * i);
-                const uint32_t kst = st0 + (uint32_t)s * L.stage_bytes;
-                if (lane == 0) {
-                    // metadata slot jk % 4 is free: block jk - 4's softmax ended before
-                    // S_{jk-2} was issued, and K_jk waited for S_{jk-2}
-                    int32_t* mt = meta + 4 * (jk & (kTcMetaSlots - 1));
-                    mt[0] = bkb;
-                    mt[1] = (int32_t)bfl;
-                    mt[2] = bhis;
-                    mbar_arrive(meta_full(jk & (kTcMetaSlots - 1)));
-                    mbar_arrive_expect_tx(k_full(s), (uint32_t)bn * KH * 2048u);
+                if (!isv) {
+                    const int32_t bkb = __shfl_sync(0xffffffffu, mykb, 4 * i);
+                    const uint32_t bfl = __shfl_sync(0xffffffffu, myflags, 4 * i);
+                    const int32_t bhis = __shfl_sync(0xffffffffu, his, 4 * i);
+                    if (lane == 0) {
+                        // metadata slot jk % 4 is free: block jk - 4's softmax ended before
+                        // S_{jk-2} was issued, and K_jk waited for S_{jk-2}
+                        int32_t* mt = meta + 4 * (jk & (kTcMetaSlots - 1));
+                        mt[0] = bkb;
+                        mt[1] = (int32_t)bfl;
+                        mt[2] = bhis;
+                        mbar_arrive(meta_full(jk & (kTcMetaSlots - 1)));
+                    }
                 }
+                if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)bn * KH * 2048u);
                 __syncwarp();
                 if (grp == i && hi > 0) {
+                    const uint32_t dst = st0 + (uint32_t)s * L.stage_bytes + u * 2048u;
 #pragma unroll
                     for (int hh = 0; hh < KH; ++hh)
-                        tma_load_3d(kst + hh * half_bytes + u * 2048u, &tmap_k, 0, y, hh,
-                                    k_full(s), pol);
+                        tma_load_3d(dst + hh * half_bytes, tmap, 0, y, hh, full, pol);
                 }
                 ++jk;
-                if (jk > 1) ok = issue_v();
-                // block i's V copy is owed next (lane u takes tile u's row and length)
-                vy = __shfl_sync(0xffffffffu, y, 4 * i + u);
-                vhi = __shfl_sync(0xffffffffu, hi, 4 * i + u);
-                vn = bn;
-                if (!ok) break;
             }
+            mykb = nkb;
+            myflags = nflags;
+            cnt = ncnt;
+            page = npage;
         }
-        if (ok && jk > 0) ok = issue_v();
         // after an abort, wait (bounded in total) for copies still in flight
         if (lane == 0 && *abort_p) {
             const unsigned long long t0w = global_timer_ns();
             for (int32_t jj = max(0, jk - kTcStages); jj < jk; ++jj)
-                while (!mbar_try_wait(k_full(jj & 1), (jj >> 1) & 1) &&
-                       global_timer_ns() - t0w < kWaitLimitNs) {
-                }
-            for (int32_t jj = max(0, jv - kTcStages); jj < jv; ++jj)
-                while (!mbar_try_wait(v_full(jj & 1), (jj >> 1) & 1) &&
+                while (!mbar_try_wait(isv ? v_full(jj & 1) : k_full(jj & 1), (jj >> 1) & 1) &&
                        global_timer_ns() - t0w < kWaitLimitNs) {
                 }
         }
@@ -540,7 +536,7 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
             tc_commit(drain);
             mbar_wait(drain, 0, abort_p, p.dev_err);
         }
-    } else if (active) {
+    } else if (active && warp < kTcSoftWarps) {
         // ---------------------------------------------------------------- softmax threads
         const int r = tid;  // this thread's query row and TMEM lane
         const int32_t pos = qa * kPfBlock + r;
