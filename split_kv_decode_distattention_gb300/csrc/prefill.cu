@@ -168,6 +168,54 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Packed fp32 pairs (Blackwell's two-wide fp32 FMA and add)
+__device__ __forceinline__ uint64_t pack_f32x2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+// (r0, r1) = (x0, x1) * m + c, m and c packed pairs, each lane rounded once
+__device__ __forceinline__ void fma_f32x2(float x0, float x1, uint64_t m, uint64_t c, float& r0,
+                                          float& r1) {
+    asm("{\n\t.reg .b64 a, d;\n\tmov.b64 a, {%2, %3};\n\tfma.rn.f32x2 d, a, %4, %5;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(x0), "f"(x1), "l"(m), "l"(c));
+}
+// (a0, a1) += (b0, b1)
+__device__ __forceinline__ void add_f32x2(float& a0, float& a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%0, %1};\n\tmov.b64 b, {%2, %3};\n\t"
+        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1));
+}
+// (r0, r1) = (a0, a1) - (b0, b1)
+__device__ __forceinline__ void sub_f32x2(float a0, float a1, float b0, float b1, float& r0,
+                                          float& r1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+// maximum of 64 values over eight independent chains of three-input maxima
+__device__ __forceinline__ float row_max64(const float (&x)[64]) {
+    float m[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m[k] = fmaxf(x[k], x[k + 8]);
+#pragma unroll
+    for (int i = 16; i < 64; i += 16) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m[k] = fmax3(m[k], x[i + k], x[i + k + 8]);
+    }
+    return fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+}
+
 // Shared-memory matrix descriptor of a 128-byte-swizzled operand: start address, leading and
 // stride byte offsets (16-byte units), the descriptor version of this architecture (1 at bit
 // 46) and the 128-byte swizzle mode (2 at bits 61-63).
@@ -344,14 +392,18 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
     const int32_t nw = active ? (qa + 1 + 1 + 31) / 32 : 0;  // words over blocks 0 .. qa + 1
     if (active) {
         tc_build_bitmaps(p, b, kvh, qa, hasB, bmA, bmB, nw, tid);
-        // the query rows, in the K tiles' swizzled layout ([half][row][128 B])
+        // the query rows, in the K tiles' swizzled layout ([half][row][128 B]); with a
+        // negative scale the rows are negated (exact), so that the scores scale by |scale|
+        const uint32_t qneg = p.sl2 < 0.f ? 0x80008000u : 0u;
         for (int idx = tid; idx < kTcRows * (D / 8); idx += kTcThreads) {
             const int r = idx / (D / 8), ch = idx - r * (D / 8);
             const int32_t pos = qa * kPfBlock + r;
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (pos >= p_lo && pos < p_hi)
+            if (pos >= p_lo && pos < p_hi) {
                 v = __ldg(reinterpret_cast<const uint4*>(
                     p.q + (((int64_t)b * p.Tq + (pos - c0)) * p.Hq + h) * D) + ch);
+                v = make_uint4(v.x ^ qneg, v.y ^ qneg, v.z ^ qneg, v.w ^ qneg);
+            }
             *reinterpret_cast<uint4*>(base + L.q + (ch >> 3) * (kTcRows * 128u) +
                                       swz128((uint32_t)r, (uint32_t)(ch & 7))) = v;
         }
@@ -543,6 +595,10 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
         const bool rowok = pos >= p_lo && pos < p_hi;
         const uint32_t rbit = r >= 64 ? 2u : 1u;
         const uint32_t lanes = (uint32_t)(32 * warp) << 16;
+        // |scale| log2(e) (the rows were negated for a negative scale), at least 1e-30 so that
+        // a masked key (-inf) never meets a zero factor; at that floor every score is ~0
+        const float sl2a = fmaxf(fabsf(p.sl2), 1e-30f);
+        constexpr int32_t kFullTiles = 16 | (16 << 5) | (16 << 10) | (16 << 15);
         float m_used = kPfNegInf, m_true = kPfNegInf, l = 0.f;  // l is relative to m_used
         int32_t j = 0;
         bool ok = true;
@@ -576,23 +632,23 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
                     tc_wait_ld();
                 }
                 // mask: the row's query block keeps kb, the key is written (< length) and at
-                // or before the query. Key i of tile u is kept iff i < lim[u].
+                // or before the query. Key i of tile u is kept iff i < lim[u]; a block whose
+                // 64 keys all pass for every row of the warp skips the selects.
                 const bool keep = rowok && (flags & rbit) != 0u;
                 const int32_t cut = keep ? pos - kb * kPfBlock + 1 : 0;
-                int32_t lim[kPfTiles];
+                float mxr;  // the row maximum of the raw scores
+                if (__all_sync(0xffffffffu, cut >= kPfBlock && his == kFullTiles)) {
+                    mxr = row_max64(x);
+                } else {
+                    int32_t lim[kPfTiles];
 #pragma unroll
-                for (int u = 0; u < kPfTiles; ++u) lim[u] = min(16 * u + ((his >> (5 * u)) & 31), cut);
-                // row maximum over eight partial maxima (short dependency chains)
-                float mx8[8];
+                    for (int u = 0; u < kPfTiles; ++u)
+                        lim[u] = min(16 * u + ((his >> (5 * u)) & 31), cut);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mx8[k] = kPfNegInf;
-#pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    x[i] = i < lim[i >> 4] ? x[i] * p.sl2 : kPfNegInf;
-                    mx8[i & 7] = fmaxf(mx8[i & 7], x[i]);
+                    for (int i = 0; i < 64; ++i) x[i] = i < lim[i >> 4] ? x[i] : kPfNegInf;
+                    mxr = row_max64(x);
                 }
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                const float mx = mxr * sl2a;  // scaled (log2 units); -inf stays -inf
                 m_true = fmaxf(m_true, mx);
                 // lazy rescale of O and l when the row maximum grows by more than 2^8; the TMEM
                 // traffic is warp-collective, so a warp rescales when any of its rows must (the
@@ -617,24 +673,32 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
                 }
                 if (need) m_used = mx;
                 const float mu = m_used == kPfNegInf ? 0.f : m_used;
-                // P as two bf16 terms: hi into columns [0, 32) of the S buffer, lo into [32, 64);
-                // exp2 of a masked key (-inf) is +0. The block's sum runs over four partials.
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                // p = 2^(x |scale| log2(e) - mu) in pairs (packed fp32 FMA); a masked key (-inf)
+                // gives +0. P goes to the S buffer as two bf16 terms: hi (p cut to its upper 16
+                // bits) into columns [0, 32), lo (the exact rest, rounded) into [32, 64).
+                const uint64_t s2 = pack_f32x2(sl2a, sl2a), nmu2 = pack_f32x2(-mu, -mu);
+                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     uint32_t ph[16], pl[16];
 #pragma unroll
                     for (int cc = 0; cc < 16; ++cc) {
-                        const float p0 = ex2_approx(x[32 * hf + 2 * cc] - mu);
-                        const float p1 = ex2_approx(x[32 * hf + 2 * cc + 1] - mu);
-                        ls[cc & 3] += p0 + p1;
-                        ph[cc] = pack_bf16(p0, p1);
-                        pl[cc] = pack_bf16(p0 - bf16_lo(ph[cc]), p1 - bf16_hi(ph[cc]));
+                        float p0, p1;
+                        fma_f32x2(x[32 * hf + 2 * cc], x[32 * hf + 2 * cc + 1], s2, nmu2, p0, p1);
+                        p0 = ex2_approx(p0);
+                        p1 = ex2_approx(p1);
+                        add_f32x2(ls[2 * (cc & 3)], ls[2 * (cc & 3) + 1], p0, p1);
+                        const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+                        ph[cc] = __byte_perm(b0, b1, 0x7632);
+                        float r0, r1;
+                        sub_f32x2(p0, p1, __uint_as_float(b0 & 0xffff0000u),
+                                  __uint_as_float(b1 & 0xffff0000u), r0, r1);
+                        pl[cc] = pack_bf16(r0, r1);
                     }
                     tc_st16(sbuf + 16u * hf, ph);
                     tc_st16(sbuf + 32u + 16u * hf, pl);
                 }
-                l = l * f + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+                l = l * f + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
                 tc_wait_st();
                 // V rows past the length in a short tile hold stale pool data: zero them so
                 // that a zero weight cannot meet a NaN
