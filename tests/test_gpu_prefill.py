@@ -148,3 +148,17 @@ def test_prefill_flags_short_lengths_without_fault():
     assert int(cache.dev_err.item()) & dattn.DEVERR["LEN_OOB"]
     assert (out[0] == 0).all()            # request 0 (10 < 50 tokens) is skipped
     assert torch.isfinite(out[1]).all()   # request 1 is computed
+
+
+@pytest.mark.parametrize("scale", [-0.07, 0.0, 0.5])
+def test_prefill_scale_sign_and_zero(scale):
+    """The logit is scale * (q . k) for any real scale: a negative one flips the order of the
+    scores, zero gives the plain average of the visible V rows, a large one a peaked row."""
+    dattn = _lib()
+    from split_kv_decode_distattention_gb300.harness import PagedCache
+    case = W.Case("scale", B=2, Hq=4, Hkv=2, d=128, P=16, lens=[333, 140], seed=21)
+    case.scale = scale
+    cache = PagedCache(case, DEV)
+    q = _queries(case, 140, 9)
+    out, m, e = _run(dattn, cache, q)
+    _check(case, q, 140, out, m, e, what=f"scale {scale}")
