@@ -102,6 +102,8 @@ typedef enum {
 #define DATTN_DEVERR_TIMEOUT 0x8        /* a bounded pipeline wait ran out; output invalid */
 #define DATTN_DEVERR_CHUNK_OOB 0x10     /* chunk_req or a chunk page index out of range */
 #define DATTN_DEVERR_SELECT_OOB 0x20    /* a selected page lies beyond the request length */
+#define DATTN_DEVERR_SMEM_ALIGN 0x40    /* a kernel's shared memory base was not 1024-byte aligned;
+                                           that kernel computed nothing */
 
 /* Head kinds of the block-sparse decode [LV §2.1.2, §3.1.1]. */
 #define DATTN_HEAD_DENSE 0

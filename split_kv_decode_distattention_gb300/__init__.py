@@ -40,7 +40,7 @@ _lock = threading.Lock()
 HEAD_DENSE, HEAD_RETRIEVAL, HEAD_STREAMING = 0, 1, 2
 KV_BF16, KV_FP8_E4M3 = 0, 1
 DEVERR = {"UNMAPPED_PAGE": 0x1, "PAGE_OOB": 0x2, "LEN_OOB": 0x4, "TIMEOUT": 0x8,
-          "CHUNK_OOB": 0x10, "SELECT_OOB": 0x20}
+          "CHUNK_OOB": 0x10, "SELECT_OOB": 0x20, "SMEM_ALIGN": 0x40}
 
 
 class DattnError(RuntimeError):

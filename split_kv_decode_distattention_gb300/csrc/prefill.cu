@@ -75,9 +75,10 @@ constexpr int kTcProdWarp = 4;       // TMA producer of K (and the block metadat
 constexpr int kTcMmaWarp = 5;        // tcgen05.mma issuer
 constexpr int kTcVWarp = 6;          // TMA producer of V
 constexpr int kTcThreads = 7 * 32;
-constexpr int kTcStages = 2;         // K (and V) stages of the ring
+constexpr int kTcKStages = 2;        // K blocks in flight (also the two score buffers)
+constexpr int kTcVStages = 3;        // V blocks in flight
 constexpr int kTcMetaSlots = 4;      // per-block metadata slots (block j in slot j % 4)
-constexpr int kTcBars = 18;          // mbarriers of the pipeline
+constexpr int kTcBars = 20;          // mbarriers of the pipeline
 constexpr uint32_t kTcCols = 256;    // TMEM: O [0, 128), S0 [128, 192), S1 [192, 256)
 constexpr float kTcRescale = 8.f;    // lazy rescale threshold (log2 units)
 
@@ -239,26 +240,30 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16])
         : "memory");
 }
 
-// Shared memory of the tcgen05 prefill (offsets from a 1024-byte aligned base): the query rows
-// [D/64][128 rows][128 B], two stages of a key block's K and V ([D/64][64 rows][128 B] each),
-// the two query blocks' key-block bitmaps, the barriers, the stage metadata and the TMEM base.
+// Shared memory of the tcgen05 prefill (offsets from the dynamic shared base, which the kernel
+// checks to be 1024-byte aligned: no slack is reserved, so that two CTAs with three V stages
+// fit one SM): the query rows [D/64][128 rows][128 B], the K stages and the V stages (a key
+// block's K or V as [D/64][64 rows][128 B]), the two query blocks' key-block bitmaps, the
+// barriers, the block metadata, the TMEM base and the abort flag.
 struct TcSmem {
-    uint32_t q, stage_bytes, stages, bmA, bmB, bars, meta, taddr, total;
+    uint32_t q, blk_bytes, kst, vst, bmA, bmB, bars, meta, taddr, abort, total;
 };
 
 __host__ __device__ inline TcSmem tc_smem_layout(int D, int nwords) {
     TcSmem s;
     uint32_t o = 0;
     s.q = o;           o += (uint32_t)kTcRows * D * 2u;
-    s.stage_bytes = 2u * 64u * D * 2u;
-    s.stages = o;      o += kTcStages * s.stage_bytes;
+    s.blk_bytes = 64u * D * 2u;
+    s.kst = o;         o += kTcKStages * s.blk_bytes;
+    s.vst = o;         o += kTcVStages * s.blk_bytes;
     s.bmA = o;         o += (uint32_t)nwords * 4u;
     s.bmB = o;         o += (uint32_t)nwords * 4u;
     o = (o + 15u) & ~15u;
     s.bars = o;        o += kTcBars * 8u;
     s.meta = o;        o += kTcMetaSlots * 16u;
     s.taddr = o;       o += 16u;
-    s.total = o + 1024u;
+    s.abort = o;       o += 16u;
+    s.total = o;
     return s;
 }
 
@@ -312,15 +317,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, int32_t nwords) {
     constexpr int KH = D / 64;  // 128-byte halves of a row
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ int abort_flag;
-    uint8_t* base;
-    {
-        const uint32_t off = smem_u32(smem_raw);
-        base = smem_raw + (((off + 1023u) & ~1023u) - off);
-    }
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* base = smem_raw;
     const TcSmem L = tc_smem_layout(D, nwords);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the 128-byte swizzle of the TMA copies and the MMA operands needs 1024-byte alignment
+    if ((smem_u32(base) & 1023u) != 0u) {
+        if (tid == 0) set_err(p.dev_err, DATTN_DEVERR_SMEM_ALIGN);
+        return;
+    }
     int32_t c = blockIdx.x;
     const int32_t h = c % p.Hq;
     c /= p.Hq;
@@ -332,23 +337,25 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
     auto k_full = [&](int s) { return bars + 8u * s; };
     auto k_empty = [&](int s) { return bars + 8u * (2 + s); };
     auto v_full = [&](int s) { return bars + 8u * (4 + s); };
-    auto v_empty = [&](int s) { return bars + 8u * (6 + s); };
-    auto s_full = [&](int s) { return bars + 8u * (8 + s); };
-    auto p_full = [&](int s) { return bars + 8u * (10 + s); };
-    auto meta_full = [&](int m) { return bars + 8u * (12 + m); };
-    const uint32_t pv_done = bars + 8u * 16u, drain = bars + 8u * 17u;
+    auto v_empty = [&](int s) { return bars + 8u * (7 + s); };
+    auto s_full = [&](int s) { return bars + 8u * (10 + s); };
+    auto p_full = [&](int s) { return bars + 8u * (12 + s); };
+    auto meta_full = [&](int m) { return bars + 8u * (14 + m); };
+    const uint32_t pv_done = bars + 8u * 18u, drain = bars + 8u * 19u;
     int32_t* meta = reinterpret_cast<int32_t*>(base + L.meta);
     uint32_t* bmA = reinterpret_cast<uint32_t*>(base + L.bmA);
     uint32_t* bmB = reinterpret_cast<uint32_t*>(base + L.bmB);
-    volatile int* abort_p = &abort_flag;
+    volatile int* abort_p = reinterpret_cast<volatile int*>(base + L.abort);
     if (tid == 0) {
-        for (int s = 0; s < kTcStages; ++s) {
+        for (int s = 0; s < kTcKStages; ++s) {
             mbar_init(k_full(s), 1);
             mbar_init(k_empty(s), 1);
-            mbar_init(v_full(s), 1);
-            mbar_init(v_empty(s), 1);
             mbar_init(s_full(s), 1);
             mbar_init(p_full(s), kTcSoftWarps * 32);
+        }
+        for (int s = 0; s < kTcVStages; ++s) {
+            mbar_init(v_full(s), 1);
+            mbar_init(v_empty(s), 1);
         }
         for (int m = 0; m < kTcMetaSlots; ++m) mbar_init(meta_full(m), 1);
         mbar_init(pv_done, 1);
@@ -364,9 +371,11 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
         tc_alloc(smem_u32(base + L.taddr), kTcCols);
         tc_relinquish();
     }
-    // stale operand data must be finite: zero the query rows and both stages once
-    for (uint32_t i = tid; i < (L.stages + kTcStages * L.stage_bytes) / 16u; i += kTcThreads)
-        reinterpret_cast<uint4*>(base)[i] = make_uint4(0u, 0u, 0u, 0u);
+    // V rows the MMA reads with weight 0 (tiles that are never loaded) must hold finite data:
+    // zero the V stages once. Stale K needs no care: its scores are always masked, and a block
+    // that skips the mask has every tile freshly loaded.
+    for (uint32_t i = tid; i < kTcVStages * L.blk_bytes / 16u; i += kTcThreads)
+        reinterpret_cast<uint4*>(base + L.vst)[i] = make_uint4(0u, 0u, 0u, 0u);
     tc_fence_before();
     grid_dependency_wait();  // the lengths and the pool may come from the previous kernel
     grid_launch_dependents();
@@ -422,7 +431,8 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
         const CUtensorMap* tmap = isv ? &tmap_v : &tmap_k;
         const uint64_t pol = policy_evict_normal();
         const uint32_t half_bytes = 64u * 128u;  // one half of a K (or V) block
-        const uint32_t st0 = smem_u32(base + L.stages) + (isv ? KH * half_bytes : 0u);
+        const uint32_t st0 = smem_u32(base + (isv ? L.vst : L.kst));
+        const int nst = isv ? kTcVStages : kTcKStages;
         const int grp = lane >> 2, u = lane & 3;  // lane (grp, u): tile u of the group's block grp
         int32_t jk = 0;  // blocks issued
         bool ok = true;
@@ -483,11 +493,10 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
                 nvalid += __shfl_xor_sync(0xffffffffu, nvalid, o2);
             }
             for (int i = 0; i < cnt; ++i) {
-                const int s = jk & 1;
+                const int s = jk % nst, ph = (jk / nst) & 1;  // stage, and its fill's phase
                 const uint32_t full = isv ? v_full(s) : k_full(s);
-                if (jk >= kTcStages && lane == 0)
-                    ok = mbar_wait(isv ? v_empty(s) : k_empty(s), ((jk >> 1) + 1) & 1, abort_p,
-                                   p.dev_err);
+                if (jk >= nst && lane == 0)
+                    ok = mbar_wait(isv ? v_empty(s) : k_empty(s), ph ^ 1, abort_p, p.dev_err);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
                 const int32_t bn = __shfl_sync(0xffffffffu, nvalid, 4 * i);
@@ -508,7 +517,7 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
                 if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)bn * KH * 2048u);
                 __syncwarp();
                 if (grp == i && hi > 0) {
-                    const uint32_t dst = st0 + (uint32_t)s * L.stage_bytes + u * 2048u;
+                    const uint32_t dst = st0 + (uint32_t)s * L.blk_bytes + u * 2048u;
 #pragma unroll
                     for (int hh = 0; hh < KH; ++hh)
                         tma_load_3d(dst + hh * half_bytes, tmap, 0, y, hh, full, pol);
@@ -523,8 +532,8 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
         // after an abort, wait (bounded in total) for copies still in flight
         if (lane == 0 && *abort_p) {
             const unsigned long long t0w = global_timer_ns();
-            for (int32_t jj = max(0, jk - kTcStages); jj < jk; ++jj)
-                while (!mbar_try_wait(isv ? v_full(jj & 1) : k_full(jj & 1), (jj >> 1) & 1) &&
+            for (int32_t jj = max(0, jk - nst); jj < jk; ++jj)
+                while (!mbar_try_wait(isv ? v_full(jj % nst) : k_full(jj % nst), (jj / nst) & 1) &&
                        global_timer_ns() - t0w < kWaitLimitNs) {
                 }
         }
@@ -534,13 +543,13 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
             constexpr uint32_t idesc_s = tc_idesc(kTcRows, 64, 0);
             constexpr uint32_t idesc_o = tc_idesc(kTcRows, D, 1);
             const uint32_t qs = smem_u32(base + L.q);
-            const uint32_t st0 = smem_u32(base + L.stages);
+            const uint32_t kst0 = smem_u32(base + L.kst), vst0 = smem_u32(base + L.vst);
             const uint32_t half_bytes = 64u * 128u;
             bool ok = true;
             // S_j = Q K_j^T into S buffer j % 2 (TMEM columns 128 + 64 (j % 2))
             auto issue_s = [&](int32_t j) {
                 const int s = j & 1;
-                const uint32_t kst = st0 + (uint32_t)s * L.stage_bytes;
+                const uint32_t kst = kst0 + (uint32_t)s * L.blk_bytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t ad =
@@ -565,12 +574,13 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
                     tc_fence_after();
                     issue_s(j + 1);
                 }
+                const int sv = j % kTcVStages;
                 ok = mbar_wait(p_full(s), (j >> 1) & 1, abort_p, p.dev_err) &&
-                     mbar_wait(v_full(s), (j >> 1) & 1, abort_p, p.dev_err);
+                     mbar_wait(v_full(sv), (j / kTcVStages) & 1, abort_p, p.dev_err);
                 if (!ok) break;
                 tc_fence_after();
                 // O += P_j V_j: P from TMEM (hi terms, then lo terms), V from shared memory
-                const uint32_t vst = st0 + (uint32_t)s * L.stage_bytes + KH * half_bytes;
+                const uint32_t vst = vst0 + (uint32_t)sv * L.blk_bytes;
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
 #pragma unroll
@@ -580,7 +590,7 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
                                   (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
-                tc_commit(v_empty(s));
+                tc_commit(v_empty(sv));
                 tc_commit(pv_done);
             }
             // every product is done: the epilogue's signal, and nothing of this CTA's may
@@ -708,9 +718,10 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
                     const int32_t hi = (his >> (5 * u)) & 31;
                     short_tile = short_tile || (hi > 0 && hi < 16);
                 }
-                if (short_tile && mbar_wait(v_full(s), (j >> 1) & 1, abort_p, p.dev_err)) {
+                if (short_tile &&
+                    mbar_wait(v_full(j % kTcVStages), (j / kTcVStages) & 1, abort_p, p.dev_err)) {
                     // (V_j's stage is refilled only after P_j V_j, which waits for this warp)
-                    uint8_t* vst = base + L.stages + (uint32_t)s * L.stage_bytes + KH * 64u * 128u;
+                    uint8_t* vst = base + L.vst + (uint32_t)(j % kTcVStages) * L.blk_bytes;
                     for (int idx = r; idx < kPfTiles * 16 * KH * 8; idx += kTcSoftWarps * 32) {
                         const int u = idx / (16 * KH * 8), rem = idx - u * (16 * KH * 8);
                         const int kr = rem / (KH * 8), rem2 = rem - kr * (KH * 8);
