@@ -1076,7 +1076,7 @@ def prefill_main(args, rank: int, world: int):
         "ms_per_step": round(res["ms"], 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",
         "data": "synthetic (seeded N(0,1) bf16 K/V/Q)", "config": cfg,
-        "roofline": {"bound": "tensor", "kernel": "prefill_kernel (dattn_prefill)",
+        "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel (dattn_prefill)",
                      "achieved": round(ktf, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(ktf / peak, 4),
                      "peak_source": "measured" if "bf16_tflops" in peaks else "fallback",
