@@ -73,6 +73,12 @@ _SIGS = {
     "orc_quantize_rows_fp8": (None, [_P, _I64, _I, _P, _P]),
     "orc_dequantize_rows_fp8": (None, [_P, _P, _I64, _I, _P]),
     "orc_kv_write_fp8": (_I64, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _I64, _I64]),
+    "orc_quantize_row_int4": (None, [_P, _I, _P, _P]),
+    "orc_int4_code": (_I, [_P, _I]),
+    "orc_dequantize_row_int4": (None, [_P, ctypes.c_float, _I, _P]),
+    "orc_quantize_rows_int4": (None, [_P, _I64, _I, _P, _P]),
+    "orc_dequantize_rows_int4": (None, [_P, _P, _I64, _I, _P]),
+    "orc_kv_write_int4": (_I64, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _I64, _I64]),
     "orc_attention_f64": (None, [_P, _P, _P, _I64, _I, _P, _I64, _D, _P, _P, _P]),
     "orc_partial_f64": (None, [_P, _P, _P, _I64, _I, _P, _I64, _D, _P, _P, _P]),
 }
@@ -343,6 +349,60 @@ def kv_write_fp8(k_pool, v_pool, k_scale, v_scale, P: int, block_table_row, num_
     return int(lib.orc_kv_write_fp8(_ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), Hkv,
                                     P, d, _ptr(bt), bt.shape[0], num_pages, _ptr(k_new),
                                     _ptr(v_new), pos0, T))
+
+
+# ----------------------------------------------------------------- 4-bit KV (reading R12)
+
+def quantize_rows_int4(X, lib=None):
+    """Rows of bf16 values ([n][d] or [d], d even) -> (packed uint8 [n][d/2], scales float32
+    [n]): byte i of a row holds code + 8 of channel 2i (low nibble) and 2i + 1 (high)."""
+    lib = lib or load()
+    X = bf16_bits(X)
+    d = X.shape[-1]
+    X2 = np.ascontiguousarray(X.reshape(-1, d))
+    packed = np.zeros((X2.shape[0], d // 2), np.uint8)
+    scales = np.zeros(X2.shape[0], np.float32)
+    lib.orc_quantize_rows_int4(_ptr(X2), X2.shape[0], d, _ptr(packed), _ptr(scales))
+    return packed.reshape(X.shape[:-1] + (d // 2,)), scales.reshape(X.shape[:-1])
+
+
+def int4_codes(packed, lib=None) -> np.ndarray:
+    """The signed codes (-8 .. 7) of packed 4-bit rows ([..][d/2] -> [..][d] int8)."""
+    lib = lib or load()
+    packed = np.ascontiguousarray(packed, np.uint8)
+    h = packed.shape[-1]
+    flat = packed.reshape(-1, h)
+    out = np.zeros((flat.shape[0], 2 * h), np.int8)
+    for r in range(flat.shape[0]):
+        row = np.ascontiguousarray(flat[r])
+        for c in range(2 * h):
+            out[r, c] = lib.orc_int4_code(_ptr(row), c)
+    return out.reshape(packed.shape[:-1] + (2 * h,))
+
+
+def dequantize_rows_int4(packed, scales, lib=None) -> np.ndarray:
+    """code * scale of every packed 4-bit row, in float64 ([..][d/2] -> [..][d])."""
+    lib = lib or load()
+    packed = np.ascontiguousarray(packed, np.uint8)
+    h = packed.shape[-1]
+    p2 = packed.reshape(-1, h)
+    s2 = np.ascontiguousarray(np.asarray(scales, np.float32).reshape(-1))
+    out = np.zeros((p2.shape[0], 2 * h), np.float64)
+    lib.orc_dequantize_rows_int4(_ptr(p2), _ptr(s2), p2.shape[0], 2 * h, _ptr(out))
+    return out.reshape(packed.shape[:-1] + (2 * h,))
+
+
+def kv_write_int4(k_pool, v_pool, k_scale, v_scale, P: int, block_table_row, num_pages: int,
+                  k_new, v_new, pos0: int, lib=None) -> int:
+    """Paged 4-bit write of k_new/v_new ([T][Hkv][d] bf16) into uint8 pools
+    [num_pages][Hkv][P][d/2] and float32 scales [num_pages][Hkv][P]; returns skipped tokens."""
+    lib = lib or load()
+    k_new, v_new = bf16_bits(k_new), bf16_bits(v_new)
+    T, Hkv, d = k_new.shape
+    bt = np.ascontiguousarray(np.asarray(block_table_row, np.int32))
+    return int(lib.orc_kv_write_int4(_ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
+                                     Hkv, P, d, _ptr(bt), bt.shape[0], num_pages, _ptr(k_new),
+                                     _ptr(v_new), pos0, T))
 
 
 def attention_f64(q, K, V, scale: float, rows=None, lib=None):

@@ -48,6 +48,14 @@
  *      K and of V, scale = max|x| / 448, code = E4M3(x / scale) rounded to nearest even;
  *      attention runs over code * scale. Statistics for page selection are still taken
  *      from the bf16 keys as written.
+ *  R12 The 4-bit KV cache: the pages keep streaming heads at 4 bits and give retrieval heads
+ *      2-8 bit configurable quantization, again with no scheme. Here: symmetric integer
+ *      codes with one fp32 scale per (token, KV head) row of K and of V, scale = max|x| / 7
+ *      and code = x / scale rounded to the nearest integer, ties to even, in [-7, 7] (both
+ *      divisions in IEEE fp32). Byte i of a row holds code + 8 of channel 2i in its low
+ *      nibble and of channel 2i + 1 in its high nibble; a row whose scale is 0 has code 0
+ *      (nibble 8) everywhere. Attention runs over code * scale; statistics for page
+ *      selection are still taken from the bf16 keys as written.
  *  R11 Block-sparse prefill [LV §2.1.1, §2.1.2, §2.2.1]: key blocks of 64 tokens. Query token
  *      t of a chunk of Tq new tokens sits at position p = L - Tq + t (L counts the chunk) and
  *      attends the keys i <= p whose block kb = i / 64 its head keeps for the query's block
@@ -536,6 +544,92 @@ int64_t orc_kv_write_fp8(uint8_t *k_pool, uint8_t *v_pool, float *k_scale, float
             const int64_t src = (t * Hkv + h) * (int64_t)d;
             orc_quantize_row_fp8(k_new + src, d, k_pool + row * d, k_scale + row);
             orc_quantize_row_fp8(v_new + src, d, v_pool + row * d, v_scale + row);
+        }
+    }
+    return skipped;
+}
+
+/* ---- 4-bit KV cache (reading R12): symmetric codes with one fp32 scale per row --------- */
+
+/*
+ * One row of d bf16 values (d even) in the 4-bit format: scale = max_c |x_c| / 7 and
+ * code_c = x_c / scale rounded to the nearest integer (ties to even), kept in [-7, 7]; both
+ * divisions in IEEE fp32. Channel c goes to byte c / 2 as the nibble code_c + 8, channel 2i
+ * in the low nibble. A row whose scale is 0 has code 0 everywhere.
+ */
+void orc_quantize_row_int4(const uint16_t *x, int d, uint8_t *packed, float *scale)
+{
+    float mx = 0.0f;
+    for (int c = 0; c < d; ++c) {
+        const float v = fabsf(bf16_to_float(x[c]));
+        if (v > mx) mx = v;
+    }
+    const float s = mx / 7.0f;
+    *scale = s;
+    for (int i = 0; i < d / 2; ++i) {
+        int nib[2];
+        for (int j = 0; j < 2; ++j) {
+            int code = 0;
+            if (s > 0.0f) {
+                const float r = rintf(bf16_to_float(x[2 * i + j]) / s);
+                code = r > 7.0f ? 7 : (r < -7.0f ? -7 : (int)r);
+            }
+            nib[j] = code + 8;
+        }
+        packed[i] = (uint8_t)(nib[0] | (nib[1] << 4));
+    }
+}
+
+/* Value of code c of a packed 4-bit row (the nibble minus 8). */
+int orc_int4_code(const uint8_t *packed, int c)
+{
+    const int byte = packed[c / 2];
+    return ((c & 1) ? (byte >> 4) : (byte & 15)) - 8;
+}
+
+/* code * scale of one packed row, exactly (a small integer times an fp32 value). */
+void orc_dequantize_row_int4(const uint8_t *packed, float scale, int d, double *out)
+{
+    for (int c = 0; c < d; ++c) out[c] = (double)orc_int4_code(packed, c) * (double)scale;
+}
+
+/* The two row functions above over n consecutive rows (d values, d / 2 bytes each). */
+void orc_quantize_rows_int4(const uint16_t *x, int64_t n, int d, uint8_t *packed, float *scales)
+{
+    for (int64_t r = 0; r < n; ++r)
+        orc_quantize_row_int4(x + r * d, d, packed + r * (d / 2), scales + r);
+}
+
+void orc_dequantize_rows_int4(const uint8_t *packed, const float *scales, int64_t n, int d,
+                              double *out)
+{
+    for (int64_t r = 0; r < n; ++r)
+        orc_dequantize_row_int4(packed + r * (d / 2), scales[r], d, out + r * d);
+}
+
+/*
+ * Paged write of T new tokens in the 4-bit format [LS §4.2, with reading R12]: the packed
+ * codes of each (token, KV head) row go to k_pool / v_pool [num_pages][Hkv][P][d / 2] and its
+ * scale to k_scale / v_scale [num_pages][Hkv][P], at the place orc_kv_write uses. Returns
+ * the number of skipped tokens, as orc_kv_write does.
+ */
+int64_t orc_kv_write_int4(uint8_t *k_pool, uint8_t *v_pool, float *k_scale, float *v_scale,
+                          int Hkv, int P, int d, const int32_t *block_table_row, int max_pages,
+                          int num_pages, const uint16_t *k_new, const uint16_t *v_new,
+                          int64_t pos0, int64_t T)
+{
+    int64_t skipped = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t pos = pos0 + t;
+        const int64_t lp = pos / P;
+        if (lp >= max_pages) { ++skipped; continue; }
+        const int32_t page = block_table_row[lp];
+        if (page < 0 || page >= num_pages) { ++skipped; continue; }
+        for (int h = 0; h < Hkv; ++h) {
+            const int64_t row = ((int64_t)page * Hkv + h) * P + pos % P;
+            const int64_t src = (t * Hkv + h) * (int64_t)d;
+            orc_quantize_row_int4(k_new + src, d, k_pool + row * (d / 2), k_scale + row);
+            orc_quantize_row_int4(v_new + src, d, v_pool + row * (d / 2), v_scale + row);
         }
     }
     return skipped;

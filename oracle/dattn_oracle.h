@@ -62,6 +62,18 @@ int64_t orc_kv_write_fp8(uint8_t *k_pool, uint8_t *v_pool, float *k_scale, float
                          int num_pages, const uint16_t *k_new, const uint16_t *v_new,
                          int64_t pos0, int64_t T);
 
+/* 4-bit KV cache (reading R12) */
+void orc_quantize_row_int4(const uint16_t *x, int d, uint8_t *packed, float *scale);
+int orc_int4_code(const uint8_t *packed, int c);
+void orc_dequantize_row_int4(const uint8_t *packed, float scale, int d, double *out);
+void orc_quantize_rows_int4(const uint16_t *x, int64_t n, int d, uint8_t *packed, float *scales);
+void orc_dequantize_rows_int4(const uint8_t *packed, const float *scales, int64_t n, int d,
+                              double *out);
+int64_t orc_kv_write_int4(uint8_t *k_pool, uint8_t *v_pool, float *k_scale, float *v_scale,
+                          int Hkv, int P, int d, const int32_t *block_table_row, int max_pages,
+                          int num_pages, const uint16_t *k_new, const uint16_t *v_new,
+                          int64_t pos0, int64_t T);
+
 void orc_attention_f64(const uint16_t *q, const double *K, const double *V, int64_t row_stride,
                        int d, const int64_t *rows, int64_t n, double scale, double *out,
                        double *m_out, double *e_out);

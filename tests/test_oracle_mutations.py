@@ -3,8 +3,9 @@
 Each case plants one plausible mistake in a copy of the oracle's C source: a dropped term, a
 wrong sign, an off-by-one index, a swapped operand or a reversed tie rule (none of them
 writes outside its buffers). It builds that copy and runs every pin of test_oracle_pins.py,
-test_oracle_fp8.py and test_oracle_prefill.py against it, and at least one pin must fail. The mistakes live only in
-the temporary copy; the oracle itself is untouched.
+test_oracle_fp8.py, test_oracle_int4.py and test_oracle_prefill.py against it, and at least
+one pin must fail. The mistakes live only in the temporary copy; the oracle itself is
+untouched.
 """
 import inspect
 import os
@@ -15,6 +16,7 @@ import pytest
 
 import oracle
 import test_oracle_fp8 as pins_fp8
+import test_oracle_int4 as pins_int4
 import test_oracle_pins as pins
 import test_oracle_prefill as pins_prefill
 
@@ -65,6 +67,22 @@ MUTATIONS = [
     ("8-bit write stores the V scale in the K scale pool",
      "            orc_quantize_row_fp8(v_new + src, d, v_pool + row * d, v_scale + row);",
      "            orc_quantize_row_fp8(v_new + src, d, v_pool + row * d, k_scale + row);"),
+    ("4-bit scale over 8 instead of 7", "    const float s = mx / 7.0f;",
+     "    const float s = mx / 8.0f;"),
+    ("4-bit nibbles in the wrong order", "        packed[i] = (uint8_t)(nib[0] | (nib[1] << 4));",
+     "        packed[i] = (uint8_t)(nib[1] | (nib[0] << 4));"),
+    ("4-bit codes truncated instead of rounded",
+     "                const float r = rintf(bf16_to_float(x[2 * i + j]) / s);",
+     "                const float r = truncf(bf16_to_float(x[2 * i + j]) / s);"),
+    ("4-bit codes rounded half away from zero",
+     "                const float r = rintf(bf16_to_float(x[2 * i + j]) / s);",
+     "                const float r = roundf(bf16_to_float(x[2 * i + j]) / s);"),
+    ("4-bit decode with the wrong offset",
+     "    return ((c & 1) ? (byte >> 4) : (byte & 15)) - 8;",
+     "    return ((c & 1) ? (byte >> 4) : (byte & 15)) - 7;"),
+    ("4-bit write stores the V scale in the K scale pool",
+     "            orc_quantize_row_int4(v_new + src, d, v_pool + row * (d / 2), v_scale + row);",
+     "            orc_quantize_row_int4(v_new + src, d, v_pool + row * (d / 2), k_scale + row);"),
     ("retrieval rows skip the partial last page",
      "            for (int64_t t = p * P; t < (p + 1) * P && t < L; ++t) rows[n++] = t;",
      "            if ((p + 1) * P > L) continue;\n"
@@ -83,6 +101,7 @@ def _pin_calls():
     calls = []
     fns = inspect.getmembers(pins, inspect.isfunction) + \
         inspect.getmembers(pins_fp8, inspect.isfunction) + \
+        inspect.getmembers(pins_int4, inspect.isfunction) + \
         inspect.getmembers(pins_prefill, inspect.isfunction)
     for name, fn in fns:
         if not name.startswith("test_"):
