@@ -11,10 +11,12 @@ roofline are reported beside it. L2 is flushed before every timed step whose K/V
 four times the L2; larger steps evict it themselves and run back to back.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl dattn|reference]
-                  [--kv-format bf16|fp8] [--queries T]
+                  [--kv-format bf16|fp8|int4] [--queries T]
 
 --kv-format fp8 runs the same workload over the 8-bit pool (FP8 E4M3 codes with one fp32
 scale per (token, KV head) row): a K or V row then moves d + 4 bytes instead of 2 d.
+--kv-format int4 runs it over the 4-bit pool (symmetric 4-bit codes, two per byte, with the
+same scales): d / 2 + 4 bytes per row.
 
 --queries T (dense workloads) makes each step a chunked one: T new tokens per request are
 appended, then dattn_decode_multi attends all T query tokens, causal over the new tokens.
@@ -72,7 +74,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="mha-32k", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--impl", default="dattn", choices=["dattn", "reference"])
-    ap.add_argument("--kv-format", default="bf16", choices=["bf16", "fp8"],
+    ap.add_argument("--kv-format", default="bf16", choices=["bf16", "fp8", "int4"],
                     help="element format of the paged KV pool")
     ap.add_argument("--prefill-dense", action="store_true",
                     help="prefill-32k: every head dense (causal) instead of the LServe mix")
@@ -125,16 +127,25 @@ def make_case(args):
     return case
 
 
-def row_bytes(d: int, fp8: bool) -> int:
-    """Bytes of one K (or V) row of one token and KV head in the pool."""
-    return d + 4 if fp8 else 2 * d
+KV_FORMAT_NOTE = {
+    "bf16": "bf16",
+    "fp8": "fp8_e4m3 codes + one fp32 scale per (token, KV head) row",
+    "int4": "symmetric 4-bit codes (two per byte) + one fp32 scale per (token, KV head) row",
+}
+QUANT_NOTE = {"fp8": " over the dequantized 8-bit rows", "int4": " over the dequantized 4-bit rows"}
 
 
-def step_bytes(case, lens_after, sparse_sel_step: bool, fp8: bool = False, T: int = 1) -> dict:
+def row_bytes(d: int, fmt: str) -> int:
+    """Bytes of one K (or V) row of one token and KV head in the pool (format bf16, fp8 or
+    int4; the quantized formats count their fp32 row scale)."""
+    return {"bf16": 2 * d, "fp8": d + 4, "int4": d // 2 + 4}[fmt]
+
+
+def step_bytes(case, lens_after, sparse_sel_step: bool, fmt: str = "bf16", T: int = 1) -> dict:
     """Algorithmic bytes of one layer-step, given the lengths after the append (T query
     tokens per request: T appended tokens, T queries and outputs, the K/V read once)."""
     B, Hq, Hkv, d, P = case.B, case.Hq, case.Hkv, case.d, case.P
-    rb = row_bytes(d, fp8)
+    rb = row_bytes(d, fmt)
     q_bytes = T * B * Hq * d * 2
     out_bytes = T * (B * Hq * d * 4 + 2 * B * Hq * 4)
     new_kv = T * B * Hkv * (d * 2 + rb) * 2  # read k_new/v_new (bf16), write into the pool
@@ -240,7 +251,7 @@ def kernel_source_hash() -> str:
 
 
 def traffic_key(args) -> str:
-    return (args.config + ("/fp8" if args.kv_format == "fp8" else "") +
+    return (args.config + (f"/{args.kv_format}" if args.kv_format != "bf16" else "") +
             (f"/T{args.queries}" if args.queries > 1 else ""))
 
 
@@ -292,9 +303,10 @@ def run_dattn(args, rank: int, world: int):
     dev = torch.device("cuda", torch.cuda.current_device())
     case = make_case(args)
     sparse = case.head_kind is not None
-    fp8 = args.kv_format == "fp8"
+    fmt = args.kv_format
     cache = PagedCache(case, dev, with_stats=sparse, chunk_tokens=16384,
-                       kv_format=dattn.KV_FP8_E4M3 if fp8 else dattn.KV_BF16)
+                       kv_format={"bf16": dattn.KV_BF16, "fp8": dattn.KV_FP8_E4M3,
+                                  "int4": dattn.KV_INT4}[fmt])
     B, Hq, d = case.B, case.Hq, case.d
     T = args.queries
     ws = cache.workspace(top_k=case.top_k, num_splits=args.num_splits, queries=T)
@@ -324,7 +336,7 @@ def run_dattn(args, rank: int, world: int):
     # previous step left there, so it is timed back to back; smaller steps are preceded by
     # an L2 flush (see L2Flush).
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    sb0 = step_bytes(case, list(cache.lens), sparse, fp8, T)
+    sb0 = step_bytes(case, list(cache.lens), sparse, fmt, T)
     do_flush = sb0["decode"] < 4 * l2 or args.flush
     flush = L2Flush(dev)
     torch.cuda.synchronize()
@@ -412,7 +424,7 @@ def run_dattn(args, rank: int, world: int):
             launches += n1 + n2
         e1.record(stream)
         lens_after = [L + (i + 1) * T for L in lens0]
-        sb = step_bytes(case, lens_after, sparse and s % case.reuse == 0, fp8, T)
+        sb = step_bytes(case, lens_after, sparse and s % case.reuse == 0, fmt, T)
         bytes_total += sb["step"]
         step_ms.append((e0, e1))
         if kev is not None:
@@ -572,7 +584,7 @@ def run_e2e(args, case, cache, ws, spc, sel, flush, dev):
             pairs.append((e0, e1))
         lens_after = [L + (i + 1) * T for L in lens0]
         tot_bytes += step_bytes(case, lens_after, spc is not None and i % case.reuse == 0,
-                                args.kv_format == "fp8", T)["step"]
+                                args.kv_format, T)["step"]
     if flush is None:
         e_all1.record(stream)
     torch.cuda.synchronize()
@@ -587,10 +599,11 @@ def run_e2e(args, case, cache, ws, spc, sel, flush, dev):
 
 # ------------------------------------------------------------------------------ CPU oracle
 
-def oracle_sample(case, device, max_pairs: int, seed_step: int = 0, fp8: bool = False):
+def oracle_sample(case, device, max_pairs: int, seed_step: int = 0, fmt: str = "bf16"):
     """Host copies of a bounded sample of the workload: evenly spaced (request, query head)
-    pairs over their full contexts. Only the KV heads the sample reads are copied. With fp8
-    the rows are the oracle's dequantized 8-bit values (float64), made before any timing."""
+    pairs over their full contexts. Only the KV heads the sample reads are copied. With a
+    quantized format the rows are the oracle's dequantized values (float64), made before
+    any timing."""
     import oracle
     allp = [(b, h) for b in range(case.B) for h in range(case.Hq)]
     stride = max(1, len(allp) // max_pairs)
@@ -612,23 +625,26 @@ def oracle_sample(case, device, max_pairs: int, seed_step: int = 0, fp8: bool = 
                 arrs[h][0][t0:t1] = oracle.bf16_bits(K[:, h])
                 arrs[h][1][t0:t1] = oracle.bf16_bits(V[:, h])
         for h in kvhs:
-            kv[(b, h)] = dequantized(arrs[h]) if fp8 else arrs[h]
+            kv[(b, h)] = dequantized(arrs[h], fmt) if fmt != "bf16" else arrs[h]
     return q, pairs, kv
 
 
-def dequantized(kv):
-    """The oracle's 8-bit round trip of (K, V) rows: float64 code * scale."""
+def dequantized(kv, fmt: str):
+    """The oracle's round trip of (K, V) rows through a quantized format: float64
+    code * scale."""
     import oracle
+    if fmt == "int4":
+        return tuple(oracle.dequantize_rows_int4(*oracle.quantize_rows_int4(x)) for x in kv)
     return tuple(oracle.dequantize_rows_fp8(*oracle.quantize_rows_fp8(x)) for x in kv)
 
 
-def time_oracle(case, q, pairs, kv, nthreads, fp8: bool = False, qs=None):
+def time_oracle(case, q, pairs, kv, nthreads, fmt: str = "bf16", qs=None):
     """Wall time of the oracle's dense attention over the sampled pairs, run on nthreads
     host threads (each call is one plain C routine that releases the GIL). With qs (T query
     arrays) each pair attends T query tokens, token t over the rows 0 .. L - T + t."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
-    attend = oracle.attention_f64 if fp8 else oracle.attention
+    attend = oracle.attention_f64 if fmt != "bf16" else oracle.attention
 
     def one(pair):
         b, h = pair
@@ -640,7 +656,7 @@ def time_oracle(case, q, pairs, kv, nthreads, fp8: bool = False, qs=None):
             for t in range(T):
                 attend(qs[t][b, h], K, V, case.scale,
                        rows=np.arange(max(0, L - T + t + 1), dtype=np.int64))
-        return K.shape[0] * row_bytes(case.d, fp8) * 2
+        return K.shape[0] * row_bytes(case.d, fmt) * 2
 
     t0 = time.perf_counter()
     with ThreadPoolExecutor(max_workers=nthreads) as ex:
@@ -679,13 +695,13 @@ class SparseOracleStep:
     start of each reuse window and attends the selected tokens; a streaming head attends its
     sinks and local window. Bytes are counted as the GPU metric counts them."""
 
-    def __init__(self, case, q, b, ret, strm, kv, nthreads, fp8: bool = False):
+    def __init__(self, case, q, b, ret, strm, kv, nthreads, fmt: str = "bf16"):
         from concurrent.futures import ThreadPoolExecutor
         self.case, self.q, self.b, self.ret, self.strm, self.kv = case, q, b, ret, strm, kv
-        # with fp8 the attention runs over the dequantized 8-bit rows (the selection still
-        # reads the bf16 keys, as the statistics do)
-        self.fp8 = fp8
-        self.att = {h: dequantized(kv[h]) for h in kv} if fp8 else kv
+        # with a quantized format the attention runs over the dequantized rows (the
+        # selection still reads the bf16 keys, as the statistics do)
+        self.fmt = fmt
+        self.att = {h: dequantized(kv[h], fmt) for h in kv} if fmt != "bf16" else kv
         self.used = min(nthreads, len(ret) + len(strm))
         self.ex = ThreadPoolExecutor(max_workers=self.used)
         self.sels = {}
@@ -709,7 +725,7 @@ class SparseOracleStep:
         c, b = self.case, self.b
         L, g = c.lens[b], c.g
 
-        attend = oracle.attention_f64 if self.fp8 else oracle.attention
+        attend = oracle.attention_f64 if self.fmt != "bf16" else oracle.attention
 
         def one(h):
             K, V = self.att[h]
@@ -719,7 +735,7 @@ class SparseOracleStep:
                 rows = np.arange(K.shape[0], dtype=np.int64)
             for j in range(g):
                 attend(self.q[b, h * g + j], K, V, c.scale, rows=rows)
-            return rows.shape[0] * row_bytes(c.d, self.fp8) * 2
+            return rows.shape[0] * row_bytes(c.d, self.fmt) * 2
         t0 = time.perf_counter()
         nbytes = sum(self.ex.map(one, self.ret + self.strm))
         return time.perf_counter() - t0, nbytes
@@ -733,12 +749,12 @@ class SparseOracleStep:
         return secs, nbytes
 
 
-def cpu_baseline_sparse(case, device, fp8: bool = False):
+def cpu_baseline_sparse(case, device, fmt: str = "bf16"):
     import oracle
     oracle.load()
     nthreads = len(os.sched_getaffinity(0))
     q, b, ret, strm, kv = sparse_oracle_sample(case, device)
-    st = SparseOracleStep(case, q, b, ret, strm, kv, nthreads, fp8)
+    st = SparseOracleStep(case, q, b, ret, strm, kv, nthreads, fmt)
     secs, nbytes = st.window()
     windows = 1
     while secs * st.used < 10.0 and windows < 8:
@@ -752,34 +768,34 @@ def cpu_baseline_sparse(case, device, fp8: bool = False):
                       f"window(s) of 1 selection + {case.reuse} steps, {secs:.1f} s wall"}
 
 
-def cpu_baseline(case, device, fp8: bool = False, T: int = 1):
+def cpu_baseline(case, device, fmt: str = "bf16", T: int = 1):
     import oracle
     if case.head_kind is not None:
-        return cpu_baseline_sparse(case, device, fp8)
+        return cpu_baseline_sparse(case, device, fmt)
     oracle.load()
     nthreads = len(os.sched_getaffinity(0))
-    per_pair = max(1, sum(case.lens) // case.B) * case.d * (16 if fp8 else 4)
+    per_pair = max(1, sum(case.lens) // case.B) * case.d * (16 if fmt != "bf16" else 4)
     budget = max(nthreads, min(case.B * case.Hq, int(4e9 // per_pair) // T))
-    q, pairs, kv = oracle_sample(case, device, budget, fp8=fp8)
+    q, pairs, kv = oracle_sample(case, device, budget, fmt=fmt)
     qs = None if T == 1 else [oracle.bf16_bits(case.q(t, device)) for t in range(T)]
     # repeat the sample until about 10 s of CPU work has been timed
-    secs, nbytes, used = time_oracle(case, q, pairs, kv, nthreads, fp8, qs)
+    secs, nbytes, used = time_oracle(case, q, pairs, kv, nthreads, fmt, qs)
     reps = 1
     while secs * used < 10.0 and reps < 64:
-        s2, n2, _ = time_oracle(case, q, pairs, kv, nthreads, fp8, qs)
+        s2, n2, _ = time_oracle(case, q, pairs, kv, nthreads, fmt, qs)
         secs, nbytes, reps = secs + s2, nbytes + n2, reps + 1
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": used,
             "kind": "oracle",
             "sample": f"{len(pairs)} of {case.B * case.Hq} (request, query head) pairs of the "
                       f"{case.name} workload over their full contexts (fp64 dense attention"
-                      f"{' over the dequantized 8-bit rows' if fp8 else ''}"
+                      f"{QUANT_NOTE.get(fmt, '')}"
                       f"{f', {T} causal query tokens each' if T > 1 else ''}), "
                       f"repeated {reps}x: {secs:.1f} s wall on {used} threads"}
 
 
 def run_reference_sparse(args, world, case, device, nthreads):
     q, b, ret, strm, kv = sparse_oracle_sample(case, device)
-    st = SparseOracleStep(case, q, b, ret, strm, kv, nthreads, args.kv_format == "fp8")
+    st = SparseOracleStep(case, q, b, ret, strm, kv, nthreads, args.kv_format)
     st.select()
     for _ in range(min(args.warmup, 1)):
         st.attend()
@@ -840,17 +856,17 @@ def run_reference(args, rank, world):
     if case.head_kind is not None:
         run_reference_sparse(args, world, case, device, nthreads)
         return
-    fp8 = args.kv_format == "fp8"
-    per_pair = max(1, sum(case.lens) // case.B) * case.d * (16 if fp8 else 4)
+    fmt = args.kv_format
+    per_pair = max(1, sum(case.lens) // case.B) * case.d * (16 if fmt != "bf16" else 4)
     budget = max(nthreads, min(case.B * case.Hq, int(1e9 // per_pair)))
-    q, pairs, kv = oracle_sample(case, device, budget, fp8=fp8)
+    q, pairs, kv = oracle_sample(case, device, budget, fmt=fmt)
     T = args.queries
     qs = None if T == 1 else [oracle.bf16_bits(case.q(t, device)) for t in range(T)]
     for _ in range(min(args.warmup, 1)):
-        time_oracle(case, q, pairs[:nthreads], kv, nthreads, fp8, qs)
+        time_oracle(case, q, pairs[:nthreads], kv, nthreads, fmt, qs)
     times, used, nbytes = [], nthreads, 0
     for _ in range(args.steps):
-        secs, nb, used = time_oracle(case, q, pairs, kv, nthreads, fp8, qs)
+        secs, nb, used = time_oracle(case, q, pairs, kv, nthreads, fmt, qs)
         times.append(secs)
         nbytes += nb
     total = sum(times)
@@ -1098,8 +1114,7 @@ def config_obj(case, args):
          "context_tokens": (case.lens[0] if len(set(case.lens)) == 1 else
                             f"{min(case.lens)}-{max(case.lens)} (sum {sum(case.lens)})"),
          "seed": args.seed,
-         "kv_format": ("fp8_e4m3 codes + one fp32 scale per (token, KV head) row"
-                       if args.kv_format == "fp8" else "bf16"),
+         "kv_format": KV_FORMAT_NOTE[args.kv_format],
          "parallelism": "replicas" if args.gpus > 1 else "single GPU",
          "step": ("dattn_kv_append (1 token/request) + dattn_decode" +
                   (" + dattn_page_select every 16 steps (block-sparse)"
@@ -1140,7 +1155,7 @@ def main():
     case = res["case"]
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(case, "cuda", args.kv_format == "fp8", args.queries)
+        cpu = cpu_baseline(case, "cuda", args.kv_format, args.queries)
     if world > 1:
         dist.destroy_process_group()
     if rank != 0:
@@ -1156,10 +1171,12 @@ def main():
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("fp8_e4m3 KV (fp16 tensor-core products, fp32 accumulate)"
-                  if args.kv_format == "fp8" else "bf16"),
+        "dtype": {"bf16": "bf16",
+                  "fp8": "fp8_e4m3 KV (fp16 tensor-core products, fp32 accumulate)",
+                  "int4": "int4 KV (fp16 tensor-core products, fp32 accumulate)"}[args.kv_format],
         "data": "synthetic (seeded N(0,1) bf16 K/V/Q" +
-                ("; K/V quantized to 8 bits by the append)" if args.kv_format == "fp8" else ")"),
+                {"bf16": ")", "fp8": "; K/V quantized to 8 bits by the append)",
+                 "int4": "; K/V quantized to 4 bits by the append)"}[args.kv_format],
         "us_per_layer_step": round(ms_step * 1e3, 2),
         "frac_of_8tbs": round(value / ROOFLINE_8TBS, 4),
         "config": dict(config_obj(case, args), l2=res["l2_policy"]),

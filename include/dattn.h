@@ -1,6 +1,7 @@
 /*
- * dattn: split-KV decode attention over a paged KV cache (bf16, or 8-bit FP8 E4M3 codes with
- * one fp32 scale per row), for GB300 (sm_103a).
+ * dattn: split-KV decode attention over a paged KV cache (bf16, 8-bit FP8 E4M3 codes or
+ * 4-bit integer codes, the quantized formats with one fp32 scale per row), for GB300
+ * (sm_103a).
  *
  * The C ABI of libdattn.so. Every entry point takes plain pointers and sizes: no C++ and
  * no framework types. It validates its arguments on the host, then launches asynchronously
@@ -31,7 +32,8 @@
  *       and the top-K pages are selected. §3.1.1: streaming heads attend sink tokens plus
  *       a local window. The streaming and retrieval heads run in one fused kernel.
  *       §3.2.1: the retrieval-head cache is paged and quantized at a configurable 2-8 bits,
- *       with no scheme given; the 8-bit format below is this library's reading of it.
+ *       the streaming-head cache at 4 bits, with no scheme given; the 8-bit and 4-bit
+ *       formats below are this library's reading of it.
  *
  * Here the "instances" are CTAs on one GPU. The KV of every (request, KV head) is split
  * into 16-token tiles. The tiles are spread evenly over num_splits CTAs, so each CTA
@@ -48,7 +50,8 @@
  *  - Sequence length L_b = seq_lens[b]: tokens 0..L_b-1 of request b are valid. Token t
  *    lives in physical page block_table[b * max_pages_per_req + t / P], slot t % P.
  *  - Pool layout: k_pool and v_pool are [num_pages][Hkv][P][d] elements of the layout's
- *    kv_format. Every (page, KV head) tile is one contiguous P*d run.
+ *    kv_format (the 4-bit format packs two elements per byte: [num_pages][Hkv][P][d/2]
+ *    bytes). Every (page, KV head) tile is one contiguous run.
  *  - The 8-bit format (kv_format = DATTN_KV_FP8_E4M3): every (token, KV head) row x of d
  *    values is stored as d one-byte codes plus one fp32 scale. The scales of the 16 tokens
  *    of logical page lp of (page, KV head) form one 128-byte run of kv_scale
@@ -59,6 +62,14 @@
  *    rounded to nearest even and saturated to +-448. A row with scale 0 has +0 codes. The
  *    row's values are code_i * scale, and the attention runs over exactly these values.
  *    The query stays bf16; the statistics are still taken from the bf16 keys.
+ *  - The 4-bit format (kv_format = DATTN_KV_INT4) [LV §3.2.1: streaming heads at 4 bits,
+ *    retrieval heads at 2-8 configurable bits; the page names no scheme]: every (token, KV
+ *    head) row x of d values is stored as d/2 bytes plus one fp32 scale in kv_scale, laid
+ *    out as for the 8-bit format. scale = max_i |x_i| / 7 and code_i = x_i / scale rounded
+ *    to the nearest integer, ties to even, in [-7, 7] (both divisions in IEEE fp32). Byte j
+ *    of the row holds code_{2j} + 8 in its low nibble and code_{2j+1} + 8 in its high
+ *    nibble. A row with scale 0 has code 0. The row's values are code_i * scale, and the
+ *    attention runs over exactly these values.
  *  - Statistics layout: stats is [num_pages][Hkv][P/16][2][d]. Entry [..][lp][0][:] is
  *    k_max and [..][lp][1][:] is k_min of logical page lp, the 16 tokens
  *    lp*16..lp*16+15 of that physical page.
@@ -113,6 +124,7 @@ typedef enum {
 /* Element formats of the KV pool (dattn_kv_layout.kv_format). */
 #define DATTN_KV_BF16 0      /* bf16 values */
 #define DATTN_KV_FP8_E4M3 1  /* FP8 E4M3 codes with one fp32 scale per (token, KV head) row */
+#define DATTN_KV_INT4 2      /* symmetric 4-bit codes, two per byte, one fp32 scale per row */
 
 /* Shape of the paged KV pool and the block table. A zero-initialised tail (kv_format 0,
  * NULL scales) is the bf16 pool. */
@@ -123,10 +135,10 @@ typedef struct dattn_kv_layout {
     int32_t page_size;          /* P: tokens per physical page, a multiple of 16 */
     const int32_t *block_table; /* (device) [B][max_pages_per_req]; -1 = unmapped */
     int32_t max_pages_per_req;  /* row width of block_table */
-    int32_t kv_format;          /* DATTN_KV_BF16 or DATTN_KV_FP8_E4M3 */
+    int32_t kv_format;          /* DATTN_KV_BF16, DATTN_KV_FP8_E4M3 or DATTN_KV_INT4 */
     float *kv_scale;            /* (device) fp32 [num_pages][Hkv][P/16][2][16], 16-byte aligned:
-                                   the 8-bit format's row scales (ignored for bf16), written by
-                                   dattn_kv_append; see the layout note above */
+                                   the row scales of the 8-bit and 4-bit formats (ignored for
+                                   bf16), written by dattn_kv_append; see the layout notes */
 } dattn_kv_layout;
 
 /* Block-sparse decode settings [LV §2.2.2, §3.1.1, §3.1.2]. */
@@ -145,8 +157,9 @@ typedef struct dattn_sparse {
  * token's KV locally]. If stats is not NULL, also update the logical-page statistics
  * [LV §3.1.2: computed at KV-write time].
  *
- *   k_pool, v_pool (device) the pool in the layout's kv_format; for the 8-bit format each
- *                row is quantized as described above and its scales go to layout->kv_scale.
+ *   k_pool, v_pool (device) the pool in the layout's kv_format; for the 8-bit and 4-bit
+ *                formats each row is quantized as described above and its scales go to
+ *                layout->kv_scale.
  *   k_new, v_new (device) bf16 [B][T][Hkv][d]. Token t of request b is written at
  *                position seq_lens[b] + t.
  *   stats        (device, nullable) bf16 [num_pages][Hkv][P/16][2][d]. When a token
@@ -314,7 +327,8 @@ typedef struct dattn_prefill_sparse {
  * One CTA computes one 64-token query block of one query head over all its key blocks, so
  * no workspace is needed.
  *
- *   k_pool, v_pool (device) the pool, bf16 only (DATTN_ERR_UNSUPPORTED for the 8-bit format)
+ *   k_pool, v_pool (device) the pool, bf16 only (DATTN_ERR_UNSUPPORTED for the quantized
+ *            formats)
  *   q        (device) bf16 [B][Tq][Hq][d];  seq_lens (device) int32 [B]
  *   out      (device) fp32 [B][Tq][Hq][d]
  *   m, e     (device, nullable) fp32 [B][Tq][Hq]: the row max (natural-log units) and sum,

@@ -30,6 +30,7 @@ __all__ = [
     "dattn_workspace_size", "dattn_workspace_init", "dattn_auto_splits", "dattn_split_range",
     "dattn_split_owner", "dattn_status_string", "dattn_version", "Workspace",
     "HEAD_DENSE", "HEAD_RETRIEVAL", "HEAD_STREAMING", "DEVERR", "KV_BF16", "KV_FP8_E4M3",
+    "KV_INT4",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -38,7 +39,7 @@ _lib = None
 _lock = threading.Lock()
 
 HEAD_DENSE, HEAD_RETRIEVAL, HEAD_STREAMING = 0, 1, 2
-KV_BF16, KV_FP8_E4M3 = 0, 1
+KV_BF16, KV_FP8_E4M3, KV_INT4 = 0, 1, 2
 DEVERR = {"UNMAPPED_PAGE": 0x1, "PAGE_OOB": 0x2, "LEN_OOB": 0x4, "TIMEOUT": 0x8,
           "CHUNK_OOB": 0x10, "SELECT_OOB": 0x20, "SMEM_ALIGN": 0x40}
 
@@ -161,8 +162,9 @@ def _f32(t, name):
 
 
 def _pool(layout, t, name):
-    """A K or V pool must hold the layout's element type: bf16, or uint8 E4M3 codes."""
-    want = torch.uint8 if layout.kv_format == KV_FP8_E4M3 else torch.bfloat16
+    """A K or V pool must hold the layout's element type: bf16, uint8 E4M3 codes, or uint8
+    bytes of two 4-bit codes."""
+    want = torch.uint8 if layout.kv_format in (KV_FP8_E4M3, KV_INT4) else torch.bfloat16
     if t is not None and t.dtype != want and not (
             want == torch.uint8 and t.dtype == getattr(torch, "float8_e4m3fn", None)):
         raise TypeError(f"{name} must be {want} for this layout")
@@ -174,16 +176,18 @@ class KVLayout:
 
     kv_format KV_BF16: the pools hold bf16 values. KV_FP8_E4M3: they hold uint8 E4M3 codes,
     and kv_scale (float32 [num_pages][Hkv][P/16][2][16]) holds one scale per row: for the 16
-    tokens of each logical page, their K scales, then their V scales.
+    tokens of each logical page, their K scales, then their V scales. KV_INT4: they hold
+    [num_pages][Hkv][P][d/2] bytes of two 4-bit codes each (code + 8, even channel in the low
+    nibble), with kv_scale as for KV_FP8_E4M3.
     """
 
     def __init__(self, num_pages: int, num_kv_heads: int, head_dim: int, page_size: int,
                  block_table: torch.Tensor, kv_format: int = KV_BF16,
                  kv_scale: torch.Tensor | None = None):
         _i32(block_table, "block_table")
-        if kv_format == KV_FP8_E4M3:
+        if kv_format in (KV_FP8_E4M3, KV_INT4):
             if kv_scale is None:
-                raise ValueError("the 8-bit format needs kv_scale")
+                raise ValueError("the quantized formats need kv_scale")
             _f32(kv_scale, "kv_scale")
         self.block_table = block_table  # keeps the tensors alive
         self.kv_scale = kv_scale

@@ -47,9 +47,10 @@ dattn_status_t check_layout(const dattn_kv_layout* L) {
     if ((int64_t)L->num_pages * L->num_kv_heads * L->page_size >= (1ll << 31))
         return DATTN_ERR_UNSUPPORTED;
     if ((int64_t)L->max_pages_per_req * L->page_size >= (1ll << 30)) return DATTN_ERR_UNSUPPORTED;
-    if (L->kv_format != DATTN_KV_BF16 && L->kv_format != DATTN_KV_FP8_E4M3)
+    if (L->kv_format != DATTN_KV_BF16 && L->kv_format != DATTN_KV_FP8_E4M3 &&
+        L->kv_format != DATTN_KV_INT4)
         return DATTN_ERR_INVALID_ARG;
-    if (L->kv_format == DATTN_KV_FP8_E4M3 && (!L->kv_scale || !aligned16(L->kv_scale)))
+    if (L->kv_format != DATTN_KV_BF16 && (!L->kv_scale || !aligned16(L->kv_scale)))
         return DATTN_ERR_INVALID_ARG;
     return DATTN_OK;
 }
@@ -99,20 +100,25 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D map over a pool of 8-bit codes seen as rows of d bytes: one box {d, 16} is a 16-token
-// row group of one (page, KV head), landing as [row][d bytes] with the 128-byte (d = 128)
-// or 64-byte (d = 64) swizzle, which keeps ldmatrix conflict-free.
-dattn_status_t make_kv_tensor_map_u8(void* tmap_out, const void* pool, int64_t rows, int D) {
+// 2-D map over a pool of codes seen as rows of row_bytes bytes (8-bit: d; packed 4-bit:
+// d / 2): one box {row_bytes, 16} is a 16-token row group of one (page, KV head), landing as
+// [row][row_bytes] with the swizzle of the row's size (128, 64 or 32 bytes), which keeps
+// ldmatrix conflict-free.
+dattn_status_t make_kv_tensor_map_u8(void* tmap_out, const void* pool, int64_t rows,
+                                     int row_bytes) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (fn == nullptr) return DATTN_ERR_CUDA;
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D};
-    cuuint32_t box[2] = {(cuuint32_t)D, 16};
+    if (row_bytes != 128 && row_bytes != 64 && row_bytes != 32) return DATTN_ERR_UNSUPPORTED;
+    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)row_bytes, 16};
     cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle swz = row_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                     : CU_TENSOR_MAP_SWIZZLE_32B;
     CUresult r = fn(static_cast<CUtensorMap*>(tmap_out), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
                     const_cast<void*>(pool), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? DATTN_OK : DATTN_ERR_CUDA;
 }
@@ -262,7 +268,7 @@ dattn_status_t dattn_partial(const dattn_kv_layout* layout, const void* k_pool,
     p.nseg = C * p.Hkv;
     p.nitems = C;
     p.dev_err = dev_err;
-    p.f8 = layout->kv_format == DATTN_KV_FP8_E4M3 ? 1 : 0;
+    p.fmt = layout->kv_format;
     p.kv_scale = layout->kv_scale;
     return launch_attention(p, k_pool, v_pool, layout->head_dim, num_splits, ws, ws_bytes,
                             static_cast<cudaStream_t>(stream), bound);
@@ -344,7 +350,7 @@ dattn_status_t decode_impl(const dattn_kv_layout* layout, const void* k_pool, co
     p.nseg = B * p.Hkv;
     p.nitems = B;
     p.dev_err = dev_err;
-    p.f8 = layout->kv_format == DATTN_KV_FP8_E4M3 ? 1 : 0;
+    p.fmt = layout->kv_format;
     p.kv_scale = layout->kv_scale;
     return launch_attention(p, k_pool, v_pool, layout->head_dim, num_splits, ws, ws_bytes,
                             static_cast<cudaStream_t>(stream), bound);

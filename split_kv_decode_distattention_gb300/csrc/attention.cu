@@ -71,11 +71,6 @@ struct Smem {
     }
 };
 
-// Byte offset of 16-byte chunk `chunk` of row `row` in an 8-bit tile of d-byte rows.
-template <int D>
-__device__ __forceinline__ uint32_t swz_u8(uint32_t row, uint32_t chunk) {
-    return D == 128 ? swz128(row, chunk) : swz64(row, chunk);
-}
 
 __device__ __forceinline__ int32_t ceil16(int32_t x) { return (x + 15) >> 4; }
 
@@ -289,9 +284,12 @@ __device__ __forceinline__ void write_final(const AttnParams& p, int32_t s, int3
 // when a tile brings a larger one). So 0 <= w_i <= 2^15 always fits fp16, and w_i is
 // split into two fp16 terms (22 significant bits) as the bf16 path splits p_i. The
 // accumulator is multiplied by r * 2^-15 when the piece is published.
-template <int D, bool F8>
+template <int D, int FMT>
 struct Consumer {
     static constexpr int KS = D / 16;  // k-steps of QK^T and m-tiles of PV
+    static constexpr bool Q = FMT != DATTN_KV_BF16;  // a quantized pool with row scales
+    static constexpr bool I4 = FMT == DATTN_KV_INT4;
+    static_assert(!I4 || Q, "the 4-bit pool is a quantized pool");
 
     const AttnParams& p;
     const Smem& sm;
@@ -336,7 +334,7 @@ struct Consumer {
         const int32_t t = ok ? n / p.g : 0, j = ok ? n - t * p.g : 0;
         const uint32_t* qv = reinterpret_cast<const uint32_t*>(
             p.q + (((int64_t)(ok ? b : 0) * p.T + t) * p.Hq + kvh * p.g + j) * D);
-        if constexpr (!F8) {
+        if constexpr (!Q) {
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 dst[ks][0] = ok ? __ldg(qv + ks * 8 + tig) : 0u;
@@ -344,13 +342,26 @@ struct Consumer {
             }
             qs = p.sl2;
         } else {
-            // k-step ks covers channels 16ks..16ks+15 in the order the 8-bit K fragment
-            // brings them: b0 = channels 16ks + 4tig + {0, 1}, b1 = 16ks + 4tig + {2, 3}
+            // The channels come in the order the quantized K fragment brings them.
+            // 8-bit: k-step ks covers channels 16ks..16ks+15, b0 = 16ks + 4tig + {0, 1},
+            // b1 = 16ks + 4tig + {2, 3}.
+            // 4-bit: k-step ks takes channels c0 + {0..7} of the 32-channel chunk ks / 2,
+            // c0 = 32 (ks / 2) + 8tig, in nibble pairs: sub-step ks % 2 = 0 has b0 = c0 + {0, 4}
+            // and b1 = c0 + {1, 5}, sub-step 1 has b0 = c0 + {2, 6} and b1 = c0 + {3, 7}.
             float mx = 0.f;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                dst[ks][0] = ok ? __ldg(qv + ks * 8 + 2 * tig) : 0u;
-                dst[ks][1] = ok ? __ldg(qv + ks * 8 + 2 * tig + 1) : 0u;
+                if constexpr (I4) {
+                    const uint4 w = ok ? __ldg(reinterpret_cast<const uint4*>(qv + (ks >> 1) * 16 +
+                                                                             4 * tig))
+                                       : make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t e = (ks & 1) ? w.y : w.x, o4 = (ks & 1) ? w.w : w.z;
+                    dst[ks][0] = __byte_perm(e, o4, 0x5410);
+                    dst[ks][1] = __byte_perm(e, o4, 0x7632);
+                } else {
+                    dst[ks][0] = ok ? __ldg(qv + ks * 8 + 2 * tig) : 0u;
+                    dst[ks][1] = ok ? __ldg(qv + ks * 8 + 2 * tig + 1) : 0u;
+                }
                 mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_lo(dst[ks][0])), fabsf(bf16_hi(dst[ks][0]))),
                                      fmaxf(fabsf(bf16_lo(dst[ks][1])), fabsf(bf16_hi(dst[ks][1])))));
             }
@@ -416,7 +427,6 @@ struct Consumer {
     // masked for query token t when r > cut + t.
     __device__ void tile(uint32_t st, int lo, int hi, int cut) {
         const uint32_t kbase = st, vbase = st + (uint32_t)(D / 64) * 2048u;
-        const int g8 = lane >> 2;
         // ---- S^T = K Q^T (tokens x heads) -------------------------------------------
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
         {
@@ -489,7 +499,7 @@ struct Consumer {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
             uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
-            ldsm_x4(kbase + swz_u8<D>(row, 2u * c + csel), r0, r1, r2, r3);
+            ldsm_x4(kbase + swz_rows<D>(row, 2u * c + csel), r0, r1, r2, r3);
             e4m3x4_to_f16(r0, a0, a2);
             e4m3x4_to_f16(r1, a1, a3);
             mma_f16(sa, a0, a1, a2, a3, qf[2 * c][0], qf[2 * c][1]);
@@ -548,7 +558,7 @@ struct Consumer {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
             uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
-            ldsm_x4_trans(vbase + swz_u8<D>(row, 2u * c + csel), r0, r1, r2, r3);
+            ldsm_x4_trans(vbase + swz_rows<D>(row, 2u * c + csel), r0, r1, r2, r3);
             // [t0 cA, t0 cB, t1 cA, t1 cB] -> [t0 cA, t1 cA, t0 cB, t1 cB]
             r0 = __byte_perm(r0 & mlo, 0u, 0x3120);
             r1 = __byte_perm(r1 & mhi, 0u, 0x3120);
@@ -562,6 +572,106 @@ struct Consumer {
             e4m3x4_to_f16(r3, a2, a3);
             mma_f16(o[2 * c + 1], a0, a1, a2, a3, bh0, bh1);
             mma_f16(o[2 * c + 1], a0, a1, a2, a3, bl0, bl1);
+        }
+    }
+
+    // One 16-token tile of the 4-bit pool in stage buffer `st` (K codes, then V codes, rows of
+    // d/2 bytes, two codes per byte) with its row scales `sc`; rows are masked as in tile().
+    // The scales enter exactly as in tile_f8; every code converts exactly to fp16.
+    __device__ void tile_i4(uint32_t st, const float* sc, int lo, int hi, int cut) {
+        constexpr uint32_t RB = D / 2;  // bytes of a row
+        const uint32_t kbase = st, vbase = st + 16u * RB;
+        const int g8 = lane >> 2;
+        // ldmatrix lane addresses: matrices (rows 0-7 | 8-15) x (chunk 2c | 2c + 1)
+        const uint32_t row = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const uint32_t csel = lane >> 4;
+        // ---- S^T = K Q^T: a thread's register holds 8 adjacent channels of one token; nibble
+        // pairs (k, k + 4) form the fragments in the order load_q takes the query ------
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+            uint32_t r0, r1, r2, r3;  // chunk 2c: tokens g8, g8 + 8; chunk 2c + 1: the same
+            ldsm_x4(kbase + swz_rows<RB>(row, 2u * c + csel), r0, r1, r2, r3);
+            mma_f16(sa, i4pair_to_f16<0>(r0), i4pair_to_f16<0>(r1), i4pair_to_f16<1>(r0),
+                    i4pair_to_f16<1>(r1), qf[4 * c][0], qf[4 * c][1]);
+            mma_f16(sb, i4pair_to_f16<2>(r0), i4pair_to_f16<2>(r1), i4pair_to_f16<3>(r0),
+                    i4pair_to_f16<3>(r1), qf[4 * c + 1][0], qf[4 * c + 1][1]);
+            mma_f16(sa, i4pair_to_f16<0>(r2), i4pair_to_f16<0>(r3), i4pair_to_f16<1>(r2),
+                    i4pair_to_f16<1>(r3), qf[4 * c + 2][0], qf[4 * c + 2][1]);
+            mma_f16(sb, i4pair_to_f16<2>(r2), i4pair_to_f16<2>(r3), i4pair_to_f16<3>(r2),
+                    i4pair_to_f16<3>(r3), qf[4 * c + 3][0], qf[4 * c + 3][1]);
+        }
+        const bool v0 = g8 >= lo && g8 < hi, v1 = g8 + 8 >= lo && g8 + 8 < hi;
+        const float kc0 = sc[g8] * qsc, kc1 = sc[g8 + 8] * qsc;
+        bool a0, a1, a2, a3;
+        visible(lo, hi, cut, a0, a1, a2, a3);
+        const float s0 = a0 ? (sa[0] + sb[0]) * kc0 : kNegInf;
+        const float s1 = a1 ? (sa[1] + sb[1]) * kc0 : kNegInf;
+        const float s2 = a2 ? (sa[2] + sb[2]) * kc1 : kNegInf;
+        const float s3 = a3 ? (sa[3] + sb[3]) * kc1 : kNegInf;
+        float p0, p1, p2, p3;
+        softmax(s0, s1, s2, s3, p0, p1, p2, p3);
+        // ---- V scales: raise r to a power of two >= every V scale of the tile ---------
+        const float vs0 = v0 ? sc[16 + g8] : 0.f, vs1 = v1 ? sc[24 + g8] : 0.f;
+        float vt = fmaxf(vs0, vs1);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) vt = fmaxf(vt, __shfl_xor_sync(0xffffffffu, vt, off));
+        if (vt > rv) {  // warp-uniform; vt > 2^-112 is a normal number
+            const int32_t bits = __float_as_int(vt);
+            const int32_t k = min(127, ((bits >> 23) & 0xff) - 127 + ((bits & 0x7fffff) != 0));
+            const int32_t dk = rk - k;
+            const float f = dk >= -126 ? __int_as_float((127 + dk) << 23) : 0.f;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                o[mt][0] *= f; o[mt][1] *= f; o[mt][2] *= f; o[mt][3] *= f;
+            }
+            rk = k;
+            rv = __int_as_float((127 + k) << 23);
+            inv = __int_as_float((142 - k) << 23);
+        }
+        const float vn0 = vs0 * inv, vn1 = vs1 * inv;  // in [0, 2^15], exact
+        const float w0 = p0 * vn0, w1 = p1 * vn0, w2 = p2 * vn1, w3 = p3 * vn1;
+        // ---- W^T as the B operand: two fp16 terms, transposed with movmatrix ----------
+        const uint32_t h01 = pack_f16(w0, w1), h23 = pack_f16(w2, w3);
+        const uint32_t l01 = pack_f16(w0 - f16_lo(h01), w1 - f16_hi(h01));
+        const uint32_t l23 = pack_f16(w2 - f16_lo(h23), w3 - f16_hi(h23));
+        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+        const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+        // ---- O^T += V^T W^T ------------------------------------------------------------
+        // After the transposing ldmatrix a thread holds tokens 2tig, 2tig + 1 (r0, r2) or
+        // 8 + 2tig, 9 + 2tig (r1, r3) of channels 4g8 .. 4g8 + 3 of a 32-channel chunk, and
+        // nibble k of both halves is channel 4g8 + k of the two tokens: exactly an A
+        // fragment. M-tile mt takes channels 32 (mt / 2) + 4g8 + 2 (mt % 2) + {0, 1} as its
+        // rows g8 and g8 + 8. Every code is a finite value, so a masked row (weight 0)
+        // needs no zeroing.
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_trans(vbase + swz_rows<RB>(row, 2u * c + csel), r0, r1, r2, r3);
+            {
+                const uint32_t x0 = i4pair_to_f16<0>(r0), x1 = i4pair_to_f16<1>(r0);
+                const uint32_t x2 = i4pair_to_f16<0>(r1), x3 = i4pair_to_f16<1>(r1);
+                mma_f16(o[4 * c], x0, x1, x2, x3, bh0, bh1);
+                mma_f16(o[4 * c], x0, x1, x2, x3, bl0, bl1);
+            }
+            {
+                const uint32_t x0 = i4pair_to_f16<2>(r0), x1 = i4pair_to_f16<3>(r0);
+                const uint32_t x2 = i4pair_to_f16<2>(r1), x3 = i4pair_to_f16<3>(r1);
+                mma_f16(o[4 * c + 1], x0, x1, x2, x3, bh0, bh1);
+                mma_f16(o[4 * c + 1], x0, x1, x2, x3, bl0, bl1);
+            }
+            {
+                const uint32_t x0 = i4pair_to_f16<0>(r2), x1 = i4pair_to_f16<1>(r2);
+                const uint32_t x2 = i4pair_to_f16<0>(r3), x3 = i4pair_to_f16<1>(r3);
+                mma_f16(o[4 * c + 2], x0, x1, x2, x3, bh0, bh1);
+                mma_f16(o[4 * c + 2], x0, x1, x2, x3, bl0, bl1);
+            }
+            {
+                const uint32_t x0 = i4pair_to_f16<2>(r2), x1 = i4pair_to_f16<3>(r2);
+                const uint32_t x2 = i4pair_to_f16<2>(r3), x3 = i4pair_to_f16<3>(r3);
+                mma_f16(o[4 * c + 3], x0, x1, x2, x3, bh0, bh1);
+                mma_f16(o[4 * c + 3], x0, x1, x2, x3, bl0, bl1);
+            }
         }
     }
 
@@ -582,7 +692,7 @@ struct Consumer {
             if (hA < p.gq) { wm[hA] = m0; we[hA] = t0; }
             if (hB < p.gq) { wm[hB] = m1; we[hB] = t1; }
         }
-        if constexpr (!F8) {
+        if constexpr (!Q) {
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 const int dd = mt * 16 + g8;
@@ -593,7 +703,9 @@ struct Consumer {
             const float rs = rv * 3.0517578125e-05f;  // r * 2^-15, exact
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
-                const int dd = mt * 16 + 2 * g8;
+                // rows g8 and g8 + 8 of m-tile mt are channels dd and dd + 1 (4-bit: m-tile
+                // mt covers channels 32 (mt / 2) + 4 g8 + 2 (mt % 2) + {0, 1}, see tile_i4)
+                const int dd = I4 ? 32 * (mt >> 1) + 4 * g8 + 2 * (mt & 1) : mt * 16 + 2 * g8;
                 if (hA < p.gq)
                     *reinterpret_cast<float2*>(wo + hA * D + dd) =
                         make_float2(o[mt][0] * rs, o[mt][2] * rs);
@@ -605,7 +717,7 @@ struct Consumer {
     }
 };
 
-template <int D, bool F8>
+template <int D, int FMT>
 __global__ void __launch_bounds__(kAttnThreads)
 attention_kernel(const __grid_constant__ AttnParams p,
                  const __grid_constant__ CUtensorMap tmap_k,
@@ -616,10 +728,11 @@ attention_kernel(const __grid_constant__ AttnParams p,
         const uint32_t off = smem_u32(smem_raw);
         sm.base = smem_raw + (((off + 1023u) & ~1023u) - off);
     }
-    sm.L = attn_smem_layout(D, p.gq, p.nitems, p.Hkv, p.mode == MODE_SPARSE, F8);
+    constexpr bool Q = FMT != DATTN_KV_BF16;  // a quantized pool with row scales
+    sm.L = attn_smem_layout(D, p.gq, p.nitems, p.Hkv, p.mode == MODE_SPARSE, FMT);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t G = gridDim.x, cta = blockIdx.x;
-    constexpr int NS = attn_stages(F8);
+    constexpr int NS = attn_stages(FMT);
 
     // ---------------------------------------------------------------- setup
     // Before the dependency wait: only state that no kernel of this library writes.
@@ -760,8 +873,8 @@ attention_kernel(const __grid_constant__ AttnParams p,
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer warp
         const uint64_t pol = policy_evict_first();
-        const uint32_t tile_bytes = (F8 ? 16u : 32u) * (uint32_t)D;
-        const uint32_t tx = 2u * tile_bytes + (F8 ? 128u : 0u);  // + the tile's 32 scales
+        const uint32_t tile_bytes = attn_tile_bytes(FMT, D);
+        const uint32_t tx = 2u * tile_bytes + (Q ? 128u : 0u);  // + the tile's 32 scales
         const uint32_t stages0 = smem_u32(sm.base + sm.L.stages);
         int32_t k = 0;  // real tiles issued so far: tile k uses stage k % NS
         bool stop = false;
@@ -795,7 +908,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
                             } else {
                                 mbar_arrive_expect_tx(full, tx);
                                 const uint32_t dst = stages0 + (uint32_t)stg * sm.L.stage_bytes;
-                                if constexpr (F8) {
+                                if constexpr (Q) {
                                     tma_load_2d(dst, &tmap_k, 0, y, full, pol);
                                     tma_load_2d(dst + tile_bytes, &tmap_v, 0, y, full, pol);
                                     // the tile's scales: 128 bytes at tile index y / 16
@@ -831,17 +944,17 @@ attention_kernel(const __grid_constant__ AttnParams p,
     }
 
     // ---------------------------------------------------------------- consumer warps
-    Consumer<D, F8> cons(p, sm, warp, lane);
+    Consumer<D, FMT> cons(p, sm, warp, lane);
     const uint32_t stage0 = smem_u32(sm.base + sm.L.stages);
     int32_t kbase = 0;  // real tiles of earlier pieces
     int32_t s = s_first, sst, sreal, r0, r1;
     bool have = plan.next_piece(s, X0, X1, sst, sreal, r0, r1);
-    uint32_t qn[Consumer<D, F8>::KS][2];
+    uint32_t qn[Consumer<D, FMT>::KS][2];
     float qsn = 0.f;
     if (have) cons.load_q(s, qn, qsn);
     while (have) {
 #pragma unroll
-        for (int ks = 0; ks < Consumer<D, F8>::KS; ++ks) {
+        for (int ks = 0; ks < Consumer<D, FMT>::KS; ++ks) {
             cons.qf[ks][0] = qn[ks][0];
             cons.qf[ks][1] = qn[ks][1];
         }
@@ -862,7 +975,10 @@ attention_kernel(const __grid_constant__ AttnParams p,
             const int32_t lohi = sm.meta()[stg];
             const int lo = tile_lo(lohi), hi = tile_hi(lohi), cut = tile_cut(lohi);
             if (ok && !(lohi & kTileSkip)) {
-                if constexpr (F8) {
+                if constexpr (FMT == DATTN_KV_INT4) {
+                    cons.tile_i4(stage0 + (uint32_t)stg * sm.L.stage_bytes, sm.scales(stg), lo, hi,
+                                 cut);
+                } else if constexpr (Q) {
                     cons.tile_f8(stage0 + (uint32_t)stg * sm.L.stage_bytes, sm.scales(stg), lo, hi,
                                  cut);
                 } else {
@@ -1003,7 +1119,7 @@ struct KernelInfo {
     int max_smem_set = 0;
 };
 
-template <int D, bool F8>
+template <int D, int FMT>
 KernelInfo& kernel_info() {
     static KernelInfo info;
     return info;
@@ -1011,12 +1127,12 @@ KernelInfo& kernel_info() {
 
 std::mutex g_attr_mutex;
 
-template <int D, bool F8>
+template <int D, int FMT>
 dattn_status_t ensure_smem(uint32_t bytes) {
     std::lock_guard<std::mutex> lock(g_attr_mutex);
-    KernelInfo& ki = kernel_info<D, F8>();
+    KernelInfo& ki = kernel_info<D, FMT>();
     if ((int)bytes > ki.max_smem_set) {
-        if (cudaFuncSetAttribute(attention_kernel<D, F8>,
+        if (cudaFuncSetAttribute(attention_kernel<D, FMT>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bytes) != cudaSuccess)
             return DATTN_ERR_CUDA;
@@ -1025,10 +1141,10 @@ dattn_status_t ensure_smem(uint32_t bytes) {
     return DATTN_OK;
 }
 
-template <int D, bool F8>
+template <int D, int FMT>
 int occupancy(uint32_t smem) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attention_kernel<D, F8>, kAttnThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attention_kernel<D, FMT>, kAttnThreads,
                                                       smem) != cudaSuccess)
         return 1;
     return n < 1 ? 1 : n;
@@ -1041,15 +1157,15 @@ size_t attn_workspace_bytes(int32_t nseg, int32_t g, int32_t D, int32_t G) {
     return counters + (size_t)(G + nseg) * slot_floats(g, D) * 4;
 }
 
-template <int D, bool F8>
+template <int D, int FMT>
 static dattn_status_t launch_d(const AttnParams& p0, const void* k_pool, const void* v_pool,
                                int32_t num_splits, void* ws, size_t ws_bytes,
                                cudaStream_t stream, int64_t tiles_bound) {
     AttnParams p = p0;
-    const AttnSmem L = attn_smem_layout(D, p.gq, p.nitems, p.Hkv, p.mode == MODE_SPARSE, F8);
-    dattn_status_t st = ensure_smem<D, F8>(L.total);
+    const AttnSmem L = attn_smem_layout(D, p.gq, p.nitems, p.Hkv, p.mode == MODE_SPARSE, FMT);
+    dattn_status_t st = ensure_smem<D, FMT>(L.total);
     if (st != DATTN_OK) return st;
-    const int32_t G = choose_splits(tiles_bound, num_splits, occupancy<D, F8>(L.total));
+    const int32_t G = choose_splits(tiles_bound, num_splits, occupancy<D, FMT>(L.total));
     const size_t counters = ((size_t)p.nseg * 4 + 255) & ~(size_t)255;
     if (ws == nullptr || ws_bytes < attn_workspace_bytes(p.nseg, p.gq, D, G) ||
         (reinterpret_cast<uintptr_t>(ws) & 255))
@@ -1059,10 +1175,15 @@ static dattn_status_t launch_d(const AttnParams& p0, const void* k_pool, const v
     alignas(64) CUtensorMap tk;
     alignas(64) CUtensorMap tv;
     const int64_t rows = (int64_t)p.num_pages * p.Hkv * p.P;
-    auto make_map = F8 ? make_kv_tensor_map_u8 : make_kv_tensor_map;
-    if ((st = make_map(&tk, k_pool, rows, D)) != DATTN_OK) return st;
-    if ((st = make_map(&tv, v_pool, rows, D)) != DATTN_OK) return st;
-    if (launch_pdl(attention_kernel<D, F8>, dim3(G), dim3(kAttnThreads), L.total, stream, p, tk,
+    if constexpr (FMT == DATTN_KV_BF16) {
+        if ((st = make_kv_tensor_map(&tk, k_pool, rows, D)) != DATTN_OK) return st;
+        if ((st = make_kv_tensor_map(&tv, v_pool, rows, D)) != DATTN_OK) return st;
+    } else {
+        const int row_bytes = FMT == DATTN_KV_INT4 ? D / 2 : D;
+        if ((st = make_kv_tensor_map_u8(&tk, k_pool, rows, row_bytes)) != DATTN_OK) return st;
+        if ((st = make_kv_tensor_map_u8(&tv, v_pool, rows, row_bytes)) != DATTN_OK) return st;
+    }
+    if (launch_pdl(attention_kernel<D, FMT>, dim3(G), dim3(kAttnThreads), L.total, stream, p, tk,
                    tv) != cudaSuccess)
         return DATTN_ERR_CUDA;
     return DATTN_OK;
@@ -1071,10 +1192,14 @@ static dattn_status_t launch_d(const AttnParams& p0, const void* k_pool, const v
 dattn_status_t launch_attention(const AttnParams& p, const void* k_pool, const void* v_pool,
                                 int D, int32_t num_splits, void* ws, size_t ws_bytes,
                                 cudaStream_t stream, int64_t tiles_bound) {
-    const bool f8 = p.f8 != 0;
-    auto launch = D == 64 ? (f8 ? launch_d<64, true> : launch_d<64, false>)
-                          : (f8 ? launch_d<128, true> : launch_d<128, false>);
     if (D != 64 && D != 128) return DATTN_ERR_UNSUPPORTED;
+    auto pick = [&](auto bf16, auto f8, auto i4) {
+        return p.fmt == DATTN_KV_INT4 ? i4 : p.fmt == DATTN_KV_FP8_E4M3 ? f8 : bf16;
+    };
+    auto launch = D == 64 ? pick(launch_d<64, DATTN_KV_BF16>, launch_d<64, DATTN_KV_FP8_E4M3>,
+                                 launch_d<64, DATTN_KV_INT4>)
+                          : pick(launch_d<128, DATTN_KV_BF16>, launch_d<128, DATTN_KV_FP8_E4M3>,
+                                 launch_d<128, DATTN_KV_INT4>);
     return launch(p, k_pool, v_pool, num_splits, ws, ws_bytes, stream, tiles_bound);
 }
 

@@ -253,6 +253,31 @@ __device__ __forceinline__ uint32_t swz64(uint32_t row, uint32_t chunk) {
     return row * 64u + ((chunk ^ ((row >> 1) & 3u)) << 4);
 }
 
+// Byte offset of 16-byte chunk `chunk` of row `row` in a [rows][32 B] box written by TMA
+// with CU_TENSOR_MAP_SWIZZLE_32B (the box base is 256-byte aligned).
+__device__ __forceinline__ uint32_t swz32(uint32_t row, uint32_t chunk) {
+    return row * 32u + ((chunk ^ ((row >> 2) & 1u)) << 4);
+}
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a [rows][RB bytes] box written by TMA
+// with the swizzle of that row size.
+template <uint32_t RB>
+__device__ __forceinline__ uint32_t swz_rows(uint32_t row, uint32_t chunk) {
+    static_assert(RB == 128 || RB == 64 || RB == 32, "swizzled rows are 32, 64 or 128 bytes");
+    return RB == 128 ? swz128(row, chunk) : RB == 64 ? swz64(row, chunk) : swz32(row, chunk);
+}
+
+// The 4-bit codes at nibble K of each 16-bit half of x (bits 4K..4K+3 and 16+4K..16+4K+3,
+// each code stored as code + 8) as two exact fp16 values: 0x6400 | n is the fp16 value
+// 1024 + n, and subtracting 1032 leaves n - 8.
+template <int K>
+__device__ __forceinline__ uint32_t i4pair_to_f16(uint32_t x) {
+    const uint32_t v = ((x >> (4 * K)) & 0x000f000fu) | 0x64006400u;
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x64086408u));
+    return r;
+}
+
 // Programmatic dependent launch: a kernel launched with programmatic stream serialization may
 // start while the previous kernel on the stream is still running. It must wait here before it
 // reads anything that kernel writes. Without a programmatic launch this returns at once.

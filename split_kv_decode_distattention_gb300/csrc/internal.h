@@ -14,10 +14,18 @@ constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
 // Pipeline depth, a multiple of kConsumerWarps: consumer warp w takes the tiles k = w mod 4,
 // so it has depth/4 - 1 tiles loading while it works on one. The 8-bit stages are half as
 // large; 12 of them (48 KB for d = 128) keep more bytes in flight per warp without lowering
-// the CTAs per SM, which 16 stages did for grouped heads.
+// the CTAs per SM, which 16 stages did for grouped heads. The 4-bit stages are a quarter as
+// large, and 24 of them take about the shared memory of the 8-bit ring.
 constexpr int kStagesBf16 = 8;
 constexpr int kStagesF8 = 12;
-__host__ __device__ constexpr int attn_stages(bool f8) { return f8 ? kStagesF8 : kStagesBf16; }
+constexpr int kStagesI4 = 24;
+__host__ __device__ constexpr int attn_stages(int fmt) {
+    return fmt == DATTN_KV_INT4 ? kStagesI4 : fmt == DATTN_KV_FP8_E4M3 ? kStagesF8 : kStagesBf16;
+}
+// Bytes of one K (or V) tile of 16 tokens in shared memory for a pool format.
+__host__ __device__ constexpr uint32_t attn_tile_bytes(int fmt, int D) {
+    return (fmt == DATTN_KV_INT4 ? 8u : fmt == DATTN_KV_FP8_E4M3 ? 16u : 32u) * (uint32_t)D;
+}
 constexpr int kMaxItems = 4096;     // B (or C) bound
 constexpr int kMaxKvHeads = 256;
 constexpr int kMaxGroup = 8;        // query heads per KV head
@@ -59,9 +67,10 @@ struct AttnParams {
     int32_t nseg;
     int32_t nitems;     // B for dense / sparse, C for partial
     int32_t* dev_err;
-    // 8-bit pool: FP8 E4M3 codes plus one fp32 scale per (token, KV head) row; the scales
-    // of a 16-token tile are one 128-byte run [16 K scales][16 V scales]
-    int32_t f8;
+    // pool format (DATTN_KV_*). The 8-bit (FP8 E4M3) and 4-bit (symmetric integer) pools keep
+    // one fp32 scale per (token, KV head) row; the scales of a 16-token tile are one 128-byte
+    // run [16 K scales][16 V scales]
+    int32_t fmt;
     const float* kv_scale;
 };
 
@@ -72,22 +81,22 @@ __host__ __device__ inline int32_t slot_floats(int32_t g, int32_t D) {
 }
 
 // Shared-memory layout of the attention engine, identical on host and device. A stage holds
-// the K tile then the V tile of 16 tokens (bf16: 32*d bytes each; 8-bit: 16*d bytes each);
-// with the 8-bit pool, the stage's 16 K scales and 16 V scales sit in `scales`.
+// the K tile then the V tile of 16 tokens (bf16: 32*d bytes each; 8-bit: 16*d; 4-bit: 8*d);
+// with a quantized pool, the stage's 16 K scales and 16 V scales sit in `scales`.
 struct AttnSmem {
     uint32_t nstages, stage_bytes, stages, scales, bars, meta, flags, ws_m, ws_e, ws_o, kind_before,
         kinds, item_start, item_len, scan, total;
 };
 
 __host__ __device__ inline AttnSmem attn_smem_layout(int D, int g, int nitems, int Hkv,
-                                                     bool sparse, bool f8) {
+                                                     bool sparse, int fmt) {
     AttnSmem s;
-    const uint32_t ns = (uint32_t)attn_stages(f8);
+    const uint32_t ns = (uint32_t)attn_stages(fmt);
     s.nstages = ns;
-    s.stage_bytes = (f8 ? 32u : 64u) * (uint32_t)D;
+    s.stage_bytes = 2u * attn_tile_bytes(fmt, D);
     uint32_t o = 0;
     s.stages = o;      o += ns * s.stage_bytes;
-    s.scales = o;      o += f8 ? ns * 128u : 0u;
+    s.scales = o;      o += fmt != DATTN_KV_BF16 ? ns * 128u : 0u;
     s.bars = o;        o += 2u * ns * 8u;
     s.meta = o;        o += ns * 4u;
     s.flags = o;       o += 16u;
@@ -108,7 +117,10 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int D, int g, int nitems, i
 // Device properties and cached driver entry points.
 int sm_count_current();
 dattn_status_t make_kv_tensor_map(void* tmap_out, const void* pool, int64_t rows, int D);
-dattn_status_t make_kv_tensor_map_u8(void* tmap_out, const void* pool, int64_t rows, int D);
+// 2-D map over rows of `row_bytes` one-byte elements (8-bit codes: d; packed 4-bit codes:
+// d / 2), one box of 16 rows, swizzled by the row size (128, 64 or 32 bytes).
+dattn_status_t make_kv_tensor_map_u8(void* tmap_out, const void* pool, int64_t rows,
+                                     int row_bytes);
 
 dattn_status_t launch_attention(const AttnParams& p, const void* k_pool, const void* v_pool,
                                 int D, int32_t num_splits, void* ws, size_t ws_bytes,

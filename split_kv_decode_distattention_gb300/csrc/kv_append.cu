@@ -20,6 +20,11 @@
 // reduction among them. scale = max|x| / 448 and each code is E4M3(x / scale), both
 // divisions in IEEE fp32, the conversion rounding to nearest even with saturation. The
 // statistics are still taken from the bf16 key.
+//
+// The 4-bit pool (the streaming-head cache of that section is 4-bit): scale = max|x| / 7 and
+// each code is x / scale rounded to the nearest integer (ties to even) in [-7, 7], both
+// divisions in IEEE fp32, stored as the nibble code + 8 with channel 2j in the low nibble of
+// byte j. A thread's 8 channels become one 32-bit word.
 #include "common.cuh"
 #include "internal.h"
 
@@ -86,7 +91,31 @@ __device__ __forceinline__ uint2 quant_row_chunk(const uint4& v, unsigned mask, 
     return scale > 0.f ? quant8(v, scale) : make_uint2(0u, 0u);
 }
 
-template <int D, bool F8>
+// 4-bit codes of the 8 bf16 values of a chunk divided by s (s > 0): code c + 8 of channel
+// 2j in the low nibble of byte j, of channel 2j + 1 in its high nibble.
+__device__ __forceinline__ uint32_t quant4(const uint4& v, float s) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int c0 = min(7, max(-7, __float2int_rn(__fdiv_rn(bf(w[i] & 0xffffu), s))));
+        const int c1 = min(7, max(-7, __float2int_rn(__fdiv_rn(bf(w[i] >> 16), s))));
+        out |= (uint32_t)((c0 + 8) | ((c1 + 8) << 4)) << (8 * i);
+    }
+    return out;
+}
+
+// Row scale and packed 4-bit codes of one 8-channel chunk (lanes as in quant_row_chunk).
+template <int VPR>
+__device__ __forceinline__ uint32_t quant4_row_chunk(const uint4& v, unsigned mask, float& scale) {
+    float m = absmax8(v);
+#pragma unroll
+    for (int off = 1; off < VPR; off <<= 1) m = fmaxf(m, __shfl_xor_sync(mask, m, off));
+    scale = __fdiv_rn(m, 7.0f);
+    return scale > 0.f ? quant4(v, scale) : 0x88888888u;
+}
+
+template <int D, int FMT>
 __global__ void __launch_bounds__(kAppendMaxThreads)
 kv_append_kernel(dattn_kv_layout L, void* __restrict__ k_pool_v, void* __restrict__ v_pool_v,
                  uint16_t* __restrict__ stats, const uint16_t* __restrict__ k_new,
@@ -157,7 +186,22 @@ kv_append_kernel(dattn_kv_layout L, void* __restrict__ k_pool_v, void* __restric
                     else page = pg;
                 }
             }
-            if constexpr (F8) {
+            if constexpr (FMT == DATTN_KV_INT4) {
+                // every lane of a row takes part in the reductions, mapped page or not
+                float ks, vs;
+                const uint32_t kc = quant4_row_chunk<VPR>(kv, mask, ks);
+                const uint32_t vc = quant4_row_chunk<VPR>(vv, mask, vs);
+                if (page >= 0) {
+                    const int64_t row = ((int64_t)page * Hkv + h) * P + (t - lp * P);
+                    *reinterpret_cast<uint32_t*>(k_code + row * (D / 2) + c8 * 4) = kc;
+                    *reinterpret_cast<uint32_t*>(v_code + row * (D / 2) + c8 * 4) = vc;
+                    if (c8 == 0) {  // [row / 16][K, V][row % 16]
+                        float* sc = L.kv_scale + (row >> 4) * 32 + (row & 15);
+                        sc[0] = ks;
+                        sc[16] = vs;
+                    }
+                }
+            } else if constexpr (FMT == DATTN_KV_FP8_E4M3) {
                 // every lane of a row takes part in the reductions, mapped page or not
                 float ks, vs;
                 const uint2 kc = quant_row_chunk<VPR>(kv, mask, ks);
@@ -232,9 +276,15 @@ dattn_status_t launch_kv_append(const dattn_kv_layout& L, void* k_pool, void* v_
     const int32_t inplace = single ? 1 : 0;
     const int32_t items = L.num_kv_heads * (L.head_dim / 8);
     const dim3 block(min(kAppendMaxThreads, (items + 31) / 32 * 32));
-    const bool f8 = L.kv_format == DATTN_KV_FP8_E4M3;
-    auto kern = L.head_dim == 64 ? (f8 ? kv_append_kernel<64, true> : kv_append_kernel<64, false>)
-                                 : (f8 ? kv_append_kernel<128, true> : kv_append_kernel<128, false>);
+    auto pick = [&](auto bf16, auto f8, auto i4) {
+        return L.kv_format == DATTN_KV_INT4 ? i4 : L.kv_format == DATTN_KV_FP8_E4M3 ? f8 : bf16;
+    };
+    auto kern = L.head_dim == 64
+                    ? pick(kv_append_kernel<64, DATTN_KV_BF16>, kv_append_kernel<64, DATTN_KV_FP8_E4M3>,
+                           kv_append_kernel<64, DATTN_KV_INT4>)
+                    : pick(kv_append_kernel<128, DATTN_KV_BF16>,
+                           kv_append_kernel<128, DATTN_KV_FP8_E4M3>,
+                           kv_append_kernel<128, DATTN_KV_INT4>);
     const cudaError_t e = launch_pdl(kern, grid, block, 0, stream, L, k_pool, v_pool, stats,
                                      k_new, v_new, T, seq_lens, inplace, dev_err);
     if (e != cudaSuccess) return DATTN_ERR_CUDA;

@@ -876,8 +876,9 @@ extern "C" dattn_status_t dattn_prefill(const dattn_kv_layout* layout, const voi
     if ((int64_t)layout->max_pages_per_req * layout->page_size >= (1ll << 30))
         return DATTN_ERR_UNSUPPORTED;
     if (layout->kv_format != DATTN_KV_BF16) {
-        return layout->kv_format == DATTN_KV_FP8_E4M3 ? DATTN_ERR_UNSUPPORTED
-                                                      : DATTN_ERR_INVALID_ARG;
+        return layout->kv_format == DATTN_KV_FP8_E4M3 || layout->kv_format == DATTN_KV_INT4
+                   ? DATTN_ERR_UNSUPPORTED
+                   : DATTN_ERR_INVALID_ARG;
     }
     // the call's own arguments
     if (B < 0 || Tq < 0 || Hq <= 0 || Hq % layout->num_kv_heads != 0) return DATTN_ERR_INVALID_ARG;

@@ -7,7 +7,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (KV_BF16, KV_FP8_E4M3, KVLayout, SparseConfig, Workspace, dattn_decode,
+from . import (KV_BF16, KV_FP8_E4M3, KV_INT4, KVLayout, SparseConfig, Workspace, dattn_decode,
                dattn_decode_multi, dattn_kv_append, dattn_page_select)
 from .workloads import Case
 
@@ -17,7 +17,8 @@ class PagedCache:
 
     kv_format KV_BF16 keeps bf16 values; KV_FP8_E4M3 keeps uint8 E4M3 codes plus one float32
     scale per (token, KV head) row in kv_scale [num_pages][Hkv][P/16][2][16] (per logical
-    page: 16 K scales, then 16 V scales).
+    page: 16 K scales, then 16 V scales); KV_INT4 keeps [num_pages][Hkv][P][d/2] bytes of two
+    4-bit codes each, with kv_scale as for KV_FP8_E4M3.
     """
 
     def __init__(self, case: Case, device="cuda", with_stats: bool = False, fill: bool = True,
@@ -27,11 +28,13 @@ class PagedCache:
         c = case
         alloc = torch.zeros if zero_pool else torch.empty
         self.kv_format = kv_format
-        elem = torch.uint8 if kv_format == KV_FP8_E4M3 else torch.bfloat16
-        self.k_pool = alloc(c.num_pages, c.Hkv, c.P, c.d, dtype=elem, device=device)
-        self.v_pool = alloc(c.num_pages, c.Hkv, c.P, c.d, dtype=elem, device=device)
+        quant = kv_format in (KV_FP8_E4M3, KV_INT4)
+        elem = torch.uint8 if quant else torch.bfloat16
+        row = c.d // 2 if kv_format == KV_INT4 else c.d
+        self.k_pool = alloc(c.num_pages, c.Hkv, c.P, row, dtype=elem, device=device)
+        self.v_pool = alloc(c.num_pages, c.Hkv, c.P, row, dtype=elem, device=device)
         self.kv_scale = None
-        if kv_format == KV_FP8_E4M3:
+        if quant:
             self.kv_scale = alloc(c.num_pages, c.Hkv, c.P // 16, 2, 16, dtype=torch.float32,
                                   device=device)
         self.stats = None

@@ -123,16 +123,18 @@ def test_kv_format_is_validated(dattn):
         out.c.kv_format, out.c.kv_scale = fmt, kv_scale
         return out
 
-    assert _decode_status(dattn, lay(2, None)) == INVALID    # unknown format
+    assert _decode_status(dattn, lay(3, 128)) == INVALID     # unknown format
     assert _decode_status(dattn, lay(-1, None)) == INVALID
-    assert _decode_status(dattn, lay(1, None)) == INVALID    # the scale pool missing
-    assert _decode_status(dattn, lay(1, 72)) == INVALID      # not 16-byte aligned
-    # well-formed layouts pass the layout checks: the group-size check answers next
-    assert _decode_status(dattn, lay(1, 128), Hq=36) == UNSUPPORTED
+    for fmt in (dattn.KV_FP8_E4M3, dattn.KV_INT4):
+        assert _decode_status(dattn, lay(fmt, None)) == INVALID  # the scale pool missing
+        assert _decode_status(dattn, lay(fmt, 72)) == INVALID    # not 16-byte aligned
+        # well-formed layouts pass the layout checks: the group-size check answers next
+        assert _decode_status(dattn, lay(fmt, 128), Hq=36) == UNSUPPORTED
     assert _decode_status(dattn, lay(0, None), Hq=36) == UNSUPPORTED
     import torch
-    with pytest.raises(ValueError):
-        dattn.KVLayout(8, 2, 128, 16, torch.zeros(1, 4, dtype=torch.int32), kv_format=1)
+    for fmt in (dattn.KV_FP8_E4M3, dattn.KV_INT4):
+        with pytest.raises(ValueError):
+            dattn.KVLayout(8, 2, 128, 16, torch.zeros(1, 4, dtype=torch.int32), kv_format=fmt)
 
 
 def test_decode_multi_is_validated(dattn):

@@ -1,9 +1,11 @@
-"""GPU parity of the 8-bit KV path (FP8 E4M3 codes with one fp32 scale per row).
+"""GPU parity of the quantized KV paths: the 8-bit pool (FP8 E4M3 codes) and the 4-bit pool
+(symmetric integer codes, two per byte), each with one fp32 scale per row.
 
-The append is compared bit for bit with the oracle's 8-bit write of the same bf16 inputs:
-codes, scales and the logical-page statistics. Every attention result is compared with the
-oracle's float64 attention over the oracle's own dequantized values (code * scale), never
-over anything read back from the GPU pool. The tolerance is the bf16 path's.
+The append is compared bit for bit with the oracle's write of the same bf16 inputs in the
+same format: codes, scales and the logical-page statistics. Every attention result is
+compared with the oracle's float64 attention over the oracle's own dequantized values
+(code * scale), never over anything read back from the GPU pool. The tolerance is the bf16
+path's.
 """
 import numpy as np
 import pytest
@@ -25,26 +27,37 @@ def _lib():
     return dattn
 
 
-def _cache(case, **kw):
-    from split_kv_decode_distattention_gb300 import KV_FP8_E4M3
+FORMATS = ["fp8", "int4"]
+
+
+def _cache(case, fmt, **kw):
+    from split_kv_decode_distattention_gb300 import KV_FP8_E4M3, KV_INT4
     from split_kv_decode_distattention_gb300.harness import PagedCache
-    return PagedCache(case, DEV, kv_format=KV_FP8_E4M3, **kw)
+    return PagedCache(case, DEV, kv_format=KV_INT4 if fmt == "int4" else KV_FP8_E4M3, **kw)
 
 
-def _deq(K, V):
-    """The oracle's 8-bit round trip of token-ordered bf16 rows [L][Hkv][d] (float64)."""
-    kc, ks = oracle.quantize_rows_fp8(K)
-    vc, vs = oracle.quantize_rows_fp8(V)
-    return oracle.dequantize_rows_fp8(kc, ks), oracle.dequantize_rows_fp8(vc, vs)
+def _quant(fmt):
+    """The oracle's row quantizer, dequantizer and paged write of a format."""
+    if fmt == "int4":
+        return oracle.quantize_rows_int4, oracle.dequantize_rows_int4, oracle.kv_write_int4
+    return oracle.quantize_rows_fp8, oracle.dequantize_rows_fp8, oracle.kv_write_fp8
 
 
-def _ref_dense(case, q, lens, kv=None):
+def _deq(K, V, fmt):
+    """The oracle's round trip of token-ordered bf16 rows [L][Hkv][d] (float64)."""
+    quant, deq, _ = _quant(fmt)
+    kc, ks = quant(K)
+    vc, vs = quant(V)
+    return deq(kc, ks), deq(vc, vs)
+
+
+def _ref_dense(case, q, lens, fmt, kv=None):
     """Oracle attention of every (b, h) over the dequantized tokens 0..L-1."""
     qb = oracle.bf16_bits(q)
     res = {}
     for b in range(case.B):
         K, V = kv[b] if kv is not None else host_kv(case, b, lens[b], DEV)
-        Kd, Vd = _deq(K, V)
+        Kd, Vd = _deq(K, V, fmt)
         for h in range(case.Hq):
             kvh = h // case.g
             res[(b, h)] = oracle.attention_f64(qb[b, h], Kd[:, kvh], Vd[:, kvh], case.scale)
@@ -62,18 +75,18 @@ def _check(res, out, m_g, e_g, lens, what):
             assert_e_close(eg[b, h], re, f"{what} b={b} h={h}")
 
 
-def _oracle_pool(case, lens, kv=None):
+def _oracle_pool(case, lens, fmt, kv=None):
     """Codes, scales and statistics the oracle writes for every request's tokens."""
     P, d = case.P, case.d
-    kp = np.zeros((case.num_pages, case.Hkv, P, d), np.uint8)
+    write = _quant(fmt)[2]
+    kp = np.zeros((case.num_pages, case.Hkv, P, d // 2 if fmt == "int4" else d), np.uint8)
     vp = np.zeros_like(kp)
     ks = np.zeros((case.num_pages, case.Hkv, P), np.float32)
     vs = np.zeros_like(ks)
     st = np.zeros((case.num_pages, case.Hkv, P // 16, 2, d), np.uint16)
     for b in range(case.B):
         K, V = kv[b] if kv is not None else host_kv(case, b, lens[b], DEV)
-        assert oracle.kv_write_fp8(kp, vp, ks, vs, P, case.block_table[b], case.num_pages,
-                                   K, V, 0) == 0
+        assert write(kp, vp, ks, vs, P, case.block_table[b], case.num_pages, K, V, 0) == 0
         for h in range(case.Hkv):
             for t0 in range(0, lens[b], 16):
                 kmax, kmin = oracle.logical_page_stats(K[:, h].copy(), t0, min(t0 + 16, lens[b]))
@@ -98,13 +111,14 @@ def _assert_pool(cache, want):
         np.testing.assert_array_equal(oracle.bf16_bits(cache.stats), st)
 
 
-# ---------------------------------------------------------------- 8-bit append
+# ---------------------------------------------------------------- quantized append
 
+@pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("d,P,chunk", [(128, 16, 37), (64, 64, 200), (128, 64, 5), (64, 16, 64)])
-def test_fp8_append_codes_scales_and_stats_bit_exact(d, P, chunk):
+def test_quant_append_codes_scales_and_stats_bit_exact(fmt, d, P, chunk):
     _lib()
     case = W.Case("append8", B=3, Hq=4, Hkv=2, d=d, P=P, lens=[0, 131, 290], seed=3)
-    cache = _cache(case, with_stats=True, fill=False, zero_pool=True, chunk_tokens=chunk)
+    cache = _cache(case, fmt, with_stats=True, fill=False, zero_pool=True, chunk_tokens=chunk)
     cache.fill()
     for _ in range(3):  # decode-style single-token appends for every request
         kn, vn = cache.new_tokens(1)
@@ -112,12 +126,13 @@ def test_fp8_append_codes_scales_and_stats_bit_exact(d, P, chunk):
     torch.cuda.synchronize()
     assert int(cache.dev_err.item()) == 0
     assert cache.seq_lens.tolist() == cache.lens
-    _assert_pool(cache, _oracle_pool(case, cache.lens))
+    _assert_pool(cache, _oracle_pool(case, cache.lens, fmt))
 
 
 def _special_rows(Hkv, d, T, seed):
-    """bf16 rows that reach the corners of the format: zero rows, -0, rows whose small
-    elements fall to E4M3 subnormals or to zero, exact ties, and a wide range of row scales."""
+    """bf16 rows that reach the corners of the formats: zero rows, -0, rows whose small
+    elements fall to E4M3 subnormals or to zero, exact ties of both formats, and a wide range
+    of row scales."""
     rng = np.random.default_rng(seed)
     x = rng.normal(size=(T, Hkv, d)).astype(np.float32)
     x *= np.exp2(rng.integers(-30, 30, size=(T, Hkv, 1))).astype(np.float32)  # row scales
@@ -131,14 +146,17 @@ def _special_rows(Hkv, d, T, seed):
     x[4, :, :] = np.float32(1.0 + 1.0 / 16)  # halfway between two codes after scaling...
     x[4, :, 0] = 448.0                       # ...by 1: ties go to the even code
     x[5, :, :] = rng.choice([-3.0, 3.0], size=(Hkv, d))
+    x[6, :, :] = rng.choice([0.5, 1.5, 2.5, -0.5, -1.5, -6.5], size=(Hkv, d))
+    x[6, :, 0] = 7.0                         # 4-bit scale 1: every element is a tie
     return torch.from_numpy(x).to(torch.bfloat16)
 
 
-def test_fp8_append_corner_rows_bit_exact():
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_quant_append_corner_rows_bit_exact(fmt):
     dattn = _lib()
     case = W.Case("corner8", B=1, Hq=2, Hkv=2, d=128, P=16, lens=[0], seed=1, shuffle=True,
                   reserve_tokens=64)
-    cache = _cache(case, fill=False, zero_pool=True)
+    cache = _cache(case, fmt, fill=False, zero_pool=True)
     K = _special_rows(2, 128, 40, 7)
     V = _special_rows(2, 128, 40, 8)
     dattn.dattn_kv_append(cache.layout, cache.k_pool, cache.v_pool, None,
@@ -148,10 +166,10 @@ def test_fp8_append_corner_rows_bit_exact():
     torch.cuda.synchronize()
     assert int(cache.dev_err.item()) == 0
     kv = [(oracle.bf16_bits(K), oracle.bf16_bits(V))]
-    _assert_pool(cache, _oracle_pool(case, [40], kv=kv))
+    _assert_pool(cache, _oracle_pool(case, [40], fmt, kv=kv))
 
 
-# ---------------------------------------------------------------- 8-bit fused dense decode
+# ---------------------------------------------------------------- quantized fused dense decode
 
 FP8_DENSE_CASES = [
     # (d, Hq, Hkv, P, lens, num_splits)
@@ -166,12 +184,13 @@ FP8_DENSE_CASES = [
 ]
 
 
+@pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("d,Hq,Hkv,P,lens,splits", FP8_DENSE_CASES)
-def test_fp8_decode_dense_matches_oracle(d, Hq, Hkv, P, lens, splits):
+def test_quant_decode_dense_matches_oracle(fmt, d, Hq, Hkv, P, lens, splits):
     _lib()
     case = W.Case("dense8", B=len(lens), Hq=Hq, Hkv=Hkv, d=d, P=P, lens=lens,
                   seed=hash((d, Hq, P, tuple(lens))) % 1000 + 1)
-    cache = _cache(case)
+    cache = _cache(case, fmt)
     q = case.q(0, DEV)
     out = torch.full((case.B, Hq, d), float("nan"), device=DEV)
     m_g = torch.full((case.B, Hq), float("nan"), device=DEV)
@@ -180,22 +199,23 @@ def test_fp8_decode_dense_matches_oracle(d, Hq, Hkv, P, lens, splits):
     cache.decode(q, out, ws, m_g=m_g, e_g=e_g, num_splits=splits)
     torch.cuda.synchronize()
     assert int(cache.dev_err.item()) == 0
-    _check(_ref_dense(case, q, cache.lens), out, m_g, e_g, cache.lens, "fp8 decode")
+    _check(_ref_dense(case, q, cache.lens, fmt), out, m_g, e_g, cache.lens, f"{fmt} decode")
     out2 = torch.empty_like(out)
     cache.decode(q, out2, ws, num_splits=splits)
     torch.cuda.synchronize()
     assert torch.equal(out, out2)
 
 
+@pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("q_exp", [-40, 0, 40])
-def test_fp8_decode_wide_value_ranges(q_exp):
+def test_quant_decode_wide_value_ranges(fmt, q_exp):
     """Row scales spread over 2^-30..2^30 (the V-scale bound r is raised many times inside a
     piece), rows that quantize to subnormals and zeros, and queries far outside the fp16
     range (the per-piece power-of-two query scaling)."""
     dattn = _lib()
     case = W.Case("wide8", B=2, Hq=8, Hkv=2, d=128, P=16, lens=[0, 0], seed=2,
                   reserve_tokens=700)
-    cache = _cache(case, fill=False)
+    cache = _cache(case, fmt, fill=False)
     lens = [600, 77]
     kv = []
     for b, L in enumerate(lens):
@@ -221,7 +241,7 @@ def test_fp8_decode_wide_value_ranges(q_exp):
     qb = oracle.bf16_bits(q)
     o, mg, eg = out.cpu().numpy(), m_g.cpu().numpy(), e_g.cpu().numpy()
     for b in range(case.B):
-        Kd, Vd = _deq(*kv[b])
+        Kd, Vd = _deq(*kv[b], fmt)
         for h in range(case.Hq):
             kvh = h // case.g
             r, rm, re = oracle.attention_f64(qb[b, h], Kd[:, kvh], Vd[:, kvh], scale)
@@ -232,14 +252,15 @@ def test_fp8_decode_wide_value_ranges(q_exp):
             assert_e_close(eg[b, h], re, f"b={b} h={h}")
 
 
-# ---------------------------------------------------------------- 8-bit partials and merge
+# ---------------------------------------------------------------- quantized partials and merge
 
+@pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("seed", [0, 1])
-def test_fp8_partial_then_merge(seed):
+def test_quant_partial_then_merge(fmt, seed):
     """Batch 1, 8 q / 2 KV heads, d 64, 4096 tokens, 4 chunks of 1024 (identity table)."""
     dattn = _lib()
     case = W.dense_tiny(seed=seed)
-    cache = _cache(case)
+    cache = _cache(case, fmt)
     q = case.q(0, DEV)
     pages_per_chunk = case.chunk_tokens // case.P
     C = 4
@@ -262,7 +283,7 @@ def test_fp8_partial_then_merge(seed):
     torch.cuda.synchronize()
     assert int(cache.dev_err.item()) == 0
     K, V = host_kv(case, 0, 4096, DEV)
-    Kd, Vd = _deq(K, V)
+    Kd, Vd = _deq(K, V, fmt)
     qb = oracle.bf16_bits(q)
     for h in range(case.Hq):
         kvh = h // case.g
@@ -274,18 +295,19 @@ def test_fp8_partial_then_merge(seed):
             assert_e_close(e[c, h].item(), re, f"chunk {c} head {h}")
             assert_out_close(MA[c, h].cpu().numpy() / e[c, h].item(), rMA / re,
                              f"chunk {c} head {h}")
-    _check(_ref_dense(case, q, [4096]), out, m_g, e_g, [4096], "fp8 merged")
+    _check(_ref_dense(case, q, [4096], fmt), out, m_g, e_g, [4096], f"{fmt} merged")
 
 
-# ---------------------------------------------------------------- 8-bit block-sparse decode
+# ---------------------------------------------------------------- quantized block-sparse decode
 
+@pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("P,lens,splits", [(64, [64 * 200 + 5, 3000, 12, 5], 0),
                                            (16, [2000, 700], 9)])
-def test_fp8_sparse_decode_matches_oracle_token_sets(P, lens, splits):
+def test_quant_sparse_decode_matches_oracle_token_sets(fmt, P, lens, splits):
     _lib()
     case = W.Case("sparse8", B=len(lens), Hq=16, Hkv=4, d=128, P=P, lens=lens, seed=21,
                   head_kind=[1, 2, 1, 2], top_k=16, sinks=4, local=8, n_highsim=6)
-    cache = _cache(case, with_stats=True)
+    cache = _cache(case, fmt, with_stats=True)
     q0 = case.q(0, DEV)
     sel = torch.empty(case.B, case.Hkv, case.top_k, dtype=torch.int32, device=DEV)
     cache.select(q0, sel, cache.workspace(top_k=case.top_k))
@@ -317,7 +339,7 @@ def test_fp8_sparse_decode_matches_oracle_token_sets(P, lens, splits):
         o, mg, eg = out.cpu().numpy(), m_g.cpu().numpy(), e_g.cpu().numpy()
         for b in range(case.B):
             L = cache.lens[b]
-            Kd, Vd = _deq(*host_kv(case, b, L, DEV))
+            Kd, Vd = _deq(*host_kv(case, b, L, DEV), fmt)
             for h in range(case.Hq):
                 kvh = h // case.g
                 rows = oracle.sparse_rows(case.head_kind[kvh], L, P, want_sel[b, kvh],
@@ -329,10 +351,11 @@ def test_fp8_sparse_decode_matches_oracle_token_sets(P, lens, splits):
                 assert_e_close(eg[b, h], re, f"step {step} b={b} h={h}")
 
 
-def test_fp8_decode_flags_unmapped_page_without_fault():
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_quant_decode_flags_unmapped_page_without_fault(fmt):
     dattn = _lib()
     case = W.Case("unm8", B=1, Hq=4, Hkv=4, d=128, P=16, lens=[100], seed=2)
-    cache = _cache(case)
+    cache = _cache(case, fmt)
     cache.block_table[0, 2] = -1
     cache.block_table[0, 3] = case.num_pages + 5
     q = case.q(0, DEV)
@@ -342,7 +365,7 @@ def test_fp8_decode_flags_unmapped_page_without_fault():
     err = int(cache.dev_err.item())
     assert err & dattn.DEVERR["UNMAPPED_PAGE"] and err & dattn.DEVERR["PAGE_OOB"]
     K, V = host_kv(case, 0, 100, DEV)
-    Kd, Vd = _deq(K, V)
+    Kd, Vd = _deq(K, V, fmt)
     rows = [t for t in range(100) if t // 16 not in (2, 3)]
     qb = oracle.bf16_bits(q)
     for h in range(4):
