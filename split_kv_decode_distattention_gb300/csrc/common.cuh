@@ -268,13 +268,23 @@ __device__ __forceinline__ uint32_t swz_rows(uint32_t row, uint32_t chunk) {
 }
 
 // The 4-bit codes at nibble K of each 16-bit half of x (bits 4K..4K+3 and 16+4K..16+4K+3,
-// each code stored as code + 8) as two exact fp16 values: 0x6400 | n is the fp16 value
-// 1024 + n, and subtracting 1032 leaves n - 8.
+// each code stored as n = code + 8) as two exact fp16 values. Nibbles 2 and 3 are first
+// shifted down by 8 bits (one shift serves both). A nibble in bits 0-3 ORed into 0x6400 is
+// the fp16 value 1024 + n, and subtracting 1032 leaves n - 8. A nibble in bits 4-7 ORed into
+// 0x6400 is 1024 + 16n, and (1024 + 16n) / 16 - 72 = n - 8 in one fused multiply-add. Every
+// step is exact: the values are integers well inside fp16's 11-bit significand.
 template <int K>
 __device__ __forceinline__ uint32_t i4pair_to_f16(uint32_t x) {
-    const uint32_t v = ((x >> (4 * K)) & 0x000f000fu) | 0x64006400u;
+    const uint32_t y = K >= 2 ? x >> 8 : x;
     uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x64086408u));
+    if constexpr ((K & 1) == 0) {
+        const uint32_t v = (y & 0x000f000fu) | 0x64006400u;
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x64086408u));
+    } else {
+        const uint32_t v = (y & 0x00f000f0u) | 0x64006400u;
+        // 0x2C00 = 1/16, 0xD480 = -72
+        asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(0x2C002C00u), "r"(0xD480D480u));
+    }
     return r;
 }
 
