@@ -575,19 +575,19 @@ struct Consumer {
         }
     }
 
-    // One 16-token tile of the 4-bit pool in stage buffer `st` (K codes, then V codes, rows of
-    // d/2 bytes, two codes per byte) with its row scales `sc`; rows are masked as in tile().
-    // The scales enter exactly as in tile_f8; every code converts exactly to fp16.
-    __device__ void tile_i4(uint32_t st, const float* sc, int lo, int hi, int cut) {
-        constexpr uint32_t RB = D / 2;  // bytes of a row
-        const uint32_t kbase = st, vbase = st + 16u * RB;
-        const int g8 = lane >> 2;
+    // ---- 4-bit pool ------------------------------------------------------------------
+    // A tile in a stage buffer is K codes then V codes, rows of d/2 bytes (two codes per
+    // byte), with its row scales in `sc`; the scales enter exactly as in tile_f8, and every
+    // code converts exactly to fp16.
+
+    // S^T = K Q^T of one tile into two accumulator chains: a thread's ldmatrix register holds
+    // 8 adjacent channels of one token, and nibble pairs (k, k + 4) form the fragments in the
+    // order load_q takes the query.
+    __device__ __forceinline__ void qk_i4(uint32_t kbase, float (&sa)[4], float (&sb)[4]) const {
+        constexpr uint32_t RB = D / 2;
         // ldmatrix lane addresses: matrices (rows 0-7 | 8-15) x (chunk 2c | 2c + 1)
         const uint32_t row = (lane & 7) + ((lane >> 3) & 1) * 8;
         const uint32_t csel = lane >> 4;
-        // ---- S^T = K Q^T: a thread's register holds 8 adjacent channels of one token; nibble
-        // pairs (k, k + 4) form the fragments in the order load_q takes the query ------
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
             uint32_t r0, r1, r2, r3;  // chunk 2c: tokens g8, g8 + 8; chunk 2c + 1: the same
@@ -601,21 +601,11 @@ struct Consumer {
             mma_f16(sb, i4pair_to_f16<2>(r2), i4pair_to_f16<2>(r3), i4pair_to_f16<3>(r2),
                     i4pair_to_f16<3>(r3), qf[4 * c + 3][0], qf[4 * c + 3][1]);
         }
-        const bool v0 = g8 >= lo && g8 < hi, v1 = g8 + 8 >= lo && g8 + 8 < hi;
-        const float kc0 = sc[g8] * qsc, kc1 = sc[g8 + 8] * qsc;
-        bool a0, a1, a2, a3;
-        visible(lo, hi, cut, a0, a1, a2, a3);
-        const float s0 = a0 ? (sa[0] + sb[0]) * kc0 : kNegInf;
-        const float s1 = a1 ? (sa[1] + sb[1]) * kc0 : kNegInf;
-        const float s2 = a2 ? (sa[2] + sb[2]) * kc1 : kNegInf;
-        const float s3 = a3 ? (sa[3] + sb[3]) * kc1 : kNegInf;
-        float p0, p1, p2, p3;
-        softmax(s0, s1, s2, s3, p0, p1, p2, p3);
-        // ---- V scales: raise r to a power of two >= every V scale of the tile ---------
-        const float vs0 = v0 ? sc[16 + g8] : 0.f, vs1 = v1 ? sc[24 + g8] : 0.f;
-        float vt = fmaxf(vs0, vs1);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) vt = fmaxf(vt, __shfl_xor_sync(0xffffffffu, vt, off));
+    }
+
+    // Raises r to a power of two >= vt (the largest V scale of the tiles at hand, reduced over
+    // the warp), rescaling O, exactly as tile_f8 does.
+    __device__ __forceinline__ void raise_r(float vt) {
         if (vt > rv) {  // warp-uniform; vt > 2^-112 is a normal number
             const int32_t bits = __float_as_int(vt);
             const int32_t k = min(127, ((bits >> 23) & 0xff) - 127 + ((bits & 0x7fffff) != 0));
@@ -629,21 +619,25 @@ struct Consumer {
             rv = __int_as_float((127 + k) << 23);
             inv = __int_as_float((142 - k) << 23);
         }
-        const float vn0 = vs0 * inv, vn1 = vs1 * inv;  // in [0, 2^15], exact
-        const float w0 = p0 * vn0, w1 = p1 * vn0, w2 = p2 * vn1, w3 = p3 * vn1;
-        // ---- W^T as the B operand: two fp16 terms, transposed with movmatrix ----------
+    }
+
+    // O^T += V^T W^T for one tile with this lane's weights (rows g8: w0, w1; g8 + 8: w2, w3).
+    // After the transposing ldmatrix a thread holds tokens 2tig, 2tig + 1 (r0, r2) or
+    // 8 + 2tig, 9 + 2tig (r1, r3) of channels 4g8 .. 4g8 + 3 of a 32-channel chunk, and nibble
+    // k of both halves is channel 4g8 + k of the two tokens: exactly an A fragment. M-tile mt
+    // takes channels 32 (mt / 2) + 4g8 + 2 (mt % 2) + {0, 1} as its rows g8 and g8 + 8. Every
+    // code is a finite value, so a masked row (weight 0) needs no zeroing.
+    __device__ __forceinline__ void pv_i4(uint32_t vbase, float w0, float w1, float w2,
+                                          float w3) {
+        constexpr uint32_t RB = D / 2;
+        const uint32_t row = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const uint32_t csel = lane >> 4;
+        // W^T as the B operand: two fp16 terms, transposed with movmatrix
         const uint32_t h01 = pack_f16(w0, w1), h23 = pack_f16(w2, w3);
         const uint32_t l01 = pack_f16(w0 - f16_lo(h01), w1 - f16_hi(h01));
         const uint32_t l23 = pack_f16(w2 - f16_lo(h23), w3 - f16_hi(h23));
         const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
         const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
-        // ---- O^T += V^T W^T ------------------------------------------------------------
-        // After the transposing ldmatrix a thread holds tokens 2tig, 2tig + 1 (r0, r2) or
-        // 8 + 2tig, 9 + 2tig (r1, r3) of channels 4g8 .. 4g8 + 3 of a 32-channel chunk, and
-        // nibble k of both halves is channel 4g8 + k of the two tokens: exactly an A
-        // fragment. M-tile mt takes channels 32 (mt / 2) + 4g8 + 2 (mt % 2) + {0, 1} as its
-        // rows g8 and g8 + 8. Every code is a finite value, so a masked row (weight 0)
-        // needs no zeroing.
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
             uint32_t r0, r1, r2, r3;
@@ -673,6 +667,97 @@ struct Consumer {
                 mma_f16(o[4 * c + 3], x0, x1, x2, x3, bl0, bl1);
             }
         }
+    }
+
+    // Largest V scale of this lane's visible rows, reduced over the warp's row groups.
+    __device__ __forceinline__ float warp_vmax(float v) const {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+        return v;
+    }
+
+    // One tile of the 4-bit pool; rows are masked as in tile().
+    __device__ void tile_i4(uint32_t st, const float* sc, int lo, int hi, int cut) {
+        const int g8 = lane >> 2;
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        qk_i4(st, sa, sb);
+        const bool v0 = g8 >= lo && g8 < hi, v1 = g8 + 8 >= lo && g8 + 8 < hi;
+        const float kc0 = sc[g8] * qsc, kc1 = sc[g8 + 8] * qsc;
+        bool a0, a1, a2, a3;
+        visible(lo, hi, cut, a0, a1, a2, a3);
+        const float s0 = a0 ? (sa[0] + sb[0]) * kc0 : kNegInf;
+        const float s1 = a1 ? (sa[1] + sb[1]) * kc0 : kNegInf;
+        const float s2 = a2 ? (sa[2] + sb[2]) * kc1 : kNegInf;
+        const float s3 = a3 ? (sa[3] + sb[3]) * kc1 : kNegInf;
+        float p0, p1, p2, p3;
+        softmax(s0, s1, s2, s3, p0, p1, p2, p3);
+        const float vs0 = v0 ? sc[16 + g8] : 0.f, vs1 = v1 ? sc[24 + g8] : 0.f;
+        raise_r(warp_vmax(fmaxf(vs0, vs1)));
+        const float vn0 = vs0 * inv, vn1 = vs1 * inv;  // in [0, 2^15], exact
+        pv_i4(st + 8u * D, p0 * vn0, p1 * vn0, p2 * vn1, p3 * vn1);
+    }
+
+    // Online softmax (base 2) over two tiles' logits at once (s[0..3] tile A, s[4..7] tile B,
+    // in softmax()'s order): one reduction of the running max for 32 rows.
+    __device__ __forceinline__ void softmax2(const float (&s)[8], float (&pr)[8]) {
+        float c0 = fmaxf(fmaxf(s[0], s[2]), fmaxf(s[4], s[6]));
+        float c1 = fmaxf(fmaxf(s[1], s[3]), fmaxf(s[5], s[7]));
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            c0 = fmaxf(c0, __shfl_xor_sync(0xffffffffu, c0, off));
+            c1 = fmaxf(c1, __shfl_xor_sync(0xffffffffu, c1, off));
+        }
+        const float mn0 = fmaxf(m0, c0), mn1 = fmaxf(m1, c1);
+        const float mu0 = mn0 == kNegInf ? 0.f : mn0, mu1 = mn1 == kNegInf ? 0.f : mn1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pr[i] = exp2f(s[i] - ((i & 1) ? mu1 : mu0));
+        if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
+            const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
+            e0 *= al0;
+            e1 *= al1;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+            }
+        }
+        m0 = mn0;
+        m1 = mn1;
+        e0 += (pr[0] + pr[2]) + (pr[4] + pr[6]);
+        e1 += (pr[1] + pr[3]) + (pr[5] + pr[7]);
+    }
+
+    // Two consecutive tiles A and B of the 4-bit pool with one softmax and one V-scale
+    // update: the same results as tile_i4 on A, then on B, up to rounding order.
+    __device__ void tile2_i4(uint32_t stA, const float* scA, int loA, int hiA, int cutA,
+                             uint32_t stB, const float* scB, int loB, int hiB, int cutB) {
+        const int g8 = lane >> 2;
+        float saA[4] = {0.f, 0.f, 0.f, 0.f}, sbA[4] = {0.f, 0.f, 0.f, 0.f};
+        float saB[4] = {0.f, 0.f, 0.f, 0.f}, sbB[4] = {0.f, 0.f, 0.f, 0.f};
+        qk_i4(stA, saA, sbA);
+        qk_i4(stB, saB, sbB);
+        bool a0, a1, a2, a3, b0, b1, b2, b3;
+        visible(loA, hiA, cutA, a0, a1, a2, a3);
+        visible(loB, hiB, cutB, b0, b1, b2, b3);
+        const float kA0 = scA[g8] * qsc, kA1 = scA[g8 + 8] * qsc;
+        const float kB0 = scB[g8] * qsc, kB1 = scB[g8 + 8] * qsc;
+        const float s[8] = {a0 ? (saA[0] + sbA[0]) * kA0 : kNegInf,
+                            a1 ? (saA[1] + sbA[1]) * kA0 : kNegInf,
+                            a2 ? (saA[2] + sbA[2]) * kA1 : kNegInf,
+                            a3 ? (saA[3] + sbA[3]) * kA1 : kNegInf,
+                            b0 ? (saB[0] + sbB[0]) * kB0 : kNegInf,
+                            b1 ? (saB[1] + sbB[1]) * kB0 : kNegInf,
+                            b2 ? (saB[2] + sbB[2]) * kB1 : kNegInf,
+                            b3 ? (saB[3] + sbB[3]) * kB1 : kNegInf};
+        float pr[8];
+        softmax2(s, pr);
+        const float vA0 = g8 >= loA && g8 < hiA ? scA[16 + g8] : 0.f;
+        const float vA1 = g8 + 8 >= loA && g8 + 8 < hiA ? scA[24 + g8] : 0.f;
+        const float vB0 = g8 >= loB && g8 < hiB ? scB[16 + g8] : 0.f;
+        const float vB1 = g8 + 8 >= loB && g8 + 8 < hiB ? scB[24 + g8] : 0.f;
+        raise_r(warp_vmax(fmaxf(fmaxf(vA0, vA1), fmaxf(vB0, vB1))));
+        const float nA0 = vA0 * inv, nA1 = vA1 * inv, nB0 = vB0 * inv, nB1 = vB1 * inv;
+        pv_i4(stA + 8u * D, pr[0] * nA0, pr[1] * nA0, pr[2] * nA1, pr[3] * nA1);
+        pv_i4(stB + 8u * D, pr[4] * nB0, pr[5] * nB0, pr[6] * nB1, pr[7] * nB1);
     }
 
     // Publishes this warp's state for the CTA-level merge of the piece.
@@ -717,8 +802,13 @@ struct Consumer {
     }
 };
 
+// Resident CTAs per SM the register budget is held to: three at d = 128, four at d = 64
+// (the 4-bit kernel processes tiles in pairs and would otherwise take more registers).
+template <int D>
+constexpr int attn_min_blocks() { return D == 64 ? 4 : 3; }
+
 template <int D, int FMT>
-__global__ void __launch_bounds__(kAttnThreads)
+__global__ void __launch_bounds__(kAttnThreads, attn_min_blocks<D>())
 attention_kernel(const __grid_constant__ AttnParams p,
                  const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v) {
@@ -965,8 +1055,49 @@ attention_kernel(const __grid_constant__ AttnParams p,
         if (have2) cons.load_q(s2, qn, qsn);
         cons.reset();
         const int32_t nr = r1 - r0;
+        if constexpr (FMT == DATTN_KV_INT4) {
+            // Tiles go to the warps in pairs: pair P holds the tiles 2P and 2P + 1 of the CTA's
+            // sequence, and warp P mod 4 takes it, so (the ring being a multiple of 8 stages)
+            // every stage keeps one owner. Both tiles of a pair inside this piece share one
+            // softmax and one V-scale update; a pair cut by the piece boundary is processed
+            // as the single tile this piece holds.
+            static_assert(NS % (2 * kConsumerWarps) == 0, "pairs of stages per consumer warp");
+            const int32_t k1 = kbase + nr;
+            int32_t P = kbase >> 1;
+            P += (warp - P % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
+            for (; 2 * P < k1; P += kConsumerWarps) {
+                const int32_t ka = 2 * P, kb = 2 * P + 1;
+                const bool ina = ka >= kbase, inb = kb < k1;
+                const int ga = ka % NS, gb = kb % NS;
+                bool oka = true, okb = true;
+                if (ina)
+                    oka = mbar_wait(sm.full_bar(ga), (ka / NS) & 1, sm.abort_flag(), p.dev_err);
+                if (inb)
+                    okb = mbar_wait(sm.full_bar(gb), (kb / NS) & 1, sm.abort_flag(), p.dev_err);
+                // warp-uniform: the tiles' ldmatrix / mma / movmatrix are warp-collective
+                const bool ok = __all_sync(0xffffffffu, oka && okb);
+                const int32_t la = ina ? sm.meta()[ga] : kTileSkip;
+                const int32_t lb = inb ? sm.meta()[gb] : kTileSkip;
+                const bool da = ok && !(la & kTileSkip), db = ok && !(lb & kTileSkip);
+                const uint32_t sta = stage0 + (uint32_t)ga * sm.L.stage_bytes;
+                const uint32_t stb = stage0 + (uint32_t)gb * sm.L.stage_bytes;
+                if (da && db) {
+                    cons.tile2_i4(sta, sm.scales(ga), tile_lo(la), tile_hi(la), tile_cut(la), stb,
+                                  sm.scales(gb), tile_lo(lb), tile_hi(lb), tile_cut(lb));
+                } else if (da) {
+                    cons.tile_i4(sta, sm.scales(ga), tile_lo(la), tile_hi(la), tile_cut(la));
+                } else if (db) {
+                    cons.tile_i4(stb, sm.scales(gb), tile_lo(lb), tile_hi(lb), tile_cut(lb));
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    if (ina) mbar_arrive(sm.empty_bar(ga));
+                    if (inb) mbar_arrive(sm.empty_bar(gb));
+                }
+            }
+        }
         for (int32_t i = (warp - kbase % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
-             i < nr; i += kConsumerWarps) {
+             FMT != DATTN_KV_INT4 && i < nr; i += kConsumerWarps) {
             const int32_t k = kbase + i;
             const int stg = k % NS;
             // warp-uniform: the tile's ldmatrix / mma / movmatrix are warp-collective
@@ -975,10 +1106,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
             const int32_t lohi = sm.meta()[stg];
             const int lo = tile_lo(lohi), hi = tile_hi(lohi), cut = tile_cut(lohi);
             if (ok && !(lohi & kTileSkip)) {
-                if constexpr (FMT == DATTN_KV_INT4) {
-                    cons.tile_i4(stage0 + (uint32_t)stg * sm.L.stage_bytes, sm.scales(stg), lo, hi,
-                                 cut);
-                } else if constexpr (Q) {
+                if constexpr (Q) {
                     cons.tile_f8(stage0 + (uint32_t)stg * sm.L.stage_bytes, sm.scales(stg), lo, hi,
                                  cut);
                 } else {
