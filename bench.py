@@ -270,6 +270,21 @@ def traffic_record(config: str):
 
 # ------------------------------------------------------------------------------ GPU arm
 
+def reduce_over_ranks(ms_total: float, units: float, world: int, device) -> tuple:
+    """Whole-job figures of a run on `world` ranks, each timing its own replica of the
+    workload (weak scaling): the slowest rank's time and the units (bytes or flops) of all
+    ranks. Collective over the default process group when world > 1."""
+    if world <= 1:
+        return ms_total, units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms_total, float(units)], dtype=torch.float64, device=device)
+    tmax = t.clone()
+    dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(tmax[0]), float(t[1])
+
+
 KERNEL_EVERY = 8  # steps between the ones whose decode kernel is timed on its own
 
 
@@ -439,15 +454,7 @@ def run_dattn(args, rank: int, world: int):
     err = int(cache.dev_err.item())
     if err:
         raise RuntimeError(f"device error word {err:#x}")
-    ms_total = sum(step_t)
-    if world > 1:
-        t = torch.tensor([ms_total, float(bytes_total)], dtype=torch.float64, device=dev)
-        tmax = t.clone()
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        ms_max, bytes_all = float(tmax[0]), float(t[1])
-    else:
-        ms_max, bytes_all = ms_total, float(bytes_total)
+    ms_max, bytes_all = reduce_over_ranks(sum(step_t), float(bytes_total), world, dev)
     res = {
         "l2_policy": (f"flushed before every timed step ({L2Flush.TEXT})" if do_flush else
                       f"inputs larger than L2: {sb0['decode'] / 1e9:.2f} GB of K/V per step "
@@ -967,8 +974,11 @@ def run_prefill(args, rank: int, world: int):
     for _ in range(args.warmup):
         cache.seq_lens.zero_()
         step()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(dev.index) if not args.no_clocks else None
+    clocks = ClockSampler(dev.index) if (rank == 0 and not args.no_clocks) else None
     if clocks:
         clocks.start()
     times, kern = [], []
@@ -983,16 +993,20 @@ def run_prefill(args, rank: int, world: int):
         times.append((e0, e1))
         kern.append(kev)
     torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
     clk = clocks.stop() if clocks else None
     err = int(cache.dev_err.item())
     if err:
         raise RuntimeError(f"device error word {err:#x}")
     step_ms = [a.elapsed_time(b) for a, b in times]
     kern_ms = [a.elapsed_time(b) for a, b in kern]
-    ms = sum(step_ms) / len(step_ms)
+    # whole job: the slowest rank's time, every rank's flops
+    ms_all, flops_all = reduce_over_ranks(sum(step_ms), flops * len(step_ms), world, dev)
+    ms = ms_all / len(step_ms)
     kms = sum(kern_ms) / len(kern_ms)
-    res = {"flops": flops, "ms": ms, "kms": kms, "kern_ms": kern_ms, "clocks": clk,
-           "case": case, "Tq": Tq}
+    res = {"flops": flops_all / len(step_ms), "flops_rank": flops, "ms": ms, "kms": kms,
+           "kern_ms": kern_ms, "clocks": clk, "case": case, "Tq": Tq}
     # end to end: the chunk's q and K/V from pinned host memory, out back to pinned memory
     if not args.no_e2e:
         hq, hk, hv = q.cpu().pin_memory(), kn.cpu().pin_memory(), vn.cpu().pin_memory()
@@ -1077,7 +1091,7 @@ def prefill_main(args, rank: int, world: int):
         pass
     peak = float(peaks.get("bf16_tflops", 1900.0))
     tflops = res["flops"] / (res["ms"] * 1e-3) / 1e12
-    ktf = res["flops"] / (res["kms"] * 1e-3) / 1e12
+    ktf = res["flops_rank"] / (res["kms"] * 1e-3) / 1e12
     cfg = {"workload": f"{case.name}: {WORKLOAD_TEXT[case.name]}" +
                        (" (every head dense: causal attention)" if dense else ""),
            "batch": case.B, "q_heads": case.Hq, "kv_heads": case.Hkv, "head_dim": case.d,
@@ -1096,7 +1110,7 @@ def prefill_main(args, rank: int, world: int):
                      "achieved": round(ktf, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(ktf / peak, 4),
                      "peak_source": "measured" if "bf16_tflops" in peaks else "fallback",
-                     "traffic": None, "algorithmic_flops_per_launch": int(res["flops"]),
+                     "traffic": None, "algorithmic_flops_per_launch": int(res["flops_rank"]),
                      "avg_launch_ms": round(res["kms"], 4),
                      "kernel_timing": "CUDA events around the prefill kernel in every step"},
         # the chunk's append is two launches (the kernel, then the length update), then one
