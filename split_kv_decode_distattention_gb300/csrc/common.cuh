@@ -276,12 +276,15 @@ __device__ __forceinline__ uint32_t swz_rows(uint32_t row, uint32_t chunk) {
 template <int K>
 __device__ __forceinline__ uint32_t i4pair_to_f16(uint32_t x) {
     const uint32_t y = K >= 2 ? x >> 8 : x;
+    // (y & mask) | 0x6400 in both halves as one three-input logic operation (LUT 0xEA)
+    uint32_t v;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;"
+        : "=r"(v)
+        : "r"(y), "r"((K & 1) == 0 ? 0x000f000fu : 0x00f000f0u), "r"(0x64006400u));
     uint32_t r;
     if constexpr ((K & 1) == 0) {
-        const uint32_t v = (y & 0x000f000fu) | 0x64006400u;
         asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x64086408u));
     } else {
-        const uint32_t v = (y & 0x00f000f0u) | 0x64006400u;
         // 0x2C00 = 1/16, 0xD480 = -72
         asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(0x2C002C00u), "r"(0xD480D480u));
     }
