@@ -8,23 +8,27 @@
 // iterator, so the compute loop has no branches on the mask.
 //
 // GB300 design: the contraction runs on the 5th-generation tensor cores. One CTA takes 128
-// query rows (two 64-token query blocks) of one query head; the g heads of a KV head are
-// neighbouring CTAs, so their K/V reads meet in L2, and a request's last rows (the most key
-// blocks under the causal mask) start first. The key blocks both query blocks keep are built
-// into shared-memory bitmaps, and every role walks their union in the same order: the block
-// iterator. Six warps:
-//   - a producer warp streams each key block's four 16-token tiles by TMA, one lane per
-//     tile, into a two-stage ring (K and V as [d/64 halves][64 rows][128 B] with the 128-byte
-//     swizzle, one box per half and tile);
+// query rows: one 64-token query block of two query heads of a KV head when the group is
+// even (both halves keep the same key blocks), else two query blocks of one query head. The
+// heads of a KV head are neighbouring CTAs, so their K/V reads meet in L2, and a request's
+// last rows (the most key blocks under the causal mask) start first. The key blocks each
+// half keeps are built into shared-memory bitmaps, and every role walks their union in the
+// same order: the block iterator. Seven warps:
+//   - two producer warps, one for K and one for V, stream each key block's four 16-token
+//     tiles by TMA (as [d/64 halves][64 rows][128 B] with the 128-byte swizzle, one box per
+//     half and tile) into a two-stage K ring and a three-stage V ring; each resolves the
+//     pages of eight blocks at once, one lane per tile, and the K warp also publishes each
+//     block's metadata (index, which half keeps it, tile lengths);
 //   - one thread issues tcgen05.mma: S = Q K^T (M 128, N 64, K d; Q and K from shared
 //     memory, fp32 accumulator in tensor memory, double-buffered so the next block's scores
 //     are computed during this block's softmax), then O += P V (M 128, N d, K 64; P from
 //     tensor memory, V from shared memory as an MN-major operand), and commits each to an
-//     mbarrier;
+//     mbarrier; K's stage is released when S is done, V's when P V is;
 //   - four warps hold one query row per thread: they read the row's 64 scores from tensor
-//     memory, mask them (the row's query block keeps the block, the key is written and at or
-//     before the query), keep the online softmax in base 2 and write P back into the score
-//     buffer as two bf16 terms (hi + lo, 16 significant bits), which the PV product reads.
+//     memory, mask them (the row's half keeps the block, the key is written and at or before
+//     the query), keep the online softmax in base 2 on packed fp32 pairs and write P back
+//     into the score buffer as two bf16 terms (hi: p cut to 16 bits; lo: the rest, rounded),
+//     which the PV product reads.
 // O is rescaled lazily, only when a row's maximum grows by more than 2^8, so most blocks touch
 // tensor memory only through the products. No CTA depends on another: no workspace, no merge.
 #include <cudaTypedefs.h>
@@ -50,7 +54,10 @@ struct PfParams {
     int32_t B, Tq, Hq, g;
     float sl2;  // scale * log2(e)
     const int32_t* seq_lens;
-    int32_t nqb;  // query-block slots per (request, head): ceil(Tq / 64) + 1
+    int32_t nqb;  // 128-row tiles per (request, head slot) a chunk can touch
+    // 1: a CTA's 128 rows are one 64-token query block of two query heads of one KV head
+    // (even g; both halves keep the same key blocks); 0: two query blocks of one query head
+    int32_t head_pairs;
     // block sparsity (head_kind == nullptr: dense causal)
     const int8_t* head_kind;
     int32_t sink_blocks, local_blocks, max_sel, qblock_stride;
@@ -326,11 +333,16 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
         if (tid == 0) set_err(p.dev_err, DATTN_DEVERR_SMEM_ALIGN);
         return;
     }
+    // CTA -> (request b, head slot hs, tile J): the head slots of a KV head are neighbouring
+    // CTAs, so their K/V reads meet in L2, and a request's last tiles start first
+    const bool hp = p.head_pairs != 0;
+    const int32_t nslots = hp ? p.Hq / 2 : p.Hq;
     int32_t c = blockIdx.x;
-    const int32_t h = c % p.Hq;
-    c /= p.Hq;
-    const int32_t J = p.nqb - 1 - c % p.nqb;  // 128-row tile; the last ones start first
+    const int32_t hs = c % nslots;
+    c /= nslots;
+    const int32_t J = p.nqb - 1 - c % p.nqb;
     const int32_t b = c / p.nqb;
+    const int32_t h = hp ? 2 * hs : hs;  // the query head of rows 0-63 (rows 64-127: h + hp)
     const uint32_t bars = smem_u32(base + L.bars);
     // K and V stages are tracked apart: K_j's stage is free once S_j is computed, V_j's once
     // P_j V_j is, so the next key blocks' K loads run during this block's softmax.
@@ -386,12 +398,17 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
     // ---- the CTA's query rows and key blocks (uniform over the CTA) --------------------------
     const int32_t Ln = p.seq_lens[b];
     bool active = Ln >= p.Tq && Ln <= p.max_pages * p.P;
-    if (!active && tid == 0 && h == 0 && J == 0) set_err(p.dev_err, DATTN_DEVERR_LEN_OOB);
+    if (!active && tid == 0 && hs == 0 && J == 0) set_err(p.dev_err, DATTN_DEVERR_LEN_OOB);
     const int32_t c0 = Ln - p.Tq;
-    const int32_t qa = (active ? c0 : 0) / kPfBlock + 2 * J;
-    const int32_t p_lo = max(c0, qa * kPfBlock), p_hi = min(Ln, qa * kPfBlock + kTcRows);
+    // Query block qa holds rows 0-63. Without head pairs rows 64-127 are block qa + 1 of the
+    // same head; with head pairs they are block qa of head h + 1. Row r sits at position
+    // qa * 64 + r (qa * 64 + r % 64 with head pairs), and the chunk's rows of the tile are the
+    // positions in [p_lo, p_hi).
+    const int32_t qa = (active ? c0 : 0) / kPfBlock + (hp ? J : 2 * J);
+    const int32_t p_lo = max(c0, qa * kPfBlock);
+    const int32_t p_hi = min(Ln, qa * kPfBlock + (hp ? kPfBlock : kTcRows));
     active = active && p_lo < p_hi;
-    const bool hasB = p_hi > (qa + 1) * kPfBlock;
+    const bool hasB = !hp && p_hi > (qa + 1) * kPfBlock;
     const int32_t kvh = h / p.g;
     if (active && p.head_kind != nullptr && p.head_kind[kvh] == DATTN_HEAD_RETRIEVAL &&
         (qa + (hasB ? 1 : 0)) >= p.qblock_stride) {
@@ -401,16 +418,21 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
     const int32_t nw = active ? (qa + 1 + 1 + 31) / 32 : 0;  // words over blocks 0 .. qa + 1
     if (active) {
         tc_build_bitmaps(p, b, kvh, qa, hasB, bmA, bmB, nw, tid);
+        if (hp) {  // both halves keep query block qa's key blocks
+            __syncthreads();
+            for (int32_t w = tid; w < nw; w += kTcThreads) bmB[w] = bmA[w];
+        }
         // the query rows, in the K tiles' swizzled layout ([half][row][128 B]); with a
         // negative scale the rows are negated (exact), so that the scores scale by |scale|
         const uint32_t qneg = p.sl2 < 0.f ? 0x80008000u : 0u;
         for (int idx = tid; idx < kTcRows * (D / 8); idx += kTcThreads) {
             const int r = idx / (D / 8), ch = idx - r * (D / 8);
-            const int32_t pos = qa * kPfBlock + r;
+            const int32_t pos = qa * kPfBlock + (hp ? (r & (kPfBlock - 1)) : r);
+            const int32_t hr = h + (hp && r >= kPfBlock ? 1 : 0);
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
             if (pos >= p_lo && pos < p_hi) {
                 v = __ldg(reinterpret_cast<const uint4*>(
-                    p.q + (((int64_t)b * p.Tq + (pos - c0)) * p.Hq + h) * D) + ch);
+                    p.q + (((int64_t)b * p.Tq + (pos - c0)) * p.Hq + hr) * D) + ch);
                 v = make_uint4(v.x ^ qneg, v.y ^ qneg, v.z ^ qneg, v.w ^ qneg);
             }
             *reinterpret_cast<uint4*>(base + L.q + (ch >> 3) * (kTcRows * 128u) +
@@ -601,7 +623,8 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
     } else if (active && warp < kTcSoftWarps) {
         // ---------------------------------------------------------------- softmax threads
         const int r = tid;  // this thread's query row and TMEM lane
-        const int32_t pos = qa * kPfBlock + r;
+        const int32_t pos = qa * kPfBlock + (hp ? (r & (kPfBlock - 1)) : r);
+        const int32_t hr = h + (hp && r >= kPfBlock ? 1 : 0);  // this row's query head
         const bool rowok = pos >= p_lo && pos < p_hi;
         const uint32_t rbit = r >= 64 ? 2u : 1u;
         const uint32_t lanes = (uint32_t)(32 * warp) << 16;
@@ -747,7 +770,7 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
             tc_fence_after();
         }
         ok = __all_sync(0xffffffffu, ok);
-        const int64_t row = ((int64_t)b * p.Tq + (rowok ? pos - c0 : 0)) * p.Hq + h;
+        const int64_t row = ((int64_t)b * p.Tq + (rowok ? pos - c0 : 0)) * p.Hq + hr;
         float* orow = p.out + row * D;
         const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
@@ -821,8 +844,13 @@ template <int D>
 dattn_status_t launch_prefill_tc_d(const PfParams& p0, const void* k_pool, const void* v_pool,
                                    cudaStream_t stream) {
     PfParams p = p0;
-    p.nqb = ((p.Tq + kPfBlock - 1) / kPfBlock + 2) / 2;  // 128-row tiles a chunk can touch
-    const int64_t ctas = (int64_t)p.B * p.nqb * p.Hq;
+    // Head pairs when a KV head has an even number of query heads: a tile is one query block
+    // (a chunk touches at most ceil(Tq / 64) + 1 of them) of two heads; otherwise two query
+    // blocks of one head.
+    p.head_pairs = (p.g % 2 == 0) ? 1 : 0;
+    const int32_t blocks = (p.Tq + kPfBlock - 1) / kPfBlock + 1;
+    p.nqb = p.head_pairs ? blocks : (blocks + 1) / 2;
+    const int64_t ctas = (int64_t)p.B * p.nqb * (p.head_pairs ? p.Hq / 2 : p.Hq);
     if (ctas >= (1ll << 31)) return DATTN_ERR_UNSUPPORTED;
     const int32_t nwords = (p.max_pages * p.P / kPfBlock + 2 + 31) / 32;
     const TcSmem L = tc_smem_layout(D, nwords);

@@ -99,14 +99,18 @@ def test_causal_prefill_matches_oracle(d, Hq, Hkv, P, lens, Tq):
     assert torch.equal(out, out2)
 
 
-@pytest.mark.parametrize("P,lens,Tq,sinks,local", [(16, [700, 333], 300, 1, 2),
-                                                   (64, [1024], 1024, 2, 3),
-                                                   (16, [200, 64], 64, 0, 1)])
-def test_block_sparse_prefill_matches_oracle(P, lens, Tq, sinks, local):
+@pytest.mark.parametrize("P,lens,Tq,sinks,local,Hq", [(16, [700, 333], 300, 1, 2, 8),
+                                                      (64, [1024], 1024, 2, 3, 8),
+                                                      (16, [200, 64], 64, 0, 1, 8),
+                                                      (16, [700, 333], 300, 1, 2, 12),
+                                                      (64, [1024], 1000, 2, 3, 4)])
+def test_block_sparse_prefill_matches_oracle(P, lens, Tq, sinks, local, Hq):
+    """Group 2 (a CTA takes one query block of two heads) and groups 3 and 1 (a CTA takes two
+    query blocks of one head)."""
     dattn = _lib()
     from split_kv_decode_distattention_gb300.harness import PagedCache
     kinds = [0, 1, 2, 1]
-    case = W.Case("bsprefill", B=len(lens), Hq=8, Hkv=4, d=128, P=P, lens=lens, seed=Tq + P)
+    case = W.Case("bsprefill", B=len(lens), Hq=Hq, Hkv=4, d=128, P=P, lens=lens, seed=Tq + P)
     cache = PagedCache(case, DEV)
     q = _queries(case, Tq, 6)
     stride = max(lens) // 64 + 1
