@@ -1,8 +1,9 @@
-"""Full-size parity of the five workloads, run in the launch configuration the benchmark
-times (automatic split count). Outputs are checked against the oracle on sampled
-(request, head) pairs, which the oracle computes one at a time. Properties that hold at any
-size are checked on everything: the page-set merge equals the fused decode, the selection
-is bit-exact, and no device error is flagged."""
+"""Full-size parity of the five workloads, of mha-32k over the 8-bit and 4-bit pools and of
+the 32K prefill, run in the launch configuration the benchmark times (automatic split
+count). Outputs are checked against the oracle on sampled (request, head) pairs or query
+rows, which the oracle computes one at a time. Properties that hold at any size are checked
+on everything: the page-set merge equals the fused decode, the selection is bit-exact, and
+no device error is flagged."""
 import numpy as np
 import pytest
 import torch
@@ -179,3 +180,75 @@ def test_sparse_512k_full_size(seed):
                                   case.sinks, case.local)
     pairs = [(0, 0), (0, 17), (3, 8), (7, 15), (7, 31), (5, 20)]
     _check_pairs(case, q, cache.lens, out, m_g, e_g, pairs, "sparse-512k", rows_of=rows_of)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int4"])
+def test_mha_32k_quantized_pools_full_size(fmt):
+    """mha-32k over the 8-bit and the 4-bit pool: the append quantizes the seeded rows, the
+    decode attends them; sampled pairs against the oracle's float64 attention over its own
+    dequantized rows."""
+    dattn = _lib()
+    case = W.mha_32k(seed=0)
+    kv_format = dattn.KV_FP8_E4M3 if fmt == "fp8" else dattn.KV_INT4
+    quant, deq = ((oracle.quantize_rows_fp8, oracle.dequantize_rows_fp8) if fmt == "fp8" else
+                  (oracle.quantize_rows_int4, oracle.dequantize_rows_int4))
+    cache = _cache(case, kv_format=kv_format)
+    q, out, m_g, e_g = _step(cache, case)
+    assert torch.isfinite(out).all()
+    qb = oracle.bf16_bits(q)
+    o, mg, eg = out.cpu().numpy(), m_g.cpu().numpy(), e_g.cpu().numpy()
+    for b, h in [(0, 0), (3, 17), (7, 31)]:
+        Ks, Vs = _host_heads(case, b, cache.lens[b], [h])
+        Kd, Vd = deq(*quant(Ks[0])), deq(*quant(Vs[0]))
+        r, rm, re = oracle.attention_f64(qb[b, h], Kd, Vd, case.scale)
+        assert_out_close(o[b, h], r, f"mha-32k {fmt} b={b} h={h}")
+        assert_m_close(mg[b, h], rm, f"mha-32k {fmt} b={b} h={h}")
+        assert_e_close(eg[b, h], re, f"mha-32k {fmt} b={b} h={h}")
+
+
+@pytest.mark.parametrize("dense", [False, True])
+def test_prefill_32k_full_size(dense):
+    """The 32K prefill exactly as the benchmark runs it: one 32K-token chunk, 32 q / 8 KV
+    heads, retrieval heads keeping a seeded 65% of the earlier blocks, streaming heads one
+    sink and 16 local blocks (or every head causal). Sampled query rows across the chunk
+    against the oracle's attention over their prefill rows."""
+    dattn = _lib()
+    from split_kv_decode_distattention_gb300.harness import PagedCache
+    case = W.prefill_32k(seed=0)
+    L = case.lens[0]
+    cache = PagedCache(case, DEV, fill=False)
+    q = case.prefill_queries(L, DEV)
+    K, V = case.kv(0, 0, L, DEV)
+    cache.append(K.unsqueeze(0).contiguous(), V.unsqueeze(0).contiguous())
+    del K, V
+    kinds = [0] * case.Hkv if dense else list(case.head_kind)
+    lists = case.prefill_block_lists(W.PREFILL_KEEP)
+    sinks, local = W.PREFILL_SINK_BLOCKS, W.PREFILL_LOCAL_BLOCKS
+    sp = None
+    if not dense:
+        sp = dattn.PrefillSparseConfig(torch.tensor(kinds, dtype=torch.int8, device=DEV), sinks,
+                                       local, torch.from_numpy(lists).to(DEV))
+    out = torch.empty(1, L, case.Hq, case.d, device=DEV)
+    m = torch.empty(1, L, case.Hq, device=DEV)
+    e = torch.empty_like(m)
+    dattn.dattn_prefill(cache.layout, cache.k_pool, cache.v_pool, q, case.scale, cache.seq_lens,
+                        out, m, e, sparse=sp, dev_err=cache.dev_err)
+    torch.cuda.synchronize()
+    assert int(cache.dev_err.item()) == 0
+    qb = oracle.bf16_bits(q[0, [0, 64, 5000, 20000, L - 1]])
+    ts = [0, 64, 5000, 20000, L - 1]
+    heads = [0, 5, 13, 18, 27, 31]  # KV heads 0, 1, 3 (retrieval) and 4, 6, 7 (streaming)
+    kvhs = sorted({h // case.g for h in heads})
+    Ks, Vs = _host_heads(case, 0, L, kvhs)
+    o, mm, ee = out[0, ts].cpu().numpy(), m[0, ts].cpu().numpy(), e[0, ts].cpu().numpy()
+    for i, t in enumerate(ts):
+        for h in heads:
+            kvh = h // case.g
+            blocks = lists[0, kvh, t // 64] if kinds[kvh] == W.HEAD_RETRIEVAL else None
+            rows = oracle.prefill_rows(kinds[kvh], L, L, t, sinks, local, blocks=blocks)
+            j = kvhs.index(kvh)
+            r, rm, re = oracle.attention(qb[i, h], Ks[j], Vs[j], case.scale, rows=rows)
+            tag = f"prefill-32k{' dense' if dense else ''} t={t} h={h}"
+            assert_out_close(o[i, h], r, tag)
+            assert_m_close(mm[i, h], rm, tag)
+            assert_e_close(ee[i, h], re, tag)
