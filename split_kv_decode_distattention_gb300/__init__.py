@@ -161,6 +161,27 @@ def _f32(t, name):
     return t
 
 
+def _size(t, n: int, name: str):
+    """A tensor argument must hold at least the n elements the call will touch: the kernels
+    see only a pointer, so a short tensor would be read or written past its end."""
+    if t is not None and t.numel() < n:
+        raise ValueError(f"{name} holds {t.numel()} elements; the call needs {n}")
+    return t
+
+
+def _layout_sizes(layout, B: int, k_pool, v_pool, stats=None):
+    """The pools, block table, scales and statistics must cover the layout for B requests."""
+    c = layout.c
+    row = c.head_dim // 2 if c.kv_format == KV_INT4 else c.head_dim
+    n = c.num_pages * c.num_kv_heads * c.page_size
+    _size(k_pool, n * row, "k_pool")
+    _size(v_pool, n * row, "v_pool")
+    _size(layout.block_table, B * c.max_pages_per_req, "block_table")
+    if c.kv_format in (KV_FP8_E4M3, KV_INT4):
+        _size(layout.kv_scale, 2 * n, "kv_scale")
+    _size(stats, n // 16 * 2 * c.head_dim, "stats")
+
+
 def _pool(layout, t, name):
     """A K or V pool must hold the layout's element type: bf16, uint8 E4M3 codes, or uint8
     bytes of two 4-bit codes."""
@@ -287,6 +308,10 @@ def dattn_kv_append(layout: KVLayout, k_pool, v_pool, stats, k_new, v_new, seq_l
     _pool(layout, k_pool, "k_pool"); _pool(layout, v_pool, "v_pool"); _bf16(stats, "stats")
     _bf16(k_new, "k_new"); _bf16(v_new, "v_new"); _i32(seq_lens, "seq_lens")
     B, T = k_new.shape[0], k_new.shape[1]
+    Hkv, d = layout.num_kv_heads, layout.head_dim
+    _layout_sizes(layout, B, k_pool, v_pool, stats)
+    _size(k_new, B * T * Hkv * d, "k_new"); _size(v_new, B * T * Hkv * d, "v_new")
+    _size(seq_lens, B, "seq_lens")
     _check(load_library().dattn_kv_append(
         ctypes.byref(layout.c), _ptr(k_pool), _ptr(v_pool), _ptr(stats), _ptr(k_new),
         _ptr(v_new), B, T, _ptr(seq_lens), _ptr(dev_err), _stream(stream)), "dattn_kv_append")
@@ -301,6 +326,11 @@ def dattn_partial(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, c
     _f32(m, "m"); _f32(e, "e"); _f32(MA, "MA")
     B, Hq = q.shape[0], q.shape[1]
     C = chunk_req.shape[0]
+    d = layout.head_dim
+    _layout_sizes(layout, B, k_pool, v_pool)
+    _size(q, B * Hq * d, "q"); _size(seq_lens, B, "seq_lens")
+    _size(chunk_page_indptr, C + 1, "chunk_page_indptr")
+    _size(m, C * Hq, "m"); _size(e, C * Hq, "e"); _size(MA, C * Hq * d, "MA")
     _check(load_library().dattn_partial(
         ctypes.byref(layout.c), _ptr(k_pool), _ptr(v_pool), _ptr(q), B, Hq, scale,
         _ptr(seq_lens), C, _ptr(chunk_req), _ptr(chunk_page_indptr), _ptr(chunk_pages),
@@ -317,9 +347,22 @@ def dattn_merge(chunk_indptr, m, e, MA, out=None, m_g=None, e_g=None, MA_g=None,
         _f32(t, n)
     B = chunk_indptr.shape[0] - 1
     C, Hq, d = MA.shape
+    _size(m, C * Hq, "m"); _size(e, C * Hq, "e")
+    _size(out, B * Hq * d, "out"); _size(m_g, B * Hq, "m_g"); _size(e_g, B * Hq, "e_g")
+    _size(MA_g, B * Hq * d, "MA_g")
     _check(load_library().dattn_merge(
         B, C, Hq, d, _ptr(chunk_indptr), _ptr(m), _ptr(e), _ptr(MA), _ptr(out), _ptr(m_g),
         _ptr(e_g), _ptr(MA_g), _ptr(dev_err), _stream(stream)), "dattn_merge")
+
+
+def _decode_sizes(layout, B, T, Hq, k_pool, v_pool, q, seq_lens, out, m_g, e_g, sparse):
+    d, Hkv = layout.head_dim, layout.num_kv_heads
+    _layout_sizes(layout, B, k_pool, v_pool)
+    _size(q, B * T * Hq * d, "q"); _size(out, B * T * Hq * d, "out")
+    _size(m_g, B * T * Hq, "m_g"); _size(e_g, B * T * Hq, "e_g"); _size(seq_lens, B, "seq_lens")
+    if sparse is not None:
+        _size(sparse.head_kind, Hkv, "head_kind")
+        _size(sparse.selected, B * Hkv * sparse.c.top_k, "selected")
 
 
 def dattn_decode(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, out,
@@ -328,6 +371,7 @@ def dattn_decode(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, ou
     """Fused split-KV decode: out fp32 [B][Hq][d] (+ m_g, e_g fp32 [B][Hq])."""
     _pool(layout, k_pool, "k_pool"); _pool(layout, v_pool, "v_pool"); _bf16(q, "q"); _i32(seq_lens, "seq_lens"); _f32(out, "out")
     B, Hq = q.shape[0], q.shape[1]
+    _decode_sizes(layout, B, 1, Hq, k_pool, v_pool, q, seq_lens, out, m_g, e_g, sparse)
     sp = ctypes.byref(sparse.c) if sparse is not None else None
     _check(load_library().dattn_decode(
         ctypes.byref(layout.c), _ptr(k_pool), _ptr(v_pool), _ptr(q), B, Hq, scale,
@@ -343,6 +387,7 @@ def dattn_decode_multi(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_le
     _pool(layout, k_pool, "k_pool"); _pool(layout, v_pool, "v_pool"); _bf16(q, "q")
     _i32(seq_lens, "seq_lens"); _f32(out, "out")
     B, T, Hq = q.shape[0], q.shape[1], q.shape[2]
+    _decode_sizes(layout, B, T, Hq, k_pool, v_pool, q, seq_lens, out, m_g, e_g, None)
     _check(load_library().dattn_decode_multi(
         ctypes.byref(layout.c), _ptr(k_pool), _ptr(v_pool), _ptr(q), B, T, Hq, scale,
         _ptr(seq_lens), num_splits, _ptr(ws.buffer), ws.buffer.numel(), _ptr(out), _ptr(m_g),
@@ -356,6 +401,13 @@ def dattn_prefill(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, o
     _pool(layout, k_pool, "k_pool"); _pool(layout, v_pool, "v_pool"); _bf16(q, "q")
     _i32(seq_lens, "seq_lens"); _f32(out, "out"); _f32(m, "m"); _f32(e, "e")
     B, Tq, Hq = q.shape[0], q.shape[1], q.shape[2]
+    _decode_sizes(layout, B, Tq, Hq, k_pool, v_pool, q, seq_lens, out, m, e, None)
+    if sparse is not None:
+        _size(sparse.head_kind, layout.num_kv_heads, "head_kind")
+        if sparse.block_lists is not None and (sparse.block_lists.dim() != 4 or
+                                               sparse.block_lists.shape[0] < B or
+                                               sparse.block_lists.shape[1] < layout.num_kv_heads):
+            raise ValueError("block_lists must be int32 [B][Hkv][qblock_stride][max_sel]")
     sp = ctypes.byref(sparse.c) if sparse is not None else None
     _check(load_library().dattn_prefill(
         ctypes.byref(layout.c), _ptr(k_pool), _ptr(v_pool), _ptr(q), B, Tq, Hq, scale,
@@ -374,6 +426,7 @@ def dattn_decode_noalloc(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_
     """
     _pool(layout, k_pool, "k_pool"); _pool(layout, v_pool, "v_pool"); _bf16(q, "q"); _i32(seq_lens, "seq_lens"); _f32(out, "out")
     B, Hq = q.shape[0], q.shape[1]
+    _decode_sizes(layout, B, 1, Hq, k_pool, v_pool, q, seq_lens, out, m_g, e_g, sparse)
     sp = ctypes.byref(sparse.c) if sparse is not None else None
     _check(load_library().dattn_decode_noalloc(
         ctypes.byref(layout.c), _ptr(k_pool), _ptr(v_pool), _ptr(q), B, Hq, scale,
@@ -386,6 +439,12 @@ def dattn_page_select(layout: KVLayout, stats, q, seq_lens, head_kind, top_k: in
     """Top-K physical pages per retrieval head into selected int32 [B][Hkv][top_k]."""
     _bf16(stats, "stats"); _bf16(q, "q"); _i32(seq_lens, "seq_lens"); _i32(selected, "selected")
     B, Hq = q.shape[0], q.shape[1]
+    c = layout.c
+    _size(stats, c.num_pages * c.num_kv_heads * (c.page_size // 16) * 2 * c.head_dim, "stats")
+    _size(layout.block_table, B * c.max_pages_per_req, "block_table")
+    _size(q, B * Hq * c.head_dim, "q"); _size(seq_lens, B, "seq_lens")
+    _size(head_kind, c.num_kv_heads, "head_kind")
+    _size(selected, B * c.num_kv_heads * top_k, "selected")
     _check(load_library().dattn_page_select(
         ctypes.byref(layout.c), _ptr(stats), _ptr(q), B, Hq, _ptr(seq_lens), _ptr(head_kind),
         top_k, _ptr(selected), _ptr(ws.buffer), ws.buffer.numel(), num_splits, _ptr(dev_err),

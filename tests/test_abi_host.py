@@ -214,3 +214,30 @@ def test_workspace_size(dattn):
     assert a == 256 + (100 + 64) * (4 * 128 + 8) * 4
     c = dattn.dattn_workspace_size(8, 24, 8, 128, 0, 100)  # g = 3: 6 -> 8 trailing floats
     assert c == 256 + (100 + 64) * (3 * 128 + 8) * 4
+
+
+def test_binding_rejects_short_tensors_before_any_call(dattn):
+    """The C entry points see only pointers, so the binding checks every tensor holds the
+    elements the call touches (these tensors live on the CPU: the check comes first)."""
+    import torch
+    lay = _lay(dattn)  # 8 pages x 2 KV heads x 16 tokens x d 128, block table [1][4]
+    pool = torch.zeros(8 * 2 * 16 * 128, dtype=torch.bfloat16)
+    short = torch.zeros(10, dtype=torch.bfloat16)
+    q = torch.zeros(1, 4, 128, dtype=torch.bfloat16)
+    seq = torch.zeros(1, dtype=torch.int32)
+    out = torch.zeros(1, 4, 128)
+    ws = type("W", (), {"buffer": torch.zeros(256, dtype=torch.uint8)})()
+    with pytest.raises(ValueError, match="k_pool"):
+        dattn.dattn_decode(lay, short, pool, q, 0.1, seq, out, ws)
+    with pytest.raises(ValueError, match="out"):
+        dattn.dattn_decode(lay, pool, pool, q, 0.1, seq, torch.zeros(3), ws)
+    q_half = torch.zeros(1, 5, 4, 64, dtype=torch.bfloat16)  # d = 64 rows for a d = 128 layout
+    with pytest.raises(ValueError, match="q"):
+        dattn.dattn_prefill(lay, pool, pool, q_half, 0.1, seq, torch.zeros(1, 5, 4, 128))
+    k_half = torch.zeros(1, 2, 2, 64, dtype=torch.bfloat16)
+    v_full = torch.zeros(1, 2, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="k_new"):
+        dattn.dattn_kv_append(lay, pool, pool, None, k_half, v_full, seq)
+    with pytest.raises(ValueError, match="block_table"):
+        dattn.dattn_decode(lay, pool, pool, torch.zeros(2, 4, 128, dtype=torch.bfloat16), 0.1,
+                           torch.zeros(2, dtype=torch.int32), torch.zeros(2, 4, 128), ws)
