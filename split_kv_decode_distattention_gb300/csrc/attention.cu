@@ -404,12 +404,12 @@ struct Consumer {
         }
         const float mn0 = fmaxf(m0, c0), mn1 = fmaxf(m1, c1);
         const float mu0 = mn0 == kNegInf ? 0.f : mn0, mu1 = mn1 == kNegInf ? 0.f : mn1;
-        p0 = exp2f(s0 - mu0);
-        p1 = exp2f(s1 - mu1);
-        p2 = exp2f(s2 - mu0);
-        p3 = exp2f(s3 - mu1);
+        p0 = ex2_approx(s0 - mu0);
+        p1 = ex2_approx(s1 - mu1);
+        p2 = ex2_approx(s2 - mu0);
+        p3 = ex2_approx(s3 - mu1);
         if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
-            const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
+            const float al0 = ex2_approx(m0 - mu0), al1 = ex2_approx(m1 - mu1);
             e0 *= al0;
             e1 *= al1;
 #pragma unroll
@@ -710,9 +710,9 @@ struct Consumer {
         const float mn0 = fmaxf(m0, c0), mn1 = fmaxf(m1, c1);
         const float mu0 = mn0 == kNegInf ? 0.f : mn0, mu1 = mn1 == kNegInf ? 0.f : mn1;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) pr[i] = exp2f(s[i] - ((i & 1) ? mu1 : mu0));
+        for (int i = 0; i < 8; ++i) pr[i] = ex2_approx(s[i] - ((i & 1) ? mu1 : mu0));
         if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
-            const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
+            const float al0 = ex2_approx(m0 - mu0), al1 = ex2_approx(m1 - mu1);
             e0 *= al0;
             e1 *= al1;
 #pragma unroll

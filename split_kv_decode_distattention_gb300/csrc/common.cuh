@@ -253,6 +253,14 @@ __device__ __forceinline__ uint32_t swz64(uint32_t row, uint32_t chunk) {
     return row * 64u + ((chunk ^ ((row >> 1) & 3u)) << 4);
 }
 
+// 2^x by the special-function unit (ex2.approx.ftz: relative error near 2^-22, subnormal results
+// flushed to +0, 2^-inf = +0)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Byte offset of 16-byte chunk `chunk` of row `row` in a [rows][32 B] box written by TMA
 // with CU_TENSOR_MAP_SWIZZLE_32B (the box base is 256-byte aligned).
 __device__ __forceinline__ uint32_t swz32(uint32_t row, uint32_t chunk) {

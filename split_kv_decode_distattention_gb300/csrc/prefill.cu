@@ -168,14 +168,6 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32])
         : "memory");
 }
 
-// 2^x by the special-function unit (ex2.approx.ftz: relative error near 2^-22, subnormal results
-// flushed to +0, 2^-inf = +0)
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // Packed fp32 pairs (Blackwell's two-wide fp32 FMA and add)
 __device__ __forceinline__ uint64_t pack_f32x2(float a, float b) {
     uint64_t r;
