@@ -6,8 +6,8 @@ stream becomes the launch stream. Every step of the computation runs in the libr
 CUDA kernels. There is no CPU fallback: if the library is missing, the first call raises.
 
 Entry points, with the same names as in include/dattn.h:
-  dattn_kv_append    paged KV append (bf16, or 8-bit E4M3 codes with row scales), plus
-                     logical-page k_max/k_min statistics
+  dattn_kv_append    paged KV append (bf16, or 8-bit E4M3 or 4-bit codes with row scales),
+                     plus logical-page k_max/k_min statistics
   dattn_partial      MicroAttention partials (m, e, MA) over explicit chunks of pages
   dattn_merge        log-sum-exp aggregation of partials
   dattn_decode       fused split-KV decode, dense or block-sparse

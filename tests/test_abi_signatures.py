@@ -142,3 +142,16 @@ def test_struct_layouts_equal_the_c_compilers(tmp_path):
         assert got[(cname, ".")][1] == ctypes.sizeof(cls), f"sizeof {cname}"
         for f, t in cls._fields_:
             assert got[(cname, f)] == (getattr(cls, f).offset, ctypes.sizeof(t)), f"{cname}.{f}"
+
+
+def test_constants_equal_the_headers_defines():
+    defines = dict(re.findall(r"^#define\s+DATTN_(\w+)\s+(0x[0-9a-fA-F]+|\d+)", open(HEADER).read(),
+                              flags=re.M))
+    defines = {k: int(v, 0) for k, v in defines.items()}
+    assert {k: v for k, v in defines.items() if k.startswith("DEVERR_")} == {
+        "DEVERR_" + k: v for k, v in dattn.DEVERR.items()}
+    for k in ("HEAD_DENSE", "HEAD_RETRIEVAL", "HEAD_STREAMING", "KV_BF16", "KV_FP8_E4M3",
+              "KV_INT4"):
+        assert getattr(dattn, k) == defines[k], k
+    assert {k for k in defines if k.startswith(("HEAD_", "KV_"))} == {
+        "HEAD_DENSE", "HEAD_RETRIEVAL", "HEAD_STREAMING", "KV_BF16", "KV_FP8_E4M3", "KV_INT4"}
