@@ -237,33 +237,42 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-# the sources that build the decode kernel and choose its launch configuration
+# the sources that build the decode (prefill) kernel and choose its launch configuration
 DECODE_SOURCES = ("abi.cu", "attention.cu", "common.cuh", "internal.h")
+PREFILL_SOURCES = ("abi.cu", "prefill.cu", "common.cuh", "internal.h")
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=DECODE_SOURCES) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "split_kv_decode_distattention_gb300", "csrc")
-    for f in DECODE_SOURCES:
+    for f in sources:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
-def traffic_key(args) -> str:
+def traffic_key(args):
+    """Key of the full-size workload's record in profiles/traffic.json; None for a run
+    reduced by --batch or --ctx, which no full-size record describes."""
+    if args.batch or args.ctx:
+        return None
+    if args.config == "prefill-32k":
+        return args.config + ("/dense" if args.prefill_dense else "")
     return (args.config + (f"/{args.kv_format}" if args.kv_format != "bf16" else "") +
             (f"/T{args.queries}" if args.queries > 1 else ""))
 
 
-def traffic_record(config: str):
-    """DRAM bytes per launch of the decode kernel from the committed ncu summary, if it was
-    taken on the current kernel sources."""
+def traffic_record(config, sources=DECODE_SOURCES):
+    """DRAM bytes per launch of the workload's dominant kernel from the committed ncu
+    summary, if it was taken on the current sources of that kernel."""
+    if config is None:
+        return None
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         rec = json.load(open(p)).get(config)
     except Exception:
         return None
-    if not rec or rec.get("source_hash") != kernel_source_hash():
+    if not rec or rec.get("source_hash") != kernel_source_hash(sources):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -929,6 +938,17 @@ def prefill_pairs(case, Tq: int, kinds, lists, sinks: int, local: int) -> int:
     return total
 
 
+def prefill_bytes(case, Tq: int) -> int:
+    """Least DRAM bytes of one prefill launch: the chunk's bf16 queries read, the K/V of
+    every valid token read once (bf16), the fp32 outputs written, and the block table."""
+    L = case.lens[0]
+    q = case.B * Tq * case.Hq * case.d * 2
+    kv = case.B * L * case.Hkv * case.d * 2 * 2
+    out = case.B * Tq * case.Hq * case.d * 4
+    bt = case.B * (-(-L // case.P)) * 4
+    return q + kv + out + bt
+
+
 def run_prefill(args, rank: int, world: int):
     """One layer-step of block-sparse prefill: the chunk's K/V appended through
     dattn_kv_append, then dattn_prefill over the whole chunk (the lengths are reset outside the
@@ -1110,7 +1130,9 @@ def prefill_main(args, rank: int, world: int):
                      "achieved": round(ktf, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(ktf / peak, 4),
                      "peak_source": "measured" if "bf16_tflops" in peaks else "fallback",
-                     "traffic": None, "algorithmic_flops_per_launch": int(res["flops_rank"]),
+                     "traffic": traffic_record(traffic_key(args), PREFILL_SOURCES),
+                     "algorithmic_flops_per_launch": int(res["flops_rank"]),
+                     "algorithmic_bytes_per_launch": prefill_bytes(case, res["Tq"]),
                      "avg_launch_ms": round(res["kms"], 4),
                      "kernel_timing": "CUDA events around the prefill kernel in every step"},
         # the chunk's append is two launches (the kernel, then the length update), then one

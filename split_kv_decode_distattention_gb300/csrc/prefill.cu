@@ -325,15 +325,19 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
         if (tid == 0) set_err(p.dev_err, DATTN_DEVERR_SMEM_ALIGN);
         return;
     }
-    // CTA -> (request b, head slot hs, tile J): the head slots of a KV head are neighbouring
-    // CTAs, so their K/V reads meet in L2, and a request's last tiles start first
+    // CTA -> (request b, KV head, tile J, head slot): the head slots of a KV head are
+    // neighbouring CTAs, and all tiles of a KV head come before the next KV head's, so the
+    // CTAs in flight read one KV head's K/V (it stays in L2); a KV head's last tiles start
+    // first. Head slot hs = KV head * spk + slot covers the query heads of rows 0-63.
     const bool hp = p.head_pairs != 0;
-    const int32_t nslots = hp ? p.Hq / 2 : p.Hq;
+    const int32_t spk = hp ? p.g / 2 : p.g;  // head slots per KV head
     int32_t c = blockIdx.x;
-    const int32_t hs = c % nslots;
-    c /= nslots;
+    const int32_t sk = c % spk;
+    c /= spk;
     const int32_t J = p.nqb - 1 - c % p.nqb;
-    const int32_t b = c / p.nqb;
+    c /= p.nqb;
+    const int32_t hs = (c % p.Hkv) * spk + sk;
+    const int32_t b = c / p.Hkv;
     const int32_t h = hp ? 2 * hs : hs;  // the query head of rows 0-63 (rows 64-127: h + hp)
     const uint32_t bars = smem_u32(base + L.bars);
     // K and V stages are tracked apart: K_j's stage is free once S_j is computed, V_j's once

@@ -91,3 +91,27 @@ def test_prefill_pairs_equal_the_oracle_row_sets():
     dense = bench.prefill_pairs(case, Tq, [0] * 4, lists, sinks, local)
     assert dense == case.Hq * sum(sum(L - Tq + t + 1 for t in range(Tq)) for L in case.lens)
     assert np.all(lists[:, :, :, 0] >= 0)  # every row lists at least its own block
+
+
+def test_prefill_32k_least_bytes():
+    case = W.prefill_32k(seed=0)
+    q = 32768 * 32 * 128 * 2      # bf16 queries of the chunk
+    kv = 32768 * 8 * 128 * 2 * 2  # K and V of every token, bf16, read once
+    out = 32768 * 32 * 128 * 4    # fp32 outputs
+    assert bench.prefill_bytes(case, 32768) == q + kv + out + 2048 * 4 == 939_532_288
+
+
+def test_traffic_records_apply_to_full_size_runs_of_their_own_kernel():
+    class A:
+        config, kv_format, queries, batch, ctx, prefill_dense = "mha-32k", "bf16", 1, 0, 0, False
+    a = A()
+    assert bench.traffic_key(a) == "mha-32k"
+    a.kv_format, a.queries = "int4", 8
+    assert bench.traffic_key(a) == "mha-32k/int4/T8"
+    a.ctx = 4096  # a reduced run: no full-size record describes it
+    assert bench.traffic_key(a) is None and bench.traffic_record(None) is None
+    a.config, a.ctx, a.prefill_dense = "prefill-32k", 0, True
+    assert bench.traffic_key(a) == "prefill-32k/dense"
+    # a record is taken on one kernel's sources: the prefill's hash never matches a decode one
+    assert bench.kernel_source_hash(bench.PREFILL_SOURCES) != bench.kernel_source_hash()
+    assert bench.traffic_record("mha-32k", bench.PREFILL_SOURCES) is None
