@@ -1056,9 +1056,10 @@ def run_prefill(args, rank: int, world: int):
     return res
 
 
-def prefill_cpu_baseline(case, device, kinds, lists, sinks, local, Tq):
+def prefill_cpu_baseline(case, device, kinds, lists, sinks, local, Tq, target_s: float = 10.0):
     """The oracle's prefill attention on the host cores over a sample of query rows of two
-    heads (the first of each kind present), as TFLOP/s."""
+    heads (the first of each kind present), as TFLOP/s. Rows are taken in a seeded random
+    order of the chunk, a batch at a time, until about target_s seconds have passed."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
     oracle.load()
@@ -1070,8 +1071,8 @@ def prefill_cpu_baseline(case, device, kinds, lists, sinks, local, Tq):
     for h in heads:
         K, V = case.kv(0, 0, L, device)
         kv[h] = (oracle.bf16_bits(K[:, h]), oracle.bf16_bits(V[:, h]))
-    ts = np.linspace(0, Tq - 1, 96).astype(np.int64)
-    work = [(h, int(t)) for h in heads for t in ts]
+    order = np.random.default_rng(case.seed).permutation(Tq)
+    per_batch = 16 * nthreads
 
     def one(ht):
         h, t = ht
@@ -1081,15 +1082,20 @@ def prefill_cpu_baseline(case, device, kinds, lists, sinks, local, Tq):
         oracle.attention(q[0, t, h * case.g], kv[h][0], kv[h][1], case.scale, rows=rows)
         return rows.shape[0]
 
+    pairs, nrows, i = 0, 0, 0
     t0 = time.perf_counter()
     with ThreadPoolExecutor(max_workers=nthreads) as ex:
-        pairs = sum(ex.map(one, work))
+        while i < Tq and (i == 0 or time.perf_counter() - t0 < target_s):
+            work = [(h, int(t)) for t in order[i:i + per_batch] for h in heads]
+            pairs += sum(ex.map(one, work))
+            nrows += len(work)
+            i += per_batch
     secs = time.perf_counter() - t0
     return {"value": round(4 * case.d * pairs / secs / 1e12, 6), "unit": "TFLOP/s",
-            "cores": min(nthreads, len(work)), "kind": "oracle",
-            "sample": f"{len(ts)} query rows spread over the chunk for KV heads {heads} "
-                      f"(one query head each), fp64 attention over their prefill rows: "
-                      f"{secs:.1f} s wall"}
+            "cores": min(nthreads, nrows), "kind": "oracle",
+            "sample": f"{nrows} query rows (a seeded random order of the chunk's rows) of KV "
+                      f"heads {heads}, one query head each, fp64 attention over their prefill "
+                      f"rows: {pairs} query-key pairs in {secs:.1f} s wall"}
 
 
 def prefill_main(args, rank: int, world: int):

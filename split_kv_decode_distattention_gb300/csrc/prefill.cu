@@ -10,8 +10,10 @@
 // GB300 design: the contraction runs on the 5th-generation tensor cores. One CTA takes 128
 // query rows: one 64-token query block of two query heads of a KV head when the group is
 // even (both halves keep the same key blocks), else two query blocks of one query head. The
-// heads of a KV head are neighbouring CTAs, so their K/V reads meet in L2, and a request's
-// last rows (the most key blocks under the causal mask) start first. The key blocks each
+// heads of a KV head are neighbouring CTAs, so their K/V reads meet in L2. KV heads run in
+// groups, each group's last rows (the most key blocks under the causal mask) first: a group
+// is one KV head when its tiles fill three waves, so the K/V in flight stays in L2, else as
+// many KV heads as it takes to fill them, so no long tile starts late. The key blocks each
 // half keeps are built into shared-memory bitmaps, and every role walks their union in the
 // same order: the block iterator. Seven warps:
 //   - two producer warps, one for K and one for V, stream each key block's four 16-token
@@ -58,6 +60,7 @@ struct PfParams {
     // 1: a CTA's 128 rows are one 64-token query block of two query heads of one KV head
     // (even g; both halves keep the same key blocks); 0: two query blocks of one query head
     int32_t head_pairs;
+    int32_t kv_group;  // KV heads whose tiles run together (a divisor of Hkv)
     // block sparsity (head_kind == nullptr: dense causal)
     const int8_t* head_kind;
     int32_t sink_blocks, local_blocks, max_sel, qblock_stride;
@@ -325,19 +328,23 @@ prefill_tc_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CU
         if (tid == 0) set_err(p.dev_err, DATTN_DEVERR_SMEM_ALIGN);
         return;
     }
-    // CTA -> (request b, KV head, tile J, head slot): the head slots of a KV head are
-    // neighbouring CTAs, and all tiles of a KV head come before the next KV head's, so the
-    // CTAs in flight read one KV head's K/V (it stays in L2); a KV head's last tiles start
-    // first. Head slot hs = KV head * spk + slot covers the query heads of rows 0-63.
+    // CTA -> (request b, group of kv_group KV heads, tile J, KV head in the group, head
+    // slot): the head slots of a KV head are neighbouring CTAs, a group's tiles run together
+    // with its last (longest) tiles first, and the CTAs in flight read the K/V of one group
+    // only (it stays in L2). Head slot hs = KV head * spk + slot covers the query heads of
+    // rows 0-63.
     const bool hp = p.head_pairs != 0;
     const int32_t spk = hp ? p.g / 2 : p.g;  // head slots per KV head
+    const int32_t ngrp = p.Hkv / p.kv_group;
     int32_t c = blockIdx.x;
     const int32_t sk = c % spk;
     c /= spk;
+    const int32_t hg = c % p.kv_group;
+    c /= p.kv_group;
     const int32_t J = p.nqb - 1 - c % p.nqb;
     c /= p.nqb;
-    const int32_t hs = (c % p.Hkv) * spk + sk;
-    const int32_t b = c / p.Hkv;
+    const int32_t hs = ((c % ngrp) * p.kv_group + hg) * spk + sk;
+    const int32_t b = c / ngrp;
     const int32_t h = hp ? 2 * hs : hs;  // the query head of rows 0-63 (rows 64-127: h + hp)
     const uint32_t bars = smem_u32(base + L.bars);
     // K and V stages are tracked apart: K_j's stage is free once S_j is computed, V_j's once
@@ -848,6 +855,20 @@ dattn_status_t launch_prefill_tc_d(const PfParams& p0, const void* k_pool, const
     p.nqb = p.head_pairs ? blocks : (blocks + 1) / 2;
     const int64_t ctas = (int64_t)p.B * p.nqb * (p.head_pairs ? p.Hq / 2 : p.Hq);
     if (ctas >= (1ll << 31)) return DATTN_ERR_UNSUPPORTED;
+    // The smallest group of KV heads whose tiles fill three waves of resident CTAs (two per
+    // SM: each holds half the tensor memory). One KV head per group keeps the K/V in flight
+    // L2-resident; a group spanning fewer waves would start a later group's long tiles so
+    // late that they run alone at the end, so small chunks group all KV heads.
+    {
+        const int64_t per_head = (int64_t)p.nqb * (p.head_pairs ? p.g / 2 : p.g);
+        const int64_t three_waves = 3ll * 2 * sm_count_current();
+        p.kv_group = p.Hkv;
+        for (int32_t G = 1; G < p.Hkv; ++G)
+            if (p.Hkv % G == 0 && G * per_head >= three_waves) {
+                p.kv_group = G;
+                break;
+            }
+    }
     const int32_t nwords = (p.max_pages * p.P / kPfBlock + 2 + 31) / 32;
     const TcSmem L = tc_smem_layout(D, nwords);
     if (L.total > 227u * 1024u) return DATTN_ERR_UNSUPPORTED;
