@@ -115,3 +115,22 @@ def test_traffic_records_apply_to_full_size_runs_of_their_own_kernel():
     # a record is taken on one kernel's sources: the prefill's hash never matches a decode one
     assert bench.kernel_source_hash(bench.PREFILL_SOURCES) != bench.kernel_source_hash()
     assert bench.traffic_record("mha-32k", bench.PREFILL_SOURCES) is None
+
+
+def test_prefill_cpu_sample_is_bounded_and_covers_rows_once():
+    oracle.build_oracle()
+    case = W.prefill_32k(seed=0, L=640)
+    kinds = list(case.head_kind)
+    lists = case.prefill_block_lists(W.PREFILL_KEEP)
+    args = (case, "cpu", kinds, lists, W.PREFILL_SINK_BLOCKS, W.PREFILL_LOCAL_BLOCKS, 640)
+    heads = sorted({kinds.index(k) for k in set(kinds)})
+    want = sum(oracle.prefill_rows(kinds[h], 640, 640, t, W.PREFILL_SINK_BLOCKS,
+                                   W.PREFILL_LOCAL_BLOCKS,
+                                   blocks=lists[0, h, t // 64] if kinds[h] == 1 else None).size
+               for h in heads for t in range(640))
+    full = bench.prefill_cpu_baseline(*args, target_s=1e9)
+    assert full["sample"].startswith(f"{640 * len(heads)} query rows")
+    assert f" {want} query-key pairs" in full["sample"]
+    one = bench.prefill_cpu_baseline(*args, target_s=0.0)  # stops after its first batch
+    nrows = int(one["sample"].split()[0])
+    assert 0 < nrows <= 16 * os.cpu_count() * len(heads) and nrows % len(heads) == 0
