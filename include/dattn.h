@@ -346,12 +346,11 @@ dattn_status_t dattn_prefill(const dattn_kv_layout *layout, const void *k_pool,
  * Page scoring and top-K selection for retrieval heads [LV §2.2.2, §3.1.2]. For every
  * request b and KV head h of kind DATTN_HEAD_RETRIEVAL:
  *   logical score  sigma(lp) = max over the g query heads j of
- *                  sum_d max(q_jd * kmax_d, q_jd * kmin_d)
- *                  in fp32 and a fixed order: 16 chunks of d/16 channels; per chunk a
- *                  k_max partial with max(q,0) and a k_min partial with min(q,0), each two
- *                  fused multiply-add chains from +0 (even and odd channels, ascending)
- *                  added as even + odd; the 32 partials x[0..15] (k_max), x[16..31]
- *                  (k_min) added by the tree x[i] += x[i + n], n = 16, 8, 4, 2, 1;
+ *                  sum_d max(q_jd * kmax_d, q_jd * kmin_d),
+ *                  evaluated in fp32 in a fixed order (deterministic). Each product of two
+ *                  bf16 values is exact in fp32, so the evaluation is within
+ *                  d * 2^-23 * sum_d |max(q_jd * kmax_d, q_jd * kmin_d)| of the exact score;
+ *                  pages whose scores lie within that rounding may be ranked either way;
  *   physical score = max of sigma over its logical pages that hold a token < L_b;
  *   selection      the top_k physical pages by score, ties to the lower page index.
  * They are written in ascending page order to selected[b][h][0..top_k), padded with -1.

@@ -60,8 +60,8 @@ _SIGS = {
     "orc_kv_write": (_I64, [_P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _I64, _I64]),
     "orc_logical_page_stats": (None, [_P, _I64, _I, _I64, _I64, _P, _P]),
     "orc_logical_score_f64": (_D, [_P, _P, _P, _I]),
-    "orc_logical_score_f32": (ctypes.c_float, [_P, _P, _P, _I]),
-    "orc_page_scores": (None, [_P, _I, _P, _I64, _I, _I64, _I, _I, _P]),
+    "orc_logical_score_bound": (_D, [_P, _P, _P, _I]),
+    "orc_page_scores": (None, [_P, _I, _P, _I64, _I, _I64, _I, _P, _P]),
     "orc_topk": (None, [_P, _I64, _I, _P]),
     "orc_sparse_rows": (_I64, [_I, _I64, _I, _P, _I, _I, _I, _P]),
     "orc_prefill_rows": (_I64, [_I, _I64, _I64, _I64, _I, _I, _P, _I, _P]),
@@ -217,18 +217,23 @@ def logical_page_stats(K, t0: int, t1: int, lib=None):
     return kmax, kmin
 
 
-def logical_score(q, kmax, kmin, precision64: bool = True, lib=None) -> float:
-    """Logical-page score sum_d max(q_d kmax_d, q_d kmin_d): the fp64 definition, or the
-    fp32 decision arithmetic."""
+def logical_score(q, kmax, kmin, lib=None) -> float:
+    """Logical-page score sum_d max(q_d kmax_d, q_d kmin_d) in fp64. LServe notes §3.1.2."""
     lib = lib or load()
     q, kmax, kmin = bf16_bits(q), bf16_bits(kmax), bf16_bits(kmin)
-    if precision64:
-        return float(lib.orc_logical_score_f64(_ptr(q), _ptr(kmax), _ptr(kmin), q.shape[-1]))
-    return float(lib.orc_logical_score_f32(_ptr(q), _ptr(kmax), _ptr(kmin), q.shape[-1]))
+    return float(lib.orc_logical_score_f64(_ptr(q), _ptr(kmax), _ptr(kmin), q.shape[-1]))
 
 
-def page_scores(Q, K, L: int, P: int, precision64: bool, lib=None) -> np.ndarray:
-    """Physical-page scores of one request/KV head (Q: [g][d], K: [>=L][d] token order)."""
+def logical_score_bound(q, kmax, kmin, lib=None) -> float:
+    """Bound on the error of any fp32 evaluation of logical_score (reading R9)."""
+    lib = lib or load()
+    q, kmax, kmin = bf16_bits(q), bf16_bits(kmax), bf16_bits(kmin)
+    return float(lib.orc_logical_score_bound(_ptr(q), _ptr(kmax), _ptr(kmin), q.shape[-1]))
+
+
+def page_scores(Q, K, L: int, P: int, with_bounds: bool = False, lib=None):
+    """fp64 physical-page scores of one request/KV head (Q: [g][d], K: [>=L][d] in token
+    order). With ``with_bounds`` also the fp32 error bound of each score: (score, bound)."""
     lib = lib or load()
     Q, K = bf16_bits(Q), bf16_bits(K)
     d = Q.shape[-1]
@@ -236,9 +241,9 @@ def page_scores(Q, K, L: int, P: int, precision64: bool, lib=None) -> np.ndarray
     K2 = K.reshape(-1, d)
     n = (L + P - 1) // P
     score = np.zeros(max(n, 1), np.float64)
-    lib.orc_page_scores(_ptr(Q2), Q2.shape[0], _ptr(K2), d, d, L, P, 1 if precision64 else 0,
-                        _ptr(score))
-    return score[:n]
+    bound = np.zeros(max(n, 1), np.float64)
+    lib.orc_page_scores(_ptr(Q2), Q2.shape[0], _ptr(K2), d, d, L, P, _ptr(score), _ptr(bound))
+    return (score[:n], bound[:n]) if with_bounds else score[:n]
 
 
 def topk(score, top_k: int, lib=None) -> np.ndarray:
@@ -251,8 +256,8 @@ def topk(score, top_k: int, lib=None) -> np.ndarray:
 
 
 def select_pages(Q, K, L: int, P: int, top_k: int, lib=None) -> np.ndarray:
-    """Page selection of one request/KV head, decided in the fp32 score arithmetic."""
-    return topk(page_scores(Q, K, L, P, precision64=False, lib=lib), top_k, lib=lib)
+    """Page selection of one request/KV head: the top-K of the fp64 page scores."""
+    return topk(page_scores(Q, K, L, P, lib=lib), top_k, lib=lib)
 
 
 def sparse_rows(kind: int, L: int, P: int, sel, sinks: int, local: int, lib=None) -> np.ndarray:

@@ -40,9 +40,18 @@
  *  R7  A streaming head at length L attends [0, min(S, L)) U [max(S, L - W), L).
  *  R8  k_max/k_min use strict comparison in token order, so the first-seen value wins a
  *      tie (this matters only for +0/-0).
- *  R9  The page selection is decided in the kernel's arithmetic: fp32 in a fixed order
- *      (see orc_logical_score_f32). The fp64 score is the definition, and the tests
- *      check that the two differ by less than the fp32 error bound.
+ *  R9  The page selection is defined by the fp64 score (R4, R5) and the top-K rule (R6).
+ *      A GPU computes the score in fp32, so where two pages' scores lie within the
+ *      rounding error of an fp32 evaluation the selection is not unique. The oracle
+ *      therefore returns, next to each fp64 score, a bound on the error of ANY fp32
+ *      evaluation of it (any summation order): the classical bound for a floating-point
+ *      sum of n terms, |fl(sum) - sum| <= (n-1) u / (1 - (n-1) u) * sum |t_i|
+ *      (Higham, "Accuracy and Stability of Numerical Algorithms", 2nd ed., eq. 4.4),
+ *      with u = 2^-24. It is taken as d * 2^-23 * sum |t_i|, which covers n = 2d terms
+ *      (an evaluation may add the k_max and the k_min half as separate products), plus
+ *      2d * 2^-150 for products that fall below the fp32 normal range. The tests accept a
+ *      GPU selection bit for bit where the margin between the chosen and the rejected
+ *      pages exceeds these bounds, and otherwise check that it is a valid top-K under them.
  *  R10 The 8-bit KV cache: the pages give retrieval heads 2-8 bit configurable quantization
  *      and no scheme. Here: FP8 E4M3 codes with one fp32 scale per (token, KV head) row of
  *      K and of V, scale = max|x| / 448, code = E4M3(x / scale) rounded to nearest even;
@@ -266,88 +275,55 @@ double orc_logical_score_f64(const uint16_t *q, const uint16_t *kmax, const uint
 }
 
 /*
- * One partial of the decision arithmetic: two fp32 fused multiply-add chains from +0, over
- * the even and over the odd channels of [c0, c0 + n) in ascending order, then even + odd.
- * The query factor is the positive part max(q,0) (neg == 0, paired with k_max) or the
- * negative part min(q,0) (neg == 1, paired with k_min).
+ * Bound on the error of an fp32 evaluation of a logical-page score whose exact terms are
+ * t_c = max(q_c * kmax_c, q_c * kmin_c), c < d (reading R9): d * 2^-23 * sum |t_c| plus
+ * 2d * 2^-150. Each t_c is a product of two bf16 values and so exact in fp32 unless it falls
+ * below the normal range; every addition of a sum of n <= 2d terms rounds by at most u = 2^-24
+ * relative, in whatever order the terms are added.
  */
-static float decision_partial(const uint16_t *q, const uint16_t *k, int c0, int n, int neg)
+double orc_logical_score_bound(const uint16_t *q, const uint16_t *kmax, const uint16_t *kmin,
+                               int d)
 {
-    float even = 0.0f, odd = 0.0f;
-    for (int i = 0; i < n; i += 2) {
-        const float q0 = bf16_to_float(q[c0 + i]), q1 = bf16_to_float(q[c0 + i + 1]);
-        const float f0 = neg ? (q0 >= 0.0f ? 0.0f : q0) : (q0 >= 0.0f ? q0 : 0.0f);
-        const float f1 = neg ? (q1 >= 0.0f ? 0.0f : q1) : (q1 >= 0.0f ? q1 : 0.0f);
-        even = fmaf(f0, bf16_to_float(k[c0 + i]), even);
-        odd = fmaf(f1, bf16_to_float(k[c0 + i + 1]), odd);
+    double abs_sum = 0.0;
+    for (int c = 0; c < d; ++c) {
+        const double qc = orc_bf16_to_double(q[c]);
+        const double a = qc * orc_bf16_to_double(kmax[c]);
+        const double b = qc * orc_bf16_to_double(kmin[c]);
+        abs_sum += fabs(a > b ? a : b);
     }
-    return even + odd;
-}
-
-/*
- * The same score in the arithmetic that decides the selection (reading R9). It is fp32 in
- * a fixed order, so that both sides take the same integer decision:
- *  - the channels form nch chunks of w = d/16 channels (w = 2, nch = d/2 when d < 32);
- *  - chunk c gives two partials (decision_partial): k_max with max(q,0) and k_min with
- *    min(q,0). One of the two query factors is an exact zero, so together they add exactly
- *    the product that the definition's max picks (q_d*kmax_d for q_d >= 0, else q_d*kmin_d);
- *  - x[c] is the k_max partial of chunk c and x[nch + c] its k_min partial; they are added
- *    by the tree x[i] = x[i] + x[i + n] for n = nch, nch/2, ..., 1 (i < n), and the score
- *    is x[0].
- * Each product of two bf16 values is exact in fp32; only the additions round. d must be
- * even with nch a power of two (d = 2, 4, 8, 16, or a multiple of 32).
- */
-float orc_logical_score_f32(const uint16_t *q, const uint16_t *kmax, const uint16_t *kmin, int d)
-{
-    float x[64];
-    const int w = d >= 32 ? d / 16 : 2;
-    const int nch = d / w;
-    if (d % 2 != 0 || nch > 32 || (nch & (nch - 1)) != 0 || nch * w != d) return NAN;
-    for (int c = 0; c < nch; ++c) {
-        x[c] = decision_partial(q, kmax, c * w, w, 0);
-        x[nch + c] = decision_partial(q, kmin, c * w, w, 1);
-    }
-    for (int n = nch; n >= 1; n >>= 1)
-        for (int i = 0; i < n; ++i) x[i] = x[i] + x[i + n];
-    return x[0];
+    return (double)d * ldexp(1.0, -23) * abs_sum + 2.0 * d * ldexp(1.0, -150);
 }
 
 /*
  * Physical-page scores of one request and one KV head [LV §3.1.2 score_pages: max over the
- * logical pages of a physical page], with the GQA reading R5 (max over the g query heads).
- * Logical-page statistics are recomputed here from the token-ordered keys (rows 0..L-1 of
- * K, stride row_stride). Q holds g query vectors of d entries. score has ceil(L / P)
- * entries. precision64 != 0 selects the fp64 definition; otherwise the fp32 decision
- * arithmetic is used (the result is stored in double either way).
+ * logical pages of a physical page], with the GQA reading R5 (max over the g query heads),
+ * in fp64. Logical-page statistics are recomputed here from the token-ordered keys (rows
+ * 0..L-1 of K, stride row_stride). Q holds g query vectors of d entries. score has
+ * ceil(L / P) entries. If bound is not NULL, bound[p] gets the largest fp32 error bound
+ * (orc_logical_score_bound) over the (logical page, head) pairs of page p: a max of values
+ * each off by at most its own bound is off by at most the largest of them.
  */
 void orc_page_scores(const uint16_t *Q, int g, const uint16_t *K, int64_t row_stride, int d,
-                     int64_t L, int P, int precision64, double *score)
+                     int64_t L, int P, double *score, double *bound)
 {
     const int LPG = 16; /* logical page size [LV §2.2.2: 16-token logical pages] */
     uint16_t *kmax = (uint16_t *)malloc((size_t)d * sizeof(uint16_t));
     uint16_t *kmin = (uint16_t *)malloc((size_t)d * sizeof(uint16_t));
     const int64_t npages = (L + P - 1) / P;
     for (int64_t p = 0; p < npages; ++p) {
-        double best = -INFINITY;
-        float best32 = -INFINITY;
+        double best = -INFINITY, err = 0.0;
         for (int64_t t0 = p * P; t0 < (p + 1) * P && t0 < L; t0 += LPG) {
             const int64_t t1 = (t0 + LPG < L) ? t0 + LPG : L;
             orc_logical_page_stats(K, row_stride, d, t0, t1, kmax, kmin);
             for (int j = 0; j < g; ++j) {
-                if (precision64) {
-                    const double s = orc_logical_score_f64(Q + (int64_t)j * d, kmax, kmin, d);
-                    if (s > best) best = s;
-                } else {
-                    const float s = orc_logical_score_f32(Q + (int64_t)j * d, kmax, kmin, d);
-                    if (s > best32) best32 = s;
-                }
+                const double s = orc_logical_score_f64(Q + (int64_t)j * d, kmax, kmin, d);
+                if (s > best) best = s;
+                const double e = orc_logical_score_bound(Q + (int64_t)j * d, kmax, kmin, d);
+                if (e > err) err = e;
             }
         }
-        if (precision64) {
-            score[p] = best;
-        } else {
-            score[p] = (double)(best32 + 0.0f); /* +0.0f turns a -0 score into +0 */
-        }
+        score[p] = best;
+        if (bound) bound[p] = err;
     }
     free(kmax);
     free(kmin);

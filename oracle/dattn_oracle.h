@@ -34,10 +34,11 @@ void orc_logical_page_stats(const uint16_t *K, int64_t row_stride, int d, int64_
 
 double orc_logical_score_f64(const uint16_t *q, const uint16_t *kmax, const uint16_t *kmin, int d);
 
-float orc_logical_score_f32(const uint16_t *q, const uint16_t *kmax, const uint16_t *kmin, int d);
+double orc_logical_score_bound(const uint16_t *q, const uint16_t *kmax, const uint16_t *kmin,
+                               int d);
 
 void orc_page_scores(const uint16_t *Q, int g, const uint16_t *K, int64_t row_stride, int d,
-                     int64_t L, int P, int precision64, double *score);
+                     int64_t L, int P, double *score, double *bound);
 
 void orc_topk(const double *score, int64_t n, int top_k, int32_t *sel);
 

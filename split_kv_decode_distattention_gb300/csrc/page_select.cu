@@ -31,15 +31,16 @@
 //  - At the end of a piece the eight warps' lists are merged. A head split across CTAs
 //    leaves each CTA's top K in the workspace, and the CTA that arrives last merges them.
 //
-// Decision arithmetic (the selection is an integer decided by floating point, so it is
-// fixed exactly, and the oracle repeats it). Channels form 16 chunks of d/16. For each chunk
-// c there are two partials: k_max with the positive part max(q,0), and k_min with the
-// negative part min(q,0). A partial runs two fp32 fused multiply-add chains from +0, over
-// the chunk's even and its odd channels in ascending order, and is even + odd. Since one of
-// max(q,0), min(q,0) is an exact zero, the two partials together add exactly the product
-// q*kmax or q*kmin that the score definition selects. The 32 partials x[0..15] (k_max
-// chunks) and x[16..31] (k_min chunks) are then added by the tree
-// x[i] = x[i] + x[i + n] for n = 16, 8, 4, 2, 1 (i < n), and the score is x[0].
+// Arithmetic. The score is evaluated in fp32: every product of two bf16 values is exact in
+// fp32, so only the additions round, and a sum of n such terms in any order is within
+// (n-1) 2^-24 / (1 - (n-1) 2^-24) of sum |terms| of the exact value. Pages whose scores lie
+// that close may be ranked either way; the result is still a top-K of the definition's
+// scores up to that rounding, and a fixed evaluation order makes it deterministic. Channels
+// form 16 chunks of d/16; each chunk gives a k_max partial with the positive part max(q,0)
+// and a k_min partial with the negative part min(q,0) (one of the two factors is an exact
+// zero, so together they add exactly the product the definition's max picks), each as two
+// fused multiply-add chains (even and odd channels); the 32 partials are then summed across
+// the lanes.
 #include "common.cuh"
 #include "internal.h"
 

@@ -77,3 +77,41 @@ def check_dense(case, q, lens, out, m_g, e_g, device, pairs=None, what="decode")
 
 def bf16_to_np(t: torch.Tensor) -> np.ndarray:
     return oracle.bf16_bits(t)
+
+
+def check_selection(got, score, bound, top_k, what=""):
+    """Checks one row of a GPU page selection against the fp64 page scores.
+
+    LServe article §3.1.2 keeps the top_k pages by score, ties to the lower page (reading
+    R6 of the oracle). The GPU scores in fp32, and ``bound`` holds each fp64 score's fp32
+    error bound. Where every page of the fp64 top-K stays above every other page by more
+    than their bounds, the selection is unique and the row must equal the oracle's bit for
+    bit. Otherwise the row must be a valid top-K under the bounds: no rejected page may be
+    certainly above a chosen one. Returns True for a unique row, False for an ambiguous one.
+    """
+    got = np.asarray(got)
+    score = np.asarray(score, np.float64)
+    bound = np.asarray(bound, np.float64)
+    n = score.shape[0]
+    k = min(top_k, n)
+    want = oracle.topk(score, top_k)
+    assert got.shape == (top_k,), f"{what}: row shape {got.shape}"
+    assert (got[k:] == -1).all(), f"{what}: padding {got[k:]}"
+    sel = got[:k]
+    assert ((sel >= 0) & (sel < n)).all(), f"{what}: pages out of range {sel}"
+    assert (np.diff(sel) > 0).all(), f"{what}: not strictly ascending {sel}"
+    if k == n:
+        np.testing.assert_array_equal(got, want, err_msg=what)
+        return True
+    inset = np.zeros(n, bool)
+    inset[want[:k]] = True
+    if (score - bound)[inset].min() > (score + bound)[~inset].max():
+        np.testing.assert_array_equal(got, want, err_msg=f"{what}: unique selection")
+        return True
+    chosen = np.zeros(n, bool)
+    chosen[sel] = True
+    lo = (score + bound)[chosen].min()
+    hi = (score - bound)[~chosen].max()
+    assert lo >= hi, (f"{what}: a rejected page (fp64 score - bound {hi!r}) is certainly above "
+                      f"a chosen one (score + bound {lo!r})")
+    return False

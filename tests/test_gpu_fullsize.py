@@ -2,8 +2,9 @@
 the 32K prefill, run in the launch configuration the benchmark times (automatic split
 count). Outputs are checked against the oracle on sampled (request, head) pairs or query
 rows, which the oracle computes one at a time. Properties that hold at any size are checked
-on everything: the page-set merge equals the fused decode, the selection is bit-exact, and
-no device error is flagged."""
+on everything: the page-set merge equals the fused decode, and no device error is flagged.
+The page selection is checked against the oracle's fp64 page scores: bit for bit where the
+margin exceeds the fp32 error bound, else for validity."""
 import numpy as np
 import pytest
 import torch
@@ -11,7 +12,7 @@ import torch
 import oracle
 from split_kv_decode_distattention_gb300 import workloads as W
 
-from _util import assert_e_close, assert_m_close, assert_out_close
+from _util import assert_e_close, assert_m_close, assert_out_close, check_selection
 
 pytestmark = pytest.mark.gpu
 # every workload is also run with seeds 1 and 2
@@ -164,13 +165,19 @@ def test_sparse_512k_full_size(seed):
         if case.head_kind[h] != W.HEAD_RETRIEVAL:
             assert (got[:, h] == -1).all()
     qb = oracle.bf16_bits(q0)
-    for b, h in [(0, 0), (3, 2), (7, 3)]:
-        Ks, _ = _host_heads(case, b, cache.lens[b], [h])
-        want = oracle.select_pages(qb[b, h * case.g:(h + 1) * case.g], Ks[0], cache.lens[b],
-                                   case.P, case.top_k)
-        np.testing.assert_array_equal(got[b, h], want, err_msg=f"selection b={b} h={h}")
-        # the seeded high-similarity pages are all selected
-        assert set(case.highsim_pages(b, h).tolist()) <= set(want.tolist())
+    ret = [h for h in range(case.Hkv) if case.head_kind[h] == W.HEAD_RETRIEVAL]
+    ambiguous = 0
+    for b in (0, 3, 7):
+        Ks, _ = _host_heads(case, b, cache.lens[b], ret)
+        for i, h in enumerate(ret):
+            score, bound = oracle.page_scores(qb[b, h * case.g:(h + 1) * case.g], Ks[i],
+                                              cache.lens[b], case.P, with_bounds=True)
+            ambiguous += not check_selection(got[b, h], score, bound, case.top_k,
+                                             f"selection b={b} h={h}")
+            # the seeded high-similarity pages are all selected
+            assert set(case.highsim_pages(b, h).tolist()) <= set(got[b, h].tolist())
+    print(f"sparse-512k selection: {3 * len(ret)} rows, {ambiguous} ambiguous within the "
+          f"fp32 bound")
     # decode with the selection reused for the rest of the window
     sp = cache.sparse_config(sel)
     q, out, m_g, e_g = _step(cache, case, sparse=sp)

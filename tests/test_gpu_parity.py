@@ -27,7 +27,7 @@ def _cache(case, **kw):
 
 
 from _util import (assert_e_close, assert_m_close, assert_out_close, check_dense,  # noqa: E402
-                   host_kv)
+                   check_selection, host_kv)
 
 
 # ---------------------------------------------------------------- paged append + statistics
@@ -280,17 +280,28 @@ def test_merge_of_empty_chunks():
 
 # ---------------------------------------------------------------- page selection
 
-def _oracle_selection(case, cache, q):
+def _check_selection(case, cache, q, sel):
+    """Checks every row of a GPU selection against the oracle's fp64 page scores and their
+    fp32 error bounds (check_selection); rows of other head kinds must be all -1. Prints how
+    many retrieval rows were ambiguous (margin within the bounds) and checked for validity
+    only."""
     qb = oracle.bf16_bits(q)
-    want = np.full((case.B, case.Hkv, case.top_k), -1, np.int32)
+    got = sel.cpu().numpy()
+    rows = ambiguous = 0
     for b in range(case.B):
         K, _ = host_kv(case, b, cache.lens[b], DEV)
         for h in range(case.Hkv):
             if case.head_kind[h] != W.HEAD_RETRIEVAL:
+                assert (got[b, h] == -1).all(), f"b={b} h={h}: row of a non-retrieval head"
                 continue
-            want[b, h] = oracle.select_pages(qb[b, h * case.g:(h + 1) * case.g], K[:, h].copy(),
-                                             cache.lens[b], case.P, case.top_k)
-    return want
+            score, bound = oracle.page_scores(qb[b, h * case.g:(h + 1) * case.g],
+                                              K[:, h].copy(), cache.lens[b], case.P,
+                                              with_bounds=True)
+            rows += 1
+            ambiguous += not check_selection(got[b, h], score, bound, case.top_k,
+                                             f"selection b={b} h={h}")
+    print(f"page selection: {rows} retrieval rows, {ambiguous} ambiguous within the fp32 bound")
+    return got
 
 
 @pytest.mark.parametrize("P,d,lens,top_k,splits", [
@@ -314,7 +325,7 @@ def test_page_select_bit_exact(P, d, lens, top_k, splits):
     cache.select(q, sel, cache.workspace(top_k=top_k, num_splits=splits), num_splits=splits)
     torch.cuda.synchronize()
     assert int(cache.dev_err.item()) == 0
-    np.testing.assert_array_equal(sel.cpu().numpy(), _oracle_selection(case, cache, q))
+    _check_selection(case, cache, q, sel)
 
 
 # ---------------------------------------------------------------- block-sparse decode
@@ -330,8 +341,7 @@ def test_sparse_decode_matches_oracle_token_sets(P, lens, splits):
     sel = torch.empty(case.B, case.Hkv, case.top_k, dtype=torch.int32, device=DEV)
     cache.select(q0, sel, cache.workspace(top_k=case.top_k))
     torch.cuda.synchronize()
-    want_sel = _oracle_selection(case, cache, q0)
-    np.testing.assert_array_equal(sel.cpu().numpy(), want_sel)
+    want_sel = _check_selection(case, cache, q0, sel)  # the validated GPU rows
     sp = cache.sparse_config(sel)
     ws = cache.workspace(num_splits=splits)
     for step in range(3):  # the selection is reused while tokens are appended
@@ -426,4 +436,4 @@ def test_page_select_bit_exact_group_sizes(Hq, Hkv, d, P):
     cache.select(q, sel, cache.workspace(top_k=16))
     torch.cuda.synchronize()
     assert int(cache.dev_err.item()) == 0
-    np.testing.assert_array_equal(sel.cpu().numpy(), _oracle_selection(case, cache, q))
+    _check_selection(case, cache, q, sel)

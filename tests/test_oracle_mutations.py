@@ -48,11 +48,15 @@ MUTATIONS = [
     ("stats miss the last token of a page", "        for (int64_t t = t0 + 1; t < t1; ++t) {",
      "        for (int64_t t = t0 + 1; t + 1 < t1; ++t) {"),
     ("score ignores k_min", "        acc += a > b ? a : b;", "        acc += a;"),
-    ("fp32 score pairs k_min with the positive part",
-     "        x[nch + c] = decision_partial(q, kmin, c * w, w, 1);",
-     "        x[nch + c] = decision_partial(q, kmin, c * w, w, 0);"),
-    ("physical score keeps the last logical page", "                    if (s > best) best = s;",
-     "                    best = s;"),
+    ("fp32 bound misses the factor d",
+     "    return (double)d * ldexp(1.0, -23) * abs_sum + 2.0 * d * ldexp(1.0, -150);",
+     "    return ldexp(1.0, -23) * abs_sum + 2.0 * d * ldexp(1.0, -150);"),
+    ("fp32 bound sums signed terms", "        abs_sum += fabs(a > b ? a : b);",
+     "        abs_sum += a > b ? a : b;"),
+    ("physical bound keeps the last logical page", "                if (e > err) err = e;",
+     "                err = e;"),
+    ("physical score keeps the last logical page", "                if (s > best) best = s;",
+     "                best = s;"),
     ("top-K ties go to the higher page",
      "            if (best < 0 || score[i] > score[best]) best = i; /* strict: lower index wins ties */",
      "            if (best < 0 || score[i] >= score[best]) best = i;"),

@@ -283,8 +283,7 @@ def test_page_score_worked_example(orc):
     kmax, kmin = orc.logical_page_stats(keys, 0, len(g["keys"]))
     np.testing.assert_array_equal(f64(kmax), g["kmax"])
     np.testing.assert_array_equal(f64(kmin), g["kmin"])
-    assert orc.logical_score(bf(g["q"]), kmax, kmin, precision64=True) == g["score"]
-    assert orc.logical_score(bf(g["q"]), kmax, kmin, precision64=False) == g["score"]
+    assert orc.logical_score(bf(g["q"]), kmax, kmin) == g["score"]
     np.testing.assert_array_equal(f64(keys) @ f64(bf(g["q"])), g["qk"])
 
 
@@ -296,27 +295,85 @@ def test_page_score_bounds_every_key_and_is_tight_for_one_key(orc):
         K = rand_bf(rng, n, d)
         q = rand_bf(rng, d)
         kmax, kmin = orc.logical_page_stats(K, 0, n)
-        s = orc.logical_score(q, kmax, kmin, precision64=True)
+        s = orc.logical_score(q, kmax, kmin)
         qk = f64(K) @ f64(q)
         assert np.all(qk <= s + 1e-12)
         if n == 1:
             assert s == pytest.approx(qk[0], rel=1e-15, abs=1e-15)
 
 
-def test_fp32_decision_score_within_fp32_bound_of_fp64(orc):
+def _fp32_sums(terms, rng):
+    """fp32 sums of exact fp32 terms in several orders: ascending, descending, a pairwise
+    tree, random permutations, and the 2d-term sum of a k_max half and a k_min half."""
+    t = np.asarray(terms, np.float32)
+
+    def seq(v):
+        acc = np.float32(0.0)
+        for x in v:
+            acc = np.float32(acc + x)
+        return acc
+
+    def tree(v):
+        v = list(v)
+        while len(v) > 1:
+            v = [np.float32(v[i] + v[i + 1]) if i + 1 < len(v) else v[i]
+                 for i in range(0, len(v), 2)]
+        return v[0]
+
+    sums = [seq(t), seq(t[::-1]), tree(t), tree(t[::-1])]
+    sums += [seq(rng.permutation(t)) for _ in range(4)]
+    sums += [tree(rng.permutation(t)) for _ in range(4)]
+    halves = np.concatenate([np.where(t >= 0, t, 0), np.where(t >= 0, 0, t)]).astype(np.float32)
+    sums += [tree(halves), seq(halves)]
+    return [float(x) for x in sums]
+
+
+def test_fp32_bound_covers_fp32_sums_in_any_order(orc):
+    """The error bound of reading R9 holds for fp32 evaluations of the score in any order."""
     rng = np.random.default_rng(10)
-    d = 128
-    for _ in range(50):
-        K = rand_bf(rng, 16, d)
+    for trial in range(60):
+        d = (64, 128)[trial % 2]
+        n = 1 + trial % 16
+        K = rand_bf(rng, n, d, scale=(1.0, 8.0, 1e-3)[trial % 3])
         q = rand_bf(rng, d)
-        kmax, kmin = orc.logical_page_stats(K, 0, 16)
-        s64 = orc.logical_score(q, kmax, kmin, precision64=True)
-        s32 = orc.logical_score(q, kmax, kmin, precision64=False)
+        kmax, kmin = orc.logical_page_stats(K, 0, n)
+        s64 = orc.logical_score(q, kmax, kmin)
+        bound = orc.logical_score_bound(q, kmax, kmin)
+        # products of two bf16 values are exact in fp32, so the terms are
         qd = f64(q)
-        terms = np.maximum(qd * f64(kmax), qd * f64(kmin))
-        bound = d * 2.0 ** -24 * np.abs(terms).sum()
-        assert abs(s32 - s64) <= bound
-        assert np.float32(s32) == s32  # representable in fp32
+        terms = np.where(qd >= 0, qd * f64(kmax), qd * f64(kmin))
+        assert np.all(np.float32(terms) == terms)
+        for s32 in _fp32_sums(terms, rng):
+            assert abs(s32 - s64) <= bound, (trial, s32, s64, bound)
+
+
+def test_fp32_bound_is_reached_by_adversarial_sums(orc):
+    """Sums whose fp32 evaluation loses what the bound must cover: the factor d (127 terms
+    of 2^-24 absorbed by a leading 1) and the absolute values (1 + 2^-25 - 1 evaluates to 0)."""
+    d = 128
+    q = bf(np.ones(d))
+    k = np.full(d, 2.0 ** -24)
+    k[0] = 1.0
+    kb = bf(k)
+    s64 = orc.logical_score(q, kb, kb)
+    assert s64 == 1.0 + 127 * 2.0 ** -24
+    acc = np.float32(0.0)  # sequential fp32 sum: every 2^-24 is lost against the leading 1
+    for x in f64(kb):
+        acc = np.float32(acc + np.float32(x))
+    assert float(acc) == 1.0
+    assert orc.logical_score_bound(q, kb, kb) >= s64 - 1.0
+    q2 = np.zeros(d)
+    q2[:3] = 1.0
+    k2 = np.zeros(d)
+    k2[:3] = [1.0, 2.0 ** -25, -1.0]
+    q2b, k2b = bf(q2), bf(k2)
+    s64 = orc.logical_score(q2b, k2b, k2b)
+    assert s64 == 2.0 ** -25
+    acc = np.float32(0.0)
+    for x in f64(k2b)[:3]:
+        acc = np.float32(acc + np.float32(x))
+    assert float(acc) == 0.0
+    assert orc.logical_score_bound(q2b, k2b, k2b) >= s64
 
 
 def test_physical_score_is_max_over_logical_pages_and_heads(orc):
@@ -324,15 +381,16 @@ def test_physical_score_is_max_over_logical_pages_and_heads(orc):
     d, P, L, g = 32, 64, 150, 3
     K = rand_bf(rng, L, d)
     Q = rand_bf(rng, g, d)
-    sc = orc.page_scores(Q, K, L, P, precision64=True)
-    assert sc.shape == (3,)
+    sc, bd = orc.page_scores(Q, K, L, P, with_bounds=True)
+    assert sc.shape == (3,) and bd.shape == (3,)
     for p in range(3):
-        best = -math.inf
+        best, err = -math.inf, 0.0
         for t0 in range(p * P, min((p + 1) * P, L), 16):
             kmax, kmin = orc.logical_page_stats(K, t0, min(t0 + 16, L))
             for j in range(g):
-                best = max(best, orc.logical_score(Q[j], kmax, kmin, precision64=True))
-        assert sc[p] == best
+                best = max(best, orc.logical_score(Q[j], kmax, kmin))
+                err = max(err, orc.logical_score_bound(Q[j], kmax, kmin))
+        assert sc[p] == best and bd[p] == err
     # the max over logical pages bounds every key of the physical page, for every head
     qk = f64(K) @ f64(Q).T
     for t in range(L):
