@@ -72,7 +72,7 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="mha-32k", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--config", default="mha-1m", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--impl", default="dattn", choices=["dattn", "reference"])
     ap.add_argument("--kv-format", default="bf16", choices=["bf16", "fp8", "int4"],
                     help="element format of the paged KV pool")
@@ -294,7 +294,64 @@ def reduce_over_ranks(ms_total: float, units: float, world: int, device) -> tupl
     return float(tmax[0]), float(t[1])
 
 
-KERNEL_EVERY = 8  # steps between the ones whose decode kernel is timed on its own
+KERNEL_EVERY = 8  # at most this many steps between the ones whose decode kernel is timed
+
+
+def kernel_every(steps: int) -> int:
+    """Steps between the ones whose decode kernel is timed on its own: every 8th, but often
+    enough that at least 10 launches are timed whenever there are 10 steps or more."""
+    return max(1, min(KERNEL_EVERY, steps // 10))
+
+
+L2_FALLBACK_BYTES = 129 * 10 ** 6  # GB300's L2, when no device can be asked
+
+
+def device_l2_bytes() -> int:
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except Exception:
+        pass
+    return L2_FALLBACK_BYTES
+
+
+def l2_policy(case, args) -> tuple:
+    """(flush?, text) for the timed steps: a step whose K/V is more than 4x the L2 evicts what
+    the previous step left there and runs back to back; smaller steps are preceded by an L2
+    flush (L2Flush). Both arms state the same text in their config."""
+    sparse = case.head_kind is not None
+    sb0 = step_bytes(case, list(case.lens), sparse, args.kv_format, args.queries)
+    l2 = device_l2_bytes()
+    flush = sb0["decode"] < 4 * l2 or args.flush
+    text = (f"flushed before every timed step ({L2Flush.TEXT})" if flush else
+            f"inputs larger than L2: {sb0['decode'] / 1e9:.2f} GB of K/V per step vs "
+            f"{l2 / 1e6:.0f} MB L2, timed back to back without a flush")
+    return flush, text
+
+
+def measure_read_peak(dev, gib: int = 4, reps: int = 10) -> float:
+    """A read-only HBM stream for context beside the copy peak: torch.sum over `gib` GiB of
+    fp32, best of `reps`, timed with CUDA events (GB/s of bytes read)."""
+    import torch
+    x = torch.ones(gib * (1 << 30) // 4, dtype=torch.float32, device=dev)
+    acc = torch.empty((), dtype=torch.float32, device=dev)
+    torch.sum(x, dim=0, out=acc)
+    best = float("inf")
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        torch.sum(x, dim=0, out=acc)
+        b.record()
+        b.synchronize()
+        best = min(best, a.elapsed_time(b))
+    del x
+    torch.cuda.empty_cache()
+    return gib * (1 << 30) / (best * 1e-3) / 1e9
+
+
+READ_PEAK_HOW = "torch.sum over 4 GiB of fp32, best of 10, CUDA events (bytes read)"
 
 
 class L2Flush:
@@ -356,12 +413,10 @@ def run_dattn(args, rank: int, world: int):
     news = [(k_all[:, s * T:(s + 1) * T].contiguous(), v_all[:, s * T:(s + 1) * T].contiguous())
             for s in range(total)]
     del k_all, v_all
-    # L2 hygiene: a step whose K/V working set exceeds 4x the L2 evicts everything the
-    # previous step left there, so it is timed back to back; smaller steps are preceded by
-    # an L2 flush (see L2Flush).
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    sb0 = step_bytes(case, list(cache.lens), sparse, fmt, T)
-    do_flush = sb0["decode"] < 4 * l2 or args.flush
+    # L2 hygiene (l2_policy): steps whose K/V is over 4x the L2 run back to back, smaller
+    # ones after an L2 flush
+    do_flush, l2_text = l2_policy(case, args)
+    every = kernel_every(args.steps)
     flush = L2Flush(dev)
     torch.cuda.synchronize()
 
@@ -405,7 +460,7 @@ def run_dattn(args, rank: int, world: int):
             return g, n
         for i in range(args.steps):
             s = args.warmup + i
-            if i % KERNEL_EVERY == 0:
+            if i % every == 0:
                 graphs[s] = (capture(pre_step, s), capture(dec_step, s))
             else:
                 graphs[s] = (capture(one_step, s),)
@@ -426,11 +481,11 @@ def run_dattn(args, rank: int, world: int):
             flush()  # outside the timed region
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        # Every KERNEL_EVERY-th step also brackets the decode kernel with events. An event
+        # Every `every`-th step also brackets the decode kernel with events. An event
         # between two launches keeps the second from starting early (programmatic dependent
         # launch), so the other steps run without it.
         kev = None
-        if i % KERNEL_EVERY == 0:
+        if i % every == 0:
             kev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         e0.record(stream)
         if not args.graph:
@@ -465,9 +520,7 @@ def run_dattn(args, rank: int, world: int):
         raise RuntimeError(f"device error word {err:#x}")
     ms_max, bytes_all = reduce_over_ranks(sum(step_t), float(bytes_total), world, dev)
     res = {
-        "l2_policy": (f"flushed before every timed step ({L2Flush.TEXT})" if do_flush else
-                      f"inputs larger than L2: {sb0['decode'] / 1e9:.2f} GB of K/V per step "
-                      f"vs {l2 / 1e6:.0f} MB L2, timed back to back without a flush"),
+        "l2_policy": l2_text, "kernel_every": every,
         "ms_total": ms_max, "bytes_all": bytes_all, "step_ms": step_t, "dec_ms": dec_t,
         "dec_bytes": dec_bytes_total / len(dec_ms), "launches": launches, "clocks": clk,
         "case": case, "lens0": lens0,
@@ -481,6 +534,8 @@ def run_dattn(args, rank: int, world: int):
     # ---- end to end through the public API with host buffers (pinned) ----------------
     if not args.no_e2e and not args.profile:
         res["e2e"] = run_e2e(args, case, cache, ws, spc, sel, flush if do_flush else None, dev)
+    if rank == 0 and not args.profile:
+        res["read_peak"] = measure_read_peak(dev)
     return res
 
 
@@ -859,7 +914,7 @@ def run_reference(args, rank, world):
                           "unit": "TFLOP/s", "n_gpus": world, "steps": 1, "warmup": 0,
                           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                           "dtype": "f64", "data": "synthetic", "cpu_baseline": cpu,
-                          "config": {"workload": f"{case.name}: {WORKLOAD_TEXT[case.name]}"},
+                          "config": prefill_config(case, args, case.lens[0]),
                           "e2e": {"value": cpu["value"], "unit": "TFLOP/s",
                                   "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
               flush=True)
@@ -1098,6 +1153,18 @@ def prefill_cpu_baseline(case, device, kinds, lists, sinks, local, Tq, target_s:
                       f"rows: {pairs} query-key pairs in {secs:.1f} s wall"}
 
 
+def prefill_config(case, args, Tq: int) -> dict:
+    """The config object of the prefill leg, the same in both arms."""
+    return {"workload": f"{case.name}: {WORKLOAD_TEXT[case.name]}" +
+                        (" (every head dense: causal attention)" if args.prefill_dense else ""),
+            "batch": case.B, "q_heads": case.Hq, "kv_heads": case.Hkv, "head_dim": case.d,
+            "page_size": case.P, "context_tokens": case.lens[0], "chunk_tokens": Tq,
+            "seed": args.seed, "parallelism": "replicas" if args.gpus > 1 else "single GPU",
+            "step": "dattn_kv_append (the chunk's K/V) + dattn_prefill",
+            "l2": f"flushed before every timed step ({L2Flush.TEXT})",
+            "launch": "eager library calls"}
+
+
 def prefill_main(args, rank: int, world: int):
     from split_kv_decode_distattention_gb300 import workloads as W
     res = run_prefill(args, rank, world)
@@ -1118,14 +1185,7 @@ def prefill_main(args, rank: int, world: int):
     peak = float(peaks.get("bf16_tflops", 1900.0))
     tflops = res["flops"] / (res["ms"] * 1e-3) / 1e12
     ktf = res["flops_rank"] / (res["kms"] * 1e-3) / 1e12
-    cfg = {"workload": f"{case.name}: {WORKLOAD_TEXT[case.name]}" +
-                       (" (every head dense: causal attention)" if dense else ""),
-           "batch": case.B, "q_heads": case.Hq, "kv_heads": case.Hkv, "head_dim": case.d,
-           "page_size": case.P, "context_tokens": case.lens[0], "chunk_tokens": res["Tq"],
-           "seed": args.seed, "parallelism": "replicas" if args.gpus > 1 else "single GPU",
-           "step": "dattn_kv_append (the chunk's K/V) + dattn_prefill",
-           "l2": f"flushed before every timed step ({L2Flush.TEXT})",
-           "launch": "eager library calls"}
+    cfg = prefill_config(case, args, res["Tq"])
     line = {
         "metric": PREFILL_METRIC, "value": round(tflops, 2), "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -1165,7 +1225,8 @@ def config_obj(case, args):
                   f"dattn_kv_append ({args.queries} tokens/request) + dattn_decode_multi "
                   f"({args.queries} query tokens/request, causal over the new tokens)"),
          "launch": ("one CUDA graph per step, captured from the library calls"
-                    if getattr(args, "graph", False) else "eager library calls")}
+                    if getattr(args, "graph", False) else "eager library calls"),
+         "l2": l2_policy(case, args)[1]}
     if args.queries > 1:
         c["queries_per_request"] = args.queries
     if args.batch or args.ctx:
@@ -1206,6 +1267,7 @@ def main():
     ms_step = res["ms_total"] / steps
     value = res["bytes_all"] / (res["ms_total"] * 1e-3) / 1e9
     dec_avg_ms = sum(res["dec_ms"]) / len(res["dec_ms"])
+    dec_med_ms = statistics.median(res["dec_ms"])
     achieved = res["dec_bytes"] / (dec_avg_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
     traffic = traffic_record(traffic_key(args))
@@ -1221,15 +1283,20 @@ def main():
                  "int4": "; K/V quantized to 4 bits by the append)"}[args.kv_format],
         "us_per_layer_step": round(ms_step * 1e3, 2),
         "frac_of_8tbs": round(value / ROOFLINE_8TBS, 4),
-        "config": dict(config_obj(case, args), l2=res["l2_policy"]),
+        "config": config_obj(case, args),
         "roofline": {"bound": "hbm", "kernel": "attention_kernel (dattn_decode)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "frac": round(achieved / peak, 4),
+                     "peak_source": (f"{peak_kind}: HBM copy bandwidth (read + write bytes of a "
+                                     f"copy); the decode kernel only reads, see read_peak"),
                      "traffic": traffic, "algorithmic_bytes_per_launch": int(res["dec_bytes"]),
                      "avg_launch_us": round(dec_avg_ms * 1e3, 2),
+                     "median_launch_us": round(dec_med_ms * 1e3, 2),
+                     "achieved_at_median": round(res["dec_bytes"] / (dec_med_ms * 1e-3) / 1e9, 1),
+                     "frac_of_8tbs": round(achieved / ROOFLINE_8TBS, 4),
                      "timed_launches": len(res["dec_ms"]),
                      "kernel_timing": f"CUDA events around the decode kernel in every "
-                                      f"{KERNEL_EVERY}th timed step",
+                                      f"{res['kernel_every']}th timed step",
                      "launch_us_min_med_max": [round(min(res["dec_ms"]) * 1e3, 1),
                                                round(statistics.median(res["dec_ms"]) * 1e3, 1),
                                                round(max(res["dec_ms"]) * 1e3, 1)]},
@@ -1237,6 +1304,9 @@ def main():
         "clocks": res["clocks"],
         "cpu_baseline": cpu,
     }
+    if "read_peak" in res:
+        line["roofline"]["read_peak"] = {"gbs": round(res["read_peak"], 1), "how": READ_PEAK_HOW,
+                                         "frac": round(achieved / res["read_peak"], 4)}
     if "info" in res:
         line["info"] = res["info"]
     if "e2e" in res:

@@ -191,7 +191,10 @@ dattn_status_t dattn_kv_append(const dattn_kv_layout *layout, void *k_pool,
  *   q          (device) bf16 [B][Hq][d]
  *   seq_lens   (device) int32 [B]
  *   chunk_req  (device) int32 [C]
- *   chunk_page_indptr (device) int32 [C+1], non-decreasing, starting at 0
+ *   chunk_page_indptr (device) int32 [C+1], non-decreasing, starting at 0. A chunk whose
+ *              range is reversed, starts below 0, ends past chunk_page_indptr[C] or holds
+ *              more than max_pages_per_req pages is flagged with DATTN_DEVERR_CHUNK_OOB and
+ *              left empty; its pages are not read.
  *   chunk_pages (device) int32 [chunk_page_indptr[C]]
  *   m, e       (device) fp32 [C][Hq];  MA (device) fp32 [C][Hq][d]
  *   ws, ws_bytes  workspace, at least dattn_workspace_size(C, Hq, Hkv, d, 0, num_splits)

@@ -888,8 +888,11 @@ attention_kernel(const __grid_constant__ AttnParams p,
             int32_t cnt;
             if (p.mode == MODE_PARTIAL) {
                 const int32_t b = p.chunk_req[i];
-                int32_t npg = p.chunk_indptr[i + 1] - p.chunk_indptr[i];
-                if (b < 0 || b >= p.B || npg < 0 || npg > p.max_pages) {
+                const int32_t c0 = p.chunk_indptr[i], c1 = p.chunk_indptr[i + 1];
+                int32_t npg = c1 - c0;
+                // the chunk's page list must lie inside chunk_pages[0, chunk_indptr[C])
+                if (b < 0 || b >= p.B || c0 < 0 || c1 > p.chunk_indptr[p.C] || npg < 0 ||
+                    npg > p.max_pages) {
                     set_err(p.dev_err, DATTN_DEVERR_CHUNK_OOB);
                     npg = 0;
                 }

@@ -188,6 +188,41 @@ def test_dense_tiny_partial_then_merge(seed):
     check_dense(case, q, [4096], out, m_g, e_g, DEV, what="merged")
 
 
+def test_partial_flags_chunk_page_ranges_outside_the_list():
+    """A chunk whose page range starts below 0, or ends past chunk_page_indptr[C], is flagged
+    with CHUNK_OOB and left empty (m = -inf, e = 0, MA = 0); its pages are never read. The
+    valid chunk beside it is computed as usual."""
+    dattn = _lib()
+    case = W.Case("badchunk", B=1, Hq=4, Hkv=2, d=64, P=16, lens=[160], seed=4)
+    cache = _cache(case)
+    q = case.q(0, DEV)
+    # list ranges: chunk 0 [0, 3) is valid; chunk 1 [3, -2) has a negative count; chunk 2
+    # [-2, 7) starts before the list and ends past indptr[C] = 5; chunk 3 [7, 5) lies past the
+    # end. Only chunk 0 is computed.
+    C = 4
+    chunk_req = torch.zeros(C, dtype=torch.int32, device=DEV)
+    indptr = torch.tensor([0, 3, -2, 7, 5], dtype=torch.int32, device=DEV)
+    pages = torch.tensor([0, 1, 2, 5, 6], dtype=torch.int32, device=DEV)
+    m = torch.empty(C, case.Hq, device=DEV)
+    e = torch.empty_like(m)
+    MA = torch.empty(C, case.Hq, case.d, device=DEV)
+    ws = dattn.Workspace(C, case.Hq, case.Hkv, case.d)
+    dattn.dattn_partial(cache.layout, cache.k_pool, cache.v_pool, q, case.scale, cache.seq_lens,
+                        chunk_req, indptr, pages, m, e, MA, ws, dev_err=cache.dev_err)
+    torch.cuda.synchronize()
+    assert int(cache.dev_err.item()) & dattn.DEVERR["CHUNK_OOB"]
+    for c in (1, 2, 3):
+        assert (m[c] == -math.inf).all() and (e[c] == 0).all() and (MA[c] == 0).all(), c
+    K, V = host_kv(case, 0, 160, DEV)
+    qb = oracle.bf16_bits(q)
+    for h in range(case.Hq):
+        rm, re, rMA = oracle.partial(qb[0, h], K[:, h // case.g].copy(),
+                                     V[:, h // case.g].copy(), case.scale, rows=np.arange(48))
+        assert_m_close(m[0, h].item(), rm, f"chunk 0 head {h}")
+        assert_e_close(e[0, h].item(), re, f"chunk 0 head {h}")
+        assert_out_close(MA[0, h].cpu().numpy() / e[0, h].item(), rMA / re, f"chunk 0 head {h}")
+
+
 def test_page_sets_partials_merge_to_fused_decode():
     """Ragged GQA batch; each request's pages split into 2-8 disjoint non-contiguous sets."""
     dattn = _lib()

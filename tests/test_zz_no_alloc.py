@@ -4,9 +4,10 @@ Some callers cannot allocate device memory: a plugin or custom op given only its
 output pointers, code under a framework allocator that owns all device memory, or a
 latency-critical path that cannot risk cudaMalloc's implicit synchronisation. For them the
 library keeps its decode scratch in a static 8 MiB device array. This test checks that two
-calls in a row through that entry point match the workspace-based dattn_decode within the
-parity tolerance used everywhere else. Between the calls the query changes, and the shared
-scratch must not carry state from one call to the next. It runs alone in a fresh process
+calls in a row through that entry point match the workspace-based dattn_decode, and the
+oracle's full softmax attention, within the parity tolerance used everywhere else. Between
+the calls the query changes, and the shared scratch must not carry state from one call to
+the next: a stale merge counter would leave heads unmerged and fail the oracle check. It runs alone in a fresh process
 as well as after the rest of the suite, which is why pytest collects it last.
 """
 import ctypes
@@ -14,14 +15,12 @@ import ctypes
 import pytest
 import torch
 
-from _util import assert_out_close
+from _util import assert_out_close, check_dense
 
 pytestmark = pytest.mark.gpu
 
 
 def _lib():
-    from split_kv_decode_distattention_gb300 import _build
-    _build.build()
     import split_kv_decode_distattention_gb300 as dattn
     dattn.load_library()
     return dattn
@@ -53,6 +52,7 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls(splits):
         assert_out_close(out.cpu().numpy(), ref.cpu().numpy(), f"call {call}")
         assert torch.allclose(m_g, ref_m, rtol=1e-5, atol=0)
         assert torch.allclose(e_g, ref_e, rtol=1e-4, atol=0)
+        check_dense(case, q, case.lens, out, m_g, e_g, "cuda", what=f"noalloc call {call}")
 
 
 def test_noalloc_rejects_problems_beyond_the_static_scratch():
