@@ -84,6 +84,9 @@ def parse_args():
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling only)")
     ap.add_argument("--ctx", type=int, default=0, help="override the context (profiling only)")
     ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--unfused", action="store_true",
+                    help="step = dattn_kv_append then dattn_decode (two launches) instead of "
+                         "dattn_append_decode (bf16 pool, one query token)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -100,6 +103,12 @@ def parse_args():
 def info_steps(args) -> int:
     """Steps of each informational pass after the timed region (warm L2, CUDA graphs)."""
     return 0 if (args.profile or args.no_info) else min(64, args.steps)
+
+
+def fused_step(args) -> bool:
+    """A step is one dattn_append_decode launch (the bf16 pool, one query token per request)
+    unless --unfused asks for dattn_kv_append then dattn_decode."""
+    return not args.unfused and args.kv_format == "bf16" and args.queries == 1
 
 
 def make_case(args):
@@ -167,9 +176,10 @@ def step_bytes(case, lens_after, sparse_sel_step: bool, fmt: str = "bf16", T: in
         l0 = max(case.sinks, L - case.local)
         kv += nstr * (s_end + max(0, L - l0)) * rb * 2
     sel_rows = B * nret * case.top_k * 4
-    decode = kv + q_bytes + out_bytes + sel_rows + B * 4
+    # the decode reads the selection rows and their pool pages (dattn_sparse.selected_phys)
+    decode = kv + q_bytes + out_bytes + 2 * sel_rows + B * 4
     stats = sum(L // 16 + (1 if L % 16 else 0) for L in lens_after) * nret * 2 * d * 2
-    select = (stats + q_bytes + sel_rows + bt) if sparse_sel_step else 0
+    select = (stats + q_bytes + 2 * sel_rows + bt) if sparse_sel_step else 0
     # the stats update inside the append (read + write one logical page per request/head)
     new_kv += B * Hkv * 2 * d * 2 * 2
     return {"decode": decode, "append": new_kv, "select": select,
@@ -396,7 +406,9 @@ def run_dattn(args, rank: int, world: int):
     m_g = torch.empty(*qshape, dtype=torch.float32, device=dev)
     e_g = torch.empty(*qshape, dtype=torch.float32, device=dev)
     sel = torch.full((B, case.Hkv, max(case.top_k, 1)), -1, dtype=torch.int32, device=dev)
-    spc = cache.sparse_config(sel) if sparse else None
+    sel_phys = torch.full_like(sel, -1)
+    spc = cache.sparse_config(sel, sel_phys) if sparse else None
+    fused = fused_step(args)
     stream = torch.cuda.current_stream()
     n_info = info_steps(args)
     total = args.warmup + args.steps + 3 * n_info + 1
@@ -420,16 +432,25 @@ def run_dattn(args, rank: int, world: int):
     flush = L2Flush(dev)
     torch.cuda.synchronize()
 
-    def pre_step(s):  # the append, and at the start of a reuse window the selection
-        kn, vn = news[s]
-        cache.append(kn, vn)
+    def pre_step(s):  # the append (unless fused), and at a reuse window's start the selection
+        n = 0
+        if not fused:
+            kn, vn = news[s]
+            cache.append(kn, vn)
+            n += 1
         if sparse and s % case.reuse == 0:
-            cache.select(qs[s], sel, ws, num_splits=args.num_splits)
-            return 2
-        return 1
+            cache.select(qs[s], sel, ws, num_splits=args.num_splits, selected_phys=sel_phys)
+            n += 1
+        return n
 
     def dec_step(s):
-        cache.decode(qs[s], out, ws, m_g=m_g, e_g=e_g, sparse=spc, num_splits=args.num_splits)
+        if fused:
+            kn, vn = news[s]
+            cache.append_decode(kn, vn, qs[s], out, ws, m_g=m_g, e_g=e_g, sparse=spc,
+                                num_splits=args.num_splits)
+        else:
+            cache.decode(qs[s], out, ws, m_g=m_g, e_g=e_g, sparse=spc,
+                         num_splits=args.num_splits)
         return 1
 
     def one_step(s, ev=None):
@@ -507,7 +528,8 @@ def run_dattn(args, rank: int, world: int):
         bytes_total += sb["step"]
         step_ms.append((e0, e1))
         if kev is not None:
-            dec_bytes_total += sb["decode"]
+            # the timed kernel is the decode launch (with the fused step, also the append)
+            dec_bytes_total += sb["decode"] + (sb["append"] if fused else 0)
             dec_ms.append(kev)
     torch.cuda.synchronize()
     if world > 1:
@@ -529,23 +551,26 @@ def run_dattn(args, rank: int, world: int):
     # ---- information only (outside the timed region): warm L2, CUDA graphs, the append ---
     if n_info:
         res["info"] = run_info(args, case, cache, one_step, news, qs, ws, out, m_g, e_g, spc, sel,
-                               flush if do_flush else None, args.warmup + args.steps, n_info)
+                               flush if do_flush else None, args.warmup + args.steps, n_info,
+                               fused=fused, sel_phys=sel_phys)
 
     # ---- end to end through the public API with host buffers (pinned) ----------------
     if not args.no_e2e and not args.profile:
-        res["e2e"] = run_e2e(args, case, cache, ws, spc, sel, flush if do_flush else None, dev)
+        res["e2e"] = run_e2e(args, case, cache, ws, spc, sel, flush if do_flush else None, dev,
+                             fused=fused, sel_phys=sel_phys)
     if rank == 0 and not args.profile:
         res["read_peak"] = measure_read_peak(dev)
     return res
 
 
-def run_info(args, case, cache, one_step, news, qs, ws, out, m_g, e_g, spc, sel, flush, s0, n):
+def run_info(args, case, cache, one_step, news, qs, ws, out, m_g, e_g, spc, sel, flush, s0, n,
+             fused=False, sel_phys=None):
     """Informational timings after the timed region, microseconds per step as mean (the
     headline's averaging: it includes the steps that run the selection) and median:
     - eager: eager library calls, flushed like the timed steps;
     - graph: each step captured once in a CUDA graph and replayed, flushed likewise;
     - warm_l2: the captured steps replayed back to back without an L2 flush;
-    - append: the kv append kernel of an eager step timed on its own."""
+    - append: the kv append kernel of an eager step timed on its own (two-launch steps)."""
     import torch
     stream = torch.cuda.current_stream()
     sparse = case.head_kind is not None
@@ -564,17 +589,25 @@ def run_info(args, case, cache, one_step, news, qs, ws, out, m_g, e_g, spc, sel,
         e0, e1, e2 = ev(), ev(), ev()
         e0.record(stream)
         kn, vn = news[s]
-        cache.append(kn, vn)
-        e1.record(stream)
-        if sparse and s % case.reuse == 0:
-            cache.select(qs[s], sel, ws, num_splits=args.num_splits)
-        cache.decode(qs[s], out, ws, m_g=m_g, e_g=e_g, sparse=spc, num_splits=args.num_splits)
+        if fused:
+            if sparse and s % case.reuse == 0:
+                cache.select(qs[s], sel, ws, num_splits=args.num_splits, selected_phys=sel_phys)
+            cache.append_decode(kn, vn, qs[s], out, ws, m_g=m_g, e_g=e_g, sparse=spc,
+                                num_splits=args.num_splits)
+        else:
+            cache.append(kn, vn)
+            e1.record(stream)
+            apps.append((e0, e1))
+            if sparse and s % case.reuse == 0:
+                cache.select(qs[s], sel, ws, num_splits=args.num_splits, selected_phys=sel_phys)
+            cache.decode(qs[s], out, ws, m_g=m_g, e_g=e_g, sparse=spc,
+                         num_splits=args.num_splits)
         e2.record(stream)
         steps.append((e0, e2))
-        apps.append((e0, e1))
     torch.cuda.synchronize()
     info["eager_us_per_step"] = stat(steps)
-    info["append_us"] = stat(apps)
+    if apps:
+        info["append_us"] = stat(apps)
     # CUDA graphs: one graph per step (its inputs differ), replayed in order
     graphs = []
     side = torch.cuda.Stream()
@@ -609,7 +642,7 @@ def run_info(args, case, cache, one_step, news, qs, ws, out, m_g, e_g, spc, sel,
     return info
 
 
-def run_e2e(args, case, cache, ws, spc, sel, flush, dev):
+def run_e2e(args, case, cache, ws, spc, sel, flush, dev, fused=False, sel_phys=None):
     """The same steps through the public API with host buffers: every step copies its q and
     new K/V from pinned host memory and reads its output back into pinned host memory."""
     import torch
@@ -644,10 +677,14 @@ def run_e2e(args, case, cache, ws, spc, sel, flush, dev):
         dq.copy_(hq[i], non_blocking=True)
         dk.copy_(hk[i], non_blocking=True)
         dv.copy_(hv[i], non_blocking=True)
-        cache.append(dk, dv)
+        if not fused:
+            cache.append(dk, dv)
         if spc is not None and i % case.reuse == 0:
-            cache.select(dq, sel, ws)
-        cache.decode(dq, out, ws, sparse=spc)
+            cache.select(dq, sel, ws, selected_phys=sel_phys)
+        if fused:
+            cache.append_decode(dk, dv, dq, out, ws, sparse=spc)
+        else:
+            cache.decode(dq, out, ws, sparse=spc)
         houts[i].copy_(out, non_blocking=True)
         if flush is not None:
             e1 = torch.cuda.Event(enable_timing=True)
@@ -1218,7 +1255,9 @@ def config_obj(case, args):
          "seed": args.seed,
          "kv_format": KV_FORMAT_NOTE[args.kv_format],
          "parallelism": "replicas" if args.gpus > 1 else "single GPU",
-         "step": ("dattn_kv_append (1 token/request) + dattn_decode" +
+         "step": (("dattn_append_decode (1 token/request appended and attended in one launch)"
+                   if fused_step(args) else
+                   "dattn_kv_append (1 token/request) + dattn_decode") +
                   (" + dattn_page_select every 16 steps (block-sparse)"
                    if case.head_kind is not None else "")
                   if args.queries == 1 else
@@ -1284,7 +1323,9 @@ def main():
         "us_per_layer_step": round(ms_step * 1e3, 2),
         "frac_of_8tbs": round(value / ROOFLINE_8TBS, 4),
         "config": config_obj(case, args),
-        "roofline": {"bound": "hbm", "kernel": "attention_kernel (dattn_decode)",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("attention_kernel (dattn_append_decode)" if fused_step(args)
+                                else "attention_kernel (dattn_decode)"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "peak_source": (f"{peak_kind}: HBM copy bandwidth (read + write bytes of a "

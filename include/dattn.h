@@ -150,6 +150,13 @@ typedef struct dattn_sparse {
     const int32_t *selected;  /* (device) [B][Hkv][top_k] request-relative physical page
                                  indices from dattn_page_select; -1 entries are ignored.
                                  A page must not appear twice in one row. */
+    const int32_t *selected_phys; /* (device, nullable) [B][Hkv][top_k]: the pool pages of
+                                 `selected` (block_table[b][selected[..]]), as
+                                 dattn_page_select writes them. When given, the decode reads
+                                 them instead of looking the pages up in the block table, which
+                                 saves a dependent load before the first copy of a step. The
+                                 block-table entries of selected pages must then not change
+                                 while the selection is in use. */
 } dattn_sparse;
 
 /*
@@ -277,6 +284,30 @@ dattn_status_t dattn_decode_multi(const dattn_kv_layout *layout, const void *k_p
                                   float *m_g, float *e_g, int32_t *dev_err, void *stream);
 
 /*
+ * One decode step with its append, in one launch: exactly dattn_kv_append of one new token
+ * per request (T = 1) followed by dattn_decode, for the bf16 pool. [LS §4.2: the master saves
+ * the new token's KV locally, then every instance attends over its KV including it.] The new
+ * token of request b is written at position seq_lens[b] (and the logical-page statistics take
+ * it in when stats is not NULL); the decode attends tokens 0 .. seq_lens[b] (the new one
+ * included); on return seq_lens[b] has advanced by one. Outputs, pool, statistics, lengths
+ * and error bits are those of the two separate calls. Saving the second launch and the wait
+ * between them shortens a step by the append's latency.
+ *
+ *   k_pool, v_pool, stats, k_new, v_new  as for dattn_kv_append (bf16 [B][1][Hkv][d] new rows)
+ *   q, scale, sparse, num_splits, out, m_g, e_g  as for dattn_decode
+ *   seq_lens (device) int32 [B]: lengths before the step; advanced by one
+ *   ws, ws_bytes  workspace of at least dattn_workspace_size(B, Hq, Hkv, d, 0, num_splits)
+ * A quantized pool (kv_format != DATTN_KV_BF16) returns DATTN_ERR_UNSUPPORTED.
+ */
+dattn_status_t dattn_append_decode(const dattn_kv_layout *layout, void *k_pool, void *v_pool,
+                                   dattn_bf16 *stats, const dattn_bf16 *k_new,
+                                   const dattn_bf16 *v_new, const dattn_bf16 *q, int32_t B,
+                                   int32_t Hq, float scale, int32_t *seq_lens,
+                                   const dattn_sparse *sparse, int32_t num_splits, void *ws,
+                                   size_t ws_bytes, float *out, float *m_g, float *e_g,
+                                   int32_t *dev_err, void *stream);
+
+/*
  * dattn_decode without a workspace argument: the same fused decode as dattn_decode, with its
  * scratch in a fixed 8 MiB device array inside the library instead of in caller memory.
  * The pages have no counterpart to this call; it exists for callers that cannot allocate
@@ -363,6 +394,9 @@ dattn_status_t dattn_prefill(const dattn_kv_layout *layout, const void *k_pool,
  *   stats    (device) bf16 [num_pages][Hkv][P/16][2][d], kept by dattn_kv_append
  *   q        (device) bf16 [B][Hq][d];  seq_lens (device) int32 [B]
  *   head_kind (device) int8 [Hkv];  selected (device) int32 [B][Hkv][top_k]
+ *   selected_phys (device, nullable) int32 [B][Hkv][top_k]: the pool page of each selected
+ *            page, block_table[b][selected[b][h][i]] (-1 beside -1 entries), for
+ *            dattn_sparse.selected_phys
  *   ws, ws_bytes  workspace of at least dattn_workspace_size(B, Hq, Hkv, d, top_k, num_splits)
  * Besides the common limits it needs P/16 to be a power of two (P = 16, 32, 64, 128 or 256)
  * and returns DATTN_ERR_UNSUPPORTED otherwise.
@@ -370,8 +404,9 @@ dattn_status_t dattn_prefill(const dattn_kv_layout *layout, const void *k_pool,
 dattn_status_t dattn_page_select(const dattn_kv_layout *layout, const dattn_bf16 *stats,
                                  const dattn_bf16 *q, int32_t B, int32_t Hq,
                                  const int32_t *seq_lens, const int8_t *head_kind,
-                                 int32_t top_k, int32_t *selected, void *ws, size_t ws_bytes,
-                                 int32_t num_splits, int32_t *dev_err, void *stream);
+                                 int32_t top_k, int32_t *selected, int32_t *selected_phys,
+                                 void *ws, size_t ws_bytes, int32_t num_splits,
+                                 int32_t *dev_err, void *stream);
 
 /*
  * Workspace bytes for dattn_partial (items = C, top_k = 0), dattn_decode (items = B,

@@ -11,6 +11,7 @@ Entry points, with the same names as in include/dattn.h:
   dattn_partial      MicroAttention partials (m, e, MA) over explicit chunks of pages
   dattn_merge        log-sum-exp aggregation of partials
   dattn_decode       fused split-KV decode, dense or block-sparse
+  dattn_append_decode one decode step with its one-token append, in one launch (bf16 pool)
   dattn_decode_multi fused decode of T new query tokens per request, causal over them
   dattn_page_select  page scoring and top-K selection for retrieval heads
   dattn_prefill      block-sparse prefill of a chunk of new tokens (64-token key blocks)
@@ -26,6 +27,7 @@ import torch
 __all__ = [
     "KVLayout", "SparseConfig", "DattnError", "load_library", "library_path",
     "dattn_kv_append", "dattn_partial", "dattn_merge", "dattn_decode", "dattn_page_select",
+    "dattn_append_decode",
     "dattn_decode_noalloc", "dattn_decode_multi", "dattn_prefill", "PrefillSparseConfig",
     "dattn_workspace_size", "dattn_workspace_init", "dattn_auto_splits", "dattn_split_range",
     "dattn_split_owner", "dattn_status_string", "dattn_version", "Workspace",
@@ -58,7 +60,7 @@ class _Layout(ctypes.Structure):
 class _Sparse(ctypes.Structure):
     _fields_ = [("head_kind", ctypes.c_void_p), ("sinks", ctypes.c_int32),
                 ("local", ctypes.c_int32), ("top_k", ctypes.c_int32),
-                ("selected", ctypes.c_void_p)]
+                ("selected", ctypes.c_void_p), ("selected_phys", ctypes.c_void_p)]
 
 
 class _PrefillSparse(ctypes.Structure):
@@ -79,8 +81,10 @@ _SIGS = {
     "dattn_merge": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dattn_decode": (_I, [ctypes.POINTER(_Layout), _P, _P, _P, _I, _I, _F, _P,
                           ctypes.POINTER(_Sparse), _I, _P, _SZ, _P, _P, _P, _P, _P]),
-    "dattn_page_select": (_I, [ctypes.POINTER(_Layout), _P, _P, _I, _I, _P, _P, _I, _P, _P, _SZ,
-                               _I, _P, _P]),
+    "dattn_page_select": (_I, [ctypes.POINTER(_Layout), _P, _P, _I, _I, _P, _P, _I, _P, _P, _P,
+                               _SZ, _I, _P, _P]),
+    "dattn_append_decode": (_I, [ctypes.POINTER(_Layout), _P, _P, _P, _P, _P, _P, _I, _I, _F, _P,
+                                 ctypes.POINTER(_Sparse), _I, _P, _SZ, _P, _P, _P, _P, _P]),
     "dattn_decode_noalloc": (_I, [ctypes.POINTER(_Layout), _P, _P, _P, _I, _I, _F, _P,
                                   ctypes.POINTER(_Sparse), _I, _P, _P, _P, _P, _P]),
     "dattn_decode_multi": (_I, [ctypes.POINTER(_Layout), _P, _P, _P, _I, _I, _I, _F, _P, _I, _P,
@@ -236,12 +240,19 @@ class SparseConfig:
     """Block-sparse settings: per-KV-head kinds, streaming window and retrieval selection."""
 
     def __init__(self, head_kind: torch.Tensor, sinks: int, local: int, top_k: int,
-                 selected: torch.Tensor | None):
+                 selected: torch.Tensor | None, selected_phys: torch.Tensor | None = None):
         if head_kind.dtype != torch.int8:
             raise TypeError("head_kind must be int8")
-        self.head_kind, self.selected = head_kind, selected
+        for t, n in ((selected, "selected"), (selected_phys, "selected_phys")):
+            if t is not None and (t.dtype != torch.int32 or not t.is_contiguous()):
+                raise TypeError(f"{n} must be a contiguous int32 tensor")
+        if selected is not None and selected_phys is not None and \
+                selected_phys.numel() < selected.numel():
+            raise ValueError("selected_phys must have the shape of selected")
+        self.head_kind, self.selected, self.selected_phys = head_kind, selected, selected_phys
         self.c = _Sparse(head_kind.data_ptr(), sinks, local, top_k,
-                         selected.data_ptr() if selected is not None else None)
+                         selected.data_ptr() if selected is not None else None,
+                         selected_phys.data_ptr() if selected_phys is not None else None)
 
 
 class PrefillSparseConfig:
@@ -379,6 +390,31 @@ def dattn_decode(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, ou
         _ptr(m_g), _ptr(e_g), _ptr(dev_err), _stream(stream)), "dattn_decode")
 
 
+def dattn_append_decode(layout: KVLayout, k_pool, v_pool, stats, k_new, v_new, q, scale: float,
+                        seq_lens, out, ws: Workspace, m_g=None, e_g=None,
+                        sparse: SparseConfig | None = None, num_splits=0, dev_err=None,
+                        stream=None):
+    """dattn_kv_append of one token per request (k_new/v_new bf16 [B][1][Hkv][d]) and
+    dattn_decode over the advanced lengths, in one launch (bf16 pool): out fp32 [B][Hq][d]
+    (+ m_g, e_g fp32 [B][Hq]); seq_lens advances by one."""
+    _pool(layout, k_pool, "k_pool"); _pool(layout, v_pool, "v_pool"); _bf16(stats, "stats")
+    _bf16(k_new, "k_new"); _bf16(v_new, "v_new"); _bf16(q, "q"); _i32(seq_lens, "seq_lens")
+    _f32(out, "out")
+    B, Hq = q.shape[0], q.shape[1]
+    Hkv, d = layout.num_kv_heads, layout.head_dim
+    if k_new.dim() != 4 or k_new.shape[1] != 1 or v_new.shape != k_new.shape:
+        raise ValueError("k_new and v_new must be bf16 [B][1][Hkv][d]")
+    _layout_sizes(layout, B, k_pool, v_pool, stats)
+    _size(k_new, B * Hkv * d, "k_new"); _size(v_new, B * Hkv * d, "v_new")
+    _decode_sizes(layout, B, 1, Hq, k_pool, v_pool, q, seq_lens, out, m_g, e_g, sparse)
+    sp = ctypes.byref(sparse.c) if sparse is not None else None
+    _check(load_library().dattn_append_decode(
+        ctypes.byref(layout.c), _ptr(k_pool), _ptr(v_pool), _ptr(stats), _ptr(k_new),
+        _ptr(v_new), _ptr(q), B, Hq, scale, _ptr(seq_lens), sp, num_splits, _ptr(ws.buffer),
+        ws.buffer.numel(), _ptr(out), _ptr(m_g), _ptr(e_g), _ptr(dev_err), _stream(stream)),
+        "dattn_append_decode")
+
+
 def dattn_decode_multi(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_lens, out,
                        ws: Workspace, m_g=None, e_g=None, num_splits=0, dev_err=None, stream=None):
     """T query tokens per request (q bf16 [B][T][Hq][d]), causal over the T newest tokens:
@@ -435,9 +471,11 @@ def dattn_decode_noalloc(layout: KVLayout, k_pool, v_pool, q, scale: float, seq_
 
 
 def dattn_page_select(layout: KVLayout, stats, q, seq_lens, head_kind, top_k: int, selected,
-                      ws: Workspace, num_splits=0, dev_err=None, stream=None):
-    """Top-K physical pages per retrieval head into selected int32 [B][Hkv][top_k]."""
+                      ws: Workspace, num_splits=0, dev_err=None, stream=None, selected_phys=None):
+    """Top-K physical pages per retrieval head into selected int32 [B][Hkv][top_k] (and their
+    pool pages into selected_phys, of the same shape, when given)."""
     _bf16(stats, "stats"); _bf16(q, "q"); _i32(seq_lens, "seq_lens"); _i32(selected, "selected")
+    _i32(selected_phys, "selected_phys")
     B, Hq = q.shape[0], q.shape[1]
     c = layout.c
     _size(stats, c.num_pages * c.num_kv_heads * (c.page_size // 16) * 2 * c.head_dim, "stats")
@@ -445,7 +483,9 @@ def dattn_page_select(layout: KVLayout, stats, q, seq_lens, head_kind, top_k: in
     _size(q, B * Hq * c.head_dim, "q"); _size(seq_lens, B, "seq_lens")
     _size(head_kind, c.num_kv_heads, "head_kind")
     _size(selected, B * c.num_kv_heads * top_k, "selected")
+    if selected_phys is not None:
+        _size(selected_phys, B * c.num_kv_heads * top_k, "selected_phys")
     _check(load_library().dattn_page_select(
         ctypes.byref(layout.c), _ptr(stats), _ptr(q), B, Hq, _ptr(seq_lens), _ptr(head_kind),
-        top_k, _ptr(selected), _ptr(ws.buffer), ws.buffer.numel(), num_splits, _ptr(dev_err),
-        _stream(stream)), "dattn_page_select")
+        top_k, _ptr(selected), _ptr(selected_phys), _ptr(ws.buffer), ws.buffer.numel(),
+        num_splits, _ptr(dev_err), _stream(stream)), "dattn_page_select")

@@ -23,9 +23,9 @@ dattn_status_t launch_kv_append(const dattn_kv_layout& L, void* k_pool, void* v_
 dattn_status_t launch_page_select(const dattn_kv_layout& Lay, const uint16_t* stats,
                                   const uint16_t* q, int32_t B, int32_t Hq,
                                   const int32_t* seq_lens, const int8_t* head_kind,
-                                  int32_t top_k, int32_t* selected, void* ws, size_t ws_bytes,
-                                  int32_t num_splits, int32_t* dev_err, cudaStream_t stream,
-                                  int64_t units_bound);
+                                  int32_t top_k, int32_t* selected, int32_t* selected_phys,
+                                  void* ws, size_t ws_bytes, int32_t num_splits,
+                                  int32_t* dev_err, cudaStream_t stream, int64_t units_bound);
 
 namespace {
 
@@ -292,21 +292,41 @@ dattn_status_t dattn_merge(int32_t B, int32_t C, int32_t Hq, int32_t head_dim,
 
 namespace {
 
-// The fused decode of dattn_decode (T = 1) and dattn_decode_multi (T query tokens).
+// The fused append of dattn_append_decode (k_new != NULL): the pool, statistics and lengths
+// it writes.
+struct AppendArgs {
+    void* k_pool;
+    void* v_pool;
+    dattn_bf16* stats;
+    const dattn_bf16* k_new;
+    const dattn_bf16* v_new;
+    int32_t* seq_lens;
+};
+
+// The fused decode of dattn_decode (T = 1), dattn_decode_multi (T query tokens) and
+// dattn_append_decode (T = 1 with app != NULL).
 dattn_status_t decode_impl(const dattn_kv_layout* layout, const void* k_pool, const void* v_pool,
                            const dattn_bf16* q, int32_t B, int32_t T, int32_t Hq, float scale,
                            const int32_t* seq_lens, const dattn_sparse* sparse,
                            int32_t num_splits, void* ws, size_t ws_bytes, float* out, float* m_g,
-                           float* e_g, int32_t* dev_err, void* stream) {
+                           float* e_g, int32_t* dev_err, void* stream,
+                           const AppendArgs* app = nullptr) {
     dattn_status_t st = check_layout(layout);
     if (st != DATTN_OK) return st;
     if ((st = check_heads(layout, B, Hq)) != DATTN_OK) return st;
     if (num_splits < 0 || T < 1) return DATTN_ERR_INVALID_ARG;
     if ((Hq / layout->num_kv_heads) * (int64_t)T > kMaxGroup) return DATTN_ERR_UNSUPPORTED;
     if (T > 1 && sparse != nullptr) return DATTN_ERR_UNSUPPORTED;
+    if (app != nullptr && layout->kv_format != DATTN_KV_BF16) return DATTN_ERR_UNSUPPORTED;
     if (B == 0) return DATTN_OK;
     if (!k_pool || !v_pool || !q || !seq_lens || !out) return DATTN_ERR_INVALID_ARG;
     if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(q)) return DATTN_ERR_INVALID_ARG;
+    if (app != nullptr) {
+        if (!app->k_new || !app->v_new) return DATTN_ERR_INVALID_ARG;
+        if (!aligned16(app->k_new) || !aligned16(app->v_new) ||
+            (app->stats && !aligned16(app->stats)))
+            return DATTN_ERR_INVALID_ARG;
+    }
     const int32_t per_page = layout->page_size / 16;
     const int64_t dense_tiles = (int64_t)layout->max_pages_per_req * per_page;
     int64_t per_head = dense_tiles;
@@ -324,6 +344,7 @@ dattn_status_t decode_impl(const dattn_kv_layout* layout, const void* k_pool, co
         p.local = sparse->local;
         p.top_k = sparse->top_k;
         p.selected = sparse->selected;
+        p.selected_phys = sparse->selected_phys;
         const int64_t retr = (int64_t)sparse->top_k * per_page;
         const int64_t strm = (sparse->sinks + 15) / 16 + (sparse->local + 15) / 16 + 1;
         if (retr > per_head) per_head = retr;
@@ -352,6 +373,15 @@ dattn_status_t decode_impl(const dattn_kv_layout* layout, const void* k_pool, co
     p.dev_err = dev_err;
     p.fmt = layout->kv_format;
     p.kv_scale = layout->kv_scale;
+    if (app != nullptr) {
+        p.append = 1;
+        p.k_new = app->k_new;
+        p.v_new = app->v_new;
+        p.k_pool_w = static_cast<uint16_t*>(app->k_pool);
+        p.v_pool_w = static_cast<uint16_t*>(app->v_pool);
+        p.stats = app->stats;
+        p.seq_lens_w = app->seq_lens;
+    }
     return launch_attention(p, k_pool, v_pool, layout->head_dim, num_splits, ws, ws_bytes,
                             static_cast<cudaStream_t>(stream), bound);
 }
@@ -370,6 +400,18 @@ dattn_status_t dattn_decode(const dattn_kv_layout* layout, const void* k_pool,
                        ws, ws_bytes, out, m_g, e_g, dev_err, stream);
 }
 
+dattn_status_t dattn_append_decode(const dattn_kv_layout* layout, void* k_pool, void* v_pool,
+                                   dattn_bf16* stats, const dattn_bf16* k_new,
+                                   const dattn_bf16* v_new, const dattn_bf16* q, int32_t B,
+                                   int32_t Hq, float scale, int32_t* seq_lens,
+                                   const dattn_sparse* sparse, int32_t num_splits, void* ws,
+                                   size_t ws_bytes, float* out, float* m_g, float* e_g,
+                                   int32_t* dev_err, void* stream) {
+    const AppendArgs app{k_pool, v_pool, stats, k_new, v_new, seq_lens};
+    return decode_impl(layout, k_pool, v_pool, q, B, 1, Hq, scale, seq_lens, sparse, num_splits,
+                       ws, ws_bytes, out, m_g, e_g, dev_err, stream, &app);
+}
+
 dattn_status_t dattn_decode_multi(const dattn_kv_layout* layout, const void* k_pool,
                                   const void* v_pool, const dattn_bf16* q, int32_t B, int32_t T,
                                   int32_t Hq, float scale, const int32_t* seq_lens,
@@ -382,8 +424,9 @@ dattn_status_t dattn_decode_multi(const dattn_kv_layout* layout, const void* k_p
 dattn_status_t dattn_page_select(const dattn_kv_layout* layout, const dattn_bf16* stats,
                                  const dattn_bf16* q, int32_t B, int32_t Hq,
                                  const int32_t* seq_lens, const int8_t* head_kind,
-                                 int32_t top_k, int32_t* selected, void* ws, size_t ws_bytes,
-                                 int32_t num_splits, int32_t* dev_err, void* stream) {
+                                 int32_t top_k, int32_t* selected, int32_t* selected_phys,
+                                 void* ws, size_t ws_bytes, int32_t num_splits,
+                                 int32_t* dev_err, void* stream) {
     dattn_status_t st = check_layout(layout);
     if (st != DATTN_OK) return st;
     if ((st = check_heads(layout, B, Hq)) != DATTN_OK) return st;
@@ -396,9 +439,9 @@ dattn_status_t dattn_page_select(const dattn_kv_layout* layout, const dattn_bf16
     if (!aligned16(stats)) return DATTN_ERR_INVALID_ARG;
     const int64_t bound = (int64_t)B * layout->num_kv_heads * layout->max_pages_per_req;
     if (bound * 4 >= (1ll << 31)) return DATTN_ERR_UNSUPPORTED;
-    return launch_page_select(*layout, stats, q, B, Hq, seq_lens, head_kind, top_k, selected, ws,
-                              ws_bytes, num_splits, dev_err, static_cast<cudaStream_t>(stream),
-                              bound);
+    return launch_page_select(*layout, stats, q, B, Hq, seq_lens, head_kind, top_k, selected,
+                              selected_phys, ws, ws_bytes, num_splits, dev_err,
+                              static_cast<cudaStream_t>(stream), bound);
 }
 
 }  // extern "C"

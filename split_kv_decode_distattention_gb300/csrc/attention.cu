@@ -64,6 +64,13 @@ struct Smem {
         return reinterpret_cast<int32_t*>(base + L.item_start);
     }
     __device__ int32_t* item_len() const { return reinterpret_cast<int32_t*>(base + L.item_len); }
+    // fused append: the position of request i's new token (its length before the append;
+    // negative when nothing is appended)
+    __device__ int32_t* item_pos() const { return reinterpret_cast<int32_t*>(base + L.item_pos); }
+    // the CTA's plan constants: aligned, W, Gw, X0, X1
+    __device__ int32_t* cplan() const { return reinterpret_cast<int32_t*>(base + L.flags + 8); }
+    // head-aligned plan: kAplanScalars scalars, the retrieval heads, the streaming heads
+    __device__ int32_t* aplan() const { return reinterpret_cast<int32_t*>(base + L.aplan); }
     __device__ int32_t* scan() const { return reinterpret_cast<int32_t*>(base + L.scan); }
     // the 8-bit pool's row scales of stage s: 16 K scales, then 16 V scales
     __device__ const float* scales(int s) const {
@@ -99,6 +106,64 @@ __device__ __forceinline__ int32_t head_tiles(int kind, int32_t L, const AttnPar
 // query, merging the warps, handing over a partial). The balanced split cuts the cost space,
 // so a CTA whose range crosses many small segments gets fewer tiles. The extra units are
 // never loaded or scheduled: producer and consumers walk real tiles only.
+
+// Head-aligned plan of a block-sparse launch in which every KV head is a retrieval or a
+// streaming head. A retrieval segment then always holds R = top_k * P/16 tile slots and a
+// streaming segment S = ceil(sinks/16) + ceil((local+15)/16) slots; the producer skips the
+// slots the current length leaves empty. So the plan does not depend on the lengths and is
+// made before the dependency wait. Each retrieval segment gets k CTAs of its own, which split
+// its slots evenly: no CTA carries pieces of two retrieval segments, and every retrieval
+// segment is merged from exactly k pieces. The other G - n_r k CTAs take the streaming
+// segments, each whole. k follows the cost units of the balanced split (real tiles plus
+// kSegCost per segment), rounded to the nearest integer, but leaves every streaming segment
+// a CTA of its own when the grid allows: their pieces are short and bound by latency, and a
+// CTA runs its pieces one after another.
+enum AplanIdx : int { AP_ON = 0, AP_K, AP_GR, AP_GS, AP_NRET, AP_NSTR, AP_R, AP_S };
+
+__device__ void make_aligned_plan(const AttnParams& p, const Smem& sm, int32_t G) {
+    int32_t* a = sm.aplan();
+    int32_t* ret = a + kAplanScalars;
+    int32_t* str = ret + p.Hkv;
+    int32_t nret = 0, nstr = 0, ndense = 0;
+    for (int h = 0; h < p.Hkv; ++h) {
+        const int k = sm.kinds()[h];
+        if (k == DATTN_HEAD_RETRIEVAL) ret[nret++] = h;
+        else if (k == DATTN_HEAD_STREAMING) str[nstr++] = h;
+        else ++ndense;
+    }
+    const int32_t R = p.top_k * (p.P >> 4);
+    const int32_t S = (p.sinks + 15) / 16 + (p.local > 0 ? (p.local + 30) / 16 : 0);
+    const int64_t nr = (int64_t)p.B * nret, ns = (int64_t)p.B * nstr;
+    int64_t k = 0;
+    bool on = ndense == 0 && p.T == 1 && (nr > 0 || ns > 0) && (nret == 0 || R > 0) &&
+              (nstr == 0 || S > 0);
+    if (on && nr > 0) {
+        const int64_t cr = R + kSegCost, cs = S + kSegCost;
+        const int64_t W = nr * cr + ns * cs;
+        k = (cr * G + W / 2) / W;
+        k = min(max(k, (int64_t)1), (int64_t)R);
+        // Streaming segments are short and bound by latency, so several in one CTA run one
+        // after another: leave each its own CTA when the grid allows it, else at least one
+        // CTA for all of them.
+        if (ns > 0 && G - ns >= nr) k = min(k, ((int64_t)G - ns) / nr);
+        k = min(k, (ns > 0 ? (int64_t)G - 1 : (int64_t)G) / nr);
+        on = k >= 1;
+    }
+    a[AP_ON] = on ? 1 : 0;
+    a[AP_K] = (int32_t)k;
+    a[AP_GR] = (int32_t)(nr * k);
+    a[AP_GS] = G - (int32_t)(nr * k);
+    a[AP_NRET] = nret;
+    a[AP_NSTR] = nstr;
+    a[AP_R] = R;
+    a[AP_S] = S;
+}
+
+// A piece: the real tiles [r0, r1) of segment s computed in this CTA. The segment's pieces
+// lie in the consecutive CTAs cfirst .. clast (cfirst == clast: the segment is finished here).
+struct Piece {
+    int32_t s, r0, r1, cfirst, clast;
+};
 
 // Segment geometry derived from the per-item prefix sums (in cost units) in shared memory.
 struct Plan {
@@ -177,22 +242,93 @@ struct Plan {
     }
 };
 
+// The pieces of one CTA in order, under either plan. A cursor starts at 0; piece() returns
+// the piece at the cursor, or false when there is none, and advance() moves past it.
+// The CTA's constants of its plan sit in shared memory (sm.cplan(): aligned, W, Gw, X0, X1),
+// so that they occupy no registers across the consumer loop.
+struct PieceIter {
+    const AttnParams& p;
+    const Smem& sm;
+    const Plan& plan;
+    int32_t cta;
+    __device__ PieceIter(const AttnParams& p_, const Smem& sm_, const Plan& pl, int32_t c)
+        : p(p_), sm(sm_), plan(pl), cta(c) {}
+
+    __device__ bool aligned() const { return sm.cplan()[0] != 0; }
+
+    // Cursor: the segment to look from (balanced split) or the piece index (aligned plan).
+    __device__ int32_t start() const {
+        const int32_t* cp = sm.cplan();
+        return cp[0] ? 0 : (cp[3] < cp[4] ? plan.segment_at(cp[3]) : p.nseg);
+    }
+
+    __device__ bool piece(int32_t& cur, Piece& pc) const {
+        const int32_t* cp = sm.cplan();
+        if (!cp[0]) {
+            const int32_t W = cp[1], Gw = cp[2], X0 = cp[3], X1 = cp[4];
+            int32_t cs, real, r0, r1;
+            if (!plan.next_piece(cur, X0, X1, cs, real, r0, r1)) return false;
+            pc.s = cur;
+            pc.r0 = r0;
+            pc.r1 = r1;
+            pc.cfirst = split_owner(cs, W, Gw);
+            pc.clast = split_owner(cs + real - 1, W, Gw);
+            return true;
+        }
+        const int32_t* a = sm.aplan();
+        const int32_t k = a[AP_K], Gr = a[AP_GR], Gs = a[AP_GS];
+        if (cta < Gr) {
+            if (cur != 0) return false;
+            const int32_t r = cta / k, j = cta - r * k, R = a[AP_R], nret = a[AP_NRET];
+            const int32_t b = r / nret;
+            pc.s = b * p.Hkv + a[kAplanScalars + (r - b * nret)];
+            pc.r0 = (int32_t)((int64_t)j * R / k);
+            pc.r1 = (int32_t)((int64_t)(j + 1) * R / k);
+            pc.cfirst = r * k;
+            pc.clast = r * k + k - 1;
+            return true;
+        }
+        const int32_t j = cta - Gr, nstr = a[AP_NSTR];
+        const int64_t ns = (int64_t)p.B * nstr;
+        if (j >= Gs || ns == 0) return false;
+        const int64_t m = ns * j / Gs + cur;
+        if (m >= ns * (j + 1) / Gs) return false;
+        const int32_t b = (int32_t)(m / nstr);
+        pc.s = b * p.Hkv + a[kAplanScalars + p.Hkv + (int32_t)(m - (int64_t)b * nstr)];
+        pc.r0 = 0;
+        pc.r1 = a[AP_S];
+        pc.cfirst = pc.clast = cta;
+        return true;
+    }
+
+    __device__ void advance(int32_t& cur) const { ++cur; }
+};
+
 // Resolved tile: TMA row coordinate, the valid token range [lo, hi) within its 16 rows and
 // the causal cut of multi-query decode: row r is visible to query token t iff r <= cut + t.
+// With the fused append, the tile that holds the new token carries its row: the consumer
+// writes the new token's K and V into that row of the stage before using it.
 struct TileRef {
     int32_t y;
-    int32_t lohi;  // lo | hi << 8 | skip << 16 | (cut + 16) << 24, cut clamped to [-16, 16]
+    int32_t lohi;  // lo | hi << 8 | skip << 16 | patch << 17 | patch row << 18 |
+                   // (cut + 16) << 24, cut clamped to [-16, 16]
 };
 constexpr int32_t kTileSkip = 1 << 16;
+constexpr int32_t kTilePatch = 1 << 17;
 __device__ __forceinline__ int32_t tile_lo(int32_t m) { return m & 0xff; }
 __device__ __forceinline__ int32_t tile_hi(int32_t m) { return (m >> 8) & 0xff; }
 __device__ __forceinline__ int32_t tile_cut(int32_t m) { return ((m >> 24) & 63) - 16; }
+__device__ __forceinline__ int32_t tile_patch_row(int32_t m) { return (m >> 18) & 15; }
 
+// Tile `local` of segment s. `aligned`: the head-aligned plan's fixed slot layout (streaming
+// segments: ceil(sinks/16) sink slots, then the local-window slots; retrieval segments have
+// slots even when the length is 0).
 __device__ __forceinline__ TileRef resolve_tile(const AttnParams& p, const Smem& sm, int32_t s,
-                                                int32_t local) {
+                                                int32_t local, bool aligned) {
     TileRef r{0, kTileSkip};
     const int32_t item = s / p.Hkv, h = s - item * p.Hkv;
     int32_t b, L, t0, lo = 0, hi = 16, cut = 16;
+    int32_t page = -2;  // -2: look the page up in the block table
     if (p.mode == MODE_PARTIAL) {
         b = __ldg(p.chunk_req + item);
         if (b < 0 || b >= p.B) return r;  // such a chunk has no tiles
@@ -211,9 +347,12 @@ __device__ __forceinline__ TileRef resolve_tile(const AttnParams& p, const Smem&
         L = sm.item_len()[item];
         const int kind = p.mode == MODE_SPARSE ? sm.kinds()[h] : DATTN_HEAD_DENSE;
         if (kind == DATTN_HEAD_RETRIEVAL) {
+            if (L == 0) return r;  // (aligned plan) nothing is attended
             const int32_t per_page = p.P >> 4;
             const int32_t si = local / per_page;
-            const int32_t pg = __ldg(p.selected + ((int64_t)b * p.Hkv + h) * p.top_k + si);
+            const int64_t at = ((int64_t)b * p.Hkv + h) * p.top_k + si;
+            const int32_t pg = __ldg(p.selected + at);
+            if (p.selected_phys) page = __ldg(p.selected_phys + at);
             if (pg < 0) return r;
             if (pg >= (L + p.P - 1) / p.P) {
                 set_err(p.dev_err, DATTN_DEVERR_SELECT_OOB);
@@ -225,11 +364,21 @@ __device__ __forceinline__ TileRef resolve_tile(const AttnParams& p, const Smem&
         } else if (kind == DATTN_HEAD_STREAMING) {
             int32_t s_end, nsink, l0, nlocal;
             stream_geometry(L, p.sinks, p.local, s_end, nsink, l0, nlocal);
-            if (local < nsink) {
-                t0 = local * 16;
+            int32_t j = local;  // the slot as a sink tile (j < nsink) or local tile j - nsink
+            if (aligned) {
+                const int32_t nsink_max = (p.sinks + 15) / 16;
+                if (local < nsink_max) {
+                    if (local >= nsink) return r;
+                } else {
+                    j = nsink + (local - nsink_max);
+                    if (j - nsink >= nlocal) return r;
+                }
+            }
+            if (j < nsink) {
+                t0 = j * 16;
                 hi = min(16, s_end - t0);
             } else {
-                t0 = ((l0 >> 4) + (local - nsink)) * 16;
+                t0 = ((l0 >> 4) + (j - nsink)) * 16;
                 lo = max(t0, l0) - t0;
                 hi = min(t0 + 16, L) - t0;
             }
@@ -241,7 +390,7 @@ __device__ __forceinline__ TileRef resolve_tile(const AttnParams& p, const Smem&
         }
     }
     const int32_t lp = t0 / p.P;
-    const int32_t page = __ldg(p.block_table + (int64_t)b * p.max_pages + lp);
+    if (page == -2) page = __ldg(p.block_table + (int64_t)b * p.max_pages + lp);
     if (page < 0) {
         set_err(p.dev_err, DATTN_DEVERR_UNMAPPED_PAGE);
         return r;
@@ -252,6 +401,11 @@ __device__ __forceinline__ TileRef resolve_tile(const AttnParams& p, const Smem&
     }
     r.y = (page * p.Hkv + h) * p.P + (t0 - lp * p.P);
     r.lohi = lo | (hi << 8) | ((cut + 16) << 24);
+    if (p.append) {  // the new token (the last one) lies in this tile
+        const int32_t pos = sm.item_pos()[b];
+        if (pos >= 0 && pos == L - 1 && pos >= t0 + lo && pos < t0 + hi)
+            r.lohi |= kTilePatch | ((pos - t0) << 18);
+    }
     return r;
 }
 
@@ -380,6 +534,29 @@ struct Consumer {
             }
             qs = p.sl2 * down;
         }
+    }
+
+    // Fused append: this lane's 16-byte chunk of segment s's new K / V row (lanes 0 .. D/8 - 1
+    // hold the K chunks, lanes D/8 .. D/4 - 1 the V chunks).
+    __device__ uint4 load_new_row(int32_t s) const {
+        constexpr int VPR = D / 8;
+        const int32_t item = s / p.Hkv, kvh = s - item * p.Hkv;
+        if (lane >= 2 * VPR || sm.item_pos()[item] < 0) return make_uint4(0u, 0u, 0u, 0u);
+        const uint16_t* src = (lane < VPR ? p.k_new : p.v_new) +
+                              ((int64_t)item * p.Hkv + kvh) * D + (lane % VPR) * 8;
+        return __ldg(reinterpret_cast<const uint4*>(src));
+    }
+
+    // Writes the new token's K and V (this lane's chunk v from load_new_row) into row `row` of
+    // the bf16 stage `st`, in the layout the TMA boxes leave there.
+    __device__ void patch_row(uint32_t st, int row, const uint4& v) const {
+        constexpr int VPR = D / 8;
+        if (lane < 2 * VPR) {
+            const uint32_t c = (uint32_t)(lane % VPR);
+            const uint32_t half0 = lane < VPR ? 0u : (uint32_t)(D / 64) * 2048u;
+            st_shared_v4(st + half0 + (c >> 3) * 2048u + swz128((uint32_t)row, c & 7u), v);
+        }
+        __syncwarp();
     }
 
     __device__ void reset() {
@@ -802,6 +979,58 @@ struct Consumer {
     }
 };
 
+// The write half of the fused append (bf16 pool): the new token of every (request, KV head)
+// goes to its page and slot, and the open logical page's k_max / k_min take it in, exactly as
+// dattn_kv_append writes one token. The work is spread over the consumer threads of all CTAs
+// (one 8-channel chunk each). A CTA that reads the tile of a new token may see the slot
+// before or after this write; it writes the new token into its stage itself (patch_row).
+template <int D>
+__device__ void append_new_tokens(const AttnParams& p, const Smem& sm, int32_t cta, int32_t G,
+                                  int ctid) {
+    constexpr int VPR = D / 8;
+    constexpr int NT = kConsumerWarps * 32;
+    const int64_t n = (int64_t)p.B * p.Hkv * VPR;
+    for (int64_t it = (int64_t)cta * NT + ctid; it < n; it += (int64_t)G * NT) {
+        const int32_t c8 = (int32_t)(it % VPR);
+        const int64_t bh = it / VPR;
+        const int32_t b = (int32_t)(bh / p.Hkv), h = (int32_t)(bh - (int64_t)b * p.Hkv);
+        const int32_t pos = sm.item_pos()[b];
+        if (pos < 0) continue;  // flagged when the lengths were read
+        const int32_t lp = pos / p.P;
+        if (lp >= p.max_pages) {
+            set_err(p.dev_err, DATTN_DEVERR_LEN_OOB);
+            continue;
+        }
+        const int32_t page = __ldg(p.block_table + (int64_t)b * p.max_pages + lp);
+        if (page < 0) {
+            set_err(p.dev_err, DATTN_DEVERR_UNMAPPED_PAGE);
+            continue;
+        }
+        if (page >= p.num_pages) {
+            set_err(p.dev_err, DATTN_DEVERR_PAGE_OOB);
+            continue;
+        }
+        const uint4 kv = __ldg(reinterpret_cast<const uint4*>(p.k_new + bh * D + c8 * 8));
+        const uint4 vv = __ldg(reinterpret_cast<const uint4*>(p.v_new + bh * D + c8 * 8));
+        const int32_t slot = pos - lp * p.P;
+        const int64_t dst = (((int64_t)page * p.Hkv + h) * p.P + slot) * D + c8 * 8;
+        *reinterpret_cast<uint4*>(p.k_pool_w + dst) = kv;
+        *reinterpret_cast<uint4*>(p.v_pool_w + dst) = vv;
+        if (p.stats != nullptr) {
+            uint16_t* st = p.stats +
+                           (((int64_t)page * p.Hkv + h) * (p.P >> 4) + (slot >> 4)) * 2 * D + c8 * 8;
+            uint4 mx = kv, mn = kv;  // a token at position % 16 == 0 opens its logical page
+            if ((pos & 15) != 0) {
+                mx = *reinterpret_cast<const uint4*>(st);
+                mn = *reinterpret_cast<const uint4*>(st + D);
+                bf16_fold8(kv, mx, mn);
+            }
+            *reinterpret_cast<uint4*>(st) = mx;
+            *reinterpret_cast<uint4*>(st + D) = mn;
+        }
+    }
+}
+
 // Resident CTAs per SM the register budget is held to: three at d = 128, four at d = 64
 // (the 4-bit kernel processes tiles in pairs and would otherwise take more registers).
 template <int D>
@@ -819,7 +1048,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
         sm.base = smem_raw + (((off + 1023u) & ~1023u) - off);
     }
     constexpr bool Q = FMT != DATTN_KV_BF16;  // a quantized pool with row scales
-    sm.L = attn_smem_layout(D, p.gq, p.nitems, p.Hkv, p.mode == MODE_SPARSE, FMT);
+    sm.L = attn_smem_layout(D, p.gq, p.nitems, p.Hkv, p.mode == MODE_SPARSE, FMT, p.append != 0);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t G = gridDim.x, cta = blockIdx.x;
     constexpr int NS = attn_stages(FMT);
@@ -856,6 +1085,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
             }
             int32_t* kb = sm.kind_before() + 3 * p.Hkv;
             kb[0] = c0; kb[1] = c1; kb[2] = c2;
+            make_aligned_plan(p, sm, G);
         }
     }
     {  // warm L2 with the metadata read right after the wait (each line by one thread)
@@ -867,6 +1097,12 @@ attention_kernel(const __grid_constant__ AttnParams p,
         prefetch_l2_range(p.q, (size_t)p.B * p.Hq * D * 2u, gt, gn);
         if (p.mode == MODE_SPARSE && p.selected)
             prefetch_l2_range(p.selected, (size_t)p.B * p.Hkv * p.top_k * 4u, gt, gn);
+        if (p.mode == MODE_SPARSE && p.selected_phys)
+            prefetch_l2_range(p.selected_phys, (size_t)p.B * p.Hkv * p.top_k * 4u, gt, gn);
+        if (p.append) {
+            prefetch_l2_range(p.k_new, (size_t)p.B * p.Hkv * D * 2u, gt, gn);
+            prefetch_l2_range(p.v_new, (size_t)p.B * p.Hkv * D * 2u, gt, gn);
+        }
         if (p.mode == MODE_PARTIAL) {
             prefetch_l2_range(p.chunk_req, (size_t)p.C * 4u, gt, gn);
             prefetch_l2_range(p.chunk_indptr, (size_t)(p.C + 1) * 4u, gt, gn);
@@ -876,8 +1112,27 @@ attention_kernel(const __grid_constant__ AttnParams p,
     grid_dependency_wait();
     grid_launch_dependents();
     __syncthreads();
-    // per-item costs, then an exclusive scan into item_start
-    {
+    const bool aligned = p.mode == MODE_SPARSE && sm.aplan()[AP_ON] != 0;
+    // The lengths: with the fused append, request i attends one more token than seq_lens[i]
+    // holds (its new token at position seq_lens[i]), as dattn_kv_append would leave it.
+    auto length_of = [&](int32_t i) {
+        int32_t L = p.seq_lens[i];
+        const int32_t cap = p.max_pages * p.P;
+        if (p.append) {
+            sm.item_pos()[i] = L;
+            if (L >= 0 && L < cap) ++L;
+        }
+        if (L < 0 || L > cap) {
+            set_err(p.dev_err, DATTN_DEVERR_LEN_OOB);
+            L = min(max(L, 0), cap);
+        }
+        return L;
+    };
+    if (aligned) {
+        for (int32_t i = tid; i < p.nitems; i += kAttnThreads) sm.item_len()[i] = length_of(i);
+        __syncthreads();
+    } else {
+        // per-item costs, then an exclusive scan into item_start
         int32_t* st = sm.item_start();
         int32_t* ln = sm.item_len();
         const int32_t n = p.nitems;
@@ -899,12 +1154,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
                 ln[i] = npg * (p.P >> 4);  // real tiles per head
                 cnt = p.Hkv * Plan::cost_of(ln[i]);
             } else {
-                int32_t L = p.seq_lens[i];
-                const int32_t cap = p.max_pages * p.P;
-                if (L < 0 || L > cap) {
-                    set_err(p.dev_err, DATTN_DEVERR_LEN_OOB);
-                    L = min(max(L, 0), cap);
-                }
+                const int32_t L = length_of(i);
                 ln[i] = L;
                 if (p.mode == MODE_SPARSE) {
                     const int32_t* kb = sm.kind_before() + 3 * p.Hkv;
@@ -942,86 +1192,121 @@ attention_kernel(const __grid_constant__ AttnParams p,
         __syncthreads();
     }
     const Plan plan(p, sm);
-    const int32_t W = sm.item_start()[p.nitems];
-    // Only the first min(G, W) CTAs take work, so that every participating CTA owns at
-    // least one cost unit. A CTA strictly between the first and the last owner of a
-    // segment's real tiles lies inside them, so the pieces of a segment come from
-    // consecutive CTAs c_first..c_last, each of which arrives on its counter once.
-    const int32_t Gw = W < G ? (W > 0 ? W : 1) : G;
-    const int32_t X0 = cta < Gw ? (int32_t)split_begin(W, Gw, cta) : 0;
-    const int32_t X1 = cta < Gw ? (int32_t)split_begin(W, Gw, cta + 1) : 0;
-
-    // segments without tiles have no owner: CTA (s mod G) writes their empty result
-    for (int32_t s = cta; s < p.nseg; s += G) {
-        int32_t st, real, cost;
-        plan.seg_span(s, st, real, cost);
-        if (real == 0) {
-            for (int idx = tid; idx < p.gq * D; idx += kAttnThreads)
-                write_final(p, s, idx / D, idx % D, D, kNegInf, 0.f, 0.f);
+    int32_t W = 0, Gw = 1, X0 = 0, X1 = 0;
+    if (!aligned) {
+        W = sm.item_start()[p.nitems];
+        // Only the first min(G, W) CTAs take work, so that every participating CTA owns at
+        // least one cost unit. A CTA strictly between the first and the last owner of a
+        // segment's real tiles lies inside them, so the pieces of a segment come from
+        // consecutive CTAs c_first..c_last, each of which arrives on its counter once.
+        Gw = W < G ? (W > 0 ? W : 1) : G;
+        X0 = cta < Gw ? (int32_t)split_begin(W, Gw, cta) : 0;
+        X1 = cta < Gw ? (int32_t)split_begin(W, Gw, cta + 1) : 0;
+        // segments without tiles have no owner: CTA (s mod G) writes their empty result
+        for (int32_t s = cta; s < p.nseg; s += G) {
+            int32_t st, real, cost;
+            plan.seg_span(s, st, real, cost);
+            if (real == 0) {
+                for (int idx = tid; idx < p.gq * D; idx += kAttnThreads)
+                    write_final(p, s, idx / D, idx % D, D, kNegInf, 0.f, 0.f);
+            }
         }
     }
-    if (X0 >= X1) return;
-    const int32_t s_first = plan.segment_at(X0);
+    if (tid == 0) {
+        int32_t* cp = sm.cplan();
+        cp[0] = aligned ? 1 : 0;
+        cp[1] = W;
+        cp[2] = Gw;
+        cp[3] = X0;
+        cp[4] = X1;
+    }
+    __syncthreads();
+    const PieceIter pieces(p, sm, plan, cta);
+    int32_t cur0 = pieces.start();
+    Piece first;
+    const bool any = pieces.piece(cur0, first);
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer warp
+        if (!any) return;
         const uint64_t pol = policy_evict_first();
         const uint32_t tile_bytes = attn_tile_bytes(FMT, D);
         const uint32_t tx = 2u * tile_bytes + (Q ? 128u : 0u);  // + the tile's 32 scales
         const uint32_t stages0 = smem_u32(sm.base + sm.L.stages);
         int32_t k = 0;  // real tiles issued so far: tile k uses stage k % NS
         bool stop = false;
-        int32_t s = s_first, cs, real, r0, r1;
-        while (!stop && plan.next_piece(s, X0, X1, cs, real, r0, r1)) {
-            for (int32_t base = r0; base < r1 && !stop; base += 32) {
-                TileRef ref{0, 1 << 16};
-                if (base + lane < r1) ref = resolve_tile(p, sm, s, base + lane);
-                const int32_t nb = min(32, r1 - base);
-                // Tiles go out kIssue at a time, lane j of a group taking tile k + j: it waits
-                // for its stage to be released, posts the tile's token range, arms the full
-                // barrier and issues the tile's copies (K and V boxes; with the 8-bit pool
-                // also the run of 16 K and 16 V row scales).
-                for (int32_t j0 = 0; j0 < nb; j0 += kIssue) {
-                    const int32_t n = min(kIssue, nb - j0);
-                    const int32_t src = min(j0 + lane, 31);
-                    const int32_t y = __shfl_sync(0xffffffffu, ref.y, src);
-                    const int32_t lohi = __shfl_sync(0xffffffffu, ref.lohi, src);
-                    bool ok = true;
-                    if (lane < n) {
-                        const int32_t kk = k + lane;
-                        const int stg = kk % NS;
-                        if (kk >= NS)
-                            ok = mbar_wait(sm.empty_bar(stg), ((kk / NS) - 1) & 1,
-                                           sm.abort_flag(), p.dev_err);
-                        if (ok) {
-                            const uint32_t full = sm.full_bar(stg);
-                            sm.meta()[stg] = lohi;
-                            if (lohi & kTileSkip) {
-                                mbar_arrive(full);
+        // Issues the nb tiles of this warp's batch (lane j resolved tile k + j into ref).
+        // Returns false after an abort.
+        auto issue = [&](const TileRef& ref, int32_t nb) -> bool {
+            // Tiles go out kIssue at a time, lane j of a group taking tile k + j: it waits
+            // for its stage to be released, posts the tile's token range, arms the full
+            // barrier and issues the tile's copies (K and V boxes; with the 8-bit pool
+            // also the run of 16 K and 16 V row scales).
+            for (int32_t j0 = 0; j0 < nb; j0 += kIssue) {
+                const int32_t n = min(kIssue, nb - j0);
+                const int32_t src = min(j0 + lane, 31);
+                const int32_t y = __shfl_sync(0xffffffffu, ref.y, src);
+                const int32_t lohi = __shfl_sync(0xffffffffu, ref.lohi, src);
+                bool ok = true;
+                if (lane < n) {
+                    const int32_t kk = k + lane;
+                    const int stg = kk % NS;
+                    if (kk >= NS)
+                        ok = mbar_wait(sm.empty_bar(stg), ((kk / NS) - 1) & 1,
+                                       sm.abort_flag(), p.dev_err);
+                    if (ok) {
+                        const uint32_t full = sm.full_bar(stg);
+                        sm.meta()[stg] = lohi;
+                        if (lohi & kTileSkip) {
+                            mbar_arrive(full);
+                        } else {
+                            mbar_arrive_expect_tx(full, tx);
+                            const uint32_t dst = stages0 + (uint32_t)stg * sm.L.stage_bytes;
+                            if constexpr (Q) {
+                                tma_load_2d(dst, &tmap_k, 0, y, full, pol);
+                                tma_load_2d(dst + tile_bytes, &tmap_v, 0, y, full, pol);
+                                // the tile's scales: 128 bytes at tile index y / 16
+                                bulk_copy(smem_u32(sm.scales(stg)), p.kv_scale + 2 * y, 128u,
+                                          full, pol);
                             } else {
-                                mbar_arrive_expect_tx(full, tx);
-                                const uint32_t dst = stages0 + (uint32_t)stg * sm.L.stage_bytes;
-                                if constexpr (Q) {
-                                    tma_load_2d(dst, &tmap_k, 0, y, full, pol);
-                                    tma_load_2d(dst + tile_bytes, &tmap_v, 0, y, full, pol);
-                                    // the tile's scales: 128 bytes at tile index y / 16
-                                    bulk_copy(smem_u32(sm.scales(stg)), p.kv_scale + 2 * y,
-                                              128u, full, pol);
-                                } else {
-                                    tma_load_3d(dst, &tmap_k, 0, y, 0, full, pol);
-                                    tma_load_3d(dst + tile_bytes, &tmap_v, 0, y, 0, full, pol);
-                                }
+                                tma_load_3d(dst, &tmap_k, 0, y, 0, full, pol);
+                                tma_load_3d(dst + tile_bytes, &tmap_v, 0, y, 0, full, pol);
                             }
                         }
                     }
-                    k += n;
-                    if (__any_sync(0xffffffffu, !ok)) {
-                        stop = true;
-                        break;
+                }
+                k += n;
+                if (__any_sync(0xffffffffu, !ok)) return false;
+            }
+            return true;
+        };
+        {
+            int32_t cur = cur0;
+            Piece pc = first;
+            int32_t base = pc.r0;
+            bool have = true;
+            while (have && !stop) {
+                // Lanes take the next (up to) 32 tiles of the CTA's sequence, across piece
+                // boundaries, so that the lookups of many small pieces overlap.
+                int32_t my_s = -1, my_local = 0, nb = 0;
+                while (have && nb < 32) {
+                    const int32_t n = min(32 - nb, pc.r1 - base);
+                    if (lane >= nb && lane < nb + n) {
+                        my_s = pc.s;
+                        my_local = base + (lane - nb);
+                    }
+                    nb += n;
+                    base += n;
+                    if (base == pc.r1) {
+                        pieces.advance(cur);
+                        have = pieces.piece(cur, pc);
+                        if (have) base = pc.r0;
                     }
                 }
+                TileRef ref{0, kTileSkip};
+                if (my_s >= 0) ref = resolve_tile(p, sm, my_s, my_local, pieces.aligned());
+                stop = !issue(ref, nb);
             }
-            ++s;
         }
         // after an abort, wait (bounded in total) for copies still in flight before the CTA
         // exits; stages whose tiles were never issued simply run into the deadline
@@ -1037,14 +1322,37 @@ attention_kernel(const __grid_constant__ AttnParams p,
     }
 
     // ---------------------------------------------------------------- consumer warps
+    if constexpr (FMT == DATTN_KV_BF16) {
+        if (p.append) {
+            // Every thread of this CTA has read the lengths (the barrier above). The CTA that
+            // arrives last advances seq_lens, as dattn_kv_append does; no CTA waits for another.
+            if (warp == 0) {
+                int32_t last = 0;
+                if (lane == 0) {
+                    const int32_t prev = atom_add_acq_rel_gpu(p.counters + p.nseg, 1);
+                    last = prev == G - 1;
+                    if (last) p.counters[p.nseg] = 0;  // ready for the next launch
+                }
+                if (__shfl_sync(0xffffffffu, last, 0)) {
+                    for (int32_t i = lane; i < p.B; i += 32) {
+                        const int32_t L = p.seq_lens_w[i];
+                        if (L >= 0 && L < 0x7fffffff) p.seq_lens_w[i] = L + 1;
+                    }
+                }
+            }
+            append_new_tokens<D>(p, sm, cta, G, tid);
+        }
+    }
+    if (!any) return;
     Consumer<D, FMT> cons(p, sm, warp, lane);
     const uint32_t stage0 = smem_u32(sm.base + sm.L.stages);
     int32_t kbase = 0;  // real tiles of earlier pieces
-    int32_t s = s_first, sst, sreal, r0, r1;
-    bool have = plan.next_piece(s, X0, X1, sst, sreal, r0, r1);
+    int32_t cur = cur0;
+    Piece pc = first;
+    bool have = true;
     uint32_t qn[Consumer<D, FMT>::KS][2];
     float qsn = 0.f;
-    if (have) cons.load_q(s, qn, qsn);
+    cons.load_q(pc.s, qn, qsn);
     while (have) {
 #pragma unroll
         for (int ks = 0; ks < Consumer<D, FMT>::KS; ++ks) {
@@ -1052,12 +1360,25 @@ attention_kernel(const __grid_constant__ AttnParams p,
             cons.qf[ks][1] = qn[ks][1];
         }
         cons.qsc = qsn;
-        // the next piece's query is fetched while this piece streams
-        int32_t s2 = s + 1, c2, real2, a2, b2;
-        const bool have2 = plan.next_piece(s2, X0, X1, c2, real2, a2, b2);
-        if (have2) cons.load_q(s2, qn, qsn);
+        // the next piece's query is fetched while this piece streams (only its cursor stays
+        // live; the piece is looked up again at the switch)
+        int32_t cur2 = cur;
+        pieces.advance(cur2);
+        bool have2;
+        {
+            Piece nx;
+            have2 = pieces.piece(cur2, nx);
+            if (have2) cons.load_q(nx.s, qn, qsn);
+        }
+        // with the fused append, this lane's chunk of the segment's new K / V row (the tile
+        // that holds the new token gets it written into its row)
+        uint4 patch = make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (FMT == DATTN_KV_BF16) {
+            if (p.append) patch = cons.load_new_row(pc.s);
+        }
         cons.reset();
-        const int32_t nr = r1 - r0;
+        const int32_t s = pc.s;
+        const int32_t nr = pc.r1 - pc.r0;
         if constexpr (FMT == DATTN_KV_INT4) {
             // Tiles go to the warps in pairs: pair P holds the tiles 2P and 2P + 1 of the CTA's
             // sequence, and warp P mod 4 takes it, so (the ring being a multiple of 8 stages)
@@ -1113,8 +1434,12 @@ attention_kernel(const __grid_constant__ AttnParams p,
                     cons.tile_f8(stage0 + (uint32_t)stg * sm.L.stage_bytes, sm.scales(stg), lo, hi,
                                  cut);
                 } else {
-                    cons.tile(stage0 + (uint32_t)stg * sm.L.stage_bytes, lo, hi, cut);
-                    if (lo > 0 || hi < 16) fence_proxy_async_smem();
+                    const uint32_t st = stage0 + (uint32_t)stg * sm.L.stage_bytes;
+                    const bool patched = (lohi & kTilePatch) != 0;
+                    if (patched) cons.patch_row(st, tile_patch_row(lohi), patch);
+                    cons.tile(st, lo, hi, cut);
+                    // generic writes to the stage (patch, zeroed rows) before TMA refills it
+                    if (patched || lo > 0 || hi < 16) fence_proxy_async_smem();
                 }
             }
             __syncwarp();
@@ -1124,8 +1449,8 @@ attention_kernel(const __grid_constant__ AttnParams p,
         // ---- merge the four warps' states of this piece -------------------------------
         cons.publish();
         named_bar_sync(1, kConsumerWarps * 32);
-        const int32_t c_first = split_owner(sst, W, Gw);
-        const int32_t c_last = split_owner(sst + sreal - 1, W, Gw);
+        const int32_t c_first = pc.cfirst;
+        const int32_t c_last = pc.clast;
         const bool whole = c_first == c_last;
         const int ctid = tid;  // 0..127
         constexpr int kCT = kConsumerWarps * 32;
@@ -1236,12 +1561,8 @@ attention_kernel(const __grid_constant__ AttnParams p,
             }
         }
         named_bar_sync(1, kConsumerWarps * 32);  // shared state is reused by the next piece
-        s = s2;
-        sst = c2;
-        sreal = real2;
-        r0 = a2;
-        r1 = b2;
-        have = have2;
+        cur = cur2;
+        have = have2 && pieces.piece(cur, pc);
     }
 }
 
@@ -1284,20 +1605,21 @@ int occupancy(uint32_t smem) {
 }  // namespace
 
 size_t attn_workspace_bytes(int32_t nseg, int32_t g, int32_t D, int32_t G) {
-    const size_t counters = ((size_t)nseg * 4 + 255) & ~(size_t)255;
-    return counters + (size_t)(G + nseg) * slot_floats(g, D) * 4;
+    return attn_counter_bytes(nseg) + (size_t)(G + nseg) * slot_floats(g, D) * 4;
 }
+
 
 template <int D, int FMT>
 static dattn_status_t launch_d(const AttnParams& p0, const void* k_pool, const void* v_pool,
                                int32_t num_splits, void* ws, size_t ws_bytes,
                                cudaStream_t stream, int64_t tiles_bound) {
     AttnParams p = p0;
-    const AttnSmem L = attn_smem_layout(D, p.gq, p.nitems, p.Hkv, p.mode == MODE_SPARSE, FMT);
+    const AttnSmem L =
+        attn_smem_layout(D, p.gq, p.nitems, p.Hkv, p.mode == MODE_SPARSE, FMT, p.append != 0);
     dattn_status_t st = ensure_smem<D, FMT>(L.total);
     if (st != DATTN_OK) return st;
     const int32_t G = choose_splits(tiles_bound, num_splits, occupancy<D, FMT>(L.total));
-    const size_t counters = ((size_t)p.nseg * 4 + 255) & ~(size_t)255;
+    const size_t counters = attn_counter_bytes(p.nseg);
     if (ws == nullptr || ws_bytes < attn_workspace_bytes(p.nseg, p.gq, D, G) ||
         (reinterpret_cast<uintptr_t>(ws) & 255))
         return DATTN_ERR_WORKSPACE;

@@ -311,6 +311,34 @@ __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Folds 8 bf16 key channels (one 16-byte chunk) into a logical page's running k_max / k_min,
+// per channel with strict comparisons, so that on a tie the earlier value stays.
+__device__ __forceinline__ void bf16_fold8(const uint4& k, uint4& mx, uint4& mn) {
+    const uint32_t kw[4] = {k.x, k.y, k.z, k.w};
+    uint32_t xw[4] = {mx.x, mx.y, mx.z, mx.w};
+    uint32_t nw[4] = {mn.x, mn.y, mn.z, mn.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t a = kw[i] & 0xffffu, z = kw[i] >> 16;
+        uint32_t x0 = xw[i] & 0xffffu, x1 = xw[i] >> 16;
+        uint32_t n0 = nw[i] & 0xffffu, n1 = nw[i] >> 16;
+        if (bf16_lo(a) > bf16_lo(x0)) x0 = a;
+        if (bf16_lo(a) < bf16_lo(n0)) n0 = a;
+        if (bf16_lo(z) > bf16_lo(x1)) x1 = z;
+        if (bf16_lo(z) < bf16_lo(n1)) n1 = z;
+        xw[i] = x0 | (x1 << 16);
+        nw[i] = n0 | (n1 << 16);
+    }
+    mx = make_uint4(xw[0], xw[1], xw[2], xw[3]);
+    mn = make_uint4(nw[0], nw[1], nw[2], nw[3]);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ void set_err(int32_t* dev_err, int32_t bit) {
     if (dev_err) atomicOr(dev_err, bit);
 }

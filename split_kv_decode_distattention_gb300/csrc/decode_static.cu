@@ -79,7 +79,7 @@ extern "C" dattn_status_t dattn_decode_noalloc(const dattn_kv_layout* layout,
     dattn_status_t st = scratch_address(&scratch);
     if (st != DATTN_OK) return st;
     // the per-head counters must start at zero; the rest is written before it is read
-    const size_t counters = ((size_t)B * layout->num_kv_heads * 4 + 255) & ~(size_t)255;
+    const size_t counters = attn_counter_bytes(B * layout->num_kv_heads);
     if (counters > 0 &&
         cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return DATTN_ERR_CUDA;

@@ -56,13 +56,23 @@ struct AttnParams {
     const int8_t* head_kind;
     int32_t sinks, local, top_k;
     const int32_t* selected;
+    const int32_t* selected_phys;  // nullable: physical pages of `selected` (no table lookup)
+    // fused one-token append (dattn_append_decode, bf16 pool): the new token of request b is
+    // written at position seq_lens[b], attended by this launch, and seq_lens[b] advances by one
+    int32_t append;
+    const uint16_t* k_new;  // [B][Hkv][D]
+    const uint16_t* v_new;
+    uint16_t* k_pool_w;
+    uint16_t* v_pool_w;
+    uint16_t* stats;  // nullable: logical-page k_max / k_min
+    int32_t* seq_lens_w;  // seq_lens, advanced by the launch
     // outputs: decode -> out [B][Hq][D], m_out / e_out [B][Hq] (nullable)
     //          partial -> out = MA [C][Hq][D], m_out / e_out [C][Hq]
     float* out;
     float* m_out;
     float* e_out;
     // workspace
-    int32_t* counters;  // [nseg]
+    int32_t* counters;  // [nseg + 1]: per segment, then the append's arrival count
     float* slots;       // [(G + nseg)][slot_floats(g, D)]: MA [g][D], m [g], e [g], padding
     int32_t nseg;
     int32_t nitems;     // B for dense / sparse, C for partial
@@ -85,11 +95,15 @@ __host__ __device__ inline int32_t slot_floats(int32_t g, int32_t D) {
 // with a quantized pool, the stage's 16 K scales and 16 V scales sit in `scales`.
 struct AttnSmem {
     uint32_t nstages, stage_bytes, stages, scales, bars, meta, flags, ws_m, ws_e, ws_o, kind_before,
-        kinds, item_start, item_len, scan, total;
+        kinds, aplan, item_start, item_len, item_pos, scan, total;
 };
 
+// Integers of the head-aligned plan of a block-sparse launch (see the attention kernel):
+// its scalars, then the retrieval and the streaming head lists.
+constexpr int kAplanScalars = 8;
+
 __host__ __device__ inline AttnSmem attn_smem_layout(int D, int g, int nitems, int Hkv,
-                                                     bool sparse, int fmt) {
+                                                     bool sparse, int fmt, bool append = false) {
     AttnSmem s;
     const uint32_t ns = (uint32_t)attn_stages(fmt);
     s.nstages = ns;
@@ -99,15 +113,17 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int D, int g, int nitems, i
     s.scales = o;      o += fmt != DATTN_KV_BF16 ? ns * 128u : 0u;
     s.bars = o;        o += 2u * ns * 8u;
     s.meta = o;        o += ns * 4u;
-    s.flags = o;       o += 16u;
+    s.flags = o;       o += 32u;  // abort flag, last flag, then 5 plan constants
     s.ws_m = o;        o += kConsumerWarps * kMaxGroup * 4u;
     s.ws_e = o;        o += kConsumerWarps * kMaxGroup * 4u;
     s.ws_o = o;        o += (uint32_t)(kConsumerWarps * g * D) * 4u;
     s.kind_before = o; o += sparse ? (uint32_t)(Hkv + 1) * 3u * 4u : 0u;
     s.kinds = o;       o += sparse ? (uint32_t)Hkv * 4u : 0u;
+    s.aplan = o;       o += sparse ? (uint32_t)(kAplanScalars + 2 * Hkv) * 4u : 0u;
     o = (o + 15u) & ~15u;
     s.item_start = o;  o += (uint32_t)(nitems + 1) * 4u;
     s.item_len = o;    o += (uint32_t)nitems * 4u;
+    s.item_pos = o;    o += append ? (uint32_t)nitems * 4u : 0u;
     o = (o + 15u) & ~15u;
     s.scan = o;        o += 8u * 4u;
     s.total = o + 1024u;  // slack to align the dynamic base to 1024 bytes
@@ -149,6 +165,11 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // Number of CTAs for a launch with an upper bound of total_tiles tiles.
 int32_t choose_splits(int64_t total_tiles, int32_t requested, int occupancy);
 
+// Bytes of the workspace's counter region: one counter per segment and the append's arrival
+// counter, padded to 256 bytes. The partial slots follow it.
+inline size_t attn_counter_bytes(int32_t nseg) {
+    return ((size_t)(nseg + 1) * 4 + 255) & ~(size_t)255;
+}
 size_t attn_workspace_bytes(int32_t nseg, int32_t g, int32_t D, int32_t G);
 size_t select_workspace_bytes(int32_t nseg, int32_t top_k, int32_t G);
 

@@ -37,27 +37,6 @@ constexpr int kAppendWindow = 64;  // token positions per CTA, a multiple of 16
 
 __device__ __forceinline__ float bf(uint32_t h) { return __uint_as_float(h << 16); }
 
-// strict comparisons per bf16 channel: on a tie the earlier value stays
-__device__ __forceinline__ void fold8(const uint4& k, uint4& mx, uint4& mn) {
-    const uint32_t kw[4] = {k.x, k.y, k.z, k.w};
-    uint32_t xw[4] = {mx.x, mx.y, mx.z, mx.w};
-    uint32_t nw[4] = {mn.x, mn.y, mn.z, mn.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t a = kw[i] & 0xffffu, z = kw[i] >> 16;
-        uint32_t x0 = xw[i] & 0xffffu, x1 = xw[i] >> 16;
-        uint32_t n0 = nw[i] & 0xffffu, n1 = nw[i] >> 16;
-        if (bf(a) > bf(x0)) x0 = a;
-        if (bf(a) < bf(n0)) n0 = a;
-        if (bf(z) > bf(x1)) x1 = z;
-        if (bf(z) < bf(n1)) n1 = z;
-        xw[i] = x0 | (x1 << 16);
-        nw[i] = n0 | (n1 << 16);
-    }
-    mx = make_uint4(xw[0], xw[1], xw[2], xw[3]);
-    mn = make_uint4(nw[0], nw[1], nw[2], nw[3]);
-}
-
 // Max |x| of the 8 bf16 values of a 16-byte chunk.
 __device__ __forceinline__ float absmax8(const uint4& v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -242,7 +221,7 @@ kv_append_kernel(dattn_kv_layout L, void* __restrict__ k_pool_v, void* __restric
                     mn = *reinterpret_cast<const uint4*>(st + D);
                 }
             }
-            fold8(kv, mx, mn);
+            bf16_fold8(kv, mx, mn);
         }
         if (st != nullptr) {
             *reinterpret_cast<uint4*>(st) = mx;

@@ -63,6 +63,7 @@ struct SelParams {
     const int8_t* head_kind;
     int32_t top_k;
     int32_t* selected;
+    int32_t* selected_phys;  // nullable: the pool page of each selected page
     int32_t* counters;
     uint64_t* slots;
     int32_t nseg;
@@ -359,7 +360,10 @@ page_select_kernel(const __grid_constant__ SelParams p) {
         int32_t st, len;
         seg_span(s, st, len);
         if (len == 0)
-            for (int r = tid; r < K; r += NT) p.selected[(int64_t)s * K + r] = -1;
+            for (int r = tid; r < K; r += NT) {
+                p.selected[(int64_t)s * K + r] = -1;
+                if (p.selected_phys) p.selected_phys[(int64_t)s * K + r] = -1;
+            }
     }
     if (t_begin >= t_end) return;
 
@@ -397,9 +401,12 @@ page_select_kernel(const __grid_constant__ SelParams p) {
                 f[i] = (i < K && f[i] != 0ull) ? (f[i] & 0xFFFFFFFFull) : 0ull;
             __syncwarp();
             bitonic_desc(f, Kp, lane, 32, wsync);  // low word descending = page ascending
+            const int32_t* btrow = p.block_table + (int64_t)(seg / p.Hkv) * p.max_pages;
             for (int r = lane; r < K; r += 32) {
                 const uint64_t kk = f[r];
-                p.selected[(int64_t)seg * K + r] = kk ? (int32_t)(0xFFFFFFFFu - (uint32_t)kk) : -1;
+                const int32_t pg = kk ? (int32_t)(0xFFFFFFFFu - (uint32_t)kk) : -1;
+                p.selected[(int64_t)seg * K + r] = pg;
+                if (p.selected_phys) p.selected_phys[(int64_t)seg * K + r] = pg >= 0 ? btrow[pg] : -1;
             }
         }
         csync();
@@ -758,9 +765,9 @@ size_t select_workspace_bytes(int32_t nseg, int32_t top_k, int32_t G) {
 dattn_status_t launch_page_select(const dattn_kv_layout& Lay, const uint16_t* stats,
                                   const uint16_t* q, int32_t B, int32_t Hq,
                                   const int32_t* seq_lens, const int8_t* head_kind,
-                                  int32_t top_k, int32_t* selected, void* ws, size_t ws_bytes,
-                                  int32_t num_splits, int32_t* dev_err, cudaStream_t stream,
-                                  int64_t units_bound) {
+                                  int32_t top_k, int32_t* selected, int32_t* selected_phys,
+                                  void* ws, size_t ws_bytes, int32_t num_splits,
+                                  int32_t* dev_err, cudaStream_t stream, int64_t units_bound) {
     if (B == 0 || top_k == 0) return DATTN_OK;
     SelParams p{};
     p.num_pages = Lay.num_pages;
@@ -777,6 +784,7 @@ dattn_status_t launch_page_select(const dattn_kv_layout& Lay, const uint16_t* st
     p.head_kind = head_kind;
     p.top_k = top_k;
     p.selected = selected;
+    p.selected_phys = selected_phys;
     p.nseg = B * p.Hkv;
     p.dev_err = dev_err;
     const int D = Lay.head_dim;

@@ -7,8 +7,9 @@ from __future__ import annotations
 
 import torch
 
-from . import (KV_BF16, KV_FP8_E4M3, KV_INT4, KVLayout, SparseConfig, Workspace, dattn_decode,
-               dattn_decode_multi, dattn_kv_append, dattn_page_select)
+from . import (KV_BF16, KV_FP8_E4M3, KV_INT4, KVLayout, SparseConfig, Workspace,
+               dattn_append_decode, dattn_decode, dattn_decode_multi, dattn_kv_append,
+               dattn_page_select)
 from .workloads import Case
 
 
@@ -103,9 +104,9 @@ class PagedCache:
                                               device=self.device)
         return self._head_kind
 
-    def sparse_config(self, selected) -> SparseConfig:
+    def sparse_config(self, selected, selected_phys=None) -> SparseConfig:
         c = self.case
-        return SparseConfig(self.head_kind(), c.sinks, c.local, c.top_k, selected)
+        return SparseConfig(self.head_kind(), c.sinks, c.local, c.top_k, selected, selected_phys)
 
     def decode(self, q, out, ws, m_g=None, e_g=None, sparse=None, num_splits=0):
         """q [B][Hq][d]: dattn_decode; q [B][T][Hq][d]: dattn_decode_multi (dense only)."""
@@ -120,7 +121,16 @@ class PagedCache:
                      out, ws, m_g=m_g, e_g=e_g, sparse=sparse, num_splits=num_splits,
                      dev_err=self.dev_err)
 
-    def select(self, q, selected, ws, num_splits=0):
+    def append_decode(self, k_new, v_new, q, out, ws, m_g=None, e_g=None, sparse=None,
+                      num_splits=0):
+        """One-token append and decode in one launch (dattn_append_decode)."""
+        dattn_append_decode(self.layout, self.k_pool, self.v_pool, self.stats, k_new, v_new, q,
+                            self.case.scale, self.seq_lens, out, ws, m_g=m_g, e_g=e_g,
+                            sparse=sparse, num_splits=num_splits, dev_err=self.dev_err)
+        self.lens = [L + 1 for L in self.lens]
+
+    def select(self, q, selected, ws, num_splits=0, selected_phys=None):
         c = self.case
         dattn_page_select(self.layout, self.stats, q, self.seq_lens, self.head_kind(), c.top_k,
-                          selected, ws, num_splits=num_splits, dev_err=self.dev_err)
+                          selected, ws, num_splits=num_splits, dev_err=self.dev_err,
+                          selected_phys=selected_phys)

@@ -159,11 +159,11 @@ def test_page_select_needs_power_of_two_logical_pages(dattn):
     lib = dattn.load_library()
     p = ctypes.c_void_p(16)  # never dereferenced: validation fails first
     lay = _lay(dattn, page_size=48)  # three logical pages per physical page
-    assert lib.dattn_page_select(ctypes.byref(lay.c), p, p, 1, 4, p, p, 8, p, p, 1 << 20, 0,
-                                 None, None) == 2  # DATTN_ERR_UNSUPPORTED
+    assert lib.dattn_page_select(ctypes.byref(lay.c), p, p, 1, 4, p, p, 8, p, None, p, 1 << 20,
+                                 0, None, None) == 2  # DATTN_ERR_UNSUPPORTED
     lay = _lay(dattn, page_size=64)
-    assert lib.dattn_page_select(ctypes.byref(lay.c), p, p, 1, 4, p, p, 300, p, p, 1 << 20, 0,
-                                 None, None) == 2  # top_k above 256
+    assert lib.dattn_page_select(ctypes.byref(lay.c), p, p, 1, 4, p, p, 300, p, None, p,
+                                 1 << 20, 0, None, None) == 2  # top_k above 256
 
 
 def test_sparse_settings_are_validated(dattn):
@@ -198,8 +198,18 @@ def test_other_entry_points_validate(dattn):
     assert lib.dattn_partial(ctypes.byref(lay.c), p, p, p, 1, 4, 0.1, p, 2, None, p, p, p, p, p,
                              p, 1 << 20, 0, None, None) == 1
     # page select: top_k too large
-    assert lib.dattn_page_select(ctypes.byref(lay.c), p, p, 1, 4, p, p, 300, p, p, 1 << 20, 0,
-                                 None, None) == 2
+    assert lib.dattn_page_select(ctypes.byref(lay.c), p, p, 1, 4, p, p, 300, p, None, p,
+                                 1 << 20, 0, None, None) == 2
+    # fused append and decode: a quantized pool is unsupported; null new rows are invalid
+    lay8 = _lay(dattn)
+    lay8.c.kv_format = dattn.KV_FP8_E4M3
+    lay8.c.kv_scale = p
+    assert lib.dattn_append_decode(ctypes.byref(lay8.c), p, p, None, p, p, p, 1, 4, 0.1, p, None,
+                                   0, p, 1 << 20, p, None, None, None, None) == 2
+    assert lib.dattn_append_decode(ctypes.byref(lay.c), p, p, None, None, p, p, 1, 4, 0.1, p,
+                                   None, 0, p, 1 << 20, p, None, None, None, None) == 1
+    assert lib.dattn_append_decode(ctypes.byref(lay.c), p, p, None, p, ctypes.c_void_p(18), p, 1,
+                                   4, 0.1, p, None, 0, p, 1 << 20, p, None, None, None, None) == 1
 
 
 def test_workspace_size(dattn):
@@ -209,11 +219,11 @@ def test_workspace_size(dattn):
     a = dattn.dattn_workspace_size(8, 32, 8, 128, 0, 100)
     b = dattn.dattn_workspace_size(8, 32, 8, 128, 64, 100)
     assert b >= a
-    # counters (8*8 ints, padded to 256 B) + (G + segments) slots of g*d + 2g floats,
-    # rounded up to a multiple of 4 floats
-    assert a == 256 + (100 + 64) * (4 * 128 + 8) * 4
+    # counters (8*8 per segment plus the fused append's one: 65 ints, padded to 256 B) +
+    # (G + segments) slots of g*d + 2g floats, rounded up to a multiple of 4 floats
+    assert a == 512 + (100 + 64) * (4 * 128 + 8) * 4
     c = dattn.dattn_workspace_size(8, 24, 8, 128, 0, 100)  # g = 3: 6 -> 8 trailing floats
-    assert c == 256 + (100 + 64) * (3 * 128 + 8) * 4
+    assert c == 512 + (100 + 64) * (3 * 128 + 8) * 4
 
 
 def test_binding_rejects_short_tensors_before_any_call(dattn):

@@ -67,10 +67,11 @@ def test_sparse_512k_step_and_selection_bytes():
     sel_rows = 8 * 4 * 64 * 4
     retrieval = 67_108_864  # 8 x 4 heads x 64 pages x 64 tokens x (K + V) x 256 bytes
     streaming = 196_608     # 8 x 4 heads x (4 sinks + 8 local) x (K + V) x 256 bytes
-    assert plain["decode"] == retrieval + streaming + q + out + sel_rows + 8 * 4
+    # the selection rows are read with their pool pages (dattn_sparse.selected_phys)
+    assert plain["decode"] == retrieval + streaming + q + out + 2 * sel_rows + 8 * 4
     stats = 536_870_912     # 8 x 4 heads x 32768 logical pages x 512 bytes
     bt = 8 * (524288 // 64) * 4
-    assert sel["select"] == stats + q + sel_rows + bt
+    assert sel["select"] == stats + q + 2 * sel_rows + bt
     assert plain["select"] == 0
 
 
