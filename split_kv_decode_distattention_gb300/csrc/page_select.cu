@@ -14,33 +14,26 @@
 // k_min of the retrieval heads (512 B per logical page at d = 128), and it must score them
 // at that speed. The physical pages of all retrieval (request, KV head) pairs are laid end
 // to end and cut into equal contiguous ranges, one per CTA.
-//  - A warp reads one logical page per load instruction, fully coalesced: lanes 0-15 take
-//    d/16 channels each of k_max, lanes 16-31 the same channels of k_min. The query values
-//    of those channels stay in the lane's registers for the whole piece (their positive
-//    part for k_max lanes, their negative part for k_min lanes), as fp32 pairs for packed
-//    fp32x2 fused multiply-adds.
-//  - A batch is 32 / HG logical pages. Each lane leaves one partial sum per (page, head):
-//    32 values. One transposed butterfly over the 32 lanes (31 shuffles) sums them, after
-//    which lane l holds the full score of page l / HG and head l % HG.
-//  - Loads run one batch ahead: the register holding a page's data is refilled with the
-//    same page of the warp's next batch as soon as it has been used. Block-table entries of
-//    the piece are staged in shared memory first, so no load waits on another.
+//  - Scoring is a dense contraction: for a unit of 16 logical pages the scores of the g
+//    query heads are [k_max | k_min] (16 x 2d, bf16) times [max(q,0) | min(q,0)]^T (2d x g,
+//    bf16), which runs on the tensor cores (mma m16n8k16, the 16 pages on M, the heads on N).
+//    One of max(q,0), min(q,0) is an exact zero per channel, so the contraction adds exactly
+//    the products the score definition picks, and every product of two bf16 values is exact.
+//  - A unit's physical pages arrive by one bulk copy each (up to 2 KB at P = 64), staged so
+//    that the ldmatrix reads of the 16-row tile meet at most 2-way bank conflicts (see
+//    sel_stage_bytes). Sixteen warps per SM keep enough copies in flight; each holds as many
+//    units as shared memory allows and refills a stage as soon as it has read it. Units
+//    (whole physical pages) are handed to the warps by a shared counter, so faster warps take
+//    more. Block-table entries of a piece are staged in shared memory first.
+//  - Rounding: each 16-channel k-step runs with a zero accumulator and its result is added
+//    to the running sum in fp32 (round to nearest), in a fixed order. Whatever rounding the
+//    tensor core applies inside one k-step (16 exact products), the sum stays far inside the
+//    bound the selection is held to for any fp32 evaluation, d * 2^-23 * sum |terms|.
 //  - The physical-page score is a max over adjacent lanes (heads, then logical pages). Page
-//    maxima that beat the warp's running K-th key go to a per-warp candidate buffer, folded
-//    into the warp's top K by a warp-synchronous bitonic sort.
-//  - At the end of a piece the eight warps' lists are merged. A head split across CTAs
-//    leaves each CTA's top K in the workspace, and the CTA that arrives last merges them.
-//
-// Arithmetic. The score is evaluated in fp32: every product of two bf16 values is exact in
-// fp32, so only the additions round, and a sum of n such terms in any order is within
-// (n-1) 2^-24 / (1 - (n-1) 2^-24) of sum |terms| of the exact value. Pages whose scores lie
-// that close may be ranked either way; the result is still a top-K of the definition's
-// scores up to that rounding, and a fixed evaluation order makes it deterministic. Channels
-// form 16 chunks of d/16; each chunk gives a k_max partial with the positive part max(q,0)
-// and a k_min partial with the negative part min(q,0) (one of the two factors is an exact
-// zero, so together they add exactly the product the definition's max picks), each as two
-// fused multiply-add chains (even and odd channels); the 32 partials are then summed across
-// the lanes.
+//    maxima that reach the running K-th key go to a per-warp candidate buffer, folded into
+//    the warp's top K by a warp-synchronous bitonic sort.
+//  - At the end of a piece the warps' lists are merged. A head split across CTAs leaves each
+//    CTA's top K in the workspace, and the CTA that arrives last merges them.
 #include "common.cuh"
 #include "internal.h"
 
@@ -48,10 +41,11 @@ namespace dattn {
 
 namespace {
 
-// Warps per CTA (one CTA per SM): 16 when a lane scores 4 query heads, 8 when it scores 8
-// (their query values take twice the registers).
-__host__ __device__ constexpr int sel_warps(int hg) { return hg == 4 ? 16 : 8; }
-constexpr int kSelMaxWarps = 16;
+// Warps per CTA (one CTA per SM): sixteen keep enough bulk copies in flight per SM. The
+// warps' lists are merged pairwise, so the count is a power of two.
+constexpr int kSelWarps = 16;
+constexpr int kSelMaxWarps = kSelWarps;
+static_assert((kSelWarps & (kSelWarps - 1)) == 0, "pairwise list merges need 2^n warps");
 
 struct SelParams {
     int32_t num_pages, Hkv, P, max_pages;
@@ -67,7 +61,7 @@ struct SelParams {
     int32_t* counters;
     uint64_t* slots;
     int32_t nseg;
-    int32_t stages;  // statistics batches staged per warp
+    int32_t stages;  // units of statistics rows staged per warp
     int32_t* dev_err;
 };
 
@@ -85,7 +79,7 @@ struct SelSmem {
     int kp, wn, stages;
 };
 
-// nw: warps per CTA; stage_bytes: one batch of statistics rows; stages: batches staged per
+// nw: warps per CTA; stage_bytes: one unit of statistics rows; stages: units staged per
 // warp.
 __host__ __device__ inline SelSmem sel_smem_layout(int B, int Hkv, int K, int nw,
                                                    uint32_t stage_bytes, int stages) {
@@ -93,7 +87,7 @@ __host__ __device__ inline SelSmem sel_smem_layout(int B, int Hkv, int K, int nw
     s.stages = stages;
     s.kp = next_pow2(K);                     // list length: K rounded up to a power of two
     // per-warp buffer: running list, then room for max(Kp, 32) candidates (a power of two;
-    // a batch adds up to 32 before a fold)
+    // a unit adds up to 16 before a fold)
     s.wn = s.kp + (s.kp > 32 ? s.kp : 32);
     uint32_t o = 0;
     // +0: last-arrival flag, +4: abort flag, +8: next unit, +16: CTA-wide K-th key
@@ -127,28 +121,6 @@ __device__ __forceinline__ float key_score(uint64_t key) {
     if (key == 0ull) return -__int_as_float(0x7f800000);
     const uint32_t ord = (uint32_t)(key >> 32);
     return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7fffffffu) : ~ord);
-}
-
-__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-
-__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-
-// a * b, two independent IEEE fp32 products
-__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-
-// acc = a * b + acc, two independent IEEE fp32 fused multiply-adds
-__device__ __forceinline__ void fma_f32x2(uint64_t& acc, uint64_t a, uint64_t b) {
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
 
 // Bitonic sort of buf[0..n) into descending order by nthreads threads (index tid); sync()
@@ -195,41 +167,42 @@ __device__ __forceinline__ void warp_merge_desc(uint64_t* a, const uint64_t* b, 
     }
 }
 
-template <int CPL> struct ChunkVec;
-template <> struct ChunkVec<8> { using type = uint4; };  // 8 bf16 channels
-template <> struct ChunkVec<4> { using type = uint2; };  // 4 bf16 channels
 
-// Two bf16 (low half: even channel, high half: odd channel) -> the fp32 pair {even, odd},
-// built in one 64-bit register pair so that the packed FMA needs no moves.
-__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
-    uint64_t r;
-    asm("{\n\t.reg .b32 lo, hi;\n\t"
-        "shl.b32 lo, %1, 16;\n\t"
-        "and.b32 hi, %1, 0xffff0000;\n\t"
-        "mov.b64 %0, {lo, hi};\n\t}"
-        : "=l"(r)
-        : "r"(w));
-    return r;
-}
-__device__ __forceinline__ void unpack_bf16x8(const uint4& v, uint64_t (&k)[4]) {
-    k[0] = bf16x2_to_f32x2(v.x);
-    k[1] = bf16x2_to_f32x2(v.y);
-    k[2] = bf16x2_to_f32x2(v.z);
-    k[3] = bf16x2_to_f32x2(v.w);
-}
-__device__ __forceinline__ void unpack_bf16x8(const uint2& v, uint64_t (&k)[2]) {
-    k[0] = bf16x2_to_f32x2(v.x);
-    k[1] = bf16x2_to_f32x2(v.y);
+// The logical pages of one unit (the mma's M).
+constexpr int kUnitRows = 16;
+
+// Staging of a unit. With up to 4 logical pages per physical page, a physical page's rows
+// arrive by one bulk copy at a stride of LPG rows plus 16 bytes, and row i of the unit's mma
+// tile is logical page i / UPP of physical page i % UPP: the eight rows an ldmatrix reads
+// then come from at least two physical pages each in a distinct bank group (a 2-way
+// conflict at most). With 8 or 16 logical pages per physical page, every logical page has
+// its own copy and row stride 2d bf16 plus 16 bytes (no conflict).
+__host__ __device__ constexpr bool sel_page_copies(int LPG) { return LPG <= 4; }
+__host__ __device__ constexpr uint32_t sel_stage_bytes(int D, int LPG) {
+    return sel_page_copies(LPG) ? (uint32_t)(16 / LPG) * ((uint32_t)LPG * 4u * D + 16u)
+                                : 16u * (4u * (uint32_t)D + 16u);
 }
 
-// A lane's chunk of one logical page's row in a shared-memory stage.
-__device__ __forceinline__ void lds_chunk(uint4& v, uint32_t addr) {
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
+// d = a * b with a zero accumulator (m16n8k16, bf16 in, fp32 out).
+__device__ __forceinline__ void mma_bf16_zero_acc(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                  uint32_t a2, uint32_t a3, uint32_t b0,
+                                                  uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
-__device__ __forceinline__ void lds_chunk(uint2& v, uint32_t addr) {
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+
+// The positive part max(x, 0) and the negative part min(x, 0) of two bf16 values, exactly
+// (a value keeps its bits or becomes +0).
+__device__ __forceinline__ uint32_t bf16x2_pos(uint32_t w) {
+    const uint32_t neg = ((w >> 15) & 0x00010001u) * 0xffffu;
+    return w & ~neg;
+}
+__device__ __forceinline__ uint32_t bf16x2_neg(uint32_t w) {
+    const uint32_t neg = ((w >> 15) & 0x00010001u) * 0xffffu;
+    return w & neg;
 }
 
 // Adds bytes to the transaction count of the barrier's current phase (no arrival).
@@ -238,26 +211,27 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                  : "memory");
 }
 
-// D: head_dim; HG: query heads scored per KV head (4 or 8, unused ones masked);
-// LPG: logical pages per physical page (P / 16, a power of two).
-template <int D, int HG, int LPG>
-__global__ void __launch_bounds__(sel_warps(HG) * 32, 1)
+// D: head_dim; LPG: logical pages per physical page (P / 16, a power of two).
+template <int D, int LPG>
+__global__ void __launch_bounds__(kSelWarps * 32, 1)
 page_select_kernel(const __grid_constant__ SelParams p) {
-    constexpr int NW = sel_warps(HG);        // warps per CTA
+    constexpr int NW = kSelWarps;
     constexpr int NT = NW * 32;
-    constexpr int CPL = D / 16;              // channels per lane
-    constexpr int NPR = CPL / 2;             // channel pairs per lane
-    constexpr int R = 32 / HG;               // logical pages per batch
-    constexpr int UNIT = LPG > R ? LPG : R;  // logical pages per warp unit (whole pages)
-    constexpr int NB = UNIT / R;             // batches per unit
-    constexpr int PPU = UNIT / LPG;          // physical pages per unit
-    using Vec = typename ChunkVec<CPL>::type;
+    constexpr int KS = 2 * D / 16;             // k-steps over the 2d channels [k_max | k_min]
+    constexpr int UPP = kUnitRows / LPG;       // physical pages per unit
+    constexpr uint32_t kRowBytes = 4u * D;     // one logical page's row: k_max and k_min
+    constexpr bool kPageCopies = sel_page_copies(LPG);
+    // byte offset of a physical page and of a row within it in a stage
+    constexpr uint32_t kPageStride = kPageCopies ? LPG * kRowBytes + 16u : LPG * (kRowBytes + 16u);
+    constexpr uint32_t kRowStride = kPageCopies ? kRowBytes : kRowBytes + 16u;
+    constexpr uint32_t kStageBytes = sel_stage_bytes(D, LPG);
+    static_assert(kStageBytes >= UPP * kPageStride, "stage holds the unit");
     const float kNInf = -__int_as_float(0x7f800000);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_off = smem_u32(smem_raw);
     uint8_t* base = smem_raw + (((raw_off + 127u) & ~127u) - raw_off);
     const int K = p.top_k;
-    const SelSmem L = sel_smem_layout(p.B, p.Hkv, K, NW, R * 4u * D, p.stages);
+    const SelSmem L = sel_smem_layout(p.B, p.Hkv, K, NW, kStageBytes, p.stages);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t G = gridDim.x, cta = blockIdx.x;
     int* last_flag = reinterpret_cast<int*>(base + L.flags);
@@ -414,25 +388,22 @@ page_select_kernel(const __grid_constant__ SelParams p) {
 
     const uint64_t pol = policy_evict_first();
     int32_t* bt_s = reinterpret_cast<int32_t*>(base + L.bt);
-    const int half = lane >> 4;           // 0: k_max lanes, 1: k_min lanes
-    const int c0 = CPL * (lane & 15);     // first channel of the lane
-    const int lane_off = half * D + c0;   // element offset inside a logical-page row
-    const int hj = lane % HG;             // head of the score the lane holds after reduction
-    const int ri = lane / HG;             // logical page (in the batch) of that score
-    constexpr int LPB = LPG < R ? LPG : R;  // logical pages of one physical page in a batch
-    constexpr int PPB = R / LPB;            // physical pages in a batch
-    constexpr uint32_t kRowBytes = 4 * D;   // one logical page's row: k_max and k_min
-    constexpr uint32_t kStageBytes = R * kRowBytes;
-    // Lane l computes its partials in a permuted order: register slot (i, j) holds the
-    // partial of logical page i ^ ri and head j ^ hj. Then in every level of the transposed
-    // butterfly the half a lane keeps is the same register range in all lanes, and the
-    // reduction needs no selects; afterwards lane l holds (page ri, head hj).
-    // This warp's stages: S buffers of one batch each, filled by bulk copies.
+    const int g8 = lane >> 2, tig = lane & 3;
+    // ldmatrix lane address within a unit: tile row i = (lane & 7) + 8 ((lane >> 3) & 1),
+    // 16-byte chunk lane >> 4 of the k-step's 32 bytes. Row i is logical page (i / UPP) of
+    // physical page (i % UPP) with page copies, else logical page (i % LPG) of physical page
+    // (i / LPG).
+    const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t lrow_off =
+        (kPageCopies ? (uint32_t)(lrow % UPP) * kPageStride + (uint32_t)(lrow / UPP) * kRowStride
+                     : (uint32_t)(lrow / LPG) * kPageStride + (uint32_t)(lrow % LPG) * kRowStride) +
+        (uint32_t)(lane >> 4) * 16u;
+    // This warp's stages: S units of 16 padded rows each, filled by bulk copies.
     const int S = L.stages;
     const uint32_t stage0 = smem_u32(base + L.stage) + (uint32_t)(warp * S) * kStageBytes;
     const uint32_t bar0 = smem_u32(base + L.bars) + (uint32_t)(warp * S) * 8u;
     uint32_t* smask = reinterpret_cast<uint32_t*>(base + L.masks) + warp * S;
-    int32_t* sbatch = reinterpret_cast<int32_t*>(base + L.batches) + warp * S;
+    int32_t* sunit = reinterpret_cast<int32_t*>(base + L.batches) + warp * S;
     int32_t* next_unit = reinterpret_cast<int32_t*>(base + L.flags + 8);
     unsigned long long* cta_thresh_u = reinterpret_cast<unsigned long long*>(base + L.flags + 16);
     volatile uint64_t* cta_thresh = reinterpret_cast<volatile uint64_t*>(cta_thresh_u);
@@ -441,8 +412,8 @@ page_select_kernel(const __grid_constant__ SelParams p) {
     fence_mbar_init();
     __syncwarp();
     // The warp uses its stages round robin over the whole kernel. (st, par) is the stage of
-    // the next batch to wait for and the parity of the phase that batch completes; every
-    // batch issued is eventually waited for or skipped with advance().
+    // the next unit to wait for and the parity of the phase that unit completes; every unit
+    // issued is eventually waited for or skipped with advance().
     int st = 0;
     uint32_t par = 0u;
     auto advance = [&]() {
@@ -461,21 +432,21 @@ page_select_kernel(const __grid_constant__ SelParams p) {
         const int32_t pe = min(sst + slen, t_end);
         const int32_t b = s / p.Hkv, h = s - b * p.Hkv;
         const int32_t Lb = item_len[b];
-        // query values of the lane's channels: positive part (k_max lanes) or negative part
-        // (k_min lanes), as fp32 pairs {even channel, odd channel}
-        uint64_t qv[HG][NPR];
+        // B fragments of [max(q,0) | min(q,0)]^T: lane holds column (query head) g8 at the
+        // k-step's channel pairs 2 tig, 2 tig + 1 and 2 tig + 8, 2 tig + 9 (heads >= g are 0)
+        uint32_t bq[KS][2];
+        {
+            const bool ok = g8 < p.g;
+            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                p.q + ((int64_t)b * p.Hq + h * p.g + (ok ? g8 : 0)) * D);
 #pragma unroll
-        for (int j = 0; j < HG; ++j) {
-            Vec w{};
-            const int jj = j ^ hj;  // head of register slot j
-            if (jj < p.g)
-                w = *reinterpret_cast<const Vec*>(p.q + ((int64_t)b * p.Hq + h * p.g + jj) * D + c0);
-            const uint32_t* ww = reinterpret_cast<const uint32_t*>(&w);
-#pragma unroll
-            for (int m = 0; m < NPR; ++m) {
-                const float q0 = bf16_lo(ww[m]), q1 = bf16_hi(ww[m]);
-                qv[j][m] = half == 0 ? pack_f32x2(q0 >= 0.f ? q0 : 0.f, q1 >= 0.f ? q1 : 0.f)
-                                     : pack_f32x2(q0 >= 0.f ? 0.f : q0, q1 >= 0.f ? 0.f : q1);
+            for (int ks = 0; ks < KS; ++ks) {
+                const int c = (16 * ks) % D;  // channel of the k-step within q
+                const uint32_t w0 = ok ? __ldg(qrow + c / 2 + tig) : 0u;
+                const uint32_t w1 = ok ? __ldg(qrow + c / 2 + 4 + tig) : 0u;
+                const bool posp = 16 * ks < D;  // k_max half: max(q,0); k_min half: min(q,0)
+                bq[ks][0] = posp ? bf16x2_pos(w0) : bf16x2_neg(w0);
+                bq[ks][1] = posp ? bf16x2_pos(w1) : bf16x2_neg(w1);
             }
         }
         for (int i = lane; i < L.wn; i += 32) wbuf[i] = 0ull;
@@ -493,153 +464,72 @@ page_select_kernel(const __grid_constant__ SelParams p) {
                 if (cb == 0) *cta_thresh = 0ull;
             }
             csync();
-            const int32_t nunits = (nc + PPU - 1) / PPU;
-            // Units (PPU physical pages, NB batches) are handed out to the warps by a shared
-            // counter, so warps that run faster take more of them. A warp takes a unit when
-            // it issues the copies of its first batch, S batches before it scores it. Batch
-            // index bi = unit * NB + sub; its R logical pages are PPB physical pages
-            // (block-relative first page pc_of(bi)) of LPB logical pages each, starting at
-            // logical page lp_of(bi).
-            auto pc_of = [&](int32_t bi) { return (bi / NB) * PPU; };
-            auto lp_of = [&](int32_t bi) { return (bi % NB) * R; };
-            int32_t iss_unit = 0, iss_sub = NB;  // the unit whose sub-batches are being issued
-            // Issues the next batch of this warp into stage st, or marks the stage empty
-            // (batch -1) once the units are exhausted. Lane t < PPB takes physical page t of
-            // the batch: its logical pages that hold tokens are one contiguous run of rows.
-            // smask[st] gets the mask of rows (in batch order) that were copied; the others
-            // are never read as scores.
+            const int32_t nunits = (nc + UPP - 1) / UPP;
+            // Issues the next unit of this warp into stage st, or marks the stage empty (-1)
+            // once the units are exhausted. With page copies lane t < UPP takes physical page
+            // t of the unit: its logical pages that hold tokens are a prefix of nv rows,
+            // copied at once. Otherwise lane r < 16 takes logical page r % LPG of physical
+            // page r / LPG. smask[st] gets the mask of tile rows copied; the others are never
+            // scored.
             auto issue = [&](int st) {
-                if (iss_sub == NB) {
-                    int32_t u = 0;
-                    if (lane == 0) u = atomicAdd(next_unit, 1);
-                    iss_unit = __shfl_sync(0xffffffffu, u, 0);
-                    iss_sub = 0;
-                }
-                const int32_t bi = iss_unit < nunits ? iss_unit * NB + iss_sub : -1;
-                ++iss_sub;
+                int32_t u = 0;
+                if (lane == 0) u = atomicAdd(next_unit, 1);
+                u = __shfl_sync(0xffffffffu, u, 0);
+                const int32_t bi = u < nunits ? u : -1;
                 const uint32_t bar = bar0 + 8u * st;
-                uint32_t part = 0u, bytes = 0u;
-                int32_t phys = -1;
-                if (bi >= 0 && lane < PPB) {
-                    const int32_t pc = pc_of(bi) + lane, lp0 = lp_of(bi);
+                constexpr int kLanes = kPageCopies ? UPP : kUnitRows;
+                int32_t nv = 0, phys = -1, t = 0, lp = 0;
+                if (bi >= 0 && lane < kLanes) {
+                    t = kPageCopies ? lane : lane / LPG;
+                    lp = kPageCopies ? 0 : lane % LPG;
+                    const int32_t pc = bi * UPP + t;
                     if (pc < nc) {
-                        const int32_t rem = Lb - (pg0 + pc) * p.P - lp0 * 16;
-                        const int32_t nv = min(max((rem + 15) >> 4, 0), LPB);
+                        const int32_t rem = Lb - (pg0 + pc) * p.P - lp * 16;
+                        nv = min(max((rem + 15) >> 4, 0), kPageCopies ? LPG : 1);
                         phys = bt_s[pc];
                         if (nv > 0 && (phys < 0 || phys >= p.num_pages)) {
-                            if (lp0 == 0)
+                            if (lp == 0)
                                 set_err(p.dev_err, phys < 0 ? DATTN_DEVERR_UNMAPPED_PAGE
                                                             : DATTN_DEVERR_PAGE_OOB);
-                        } else if (nv > 0) {
-                            part = ((1u << nv) - 1u) << (lane * LPB);
-                            bytes = (uint32_t)nv * kRowBytes;
+                            nv = 0;
                         }
                     }
                 }
+                // tile rows copied: with page copies rows t + UPP lp for lp < nv, else row lane
+                uint32_t part = 0u;
+                if (kPageCopies) {
+                    for (int l = 0; l < nv; ++l) part |= 1u << (t + UPP * l);
+                } else if (nv > 0) {
+                    part = 1u << lane;
+                }
                 const uint32_t mask = __reduce_or_sync(0xffffffffu, part);
+                const uint32_t bytes = (uint32_t)nv * kRowBytes;
                 if (bytes) mbar_expect_tx(bar, bytes);
                 __syncwarp();
                 if (lane == 0) {
                     smask[st] = mask;
-                    sbatch[st] = bi;
+                    sunit[st] = bi;
                     mbar_arrive(bar);
                 }
                 if (bytes) {
                     const uint16_t* src =
-                        p.stats + (((int64_t)phys * p.Hkv + h) * LPG + lp_of(bi)) * (2 * D);
-                    bulk_copy(stage0 + (uint32_t)st * kStageBytes + (uint32_t)(lane * LPB) * kRowBytes,
+                        p.stats + (((int64_t)phys * p.Hkv + h) * LPG + lp) * (2 * D);
+                    bulk_copy(stage0 + (uint32_t)st * kStageBytes + (uint32_t)t * kPageStride +
+                                  (uint32_t)lp * kRowStride,
                               src, bytes, bar, pol);
                 }
             };
             for (int k = 0, t = st; k < S; ++k, t = (t + 1 == S) ? 0 : t + 1) issue(t);
-            int32_t pending = S;  // batches issued and not yet waited for
-            float pmax = kNInf;  // running physical-page max when a page spans batches
-            while (true) {
-                // warp-uniform, bounded wait for the stage's copies
-                const bool ok = __all_sync(0xffffffffu,
-                                           mbar_wait(bar0 + 8u * st, par, abort_flag, p.dev_err));
-                if (!ok) break;
-                const int cst = st;
-                advance();
-                --pending;
-                const int32_t bi = sbatch[cst];
-                if (bi < 0) break;  // the units are exhausted; later stages are empty too
-                const uint32_t mask = smask[cst];
-                const uint32_t sbase = stage0 + (uint32_t)cst * kStageBytes + (uint32_t)lane_off * 2u;
-                // Partials of row slots i and i + R/2 are made together so that the first
-                // butterfly level (offset 16, which pairs exactly those two slots) can run at
-                // once and only 16 values stay live. Transposed butterfly: at offset o every
-                // lane keeps x[t] and adds the partner's x[t + n], which thanks to the
-                // permutation holds the same (page, head) partial.
-                float x[16];
-#pragma unroll
-                for (int ip = 0; ip < R / 2; ++ip) {
-                    float y[2][HG];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int i = ip + u * (R / 2);
-                        Vec v;
-                        lds_chunk(v, sbase + (uint32_t)(i ^ ri) * kRowBytes);
-                        uint64_t kp[NPR];
-                        unpack_bf16x8(v, kp);
-#pragma unroll
-                        for (int j = 0; j < HG; ++j) {
-                            // {even, odd} chains; the first term is an exact product (two
-                            // bf16 values), the same as a fused multiply-add onto +0 except
-                            // for the sign of an exact zero, which keys do not see
-                            uint64_t acc = mul_f32x2(qv[j][0], kp[0]);
-#pragma unroll
-                            for (int m = 1; m < NPR; ++m) fma_f32x2(acc, qv[j][m], kp[m]);
-                            float ev, od;
-                            unpack_f32x2(acc, ev, od);
-                            y[u][j] = ev + od;
-                        }
-                    }
-#pragma unroll
-                    for (int j = 0; j < HG; ++j)
-                        x[ip * HG + j] = y[0][j] + __shfl_xor_sync(0xffffffffu, y[1][j], 16);
-                }
-                // every lane has read the stage: refill it with the warp's next batch
-                __syncwarp();
-                fence_proxy_async_smem();
-                issue(cst);
-                ++pending;
-#pragma unroll
-                for (int lv = 1; lv < 5; ++lv) {
-                    const int o = 16 >> lv, n = 16 >> lv;
-#pragma unroll
-                    for (int t = 0; t < n; ++t)
-                        x[t] = x[t] + __shfl_xor_sync(0xffffffffu, x[t + n], o);
-                }
-                // lane holds the score of logical page ri, head hj
-                float sc = (hj < p.g && ((mask >> ri) & 1u)) ? x[0] : kNInf;
-#pragma unroll
-                for (int o = 1; o < HG; o <<= 1)
-                    sc = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, o));
-#pragma unroll
-                for (int o = HG; o < HG * LPB; o <<= 1)
-                    sc = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, o));
-                // the lanes that own a physical page's score, and that score
-                bool own;
-                int32_t own_pc;
-                if constexpr (NB == 1) {
-                    own = lane % (HG * LPB) == 0;
-                    own_pc = pc_of(bi) + lane / (HG * LPB);
-                } else {
-                    pmax = fmaxf(pmax, sc);
-                    own = lane == 0 && bi % NB == NB - 1;
-                    own_pc = pc_of(bi);
-                    sc = pmax;
-                    if (bi % NB == NB - 1) pmax = kNInf;
-                }
-                // Keys are built only when some page reaches the K-th score so far (the
-                // larger of the warp's and the CTA's); ties are settled by the full key,
-                // which includes the page.
+            int32_t pending = S;  // units issued and not yet waited for
+            // Offers the score sc of physical page pc (block-relative) held by this lane when
+            // own: keys are built only when some page reaches the K-th score so far (the
+            // larger of the warp's and the CTA's); ties are settled by the full key.
+            auto offer = [&](bool own, int32_t pc, float sc) {
                 const uint64_t th = max(thresh, *cta_thresh);
                 const float th_sc = th == thresh ? thr_sc : key_score(th);
                 const bool cand = own && sc != kNInf && sc >= th_sc;
                 if (__any_sync(0xffffffffu, cand)) {
-                    const uint64_t key = cand ? make_key(sc, pg0 + own_pc) : 0ull;
+                    const uint64_t key = cand ? make_key(sc, pg0 + pc) : 0ull;
                     const bool take = key > th;
                     const uint32_t bal = __ballot_sync(0xffffffffu, take);
                     if (take) wbuf[Kp + cnt_c + __popc(bal & ((1u << lane) - 1u))] = key;
@@ -653,8 +543,79 @@ page_select_kernel(const __grid_constant__ SelParams p) {
                         if (lane == 0 && thresh) atomicMax(cta_thresh_u, thresh);
                     }
                 }
+            };
+            while (true) {
+                // warp-uniform, bounded wait for the stage's copies
+                const bool ok = __all_sync(0xffffffffu,
+                                           mbar_wait(bar0 + 8u * st, par, abort_flag, p.dev_err));
+                if (!ok) break;
+                const int cst = st;
+                advance();
+                --pending;
+                const int32_t bi = sunit[cst];
+                if (bi < 0) break;  // the units are exhausted; later stages are empty too
+                const uint32_t mask = smask[cst];
+                // scores of the unit's 16 logical pages (rows) for the 8 query-head columns:
+                // one zero-accumulator mma per 16-channel k-step, summed in fp32 in k order
+                const uint32_t sbase = stage0 + (uint32_t)cst * kStageBytes + lrow_off;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(sbase + (uint32_t)ks * 32u, a0, a1, a2, a3);
+                    float t[4];
+                    mma_bf16_zero_acc(t, a0, a1, a2, a3, bq[ks][0], bq[ks][1]);
+                    acc[0] += t[0];
+                    acc[1] += t[1];
+                    acc[2] += t[2];
+                    acc[3] += t[3];
+                }
+                // every lane has read the stage: refill it with the warp's next unit
+                __syncwarp();
+                fence_proxy_async_smem();
+                issue(cst);
+                ++pending;
+                // lane: tile rows g8 and g8 + 8, heads 2 tig and 2 tig + 1; max over the g
+                // heads, then over the logical pages of each physical page
+                const bool h0 = 2 * tig < p.g, h1 = 2 * tig + 1 < p.g;
+                float vlo = ((mask >> g8) & 1u) ? fmaxf(h0 ? acc[0] : kNInf, h1 ? acc[1] : kNInf)
+                                                : kNInf;
+                float vhi = ((mask >> (g8 + 8)) & 1u)
+                                ? fmaxf(h0 ? acc[2] : kNInf, h1 ? acc[3] : kNInf)
+                                : kNInf;
+#pragma unroll
+                for (int o = 1; o < 4; o <<= 1) {
+                    vlo = fmaxf(vlo, __shfl_xor_sync(0xffffffffu, vlo, o));
+                    vhi = fmaxf(vhi, __shfl_xor_sync(0xffffffffu, vhi, o));
+                }
+                if constexpr (LPG == 1) {
+                    // rows g8 and g8 + 8 are physical pages g8 and g8 + 8
+                    offer(tig == 0, bi * UPP + g8, vlo);
+                    offer(tig == 0, bi * UPP + g8 + 8, vhi);
+                } else if constexpr (kPageCopies) {
+                    // rows g8 and g8 + 8 are logical pages of physical page g8 % UPP; the
+                    // lanes g8 + UPP m hold its other logical pages
+                    float v = fmaxf(vlo, vhi);
+#pragma unroll
+                    for (int o = 4 * UPP; o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+                    offer(tig == 0 && g8 < UPP, bi * UPP + g8, v);
+                } else {
+                    // rows g8 and g8 + 8 are logical pages of physical pages g8 / LPG and
+                    // (g8 + 8) / LPG
+#pragma unroll
+                    for (int o = 4; o < 4 * 8; o <<= 1) {
+                        vlo = fmaxf(vlo, __shfl_xor_sync(0xffffffffu, vlo, o));
+                        vhi = fmaxf(vhi, __shfl_xor_sync(0xffffffffu, vhi, o));
+                    }
+                    if constexpr (LPG == 16) {
+                        offer(lane == 0, bi * UPP, fmaxf(vlo, vhi));
+                    } else {
+                        offer(lane == 0, bi * UPP, vlo);
+                        offer(lane == 0, bi * UPP + 1, vhi);
+                    }
+                }
             }
-            // Step over the batches issued and not waited for. After a normal end they are
+            // Step over the units issued and not waited for. After a normal end they are
             // empty stages (no copies, their phases complete at once); after an abort, wait
             // (bounded) for the copies still in flight.
             for (; pending > 0; --pending) {
@@ -689,7 +650,7 @@ page_select_kernel(const __grid_constant__ SelParams p) {
             }
             csync();
             if (*last_flag) {
-                // warp w folds pieces w, w + 8, ... into its running list, then the warps'
+                // warp w folds pieces w, w + NW, ... into its running list, then the warps'
                 // lists are merged
                 for (int i = lane; i < Kp; i += 32) wbuf[i] = 0ull;
                 uint64_t* scratch = wbuf + Kp;
@@ -710,27 +671,27 @@ page_select_kernel(const __grid_constant__ SelParams p) {
     }
 }
 
-template <int D, int HG, int LPG>
+template <int D, int LPG>
 int sel_prepare(uint32_t smem) {
     static int max_set = 0;
     if ((int)smem > max_set) {
-        if (cudaFuncSetAttribute(page_select_kernel<D, HG, LPG>,
+        if (cudaFuncSetAttribute(page_select_kernel<D, LPG>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return -1;
         max_set = (int)smem;
     }
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, page_select_kernel<D, HG, LPG>,
-                                                      sel_warps(HG) * 32, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, page_select_kernel<D, LPG>,
+                                                      kSelWarps * 32, smem) != cudaSuccess)
         return 1;
     return n < 1 ? 1 : n;
 }
 
-template <int D, int HG, int LPG>
+template <int D, int LPG>
 cudaError_t sel_go(int32_t G_req, int64_t units_bound, uint32_t smem, cudaStream_t stream,
                    SelParams& p, void* ws, size_t ws_bytes, bool& ws_ok) {
-    const int occ = sel_prepare<D, HG, LPG>(smem);
+    const int occ = sel_prepare<D, LPG>(smem);
     if (occ < 0) return cudaErrorInvalidValue;
     const int32_t G = choose_splits(units_bound * 4, G_req, occ);
     const size_t counters = ((size_t)p.nseg * 4 + 255) & ~(size_t)255;
@@ -739,19 +700,18 @@ cudaError_t sel_go(int32_t G_req, int64_t units_bound, uint32_t smem, cudaStream
     if (!ws_ok) return cudaSuccess;
     p.counters = static_cast<int32_t*>(ws);
     p.slots = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + counters);
-    return launch_pdl(page_select_kernel<D, HG, LPG>, dim3(G), dim3(sel_warps(HG) * 32), smem, stream,
-                      p);
+    return launch_pdl(page_select_kernel<D, LPG>, dim3(G), dim3(kSelWarps * 32), smem, stream, p);
 }
 
-template <int D, int HG>
+template <int D>
 cudaError_t sel_go_lpg(int lpg, int32_t G_req, int64_t units_bound, uint32_t smem,
                        cudaStream_t stream, SelParams& p, void* ws, size_t ws_bytes, bool& ok) {
     switch (lpg) {
-        case 1: return sel_go<D, HG, 1>(G_req, units_bound, smem, stream, p, ws, ws_bytes, ok);
-        case 2: return sel_go<D, HG, 2>(G_req, units_bound, smem, stream, p, ws, ws_bytes, ok);
-        case 4: return sel_go<D, HG, 4>(G_req, units_bound, smem, stream, p, ws, ws_bytes, ok);
-        case 8: return sel_go<D, HG, 8>(G_req, units_bound, smem, stream, p, ws, ws_bytes, ok);
-        default: return sel_go<D, HG, 16>(G_req, units_bound, smem, stream, p, ws, ws_bytes, ok);
+        case 1: return sel_go<D, 1>(G_req, units_bound, smem, stream, p, ws, ws_bytes, ok);
+        case 2: return sel_go<D, 2>(G_req, units_bound, smem, stream, p, ws, ws_bytes, ok);
+        case 4: return sel_go<D, 4>(G_req, units_bound, smem, stream, p, ws, ws_bytes, ok);
+        case 8: return sel_go<D, 8>(G_req, units_bound, smem, stream, p, ws, ws_bytes, ok);
+        default: return sel_go<D, 16>(G_req, units_bound, smem, stream, p, ws, ws_bytes, ok);
     }
 }
 
@@ -790,29 +750,22 @@ dattn_status_t launch_page_select(const dattn_kv_layout& Lay, const uint16_t* st
     const int D = Lay.head_dim;
     const int lpg = p.P / 16;
     if (lpg & (lpg - 1)) return DATTN_ERR_UNSUPPORTED;  // P / 16 must be a power of two
-    const bool wide = p.g > 4;  // 8 query heads per KV head instead of 4
-    // one batch is 32 / (4 or 8) logical pages of 4d bytes; up to three batches in flight
-    // per warp, as many as the shared memory of one CTA per SM holds
-    const uint32_t stage_bytes = (wide ? 4u : 8u) * 4u * (uint32_t)D;
-    const int nw = sel_warps(wide ? 8 : 4);
+    // one unit is 16 padded logical-page rows; up to three units in flight per warp, as
+    // many as the shared memory of one CTA per SM holds
+    const uint32_t stage_bytes = sel_stage_bytes(D, lpg);
     SelSmem L{};
     for (p.stages = 3; p.stages >= 1; --p.stages) {
-        L = sel_smem_layout(B, p.Hkv, top_k, nw, stage_bytes, p.stages);
+        L = sel_smem_layout(B, p.Hkv, top_k, kSelWarps, stage_bytes, p.stages);
         if (L.total <= 227u * 1024u) break;
     }
     if (p.stages < 1) return DATTN_ERR_UNSUPPORTED;
     bool ws_ok = true;
     cudaError_t e;
     if (D == 64)
-        e = wide ? sel_go_lpg<64, 8>(lpg, num_splits, units_bound, L.total, stream, p, ws,
-                                     ws_bytes, ws_ok)
-                 : sel_go_lpg<64, 4>(lpg, num_splits, units_bound, L.total, stream, p, ws,
-                                     ws_bytes, ws_ok);
+        e = sel_go_lpg<64>(lpg, num_splits, units_bound, L.total, stream, p, ws, ws_bytes, ws_ok);
     else
-        e = wide ? sel_go_lpg<128, 8>(lpg, num_splits, units_bound, L.total, stream, p, ws,
-                                      ws_bytes, ws_ok)
-                 : sel_go_lpg<128, 4>(lpg, num_splits, units_bound, L.total, stream, p, ws,
-                                      ws_bytes, ws_ok);
+        e = sel_go_lpg<128>(lpg, num_splits, units_bound, L.total, stream, p, ws, ws_bytes,
+                            ws_ok);
     if (!ws_ok) return DATTN_ERR_WORKSPACE;
     return e == cudaSuccess ? DATTN_OK : DATTN_ERR_CUDA;
 }
