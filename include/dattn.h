@@ -237,6 +237,23 @@ dattn_status_t dattn_merge(int32_t B, int32_t C, int32_t Hq, int32_t head_dim,
                            int32_t *dev_err, void *stream);
 
 /*
+ * The aggregation of partials gathered from R ranks: the cross-GPU form of DistAttention
+ * [IL, 结果聚合与通信开销降低: the instances send their partial results back and they are
+ * aggregated; LS §4.2: in multi-master decoding every instance computes local attention
+ * over its KV and the results are merged]. Rank r ran dattn_partial over its share of each
+ * request's KV pages, one chunk per request, and an all-gather stacked the ranks' partials:
+ *   m, e (device) fp32 [R][B][Hq];  MA (device) fp32 [R][B][Hq][d]
+ * For request b and query head h the R partials [r][b][h] are merged exactly as dattn_merge
+ * merges one request's chunks; a rank that holds none of the request's pages contributes an
+ * empty partial (m = -inf), which adds nothing. R = 0 gives the empty result.
+ *   out (device, nullable) fp32 [B][Hq][d];  m_g, e_g, MA_g (device, nullable) as dattn_merge
+ */
+dattn_status_t dattn_merge_gathered(int32_t B, int32_t R, int32_t Hq, int32_t head_dim,
+                                    const float *m, const float *e, const float *MA, float *out,
+                                    float *m_g, float *e_g, float *MA_g, int32_t *dev_err,
+                                    void *stream);
+
+/*
  * Fused single-launch decode: split-KV partials plus merge, dense or block-sparse.
  * Dense (sparse == NULL): every query head of request b attends tokens 0..L_b-1.
  * Block-sparse [LV §2.2.2, §3.1.1]: per KV head kind,

@@ -27,7 +27,7 @@ import torch
 __all__ = [
     "KVLayout", "SparseConfig", "DattnError", "load_library", "library_path",
     "dattn_kv_append", "dattn_partial", "dattn_merge", "dattn_decode", "dattn_page_select",
-    "dattn_append_decode",
+    "dattn_append_decode", "dattn_merge_gathered",
     "dattn_decode_noalloc", "dattn_decode_multi", "dattn_prefill", "PrefillSparseConfig",
     "dattn_workspace_size", "dattn_workspace_init", "dattn_auto_splits", "dattn_split_range",
     "dattn_split_owner", "dattn_status_string", "dattn_version", "Workspace",
@@ -79,6 +79,7 @@ _SIGS = {
     "dattn_partial": (_I, [ctypes.POINTER(_Layout), _P, _P, _P, _I, _I, _F, _P, _I, _P, _P, _P,
                            _P, _P, _P, _P, _SZ, _I, _P, _P]),
     "dattn_merge": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "dattn_merge_gathered": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dattn_decode": (_I, [ctypes.POINTER(_Layout), _P, _P, _P, _I, _I, _F, _P,
                           ctypes.POINTER(_Sparse), _I, _P, _SZ, _P, _P, _P, _P, _P]),
     "dattn_page_select": (_I, [ctypes.POINTER(_Layout), _P, _P, _I, _I, _P, _P, _I, _P, _P, _P,
@@ -364,6 +365,24 @@ def dattn_merge(chunk_indptr, m, e, MA, out=None, m_g=None, e_g=None, MA_g=None,
     _check(load_library().dattn_merge(
         B, C, Hq, d, _ptr(chunk_indptr), _ptr(m), _ptr(e), _ptr(MA), _ptr(out), _ptr(m_g),
         _ptr(e_g), _ptr(MA_g), _ptr(dev_err), _stream(stream)), "dattn_merge")
+
+
+def dattn_merge_gathered(m, e, MA, out=None, m_g=None, e_g=None, MA_g=None, dev_err=None,
+                         stream=None):
+    """Aggregate partials gathered from R ranks: m, e fp32 [R][B][Hq], MA fp32 [R][B][Hq][d]
+    (rank r's dattn_partial over its pages, one chunk per request) -> out fp32 [B][Hq][d]."""
+    for t, n in ((m, "m"), (e, "e"), (MA, "MA"), (out, "out"), (m_g, "m_g"), (e_g, "e_g"),
+                 (MA_g, "MA_g")):
+        _f32(t, n)
+    if MA.dim() != 4:
+        raise ValueError("MA must be fp32 [R][B][Hq][d]")
+    R, B, Hq, d = MA.shape
+    _size(m, R * B * Hq, "m"); _size(e, R * B * Hq, "e")
+    _size(out, B * Hq * d, "out"); _size(m_g, B * Hq, "m_g"); _size(e_g, B * Hq, "e_g")
+    _size(MA_g, B * Hq * d, "MA_g")
+    _check(load_library().dattn_merge_gathered(
+        B, R, Hq, d, _ptr(m), _ptr(e), _ptr(MA), _ptr(out), _ptr(m_g), _ptr(e_g), _ptr(MA_g),
+        _ptr(dev_err), _stream(stream)), "dattn_merge_gathered")
 
 
 def _decode_sizes(layout, B, T, Hq, k_pool, v_pool, q, seq_lens, out, m_g, e_g, sparse):

@@ -13,8 +13,8 @@
 namespace dattn {
 
 dattn_status_t launch_merge(int32_t B, int32_t C, int32_t Hq, int32_t D, const int32_t* indptr,
-                            const float* m, const float* e, const float* MA, float* out,
-                            float* m_g, float* e_g, float* MA_g, int32_t* dev_err,
+                            int32_t R, const float* m, const float* e, const float* MA,
+                            float* out, float* m_g, float* e_g, float* MA_g, int32_t* dev_err,
                             cudaStream_t stream);
 dattn_status_t launch_kv_append(const dattn_kv_layout& L, void* k_pool, void* v_pool,
                                 uint16_t* stats, const uint16_t* k_new, const uint16_t* v_new,
@@ -284,8 +284,21 @@ dattn_status_t dattn_merge(int32_t B, int32_t C, int32_t Hq, int32_t head_dim,
     if (B > 65535) return DATTN_ERR_UNSUPPORTED;
     if (!chunk_indptr) return DATTN_ERR_INVALID_ARG;
     if (C > 0 && (!m || !e || !MA)) return DATTN_ERR_INVALID_ARG;
-    return launch_merge(B, C, Hq, head_dim, chunk_indptr, m, e, MA, out, m_g, e_g, MA_g, dev_err,
-                        static_cast<cudaStream_t>(stream));
+    return launch_merge(B, C, Hq, head_dim, chunk_indptr, 0, m, e, MA, out, m_g, e_g, MA_g,
+                        dev_err, static_cast<cudaStream_t>(stream));
+}
+
+dattn_status_t dattn_merge_gathered(int32_t B, int32_t R, int32_t Hq, int32_t head_dim,
+                                    const float* m, const float* e, const float* MA, float* out,
+                                    float* m_g, float* e_g, float* MA_g, int32_t* dev_err,
+                                    void* stream) {
+    if (B < 0 || R < 0 || Hq < 0) return DATTN_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return DATTN_ERR_UNSUPPORTED;
+    if (B > kMaxItems || (int64_t)R * B > (1ll << 30)) return DATTN_ERR_UNSUPPORTED;
+    if (B == 0 || Hq == 0) return DATTN_OK;
+    if (R > 0 && (!m || !e || !MA)) return DATTN_ERR_INVALID_ARG;
+    return launch_merge(B, R * B, Hq, head_dim, nullptr, R, m, e, MA, out, m_g, e_g, MA_g,
+                        dev_err, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"
