@@ -11,12 +11,14 @@ roofline are reported beside it. L2 is flushed before every timed step whose K/V
 four times the L2; larger steps evict it themselves and run back to back.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl dattn|reference]
-                  [--kv-format bf16|fp8|int4] [--queries T]
+                  [--kv-format bf16|fp8|int4|mixed] [--queries T]
 
 --kv-format fp8 runs the same workload over the 8-bit pool (FP8 E4M3 codes with one fp32
 scale per (token, KV head) row): a K or V row then moves d + 4 bytes instead of 2 d.
 --kv-format int4 runs it over the 4-bit pool (symmetric 4-bit codes, two per byte, with the
 same scales): d / 2 + 4 bytes per row.
+--kv-format mixed (block-sparse workloads) keeps every KV head in the format of its kind in
+one pool: streaming heads 4-bit, retrieval and dense heads 8-bit, decoded in one launch.
 
 --queries T (dense workloads) makes each step a chunked one: T new tokens per request are
 appended, then dattn_decode_multi attends all T query tokens, causal over the new tokens.
@@ -74,7 +76,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="mha-1m", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--impl", default="dattn", choices=["dattn", "reference"])
-    ap.add_argument("--kv-format", default="bf16", choices=["bf16", "fp8", "int4"],
+    ap.add_argument("--kv-format", default="bf16", choices=["bf16", "fp8", "int4", "mixed"],
                     help="element format of the paged KV pool")
     ap.add_argument("--prefill-dense", action="store_true",
                     help="prefill-32k: every head dense (causal) instead of the LServe mix")
@@ -140,8 +142,11 @@ KV_FORMAT_NOTE = {
     "bf16": "bf16",
     "fp8": "fp8_e4m3 codes + one fp32 scale per (token, KV head) row",
     "int4": "symmetric 4-bit codes (two per byte) + one fp32 scale per (token, KV head) row",
+    "mixed": "per KV head kind: fp8_e4m3 codes (retrieval, dense) or symmetric 4-bit codes "
+             "(streaming), one fp32 scale per (token, KV head) row, one pool",
 }
-QUANT_NOTE = {"fp8": " over the dequantized 8-bit rows", "int4": " over the dequantized 4-bit rows"}
+QUANT_NOTE = {"fp8": " over the dequantized 8-bit rows", "int4": " over the dequantized 4-bit rows",
+              "mixed": " over the dequantized rows (8-bit retrieval, 4-bit streaming heads)"}
 
 
 def row_bytes(d: int, fmt: str) -> int:
@@ -150,16 +155,26 @@ def row_bytes(d: int, fmt: str) -> int:
     return {"bf16": 2 * d, "fp8": d + 4, "int4": d // 2 + 4}[fmt]
 
 
+def head_format(fmt: str, kind: int) -> str:
+    """The format of a KV head of kind `kind` in a pool of format fmt: the mixed pool keeps
+    streaming heads at 4 bits and the other heads at 8 bits."""
+    if fmt != "mixed":
+        return fmt
+    return "int4" if kind == 2 else "fp8"
+
+
 def step_bytes(case, lens_after, sparse_sel_step: bool, fmt: str = "bf16", T: int = 1) -> dict:
     """Algorithmic bytes of one layer-step, given the lengths after the append (T query
     tokens per request: T appended tokens, T queries and outputs, the K/V read once)."""
     B, Hq, Hkv, d, P = case.B, case.Hq, case.Hkv, case.d, case.P
-    rb = row_bytes(d, fmt)
     q_bytes = T * B * Hq * d * 2
     out_bytes = T * (B * Hq * d * 4 + 2 * B * Hq * 4)
-    new_kv = T * B * Hkv * (d * 2 + rb) * 2  # read k_new/v_new (bf16), write into the pool
     bt = sum(-(-L // P) for L in lens_after) * 4
     if case.head_kind is None:
+        if fmt == "mixed":
+            raise ValueError("the mixed pool takes its formats from the head kinds")
+        rb = row_bytes(d, fmt)
+        new_kv = T * B * Hkv * (d * 2 + rb) * 2  # read k_new/v_new (bf16), write the pool
         kv = sum(lens_after) * Hkv * rb * 2
         decode = kv + q_bytes + out_bytes + bt + B * 4
         return {"decode": decode, "append": new_kv, "select": 0,
@@ -168,13 +183,16 @@ def step_bytes(case, lens_after, sparse_sel_step: bool, fmt: str = "bf16", T: in
     nret = sum(1 for k in kinds if k == 1)
     nstr = sum(1 for k in kinds if k == 2)
     nden = sum(1 for k in kinds if k == 0)
+    rb_of = [row_bytes(d, head_format(fmt, k)) for k in (0, 1, 2)]  # by head kind
+    # read k_new/v_new (bf16), write into the pool in each head's format
+    new_kv = T * B * sum(d * 2 + rb_of[k] for k in kinds) * 2
     kv = 0
     for L in lens_after:
-        kv += nden * L * rb * 2
-        kv += nret * min(case.top_k * P, L) * rb * 2
+        kv += nden * L * rb_of[0] * 2
+        kv += nret * min(case.top_k * P, L) * rb_of[1] * 2
         s_end = min(case.sinks, L)
         l0 = max(case.sinks, L - case.local)
-        kv += nstr * (s_end + max(0, L - l0)) * rb * 2
+        kv += nstr * (s_end + max(0, L - l0)) * rb_of[2] * 2
     sel_rows = B * nret * case.top_k * 4
     # the decode reads the selection rows and their pool pages (dattn_sparse.selected_phys)
     decode = kv + q_bytes + out_bytes + 2 * sel_rows + B * 4
@@ -395,9 +413,16 @@ def run_dattn(args, rank: int, world: int):
     case = make_case(args)
     sparse = case.head_kind is not None
     fmt = args.kv_format
+    if fmt == "mixed" and not sparse:
+        raise SystemExit("--kv-format mixed needs a block-sparse workload (its head kinds)")
+    hfmt = None
+    if fmt == "mixed":
+        hfmt = [dattn.KV_INT4 if head_format(fmt, k) == "int4" else dattn.KV_FP8_E4M3
+                for k in case.head_kind]
     cache = PagedCache(case, dev, with_stats=sparse, chunk_tokens=16384,
                        kv_format={"bf16": dattn.KV_BF16, "fp8": dattn.KV_FP8_E4M3,
-                                  "int4": dattn.KV_INT4}[fmt])
+                                  "int4": dattn.KV_INT4, "mixed": dattn.KV_MIXED}[fmt],
+                       head_format=hfmt)
     B, Hq, d = case.B, case.Hq, case.d
     T = args.queries
     ws = cache.workspace(top_k=case.top_k, num_splits=args.num_splits, queries=T)
@@ -809,7 +834,9 @@ class SparseOracleStep:
         # with a quantized format the attention runs over the dequantized rows (the
         # selection still reads the bf16 keys, as the statistics do)
         self.fmt = fmt
-        self.att = {h: dequantized(kv[h], fmt) for h in kv} if fmt != "bf16" else kv
+        self.hfmt = {h: head_format(fmt, case.head_kind[h]) for h in kv}
+        self.att = ({h: dequantized(kv[h], self.hfmt[h]) for h in kv} if fmt != "bf16"
+                    else kv)
         self.used = min(nthreads, len(ret) + len(strm))
         self.ex = ThreadPoolExecutor(max_workers=self.used)
         self.sels = {}
@@ -843,7 +870,7 @@ class SparseOracleStep:
                 rows = np.arange(K.shape[0], dtype=np.int64)
             for j in range(g):
                 attend(self.q[b, h * g + j], K, V, c.scale, rows=rows)
-            return rows.shape[0] * row_bytes(c.d, self.fmt) * 2
+            return rows.shape[0] * row_bytes(c.d, self.hfmt[h]) * 2
         t0 = time.perf_counter()
         nbytes = sum(self.ex.map(one, self.ret + self.strm))
         return time.perf_counter() - t0, nbytes
@@ -873,7 +900,8 @@ def cpu_baseline_sparse(case, device, fmt: str = "bf16"):
             "sample": f"request 0, retrieval KV heads {ret} (selection from the keys, then "
                       f"attention over the selected pages) and streaming KV heads {strm} "
                       f"(sinks and local window), {case.g} query heads each; {windows} reuse "
-                      f"window(s) of 1 selection + {case.reuse} steps, {secs:.1f} s wall"}
+                      f"window(s) of 1 selection + {case.reuse} steps"
+                      f"{QUANT_NOTE.get(fmt, '')}, {secs:.1f} s wall"}
 
 
 def cpu_baseline(case, device, fmt: str = "bf16", T: int = 1):
@@ -1316,10 +1344,14 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {"bf16": "bf16",
                   "fp8": "fp8_e4m3 KV (fp16 tensor-core products, fp32 accumulate)",
-                  "int4": "int4 KV (fp16 tensor-core products, fp32 accumulate)"}[args.kv_format],
+                  "int4": "int4 KV (fp16 tensor-core products, fp32 accumulate)",
+                  "mixed": "fp8_e4m3 retrieval/dense heads + int4 streaming heads KV (fp16 "
+                           "tensor-core products, fp32 accumulate)"}[args.kv_format],
         "data": "synthetic (seeded N(0,1) bf16 K/V/Q" +
                 {"bf16": ")", "fp8": "; K/V quantized to 8 bits by the append)",
-                 "int4": "; K/V quantized to 4 bits by the append)"}[args.kv_format],
+                 "int4": "; K/V quantized to 4 bits by the append)",
+                 "mixed": "; K/V quantized by the append: 8 bits for retrieval and dense "
+                          "heads, 4 bits for streaming heads)"}[args.kv_format],
         "us_per_layer_step": round(ms_step * 1e3, 2),
         "frac_of_8tbs": round(value / ROOFLINE_8TBS, 4),
         "config": config_obj(case, args),

@@ -70,6 +70,15 @@
  *    of the row holds code_{2j} + 8 in its low nibble and code_{2j+1} + 8 in its high
  *    nibble. A row with scale 0 has code 0. The row's values are code_i * scale, and the
  *    attention runs over exactly these values.
+ *  - The mixed format (kv_format = DATTN_KV_MIXED) [LV §3.2.1: one cache with 4-bit
+ *    streaming heads and 2-8-bit retrieval heads]: every KV head h has its own format,
+ *    head_format[h] = DATTN_KV_FP8_E4M3 or DATTN_KV_INT4, and its rows are stored exactly as
+ *    in that format (codes and kv_scale as above). Of the Hkv heads, H8 are 8-bit and H4 are
+ *    4-bit; a head's index within its own format is the number of earlier heads of that
+ *    format. The pool is the 8-bit region [num_pages][H8][P][d] bytes followed by the 4-bit
+ *    region [num_pages][H4][P][d/2] bytes (this replaces the [num_pages][Hkv][P][d] layout
+ *    above); kv_scale keeps the [num_pages][Hkv][P/16][2][16] layout over all heads. One
+ *    decode launch reads both regions.
  *  - Statistics layout: stats is [num_pages][Hkv][P/16][2][d]. Entry [..][lp][0][:] is
  *    k_max and [..][lp][1][:] is k_min of logical page lp, the 16 tokens
  *    lp*16..lp*16+15 of that physical page.
@@ -125,6 +134,7 @@ typedef enum {
 #define DATTN_KV_BF16 0      /* bf16 values */
 #define DATTN_KV_FP8_E4M3 1  /* FP8 E4M3 codes with one fp32 scale per (token, KV head) row */
 #define DATTN_KV_INT4 2      /* symmetric 4-bit codes, two per byte, one fp32 scale per row */
+#define DATTN_KV_MIXED 3     /* per KV head: FP8 E4M3 or 4-bit rows (layout.head_format) */
 
 /* Shape of the paged KV pool and the block table. A zero-initialised tail (kv_format 0,
  * NULL scales) is the bf16 pool. */
@@ -135,10 +145,14 @@ typedef struct dattn_kv_layout {
     int32_t page_size;          /* P: tokens per physical page, a multiple of 16 */
     const int32_t *block_table; /* (device) [B][max_pages_per_req]; -1 = unmapped */
     int32_t max_pages_per_req;  /* row width of block_table */
-    int32_t kv_format;          /* DATTN_KV_BF16, DATTN_KV_FP8_E4M3 or DATTN_KV_INT4 */
+    int32_t kv_format;          /* DATTN_KV_BF16, DATTN_KV_FP8_E4M3, DATTN_KV_INT4 or
+                                   DATTN_KV_MIXED */
     float *kv_scale;            /* (device) fp32 [num_pages][Hkv][P/16][2][16], 16-byte aligned:
                                    the row scales of the 8-bit and 4-bit formats (ignored for
                                    bf16), written by dattn_kv_append; see the layout notes */
+    const int8_t *head_format;  /* (host) [Hkv], read during the call, DATTN_KV_MIXED only:
+                                   DATTN_KV_FP8_E4M3 or DATTN_KV_INT4 per KV head; NULL or
+                                   another value is DATTN_ERR_INVALID_ARG */
 } dattn_kv_layout;
 
 /* Block-sparse decode settings [LV §2.2.2, §3.1.1, §3.1.2]. */
@@ -166,7 +180,8 @@ typedef struct dattn_sparse {
  *
  *   k_pool, v_pool (device) the pool in the layout's kv_format; for the 8-bit and 4-bit
  *                formats each row is quantized as described above and its scales go to
- *                layout->kv_scale.
+ *                layout->kv_scale; for the mixed format each KV head's rows are quantized in
+ *                that head's format and go to its region.
  *   k_new, v_new (device) bf16 [B][T][Hkv][d]. Token t of request b is written at
  *                position seq_lens[b] + t.
  *   stats        (device, nullable) bf16 [num_pages][Hkv][P/16][2][d]. When a token

@@ -32,7 +32,7 @@ __all__ = [
     "dattn_workspace_size", "dattn_workspace_init", "dattn_auto_splits", "dattn_split_range",
     "dattn_split_owner", "dattn_status_string", "dattn_version", "Workspace",
     "HEAD_DENSE", "HEAD_RETRIEVAL", "HEAD_STREAMING", "DEVERR", "KV_BF16", "KV_FP8_E4M3",
-    "KV_INT4",
+    "KV_INT4", "KV_MIXED", "mixed_pool_bytes",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -41,7 +41,8 @@ _lib = None
 _lock = threading.Lock()
 
 HEAD_DENSE, HEAD_RETRIEVAL, HEAD_STREAMING = 0, 1, 2
-KV_BF16, KV_FP8_E4M3, KV_INT4 = 0, 1, 2
+KV_BF16, KV_FP8_E4M3, KV_INT4, KV_MIXED = 0, 1, 2, 3
+_QUANT = (KV_FP8_E4M3, KV_INT4, KV_MIXED)
 DEVERR = {"UNMAPPED_PAGE": 0x1, "PAGE_OOB": 0x2, "LEN_OOB": 0x4, "TIMEOUT": 0x8,
           "CHUNK_OOB": 0x10, "SELECT_OOB": 0x20, "SMEM_ALIGN": 0x40}
 
@@ -54,7 +55,8 @@ class _Layout(ctypes.Structure):
     _fields_ = [("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("block_table", ctypes.c_void_p), ("max_pages_per_req", ctypes.c_int32),
-                ("kv_format", ctypes.c_int32), ("kv_scale", ctypes.c_void_p)]
+                ("kv_format", ctypes.c_int32), ("kv_scale", ctypes.c_void_p),
+                ("head_format", ctypes.c_void_p)]
 
 
 class _Sparse(ctypes.Structure):
@@ -174,23 +176,34 @@ def _size(t, n: int, name: str):
     return t
 
 
+def mixed_pool_bytes(num_pages: int, head_format, head_dim: int, page_size: int) -> int:
+    """Bytes of one (K or V) mixed pool: the 8-bit region [num_pages][H8][P][d], then the 4-bit
+    region [num_pages][H4][P][d/2]."""
+    h4 = sum(1 for f in head_format if f == KV_INT4)
+    h8 = len(head_format) - h4
+    return num_pages * page_size * (h8 * head_dim + h4 * (head_dim // 2))
+
+
 def _layout_sizes(layout, B: int, k_pool, v_pool, stats=None):
     """The pools, block table, scales and statistics must cover the layout for B requests."""
     c = layout.c
-    row = c.head_dim // 2 if c.kv_format == KV_INT4 else c.head_dim
     n = c.num_pages * c.num_kv_heads * c.page_size
-    _size(k_pool, n * row, "k_pool")
-    _size(v_pool, n * row, "v_pool")
+    if c.kv_format == KV_MIXED:
+        pool = mixed_pool_bytes(c.num_pages, layout.head_format, c.head_dim, c.page_size)
+    else:
+        pool = n * (c.head_dim // 2 if c.kv_format == KV_INT4 else c.head_dim)
+    _size(k_pool, pool, "k_pool")
+    _size(v_pool, pool, "v_pool")
     _size(layout.block_table, B * c.max_pages_per_req, "block_table")
-    if c.kv_format in (KV_FP8_E4M3, KV_INT4):
+    if c.kv_format in _QUANT:
         _size(layout.kv_scale, 2 * n, "kv_scale")
     _size(stats, n // 16 * 2 * c.head_dim, "stats")
 
 
 def _pool(layout, t, name):
     """A K or V pool must hold the layout's element type: bf16, uint8 E4M3 codes, or uint8
-    bytes of two 4-bit codes."""
-    want = torch.uint8 if layout.kv_format in (KV_FP8_E4M3, KV_INT4) else torch.bfloat16
+    bytes of two 4-bit codes (the mixed pool: both kinds of bytes)."""
+    want = torch.uint8 if layout.kv_format in _QUANT else torch.bfloat16
     if t is not None and t.dtype != want and not (
             want == torch.uint8 and t.dtype == getattr(torch, "float8_e4m3fn", None)):
         raise TypeError(f"{name} must be {want} for this layout")
@@ -204,22 +217,34 @@ class KVLayout:
     and kv_scale (float32 [num_pages][Hkv][P/16][2][16]) holds one scale per row: for the 16
     tokens of each logical page, their K scales, then their V scales. KV_INT4: they hold
     [num_pages][Hkv][P][d/2] bytes of two 4-bit codes each (code + 8, even channel in the low
-    nibble), with kv_scale as for KV_FP8_E4M3.
+    nibble), with kv_scale as for KV_FP8_E4M3. KV_MIXED: head_format[h] (KV_FP8_E4M3 or
+    KV_INT4) gives each KV head's format; the pools are that many bytes
+    (mixed_pool_bytes): the 8-bit heads' region, then the 4-bit heads' region, each head at
+    its index among the heads of its format.
     """
 
     def __init__(self, num_pages: int, num_kv_heads: int, head_dim: int, page_size: int,
                  block_table: torch.Tensor, kv_format: int = KV_BF16,
-                 kv_scale: torch.Tensor | None = None):
+                 kv_scale: torch.Tensor | None = None, head_format=None):
         _i32(block_table, "block_table")
-        if kv_format in (KV_FP8_E4M3, KV_INT4):
+        if kv_format in _QUANT:
             if kv_scale is None:
                 raise ValueError("the quantized formats need kv_scale")
             _f32(kv_scale, "kv_scale")
+        self.head_format = None
+        self._head_format_c = None
+        if kv_format == KV_MIXED:
+            if head_format is None or len(head_format) != num_kv_heads:
+                raise ValueError("the mixed format needs one head_format entry per KV head")
+            self.head_format = [int(f) for f in head_format]
+            self._head_format_c = (ctypes.c_int8 * num_kv_heads)(*self.head_format)
         self.block_table = block_table  # keeps the tensors alive
         self.kv_scale = kv_scale
         self.c = _Layout(num_pages, num_kv_heads, head_dim, page_size,
                          block_table.data_ptr(), block_table.shape[-1], kv_format,
-                         kv_scale.data_ptr() if kv_scale is not None else None)
+                         kv_scale.data_ptr() if kv_scale is not None else None,
+                         ctypes.addressof(self._head_format_c)
+                         if self._head_format_c is not None else None)
 
     @property
     def kv_format(self): return self.c.kv_format

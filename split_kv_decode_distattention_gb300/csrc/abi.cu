@@ -48,11 +48,12 @@ dattn_status_t check_layout(const dattn_kv_layout* L) {
         return DATTN_ERR_UNSUPPORTED;
     if ((int64_t)L->max_pages_per_req * L->page_size >= (1ll << 30)) return DATTN_ERR_UNSUPPORTED;
     if (L->kv_format != DATTN_KV_BF16 && L->kv_format != DATTN_KV_FP8_E4M3 &&
-        L->kv_format != DATTN_KV_INT4)
+        L->kv_format != DATTN_KV_INT4 && L->kv_format != DATTN_KV_MIXED)
         return DATTN_ERR_INVALID_ARG;
     if (L->kv_format != DATTN_KV_BF16 && (!L->kv_scale || !aligned16(L->kv_scale)))
         return DATTN_ERR_INVALID_ARG;
-    return DATTN_OK;
+    KvHeadFormats f;
+    return head_formats(*L, f);
 }
 
 dattn_status_t check_heads(const dattn_kv_layout* L, int32_t B, int32_t Hq) {
@@ -64,6 +65,21 @@ dattn_status_t check_heads(const dattn_kv_layout* L, int32_t B, int32_t Hq) {
 }
 
 }  // namespace
+
+dattn_status_t head_formats(const dattn_kv_layout& L, KvHeadFormats& f) {
+    f = KvHeadFormats{};
+    if (L.kv_format != DATTN_KV_MIXED) return DATTN_OK;
+    if (L.head_format == nullptr) return DATTN_ERR_INVALID_ARG;
+    for (int32_t h = 0; h < L.num_kv_heads; ++h) {
+        const int8_t v = L.head_format[h];
+        if (v != DATTN_KV_FP8_E4M3 && v != DATTN_KV_INT4) return DATTN_ERR_INVALID_ARG;
+        if (v == DATTN_KV_INT4) {
+            f.i4[h >> 5] |= 1u << (h & 31);
+            ++f.h4;
+        }
+    }
+    return DATTN_OK;
+}
 
 int sm_count_current() {
     int dev = 0;
@@ -270,6 +286,7 @@ dattn_status_t dattn_partial(const dattn_kv_layout* layout, const void* k_pool,
     p.dev_err = dev_err;
     p.fmt = layout->kv_format;
     p.kv_scale = layout->kv_scale;
+    head_formats(*layout, p.hf);  // checked with the layout
     return launch_attention(p, k_pool, v_pool, layout->head_dim, num_splits, ws, ws_bytes,
                             static_cast<cudaStream_t>(stream), bound);
 }
@@ -386,6 +403,7 @@ dattn_status_t decode_impl(const dattn_kv_layout* layout, const void* k_pool, co
     p.dev_err = dev_err;
     p.fmt = layout->kv_format;
     p.kv_scale = layout->kv_scale;
+    head_formats(*layout, p.hf);  // checked with the layout
     if (app != nullptr) {
         p.append = 1;
         p.k_new = app->k_new;

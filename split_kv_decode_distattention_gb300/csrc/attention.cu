@@ -308,13 +308,17 @@ struct PieceIter {
 // the causal cut of multi-query decode: row r is visible to query token t iff r <= cut + t.
 // With the fused append, the tile that holds the new token carries its row: the consumer
 // writes the new token's K and V into that row of the stage before using it.
+// With the mixed pool, yc is the tile's row in its format's region (y, over all heads, still
+// addresses the row scales) and kTileI4 marks a 4-bit tile.
 struct TileRef {
     int32_t y;
-    int32_t lohi;  // lo | hi << 8 | skip << 16 | patch << 17 | patch row << 18 |
+    int32_t lohi;  // lo | hi << 8 | skip << 16 | patch << 17 | patch row << 18 | 4-bit << 22 |
                    // (cut + 16) << 24, cut clamped to [-16, 16]
+    int32_t yc;
 };
 constexpr int32_t kTileSkip = 1 << 16;
 constexpr int32_t kTilePatch = 1 << 17;
+constexpr int32_t kTileI4 = 1 << 22;
 __device__ __forceinline__ int32_t tile_lo(int32_t m) { return m & 0xff; }
 __device__ __forceinline__ int32_t tile_hi(int32_t m) { return (m >> 8) & 0xff; }
 __device__ __forceinline__ int32_t tile_cut(int32_t m) { return ((m >> 24) & 63) - 16; }
@@ -325,7 +329,7 @@ __device__ __forceinline__ int32_t tile_patch_row(int32_t m) { return (m >> 18) 
 // slots even when the length is 0).
 __device__ __forceinline__ TileRef resolve_tile(const AttnParams& p, const Smem& sm, int32_t s,
                                                 int32_t local, bool aligned) {
-    TileRef r{0, kTileSkip};
+    TileRef r{0, kTileSkip, 0};
     const int32_t item = s / p.Hkv, h = s - item * p.Hkv;
     int32_t b, L, t0, lo = 0, hi = 16, cut = 16;
     int32_t page = -2;  // -2: look the page up in the block table
@@ -401,6 +405,12 @@ __device__ __forceinline__ TileRef resolve_tile(const AttnParams& p, const Smem&
     }
     r.y = (page * p.Hkv + h) * p.P + (t0 - lp * p.P);
     r.lohi = lo | (hi << 8) | ((cut + 16) << 24);
+    if (p.fmt == DATTN_KV_MIXED) {
+        const bool i4 = head_is_i4(p.hf, h);
+        const int32_t hc = i4 ? p.hf.h4 : p.Hkv - p.hf.h4;
+        r.yc = (page * hc + head_class_index(p.hf, h, i4)) * p.P + (t0 - lp * p.P);
+        if (i4) r.lohi |= kTileI4;
+    }
     if (p.append) {  // the new token (the last one) lies in this tile
         const int32_t pos = sm.item_pos()[b];
         if (pos >= 0 && pos == L - 1 && pos >= t0 + lo && pos < t0 + hi)
@@ -443,7 +453,9 @@ struct Consumer {
     static constexpr int KS = D / 16;  // k-steps of QK^T and m-tiles of PV
     static constexpr bool Q = FMT != DATTN_KV_BF16;  // a quantized pool with row scales
     static constexpr bool I4 = FMT == DATTN_KV_INT4;
+    static constexpr bool MIX = FMT == DATTN_KV_MIXED;  // 8-bit or 4-bit per KV head
     static_assert(!I4 || Q, "the 4-bit pool is a quantized pool");
+    static_assert(!MIX || Q, "the mixed pool is a quantized pool");
 
     const AttnParams& p;
     const Smem& sm;
@@ -454,6 +466,7 @@ struct Consumer {
     float qsc;     // scale * log2(e) (8-bit pool: times 2^-a) for the current piece's query
     int32_t rk;    // 8-bit pool: r = 2^rk bounds the V scales seen in this piece
     float rv, inv;  // 8-bit pool: r and 2^15 / r
+    bool i4 = I4;   // the current piece's KV head is 4-bit (set per piece in a mixed pool)
 
     __device__ Consumer(const AttnParams& p_, const Smem& sm_, int w, int l)
         : p(p_), sm(sm_), warp(w), lane(l) {}
@@ -502,10 +515,11 @@ struct Consumer {
             // 4-bit: k-step ks takes channels c0 + {0..7} of the 32-channel chunk ks / 2,
             // c0 = 32 (ks / 2) + 8tig, in nibble pairs: sub-step ks % 2 = 0 has b0 = c0 + {0, 4}
             // and b1 = c0 + {1, 5}, sub-step 1 has b0 = c0 + {2, 6} and b1 = c0 + {3, 7}.
+            const bool f4 = MIX ? head_is_i4(p.hf, kvh) : I4;
             float mx = 0.f;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                if constexpr (I4) {
+                if (f4) {
                     const uint4 w = ok ? __ldg(reinterpret_cast<const uint4*>(qv + (ks >> 1) * 16 +
                                                                              4 * tig))
                                        : make_uint4(0u, 0u, 0u, 0u);
@@ -967,7 +981,8 @@ struct Consumer {
             for (int mt = 0; mt < KS; ++mt) {
                 // rows g8 and g8 + 8 of m-tile mt are channels dd and dd + 1 (4-bit: m-tile
                 // mt covers channels 32 (mt / 2) + 4 g8 + 2 (mt % 2) + {0, 1}, see tile_i4)
-                const int dd = I4 ? 32 * (mt >> 1) + 4 * g8 + 2 * (mt & 1) : mt * 16 + 2 * g8;
+                const int dd = (MIX ? i4 : I4) ? 32 * (mt >> 1) + 4 * g8 + 2 * (mt & 1)
+                                               : mt * 16 + 2 * g8;
                 if (hA < p.gq)
                     *reinterpret_cast<float2*>(wo + hA * D + dd) =
                         make_float2(o[mt][0] * rs, o[mt][2] * rs);
@@ -1040,7 +1055,11 @@ template <int D, int FMT>
 __global__ void __launch_bounds__(kAttnThreads, attn_min_blocks<D>())
 attention_kernel(const __grid_constant__ AttnParams p,
                  const __grid_constant__ CUtensorMap tmap_k,
-                 const __grid_constant__ CUtensorMap tmap_v) {
+                 const __grid_constant__ CUtensorMap tmap_v,
+                 const __grid_constant__ CUtensorMap tmap_k4,
+                 const __grid_constant__ CUtensorMap tmap_v4) {
+    // tmap_k / tmap_v: the pool (the mixed pool: its 8-bit region); tmap_k4 / tmap_v4: the
+    // mixed pool's 4-bit region (unused otherwise)
     extern __shared__ uint8_t smem_raw[];
     Smem sm;
     {  // align by the shared-window offset: the TMA swizzle pattern is defined on it
@@ -1066,6 +1085,10 @@ attention_kernel(const __grid_constant__ AttnParams p,
     if (warp == kConsumerWarps && lane == 0) {
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_v);
+        if constexpr (FMT == DATTN_KV_MIXED) {
+            prefetch_tmap(&tmap_k4);
+            prefetch_tmap(&tmap_v4);
+        }
     }
     if (p.mode == MODE_SPARSE) {
         for (int h = tid; h < p.Hkv; h += kAttnThreads) {
@@ -1247,6 +1270,8 @@ attention_kernel(const __grid_constant__ AttnParams p,
                 const int32_t src = min(j0 + lane, 31);
                 const int32_t y = __shfl_sync(0xffffffffu, ref.y, src);
                 const int32_t lohi = __shfl_sync(0xffffffffu, ref.lohi, src);
+                int32_t yc = y;
+                if constexpr (FMT == DATTN_KV_MIXED) yc = __shfl_sync(0xffffffffu, ref.yc, src);
                 bool ok = true;
                 if (lane < n) {
                     const int32_t kk = k + lane;
@@ -1259,6 +1284,17 @@ attention_kernel(const __grid_constant__ AttnParams p,
                         sm.meta()[stg] = lohi;
                         if (lohi & kTileSkip) {
                             mbar_arrive(full);
+                        } else if constexpr (FMT == DATTN_KV_MIXED) {
+                            // a 4-bit tile takes the first half of the 8-bit stage: K codes,
+                            // then V codes at 8 d bytes, where the 4-bit consumer reads them
+                            const bool f4 = (lohi & kTileI4) != 0;
+                            const uint32_t tb = f4 ? tile_bytes / 2u : tile_bytes;
+                            mbar_arrive_expect_tx(full, 2u * tb + 128u);
+                            const uint32_t dst = stages0 + (uint32_t)stg * sm.L.stage_bytes;
+                            tma_load_2d(dst, f4 ? &tmap_k4 : &tmap_k, 0, yc, full, pol);
+                            tma_load_2d(dst + tb, f4 ? &tmap_v4 : &tmap_v, 0, yc, full, pol);
+                            bulk_copy(smem_u32(sm.scales(stg)), p.kv_scale + 2 * y, 128u, full,
+                                      pol);
                         } else {
                             mbar_arrive_expect_tx(full, tx);
                             const uint32_t dst = stages0 + (uint32_t)stg * sm.L.stage_bytes;
@@ -1303,7 +1339,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
                         if (have) base = pc.r0;
                     }
                 }
-                TileRef ref{0, kTileSkip};
+                TileRef ref{0, kTileSkip, 0};
                 if (my_s >= 0) ref = resolve_tile(p, sm, my_s, my_local, pieces.aligned());
                 stop = !issue(ref, nb);
             }
@@ -1377,6 +1413,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
             if (p.append) patch = cons.load_new_row(pc.s);
         }
         cons.reset();
+        if constexpr (FMT == DATTN_KV_MIXED) cons.i4 = head_is_i4(p.hf, pc.s % p.Hkv);
         const int32_t s = pc.s;
         const int32_t nr = pc.r1 - pc.r0;
         if constexpr (FMT == DATTN_KV_INT4) {
@@ -1430,7 +1467,11 @@ attention_kernel(const __grid_constant__ AttnParams p,
             const int32_t lohi = sm.meta()[stg];
             const int lo = tile_lo(lohi), hi = tile_hi(lohi), cut = tile_cut(lohi);
             if (ok && !(lohi & kTileSkip)) {
-                if constexpr (Q) {
+                if constexpr (FMT == DATTN_KV_MIXED) {
+                    const uint32_t st = stage0 + (uint32_t)stg * sm.L.stage_bytes;
+                    if (lohi & kTileI4) cons.tile_i4(st, sm.scales(stg), lo, hi, cut);
+                    else                cons.tile_f8(st, sm.scales(stg), lo, hi, cut);
+                } else if constexpr (Q) {
                     cons.tile_f8(stage0 + (uint32_t)stg * sm.L.stage_bytes, sm.scales(stg), lo, hi,
                                  cut);
                 } else {
@@ -1627,17 +1668,37 @@ static dattn_status_t launch_d(const AttnParams& p0, const void* k_pool, const v
     p.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + counters);
     alignas(64) CUtensorMap tk;
     alignas(64) CUtensorMap tv;
+    alignas(64) CUtensorMap tk4;
+    alignas(64) CUtensorMap tv4;
     const int64_t rows = (int64_t)p.num_pages * p.Hkv * p.P;
     if constexpr (FMT == DATTN_KV_BF16) {
         if ((st = make_kv_tensor_map(&tk, k_pool, rows, D)) != DATTN_OK) return st;
         if ((st = make_kv_tensor_map(&tv, v_pool, rows, D)) != DATTN_OK) return st;
+    } else if constexpr (FMT == DATTN_KV_MIXED) {
+        // the 8-bit region [num_pages][H8][P][d], then the 4-bit region [num_pages][H4][P][d/2];
+        // a format without heads gets the other region's map (no tile uses it)
+        const int64_t rows8 = (int64_t)p.num_pages * (p.Hkv - p.hf.h4) * p.P;
+        const int64_t rows4 = (int64_t)p.num_pages * p.hf.h4 * p.P;
+        const uint8_t* k4 = static_cast<const uint8_t*>(k_pool) + rows8 * D;
+        const uint8_t* v4 = static_cast<const uint8_t*>(v_pool) + rows8 * D;
+        if (rows4 > 0) {
+            if ((st = make_kv_tensor_map_u8(&tk4, k4, rows4, D / 2)) != DATTN_OK) return st;
+            if ((st = make_kv_tensor_map_u8(&tv4, v4, rows4, D / 2)) != DATTN_OK) return st;
+        }
+        if (rows8 > 0) {
+            if ((st = make_kv_tensor_map_u8(&tk, k_pool, rows8, D)) != DATTN_OK) return st;
+            if ((st = make_kv_tensor_map_u8(&tv, v_pool, rows8, D)) != DATTN_OK) return st;
+        }
+        if (rows4 == 0) tk4 = tk, tv4 = tv;
+        if (rows8 == 0) tk = tk4, tv = tv4;
     } else {
         const int row_bytes = FMT == DATTN_KV_INT4 ? D / 2 : D;
         if ((st = make_kv_tensor_map_u8(&tk, k_pool, rows, row_bytes)) != DATTN_OK) return st;
         if ((st = make_kv_tensor_map_u8(&tv, v_pool, rows, row_bytes)) != DATTN_OK) return st;
     }
+    if constexpr (FMT != DATTN_KV_MIXED) tk4 = tk, tv4 = tv;  // not read
     if (launch_pdl(attention_kernel<D, FMT>, dim3(G), dim3(kAttnThreads), L.total, stream, p, tk,
-                   tv) != cudaSuccess)
+                   tv, tk4, tv4) != cudaSuccess)
         return DATTN_ERR_CUDA;
     return DATTN_OK;
 }
@@ -1646,13 +1707,16 @@ dattn_status_t launch_attention(const AttnParams& p, const void* k_pool, const v
                                 int D, int32_t num_splits, void* ws, size_t ws_bytes,
                                 cudaStream_t stream, int64_t tiles_bound) {
     if (D != 64 && D != 128) return DATTN_ERR_UNSUPPORTED;
-    auto pick = [&](auto bf16, auto f8, auto i4) {
-        return p.fmt == DATTN_KV_INT4 ? i4 : p.fmt == DATTN_KV_FP8_E4M3 ? f8 : bf16;
+    auto pick = [&](auto bf16, auto f8, auto i4, auto mix) {
+        return p.fmt == DATTN_KV_MIXED    ? mix
+             : p.fmt == DATTN_KV_INT4     ? i4
+             : p.fmt == DATTN_KV_FP8_E4M3 ? f8
+                                          : bf16;
     };
     auto launch = D == 64 ? pick(launch_d<64, DATTN_KV_BF16>, launch_d<64, DATTN_KV_FP8_E4M3>,
-                                 launch_d<64, DATTN_KV_INT4>)
+                                 launch_d<64, DATTN_KV_INT4>, launch_d<64, DATTN_KV_MIXED>)
                           : pick(launch_d<128, DATTN_KV_BF16>, launch_d<128, DATTN_KV_FP8_E4M3>,
-                                 launch_d<128, DATTN_KV_INT4>);
+                                 launch_d<128, DATTN_KV_INT4>, launch_d<128, DATTN_KV_MIXED>);
     return launch(p, k_pool, v_pool, num_splits, ws, ws_bytes, stream, tiles_bound);
 }
 

@@ -19,12 +19,18 @@ constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStagesBf16 = 8;
 constexpr int kStagesF8 = 12;
 constexpr int kStagesI4 = 24;
+// The mixed pool's stages are 8-bit stages; a 4-bit tile fills half of one.
 __host__ __device__ constexpr int attn_stages(int fmt) {
-    return fmt == DATTN_KV_INT4 ? kStagesI4 : fmt == DATTN_KV_FP8_E4M3 ? kStagesF8 : kStagesBf16;
+    return fmt == DATTN_KV_INT4 ? kStagesI4
+         : (fmt == DATTN_KV_FP8_E4M3 || fmt == DATTN_KV_MIXED) ? kStagesF8
+                                                                : kStagesBf16;
 }
-// Bytes of one K (or V) tile of 16 tokens in shared memory for a pool format.
+// Bytes of one K (or V) tile of 16 tokens in shared memory for a pool format (the mixed
+// pool: the larger, 8-bit tile).
 __host__ __device__ constexpr uint32_t attn_tile_bytes(int fmt, int D) {
-    return (fmt == DATTN_KV_INT4 ? 8u : fmt == DATTN_KV_FP8_E4M3 ? 16u : 32u) * (uint32_t)D;
+    return (fmt == DATTN_KV_INT4 ? 8u
+            : (fmt == DATTN_KV_FP8_E4M3 || fmt == DATTN_KV_MIXED) ? 16u
+                                                                   : 32u) * (uint32_t)D;
 }
 constexpr int kMaxItems = 4096;     // B (or C) bound
 constexpr int kMaxKvHeads = 256;
@@ -34,6 +40,37 @@ constexpr int kMaxCtasPerSm = 4;    // bound used for workspace sizing with auto
 constexpr int32_t kSegCost = 6;     // cost units per segment in the balanced split
 
 enum AttnMode : int { MODE_PARTIAL = 0, MODE_DENSE = 1, MODE_SPARSE = 2 };
+
+// The per-KV-head formats of a mixed pool: bit h of i4 is set when KV head h is 4-bit (else
+// 8-bit); h4 heads are 4-bit. A head's row within its region uses its index among the heads
+// of its own format.
+struct KvHeadFormats {
+    int32_t h4;
+    uint32_t i4[kMaxKvHeads / 32];
+};
+// Fills f from a layout (all-zero unless the layout is mixed); INVALID_ARG when a mixed
+// layout's head_format is missing or names another format.
+dattn_status_t head_formats(const dattn_kv_layout& L, KvHeadFormats& f);
+
+__host__ __device__ __forceinline__ int32_t popc32(uint32_t x) {
+#ifdef __CUDA_ARCH__
+    return __popc(x);
+#else
+    return __builtin_popcount(x);
+#endif
+}
+__host__ __device__ __forceinline__ bool head_is_i4(const KvHeadFormats& f, int32_t h) {
+    return (f.i4[h >> 5] >> (h & 31)) & 1u;
+}
+// Index of KV head h among the heads of its own format.
+__host__ __device__ __forceinline__ int32_t head_class_index(const KvHeadFormats& f, int32_t h,
+                                                             bool i4) {
+    int32_t n = 0;
+    for (int32_t w = 0; w < (h >> 5); ++w) n += popc32(f.i4[w]);
+    const uint32_t below = (h & 31) ? f.i4[h >> 5] & ((1u << (h & 31)) - 1u) : 0u;
+    n += popc32(below);
+    return i4 ? n : h - n;
+}
 
 // Everything one launch of the attention engine needs (device pointers unless noted).
 struct AttnParams {
@@ -82,6 +119,7 @@ struct AttnParams {
     // run [16 K scales][16 V scales]
     int32_t fmt;
     const float* kv_scale;
+    KvHeadFormats hf;  // DATTN_KV_MIXED: the per-head formats
 };
 
 // Floats of one workspace slot (a piece's partial): MA [g][D], then m [g] and e [g],

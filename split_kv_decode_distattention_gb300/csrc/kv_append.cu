@@ -25,6 +25,9 @@
 // each code is x / scale rounded to the nearest integer (ties to even) in [-7, 7], both
 // divisions in IEEE fp32, stored as the nibble code + 8 with channel 2j in the low nibble of
 // byte j. A thread's 8 channels become one 32-bit word.
+//
+// The mixed pool quantizes each KV head's rows in that head's format (8-bit or 4-bit) and
+// writes them to the region of that format, at the head's index among its format's heads.
 #include "common.cuh"
 #include "internal.h"
 
@@ -59,13 +62,18 @@ __device__ __forceinline__ uint2 quant8(const uint4& v, float s) {
     return make_uint2(f32x4_to_e4m3(x[0], x[1], x[2], x[3]), f32x4_to_e4m3(x[4], x[5], x[6], x[7]));
 }
 
-// Row scale and codes of one 8-channel chunk; `mask` holds the lanes of this warp in the
-// loop, and the VPR lanes of a row are consecutive and all in it.
+// Max |x| of a row, from this lane's 8-channel chunk; `mask` holds the lanes of this warp in
+// the loop, and the VPR lanes of a row are consecutive and all in it.
 template <int VPR>
-__device__ __forceinline__ uint2 quant_row_chunk(const uint4& v, unsigned mask, float& scale) {
+__device__ __forceinline__ float row_absmax(const uint4& v, unsigned mask) {
     float m = absmax8(v);
 #pragma unroll
     for (int off = 1; off < VPR; off <<= 1) m = fmaxf(m, __shfl_xor_sync(mask, m, off));
+    return m;
+}
+
+// 8-bit row scale (row max |x| = m) and the E4M3 codes of one chunk.
+__device__ __forceinline__ uint2 quant8_chunk(const uint4& v, float m, float& scale) {
     scale = __fdiv_rn(m, 448.0f);
     return scale > 0.f ? quant8(v, scale) : make_uint2(0u, 0u);
 }
@@ -84,19 +92,16 @@ __device__ __forceinline__ uint32_t quant4(const uint4& v, float s) {
     return out;
 }
 
-// Row scale and packed 4-bit codes of one 8-channel chunk (lanes as in quant_row_chunk).
-template <int VPR>
-__device__ __forceinline__ uint32_t quant4_row_chunk(const uint4& v, unsigned mask, float& scale) {
-    float m = absmax8(v);
-#pragma unroll
-    for (int off = 1; off < VPR; off <<= 1) m = fmaxf(m, __shfl_xor_sync(mask, m, off));
+// 4-bit row scale (row max |x| = m) and the packed codes of one chunk.
+__device__ __forceinline__ uint32_t quant4_chunk(const uint4& v, float m, float& scale) {
     scale = __fdiv_rn(m, 7.0f);
     return scale > 0.f ? quant4(v, scale) : 0x88888888u;
 }
 
 template <int D, int FMT>
 __global__ void __launch_bounds__(kAppendMaxThreads)
-kv_append_kernel(dattn_kv_layout L, void* __restrict__ k_pool_v, void* __restrict__ v_pool_v,
+kv_append_kernel(dattn_kv_layout L, const __grid_constant__ KvHeadFormats hf,
+                 void* __restrict__ k_pool_v, void* __restrict__ v_pool_v,
                  uint16_t* __restrict__ stats, const uint16_t* __restrict__ k_new,
                  const uint16_t* __restrict__ v_new, int32_t T, int32_t* seq_lens,
                  int32_t update_in_place, int32_t* dev_err) {
@@ -165,30 +170,39 @@ kv_append_kernel(dattn_kv_layout L, void* __restrict__ k_pool_v, void* __restric
                     else page = pg;
                 }
             }
-            if constexpr (FMT == DATTN_KV_INT4) {
+            if constexpr (FMT != DATTN_KV_BF16) {
                 // every lane of a row takes part in the reductions, mapped page or not
-                float ks, vs;
-                const uint32_t kc = quant4_row_chunk<VPR>(kv, mask, ks);
-                const uint32_t vc = quant4_row_chunk<VPR>(vv, mask, vs);
+                const float mk = row_absmax<VPR>(kv, mask), mv = row_absmax<VPR>(vv, mask);
+                const bool i4 = FMT == DATTN_KV_INT4 || (FMT == DATTN_KV_MIXED && head_is_i4(hf, h));
                 if (page >= 0) {
-                    const int64_t row = ((int64_t)page * Hkv + h) * P + (t - lp * P);
-                    *reinterpret_cast<uint32_t*>(k_code + row * (D / 2) + c8 * 4) = kc;
-                    *reinterpret_cast<uint32_t*>(v_code + row * (D / 2) + c8 * 4) = vc;
-                    if (c8 == 0) {  // [row / 16][K, V][row % 16]
-                        float* sc = L.kv_scale + (row >> 4) * 32 + (row & 15);
-                        sc[0] = ks;
-                        sc[16] = vs;
+                    const int32_t slot = t - lp * P;
+                    const int64_t row = ((int64_t)page * Hkv + h) * P + slot;  // the scales' row
+                    // the codes' row: the mixed pool keeps each format in its own region
+                    int64_t crow = row;
+                    uint8_t* kd = k_code;
+                    uint8_t* vd = v_code;
+                    if constexpr (FMT == DATTN_KV_MIXED) {
+                        const int32_t h4 = hf.h4, h8 = Hkv - h4;
+                        crow = ((int64_t)page * (i4 ? h4 : h8) + head_class_index(hf, h, i4)) * P +
+                               slot;
+                        if (i4) {
+                            const int64_t region8 = (int64_t)L.num_pages * h8 * P * D;
+                            kd += region8;
+                            vd += region8;
+                        }
                     }
-                }
-            } else if constexpr (FMT == DATTN_KV_FP8_E4M3) {
-                // every lane of a row takes part in the reductions, mapped page or not
-                float ks, vs;
-                const uint2 kc = quant_row_chunk<VPR>(kv, mask, ks);
-                const uint2 vc = quant_row_chunk<VPR>(vv, mask, vs);
-                if (page >= 0) {
-                    const int64_t row = ((int64_t)page * Hkv + h) * P + (t - lp * P);
-                    *reinterpret_cast<uint2*>(k_code + row * D + c8 * 8) = kc;
-                    *reinterpret_cast<uint2*>(v_code + row * D + c8 * 8) = vc;
+                    float ks, vs;
+                    if (i4) {
+                        const uint32_t kc = quant4_chunk(kv, mk, ks);
+                        const uint32_t vc = quant4_chunk(vv, mv, vs);
+                        *reinterpret_cast<uint32_t*>(kd + crow * (D / 2) + c8 * 4) = kc;
+                        *reinterpret_cast<uint32_t*>(vd + crow * (D / 2) + c8 * 4) = vc;
+                    } else {
+                        const uint2 kc = quant8_chunk(kv, mk, ks);
+                        const uint2 vc = quant8_chunk(vv, mv, vs);
+                        *reinterpret_cast<uint2*>(kd + crow * D + c8 * 8) = kc;
+                        *reinterpret_cast<uint2*>(vd + crow * D + c8 * 8) = vc;
+                    }
                     if (c8 == 0) {  // [row / 16][K, V][row % 16]
                         float* sc = L.kv_scale + (row >> 4) * 32 + (row & 15);
                         sc[0] = ks;
@@ -255,16 +269,24 @@ dattn_status_t launch_kv_append(const dattn_kv_layout& L, void* k_pool, void* v_
     const int32_t inplace = single ? 1 : 0;
     const int32_t items = L.num_kv_heads * (L.head_dim / 8);
     const dim3 block(min(kAppendMaxThreads, (items + 31) / 32 * 32));
-    auto pick = [&](auto bf16, auto f8, auto i4) {
-        return L.kv_format == DATTN_KV_INT4 ? i4 : L.kv_format == DATTN_KV_FP8_E4M3 ? f8 : bf16;
+    auto pick = [&](auto bf16, auto f8, auto i4, auto mix) {
+        return L.kv_format == DATTN_KV_MIXED  ? mix
+             : L.kv_format == DATTN_KV_INT4   ? i4
+             : L.kv_format == DATTN_KV_FP8_E4M3 ? f8
+                                                : bf16;
     };
     auto kern = L.head_dim == 64
                     ? pick(kv_append_kernel<64, DATTN_KV_BF16>, kv_append_kernel<64, DATTN_KV_FP8_E4M3>,
-                           kv_append_kernel<64, DATTN_KV_INT4>)
+                           kv_append_kernel<64, DATTN_KV_INT4>, kv_append_kernel<64, DATTN_KV_MIXED>)
                     : pick(kv_append_kernel<128, DATTN_KV_BF16>,
                            kv_append_kernel<128, DATTN_KV_FP8_E4M3>,
-                           kv_append_kernel<128, DATTN_KV_INT4>);
-    const cudaError_t e = launch_pdl(kern, grid, block, 0, stream, L, k_pool, v_pool, stats,
+                           kv_append_kernel<128, DATTN_KV_INT4>,
+                           kv_append_kernel<128, DATTN_KV_MIXED>);
+    KvHeadFormats hf;
+    if (head_formats(L, hf) != DATTN_OK) return DATTN_ERR_INVALID_ARG;
+    dattn_kv_layout Ld = L;
+    Ld.head_format = nullptr;  // a host array: the kernel reads hf
+    const cudaError_t e = launch_pdl(kern, grid, block, 0, stream, Ld, hf, k_pool, v_pool, stats,
                                      k_new, v_new, T, seq_lens, inplace, dev_err);
     if (e != cudaSuccess) return DATTN_ERR_CUDA;
     if (!single) {

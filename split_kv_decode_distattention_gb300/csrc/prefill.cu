@@ -921,7 +921,8 @@ extern "C" dattn_status_t dattn_prefill(const dattn_kv_layout* layout, const voi
     if ((int64_t)layout->max_pages_per_req * layout->page_size >= (1ll << 30))
         return DATTN_ERR_UNSUPPORTED;
     if (layout->kv_format != DATTN_KV_BF16) {
-        return layout->kv_format == DATTN_KV_FP8_E4M3 || layout->kv_format == DATTN_KV_INT4
+        return layout->kv_format == DATTN_KV_FP8_E4M3 || layout->kv_format == DATTN_KV_INT4 ||
+                       layout->kv_format == DATTN_KV_MIXED
                    ? DATTN_ERR_UNSUPPORTED
                    : DATTN_ERR_INVALID_ARG;
     }

@@ -7,7 +7,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (KV_BF16, KV_FP8_E4M3, KV_INT4, KVLayout, SparseConfig, Workspace,
+from . import (KV_BF16, KV_FP8_E4M3, KV_INT4, KV_MIXED, KVLayout, SparseConfig, Workspace,
+               mixed_pool_bytes,
                dattn_append_decode, dattn_decode, dattn_decode_multi, dattn_kv_append,
                dattn_page_select)
 from .workloads import Case
@@ -19,21 +20,30 @@ class PagedCache:
     kv_format KV_BF16 keeps bf16 values; KV_FP8_E4M3 keeps uint8 E4M3 codes plus one float32
     scale per (token, KV head) row in kv_scale [num_pages][Hkv][P/16][2][16] (per logical
     page: 16 K scales, then 16 V scales); KV_INT4 keeps [num_pages][Hkv][P][d/2] bytes of two
-    4-bit codes each, with kv_scale as for KV_FP8_E4M3.
+    4-bit codes each, with kv_scale as for KV_FP8_E4M3. KV_MIXED keeps each KV head in the
+    format head_format[h] names (flat uint8 pools: the 8-bit heads' region, then the 4-bit
+    heads' region).
     """
 
     def __init__(self, case: Case, device="cuda", with_stats: bool = False, fill: bool = True,
-                 chunk_tokens: int = 8192, zero_pool: bool = False, kv_format: int = KV_BF16):
+                 chunk_tokens: int = 8192, zero_pool: bool = False, kv_format: int = KV_BF16,
+                 head_format=None):
         self.case = case
         self.device = torch.device(device)
         c = case
         alloc = torch.zeros if zero_pool else torch.empty
         self.kv_format = kv_format
-        quant = kv_format in (KV_FP8_E4M3, KV_INT4)
+        self.head_format = list(head_format) if head_format is not None else None
+        quant = kv_format in (KV_FP8_E4M3, KV_INT4, KV_MIXED)
         elem = torch.uint8 if quant else torch.bfloat16
-        row = c.d // 2 if kv_format == KV_INT4 else c.d
-        self.k_pool = alloc(c.num_pages, c.Hkv, c.P, row, dtype=elem, device=device)
-        self.v_pool = alloc(c.num_pages, c.Hkv, c.P, row, dtype=elem, device=device)
+        if kv_format == KV_MIXED:
+            nbytes = mixed_pool_bytes(c.num_pages, self.head_format, c.d, c.P)
+            self.k_pool = alloc(nbytes, dtype=elem, device=device)
+            self.v_pool = alloc(nbytes, dtype=elem, device=device)
+        else:
+            row = c.d // 2 if kv_format == KV_INT4 else c.d
+            self.k_pool = alloc(c.num_pages, c.Hkv, c.P, row, dtype=elem, device=device)
+            self.v_pool = alloc(c.num_pages, c.Hkv, c.P, row, dtype=elem, device=device)
         self.kv_scale = None
         if quant:
             self.kv_scale = alloc(c.num_pages, c.Hkv, c.P // 16, 2, 16, dtype=torch.float32,
@@ -55,7 +65,7 @@ class PagedCache:
     def _layout(self, block_table) -> KVLayout:
         c = self.case
         return KVLayout(c.num_pages, c.Hkv, c.d, c.P, block_table, self.kv_format,
-                        self.kv_scale)
+                        self.kv_scale, head_format=self.head_format)
 
     def _row_layout(self, b: int) -> KVLayout:
         return self._layout(self.block_table[b:b + 1])

@@ -123,7 +123,7 @@ def test_kv_format_is_validated(dattn):
         out.c.kv_format, out.c.kv_scale = fmt, kv_scale
         return out
 
-    assert _decode_status(dattn, lay(3, 128)) == INVALID     # unknown format
+    assert _decode_status(dattn, lay(4, 128)) == INVALID     # unknown format
     assert _decode_status(dattn, lay(-1, None)) == INVALID
     for fmt in (dattn.KV_FP8_E4M3, dattn.KV_INT4):
         assert _decode_status(dattn, lay(fmt, None)) == INVALID  # the scale pool missing
@@ -135,6 +135,40 @@ def test_kv_format_is_validated(dattn):
     for fmt in (dattn.KV_FP8_E4M3, dattn.KV_INT4):
         with pytest.raises(ValueError):
             dattn.KVLayout(8, 2, 128, 16, torch.zeros(1, 4, dtype=torch.int32), kv_format=fmt)
+
+
+def test_mixed_format_is_validated(dattn):
+    """A mixed layout needs one FP8 or 4-bit entry per KV head in its host head_format."""
+    INVALID, UNSUPPORTED = 1, 2
+    import torch
+
+    def lay(formats):
+        out = _lay(dattn)
+        out.c.kv_format, out.c.kv_scale = dattn.KV_MIXED, 128
+        arr = None
+        if formats is not None:
+            arr = (ctypes.c_int8 * len(formats))(*formats)
+            out.c.head_format = ctypes.addressof(arr)
+        return out, arr
+
+    for formats, want in [(None, INVALID),                                      # no table
+                          ([dattn.KV_FP8_E4M3, dattn.KV_BF16], INVALID),        # bf16 head
+                          ([dattn.KV_INT4, 7], INVALID),                        # unknown
+                          ([dattn.KV_FP8_E4M3, dattn.KV_INT4], UNSUPPORTED),    # well formed:
+                          ([dattn.KV_INT4, dattn.KV_INT4], UNSUPPORTED)]:       # the group size
+        layout, keep = lay(formats)                                             # answers next
+        assert _decode_status(dattn, layout, Hq=36) == want, formats
+    bt = torch.zeros(1, 4, dtype=torch.int32)
+    sc = torch.zeros(8 * 2 * 16 * 2, dtype=torch.float32)
+    with pytest.raises(ValueError):
+        dattn.KVLayout(8, 2, 128, 16, bt, kv_format=dattn.KV_MIXED, kv_scale=sc)
+    with pytest.raises(ValueError):
+        dattn.KVLayout(8, 2, 128, 16, bt, kv_format=dattn.KV_MIXED, kv_scale=sc,
+                       head_format=[dattn.KV_INT4])
+    ok = dattn.KVLayout(8, 2, 128, 16, bt, kv_format=dattn.KV_MIXED, kv_scale=sc,
+                        head_format=[dattn.KV_INT4, dattn.KV_FP8_E4M3])
+    # 8 pages x 16 tokens: one 8-bit head of 128 bytes per row, one 4-bit head of 64
+    assert dattn.mixed_pool_bytes(8, ok.head_format, 128, 16) == 8 * 16 * (128 + 64)
 
 
 def test_decode_multi_is_validated(dattn):

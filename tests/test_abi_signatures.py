@@ -151,7 +151,8 @@ def test_constants_equal_the_headers_defines():
     assert {k: v for k, v in defines.items() if k.startswith("DEVERR_")} == {
         "DEVERR_" + k: v for k, v in dattn.DEVERR.items()}
     for k in ("HEAD_DENSE", "HEAD_RETRIEVAL", "HEAD_STREAMING", "KV_BF16", "KV_FP8_E4M3",
-              "KV_INT4"):
+              "KV_INT4", "KV_MIXED"):
         assert getattr(dattn, k) == defines[k], k
     assert {k for k in defines if k.startswith(("HEAD_", "KV_"))} == {
-        "HEAD_DENSE", "HEAD_RETRIEVAL", "HEAD_STREAMING", "KV_BF16", "KV_FP8_E4M3", "KV_INT4"}
+        "HEAD_DENSE", "HEAD_RETRIEVAL", "HEAD_STREAMING", "KV_BF16", "KV_FP8_E4M3", "KV_INT4",
+        "KV_MIXED"}
