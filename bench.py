@@ -1,8 +1,10 @@
 """Benchmark of the split-KV decode path on GB300.
 
 One step is one decode layer-step of the whole batch through the library's C ABI:
-  dense workloads:  dattn_kv_append (one new token per request), then dattn_decode
-                    (split-KV MicroAttention partials plus the in-launch merge);
+  dense workloads:  dattn_append_decode (one new token per request appended and attended
+                    in one launch: split-KV MicroAttention partials plus the in-launch
+                    merge); with a quantized pool, or --unfused, dattn_kv_append then
+                    dattn_decode;
   sparse-512k:      the same, plus dattn_page_select at the start of every reuse window.
 The metric is achieved HBM bandwidth in GB/s: the algorithmic bytes of the step (valid K/V
 read, statistics scanned, new tokens written, queries, outputs, block table) divided by
@@ -23,6 +25,9 @@ one pool: streaming heads 4-bit, retrieval and dense heads 8-bit, decoded in one
 --queries T (dense workloads) makes each step a chunked one: T new tokens per request are
 appended, then dattn_decode_multi attends all T query tokens, causal over the new tokens.
 The K/V is read once per step, as for T = 1; queries, outputs and appends scale with T.
+
+The default run (mha-1m, bf16) also times sparse-512k afterwards and reports it under
+"also" in the same line (--also none skips it, --also NAME picks another workload).
 
 --impl reference times the CPU oracle (test infrastructure) on the host cores over a
 bounded sample of the same workload and prints the same JSON line with "impl": "reference".
@@ -90,6 +95,10 @@ def parse_args():
                     help="step = dattn_kv_append then dattn_decode (two launches) instead of "
                          "dattn_append_decode (bf16 pool, one query token)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--also", default="auto",
+                    help="a second workload timed after the first and summarised in the same "
+                         "line under 'also' (auto: sparse-512k after the default mha-1m bf16 "
+                         "run; none: no second workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--graph", action="store_true",
@@ -1322,6 +1331,8 @@ def main():
             dist.destroy_process_group()
         return
     res = run_dattn(args, rank, world)
+    also_args = also_config(args)
+    res_also = run_dattn(also_args, rank, world) if also_args is not None else None
     case = res["case"]
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -1384,7 +1395,53 @@ def main():
         line["info"] = res["info"]
     if "e2e" in res:
         line["e2e"] = res["e2e"]
+    if res_also is not None:
+        line["also"] = also_summary(res_also, also_args, peak)
     print(json.dumps(line), flush=True)
+
+
+def also_config(args):
+    """The arguments of the second workload (None: no second workload). The default run adds
+    the block-sparse workload, so that one line carries both decode paths."""
+    name = args.also
+    if name == "auto":
+        plain = (args.config == "mha-1m" and args.kv_format == "bf16" and args.queries == 1
+                 and not (args.batch or args.ctx or args.profile))
+        name = "sparse-512k" if plain else "none"
+    if name in ("none", args.config):
+        return None
+    if name not in WORKLOAD_TEXT or name == "prefill-32k":
+        raise SystemExit(f"--also {name}: not a decode workload")
+    a = argparse.Namespace(**vars(args))
+    a.config, a.also, a.no_cpu_baseline = name, "none", True
+    return a
+
+
+def also_summary(res, args, peak) -> dict:
+    """The second workload's figures: its steps' value and time and its decode kernel's
+    roofline, timed as the main line's."""
+    case = res["case"]
+    ms_step = res["ms_total"] / args.steps
+    value = res["bytes_all"] / (res["ms_total"] * 1e-3) / 1e9
+    dec_avg_ms = sum(res["dec_ms"]) / len(res["dec_ms"])
+    achieved = res["dec_bytes"] / (dec_avg_ms * 1e-3) / 1e9
+    out = {"config": config_obj(case, args), "value": round(value, 2), "unit": "GB/s",
+           "steps": args.steps, "us_per_layer_step": round(ms_step * 1e3, 2),
+           "frac_of_8tbs": round(value / ROOFLINE_8TBS, 4),
+           "roofline": {"bound": "hbm",
+                        "kernel": ("attention_kernel (dattn_append_decode)" if fused_step(args)
+                                   else "attention_kernel (dattn_decode)"),
+                        "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(achieved / peak, 4),
+                        "traffic": traffic_record(traffic_key(args)),
+                        "algorithmic_bytes_per_launch": int(res["dec_bytes"]),
+                        "avg_launch_us": round(dec_avg_ms * 1e3, 2),
+                        "median_launch_us": round(statistics.median(res["dec_ms"]) * 1e3, 2),
+                        "timed_launches": len(res["dec_ms"])},
+           "gpu_launches": res["launches"], "clocks": res["clocks"]}
+    if "e2e" in res:
+        out["e2e"] = res["e2e"]
+    return out
 
 
 if __name__ == "__main__":

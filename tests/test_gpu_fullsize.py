@@ -189,6 +189,81 @@ def test_sparse_512k_full_size(seed):
     _check_pairs(case, q, cache.lens, out, m_g, e_g, pairs, "sparse-512k", rows_of=rows_of)
 
 
+def _select_full(case, cache):
+    """The window's first step: append one token, then select (with the pool pages)."""
+    kn, vn = cache.new_tokens(1)
+    cache.append(kn, vn)
+    sel = torch.empty(case.B, case.Hkv, case.top_k, dtype=torch.int32, device=DEV)
+    phys = torch.empty_like(sel)
+    cache.select(case.q(0, DEV), sel, cache.workspace(top_k=case.top_k), selected_phys=phys)
+    torch.cuda.synchronize()
+    assert int(cache.dev_err.item()) == 0
+    return sel, phys
+
+
+def test_sparse_512k_fused_step_full_size():
+    """The benchmark's step: dattn_append_decode with the selector's pool pages, two steps
+    of the window, sampled pairs against the oracle over the token sets of the selection."""
+    _lib()
+    case = W.sparse_512k(seed=0)
+    cache = _cache(case, with_stats=True)
+    sel, phys = _select_full(case, cache)
+    got = sel.cpu().numpy()
+    sp = cache.sparse_config(sel, phys)
+    ws = cache.workspace()
+    for step in (1, 2):
+        kn, vn = cache.new_tokens(1)
+        q = case.q(step, DEV)
+        out = torch.empty(case.B, case.Hq, case.d, device=DEV)
+        m_g = torch.empty(case.B, case.Hq, device=DEV)
+        e_g = torch.empty_like(m_g)
+        cache.append_decode(kn, vn, q, out, ws, m_g=m_g, e_g=e_g, sparse=sp)
+        torch.cuda.synchronize()
+        assert int(cache.dev_err.item()) == 0
+        assert cache.seq_lens.tolist() == cache.lens
+
+    def rows_of(b, kvh):
+        return oracle.sparse_rows(case.head_kind[kvh], cache.lens[b], case.P, got[b, kvh],
+                                  case.sinks, case.local)
+    pairs = [(0, 1), (2, 9), (4, 18), (6, 27), (7, 30)]
+    _check_pairs(case, q, cache.lens, out, m_g, e_g, pairs, "sparse-512k fused",
+                 rows_of=rows_of)
+
+
+def test_sparse_512k_mixed_pool_full_size():
+    """sparse-512k over the mixed pool (retrieval and dense heads 8-bit, streaming heads
+    4-bit): sampled pairs of both kinds against the oracle's float64 attention over its own
+    dequantized rows of each head's format."""
+    dattn = _lib()
+    case = W.sparse_512k(seed=1)
+    formats = [dattn.KV_INT4 if k == W.HEAD_STREAMING else dattn.KV_FP8_E4M3
+               for k in case.head_kind]
+    cache = _cache(case, with_stats=True, kv_format=dattn.KV_MIXED, head_format=formats)
+    sel, _ = _select_full(case, cache)
+    got = sel.cpu().numpy()
+    q, out, m_g, e_g = _step(cache, case, sparse=cache.sparse_config(sel))
+    qb = oracle.bf16_bits(q)
+    o, mg, eg = out.cpu().numpy(), m_g.cpu().numpy(), e_g.cpu().numpy()
+    kinds_seen = set()
+    for b, h in [(0, 0), (1, 5), (3, 13), (6, 22), (7, 31)]:
+        kvh = h // case.g
+        kind = case.head_kind[kvh]
+        kinds_seen.add(kind)
+        if kind == W.HEAD_STREAMING:
+            quant, deq = oracle.quantize_rows_int4, oracle.dequantize_rows_int4
+        else:
+            quant, deq = oracle.quantize_rows_fp8, oracle.dequantize_rows_fp8
+        Ks, Vs = _host_heads(case, b, cache.lens[b], [kvh])
+        Kd, Vd = deq(*quant(Ks[0])), deq(*quant(Vs[0]))
+        rows = oracle.sparse_rows(kind, cache.lens[b], case.P, got[b, kvh], case.sinks,
+                                  case.local)
+        r, rm, re = oracle.attention_f64(qb[b, h], Kd, Vd, case.scale, rows=rows)
+        assert_out_close(o[b, h], r, f"sparse-512k mixed b={b} h={h}")
+        assert_m_close(mg[b, h], rm, f"sparse-512k mixed b={b} h={h}")
+        assert_e_close(eg[b, h], re, f"sparse-512k mixed b={b} h={h}")
+    assert {W.HEAD_RETRIEVAL, W.HEAD_STREAMING} <= kinds_seen
+
+
 @pytest.mark.parametrize("fmt", ["fp8", "int4"])
 def test_mha_32k_quantized_pools_full_size(fmt):
     """mha-32k over the 8-bit and the 4-bit pool: the append quantizes the seeded rows, the
