@@ -299,9 +299,11 @@ def traffic_key(args):
             (f"/T{args.queries}" if args.queries > 1 else ""))
 
 
-def traffic_record(config, sources=DECODE_SOURCES):
+def traffic_record(config, sources=DECODE_SOURCES, alg_bytes=None):
     """DRAM bytes per launch of the workload's dominant kernel from the committed ncu
-    summary, if it was taken on the current sources of that kernel."""
+    summary, if it was taken on the current sources of that kernel. The records were
+    captured on reduced cases; their ratio of DRAM to algorithmic bytes scales to this run's
+    launch by its algorithmic bytes (alg_bytes), both growing with the attended tokens."""
     if config is None:
         return None
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -311,6 +313,8 @@ def traffic_record(config, sources=DECODE_SOURCES):
         return None
     if not rec or rec.get("source_hash") != kernel_source_hash(sources):
         return None
+    if alg_bytes is not None and "ratio_to_algorithmic" in rec:
+        return int(round(rec["ratio_to_algorithmic"] * alg_bytes))
     return rec.get("dram_bytes_per_launch")
 
 
@@ -1270,7 +1274,8 @@ def prefill_main(args, rank: int, world: int):
                      "achieved": round(ktf, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(ktf / peak, 4),
                      "peak_source": "measured" if "bf16_tflops" in peaks else "fallback",
-                     "traffic": traffic_record(traffic_key(args), PREFILL_SOURCES),
+                     "traffic": traffic_record(traffic_key(args), PREFILL_SOURCES,
+                                               alg_bytes=prefill_bytes(case, res["Tq"])),
                      "algorithmic_flops_per_launch": int(res["flops_rank"]),
                      "algorithmic_bytes_per_launch": prefill_bytes(case, res["Tq"]),
                      "avg_launch_ms": round(res["kms"], 4),
@@ -1348,7 +1353,7 @@ def main():
     dec_med_ms = statistics.median(res["dec_ms"])
     achieved = res["dec_bytes"] / (dec_avg_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
-    traffic = traffic_record(traffic_key(args))
+    traffic = traffic_record(traffic_key(args), alg_bytes=res["dec_bytes"])
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -1433,7 +1438,8 @@ def also_summary(res, args, peak) -> dict:
                                    else "attention_kernel (dattn_decode)"),
                         "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                         "frac": round(achieved / peak, 4),
-                        "traffic": traffic_record(traffic_key(args)),
+                        "traffic": traffic_record(traffic_key(args),
+                                                  alg_bytes=res["dec_bytes"]),
                         "algorithmic_bytes_per_launch": int(res["dec_bytes"]),
                         "avg_launch_us": round(dec_avg_ms * 1e3, 2),
                         "median_launch_us": round(statistics.median(res["dec_ms"]) * 1e3, 2),

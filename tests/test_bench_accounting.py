@@ -118,6 +118,24 @@ def test_traffic_records_apply_to_full_size_runs_of_their_own_kernel():
     assert bench.traffic_record("mha-32k", bench.PREFILL_SOURCES) is None
 
 
+def test_traffic_records_scale_to_the_run_by_their_ratio():
+    """A record's DRAM/algorithmic ratio (taken on a reduced case) scales to a run's launch
+    by that run's algorithmic bytes."""
+    import json
+    recs = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    for key, rec in recs.items():
+        if key.startswith("_"):
+            continue
+        assert 0.8 < rec["ratio_to_algorithmic"] < 1.1, key
+        want = round(rec["captured_dram_bytes_per_launch"] /
+                     rec["captured_algorithmic_bytes_per_launch"], 4)
+        assert rec["ratio_to_algorithmic"] == want, key
+    rec = recs["mha-32k"]
+    if rec["source_hash"] == bench.kernel_source_hash():  # else the record is stale: null
+        assert bench.traffic_record("mha-32k", alg_bytes=10**9) == round(
+            rec["ratio_to_algorithmic"] * 10**9)
+
+
 def test_prefill_cpu_sample_is_bounded_and_covers_rows_once():
     oracle.build_oracle()
     case = W.prefill_32k(seed=0, L=640)
