@@ -350,7 +350,7 @@ def _check_selection(case, cache, q, sel):
     (64, 128, [64 * 600, 64 * 300 + 1], 256, 0),  # the largest top_k
     (128, 64, [128 * 40 + 77, 129], 1, 2),  # top-1
 ])
-def test_page_select_bit_exact(P, d, lens, top_k, splits):
+def test_page_select_matches_fp64_scores(P, d, lens, top_k, splits):
     _lib()
     case = W.Case("sel", B=len(lens), Hq=16, Hkv=4, d=d, P=P, lens=lens, seed=P + d + top_k,
                   head_kind=[1, 2, 1, 0], top_k=top_k, n_highsim=8)
@@ -459,7 +459,7 @@ def test_decode_length_beyond_table_is_flagged_and_clamped():
 
 @pytest.mark.parametrize("Hq,Hkv,d,P", [(16, 2, 128, 64), (8, 8, 128, 16), (24, 3, 64, 64),
                                        (8, 1, 64, 128)])
-def test_page_select_bit_exact_group_sizes(Hq, Hkv, d, P):
+def test_page_select_matches_fp64_scores_group_sizes(Hq, Hkv, d, P):
     """GQA groups of 8 (8-channel chunks), 1 and 3, and 128-token pages (8 logical pages)."""
     _lib()
     kinds = [1] * Hkv
