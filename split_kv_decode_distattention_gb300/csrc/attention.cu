@@ -888,69 +888,6 @@ struct Consumer {
         pv_i4(st + 8u * D, p0 * vn0, p1 * vn0, p2 * vn1, p3 * vn1);
     }
 
-    // Online softmax (base 2) over two tiles' logits at once (s[0..3] tile A, s[4..7] tile B,
-    // in softmax()'s order): one reduction of the running max for 32 rows.
-    __device__ __forceinline__ void softmax2(const float (&s)[8], float (&pr)[8]) {
-        float c0 = fmaxf(fmaxf(s[0], s[2]), fmaxf(s[4], s[6]));
-        float c1 = fmaxf(fmaxf(s[1], s[3]), fmaxf(s[5], s[7]));
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            c0 = fmaxf(c0, __shfl_xor_sync(0xffffffffu, c0, off));
-            c1 = fmaxf(c1, __shfl_xor_sync(0xffffffffu, c1, off));
-        }
-        const float mn0 = fmaxf(m0, c0), mn1 = fmaxf(m1, c1);
-        const float mu0 = mn0 == kNegInf ? 0.f : mn0, mu1 = mn1 == kNegInf ? 0.f : mn1;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) pr[i] = ex2_approx(s[i] - ((i & 1) ? mu1 : mu0));
-        if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
-            const float al0 = ex2_approx(m0 - mu0), al1 = ex2_approx(m1 - mu1);
-            e0 *= al0;
-            e1 *= al1;
-#pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
-            }
-        }
-        m0 = mn0;
-        m1 = mn1;
-        e0 += (pr[0] + pr[2]) + (pr[4] + pr[6]);
-        e1 += (pr[1] + pr[3]) + (pr[5] + pr[7]);
-    }
-
-    // Two consecutive tiles A and B of the 4-bit pool with one softmax and one V-scale
-    // update: the same results as tile_i4 on A, then on B, up to rounding order.
-    __device__ void tile2_i4(uint32_t stA, const float* scA, int loA, int hiA, int cutA,
-                             uint32_t stB, const float* scB, int loB, int hiB, int cutB) {
-        const int g8 = lane >> 2;
-        float saA[4] = {0.f, 0.f, 0.f, 0.f}, sbA[4] = {0.f, 0.f, 0.f, 0.f};
-        float saB[4] = {0.f, 0.f, 0.f, 0.f}, sbB[4] = {0.f, 0.f, 0.f, 0.f};
-        qk_i4(stA, saA, sbA);
-        qk_i4(stB, saB, sbB);
-        bool a0, a1, a2, a3, b0, b1, b2, b3;
-        visible(loA, hiA, cutA, a0, a1, a2, a3);
-        visible(loB, hiB, cutB, b0, b1, b2, b3);
-        const float kA0 = scA[g8] * qsc, kA1 = scA[g8 + 8] * qsc;
-        const float kB0 = scB[g8] * qsc, kB1 = scB[g8 + 8] * qsc;
-        const float s[8] = {a0 ? (saA[0] + sbA[0]) * kA0 : kNegInf,
-                            a1 ? (saA[1] + sbA[1]) * kA0 : kNegInf,
-                            a2 ? (saA[2] + sbA[2]) * kA1 : kNegInf,
-                            a3 ? (saA[3] + sbA[3]) * kA1 : kNegInf,
-                            b0 ? (saB[0] + sbB[0]) * kB0 : kNegInf,
-                            b1 ? (saB[1] + sbB[1]) * kB0 : kNegInf,
-                            b2 ? (saB[2] + sbB[2]) * kB1 : kNegInf,
-                            b3 ? (saB[3] + sbB[3]) * kB1 : kNegInf};
-        float pr[8];
-        softmax2(s, pr);
-        const float vA0 = g8 >= loA && g8 < hiA ? scA[16 + g8] : 0.f;
-        const float vA1 = g8 + 8 >= loA && g8 + 8 < hiA ? scA[24 + g8] : 0.f;
-        const float vB0 = g8 >= loB && g8 < hiB ? scB[16 + g8] : 0.f;
-        const float vB1 = g8 + 8 >= loB && g8 + 8 < hiB ? scB[24 + g8] : 0.f;
-        raise_r(warp_vmax(fmaxf(fmaxf(vA0, vA1), fmaxf(vB0, vB1))));
-        const float nA0 = vA0 * inv, nA1 = vA1 * inv, nB0 = vB0 * inv, nB1 = vB1 * inv;
-        pv_i4(stA + 8u * D, pr[0] * nA0, pr[1] * nA0, pr[2] * nA1, pr[3] * nA1);
-        pv_i4(stB + 8u * D, pr[4] * nB0, pr[5] * nB0, pr[6] * nB1, pr[7] * nB1);
-    }
-
     // Publishes this warp's state for the CTA-level merge of the piece.
     __device__ void publish() {
         float t0 = e0, t1 = e1;
@@ -1046,13 +983,14 @@ __device__ void append_new_tokens(const AttnParams& p, const Smem& sm, int32_t c
     }
 }
 
-// Resident CTAs per SM the register budget is held to: three at d = 128, four at d = 64
-// (the 4-bit kernel processes tiles in pairs and would otherwise take more registers).
-template <int D>
-constexpr int attn_min_blocks() { return D == 64 ? 4 : 3; }
+// Resident CTAs per SM the register budget is held to: three at d = 128, four at d = 64 and
+// for the 4-bit pool, whose consumers bind it (96 registers; it fetches each piece's query at
+// the piece's start instead of during the previous piece, which frees 16 of them).
+template <int D, int FMT>
+constexpr int attn_min_blocks() { return (D == 64 || FMT == DATTN_KV_INT4) ? 4 : 3; }
 
 template <int D, int FMT>
-__global__ void __launch_bounds__(kAttnThreads, attn_min_blocks<D>())
+__global__ void __launch_bounds__(kAttnThreads, attn_min_blocks<D, FMT>())
 attention_kernel(const __grid_constant__ AttnParams p,
                  const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v,
@@ -1388,14 +1326,20 @@ attention_kernel(const __grid_constant__ AttnParams p,
     bool have = true;
     uint32_t qn[Consumer<D, FMT>::KS][2];
     float qsn = 0.f;
-    cons.load_q(pc.s, qn, qsn);
+    // the 4-bit pool fetches each piece's query at its start (registers for four CTAs per SM)
+    constexpr bool kPrefetchQ = FMT != DATTN_KV_INT4;
+    if constexpr (kPrefetchQ) cons.load_q(pc.s, qn, qsn);
     while (have) {
+        if constexpr (kPrefetchQ) {
 #pragma unroll
-        for (int ks = 0; ks < Consumer<D, FMT>::KS; ++ks) {
-            cons.qf[ks][0] = qn[ks][0];
-            cons.qf[ks][1] = qn[ks][1];
+            for (int ks = 0; ks < Consumer<D, FMT>::KS; ++ks) {
+                cons.qf[ks][0] = qn[ks][0];
+                cons.qf[ks][1] = qn[ks][1];
+            }
+            cons.qsc = qsn;
+        } else {
+            cons.load_q(pc.s, cons.qf, cons.qsc);
         }
-        cons.qsc = qsn;
         // the next piece's query is fetched while this piece streams (only its cursor stays
         // live; the piece is looked up again at the switch)
         int32_t cur2 = cur;
@@ -1404,7 +1348,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
         {
             Piece nx;
             have2 = pieces.piece(cur2, nx);
-            if (have2) cons.load_q(nx.s, qn, qsn);
+            if (kPrefetchQ && have2) cons.load_q(nx.s, qn, qsn);
         }
         // with the fused append, this lane's chunk of the segment's new K / V row (the tile
         // that holds the new token gets it written into its row)
@@ -1416,49 +1360,8 @@ attention_kernel(const __grid_constant__ AttnParams p,
         if constexpr (FMT == DATTN_KV_MIXED) cons.i4 = head_is_i4(p.hf, pc.s % p.Hkv);
         const int32_t s = pc.s;
         const int32_t nr = pc.r1 - pc.r0;
-        if constexpr (FMT == DATTN_KV_INT4) {
-            // Tiles go to the warps in pairs: pair P holds the tiles 2P and 2P + 1 of the CTA's
-            // sequence, and warp P mod 4 takes it, so (the ring being a multiple of 8 stages)
-            // every stage keeps one owner. Both tiles of a pair inside this piece share one
-            // softmax and one V-scale update; a pair cut by the piece boundary is processed
-            // as the single tile this piece holds.
-            static_assert(NS % (2 * kConsumerWarps) == 0, "pairs of stages per consumer warp");
-            const int32_t k1 = kbase + nr;
-            int32_t P = kbase >> 1;
-            P += (warp - P % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
-            for (; 2 * P < k1; P += kConsumerWarps) {
-                const int32_t ka = 2 * P, kb = 2 * P + 1;
-                const bool ina = ka >= kbase, inb = kb < k1;
-                const int ga = ka % NS, gb = kb % NS;
-                bool oka = true, okb = true;
-                if (ina)
-                    oka = mbar_wait(sm.full_bar(ga), (ka / NS) & 1, sm.abort_flag(), p.dev_err);
-                if (inb)
-                    okb = mbar_wait(sm.full_bar(gb), (kb / NS) & 1, sm.abort_flag(), p.dev_err);
-                // warp-uniform: the tiles' ldmatrix / mma / movmatrix are warp-collective
-                const bool ok = __all_sync(0xffffffffu, oka && okb);
-                const int32_t la = ina ? sm.meta()[ga] : kTileSkip;
-                const int32_t lb = inb ? sm.meta()[gb] : kTileSkip;
-                const bool da = ok && !(la & kTileSkip), db = ok && !(lb & kTileSkip);
-                const uint32_t sta = stage0 + (uint32_t)ga * sm.L.stage_bytes;
-                const uint32_t stb = stage0 + (uint32_t)gb * sm.L.stage_bytes;
-                if (da && db) {
-                    cons.tile2_i4(sta, sm.scales(ga), tile_lo(la), tile_hi(la), tile_cut(la), stb,
-                                  sm.scales(gb), tile_lo(lb), tile_hi(lb), tile_cut(lb));
-                } else if (da) {
-                    cons.tile_i4(sta, sm.scales(ga), tile_lo(la), tile_hi(la), tile_cut(la));
-                } else if (db) {
-                    cons.tile_i4(stb, sm.scales(gb), tile_lo(lb), tile_hi(lb), tile_cut(lb));
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    if (ina) mbar_arrive(sm.empty_bar(ga));
-                    if (inb) mbar_arrive(sm.empty_bar(gb));
-                }
-            }
-        }
         for (int32_t i = (warp - kbase % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
-             FMT != DATTN_KV_INT4 && i < nr; i += kConsumerWarps) {
+             i < nr; i += kConsumerWarps) {
             const int32_t k = kbase + i;
             const int stg = k % NS;
             // warp-uniform: the tile's ldmatrix / mma / movmatrix are warp-collective
@@ -1471,6 +1374,9 @@ attention_kernel(const __grid_constant__ AttnParams p,
                     const uint32_t st = stage0 + (uint32_t)stg * sm.L.stage_bytes;
                     if (lohi & kTileI4) cons.tile_i4(st, sm.scales(stg), lo, hi, cut);
                     else                cons.tile_f8(st, sm.scales(stg), lo, hi, cut);
+                } else if constexpr (FMT == DATTN_KV_INT4) {
+                    cons.tile_i4(stage0 + (uint32_t)stg * sm.L.stage_bytes, sm.scales(stg), lo, hi,
+                                 cut);
                 } else if constexpr (Q) {
                     cons.tile_f8(stage0 + (uint32_t)stg * sm.L.stage_bytes, sm.scales(stg), lo, hi,
                                  cut);

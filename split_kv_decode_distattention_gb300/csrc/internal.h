@@ -15,10 +15,11 @@ constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
 // so it has depth/4 - 1 tiles loading while it works on one. The 8-bit stages are half as
 // large; 12 of them (48 KB for d = 128) keep more bytes in flight per warp without lowering
 // the CTAs per SM, which 16 stages did for grouped heads. The 4-bit stages are a quarter as
-// large, and 24 of them take about the shared memory of the 8-bit ring.
+// large; the 4-bit kernel runs four CTAs per SM (its consumers, not HBM, bound it, and more
+// warps hide their latency), and 16 stages (32 KB) let the four fit in shared memory.
 constexpr int kStagesBf16 = 8;
 constexpr int kStagesF8 = 12;
-constexpr int kStagesI4 = 24;
+constexpr int kStagesI4 = 16;
 // The mixed pool's stages are 8-bit stages; a 4-bit tile fills half of one.
 __host__ __device__ constexpr int attn_stages(int fmt) {
     return fmt == DATTN_KV_INT4 ? kStagesI4
