@@ -467,6 +467,10 @@ struct Consumer {
     int32_t rk;    // 8-bit pool: r = 2^rk bounds the V scales seen in this piece
     float rv, inv;  // 8-bit pool: r and 2^15 / r
     bool i4 = I4;   // the current piece's KV head is 4-bit (set per piece in a mixed pool)
+    // 4-bit pool: 8 * 2^-24 * (sum of the query) of this lane's columns 2tig, 2tig + 1, and
+    // the running sums of this lane's PV weights of those columns (see tile_i4)
+    float qc[2] = {0.f, 0.f};
+    float ws0 = 0.f, ws1 = 0.f;
 
     __device__ Consumer(const AttnParams& p_, const Smem& sm_, int w, int l)
         : p(p_), sm(sm_), warp(w), lane(l) {}
@@ -492,7 +496,7 @@ struct Consumer {
     // B fragments of the segment's query columns for segment s (column n = lane / 4 is query
     // token n / g of query head kvh*g + n % g), and the factor that turns a raw dot product
     // into a base-2 logit.
-    __device__ void load_q(int32_t s, uint32_t (&dst)[KS][2], float& qs) const {
+    __device__ void load_q(int32_t s, uint32_t (&dst)[KS][2], float& qs, float (&qcs)[2]) const {
         const int32_t item = s / p.Hkv, kvh = s - item * p.Hkv;
         int32_t b = item;
         if (p.mode == MODE_PARTIAL) b = __ldg(p.chunk_req + item);
@@ -508,6 +512,7 @@ struct Consumer {
                 dst[ks][1] = ok ? __ldg(qv + ks * 8 + 4 + tig) : 0u;
             }
             qs = p.sl2;
+            qcs[0] = qcs[1] = 0.f;
         } else {
             // The channels come in the order the quantized K fragment brings them.
             // 8-bit: k-step ks covers channels 16ks..16ks+15, b0 = 16ks + 4tig + {0, 1},
@@ -540,13 +545,28 @@ struct Consumer {
             if (mx > 0.f) a = min(127, max(-113, 14 - (((__float_as_int(mx) >> 23) & 0xff) - 127)));
             const float up = __int_as_float((127 + a) << 23);
             const float down = a < 127 ? __int_as_float((127 - a) << 23) : 5.877471754e-39f;
+            // 4-bit: b1 meets the odd nibbles, which convert to 16 n * 2^-24 (i4pair_raw), so
+            // its query values are divided by 16 (exact for elements within 2^24 of the
+            // largest); qsum adds the values the products use, each odd one times 16
+            const float up1 = f4 ? up * 0.0625f : up;
+            float qsum = 0.f;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    dst[ks][j] = pack_f16(bf16_lo(dst[ks][j]) * up, bf16_hi(dst[ks][j]) * up);
+                dst[ks][0] = pack_f16(bf16_lo(dst[ks][0]) * up, bf16_hi(dst[ks][0]) * up);
+                dst[ks][1] = pack_f16(bf16_lo(dst[ks][1]) * up1, bf16_hi(dst[ks][1]) * up1);
+                if (f4)
+                    qsum += (f16_lo(dst[ks][0]) + f16_hi(dst[ks][0])) +
+                            16.f * (f16_lo(dst[ks][1]) + f16_hi(dst[ks][1]));
             }
             qs = p.sl2 * down;
+            qcs[0] = qcs[1] = 0.f;
+            if (f4) {
+                // the sum of column g8 over its four lanes, then columns 2tig, 2tig + 1
+                qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+                qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+                qcs[0] = __shfl_sync(0xffffffffu, qsum, 8 * tig) * 4.76837158203125e-07f;
+                qcs[1] = __shfl_sync(0xffffffffu, qsum, 8 * tig + 4) * 4.76837158203125e-07f;
+            }
         }
     }
 
@@ -578,6 +598,7 @@ struct Consumer {
         for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
         m0 = m1 = kNegInf;
         e0 = e1 = 0.f;
+        ws0 = ws1 = 0.f;
         rk = -112;
         rv = __int_as_float((127 - 112) << 23);
         inv = __int_as_float((142 + 112) << 23);
@@ -603,6 +624,10 @@ struct Consumer {
             const float al0 = ex2_approx(m0 - mu0), al1 = ex2_approx(m1 - mu1);
             e0 *= al0;
             e1 *= al1;
+            if constexpr (I4 || MIX) {
+                ws0 *= al0;
+                ws1 *= al1;
+            }
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
@@ -783,14 +808,14 @@ struct Consumer {
         for (int c = 0; c < D / 64; ++c) {
             uint32_t r0, r1, r2, r3;  // chunk 2c: tokens g8, g8 + 8; chunk 2c + 1: the same
             ldsm_x4(kbase + swz_rows<RB>(row, 2u * c + csel), r0, r1, r2, r3);
-            mma_f16(sa, i4pair_to_f16<0>(r0), i4pair_to_f16<0>(r1), i4pair_to_f16<1>(r0),
-                    i4pair_to_f16<1>(r1), qf[4 * c][0], qf[4 * c][1]);
-            mma_f16(sb, i4pair_to_f16<2>(r0), i4pair_to_f16<2>(r1), i4pair_to_f16<3>(r0),
-                    i4pair_to_f16<3>(r1), qf[4 * c + 1][0], qf[4 * c + 1][1]);
-            mma_f16(sa, i4pair_to_f16<0>(r2), i4pair_to_f16<0>(r3), i4pair_to_f16<1>(r2),
-                    i4pair_to_f16<1>(r3), qf[4 * c + 2][0], qf[4 * c + 2][1]);
-            mma_f16(sb, i4pair_to_f16<2>(r2), i4pair_to_f16<2>(r3), i4pair_to_f16<3>(r2),
-                    i4pair_to_f16<3>(r3), qf[4 * c + 3][0], qf[4 * c + 3][1]);
+            mma_f16(sa, i4pair_raw<0>(r0), i4pair_raw<0>(r1), i4pair_raw<1>(r0),
+                    i4pair_raw<1>(r1), qf[4 * c][0], qf[4 * c][1]);
+            mma_f16(sb, i4pair_raw<2>(r0), i4pair_raw<2>(r1), i4pair_raw<3>(r0),
+                    i4pair_raw<3>(r1), qf[4 * c + 1][0], qf[4 * c + 1][1]);
+            mma_f16(sa, i4pair_raw<0>(r2), i4pair_raw<0>(r3), i4pair_raw<1>(r2),
+                    i4pair_raw<1>(r3), qf[4 * c + 2][0], qf[4 * c + 2][1]);
+            mma_f16(sb, i4pair_raw<2>(r2), i4pair_raw<2>(r3), i4pair_raw<3>(r2),
+                    i4pair_raw<3>(r3), qf[4 * c + 3][0], qf[4 * c + 3][1]);
         }
     }
 
@@ -806,6 +831,8 @@ struct Consumer {
             for (int mt = 0; mt < KS; ++mt) {
                 o[mt][0] *= f; o[mt][1] *= f; o[mt][2] *= f; o[mt][3] *= f;
             }
+            ws0 *= f;
+            ws1 *= f;
             rk = k;
             rv = __int_as_float((127 + k) << 23);
             inv = __int_as_float((142 - k) << 23);
@@ -834,26 +861,26 @@ struct Consumer {
             uint32_t r0, r1, r2, r3;
             ldsm_x4_trans(vbase + swz_rows<RB>(row, 2u * c + csel), r0, r1, r2, r3);
             {
-                const uint32_t x0 = i4pair_to_f16<0>(r0), x1 = i4pair_to_f16<1>(r0);
-                const uint32_t x2 = i4pair_to_f16<0>(r1), x3 = i4pair_to_f16<1>(r1);
+                const uint32_t x0 = i4pair_raw<0>(r0), x1 = i4pair_raw<1>(r0);
+                const uint32_t x2 = i4pair_raw<0>(r1), x3 = i4pair_raw<1>(r1);
                 mma_f16(o[4 * c], x0, x1, x2, x3, bh0, bh1);
                 mma_f16(o[4 * c], x0, x1, x2, x3, bl0, bl1);
             }
             {
-                const uint32_t x0 = i4pair_to_f16<2>(r0), x1 = i4pair_to_f16<3>(r0);
-                const uint32_t x2 = i4pair_to_f16<2>(r1), x3 = i4pair_to_f16<3>(r1);
+                const uint32_t x0 = i4pair_raw<2>(r0), x1 = i4pair_raw<3>(r0);
+                const uint32_t x2 = i4pair_raw<2>(r1), x3 = i4pair_raw<3>(r1);
                 mma_f16(o[4 * c + 1], x0, x1, x2, x3, bh0, bh1);
                 mma_f16(o[4 * c + 1], x0, x1, x2, x3, bl0, bl1);
             }
             {
-                const uint32_t x0 = i4pair_to_f16<0>(r2), x1 = i4pair_to_f16<1>(r2);
-                const uint32_t x2 = i4pair_to_f16<0>(r3), x3 = i4pair_to_f16<1>(r3);
+                const uint32_t x0 = i4pair_raw<0>(r2), x1 = i4pair_raw<1>(r2);
+                const uint32_t x2 = i4pair_raw<0>(r3), x3 = i4pair_raw<1>(r3);
                 mma_f16(o[4 * c + 2], x0, x1, x2, x3, bh0, bh1);
                 mma_f16(o[4 * c + 2], x0, x1, x2, x3, bl0, bl1);
             }
             {
-                const uint32_t x0 = i4pair_to_f16<2>(r2), x1 = i4pair_to_f16<3>(r2);
-                const uint32_t x2 = i4pair_to_f16<2>(r3), x3 = i4pair_to_f16<3>(r3);
+                const uint32_t x0 = i4pair_raw<2>(r2), x1 = i4pair_raw<3>(r2);
+                const uint32_t x2 = i4pair_raw<2>(r3), x3 = i4pair_raw<3>(r3);
                 mma_f16(o[4 * c + 3], x0, x1, x2, x3, bh0, bh1);
                 mma_f16(o[4 * c + 3], x0, x1, x2, x3, bl0, bl1);
             }
@@ -867,7 +894,12 @@ struct Consumer {
         return v;
     }
 
-    // One tile of the 4-bit pool; rows are masked as in tile().
+    // One tile of the 4-bit pool; rows are masked as in tile(). The codes enter the products
+    // as n * 2^-24 (n = code + 8; odd nibbles 16 n * 2^-24 against a query divided by 16), so
+    // the raw products are 2^-24 (q' . n): the logit subtracts 8 * 2^-24 * (sum of q') (qc)
+    // and scales by 2^24; the PV accumulator's offset, 8 * 2^-24 * (sum of the weights), is
+    // taken out when the piece is published (ws0, ws1 keep those sums). Both corrections are
+    // of the size of the values they correct, so nothing cancels catastrophically.
     __device__ void tile_i4(uint32_t st, const float* sc, int lo, int hi, int cut) {
         const int g8 = lane >> 2;
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
@@ -876,16 +908,20 @@ struct Consumer {
         const float kc0 = sc[g8] * qsc, kc1 = sc[g8 + 8] * qsc;
         bool a0, a1, a2, a3;
         visible(lo, hi, cut, a0, a1, a2, a3);
-        const float s0 = a0 ? (sa[0] + sb[0]) * kc0 : kNegInf;
-        const float s1 = a1 ? (sa[1] + sb[1]) * kc0 : kNegInf;
-        const float s2 = a2 ? (sa[2] + sb[2]) * kc1 : kNegInf;
-        const float s3 = a3 ? (sa[3] + sb[3]) * kc1 : kNegInf;
+        constexpr float k24 = 16777216.f;  // 2^24
+        const float s0 = a0 ? ((sa[0] + sb[0]) - qc[0]) * k24 * kc0 : kNegInf;
+        const float s1 = a1 ? ((sa[1] + sb[1]) - qc[1]) * k24 * kc0 : kNegInf;
+        const float s2 = a2 ? ((sa[2] + sb[2]) - qc[0]) * k24 * kc1 : kNegInf;
+        const float s3 = a3 ? ((sa[3] + sb[3]) - qc[1]) * k24 * kc1 : kNegInf;
         float p0, p1, p2, p3;
         softmax(s0, s1, s2, s3, p0, p1, p2, p3);
         const float vs0 = v0 ? sc[16 + g8] : 0.f, vs1 = v1 ? sc[24 + g8] : 0.f;
         raise_r(warp_vmax(fmaxf(vs0, vs1)));
         const float vn0 = vs0 * inv, vn1 = vs1 * inv;  // in [0, 2^15], exact
-        pv_i4(st + 8u * D, p0 * vn0, p1 * vn0, p2 * vn1, p3 * vn1);
+        const float w0 = p0 * vn0, w1 = p1 * vn0, w2 = p2 * vn1, w3 = p3 * vn1;
+        ws0 += w0 + w2;
+        ws1 += w1 + w3;
+        pv_i4(st + 8u * D, w0, w1, w2, w3);
     }
 
     // Publishes this warp's state for the CTA-level merge of the piece.
@@ -914,18 +950,32 @@ struct Consumer {
             }
         } else {
             const float rs = rv * 3.0517578125e-05f;  // r * 2^-15, exact
+            const bool f4 = MIX ? i4 : I4;
+            // 4-bit: row g8 of an m-tile (an even nibble) holds 2^-24 (sum of w n), row g8 + 8
+            // (an odd nibble) 16 times that; 8 * (sum of w) is the offset of n = code + 8
+            float b0 = 0.f, b1 = 0.f;
+            if (f4) {
+                float W0 = ws0, W1 = ws1;
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    W0 += __shfl_xor_sync(0xffffffffu, W0, off);
+                    W1 += __shfl_xor_sync(0xffffffffu, W1, off);
+                }
+                b0 = 8.f * W0;
+                b1 = 8.f * W1;
+            }
+            const float ke = f4 ? 16777216.f : 1.f, ko = f4 ? 1048576.f : 1.f;  // 2^24, 2^20
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 // rows g8 and g8 + 8 of m-tile mt are channels dd and dd + 1 (4-bit: m-tile
                 // mt covers channels 32 (mt / 2) + 4 g8 + 2 (mt % 2) + {0, 1}, see tile_i4)
-                const int dd = (MIX ? i4 : I4) ? 32 * (mt >> 1) + 4 * g8 + 2 * (mt & 1)
-                                               : mt * 16 + 2 * g8;
+                const int dd = f4 ? 32 * (mt >> 1) + 4 * g8 + 2 * (mt & 1) : mt * 16 + 2 * g8;
                 if (hA < p.gq)
                     *reinterpret_cast<float2*>(wo + hA * D + dd) =
-                        make_float2(o[mt][0] * rs, o[mt][2] * rs);
+                        make_float2((o[mt][0] * ke - b0) * rs, (o[mt][2] * ko - b0) * rs);
                 if (hB < p.gq)
                     *reinterpret_cast<float2*>(wo + hB * D + dd) =
-                        make_float2(o[mt][1] * rs, o[mt][3] * rs);
+                        make_float2((o[mt][1] * ke - b1) * rs, (o[mt][3] * ko - b1) * rs);
             }
         }
     }
@@ -1328,7 +1378,8 @@ attention_kernel(const __grid_constant__ AttnParams p,
     float qsn = 0.f;
     // the 4-bit pool fetches each piece's query at its start (registers for four CTAs per SM)
     constexpr bool kPrefetchQ = FMT != DATTN_KV_INT4;
-    if constexpr (kPrefetchQ) cons.load_q(pc.s, qn, qsn);
+    float qcn[2] = {0.f, 0.f};
+    if constexpr (kPrefetchQ) cons.load_q(pc.s, qn, qsn, qcn);
     while (have) {
         if constexpr (kPrefetchQ) {
 #pragma unroll
@@ -1337,8 +1388,10 @@ attention_kernel(const __grid_constant__ AttnParams p,
                 cons.qf[ks][1] = qn[ks][1];
             }
             cons.qsc = qsn;
+            cons.qc[0] = qcn[0];
+            cons.qc[1] = qcn[1];
         } else {
-            cons.load_q(pc.s, cons.qf, cons.qsc);
+            cons.load_q(pc.s, cons.qf, cons.qsc, cons.qc);
         }
         // the next piece's query is fetched while this piece streams (only its cursor stays
         // live; the piece is looked up again at the switch)
@@ -1348,7 +1401,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
         {
             Piece nx;
             have2 = pieces.piece(cur2, nx);
-            if (kPrefetchQ && have2) cons.load_q(nx.s, qn, qsn);
+            if (kPrefetchQ && have2) cons.load_q(nx.s, qn, qsn, qcn);
         }
         // with the fused append, this lane's chunk of the segment's new K / V row (the tile
         // that holds the new token gets it written into its row)

@@ -276,27 +276,15 @@ __device__ __forceinline__ uint32_t swz_rows(uint32_t row, uint32_t chunk) {
 }
 
 // The 4-bit codes at nibble K of each 16-bit half of x (bits 4K..4K+3 and 16+4K..16+4K+3,
-// each code stored as n = code + 8) as two exact fp16 values. Nibbles 2 and 3 are first
-// shifted down by 8 bits (one shift serves both). A nibble in bits 0-3 ORed into 0x6400 is
-// the fp16 value 1024 + n, and subtracting 1032 leaves n - 8. A nibble in bits 4-7 ORed into
-// 0x6400 is 1024 + 16n, and (1024 + 16n) / 16 - 72 = n - 8 in one fused multiply-add. Every
-// step is exact: the values are integers well inside fp16's 11-bit significand.
+// each code stored as n = code + 8) as two fp16 subnormals: nibbles 0 and 2 (2 and 3 are first
+// shifted down by 8 bits, one shift serving both) masked in place are n * 2^-24, nibbles 1
+// and 3 are 16 n * 2^-24. Every value is exact; the factor 16 and the offset 8 are taken out
+// by the caller (the query of an odd nibble is divided by 16, and 8 times the sum of the
+// other operand is subtracted from the products).
 template <int K>
-__device__ __forceinline__ uint32_t i4pair_to_f16(uint32_t x) {
+__device__ __forceinline__ uint32_t i4pair_raw(uint32_t x) {
     const uint32_t y = K >= 2 ? x >> 8 : x;
-    // (y & mask) | 0x6400 in both halves as one three-input logic operation (LUT 0xEA)
-    uint32_t v;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;"
-        : "=r"(v)
-        : "r"(y), "r"((K & 1) == 0 ? 0x000f000fu : 0x00f000f0u), "r"(0x64006400u));
-    uint32_t r;
-    if constexpr ((K & 1) == 0) {
-        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x64086408u));
-    } else {
-        // 0x2C00 = 1/16, 0xD480 = -72
-        asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(0x2C002C00u), "r"(0xD480D480u));
-    }
-    return r;
+    return y & ((K & 1) == 0 ? 0x000f000fu : 0x00f000f0u);
 }
 
 // Programmatic dependent launch: a kernel launched with programmatic stream serialization may
