@@ -1,10 +1,11 @@
 """Benchmark of the split-KV decode path on GB300.
 
 One step is one decode layer-step of the whole batch through the library's C ABI:
-  dense workloads:  dattn_append_decode (one new token per request appended and attended
-                    in one launch: split-KV MicroAttention partials plus the in-launch
-                    merge); with a quantized pool, or --unfused, dattn_kv_append then
-                    dattn_decode;
+  dense workloads:  dattn_kv_append (one new token per request), then dattn_decode
+                    (split-KV MicroAttention partials plus the in-launch merge), the second
+                    launch overlapping the first's tail (programmatic dependent launch);
+                    --fused times dattn_append_decode instead (the two in one launch),
+                    which measures slower on GB300; --queries T: dattn_decode_multi;
   sparse-512k:      the same, plus dattn_page_select at the start of every reuse window.
 The metric is achieved HBM bandwidth in GB/s: the algorithmic bytes of the step (valid K/V
 read, statistics scanned, new tokens written, queries, outputs, block table) divided by
@@ -91,9 +92,9 @@ def parse_args():
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling only)")
     ap.add_argument("--ctx", type=int, default=0, help="override the context (profiling only)")
     ap.add_argument("--num-splits", type=int, default=0)
-    ap.add_argument("--unfused", action="store_true",
-                    help="step = dattn_kv_append then dattn_decode (two launches) instead of "
-                         "dattn_append_decode (bf16 pool, one query token)")
+    ap.add_argument("--fused", action="store_true",
+                    help="step = dattn_append_decode (the append and the decode in one launch) "
+                         "instead of dattn_kv_append then dattn_decode")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--also", default="auto",
                     help="a second workload timed after the first and summarised in the same "
@@ -117,9 +118,12 @@ def info_steps(args) -> int:
 
 
 def fused_step(args) -> bool:
-    """A step is one dattn_append_decode launch (the bf16 pool, one query token per request)
-    unless --unfused asks for dattn_kv_append then dattn_decode."""
-    return not args.unfused and args.kv_format == "bf16" and args.queries == 1
+    """A step is dattn_kv_append then dattn_decode (two launches), unless --fused asks for
+    one dattn_append_decode launch (one query token per request, any pool format). On GB300
+    the two launches measure faster: the append kernel's tail overlaps the decode's prologue,
+    while the fused launch's heavier kernel (its append work and the new tokens' patches)
+    costs more than the launch it saves."""
+    return args.fused and args.queries == 1
 
 
 def make_case(args):

@@ -317,7 +317,8 @@ dattn_status_t dattn_decode_multi(const dattn_kv_layout *layout, const void *k_p
 
 /*
  * One decode step with its append, in one launch: exactly dattn_kv_append of one new token
- * per request (T = 1) followed by dattn_decode, for the bf16 pool. [LS §4.2: the master saves
+ * per request (T = 1) followed by dattn_decode, for every pool format (a quantized pool
+ * stores the new rows quantized exactly as dattn_kv_append does). [LS §4.2: the master saves
  * the new token's KV locally, then every instance attends over its KV including it.] The new
  * token of request b is written at position seq_lens[b] (and the logical-page statistics take
  * it in when stats is not NULL); the decode attends tokens 0 .. seq_lens[b] (the new one
@@ -329,7 +330,6 @@ dattn_status_t dattn_decode_multi(const dattn_kv_layout *layout, const void *k_p
  *   q, scale, sparse, num_splits, out, m_g, e_g  as for dattn_decode
  *   seq_lens (device) int32 [B]: lengths before the step; advanced by one
  *   ws, ws_bytes  workspace of at least dattn_workspace_size(B, Hq, Hkv, d, 0, num_splits)
- * A quantized pool (kv_format != DATTN_KV_BF16) returns DATTN_ERR_UNSUPPORTED.
  */
 dattn_status_t dattn_append_decode(const dattn_kv_layout *layout, void *k_pool, void *v_pool,
                                    dattn_bf16 *stats, const dattn_bf16 *k_new,

@@ -439,7 +439,8 @@ def dattn_append_decode(layout: KVLayout, k_pool, v_pool, stats, k_new, v_new, q
                         sparse: SparseConfig | None = None, num_splits=0, dev_err=None,
                         stream=None):
     """dattn_kv_append of one token per request (k_new/v_new bf16 [B][1][Hkv][d]) and
-    dattn_decode over the advanced lengths, in one launch (bf16 pool): out fp32 [B][Hq][d]
+    dattn_decode over the advanced lengths, in one launch (any pool format; a quantized pool
+    stores the new rows quantized as dattn_kv_append would): out fp32 [B][Hq][d]
     (+ m_g, e_g fp32 [B][Hq]); seq_lens advances by one."""
     _pool(layout, k_pool, "k_pool"); _pool(layout, v_pool, "v_pool"); _bf16(stats, "stats")
     _bf16(k_new, "k_new"); _bf16(v_new, "v_new"); _bf16(q, "q"); _i32(seq_lens, "seq_lens")

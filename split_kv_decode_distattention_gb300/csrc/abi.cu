@@ -347,7 +347,6 @@ dattn_status_t decode_impl(const dattn_kv_layout* layout, const void* k_pool, co
     if (num_splits < 0 || T < 1) return DATTN_ERR_INVALID_ARG;
     if ((Hq / layout->num_kv_heads) * (int64_t)T > kMaxGroup) return DATTN_ERR_UNSUPPORTED;
     if (T > 1 && sparse != nullptr) return DATTN_ERR_UNSUPPORTED;
-    if (app != nullptr && layout->kv_format != DATTN_KV_BF16) return DATTN_ERR_UNSUPPORTED;
     if (B == 0) return DATTN_OK;
     if (!k_pool || !v_pool || !q || !seq_lens || !out) return DATTN_ERR_INVALID_ARG;
     if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(q)) return DATTN_ERR_INVALID_ARG;
@@ -408,8 +407,9 @@ dattn_status_t decode_impl(const dattn_kv_layout* layout, const void* k_pool, co
         p.append = 1;
         p.k_new = app->k_new;
         p.v_new = app->v_new;
-        p.k_pool_w = static_cast<uint16_t*>(app->k_pool);
-        p.v_pool_w = static_cast<uint16_t*>(app->v_pool);
+        p.k_pool_w = static_cast<uint8_t*>(app->k_pool);
+        p.v_pool_w = static_cast<uint8_t*>(app->v_pool);
+        p.kv_scale_w = layout->kv_scale;
         p.stats = app->stats;
         p.seq_lens_w = app->seq_lens;
     }

@@ -67,6 +67,8 @@ struct Smem {
     // fused append: the position of request i's new token (its length before the append;
     // negative when nothing is appended)
     __device__ int32_t* item_pos() const { return reinterpret_cast<int32_t*>(base + L.item_pos); }
+    // fused append, quantized pool: [warp][lane][3] codes and scale of the new row
+    __device__ uint32_t* qrow() const { return reinterpret_cast<uint32_t*>(base + L.qrow); }
     // the CTA's plan constants: aligned, W, Gw, X0, X1
     __device__ int32_t* cplan() const { return reinterpret_cast<int32_t*>(base + L.flags + 8); }
     // head-aligned plan: kAplanScalars scalars, the retrieval heads, the streaming heads
@@ -581,6 +583,52 @@ struct Consumer {
         return __ldg(reinterpret_cast<const uint4*>(src));
     }
 
+    // Fused append, quantized pool: this lane's codes of segment s's new K or V row (8-bit: 8
+    // bytes; 4-bit: 4 bytes) and the row's scale, quantized exactly as the write half
+    // quantizes them (the row maxima reduced over the lanes of each row; lanes as in
+    // load_new_row). Computed when a piece starts and kept in the warp's shared memory (not in
+    // registers, which the tile loop needs), for store_row_q.
+    __device__ void quant_new_row(int32_t s, bool f4) const {
+        constexpr int VPR = D / 8;
+        const uint4 v = load_new_row(s);  // zero for lanes past the two rows
+        float m = absmax8(v);
+#pragma unroll
+        for (int off = 1; off < VPR; off <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        uint32_t* r = sm.qrow() + (warp * 32 + lane) * 3;
+        float scale;
+        if (f4) {
+            r[0] = quant4_chunk(v, m, scale);
+            r[1] = 0u;
+        } else {
+            const uint2 c = quant8_chunk(v, m, scale);
+            r[0] = c.x;
+            r[1] = c.y;
+        }
+        r[2] = __float_as_uint(scale);
+    }
+
+    // Writes this lane's codes (from quant_new_row) into row `row` of the quantized stage `st`
+    // (8-bit, or 4-bit when f4), in the layout the TMA boxes leave there, and the rows' scales
+    // into the stage's scales `sc`.
+    __device__ void store_row_q(uint32_t st, float* sc, int row, bool f4) const {
+        constexpr int VPR = D / 8;
+        if (lane < 2 * VPR) {
+            const uint32_t* r = sm.qrow() + (warp * 32 + lane) * 3;
+            const bool isv = lane >= VPR;
+            const int c8 = lane % VPR;
+            if (f4)
+                st_shared_u32(st + (isv ? 8u * D : 0u) + swz_rows<D / 2>((uint32_t)row, c8 >> 2) +
+                                  (uint32_t)(c8 & 3) * 4u,
+                              r[0]);
+            else
+                st_shared_v2(st + (isv ? 16u * D : 0u) + swz_rows<D>((uint32_t)row, c8 >> 1) +
+                                 (uint32_t)(c8 & 1) * 8u,
+                             r[0], r[1]);
+            if (c8 == 0) sc[(isv ? 16 : 0) + row] = __uint_as_float(r[2]);
+        }
+        __syncwarp();
+    }
+
     // Writes the new token's K and V (this lane's chunk v from load_new_row) into row `row` of
     // the bf16 stage `st`, in the layout the TMA boxes leave there.
     __device__ void patch_row(uint32_t st, int row, const uint4& v) const {
@@ -981,12 +1029,14 @@ struct Consumer {
     }
 };
 
-// The write half of the fused append (bf16 pool): the new token of every (request, KV head)
-// goes to its page and slot, and the open logical page's k_max / k_min take it in, exactly as
-// dattn_kv_append writes one token. The work is spread over the consumer threads of all CTAs
-// (one 8-channel chunk each). A CTA that reads the tile of a new token may see the slot
-// before or after this write; it writes the new token into its stage itself (patch_row).
-template <int D>
+// The write half of the fused append: the new token of every (request, KV head) goes to its
+// page and slot, and the open logical page's k_max / k_min take it in, exactly as
+// dattn_kv_append writes one token (with a quantized pool, the row is quantized as that call
+// quantizes it: the same row maximum, scale and codes). The work is spread over the consumer
+// threads of all CTAs (one 8-channel chunk each; the chunks of a row are consecutive lanes).
+// A CTA that reads the tile of a new token may see the slot before or after this write; it
+// writes the new token into its stage itself (Consumer::patch_row, patch_row_q).
+template <int D, int FMT>
 __device__ void append_new_tokens(const AttnParams& p, const Smem& sm, int32_t cta, int32_t G,
                                   int ctid) {
     constexpr int VPR = D / 8;
@@ -996,6 +1046,17 @@ __device__ void append_new_tokens(const AttnParams& p, const Smem& sm, int32_t c
         const int32_t c8 = (int32_t)(it % VPR);
         const int64_t bh = it / VPR;
         const int32_t b = (int32_t)(bh / p.Hkv), h = (int32_t)(bh - (int64_t)b * p.Hkv);
+        const uint4 kv = __ldg(reinterpret_cast<const uint4*>(p.k_new + bh * D + c8 * 8));
+        const uint4 vv = __ldg(reinterpret_cast<const uint4*>(p.v_new + bh * D + c8 * 8));
+        float mk = 0.f, mv = 0.f;
+        if constexpr (FMT != DATTN_KV_BF16) {
+            // every lane of a row takes part in the row maxima, whatever its page; the lanes
+            // in the loop are a prefix of the warp made of whole rows
+            const int64_t warp_items = n - (it - (ctid & 31));
+            const unsigned mask = warp_items >= 32 ? 0xffffffffu : ((1u << warp_items) - 1u);
+            mk = row_absmax<VPR>(kv, mask);
+            mv = row_absmax<VPR>(vv, mask);
+        }
         const int32_t pos = sm.item_pos()[b];
         if (pos < 0) continue;  // flagged when the lengths were read
         const int32_t lp = pos / p.P;
@@ -1012,12 +1073,42 @@ __device__ void append_new_tokens(const AttnParams& p, const Smem& sm, int32_t c
             set_err(p.dev_err, DATTN_DEVERR_PAGE_OOB);
             continue;
         }
-        const uint4 kv = __ldg(reinterpret_cast<const uint4*>(p.k_new + bh * D + c8 * 8));
-        const uint4 vv = __ldg(reinterpret_cast<const uint4*>(p.v_new + bh * D + c8 * 8));
         const int32_t slot = pos - lp * p.P;
-        const int64_t dst = (((int64_t)page * p.Hkv + h) * p.P + slot) * D + c8 * 8;
-        *reinterpret_cast<uint4*>(p.k_pool_w + dst) = kv;
-        *reinterpret_cast<uint4*>(p.v_pool_w + dst) = vv;
+        const int64_t row = ((int64_t)page * p.Hkv + h) * p.P + slot;
+        if constexpr (FMT == DATTN_KV_BF16) {
+            const int64_t dst = (row * D + c8 * 8) * 2;
+            *reinterpret_cast<uint4*>(p.k_pool_w + dst) = kv;
+            *reinterpret_cast<uint4*>(p.v_pool_w + dst) = vv;
+        } else {
+            const bool i4 = FMT == DATTN_KV_INT4 || (FMT == DATTN_KV_MIXED && head_is_i4(p.hf, h));
+            // the codes' row: the mixed pool keeps each format in its own region
+            int64_t crow = row;
+            uint8_t* kd = p.k_pool_w;
+            uint8_t* vd = p.v_pool_w;
+            if constexpr (FMT == DATTN_KV_MIXED) {
+                const int32_t h4 = p.hf.h4, h8 = p.Hkv - h4;
+                crow = ((int64_t)page * (i4 ? h4 : h8) + head_class_index(p.hf, h, i4)) * p.P +
+                       slot;
+                if (i4) {
+                    const int64_t region8 = (int64_t)p.num_pages * h8 * p.P * D;
+                    kd += region8;
+                    vd += region8;
+                }
+            }
+            float ks, vs;
+            if (i4) {
+                *reinterpret_cast<uint32_t*>(kd + crow * (D / 2) + c8 * 4) = quant4_chunk(kv, mk, ks);
+                *reinterpret_cast<uint32_t*>(vd + crow * (D / 2) + c8 * 4) = quant4_chunk(vv, mv, vs);
+            } else {
+                *reinterpret_cast<uint2*>(kd + crow * D + c8 * 8) = quant8_chunk(kv, mk, ks);
+                *reinterpret_cast<uint2*>(vd + crow * D + c8 * 8) = quant8_chunk(vv, mv, vs);
+            }
+            if (c8 == 0) {  // [row / 16][K, V][row % 16]
+                float* sc = p.kv_scale_w + (row >> 4) * 32 + (row & 15);
+                sc[0] = ks;
+                sc[16] = vs;
+            }
+        }
         if (p.stats != nullptr) {
             uint16_t* st = p.stats +
                            (((int64_t)page * p.Hkv + h) * (p.P >> 4) + (slot >> 4)) * 2 * D + c8 * 8;
@@ -1039,7 +1130,10 @@ __device__ void append_new_tokens(const AttnParams& p, const Smem& sm, int32_t c
 template <int D, int FMT>
 constexpr int attn_min_blocks() { return (D == 64 || FMT == DATTN_KV_INT4) ? 4 : 3; }
 
-template <int D, int FMT>
+// APP: the launch of dattn_append_decode (the one-token append fused into the decode). It is
+// a template parameter so that the plain decode carries none of the append's code and
+// registers.
+template <int D, int FMT, bool APP>
 __global__ void __launch_bounds__(kAttnThreads, attn_min_blocks<D, FMT>())
 attention_kernel(const __grid_constant__ AttnParams p,
                  const __grid_constant__ CUtensorMap tmap_k,
@@ -1055,7 +1149,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
         sm.base = smem_raw + (((off + 1023u) & ~1023u) - off);
     }
     constexpr bool Q = FMT != DATTN_KV_BF16;  // a quantized pool with row scales
-    sm.L = attn_smem_layout(D, p.gq, p.nitems, p.Hkv, p.mode == MODE_SPARSE, FMT, p.append != 0);
+    sm.L = attn_smem_layout(D, p.gq, p.nitems, p.Hkv, p.mode == MODE_SPARSE, FMT, APP);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t G = gridDim.x, cta = blockIdx.x;
     constexpr int NS = attn_stages(FMT);
@@ -1110,7 +1204,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
             prefetch_l2_range(p.selected, (size_t)p.B * p.Hkv * p.top_k * 4u, gt, gn);
         if (p.mode == MODE_SPARSE && p.selected_phys)
             prefetch_l2_range(p.selected_phys, (size_t)p.B * p.Hkv * p.top_k * 4u, gt, gn);
-        if (p.append) {
+        if constexpr (APP) {
             prefetch_l2_range(p.k_new, (size_t)p.B * p.Hkv * D * 2u, gt, gn);
             prefetch_l2_range(p.v_new, (size_t)p.B * p.Hkv * D * 2u, gt, gn);
         }
@@ -1129,7 +1223,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
     auto length_of = [&](int32_t i) {
         int32_t L = p.seq_lens[i];
         const int32_t cap = p.max_pages * p.P;
-        if (p.append) {
+        if constexpr (APP) {
             sm.item_pos()[i] = L;
             if (L >= 0 && L < cap) ++L;
         }
@@ -1346,8 +1440,8 @@ attention_kernel(const __grid_constant__ AttnParams p,
     }
 
     // ---------------------------------------------------------------- consumer warps
-    if constexpr (FMT == DATTN_KV_BF16) {
-        if (p.append) {
+    {
+        if constexpr (APP) {
             // Every thread of this CTA has read the lengths (the barrier above). The CTA that
             // arrives last advances seq_lens, as dattn_kv_append does; no CTA waits for another.
             if (warp == 0) {
@@ -1364,7 +1458,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
                     }
                 }
             }
-            append_new_tokens<D>(p, sm, cta, G, tid);
+            append_new_tokens<D, FMT>(p, sm, cta, G, tid);
         }
     }
     if (!any) return;
@@ -1407,10 +1501,13 @@ attention_kernel(const __grid_constant__ AttnParams p,
         // that holds the new token gets it written into its row)
         uint4 patch = make_uint4(0u, 0u, 0u, 0u);
         if constexpr (FMT == DATTN_KV_BF16) {
-            if (p.append) patch = cons.load_new_row(pc.s);
+            if constexpr (APP) patch = cons.load_new_row(pc.s);
         }
         cons.reset();
         if constexpr (FMT == DATTN_KV_MIXED) cons.i4 = head_is_i4(p.hf, pc.s % p.Hkv);
+        if constexpr (Consumer<D, FMT>::Q) {
+            if constexpr (APP) cons.quant_new_row(pc.s, Consumer<D, FMT>::I4 || cons.i4);
+        }
         const int32_t s = pc.s;
         const int32_t nr = pc.r1 - pc.r0;
         for (int32_t i = (warp - kbase % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
@@ -1423,19 +1520,23 @@ attention_kernel(const __grid_constant__ AttnParams p,
             const int32_t lohi = sm.meta()[stg];
             const int lo = tile_lo(lohi), hi = tile_hi(lohi), cut = tile_cut(lohi);
             if (ok && !(lohi & kTileSkip)) {
-                if constexpr (FMT == DATTN_KV_MIXED) {
+                if constexpr (Q) {
                     const uint32_t st = stage0 + (uint32_t)stg * sm.L.stage_bytes;
-                    if (lohi & kTileI4) cons.tile_i4(st, sm.scales(stg), lo, hi, cut);
-                    else                cons.tile_f8(st, sm.scales(stg), lo, hi, cut);
-                } else if constexpr (FMT == DATTN_KV_INT4) {
-                    cons.tile_i4(stage0 + (uint32_t)stg * sm.L.stage_bytes, sm.scales(stg), lo, hi,
-                                 cut);
-                } else if constexpr (Q) {
-                    cons.tile_f8(stage0 + (uint32_t)stg * sm.L.stage_bytes, sm.scales(stg), lo, hi,
-                                 cut);
+                    const bool t4 = FMT == DATTN_KV_INT4 ||
+                                    (FMT == DATTN_KV_MIXED && (lohi & kTileI4) != 0);
+                    // fused append: the new token's codes and scales into this stage, quantized
+                    // here exactly as the write half quantizes them (the warp's lanes together)
+                    const bool patched = APP && (lohi & kTilePatch) != 0;
+                    if (patched)
+                        cons.store_row_q(st, const_cast<float*>(sm.scales(stg)),
+                                         tile_patch_row(lohi), t4);
+                    if (t4) cons.tile_i4(st, sm.scales(stg), lo, hi, cut);
+                    else    cons.tile_f8(st, sm.scales(stg), lo, hi, cut);
+                    // generic writes to the stage before TMA refills it
+                    if (patched) fence_proxy_async_smem();
                 } else {
                     const uint32_t st = stage0 + (uint32_t)stg * sm.L.stage_bytes;
-                    const bool patched = (lohi & kTilePatch) != 0;
+                    const bool patched = APP && (lohi & kTilePatch) != 0;
                     if (patched) cons.patch_row(st, tile_patch_row(lohi), patch);
                     cons.tile(st, lo, hi, cut);
                     // generic writes to the stage (patch, zeroed rows) before TMA refills it
@@ -1571,7 +1672,7 @@ struct KernelInfo {
     int max_smem_set = 0;
 };
 
-template <int D, int FMT>
+template <int D, int FMT, bool APP>
 KernelInfo& kernel_info() {
     static KernelInfo info;
     return info;
@@ -1579,12 +1680,12 @@ KernelInfo& kernel_info() {
 
 std::mutex g_attr_mutex;
 
-template <int D, int FMT>
+template <int D, int FMT, bool APP>
 dattn_status_t ensure_smem(uint32_t bytes) {
     std::lock_guard<std::mutex> lock(g_attr_mutex);
-    KernelInfo& ki = kernel_info<D, FMT>();
+    KernelInfo& ki = kernel_info<D, FMT, APP>();
     if ((int)bytes > ki.max_smem_set) {
-        if (cudaFuncSetAttribute(attention_kernel<D, FMT>,
+        if (cudaFuncSetAttribute(attention_kernel<D, FMT, APP>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bytes) != cudaSuccess)
             return DATTN_ERR_CUDA;
@@ -1593,10 +1694,10 @@ dattn_status_t ensure_smem(uint32_t bytes) {
     return DATTN_OK;
 }
 
-template <int D, int FMT>
+template <int D, int FMT, bool APP>
 int occupancy(uint32_t smem) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attention_kernel<D, FMT>, kAttnThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attention_kernel<D, FMT, APP>, kAttnThreads,
                                                       smem) != cudaSuccess)
         return 1;
     return n < 1 ? 1 : n;
@@ -1609,16 +1710,16 @@ size_t attn_workspace_bytes(int32_t nseg, int32_t g, int32_t D, int32_t G) {
 }
 
 
-template <int D, int FMT>
+template <int D, int FMT, bool APP>
 static dattn_status_t launch_d(const AttnParams& p0, const void* k_pool, const void* v_pool,
                                int32_t num_splits, void* ws, size_t ws_bytes,
                                cudaStream_t stream, int64_t tiles_bound) {
     AttnParams p = p0;
     const AttnSmem L =
-        attn_smem_layout(D, p.gq, p.nitems, p.Hkv, p.mode == MODE_SPARSE, FMT, p.append != 0);
-    dattn_status_t st = ensure_smem<D, FMT>(L.total);
+        attn_smem_layout(D, p.gq, p.nitems, p.Hkv, p.mode == MODE_SPARSE, FMT, APP);
+    dattn_status_t st = ensure_smem<D, FMT, APP>(L.total);
     if (st != DATTN_OK) return st;
-    const int32_t G = choose_splits(tiles_bound, num_splits, occupancy<D, FMT>(L.total));
+    const int32_t G = choose_splits(tiles_bound, num_splits, occupancy<D, FMT, APP>(L.total));
     const size_t counters = attn_counter_bytes(p.nseg);
     if (ws == nullptr || ws_bytes < attn_workspace_bytes(p.nseg, p.gq, D, G) ||
         (reinterpret_cast<uintptr_t>(ws) & 255))
@@ -1656,7 +1757,7 @@ static dattn_status_t launch_d(const AttnParams& p0, const void* k_pool, const v
         if ((st = make_kv_tensor_map_u8(&tv, v_pool, rows, row_bytes)) != DATTN_OK) return st;
     }
     if constexpr (FMT != DATTN_KV_MIXED) tk4 = tk, tv4 = tv;  // not read
-    if (launch_pdl(attention_kernel<D, FMT>, dim3(G), dim3(kAttnThreads), L.total, stream, p, tk,
+    if (launch_pdl(attention_kernel<D, FMT, APP>, dim3(G), dim3(kAttnThreads), L.total, stream, p, tk,
                    tv, tk4, tv4) != cudaSuccess)
         return DATTN_ERR_CUDA;
     return DATTN_OK;
@@ -1672,10 +1773,20 @@ dattn_status_t launch_attention(const AttnParams& p, const void* k_pool, const v
              : p.fmt == DATTN_KV_FP8_E4M3 ? f8
                                           : bf16;
     };
-    auto launch = D == 64 ? pick(launch_d<64, DATTN_KV_BF16>, launch_d<64, DATTN_KV_FP8_E4M3>,
-                                 launch_d<64, DATTN_KV_INT4>, launch_d<64, DATTN_KV_MIXED>)
-                          : pick(launch_d<128, DATTN_KV_BF16>, launch_d<128, DATTN_KV_FP8_E4M3>,
-                                 launch_d<128, DATTN_KV_INT4>, launch_d<128, DATTN_KV_MIXED>);
+    auto launch =
+        p.append != 0
+            ? (D == 64 ? pick(launch_d<64, DATTN_KV_BF16, true>, launch_d<64, DATTN_KV_FP8_E4M3, true>,
+                              launch_d<64, DATTN_KV_INT4, true>, launch_d<64, DATTN_KV_MIXED, true>)
+                       : pick(launch_d<128, DATTN_KV_BF16, true>,
+                              launch_d<128, DATTN_KV_FP8_E4M3, true>,
+                              launch_d<128, DATTN_KV_INT4, true>, launch_d<128, DATTN_KV_MIXED, true>))
+            : (D == 64 ? pick(launch_d<64, DATTN_KV_BF16, false>,
+                              launch_d<64, DATTN_KV_FP8_E4M3, false>,
+                              launch_d<64, DATTN_KV_INT4, false>, launch_d<64, DATTN_KV_MIXED, false>)
+                       : pick(launch_d<128, DATTN_KV_BF16, false>,
+                              launch_d<128, DATTN_KV_FP8_E4M3, false>,
+                              launch_d<128, DATTN_KV_INT4, false>,
+                              launch_d<128, DATTN_KV_MIXED, false>));
     return launch(p, k_pool, v_pool, num_splits, ws, ws_bytes, stream, tiles_bound);
 }
 

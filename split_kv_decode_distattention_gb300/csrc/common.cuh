@@ -299,6 +299,72 @@ __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---- row quantization of the 8-bit and 4-bit pools (the append and the fused append) ----
+// A row of d bf16 values is handled 8 channels (one 16-byte chunk) per lane, the lanes of a
+// row consecutive. scale = max|x| / 448 (8-bit) or / 7 (4-bit), each code from x / scale, both
+// divisions in IEEE fp32.
+
+__device__ __forceinline__ float bf(uint32_t h) { return __uint_as_float(h << 16); }
+
+// Max |x| of the 8 bf16 values of a 16-byte chunk.
+__device__ __forceinline__ float absmax8(const uint4& v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        m = fmaxf(m, fmaxf(fabsf(bf(w[i] & 0xffffu)), fabsf(bf(w[i] >> 16))));
+    return m;
+}
+
+// E4M3 codes of the 8 bf16 values of a chunk divided by s (s > 0), code i in byte i.
+__device__ __forceinline__ uint2 quant8(const uint4& v, float s) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __fdiv_rn(bf(w[i] & 0xffffu), s);
+        x[2 * i + 1] = __fdiv_rn(bf(w[i] >> 16), s);
+    }
+    return make_uint2(f32x4_to_e4m3(x[0], x[1], x[2], x[3]), f32x4_to_e4m3(x[4], x[5], x[6], x[7]));
+}
+
+// Max |x| of a row, from this lane's 8-channel chunk; `mask` holds the lanes of this warp in
+// the loop, and the VPR lanes of a row are consecutive and all in it.
+template <int VPR>
+__device__ __forceinline__ float row_absmax(const uint4& v, unsigned mask) {
+    float m = absmax8(v);
+#pragma unroll
+    for (int off = 1; off < VPR; off <<= 1) m = fmaxf(m, __shfl_xor_sync(mask, m, off));
+    return m;
+}
+
+// 8-bit row scale (row max |x| = m) and the E4M3 codes of one chunk.
+__device__ __forceinline__ uint2 quant8_chunk(const uint4& v, float m, float& scale) {
+    scale = __fdiv_rn(m, 448.0f);
+    return scale > 0.f ? quant8(v, scale) : make_uint2(0u, 0u);
+}
+
+// 4-bit codes of the 8 bf16 values of a chunk divided by s (s > 0): code c + 8 of channel
+// 2j in the low nibble of byte j, of channel 2j + 1 in its high nibble.
+__device__ __forceinline__ uint32_t quant4(const uint4& v, float s) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int c0 = min(7, max(-7, __float2int_rn(__fdiv_rn(bf(w[i] & 0xffffu), s))));
+        const int c1 = min(7, max(-7, __float2int_rn(__fdiv_rn(bf(w[i] >> 16), s))));
+        out |= (uint32_t)((c0 + 8) | ((c1 + 8) << 4)) << (8 * i);
+    }
+    return out;
+}
+
+// 4-bit row scale (row max |x| = m) and the packed codes of one chunk.
+__device__ __forceinline__ uint32_t quant4_chunk(const uint4& v, float m, float& scale) {
+    scale = __fdiv_rn(m, 7.0f);
+    return scale > 0.f ? quant4(v, scale) : 0x88888888u;
+}
+
+
 // Folds 8 bf16 key channels (one 16-byte chunk) into a logical page's running k_max / k_min,
 // per channel with strict comparisons, so that on a tie the earlier value stays.
 __device__ __forceinline__ void bf16_fold8(const uint4& k, uint4& mx, uint4& mn) {
@@ -321,6 +387,12 @@ __device__ __forceinline__ void bf16_fold8(const uint4& k, uint4& mx, uint4& mn)
     mn = make_uint4(nw[0], nw[1], nw[2], nw[3]);
 }
 
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b) {
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)

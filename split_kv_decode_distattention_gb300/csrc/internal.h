@@ -95,13 +95,15 @@ struct AttnParams {
     int32_t sinks, local, top_k;
     const int32_t* selected;
     const int32_t* selected_phys;  // nullable: physical pages of `selected` (no table lookup)
-    // fused one-token append (dattn_append_decode, bf16 pool): the new token of request b is
-    // written at position seq_lens[b], attended by this launch, and seq_lens[b] advances by one
+    // fused one-token append (dattn_append_decode): the new token of request b is written at
+    // position seq_lens[b] (quantized as the pool's format prescribes), attended by this
+    // launch, and seq_lens[b] advances by one
     int32_t append;
     const uint16_t* k_new;  // [B][Hkv][D]
     const uint16_t* v_new;
-    uint16_t* k_pool_w;
-    uint16_t* v_pool_w;
+    uint8_t* k_pool_w;      // the pools' bytes
+    uint8_t* v_pool_w;
+    float* kv_scale_w;      // the quantized pools' row scales
     uint16_t* stats;  // nullable: logical-page k_max / k_min
     int32_t* seq_lens_w;  // seq_lens, advanced by the launch
     // outputs: decode -> out [B][Hq][D], m_out / e_out [B][Hq] (nullable)
@@ -134,7 +136,7 @@ __host__ __device__ inline int32_t slot_floats(int32_t g, int32_t D) {
 // with a quantized pool, the stage's 16 K scales and 16 V scales sit in `scales`.
 struct AttnSmem {
     uint32_t nstages, stage_bytes, stages, scales, bars, meta, flags, ws_m, ws_e, ws_o, kind_before,
-        kinds, aplan, item_start, item_len, item_pos, scan, total;
+        kinds, aplan, item_start, item_len, item_pos, qrow, scan, total;
 };
 
 // Integers of the head-aligned plan of a block-sparse launch (see the attention kernel):
@@ -164,6 +166,8 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int D, int g, int nitems, i
     s.item_len = o;    o += (uint32_t)nitems * 4u;
     s.item_pos = o;    o += append ? (uint32_t)nitems * 4u : 0u;
     o = (o + 15u) & ~15u;
+    // fused append to a quantized pool: each consumer lane's codes and scale of the new row
+    s.qrow = o;        o += (append && fmt != DATTN_KV_BF16) ? kConsumerWarps * 32u * 3u * 4u : 0u;
     s.scan = o;        o += 8u * 4u;
     s.total = o + 1024u;  // slack to align the dynamic base to 1024 bytes
     return s;

@@ -38,66 +38,6 @@ namespace {
 constexpr int kAppendMaxThreads = 512;  // one thread per (KV head, 8-channel chunk)
 constexpr int kAppendWindow = 64;  // token positions per CTA, a multiple of 16
 
-__device__ __forceinline__ float bf(uint32_t h) { return __uint_as_float(h << 16); }
-
-// Max |x| of the 8 bf16 values of a 16-byte chunk.
-__device__ __forceinline__ float absmax8(const uint4& v) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float m = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        m = fmaxf(m, fmaxf(fabsf(bf(w[i] & 0xffffu)), fabsf(bf(w[i] >> 16))));
-    return m;
-}
-
-// E4M3 codes of the 8 bf16 values of a chunk divided by s (s > 0), code i in byte i.
-__device__ __forceinline__ uint2 quant8(const uint4& v, float s) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float x[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        x[2 * i] = __fdiv_rn(bf(w[i] & 0xffffu), s);
-        x[2 * i + 1] = __fdiv_rn(bf(w[i] >> 16), s);
-    }
-    return make_uint2(f32x4_to_e4m3(x[0], x[1], x[2], x[3]), f32x4_to_e4m3(x[4], x[5], x[6], x[7]));
-}
-
-// Max |x| of a row, from this lane's 8-channel chunk; `mask` holds the lanes of this warp in
-// the loop, and the VPR lanes of a row are consecutive and all in it.
-template <int VPR>
-__device__ __forceinline__ float row_absmax(const uint4& v, unsigned mask) {
-    float m = absmax8(v);
-#pragma unroll
-    for (int off = 1; off < VPR; off <<= 1) m = fmaxf(m, __shfl_xor_sync(mask, m, off));
-    return m;
-}
-
-// 8-bit row scale (row max |x| = m) and the E4M3 codes of one chunk.
-__device__ __forceinline__ uint2 quant8_chunk(const uint4& v, float m, float& scale) {
-    scale = __fdiv_rn(m, 448.0f);
-    return scale > 0.f ? quant8(v, scale) : make_uint2(0u, 0u);
-}
-
-// 4-bit codes of the 8 bf16 values of a chunk divided by s (s > 0): code c + 8 of channel
-// 2j in the low nibble of byte j, of channel 2j + 1 in its high nibble.
-__device__ __forceinline__ uint32_t quant4(const uint4& v, float s) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t out = 0u;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int c0 = min(7, max(-7, __float2int_rn(__fdiv_rn(bf(w[i] & 0xffffu), s))));
-        const int c1 = min(7, max(-7, __float2int_rn(__fdiv_rn(bf(w[i] >> 16), s))));
-        out |= (uint32_t)((c0 + 8) | ((c1 + 8) << 4)) << (8 * i);
-    }
-    return out;
-}
-
-// 4-bit row scale (row max |x| = m) and the packed codes of one chunk.
-__device__ __forceinline__ uint32_t quant4_chunk(const uint4& v, float m, float& scale) {
-    scale = __fdiv_rn(m, 7.0f);
-    return scale > 0.f ? quant4(v, scale) : 0x88888888u;
-}
-
 template <int D, int FMT>
 __global__ void __launch_bounds__(kAppendMaxThreads)
 kv_append_kernel(dattn_kv_layout L, const __grid_constant__ KvHeadFormats hf,

@@ -234,12 +234,12 @@ def test_other_entry_points_validate(dattn):
     # page select: top_k too large
     assert lib.dattn_page_select(ctypes.byref(lay.c), p, p, 1, 4, p, p, 300, p, None, p,
                                  1 << 20, 0, None, None) == 2
-    # fused append and decode: a quantized pool is unsupported; null new rows are invalid
+    # fused append and decode: null or misaligned new rows are invalid, for every pool format
     lay8 = _lay(dattn)
     lay8.c.kv_format = dattn.KV_FP8_E4M3
     lay8.c.kv_scale = p
-    assert lib.dattn_append_decode(ctypes.byref(lay8.c), p, p, None, p, p, p, 1, 4, 0.1, p, None,
-                                   0, p, 1 << 20, p, None, None, None, None) == 2
+    assert lib.dattn_append_decode(ctypes.byref(lay8.c), p, p, None, None, p, p, 1, 4, 0.1, p,
+                                   None, 0, p, 1 << 20, p, None, None, None, None) == 1
     assert lib.dattn_append_decode(ctypes.byref(lay.c), p, p, None, None, p, p, 1, 4, 0.1, p,
                                    None, 0, p, 1 << 20, p, None, None, None, None) == 1
     assert lib.dattn_append_decode(ctypes.byref(lay.c), p, p, None, p, ctypes.c_void_p(18), p, 1,

@@ -189,6 +189,20 @@ def test_sparse_512k_full_size(seed):
     _check_pairs(case, q, cache.lens, out, m_g, e_g, pairs, "sparse-512k", rows_of=rows_of)
 
 
+def _fused_step(cache, case, sparse=None):
+    """The benchmark's step: the one-token append and the decode in one launch."""
+    kn, vn = cache.new_tokens(1)
+    q = case.q(1, DEV)
+    out = torch.empty(case.B, case.Hq, case.d, device=DEV)
+    m_g = torch.empty(case.B, case.Hq, device=DEV)
+    e_g = torch.empty_like(m_g)
+    cache.append_decode(kn, vn, q, out, cache.workspace(), m_g=m_g, e_g=e_g, sparse=sparse)
+    torch.cuda.synchronize()
+    assert int(cache.dev_err.item()) == 0
+    assert cache.seq_lens.tolist() == cache.lens
+    return q, out, m_g, e_g
+
+
 def _select_full(case, cache):
     """The window's first step: append one token, then select (with the pool pages)."""
     kn, vn = cache.new_tokens(1)
@@ -232,16 +246,17 @@ def test_sparse_512k_fused_step_full_size():
 
 def test_sparse_512k_mixed_pool_full_size():
     """sparse-512k over the mixed pool (retrieval and dense heads 8-bit, streaming heads
-    4-bit): sampled pairs of both kinds against the oracle's float64 attention over its own
-    dequantized rows of each head's format."""
+    4-bit), stepped as the benchmark steps it (the fused append and decode with the
+    selector's pool pages): sampled pairs of both kinds against the oracle's float64
+    attention over its own dequantized rows of each head's format."""
     dattn = _lib()
     case = W.sparse_512k(seed=1)
     formats = [dattn.KV_INT4 if k == W.HEAD_STREAMING else dattn.KV_FP8_E4M3
                for k in case.head_kind]
     cache = _cache(case, with_stats=True, kv_format=dattn.KV_MIXED, head_format=formats)
-    sel, _ = _select_full(case, cache)
+    sel, phys = _select_full(case, cache)
     got = sel.cpu().numpy()
-    q, out, m_g, e_g = _step(cache, case, sparse=cache.sparse_config(sel))
+    q, out, m_g, e_g = _fused_step(cache, case, sparse=cache.sparse_config(sel, phys))
     qb = oracle.bf16_bits(q)
     o, mg, eg = out.cpu().numpy(), m_g.cpu().numpy(), e_g.cpu().numpy()
     kinds_seen = set()
@@ -266,16 +281,16 @@ def test_sparse_512k_mixed_pool_full_size():
 
 @pytest.mark.parametrize("fmt", ["fp8", "int4"])
 def test_mha_32k_quantized_pools_full_size(fmt):
-    """mha-32k over the 8-bit and the 4-bit pool: the append quantizes the seeded rows, the
-    decode attends them; sampled pairs against the oracle's float64 attention over its own
-    dequantized rows."""
+    """mha-32k over the 8-bit and the 4-bit pool: the append quantizes the seeded rows, and the
+    benchmark's step (the fused append and decode) attends them; sampled pairs against the
+    oracle's float64 attention over its own dequantized rows."""
     dattn = _lib()
     case = W.mha_32k(seed=0)
     kv_format = dattn.KV_FP8_E4M3 if fmt == "fp8" else dattn.KV_INT4
     quant, deq = ((oracle.quantize_rows_fp8, oracle.dequantize_rows_fp8) if fmt == "fp8" else
                   (oracle.quantize_rows_int4, oracle.dequantize_rows_int4))
     cache = _cache(case, kv_format=kv_format)
-    q, out, m_g, e_g = _step(cache, case)
+    q, out, m_g, e_g = _fused_step(cache, case)
     assert torch.isfinite(out).all()
     qb = oracle.bf16_bits(q)
     o, mg, eg = out.cpu().numpy(), m_g.cpu().numpy(), e_g.cpu().numpy()

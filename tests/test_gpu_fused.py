@@ -3,7 +3,8 @@ decode that reads it, and the head-aligned split of block-sparse launches.
 
 dattn_append_decode must leave exactly what dattn_kv_append (one token) followed by
 dattn_decode leaves: the same outputs bit for bit (the new token's K/V enters the attention
-with the same bf16 values), the same pool, statistics, lengths and error bits. The two-call
+with the same bf16 values, or with a quantized pool the same codes and scales), the same
+pool, scales, statistics, lengths and error bits. The two-call
 path is itself checked against the oracle elsewhere; the fused path is also checked against
 the oracle here, on every (request, query head), so that its parity does not rest on the
 other path alone.
@@ -15,7 +16,8 @@ import torch
 import oracle
 from split_kv_decode_distattention_gb300 import workloads as W
 
-from _util import check_dense, check_selection, host_kv, assert_out_close
+from _util import (assert_e_close, assert_m_close, assert_out_close, check_dense, check_selection,
+                   host_kv)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -46,11 +48,12 @@ def _assert_same_state(a, b, what):
     torch.cuda.synchronize()
     assert a.seq_lens.tolist() == b.seq_lens.tolist(), what
     assert int(a.dev_err.item()) == int(b.dev_err.item()), what
-    for name in ("k_pool", "v_pool", "stats"):
+    for name in ("k_pool", "v_pool", "stats", "kv_scale"):
         x, y = getattr(a, name), getattr(b, name)
         if x is None:
             continue
-        diff = (x.view(torch.int16) != y.view(torch.int16)).nonzero()
+        diff = (x.view(torch.int32) != y.view(torch.int32)).nonzero() if name == "kv_scale" \
+            else (x.view(torch.uint8) != y.view(torch.uint8)).nonzero()
         assert diff.shape[0] == 0, f"{what}: {name} differs at {diff[:4].tolist()}"
 
 
@@ -73,7 +76,7 @@ def _steps(case, sep, fus, nsteps, splits, sel=None, sel_phys=None, check_oracle
         assert torch.equal(m1, m2) and torch.equal(e1, e2), f"step {step}: m/e differ"
         if check_oracle and sel is None:
             check_dense(case, q, fus.lens, o2, m2, e2, DEV, what=f"fused step {step}")
-    return fus
+    return q, o2, m2, e2
 
 
 @pytest.mark.parametrize("d,P,lens,Hq,Hkv,splits", [
@@ -186,12 +189,63 @@ def test_append_decode_flags_unmapped_new_page_like_append():
     assert int(fus.dev_err.item()) & dattn.DEVERR["UNMAPPED_PAGE"]
 
 
-def test_append_decode_rejects_quantized_pool():
+def _fmt_kw(dattn, fmt, kinds):
+    """PagedCache arguments of a pool format ("mixed": streaming heads 4-bit, others 8-bit)."""
+    if fmt == "fp8":
+        return dict(kv_format=dattn.KV_FP8_E4M3)
+    if fmt == "int4":
+        return dict(kv_format=dattn.KV_INT4)
+    return dict(kv_format=dattn.KV_MIXED,
+                head_format=[dattn.KV_INT4 if k == W.HEAD_STREAMING else dattn.KV_FP8_E4M3
+                             for k in kinds])
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int4", "mixed"])
+@pytest.mark.parametrize("d,P,lens,Hq,Hkv,splits", [
+    (128, 16, [1000, 31, 16, 0, 511], 16, 4, 0),   # page and logical-page boundaries, L = 0
+    (64, 64, [300, 64, 127, 5000], 8, 2, 7),       # 64-token pages, few CTAs
+])
+def test_append_decode_equals_append_then_decode_quantized(fmt, d, P, lens, Hq, Hkv, splits):
+    """A quantized pool: the fused launch stores the new rows quantized exactly as
+    dattn_kv_append does (codes, scales and statistics bit for bit) and attends the same
+    codes (outputs bit for bit). The two-call path is checked against the oracle elsewhere."""
     dattn = _lib()
-    case = W.Case("q8", B=1, Hq=4, Hkv=2, d=128, P=16, lens=[40], seed=6)
-    from split_kv_decode_distattention_gb300.harness import PagedCache
-    cache = PagedCache(case, DEV, kv_format=dattn.KV_FP8_E4M3)
-    kn, vn = cache.new_tokens(1)
-    out, _, _ = _outs(case)
-    with pytest.raises(dattn.DattnError, match="UNSUPPORTED"):
-        cache.append_decode(kn, vn, case.q(0, DEV), out, cache.workspace())
+    kinds = [W.HEAD_RETRIEVAL if h % 2 == 0 else W.HEAD_STREAMING for h in range(Hkv)]
+    case = W.Case("fused-q", B=len(lens), Hq=Hq, Hkv=Hkv, d=d, P=P, lens=lens, seed=37 + d + P)
+    kw = _fmt_kw(dattn, fmt, kinds)
+    sep, fus = _pair(case, with_stats=True, **kw)
+    q, out, m_g, e_g = _steps(case, sep, fus, 3, splits, check_oracle=False)
+    # the last step against the oracle's fp64 attention over its own dequantized rows, each
+    # head in its format
+    four = [fmt == "int4" or (fmt == "mixed" and k == W.HEAD_STREAMING) for k in kinds]
+    qb = oracle.bf16_bits(q)
+    o, mg, eg = out.cpu().numpy(), m_g.cpu().numpy(), e_g.cpu().numpy()
+    for b in range(case.B):
+        K, V = host_kv(case, b, fus.lens[b], DEV)
+        for h in range(case.Hq):
+            kvh = h // case.g
+            quant, deq = ((oracle.quantize_rows_int4, oracle.dequantize_rows_int4) if four[kvh]
+                          else (oracle.quantize_rows_fp8, oracle.dequantize_rows_fp8))
+            Kd = deq(*quant(K[:, kvh].copy()))
+            Vd = deq(*quant(V[:, kvh].copy()))
+            r, rm, re = oracle.attention_f64(qb[b, h], Kd, Vd, case.scale)
+            assert_out_close(o[b, h], r, f"{fmt} b={b} h={h}")
+            assert_m_close(mg[b, h], rm, f"{fmt} b={b} h={h}")
+            assert_e_close(eg[b, h], re, f"{fmt} b={b} h={h}")
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int4", "mixed"])
+def test_append_decode_equals_append_then_decode_sparse_quantized(fmt):
+    """Block-sparse steps over a quantized pool (retrieval heads 8-bit and streaming heads
+    4-bit in the mixed one), with the selector's pool pages, against the two-call path."""
+    dattn = _lib()
+    kinds = [1, 2, 1, 2]
+    case = W.Case("fused-sq", B=4, Hq=16, Hkv=4, d=128, P=64,
+                  lens=[64 * 60 + 63, 64 * 8, 1000, 12], seed=47, head_kind=kinds, top_k=8,
+                  sinks=4, local=8, n_highsim=4)
+    sep, fus = _pair(case, with_stats=True, **_fmt_kw(dattn, fmt, kinds))
+    sel = torch.empty(case.B, case.Hkv, case.top_k, dtype=torch.int32, device=DEV)
+    phys = torch.empty_like(sel)
+    sep.select(case.q(0, DEV), sel, sep.workspace(top_k=case.top_k), selected_phys=phys)
+    torch.cuda.synchronize()
+    _steps(case, sep, fus, 3, 0, sel=sel, sel_phys=phys, check_oracle=False)

@@ -264,13 +264,3 @@ def test_mixed_sparse_decode_retrieval_8bit_streaming_4bit(kinds, splits, phys):
                                       case.local)
 
         _check_dense(case, q, cache.lens, spec, out, m_g, e_g, f"step {step}", rows_of=rows_of)
-
-
-def test_mixed_pool_unsupported_by_fused_append():
-    dattn = _lib()
-    case = W.Case("mixed-unsup", B=1, Hq=4, Hkv=2, d=128, P=16, lens=[40], seed=6)
-    cache = _cache(case, "84")
-    kn, vn = cache.new_tokens(1)
-    out, _, _ = _outs(case)
-    with pytest.raises(dattn.DattnError, match="UNSUPPORTED"):
-        cache.append_decode(kn, vn, case.q(0, DEV), out, cache.workspace())
