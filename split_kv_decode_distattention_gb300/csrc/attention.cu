@@ -672,13 +672,15 @@ struct Consumer {
             const float al0 = ex2_approx(m0 - mu0), al1 = ex2_approx(m1 - mu1);
             e0 *= al0;
             e1 *= al1;
+            float alo = al1;  // the factor of O's column 1
             if constexpr (I4 || MIX) {
                 ws0 *= al0;
                 ws1 *= al1;
+                if (p.gq == 1) alo = al0;  // column 1 holds column 0's lo terms (pv_i4<true>)
             }
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
-                o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+                o[mt][0] *= al0; o[mt][1] *= alo; o[mt][2] *= al0; o[mt][3] *= alo;
             }
         }
         m0 = mn0;
@@ -893,17 +895,33 @@ struct Consumer {
     // k of both halves is channel 4g8 + k of the two tokens: exactly an A fragment. M-tile mt
     // takes channels 32 (mt / 2) + 4g8 + 2 (mt % 2) + {0, 1} as its rows g8 and g8 + 8. Every
     // code is a finite value, so a masked row (weight 0) needs no zeroing.
+    // G1 (one query column, as in MHA decode): the hi and lo terms of the weights go to columns
+    // 0 and 1 of one B operand, so each m-tile takes one product instead of two; column 1 of
+    // the accumulator is then the lo part of column 0 (added when the piece is published).
+    template <bool G1>
     __device__ __forceinline__ void pv_i4(uint32_t vbase, float w0, float w1, float w2,
                                           float w3) {
         constexpr uint32_t RB = D / 2;
         const uint32_t row = (lane & 7) + ((lane >> 3) & 1) * 8;
         const uint32_t csel = lane >> 4;
         // W^T as the B operand: two fp16 terms, transposed with movmatrix
-        const uint32_t h01 = pack_f16(w0, w1), h23 = pack_f16(w2, w3);
-        const uint32_t l01 = pack_f16(w0 - f16_lo(h01), w1 - f16_hi(h01));
-        const uint32_t l23 = pack_f16(w2 - f16_lo(h23), w3 - f16_hi(h23));
-        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-        const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+        uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
+        if constexpr (G1) {
+            const float h0 = __half2float(__float2half_rn(w0)), h2 = __half2float(__float2half_rn(w2));
+            const bool c0 = (lane & 3) == 0;  // the lanes of column 0
+            const uint32_t h01 = c0 ? pack_f16(h0, w0 - h0) : 0u;
+            const uint32_t h23 = c0 ? pack_f16(h2, w2 - h2) : 0u;
+            bh0 = movmatrix_trans(h01);
+            bh1 = movmatrix_trans(h23);
+        } else {
+            const uint32_t h01 = pack_f16(w0, w1), h23 = pack_f16(w2, w3);
+            const uint32_t l01 = pack_f16(w0 - f16_lo(h01), w1 - f16_hi(h01));
+            const uint32_t l23 = pack_f16(w2 - f16_lo(h23), w3 - f16_hi(h23));
+            bh0 = movmatrix_trans(h01);
+            bh1 = movmatrix_trans(h23);
+            bl0 = movmatrix_trans(l01);
+            bl1 = movmatrix_trans(l23);
+        }
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
             uint32_t r0, r1, r2, r3;
@@ -912,25 +930,25 @@ struct Consumer {
                 const uint32_t x0 = i4pair_raw<0>(r0), x1 = i4pair_raw<1>(r0);
                 const uint32_t x2 = i4pair_raw<0>(r1), x3 = i4pair_raw<1>(r1);
                 mma_f16(o[4 * c], x0, x1, x2, x3, bh0, bh1);
-                mma_f16(o[4 * c], x0, x1, x2, x3, bl0, bl1);
+                if constexpr (!G1) mma_f16(o[4 * c], x0, x1, x2, x3, bl0, bl1);
             }
             {
                 const uint32_t x0 = i4pair_raw<2>(r0), x1 = i4pair_raw<3>(r0);
                 const uint32_t x2 = i4pair_raw<2>(r1), x3 = i4pair_raw<3>(r1);
                 mma_f16(o[4 * c + 1], x0, x1, x2, x3, bh0, bh1);
-                mma_f16(o[4 * c + 1], x0, x1, x2, x3, bl0, bl1);
+                if constexpr (!G1) mma_f16(o[4 * c + 1], x0, x1, x2, x3, bl0, bl1);
             }
             {
                 const uint32_t x0 = i4pair_raw<0>(r2), x1 = i4pair_raw<1>(r2);
                 const uint32_t x2 = i4pair_raw<0>(r3), x3 = i4pair_raw<1>(r3);
                 mma_f16(o[4 * c + 2], x0, x1, x2, x3, bh0, bh1);
-                mma_f16(o[4 * c + 2], x0, x1, x2, x3, bl0, bl1);
+                if constexpr (!G1) mma_f16(o[4 * c + 2], x0, x1, x2, x3, bl0, bl1);
             }
             {
                 const uint32_t x0 = i4pair_raw<2>(r2), x1 = i4pair_raw<3>(r2);
                 const uint32_t x2 = i4pair_raw<2>(r3), x3 = i4pair_raw<3>(r3);
                 mma_f16(o[4 * c + 3], x0, x1, x2, x3, bh0, bh1);
-                mma_f16(o[4 * c + 3], x0, x1, x2, x3, bl0, bl1);
+                if constexpr (!G1) mma_f16(o[4 * c + 3], x0, x1, x2, x3, bl0, bl1);
             }
         }
     }
@@ -969,7 +987,8 @@ struct Consumer {
         const float w0 = p0 * vn0, w1 = p1 * vn0, w2 = p2 * vn1, w3 = p3 * vn1;
         ws0 += w0 + w2;
         ws1 += w1 + w3;
-        pv_i4(st + 8u * D, w0, w1, w2, w3);
+        if (p.gq == 1) pv_i4<true>(st + 8u * D, w0, w1, w2, w3);
+        else           pv_i4<false>(st + 8u * D, w0, w1, w2, w3);
     }
 
     // Publishes this warp's state for the CTA-level merge of the piece.
@@ -1018,9 +1037,13 @@ struct Consumer {
                 // rows g8 and g8 + 8 of m-tile mt are channels dd and dd + 1 (4-bit: m-tile
                 // mt covers channels 32 (mt / 2) + 4 g8 + 2 (mt % 2) + {0, 1}, see tile_i4)
                 const int dd = f4 ? 32 * (mt >> 1) + 4 * g8 + 2 * (mt & 1) : mt * 16 + 2 * g8;
+                // 4-bit with one column: column 1 holds column 0's lo terms
+                const bool fold = f4 && p.gq == 1;
+                const float x0 = fold ? o[mt][0] + o[mt][1] : o[mt][0];
+                const float x2 = fold ? o[mt][2] + o[mt][3] : o[mt][2];
                 if (hA < p.gq)
                     *reinterpret_cast<float2*>(wo + hA * D + dd) =
-                        make_float2((o[mt][0] * ke - b0) * rs, (o[mt][2] * ko - b0) * rs);
+                        make_float2((x0 * ke - b0) * rs, (x2 * ko - b0) * rs);
                 if (hB < p.gq)
                     *reinterpret_cast<float2*>(wo + hB * D + dd) =
                         make_float2((o[mt][1] * ke - b1) * rs, (o[mt][3] * ko - b1) * rs);

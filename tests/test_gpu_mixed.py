@@ -171,6 +171,8 @@ def test_mixed_pool_of_one_format_is_that_format():
     ("48", 64, 16, 64, [999, 1, 2048], 5),
     ("8448", 128, 8, 16, [5000], 0),
     ("84", 128, 4, 16, [1, 15, 16, 17], 500),   # more CTAs than tiles
+    ("48", 128, 2, 16, [700, 33, 4000], 0),      # one query head per KV head (MHA)
+    ("4", 64, 1, 64, [129, 3000], 3),            # MHA, d = 64
 ])
 def test_mixed_decode_dense_matches_oracle(spec, d, Hq, P, lens, splits):
     _lib()
