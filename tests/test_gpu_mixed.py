@@ -266,3 +266,47 @@ def test_mixed_sparse_decode_retrieval_8bit_streaming_4bit(kinds, splits, phys):
                                       case.local)
 
         _check_dense(case, q, cache.lens, spec, out, m_g, e_g, f"step {step}", rows_of=rows_of)
+
+
+def test_mixed_decode_flags_bad_pages_without_fault():
+    """An unmapped page and a page outside the pool, in a mixed pool: both flagged, their
+    tiles skipped in both formats' heads, the other tokens attended as the oracle does."""
+    dattn = _lib()
+    spec = "8448"
+    case = W.Case("unm-mixed", B=1, Hq=4, Hkv=4, d=128, P=16, lens=[100], seed=4)
+    cache = _cache(case, spec)
+    cache.block_table[0, 2] = -1
+    cache.block_table[0, 3] = case.num_pages + 5
+    q = case.q(0, DEV)
+    out, m_g, e_g = _outs(case)
+    cache.decode(q, out, cache.workspace(), m_g=m_g, e_g=e_g)
+    torch.cuda.synchronize()
+    err = int(cache.dev_err.item())
+    assert err & dattn.DEVERR["UNMAPPED_PAGE"] and err & dattn.DEVERR["PAGE_OOB"]
+    rows = np.array([t for t in range(100) if t // 16 not in (2, 3)], np.int64)
+    _check_dense(case, q, [100], spec, out, m_g, e_g, "bad pages",
+                 rows_of=lambda b, kvh, L: rows)
+
+
+@pytest.mark.parametrize("spec", ["4444", "8448"])
+def test_mixed_and_4bit_pools_across_simulated_ranks(spec):
+    """The cross-GPU merge over a quantized pool: each simulated rank's dattn_partial over the
+    pages it holds, then dattn_merge_gathered, against the oracle over each head's
+    dequantized rows."""
+    _lib()
+    import split_kv_decode_distattention_gb300 as dattn
+    from split_kv_decode_distattention_gb300 import distributed as D
+    case = W.Case("dist-q", B=3, Hq=8, Hkv=4, d=128, P=16, lens=[2000, 37, 700], seed=29)
+    cache = _cache(case, spec)
+    q = case.q(0, DEV)
+    world = 3
+    m, e, MA = D.stacked_partials(world, case.B, case.Hq, case.d, DEV)
+    for r in range(world):
+        pages = [D.rank_pages(-(-L // case.P), r, world, "strided") for L in case.lens]
+        D.local_partials(cache.layout, cache.k_pool, cache.v_pool, q, case.scale,
+                         cache.seq_lens, pages, m[r], e[r], MA[r], dev_err=cache.dev_err)
+    out, m_g, e_g = _outs(case)
+    dattn.dattn_merge_gathered(m, e, MA, out=out, m_g=m_g, e_g=e_g, dev_err=cache.dev_err)
+    torch.cuda.synchronize()
+    assert int(cache.dev_err.item()) == 0
+    _check_dense(case, q, case.lens, spec, out, m_g, e_g, f"{world} ranks")
