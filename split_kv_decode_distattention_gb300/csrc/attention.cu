@@ -676,7 +676,9 @@ struct Consumer {
             if constexpr (I4 || MIX) {
                 ws0 *= al0;
                 ws1 *= al1;
-                if (p.gq == 1) alo = al0;  // column 1 holds column 0's lo terms (pv_i4<true>)
+            }
+            if constexpr (Q) {
+                if (p.gq == 1) alo = al0;  // column 1 holds column 0's lo terms (g1_weights)
             }
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
@@ -804,11 +806,20 @@ struct Consumer {
         const float vn0 = vs0 * inv, vn1 = vs1 * inv;  // in [0, 2^15], exact
         const float w0 = p0 * vn0, w1 = p1 * vn0, w2 = p2 * vn1, w3 = p3 * vn1;
         // ---- W^T as the B operand: two fp16 terms, transposed with movmatrix ----------
-        const uint32_t h01 = pack_f16(w0, w1), h23 = pack_f16(w2, w3);
-        const uint32_t l01 = pack_f16(w0 - f16_lo(h01), w1 - f16_hi(h01));
-        const uint32_t l23 = pack_f16(w2 - f16_lo(h23), w3 - f16_hi(h23));
-        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-        const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+        // (one query column: both terms in one operand, one product per m-tile)
+        const bool g1 = p.gq == 1;
+        uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
+        if (g1) {
+            g1_weights(w0, w2, bh0, bh1);
+        } else {
+            const uint32_t h01 = pack_f16(w0, w1), h23 = pack_f16(w2, w3);
+            const uint32_t l01 = pack_f16(w0 - f16_lo(h01), w1 - f16_hi(h01));
+            const uint32_t l23 = pack_f16(w2 - f16_lo(h23), w3 - f16_hi(h23));
+            bh0 = movmatrix_trans(h01);
+            bh1 = movmatrix_trans(h23);
+            bl0 = movmatrix_trans(l01);
+            bl1 = movmatrix_trans(l23);
+        }
         // ---- O^T += V^T W^T ------------------------------------------------------------
         // After the transposing ldmatrix a thread holds tokens 2tig, 2tig + 1 (or 8 + ...)
         // of channels 2g8, 2g8 + 1 of a 16-channel chunk; codes of masked tokens are zeroed
@@ -833,11 +844,11 @@ struct Consumer {
             e4m3x4_to_f16(r0, a0, a1);
             e4m3x4_to_f16(r1, a2, a3);
             mma_f16(o[2 * c], a0, a1, a2, a3, bh0, bh1);
-            mma_f16(o[2 * c], a0, a1, a2, a3, bl0, bl1);
+            if (!g1) mma_f16(o[2 * c], a0, a1, a2, a3, bl0, bl1);
             e4m3x4_to_f16(r2, a0, a1);
             e4m3x4_to_f16(r3, a2, a3);
             mma_f16(o[2 * c + 1], a0, a1, a2, a3, bh0, bh1);
-            mma_f16(o[2 * c + 1], a0, a1, a2, a3, bl0, bl1);
+            if (!g1) mma_f16(o[2 * c + 1], a0, a1, a2, a3, bl0, bl1);
         }
     }
 
@@ -895,9 +906,19 @@ struct Consumer {
     // k of both halves is channel 4g8 + k of the two tokens: exactly an A fragment. M-tile mt
     // takes channels 32 (mt / 2) + 4g8 + 2 (mt % 2) + {0, 1} as its rows g8 and g8 + 8. Every
     // code is a finite value, so a masked row (weight 0) needs no zeroing.
-    // G1 (one query column, as in MHA decode): the hi and lo terms of the weights go to columns
-    // 0 and 1 of one B operand, so each m-tile takes one product instead of two; column 1 of
-    // the accumulator is then the lo part of column 0 (added when the piece is published).
+    // One query column (as in MHA decode): the hi and lo fp16 terms of column 0's weights (rows
+    // g8: w0, g8 + 8: w2) as columns 0 and 1 of one B operand, so that each m-tile of PV takes
+    // one product instead of two; column 1 of the accumulator is then the lo part of column 0,
+    // rescaled with it and added to it when the piece is published.
+    __device__ __forceinline__ void g1_weights(float w0, float w2, uint32_t& b0,
+                                               uint32_t& b1) const {
+        const float h0 = __half2float(__float2half_rn(w0)), h2 = __half2float(__float2half_rn(w2));
+        const bool c0 = (lane & 3) == 0;  // the lanes of column 0
+        b0 = movmatrix_trans(c0 ? pack_f16(h0, w0 - h0) : 0u);
+        b1 = movmatrix_trans(c0 ? pack_f16(h2, w2 - h2) : 0u);
+    }
+
+    // G1: one query column (g1_weights).
     template <bool G1>
     __device__ __forceinline__ void pv_i4(uint32_t vbase, float w0, float w1, float w2,
                                           float w3) {
@@ -907,12 +928,7 @@ struct Consumer {
         // W^T as the B operand: two fp16 terms, transposed with movmatrix
         uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
         if constexpr (G1) {
-            const float h0 = __half2float(__float2half_rn(w0)), h2 = __half2float(__float2half_rn(w2));
-            const bool c0 = (lane & 3) == 0;  // the lanes of column 0
-            const uint32_t h01 = c0 ? pack_f16(h0, w0 - h0) : 0u;
-            const uint32_t h23 = c0 ? pack_f16(h2, w2 - h2) : 0u;
-            bh0 = movmatrix_trans(h01);
-            bh1 = movmatrix_trans(h23);
+            g1_weights(w0, w2, bh0, bh1);
         } else {
             const uint32_t h01 = pack_f16(w0, w1), h23 = pack_f16(w2, w3);
             const uint32_t l01 = pack_f16(w0 - f16_lo(h01), w1 - f16_hi(h01));
@@ -1037,8 +1053,8 @@ struct Consumer {
                 // rows g8 and g8 + 8 of m-tile mt are channels dd and dd + 1 (4-bit: m-tile
                 // mt covers channels 32 (mt / 2) + 4 g8 + 2 (mt % 2) + {0, 1}, see tile_i4)
                 const int dd = f4 ? 32 * (mt >> 1) + 4 * g8 + 2 * (mt & 1) : mt * 16 + 2 * g8;
-                // 4-bit with one column: column 1 holds column 0's lo terms
-                const bool fold = f4 && p.gq == 1;
+                // one query column: column 1 holds column 0's lo terms (g1_weights)
+                const bool fold = p.gq == 1;
                 const float x0 = fold ? o[mt][0] + o[mt][1] : o[mt][0];
                 const float x2 = fold ? o[mt][2] + o[mt][3] : o[mt][2];
                 if (hA < p.gq)
