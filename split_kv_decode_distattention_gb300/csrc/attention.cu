@@ -450,7 +450,9 @@ __device__ __forceinline__ void write_final(const AttnParams& p, int32_t s, int3
 // when a tile brings a larger one). So 0 <= w_i <= 2^15 always fits fp16, and w_i is
 // split into two fp16 terms (22 significant bits) as the bf16 path splits p_i. The
 // accumulator is multiplied by r * 2^-15 when the piece is published.
-template <int D, int FMT>
+// PK: 2 or 4 query columns over a pool with 4-bit KV heads, whose PV weights take one
+// product per m-tile (see tile_i4).
+template <int D, int FMT, bool PK>
 struct Consumer {
     static constexpr int KS = D / 16;  // k-steps of QK^T and m-tiles of PV
     static constexpr bool Q = FMT != DATTN_KV_BF16;  // a quantized pool with row scales
@@ -458,6 +460,7 @@ struct Consumer {
     static constexpr bool MIX = FMT == DATTN_KV_MIXED;  // 8-bit or 4-bit per KV head
     static_assert(!I4 || Q, "the 4-bit pool is a quantized pool");
     static_assert(!MIX || Q, "the mixed pool is a quantized pool");
+    static_assert(!PK || I4 || MIX, "packed columns are a 4-bit form");
 
     const AttnParams& p;
     const Smem& sm;
@@ -477,6 +480,15 @@ struct Consumer {
     __device__ Consumer(const AttnParams& p_, const Smem& sm_, int w, int l)
         : p(p_), sm(sm_), warp(w), lane(l) {}
 
+    // The query column whose queries column c carries: itself, except in a packed (PK) piece of
+    // a 4-bit KV head (f4), whose columns repeat the queries of column c mod gq (tile_i4).
+    __device__ __forceinline__ int dup_col(int c, bool f4) const {
+        if constexpr (PK) {
+            if (f4) return c & (p.gq - 1);
+        }
+        return c;
+    }
+
     // Visibility of this lane's four logits (rows g8, g8 + 8; columns 2tig, 2tig + 1): the row
     // lies in [lo, hi) and, in a tile of multi-query decode that holds new tokens (cut < 15,
     // warp-uniform), row r is visible to column c's query token t = c / g iff r <= cut + t.
@@ -487,7 +499,8 @@ struct Consumer {
         a0 = a1 = v0;
         a2 = a3 = v1;
         if (cut < 15) {
-            const int tA = (2 * tig) / p.g, tB = (2 * tig + 1) / p.g;
+            const bool f4 = MIX ? i4 : I4;
+            const int tA = dup_col(2 * tig, f4) / p.g, tB = dup_col(2 * tig + 1, f4) / p.g;
             a0 = a0 && g8 <= cut + tA;
             a1 = a1 && g8 <= cut + tB;
             a2 = a2 && g8 + 8 <= cut + tA;
@@ -502,7 +515,8 @@ struct Consumer {
         const int32_t item = s / p.Hkv, kvh = s - item * p.Hkv;
         int32_t b = item;
         if (p.mode == MODE_PARTIAL) b = __ldg(p.chunk_req + item);
-        const int n = lane >> 2, tig = lane & 3;
+        const bool f4 = MIX ? head_is_i4(p.hf, kvh) : I4;
+        const int n = dup_col(lane >> 2, f4), tig = lane & 3;
         const bool ok = n < p.gq && b >= 0 && b < p.B;
         const int32_t t = ok ? n / p.g : 0, j = ok ? n - t * p.g : 0;
         const uint32_t* qv = reinterpret_cast<const uint32_t*>(
@@ -522,7 +536,6 @@ struct Consumer {
             // 4-bit: k-step ks takes channels c0 + {0..7} of the 32-channel chunk ks / 2,
             // c0 = 32 (ks / 2) + 8tig, in nibble pairs: sub-step ks % 2 = 0 has b0 = c0 + {0, 4}
             // and b1 = c0 + {1, 5}, sub-step 1 has b0 = c0 + {2, 6} and b1 = c0 + {3, 7}.
-            const bool f4 = MIX ? head_is_i4(p.hf, kvh) : I4;
             float mx = 0.f;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
@@ -656,19 +669,26 @@ struct Consumer {
     // heads 2tig and 2tig + 1. Returns the weights relative to the new running max.
     __device__ __forceinline__ void softmax(float s0, float s1, float s2, float s3, float& p0,
                                             float& p1, float& p2, float& p3) {
+        // the columns' maxima over the warp are needed only when some lane's logits exceed
+        // the running maxima (rarely, once a piece is under way); otherwise they stay
         float c0 = fmaxf(s0, s2), c1 = fmaxf(s1, s3);
+        float mn0 = m0, mn1 = m1;
+        const bool raise = __any_sync(0xffffffffu, c0 > m0 || c1 > m1);
+        if (raise) {
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            c0 = fmaxf(c0, __shfl_xor_sync(0xffffffffu, c0, off));
-            c1 = fmaxf(c1, __shfl_xor_sync(0xffffffffu, c1, off));
+            for (int off = 4; off < 32; off <<= 1) {
+                c0 = fmaxf(c0, __shfl_xor_sync(0xffffffffu, c0, off));
+                c1 = fmaxf(c1, __shfl_xor_sync(0xffffffffu, c1, off));
+            }
+            mn0 = fmaxf(m0, c0);
+            mn1 = fmaxf(m1, c1);
         }
-        const float mn0 = fmaxf(m0, c0), mn1 = fmaxf(m1, c1);
         const float mu0 = mn0 == kNegInf ? 0.f : mn0, mu1 = mn1 == kNegInf ? 0.f : mn1;
         p0 = ex2_approx(s0 - mu0);
         p1 = ex2_approx(s1 - mu1);
         p2 = ex2_approx(s2 - mu0);
         p3 = ex2_approx(s3 - mu1);
-        if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
+        if (raise) {
             const float al0 = ex2_approx(m0 - mu0), al1 = ex2_approx(m1 - mu1);
             e0 *= al0;
             e1 *= al1;
@@ -787,22 +807,7 @@ struct Consumer {
         softmax(s0, s1, s2, s3, p0, p1, p2, p3);
         // ---- V scales: raise r to a power of two >= every V scale of the tile ---------
         const float vs0 = v0 ? sc[16 + g8] : 0.f, vs1 = v1 ? sc[24 + g8] : 0.f;
-        float vt = fmaxf(vs0, vs1);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) vt = fmaxf(vt, __shfl_xor_sync(0xffffffffu, vt, off));
-        if (vt > rv) {  // warp-uniform; vt > 2^-112 is a normal number
-            const int32_t bits = __float_as_int(vt);
-            const int32_t k = min(127, ((bits >> 23) & 0xff) - 127 + ((bits & 0x7fffff) != 0));
-            const int32_t dk = rk - k;
-            const float f = dk >= -126 ? __int_as_float((127 + dk) << 23) : 0.f;
-#pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                o[mt][0] *= f; o[mt][1] *= f; o[mt][2] *= f; o[mt][3] *= f;
-            }
-            rk = k;
-            rv = __int_as_float((127 + k) << 23);
-            inv = __int_as_float((142 - k) << 23);
-        }
+        raise_r(fmaxf(vs0, vs1));
         const float vn0 = vs0 * inv, vn1 = vs1 * inv;  // in [0, 2^15], exact
         const float w0 = p0 * vn0, w1 = p1 * vn0, w2 = p2 * vn1, w3 = p3 * vn1;
         // ---- W^T as the B operand: two fp16 terms, transposed with movmatrix ----------
@@ -880,10 +885,12 @@ struct Consumer {
         }
     }
 
-    // Raises r to a power of two >= vt (the largest V scale of the tiles at hand, reduced over
-    // the warp), rescaling O, exactly as tile_f8 does.
-    __device__ __forceinline__ void raise_r(float vt) {
-        if (vt > rv) {  // warp-uniform; vt > 2^-112 is a normal number
+    // Raises r to a power of two >= every lane's vl (the largest V scale of its rows), rescaling
+    // O (and the 4-bit weight sums). The maximum over the warp is taken only when some lane's
+    // exceeds r.
+    __device__ __forceinline__ void raise_r(float vl) {
+        if (__any_sync(0xffffffffu, vl > rv)) {
+            const float vt = warp_vmax(vl);  // > r >= 2^-112: a normal number
             const int32_t bits = __float_as_int(vt);
             const int32_t k = min(127, ((bits >> 23) & 0xff) - 127 + ((bits & 0x7fffff) != 0));
             const int32_t dk = rk - k;
@@ -906,10 +913,16 @@ struct Consumer {
     // k of both halves is channel 4g8 + k of the two tokens: exactly an A fragment. M-tile mt
     // takes channels 32 (mt / 2) + 4g8 + 2 (mt % 2) + {0, 1} as its rows g8 and g8 + 8. Every
     // code is a finite value, so a masked row (weight 0) needs no zeroing.
-    // One query column (as in MHA decode): the hi and lo fp16 terms of column 0's weights (rows
-    // g8: w0, g8 + 8: w2) as columns 0 and 1 of one B operand, so that each m-tile of PV takes
-    // one product instead of two; column 1 of the accumulator is then the lo part of column 0,
-    // rescaled with it and added to it when the piece is published.
+    // The weights enter as two fp16 terms, hi and lo. With 8 query columns (kPvTwo) each m-tile
+    // takes two products, one per term. One query column (kPvOne, as in MHA decode): the hi
+    // and lo terms of column 0's weights (rows g8: w0, g8 + 8: w2) as columns 0 and 1 of one B
+    // operand (g1_weights), so that each m-tile takes one product; column 1 of the accumulator
+    // is then the lo part of column 0, rescaled with it and added to it when the piece is
+    // published. 2 or 4 query columns (kPvPacked, a PK consumer): every column carries the
+    // queries of column c mod gq (dup_col), so the lanes of columns c and c + gq hold the same
+    // logits, running maxima and weights; columns [0, gq) take the hi terms and [gq, 2gq) the
+    // lo terms, again one product per m-tile, and the accumulator's columns [gq, 2gq), rescaled
+    // exactly as columns [0, gq), are added to them at publish.
     __device__ __forceinline__ void g1_weights(float w0, float w2, uint32_t& b0,
                                                uint32_t& b1) const {
         const float h0 = __half2float(__float2half_rn(w0)), h2 = __half2float(__float2half_rn(w2));
@@ -918,17 +931,26 @@ struct Consumer {
         b1 = movmatrix_trans(c0 ? pack_f16(h2, w2 - h2) : 0u);
     }
 
-    // G1: one query column (g1_weights).
-    template <bool G1>
+    static constexpr int kPvTwo = 0, kPvOne = 1, kPvPacked = 2;
+    template <int M>
     __device__ __forceinline__ void pv_i4(uint32_t vbase, float w0, float w1, float w2,
                                           float w3) {
         constexpr uint32_t RB = D / 2;
+        constexpr bool G1 = M != kPvTwo;  // one product per m-tile
         const uint32_t row = (lane & 7) + ((lane >> 3) & 1) * 8;
         const uint32_t csel = lane >> 4;
         // W^T as the B operand: two fp16 terms, transposed with movmatrix
         uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
-        if constexpr (G1) {
+        if constexpr (M == kPvOne) {
             g1_weights(w0, w2, bh0, bh1);
+        } else if constexpr (M == kPvPacked) {
+            const uint32_t h01 = pack_f16(w0, w1), h23 = pack_f16(w2, w3);
+            const uint32_t l01 = pack_f16(w0 - f16_lo(h01), w1 - f16_hi(h01));
+            const uint32_t l23 = pack_f16(w2 - f16_lo(h23), w3 - f16_hi(h23));
+            const int c0 = 2 * (lane & 3);  // this lane's columns c0, c0 + 1 (gq = 2 or 4)
+            const bool hi = c0 < p.gq, lo = !hi && c0 < 2 * p.gq;
+            bh0 = movmatrix_trans(hi ? h01 : lo ? l01 : 0u);
+            bh1 = movmatrix_trans(hi ? h23 : lo ? l23 : 0u);
         } else {
             const uint32_t h01 = pack_f16(w0, w1), h23 = pack_f16(w2, w3);
             const uint32_t l01 = pack_f16(w0 - f16_lo(h01), w1 - f16_hi(h01));
@@ -998,13 +1020,14 @@ struct Consumer {
         float p0, p1, p2, p3;
         softmax(s0, s1, s2, s3, p0, p1, p2, p3);
         const float vs0 = v0 ? sc[16 + g8] : 0.f, vs1 = v1 ? sc[24 + g8] : 0.f;
-        raise_r(warp_vmax(fmaxf(vs0, vs1)));
+        raise_r(fmaxf(vs0, vs1));
         const float vn0 = vs0 * inv, vn1 = vs1 * inv;  // in [0, 2^15], exact
         const float w0 = p0 * vn0, w1 = p1 * vn0, w2 = p2 * vn1, w3 = p3 * vn1;
         ws0 += w0 + w2;
         ws1 += w1 + w3;
-        if (p.gq == 1) pv_i4<true>(st + 8u * D, w0, w1, w2, w3);
-        else           pv_i4<false>(st + 8u * D, w0, w1, w2, w3);
+        if constexpr (PK)  pv_i4<kPvPacked>(st + 8u * D, w0, w1, w2, w3);
+        else if (p.gq == 1) pv_i4<kPvOne>(st + 8u * D, w0, w1, w2, w3);
+        else               pv_i4<kPvTwo>(st + 8u * D, w0, w1, w2, w3);
     }
 
     // Publishes this warp's state for the CTA-level merge of the piece.
@@ -1053,16 +1076,28 @@ struct Consumer {
                 // rows g8 and g8 + 8 of m-tile mt are channels dd and dd + 1 (4-bit: m-tile
                 // mt covers channels 32 (mt / 2) + 4 g8 + 2 (mt % 2) + {0, 1}, see tile_i4)
                 const int dd = f4 ? 32 * (mt >> 1) + 4 * g8 + 2 * (mt & 1) : mt * 16 + 2 * g8;
-                // one query column: column 1 holds column 0's lo terms (g1_weights)
-                const bool fold = p.gq == 1;
-                const float x0 = fold ? o[mt][0] + o[mt][1] : o[mt][0];
-                const float x2 = fold ? o[mt][2] + o[mt][3] : o[mt][2];
+                // the lo parts of the weights' products: one query column, column 1
+                // (g1_weights); a packed 4-bit piece, the lane gq/2 to the right (pv_i4)
+                float x0 = o[mt][0], x1 = o[mt][1], x2 = o[mt][2], x3 = o[mt][3];
+                if (p.gq == 1) {
+                    x0 += x1;
+                    x2 += x3;
+                }
+                if constexpr (PK) {
+                    if (f4) {
+                        const int src = lane + (p.gq >> 1);  // columns c + gq (tig < gq/2)
+                        x0 += __shfl_sync(0xffffffffu, o[mt][0], src & 31);
+                        x1 += __shfl_sync(0xffffffffu, o[mt][1], src & 31);
+                        x2 += __shfl_sync(0xffffffffu, o[mt][2], src & 31);
+                        x3 += __shfl_sync(0xffffffffu, o[mt][3], src & 31);
+                    }
+                }
                 if (hA < p.gq)
                     *reinterpret_cast<float2*>(wo + hA * D + dd) =
                         make_float2((x0 * ke - b0) * rs, (x2 * ko - b0) * rs);
                 if (hB < p.gq)
                     *reinterpret_cast<float2*>(wo + hB * D + dd) =
-                        make_float2((o[mt][1] * ke - b1) * rs, (o[mt][3] * ko - b1) * rs);
+                        make_float2((x1 * ke - b1) * rs, (x3 * ko - b1) * rs);
             }
         }
     }
@@ -1172,7 +1207,7 @@ constexpr int attn_min_blocks() { return (D == 64 || FMT == DATTN_KV_INT4) ? 4 :
 // APP: the launch of dattn_append_decode (the one-token append fused into the decode). It is
 // a template parameter so that the plain decode carries none of the append's code and
 // registers.
-template <int D, int FMT, bool APP>
+template <int D, int FMT, bool APP, bool PK>
 __global__ void __launch_bounds__(kAttnThreads, attn_min_blocks<D, FMT>())
 attention_kernel(const __grid_constant__ AttnParams p,
                  const __grid_constant__ CUtensorMap tmap_k,
@@ -1501,13 +1536,13 @@ attention_kernel(const __grid_constant__ AttnParams p,
         }
     }
     if (!any) return;
-    Consumer<D, FMT> cons(p, sm, warp, lane);
+    Consumer<D, FMT, PK> cons(p, sm, warp, lane);
     const uint32_t stage0 = smem_u32(sm.base + sm.L.stages);
     int32_t kbase = 0;  // real tiles of earlier pieces
     int32_t cur = cur0;
     Piece pc = first;
     bool have = true;
-    uint32_t qn[Consumer<D, FMT>::KS][2];
+    uint32_t qn[Consumer<D, FMT, PK>::KS][2];
     float qsn = 0.f;
     // the 4-bit pool fetches each piece's query at its start (registers for four CTAs per SM)
     constexpr bool kPrefetchQ = FMT != DATTN_KV_INT4;
@@ -1516,7 +1551,7 @@ attention_kernel(const __grid_constant__ AttnParams p,
     while (have) {
         if constexpr (kPrefetchQ) {
 #pragma unroll
-            for (int ks = 0; ks < Consumer<D, FMT>::KS; ++ks) {
+            for (int ks = 0; ks < Consumer<D, FMT, PK>::KS; ++ks) {
                 cons.qf[ks][0] = qn[ks][0];
                 cons.qf[ks][1] = qn[ks][1];
             }
@@ -1544,8 +1579,8 @@ attention_kernel(const __grid_constant__ AttnParams p,
         }
         cons.reset();
         if constexpr (FMT == DATTN_KV_MIXED) cons.i4 = head_is_i4(p.hf, pc.s % p.Hkv);
-        if constexpr (Consumer<D, FMT>::Q) {
-            if constexpr (APP) cons.quant_new_row(pc.s, Consumer<D, FMT>::I4 || cons.i4);
+        if constexpr (Consumer<D, FMT, PK>::Q) {
+            if constexpr (APP) cons.quant_new_row(pc.s, Consumer<D, FMT, PK>::I4 || cons.i4);
         }
         const int32_t s = pc.s;
         const int32_t nr = pc.r1 - pc.r0;
@@ -1711,7 +1746,7 @@ struct KernelInfo {
     int max_smem_set = 0;
 };
 
-template <int D, int FMT, bool APP>
+template <int D, int FMT, bool APP, bool PK>
 KernelInfo& kernel_info() {
     static KernelInfo info;
     return info;
@@ -1719,12 +1754,12 @@ KernelInfo& kernel_info() {
 
 std::mutex g_attr_mutex;
 
-template <int D, int FMT, bool APP>
+template <int D, int FMT, bool APP, bool PK>
 dattn_status_t ensure_smem(uint32_t bytes) {
     std::lock_guard<std::mutex> lock(g_attr_mutex);
-    KernelInfo& ki = kernel_info<D, FMT, APP>();
+    KernelInfo& ki = kernel_info<D, FMT, APP, PK>();
     if ((int)bytes > ki.max_smem_set) {
-        if (cudaFuncSetAttribute(attention_kernel<D, FMT, APP>,
+        if (cudaFuncSetAttribute(attention_kernel<D, FMT, APP, PK>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bytes) != cudaSuccess)
             return DATTN_ERR_CUDA;
@@ -1733,10 +1768,10 @@ dattn_status_t ensure_smem(uint32_t bytes) {
     return DATTN_OK;
 }
 
-template <int D, int FMT, bool APP>
+template <int D, int FMT, bool APP, bool PK>
 int occupancy(uint32_t smem) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attention_kernel<D, FMT, APP>, kAttnThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attention_kernel<D, FMT, APP, PK>, kAttnThreads,
                                                       smem) != cudaSuccess)
         return 1;
     return n < 1 ? 1 : n;
@@ -1749,16 +1784,16 @@ size_t attn_workspace_bytes(int32_t nseg, int32_t g, int32_t D, int32_t G) {
 }
 
 
-template <int D, int FMT, bool APP>
+template <int D, int FMT, bool APP, bool PK>
 static dattn_status_t launch_d(const AttnParams& p0, const void* k_pool, const void* v_pool,
                                int32_t num_splits, void* ws, size_t ws_bytes,
                                cudaStream_t stream, int64_t tiles_bound) {
     AttnParams p = p0;
     const AttnSmem L =
         attn_smem_layout(D, p.gq, p.nitems, p.Hkv, p.mode == MODE_SPARSE, FMT, APP);
-    dattn_status_t st = ensure_smem<D, FMT, APP>(L.total);
+    dattn_status_t st = ensure_smem<D, FMT, APP, PK>(L.total);
     if (st != DATTN_OK) return st;
-    const int32_t G = choose_splits(tiles_bound, num_splits, occupancy<D, FMT, APP>(L.total));
+    const int32_t G = choose_splits(tiles_bound, num_splits, occupancy<D, FMT, APP, PK>(L.total));
     const size_t counters = attn_counter_bytes(p.nseg);
     if (ws == nullptr || ws_bytes < attn_workspace_bytes(p.nseg, p.gq, D, G) ||
         (reinterpret_cast<uintptr_t>(ws) & 255))
@@ -1796,7 +1831,7 @@ static dattn_status_t launch_d(const AttnParams& p0, const void* k_pool, const v
         if ((st = make_kv_tensor_map_u8(&tv, v_pool, rows, row_bytes)) != DATTN_OK) return st;
     }
     if constexpr (FMT != DATTN_KV_MIXED) tk4 = tk, tv4 = tv;  // not read
-    if (launch_pdl(attention_kernel<D, FMT, APP>, dim3(G), dim3(kAttnThreads), L.total, stream, p, tk,
+    if (launch_pdl(attention_kernel<D, FMT, APP, PK>, dim3(G), dim3(kAttnThreads), L.total, stream, p, tk,
                    tv, tk4, tv4) != cudaSuccess)
         return DATTN_ERR_CUDA;
     return DATTN_OK;
@@ -1806,26 +1841,21 @@ dattn_status_t launch_attention(const AttnParams& p, const void* k_pool, const v
                                 int D, int32_t num_splits, void* ws, size_t ws_bytes,
                                 cudaStream_t stream, int64_t tiles_bound) {
     if (D != 64 && D != 128) return DATTN_ERR_UNSUPPORTED;
-    auto pick = [&](auto bf16, auto f8, auto i4, auto mix) {
-        return p.fmt == DATTN_KV_MIXED    ? mix
-             : p.fmt == DATTN_KV_INT4     ? i4
+    // 2 or 4 query columns over a pool with 4-bit heads: the packed-column consumers
+    const bool pk = (p.fmt == DATTN_KV_INT4 || p.fmt == DATTN_KV_MIXED) && (p.gq == 2 || p.gq == 4);
+    auto pick = [&](auto bf16, auto f8, auto i4, auto mix, auto i4p, auto mixp) {
+        return p.fmt == DATTN_KV_MIXED    ? (pk ? mixp : mix)
+             : p.fmt == DATTN_KV_INT4     ? (pk ? i4p : i4)
              : p.fmt == DATTN_KV_FP8_E4M3 ? f8
                                           : bf16;
     };
-    auto launch =
-        p.append != 0
-            ? (D == 64 ? pick(launch_d<64, DATTN_KV_BF16, true>, launch_d<64, DATTN_KV_FP8_E4M3, true>,
-                              launch_d<64, DATTN_KV_INT4, true>, launch_d<64, DATTN_KV_MIXED, true>)
-                       : pick(launch_d<128, DATTN_KV_BF16, true>,
-                              launch_d<128, DATTN_KV_FP8_E4M3, true>,
-                              launch_d<128, DATTN_KV_INT4, true>, launch_d<128, DATTN_KV_MIXED, true>))
-            : (D == 64 ? pick(launch_d<64, DATTN_KV_BF16, false>,
-                              launch_d<64, DATTN_KV_FP8_E4M3, false>,
-                              launch_d<64, DATTN_KV_INT4, false>, launch_d<64, DATTN_KV_MIXED, false>)
-                       : pick(launch_d<128, DATTN_KV_BF16, false>,
-                              launch_d<128, DATTN_KV_FP8_E4M3, false>,
-                              launch_d<128, DATTN_KV_INT4, false>,
-                              launch_d<128, DATTN_KV_MIXED, false>));
+#define DATTN_LAUNCHES(D_, APP_)                                                                \
+    pick(launch_d<D_, DATTN_KV_BF16, APP_, false>, launch_d<D_, DATTN_KV_FP8_E4M3, APP_, false>,  \
+         launch_d<D_, DATTN_KV_INT4, APP_, false>, launch_d<D_, DATTN_KV_MIXED, APP_, false>,     \
+         launch_d<D_, DATTN_KV_INT4, APP_, true>, launch_d<D_, DATTN_KV_MIXED, APP_, true>)
+    auto launch = p.append != 0 ? (D == 64 ? DATTN_LAUNCHES(64, true) : DATTN_LAUNCHES(128, true))
+                                : (D == 64 ? DATTN_LAUNCHES(64, false) : DATTN_LAUNCHES(128, false));
+#undef DATTN_LAUNCHES
     return launch(p, k_pool, v_pool, num_splits, ws, ws_bytes, stream, tiles_bound);
 }
 

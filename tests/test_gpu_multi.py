@@ -73,6 +73,8 @@ MULTI_CASES = [
     (64, 16, 2, 64, [700], 1, 0, "fp8"),                  # T = 1, group 8
     (128, 8, 8, 16, [517, 2000], 3, 5, "int4"),           # 4-bit pool, odd T
     (64, 8, 4, 64, [999, 3, 2048], 2, 0, "int4"),         # 4-bit pool, d = 64, group 2
+    (128, 4, 4, 16, [300, 1, 40, 17], 2, 0, "int4"),      # 4-bit pool, MHA, T = 2: 2 columns
+    (128, 8, 8, 16, [517, 2, 100], 4, 3, "int4"),         # 4-bit pool, MHA, T = 4: 4 columns
 ]
 
 
