@@ -468,7 +468,8 @@ struct Consumer {
     uint32_t qf[KS][2];
     float o[KS][4];
     float m0, m1, e0, e1;
-    float qsc;     // scale * log2(e) (8-bit pool: times 2^-a) for the current piece's query
+    float qsc;     // scale * log2(e) (quantized pools: times 2^-a; 4-bit: times 2^24) for the
+                   // current piece's query
     int32_t rk;    // 8-bit pool: r = 2^rk bounds the V scales seen in this piece
     float rv, inv;  // 8-bit pool: r and 2^15 / r
     bool i4 = I4;   // the current piece's KV head is 4-bit (set per piece in a mixed pool)
@@ -505,6 +506,25 @@ struct Consumer {
             a1 = a1 && g8 <= cut + tB;
             a2 = a2 && g8 + 8 <= cut + tA;
             a3 = a3 && g8 + 8 <= cut + tB;
+        }
+    }
+
+    // Masks a quantized tile's logits (rows g8: s0, s1; g8 + 8: s2, s3) to -inf and its V
+    // scales (vs0, vs1) to 0 where visible() hides them. Full tiles, the common case, skip it
+    // (warp-uniform).
+    __device__ __forceinline__ void mask_tile(int lo, int hi, int cut, float& s0, float& s1,
+                                              float& s2, float& s3, float& vs0,
+                                              float& vs1) const {
+        if (lo > 0 || hi < 16 || cut < 15) {
+            const int g8 = lane >> 2;
+            bool a0, a1, a2, a3;
+            visible(lo, hi, cut, a0, a1, a2, a3);
+            s0 = a0 ? s0 : kNegInf;
+            s1 = a1 ? s1 : kNegInf;
+            s2 = a2 ? s2 : kNegInf;
+            s3 = a3 ? s3 : kNegInf;
+            vs0 = g8 >= lo && g8 < hi ? vs0 : 0.f;
+            vs1 = g8 + 8 >= lo && g8 + 8 < hi ? vs1 : 0.f;
         }
     }
 
@@ -573,7 +593,8 @@ struct Consumer {
                     qsum += (f16_lo(dst[ks][0]) + f16_hi(dst[ks][0])) +
                             16.f * (f16_lo(dst[ks][1]) + f16_hi(dst[ks][1]));
             }
-            qs = p.sl2 * down;
+            // 4-bit: times 2^24, the scale of the subnormal codes (exact)
+            qs = f4 ? (p.sl2 * down) * 16777216.f : p.sl2 * down;
             qcs[0] = qcs[1] = 0.f;
             if (f4) {
                 // the sum of column g8 over its four lanes, then columns 2tig, 2tig + 1
@@ -795,18 +816,14 @@ struct Consumer {
             e4m3x4_to_f16(r3, a1, a3);
             mma_f16(sb, a0, a1, a2, a3, qf[2 * c + 1][0], qf[2 * c + 1][1]);
         }
-        const bool v0 = g8 >= lo && g8 < hi, v1 = g8 + 8 >= lo && g8 + 8 < hi;
         const float kc0 = sc[g8] * qsc, kc1 = sc[g8 + 8] * qsc;
-        bool a0, a1, a2, a3;
-        visible(lo, hi, cut, a0, a1, a2, a3);
-        const float s0 = a0 ? (sa[0] + sb[0]) * kc0 : kNegInf;
-        const float s1 = a1 ? (sa[1] + sb[1]) * kc0 : kNegInf;
-        const float s2 = a2 ? (sa[2] + sb[2]) * kc1 : kNegInf;
-        const float s3 = a3 ? (sa[3] + sb[3]) * kc1 : kNegInf;
+        float s0 = (sa[0] + sb[0]) * kc0, s1 = (sa[1] + sb[1]) * kc0;
+        float s2 = (sa[2] + sb[2]) * kc1, s3 = (sa[3] + sb[3]) * kc1;
+        float vs0 = sc[16 + g8], vs1 = sc[24 + g8];
+        mask_tile(lo, hi, cut, s0, s1, s2, s3, vs0, vs1);
         float p0, p1, p2, p3;
         softmax(s0, s1, s2, s3, p0, p1, p2, p3);
         // ---- V scales: raise r to a power of two >= every V scale of the tile ---------
-        const float vs0 = v0 ? sc[16 + g8] : 0.f, vs1 = v1 ? sc[24 + g8] : 0.f;
         raise_r(fmaxf(vs0, vs1));
         const float vn0 = vs0 * inv, vn1 = vs1 * inv;  // in [0, 2^15], exact
         const float w0 = p0 * vn0, w1 = p1 * vn0, w2 = p2 * vn1, w3 = p3 * vn1;
@@ -1001,25 +1018,21 @@ struct Consumer {
     // One tile of the 4-bit pool; rows are masked as in tile(). The codes enter the products
     // as n * 2^-24 (n = code + 8; odd nibbles 16 n * 2^-24 against a query divided by 16), so
     // the raw products are 2^-24 (q' . n): the logit subtracts 8 * 2^-24 * (sum of q') (qc)
-    // and scales by 2^24; the PV accumulator's offset, 8 * 2^-24 * (sum of the weights), is
+    // and scales by 2^24 (in qsc); the PV accumulator's offset, 8 * 2^-24 * (sum of the weights), is
     // taken out when the piece is published (ws0, ws1 keep those sums). Both corrections are
     // of the size of the values they correct, so nothing cancels catastrophically.
     __device__ void tile_i4(uint32_t st, const float* sc, int lo, int hi, int cut) {
         const int g8 = lane >> 2;
+        // the offset correction -qc enters as the products' initial accumulator
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
         qk_i4(st, sa, sb);
-        const bool v0 = g8 >= lo && g8 < hi, v1 = g8 + 8 >= lo && g8 + 8 < hi;
-        const float kc0 = sc[g8] * qsc, kc1 = sc[g8 + 8] * qsc;
-        bool a0, a1, a2, a3;
-        visible(lo, hi, cut, a0, a1, a2, a3);
-        constexpr float k24 = 16777216.f;  // 2^24
-        const float s0 = a0 ? ((sa[0] + sb[0]) - qc[0]) * k24 * kc0 : kNegInf;
-        const float s1 = a1 ? ((sa[1] + sb[1]) - qc[1]) * k24 * kc0 : kNegInf;
-        const float s2 = a2 ? ((sa[2] + sb[2]) - qc[0]) * k24 * kc1 : kNegInf;
-        const float s3 = a3 ? ((sa[3] + sb[3]) - qc[1]) * k24 * kc1 : kNegInf;
+        const float kc0 = sc[g8] * qsc, kc1 = sc[g8 + 8] * qsc;  // qsc carries the codes' 2^24
+        float s0 = ((sa[0] + sb[0]) - qc[0]) * kc0, s1 = ((sa[1] + sb[1]) - qc[1]) * kc0;
+        float s2 = ((sa[2] + sb[2]) - qc[0]) * kc1, s3 = ((sa[3] + sb[3]) - qc[1]) * kc1;
+        float vs0 = sc[16 + g8], vs1 = sc[24 + g8];
+        mask_tile(lo, hi, cut, s0, s1, s2, s3, vs0, vs1);
         float p0, p1, p2, p3;
         softmax(s0, s1, s2, s3, p0, p1, p2, p3);
-        const float vs0 = v0 ? sc[16 + g8] : 0.f, vs1 = v1 ? sc[24 + g8] : 0.f;
         raise_r(fmaxf(vs0, vs1));
         const float vn0 = vs0 * inv, vn1 = vs1 * inv;  // in [0, 2^15], exact
         const float w0 = p0 * vn0, w1 = p1 * vn0, w2 = p2 * vn1, w3 = p3 * vn1;
