@@ -71,7 +71,11 @@ __host__ __device__ inline int next_pow2(int x) {
     return n;
 }
 
-constexpr int kSelBT = 1024;  // block-table entries staged in shared memory at once
+// Block-table entries staged in shared memory at once. A CTA's range of one head is restaged
+// (its copies drained first) every kSelBT pages; 4096 covers the range of a CTA at the
+// sizes measured (1724 pages per CTA at 512K tokens, batch 8): 1024 took 115.4 µs, 4096
+// 112.9 µs.
+constexpr int kSelBT = 4096;
 
 struct SelSmem {
     uint32_t flags, stage, bars, masks, batches, bt, wbuf, ret_before, ret_heads, item_start,
