@@ -192,6 +192,46 @@ def test_mixed_decode_dense_matches_oracle(spec, d, Hq, P, lens, splits):
     assert torch.equal(out, out2)
 
 
+@pytest.mark.parametrize("spec,Hq,lens,T,splits", [
+    ("48", 4, [700, 2, 1500], 2, 0),       # group 2, 2 query tokens: 4 columns per KV head
+    ("4884", 4, [517, 3, 64], 4, 5),       # MHA, 4 query tokens: 4 columns
+    ("84", 2, [300, 1000], 2, 0),          # MHA, 2 query tokens: 2 columns
+    ("48", 4, [900, 5], 3, 0),             # group 2, 3 query tokens: 6 columns
+])
+def test_mixed_decode_multi_matches_oracle(spec, Hq, lens, T, splits):
+    """Multi-query decode over the mixed pool: query token t of request b attends tokens
+    0 .. L_b - T + t of each head in that head's own format."""
+    dattn = _lib()
+    case = W.Case("multi-mixed", B=len(lens), Hq=Hq, Hkv=len(spec), d=128, P=16, lens=lens,
+                  seed=(sum(map(ord, spec)) + Hq + T + sum(lens)) % 1000 + 11)
+    cache = _cache(case, spec)
+    q = torch.stack([case.q(200 + t, DEV) for t in range(T)], dim=1).contiguous()
+    out = torch.full((case.B, T, Hq, case.d), float("nan"), device=DEV)
+    m_g = torch.full((case.B, T, Hq), float("nan"), device=DEV)
+    e_g = torch.full((case.B, T, Hq), float("nan"), device=DEV)
+    ws = dattn.Workspace(case.B, T * Hq, case.Hkv, case.d, num_splits=splits)
+    dattn.dattn_decode_multi(cache.layout, cache.k_pool, cache.v_pool, q, case.scale,
+                             cache.seq_lens, out, ws, m_g=m_g, e_g=e_g, num_splits=splits,
+                             dev_err=cache.dev_err)
+    torch.cuda.synchronize()
+    assert int(cache.dev_err.item()) == 0
+    qb = oracle.bf16_bits(q)
+    o, mg, eg = out.cpu().numpy(), m_g.cpu().numpy(), e_g.cpu().numpy()
+    for b in range(case.B):
+        L = cache.lens[b]
+        Kd, Vd = _deq(*host_kv(case, b, L, DEV), spec)
+        for t in range(T):
+            rows = np.arange(max(0, L - T + t + 1), dtype=np.int64)
+            for h in range(Hq):
+                kvh = h // case.g
+                r, rm, re = oracle.attention_f64(qb[b, t, h], Kd[:, kvh], Vd[:, kvh],
+                                                 case.scale, rows=rows)
+                tag = f"mixed multi b={b} t={t} h={h} ({spec[kvh]}-bit head)"
+                assert_out_close(o[b, t, h], r, tag)
+                assert_m_close(mg[b, t, h], rm, tag)
+                assert_e_close(eg[b, t, h], re, tag)
+
+
 def test_mixed_partial_then_merge():
     """Partials over 4 chunks of 1024 tokens of a mixed pool, then the merge."""
     dattn = _lib()
