@@ -76,6 +76,12 @@ __host__ __device__ inline int next_pow2(int x) {
 // sizes measured (1724 pages per CTA at 512K tokens, batch 8): 1024 took 115.4 µs, 4096
 // 112.9 µs.
 constexpr int kSelBT = 4096;
+// Units of fixed cost per retrieval (request, KV head) in the split: the query fetch, the
+// block-table staging and pipeline fill, and the lists' merge and hand-off of a piece. The
+// split cuts pages plus these units evenly, so a CTA whose range starts a head takes fewer
+// pages. Measured at 512K tokens, batch 8 (1724 pages per CTA): 0 units 112.6 µs, 64 110.6,
+// 160 108.3, 256 104.5, 384 and 512 106.5.
+constexpr int kSelSegCost = 256;
 
 struct SelSmem {
     uint32_t flags, stage, bars, masks, batches, bt, wbuf, ret_before, ret_heads, item_start,
@@ -283,7 +289,8 @@ page_select_kernel(const __grid_constant__ SelParams p) {
                 Lb = min(max(Lb, 0), cap);
             }
             item_len[i] = Lb;
-            const int32_t cnt = nret * ((Lb + p.P - 1) / p.P);
+            const int32_t np = (Lb + p.P - 1) / p.P;
+            const int32_t cnt = nret * (np > 0 ? np + kSelSegCost : 0);
             item_start[i] = cnt;
             local_sum += cnt;
         }
@@ -311,21 +318,23 @@ page_select_kernel(const __grid_constant__ SelParams p) {
     }
     const int32_t W = item_start[p.B];
     auto npages_of = [&](int32_t b) { return (item_len[b] + p.P - 1) / p.P; };
+    // A retrieval segment of n > 0 pages spans n + kSelSegCost positions of the split: its
+    // fixed cost, then its pages. st: the span's first position; len: n (0 for other heads).
     auto seg_span = [&](int32_t s, int32_t& st, int32_t& len) {
         const int32_t b = s / p.Hkv, h = s - b * p.Hkv;
         const int32_t n = npages_of(b);
         const bool ret = p.head_kind[h] == DATTN_HEAD_RETRIEVAL;
-        st = item_start[b] + ret_before[h] * n;
+        st = item_start[b] + ret_before[h] * (n > 0 ? n + kSelSegCost : 0);
         len = ret ? n : 0;
     };
-    auto locate = [&](int32_t t) {  // segment containing unit t
+    auto locate = [&](int32_t t) {  // segment whose span holds position t
         int32_t lo = 0, hi = p.B - 1;
         while (lo < hi) {
             const int32_t mid = (lo + hi + 1) >> 1;
             if (item_start[mid] <= t) lo = mid; else hi = mid - 1;
         }
         const int32_t n = npages_of(lo);
-        const int32_t r = (t - item_start[lo]) / n;
+        const int32_t r = (t - item_start[lo]) / (n + kSelSegCost);
         return lo * p.Hkv + ret_heads[r];
     };
     // only the first min(G, W) CTAs take units, so each participating CTA owns at least one
@@ -427,13 +436,21 @@ page_select_kernel(const __grid_constant__ SelParams p) {
         }
     };
 
-    int32_t a = t_begin;
+    int32_t apos = t_begin;  // position in the split
     int32_t s = locate(t_begin);
-    while (a < t_end && !*abort_flag) {
-        int32_t sst, slen;
-        seg_span(s, sst, slen);
-        while (sst + slen <= a) { ++s; seg_span(s, sst, slen); }
-        const int32_t pe = min(sst + slen, t_end);
+    while (apos < t_end && !*abort_flag) {
+        int32_t sst0, slen;
+        seg_span(s, sst0, slen);
+        while (slen == 0 || sst0 + kSelSegCost + slen <= apos) {
+            if (++s >= p.nseg) break;
+            seg_span(s, sst0, slen);
+        }
+        if (s >= p.nseg) break;
+        // the piece: the segment's pages within [apos, t_end), in page positions a .. pe of the
+        // segment's own pages sst .. sst + slen
+        const int32_t sst = sst0 + kSelSegCost;
+        const int32_t a = max(apos, sst), pe = min(sst + slen, t_end);
+        if (a >= pe) break;  // the range ends within the segment's fixed cost
         const int32_t b = s / p.Hkv, h = s - b * p.Hkv;
         const int32_t Lb = item_len[b];
         // B fragments of [max(q,0) | min(q,0)]^T: lane holds column (query head) g8 at the
@@ -671,7 +688,7 @@ page_select_kernel(const __grid_constant__ SelParams p) {
             }
         }
         csync();
-        a = pe;
+        apos = pe;
     }
 }
 
