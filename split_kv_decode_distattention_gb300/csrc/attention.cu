@@ -450,8 +450,8 @@ __device__ __forceinline__ void write_final(const AttnParams& p, int32_t s, int3
 // when a tile brings a larger one). So 0 <= w_i <= 2^15 always fits fp16, and w_i is
 // split into two fp16 terms (22 significant bits) as the bf16 path splits p_i. The
 // accumulator is multiplied by r * 2^-15 when the piece is published.
-// PK: 2 or 4 query columns over a pool with 4-bit KV heads, whose PV weights take one
-// product per m-tile (see tile_i4).
+// PK: 2 or 4 query columns over the 4-bit pool, whose PV weights take one product per m-tile
+// (see tile_i4). (A mixed-pool instance would work the same way for its 4-bit heads.)
 template <int D, int FMT, bool PK>
 struct Consumer {
     static constexpr int KS = D / 16;  // k-steps of QK^T and m-tiles of PV
@@ -1854,10 +1854,12 @@ dattn_status_t launch_attention(const AttnParams& p, const void* k_pool, const v
                                 int D, int32_t num_splits, void* ws, size_t ws_bytes,
                                 cudaStream_t stream, int64_t tiles_bound) {
     if (D != 64 && D != 128) return DATTN_ERR_UNSUPPORTED;
-    // 2 or 4 query columns over a pool with 4-bit heads: the packed-column consumers
-    const bool pk = (p.fmt == DATTN_KV_INT4 || p.fmt == DATTN_KV_MIXED) && (p.gq == 2 || p.gq == 4);
-    auto pick = [&](auto bf16, auto f8, auto i4, auto mix, auto i4p, auto mixp) {
-        return p.fmt == DATTN_KV_MIXED    ? (pk ? mixp : mix)
+    // 2 or 4 query columns over the 4-bit pool: the packed-column consumers. (The mixed pool's
+    // 4-bit heads keep two products per m-tile: a packed instance of the mixed kernel slowed
+    // its 8-bit tiles, 27.0 against 25.1 µs per sparse-512k launch.)
+    const bool pk = p.fmt == DATTN_KV_INT4 && (p.gq == 2 || p.gq == 4);
+    auto pick = [&](auto bf16, auto f8, auto i4, auto mix, auto i4p) {
+        return p.fmt == DATTN_KV_MIXED    ? mix
              : p.fmt == DATTN_KV_INT4     ? (pk ? i4p : i4)
              : p.fmt == DATTN_KV_FP8_E4M3 ? f8
                                           : bf16;
@@ -1865,7 +1867,7 @@ dattn_status_t launch_attention(const AttnParams& p, const void* k_pool, const v
 #define DATTN_LAUNCHES(D_, APP_)                                                                \
     pick(launch_d<D_, DATTN_KV_BF16, APP_, false>, launch_d<D_, DATTN_KV_FP8_E4M3, APP_, false>,  \
          launch_d<D_, DATTN_KV_INT4, APP_, false>, launch_d<D_, DATTN_KV_MIXED, APP_, false>,     \
-         launch_d<D_, DATTN_KV_INT4, APP_, true>, launch_d<D_, DATTN_KV_MIXED, APP_, true>)
+         launch_d<D_, DATTN_KV_INT4, APP_, true>)
     auto launch = p.append != 0 ? (D == 64 ? DATTN_LAUNCHES(64, true) : DATTN_LAUNCHES(128, true))
                                 : (D == 64 ? DATTN_LAUNCHES(64, false) : DATTN_LAUNCHES(128, false));
 #undef DATTN_LAUNCHES
